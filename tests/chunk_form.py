@@ -1,0 +1,120 @@
+"""Test-only fp64 models of the chunkwise-parallel form (numpy).
+
+These are NOT the oracle.  They restate, in plain numpy, the block form that
+the CUDA kernels use, so the tests can check that algebra against the
+sequential oracle on the CPU (to ~1e-12) before any kernel runs.
+
+``chunk_form_pages`` follows the chunk form written out on the Qwen3.5-9B NPU
+model card ("How it works": N, D, O and S_T in terms of G = cumsum(g) and the
+incoming state S0), with the upper triangle of G_t - G_j masked to -inf in log
+space before exp (the Candle pull request's "Float32 overflow fix").
+
+``chunk_form_factored`` regroups the same products the way the tcgen05 prefill
+kernel does: everything that does not depend on the state is folded into
+    W  = T diag(beta e^G) K,   U  = T diag(beta) V,
+    Q' = diag(e^G) Q - P W,    U' = P U,      with T = (I + N)^-1,
+so that one chunk of the sequential pass is
+    D = U - W S,   O = Q' S + U',   S <- e^{G_C} S + K^T diag(e^{G_C - G}) D.
+T is formed by 16x16 diagonal-block forward substitution followed by blocked
+off-diagonal solves, as in the kernel.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+def _decay_matrix(G: np.ndarray, strict: bool) -> np.ndarray:
+    """exp(G_t - G_j) on the lower triangle (strict or inclusive), 0 above.
+
+    The exponent is masked in log space first, so large positive differences
+    above the diagonal never reach exp."""
+    C = G.shape[0]
+    diff = G[:, None] - G[None, :]
+    keep = np.tril(np.ones((C, C), dtype=bool), -1 if strict else 0)
+    diff = np.where(keep, diff, -np.inf)
+    return np.exp(diff)
+
+
+def _pad(x: np.ndarray, C: int) -> np.ndarray:
+    L = x.shape[0]
+    if L == C:
+        return x
+    out = np.zeros((C,) + x.shape[1:], dtype=x.dtype)
+    out[:L] = x
+    return out
+
+
+def chunk_form_pages(q, k, v, g, beta, S0, C):
+    """One head, one sequence: q, k [T, d_k], v [T, d_v], g, beta [T], S0 [d_k, d_v]."""
+    T = q.shape[0]
+    S = np.array(S0, dtype=np.float64)
+    O = np.zeros((T, v.shape[1]))
+    for c0 in range(0, T, C):
+        L = min(C, T - c0)
+        Q, K, V = (_pad(np.asarray(x[c0:c0 + L], np.float64), C) for x in (q, k, v))
+        gc = _pad(np.asarray(g[c0:c0 + L], np.float64), C)  # padding: g = 0
+        bc = _pad(np.asarray(beta[c0:c0 + L], np.float64), C)  # padding: beta = 0
+        G = np.cumsum(gc)
+        eG = np.exp(G)
+        N = bc[:, None] * _decay_matrix(G, strict=True) * (K @ K.T)
+        D = np.linalg.solve(np.eye(C) + N, bc[:, None] * (V - eG[:, None] * (K @ S)))
+        Oc = eG[:, None] * (Q @ S) + (_decay_matrix(G, strict=False) * (Q @ K.T)) @ D
+        S = np.exp(G[-1]) * S + K.T @ (np.exp(G[-1] - G)[:, None] * D)
+        O[c0:c0 + L] = Oc[:L]
+    return O, S
+
+
+def unit_lower_inverse_blocked(N: np.ndarray, b: int = 16) -> np.ndarray:
+    """(I + N)^-1 for strictly lower N: forward substitution inside each b x b
+    diagonal block, then blocked solves for the blocks below the diagonal:
+        T_ii = (I + N_ii)^-1,   T_ij = -T_ii * sum_{j <= m < i} N_im T_mj."""
+    C = N.shape[0]
+    nb = C // b
+    T = np.zeros_like(N)
+    for i in range(nb):
+        sl = slice(i * b, (i + 1) * b)
+        Nii = N[sl, sl]
+        Tii = np.eye(b)
+        for r in range(b):  # row r of T_ii: e_r - sum_{m<r} N_rm T_m
+            Tii[r] = np.eye(b)[r] - Nii[r, :r] @ Tii[:r]
+        T[sl, sl] = Tii
+    for i in range(nb):
+        si = slice(i * b, (i + 1) * b)
+        for j in range(i - 1, -1, -1):
+            sj = slice(j * b, (j + 1) * b)
+            acc = np.zeros((b, b))
+            for m in range(j, i):
+                sm = slice(m * b, (m + 1) * b)
+                acc += N[si, sm] @ T[sm, sj]
+            T[si, sj] = -T[si, si] @ acc
+    return T
+
+
+def chunk_form_factored(q, k, v, g, beta, S0, C):
+    """Same contract as ``chunk_form_pages``, regrouped as the kernel computes it."""
+    T_len = q.shape[0]
+    S = np.array(S0, dtype=np.float64)
+    O = np.zeros((T_len, v.shape[1]))
+    for c0 in range(0, T_len, C):
+        L = min(C, T_len - c0)
+        Q, K, V = (_pad(np.asarray(x[c0:c0 + L], np.float64), C) for x in (q, k, v))
+        gc = _pad(np.asarray(g[c0:c0 + L], np.float64), C)
+        bc = _pad(np.asarray(beta[c0:c0 + L], np.float64), C)
+        G = np.cumsum(gc)
+        eG = np.exp(G)
+        A_kk = K @ K.T
+        A_qk = Q @ K.T
+        N = bc[:, None] * _decay_matrix(G, strict=True) * A_kk
+        P = _decay_matrix(G, strict=False) * A_qk
+        Tm = unit_lower_inverse_blocked(N, 16 if C % 16 == 0 else C)
+        W = Tm @ ((bc * eG)[:, None] * K)
+        U = Tm @ (bc[:, None] * V)
+        Qp = eG[:, None] * Q - P @ W
+        Up = P @ U
+        # sequential part
+        D = U - W @ S
+        Oc = Qp @ S + Up
+        S = np.exp(G[-1]) * S + K.T @ (np.exp(G[-1] - G)[:, None] * D)
+        O[c0:c0 + L] = Oc[:L]
+    return O, S
