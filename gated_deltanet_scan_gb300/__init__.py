@@ -1,1 +1,199 @@
-"""Gated delta rule on GB300 (sm_103a)."""
+"""Gated delta rule on GB300 (sm_103a): a thin Python binding of libgdr.so.
+
+Every function here only marshals arguments into the C ABI declared in
+include/gdr.h (same names); all arithmetic runs in the library's CUDA kernels.
+PyTorch is used for device memory and streams only.  There is no CPU path:
+if the compiled library is missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+__all__ = [
+    "GdrError", "gdr_dims", "lib", "library_path",
+    "gdr_prefill_chunked", "gdr_decode_step", "gdr_verify_block",
+    "gdr_state_snapshot", "gdr_state_restore", "gdr_device_error", "gdr_status_string",
+    "GDR_F32", "GDR_BF16",
+]
+
+GDR_OK, GDR_ERR_INVALID_ARG, GDR_ERR_UNSUPPORTED, GDR_ERR_CUDA, GDR_ERR_DEVICE_TIMEOUT = range(5)
+GDR_F32, GDR_BF16 = 0, 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libgdr.so")
+
+
+class GdrError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {gdr_status_string(status)}")
+
+
+class gdr_dims(ctypes.Structure):
+    _fields_ = [
+        ("h_qk", ctypes.c_int32), ("h_v", ctypes.c_int32),
+        ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32),
+        ("chunk", ctypes.c_int32), ("in_dtype", ctypes.c_int32),
+        ("out_dtype", ctypes.c_int32), ("scale", ctypes.c_float),
+    ]
+
+
+_P = ctypes.c_void_p
+_SIGS = {
+    "gdr_abi_version": ([], ctypes.c_int32),
+    "gdr_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "gdr_prefill_chunked": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, ctypes.c_int64,
+                             _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "gdr_decode_step": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P],
+                        ctypes.c_int),
+    "gdr_verify_block": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, ctypes.c_int32,
+                          _P, _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "gdr_state_snapshot": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, _P, _P], ctypes.c_int),
+    "gdr_state_restore": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, _P, _P], ctypes.c_int),
+    "gdr_device_error": ([_P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
+}
+
+
+def lib():
+    """The loaded library (ctypes); raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise ImportError(
+                    f"{path} is missing: build it with `python -m gated_deltanet_scan_gb300.build` "
+                    "(there is no CPU fallback)")
+            handle = ctypes.CDLL(path)
+            for name, (argtypes, restype) in _SIGS.items():
+                fn = getattr(handle, name)
+                fn.argtypes = argtypes
+                fn.restype = restype
+            _lib = handle
+    return _lib
+
+
+def gdr_status_string(status: int) -> str:
+    try:
+        return lib().gdr_status_string(int(status)).decode()
+    except ImportError:
+        return f"gdr_status {status}"
+
+
+def _check(status: int, where: str) -> None:
+    if status != GDR_OK:
+        raise GdrError(status, where)
+
+
+# --- marshalling helpers (torch only for pointers, dtypes and streams) ----------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return GDR_BF16
+    if t.dtype == torch.float32:
+        return GDR_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream_handle(stream, device) -> Optional[int]:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_dims(q, v, o, chunk: int = 64, scale: float = 1.0) -> gdr_dims:
+    """dims from q [T, H_qk, d_k], v [T, H_v, d_v] and o (its dtype is the output type)."""
+    return gdr_dims(h_qk=q.shape[-2], h_v=v.shape[-2], d_k=q.shape[-1], d_v=v.shape[-1],
+                    chunk=chunk, in_dtype=_dtype_code(q), out_dtype=_dtype_code(o),
+                    scale=float(scale))
+
+
+def gdr_prefill_chunked(q, k, v, g, beta, state, o, cu_seqlens, *, chunk: int = 64,
+                        scale: float = 1.0, t_total: Optional[int] = None, stream=None) -> None:
+    """Chunked prefill over packed sequences (see gdr_prefill_chunked in include/gdr.h).
+
+    q, k [T, H_qk, d_k]; v [T, H_v, d_v]; g, beta [T, H_v] fp32;
+    state [n, H_v, d_k, d_v] fp32 (in/out); o [T, H_v, d_v]; cu_seqlens int32 [n+1]
+    on the device.  ``t_total`` defaults to q.shape[0]."""
+    dims = make_dims(q, v, o, chunk, scale)
+    n = cu_seqlens.shape[0] - 1
+    T = q.shape[0] if t_total is None else int(t_total)
+    st = lib().gdr_prefill_chunked(
+        ctypes.byref(dims), n, _ptr(cu_seqlens), T, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+        _ptr(beta), _ptr(state), _ptr(o), _stream_handle(stream, q.device))
+    _check(st, "gdr_prefill_chunked")
+
+
+def gdr_decode_step(q, k, v, g, beta, state, o, *, scale: float = 1.0, stream=None) -> None:
+    """One decode step for B sequences: q, k [B, H_qk, d]; v, o [B, H_v, d];
+    g, beta [B, H_v]; state [B, H_v, d, d] updated in place."""
+    dims = make_dims(q, v, o, 64, scale)
+    st = lib().gdr_decode_step(
+        ctypes.byref(dims), q.shape[0], _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+        _ptr(state), _ptr(o), _stream_handle(stream, q.device))
+    _check(st, "gdr_decode_step")
+
+
+def gdr_verify_block(q, k, v, g, beta, state, snapshot, o, n_tok: int, *, scale: float = 1.0,
+                     stream=None) -> None:
+    """n_tok (<= 16) draft tokens per sequence from the current state; the incoming
+    state is copied to ``snapshot``.  Token rows are [n_seqs * n_tok, ...]."""
+    dims = make_dims(q, v, o, 16, scale)
+    n = state.shape[0]
+    st = lib().gdr_verify_block(
+        ctypes.byref(dims), n, int(n_tok), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+        _ptr(state), _ptr(snapshot), _ptr(o), _stream_handle(stream, state.device))
+    _check(st, "gdr_verify_block")
+
+
+def _state_dims(state) -> gdr_dims:
+    _, hv, dk, dv = state.shape
+    return gdr_dims(h_qk=hv, h_v=hv, d_k=dk, d_v=dv, chunk=64, in_dtype=GDR_F32,
+                    out_dtype=GDR_F32, scale=1.0)
+
+
+def gdr_state_snapshot(state, snapshot, *, stream=None) -> None:
+    dims = _state_dims(state)
+    st = lib().gdr_state_snapshot(ctypes.byref(dims), state.shape[0], _ptr(state), _ptr(snapshot),
+                                  _stream_handle(stream, state.device))
+    _check(st, "gdr_state_snapshot")
+
+
+def gdr_state_restore(snapshot, state, *, stream=None) -> None:
+    dims = _state_dims(state)
+    st = lib().gdr_state_restore(ctypes.byref(dims), state.shape[0], _ptr(snapshot), _ptr(state),
+                                 _stream_handle(stream, state.device))
+    _check(st, "gdr_state_restore")
+
+
+def gdr_device_error(*, stream=None, device=None) -> int:
+    """Synchronise the stream and return (and clear) the device error word."""
+    code = ctypes.c_int32(0)
+    _check(lib().gdr_device_error(_stream_handle(stream, device), ctypes.byref(code)), "gdr_device_error")
+    return int(code.value)

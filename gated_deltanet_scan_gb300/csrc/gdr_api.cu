@@ -1,0 +1,194 @@
+// C-ABI entry points: argument checks on the host, then one launch each.
+#include <cuda_runtime.h>
+
+#include "gdr_internal.h"
+
+namespace gdr {
+namespace {
+
+__global__ void copy_f32_kernel(const float4 *__restrict__ src, float4 *__restrict__ dst, size_t n4) {
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride)
+        __stcs(&dst[i], __ldcs(&src[i]));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+gdr_status check_dims(const gdr_dims *d) {
+    if (!d) return GDR_ERR_INVALID_ARG;
+    if (d->h_qk <= 0 || d->h_v <= 0 || d->h_v % d->h_qk != 0) return GDR_ERR_INVALID_ARG;
+    if (d->d_k <= 0 || d->d_v <= 0) return GDR_ERR_INVALID_ARG;
+    if (d->in_dtype != GDR_F32 && d->in_dtype != GDR_BF16) return GDR_ERR_INVALID_ARG;
+    if (d->out_dtype != GDR_F32 && d->out_dtype != GDR_BF16) return GDR_ERR_INVALID_ARG;
+    if (d->chunk != 16 && d->chunk != 64) return GDR_ERR_UNSUPPORTED;
+    if (d->d_k != d->d_v) return GDR_ERR_UNSUPPORTED;
+    if (d->d_k != 32 && d->d_k != 64 && d->d_k != 128) return GDR_ERR_UNSUPPORTED;
+    return GDR_OK;
+}
+
+Args make_args(const gdr_dims *d) {
+    Args a{};
+    a.h_qk = d->h_qk;
+    a.h_v = d->h_v;
+    a.d = d->d_k;
+    a.in_bf16 = d->in_dtype == GDR_BF16;
+    a.out_bf16 = d->out_dtype == GDR_BF16;
+    a.scale = d->scale;
+    return a;
+}
+
+bool tensors_ok(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                const float *state, const void *o) {
+    const void *ps[] = {q, k, v, g, beta, state, o};
+    for (const void *p : ps)
+        if (!p || !aligned16(p)) return false;
+    return true;
+}
+
+gdr_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA; }
+
+bool use_tensor_core_prefill(const gdr_dims *d) {
+    return d->chunk == 64 && d->d_k == 128 && d->in_dtype == GDR_BF16;
+}
+
+}  // namespace
+}  // namespace gdr
+
+using namespace gdr;
+
+extern "C" {
+
+int32_t gdr_abi_version(void) { return GDR_ABI_VERSION; }
+
+const char *gdr_status_string(gdr_status st) {
+    switch (st) {
+        case GDR_OK: return "GDR_OK";
+        case GDR_ERR_INVALID_ARG: return "GDR_ERR_INVALID_ARG: invalid argument";
+        case GDR_ERR_UNSUPPORTED: return "GDR_ERR_UNSUPPORTED: shape, chunk or dtype not compiled";
+        case GDR_ERR_CUDA: return "GDR_ERR_CUDA: a CUDA launch or synchronisation failed";
+        case GDR_ERR_DEVICE_TIMEOUT: return "GDR_ERR_DEVICE_TIMEOUT: a device-side wait gave up";
+    }
+    return "unknown gdr_status";
+}
+
+gdr_status gdr_prefill_chunked(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens,
+                               int64_t t_total, const void *q, const void *k, const void *v,
+                               const float *g, const float *beta, float *state, void *o,
+                               gdr_stream_t stream) {
+    gdr_status st = check_dims(dims);
+    if (st != GDR_OK) return st;
+    if (n_seqs < 0 || t_total < 0) return GDR_ERR_INVALID_ARG;
+    if (n_seqs == 0) return t_total == 0 ? GDR_OK : GDR_ERR_INVALID_ARG;
+    if (!cu_seqlens || !aligned16(cu_seqlens) || !state || !aligned16(state)) return GDR_ERR_INVALID_ARG;
+    if (t_total > 0 && !tensors_ok(q, k, v, g, beta, state, o)) return GDR_ERR_INVALID_ARG;
+    if (t_total > ((int64_t)1 << 31) - 1) return GDR_ERR_UNSUPPORTED;
+    Args a = make_args(dims);
+    a.n_seqs = n_seqs;
+    a.cu_seqlens = cu_seqlens;
+    a.fixed_len = 0;
+    a.t_total = t_total;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.g = g;
+    a.beta = beta;
+    a.state = state;
+    a.snapshot = nullptr;
+    a.o = o;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (use_tensor_core_prefill(dims)) return from_cuda(launch_prefill_tc(a, s));
+    return from_cuda(launch_chunk_cc(a, s));
+}
+
+gdr_status gdr_decode_step(const gdr_dims *dims, int32_t batch, const void *q, const void *k,
+                           const void *v, const float *g, const float *beta, float *state, void *o,
+                           gdr_stream_t stream) {
+    gdr_status st = check_dims(dims);
+    if (st != GDR_OK) return st;
+    if (batch < 0) return GDR_ERR_INVALID_ARG;
+    if (batch == 0) return GDR_OK;
+    if (!tensors_ok(q, k, v, g, beta, state, o)) return GDR_ERR_INVALID_ARG;
+    Args a = make_args(dims);
+    a.n_seqs = batch;
+    a.cu_seqlens = nullptr;
+    a.fixed_len = 1;
+    a.t_total = batch;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.g = g;
+    a.beta = beta;
+    a.state = state;
+    a.snapshot = nullptr;
+    a.o = o;
+    return from_cuda(launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gdr_status gdr_verify_block(const gdr_dims *dims, int32_t n_seqs, int32_t n_tok, const void *q,
+                            const void *k, const void *v, const float *g, const float *beta,
+                            float *state, float *snapshot, void *o, gdr_stream_t stream) {
+    gdr_status st = check_dims(dims);
+    if (st != GDR_OK) return st;
+    if (n_seqs < 0 || n_tok < 0 || n_tok > 16) return GDR_ERR_INVALID_ARG;
+    if (n_seqs == 0) return GDR_OK;
+    if (!snapshot || !aligned16(snapshot) || !state || !aligned16(state)) return GDR_ERR_INVALID_ARG;
+    if (snapshot == state) return GDR_ERR_INVALID_ARG;
+    if (n_tok > 0 && !tensors_ok(q, k, v, g, beta, state, o)) return GDR_ERR_INVALID_ARG;
+    Args a = make_args(dims);
+    a.n_seqs = n_seqs;
+    a.cu_seqlens = nullptr;
+    a.fixed_len = n_tok;
+    a.t_total = (int64_t)n_seqs * n_tok;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.g = g;
+    a.beta = beta;
+    a.state = state;
+    a.snapshot = snapshot;
+    a.o = o;
+    return from_cuda(launch_chunk_cc(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static gdr_status copy_states(const gdr_dims *dims, int32_t n_seqs, const float *src, float *dst,
+                              gdr_stream_t stream) {
+    gdr_status st = check_dims(dims);
+    if (st != GDR_OK) return st;
+    if (n_seqs < 0) return GDR_ERR_INVALID_ARG;
+    if (n_seqs == 0) return GDR_OK;
+    if (!src || !dst || !aligned16(src) || !aligned16(dst) || src == dst) return GDR_ERR_INVALID_ARG;
+    const size_t n = (size_t)n_seqs * dims->h_v * dims->d_k * dims->d_v;
+    return from_cuda(launch_copy_f32(src, dst, n, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gdr_status gdr_state_snapshot(const gdr_dims *dims, int32_t n_seqs, const float *state,
+                              float *snapshot, gdr_stream_t stream) {
+    return copy_states(dims, n_seqs, state, snapshot, stream);
+}
+
+gdr_status gdr_state_restore(const gdr_dims *dims, int32_t n_seqs, const float *snapshot,
+                             float *state, gdr_stream_t stream) {
+    return copy_states(dims, n_seqs, snapshot, state, stream);
+}
+
+gdr_status gdr_device_error(gdr_stream_t stream, int32_t *code) {
+    if (!code) return GDR_ERR_INVALID_ARG;
+    return from_cuda(read_clear_device_error(reinterpret_cast<cudaStream_t>(stream), code));
+}
+
+}  // extern "C"
+
+namespace gdr {
+
+cudaError_t launch_copy_f32(const float *src, float *dst, size_t n, cudaStream_t s) {
+    // n is a multiple of 4: every state holds d_k * d_v floats with d in {32, 64, 128}.
+    const size_t n4 = n / 4;
+    const unsigned threads = 256;
+    unsigned blocks = (unsigned)((n4 + threads - 1) / threads);
+    if (blocks > 152u * 16u) blocks = 152u * 16u;
+    copy_f32_kernel<<<blocks, threads, 0, s>>>(reinterpret_cast<const float4 *>(src),
+                                                reinterpret_cast<float4 *>(dst), n4);
+    return cudaGetLastError();
+}
+
+}  // namespace gdr

@@ -1,0 +1,175 @@
+/*
+ * gdr.h -- C ABI of the gated delta rule library (sm_103a, one GPU).
+ *
+ * The method.  For every sequence and V head h the library runs
+ *
+ *     S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,   o_t = scale * S_t^T q_t
+ *
+ * ("Qwen3.5-9B: Giai ma kien truc Gated DeltaNet", section "Gated DeltaNet";
+ * step order as in the per-token Loop of the Qwen3.5-9B NPU model card,
+ * section "How it works": decay, recall S^T k, delta correction, read-out).
+ * The gate is passed as g_t = log(alpha_t) <= 0 (a decay; the Candle PR's
+ * "Bug 1" records that the raw value is already negative).  Each QK head feeds
+ * H_v / H_qk consecutive V heads: V head h reads q and k from QK head
+ * h / (H_v / H_qk) (for Qwen3.5-9B, 16 QK heads each shared by 2 of 32 V heads).
+ *
+ * Conventions for every entry point
+ *   - Memory.  Every tensor pointer is a DEVICE pointer allocated by the caller;
+ *     the library allocates nothing and keeps no pointer after the call returns.
+ *     Pointers must be 16-byte aligned.
+ *   - Layouts (row-major, token-major, sequences packed back to back):
+ *         q, k   [T_total][H_qk][d_k]        in_dtype  (bf16 or fp32)
+ *         v      [T_total][H_v][d_v]         in_dtype
+ *         o      [T_total][H_v][d_v]         out_dtype (fp32 or bf16)
+ *         g, beta[T_total][H_v]              fp32  (g = log alpha)
+ *         state  [n_seqs][H_v][d_k][d_v]     fp32, d_v contiguous
+ *   - Ordering.  Calls are asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and ordered like any other work on that stream.
+ *   - Errors.  Arguments are checked on the host before anything is launched:
+ *     GDR_ERR_INVALID_ARG (null or misaligned pointer, bad count, H_v not a
+ *     multiple of H_qk, verify longer than 16 tokens, ...) or GDR_ERR_UNSUPPORTED
+ *     (a head size, chunk or dtype with no compiled kernel).  GDR_ERR_CUDA means
+ *     a launch failed.  Kernels that wait on asynchronous copies give up after a
+ *     bounded number of polls and record GDR_ERR_DEVICE_TIMEOUT in a device
+ *     error word that gdr_device_error() reads; they never spin forever.
+ *   - Aliasing.  `state` is updated in place.  `o` must not overlap any input.
+ *
+ * Supported shapes: d_k == d_v in {32, 64, 128}; chunk in {16, 64}; any H_qk,
+ * H_v with H_v % H_qk == 0.  The chunk is a tiling choice, not part of the
+ * result: d_k = d_v = 128 with bf16 inputs and chunk 64 runs the tensor-core
+ * (tcgen05) prefill; every other shape runs the CUDA-core chunk kernel with
+ * 16-token chunks.
+ */
+#ifndef GDR_H_
+#define GDR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDR_ABI_VERSION 1
+
+/* Same object as cudaStream_t; declared here so callers need no CUDA header. */
+typedef struct CUstream_st *gdr_stream_t;
+
+typedef enum gdr_status {
+    GDR_OK = 0,
+    GDR_ERR_INVALID_ARG = 1,
+    GDR_ERR_UNSUPPORTED = 2,
+    GDR_ERR_CUDA = 3,
+    GDR_ERR_DEVICE_TIMEOUT = 4
+} gdr_status;
+
+typedef enum gdr_dtype { GDR_F32 = 0, GDR_BF16 = 1 } gdr_dtype;
+
+typedef struct gdr_dims {
+    int32_t h_qk;      /* QK heads */
+    int32_t h_v;       /* V heads; a multiple of h_qk */
+    int32_t d_k;       /* key/query head size */
+    int32_t d_v;       /* value head size (== d_k) */
+    int32_t chunk;     /* 16 or 64 tokens per chunk */
+    int32_t in_dtype;  /* gdr_dtype of q, k, v */
+    int32_t out_dtype; /* gdr_dtype of o */
+    float scale;       /* multiplies every output; 1.0 reproduces o_t = S_t^T q_t */
+} gdr_dims;
+
+/* GDR_ABI_VERSION of the loaded library. */
+int32_t gdr_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *gdr_status_string(gdr_status status);
+
+/*
+ * Chunked prefill over packed variable-length sequences.
+ *
+ * Computes, for every sequence s in [0, n_seqs) with tokens
+ * [cu_seqlens[s], cu_seqlens[s+1]) and every V head, the outputs o_t of all its
+ * tokens and the state after its last token, starting from state[s] (S0).
+ * It uses the chunkwise-parallel form of the Qwen3.5-9B NPU model card
+ * ("How it works": N, D = (I+N)^-1 diag(beta)(V - diag(e^G) K S0), O and S_T
+ * with G the running sum of g inside a chunk), solving the unit lower
+ * triangular system by forward substitution as in the Candle PR's
+ * "Chunked GatedDeltaNet Scan" section, carrying the state from chunk to
+ * chunk, and masking the upper triangle of G_t - G_j in log space before exp
+ * (the PR's "Float32 overflow fix").  Chunks start at each sequence start; a
+ * tail chunk is treated as padded with g = 0, beta = 0 rows (the model card's
+ * token_valid padding), which leaves the state as after the last real token;
+ * padded rows are never written.
+ *
+ *   dims        shapes, dtypes, chunk, scale (host pointer, read during the call)
+ *   n_seqs      number of sequences (>= 0; 0 is a no-op)
+ *   cu_seqlens  DEVICE int32 [n_seqs + 1], non-decreasing, cu_seqlens[0] == 0,
+ *               cu_seqlens[n_seqs] == t_total (empty sequences allowed: their
+ *               state is left unchanged)
+ *   t_total     total tokens (host value, sizes the launch)
+ *   q, k, v, g, beta   inputs (layouts above)
+ *   state       in: S0 per sequence; out: state after the last token
+ *   o           out: outputs of every token
+ */
+gdr_status gdr_prefill_chunked(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens,
+                               int64_t t_total, const void *q, const void *k, const void *v,
+                               const float *g, const float *beta, float *state, void *o,
+                               gdr_stream_t stream);
+
+/*
+ * One decode step for `batch` independent sequences (one token each).
+ *
+ * For each sequence b and V head h, with S = state[b][h] and d = exp(g):
+ *     y = S^T k,  z = S^T q,  delta = beta (v - d y),
+ *     o = scale (d z + (q . k) delta),  S <- d S + k delta^T   (in place)
+ * which is the 1-token matrix form of the Qwen3.5-9B NPU model card
+ * ("How it works": [q;k]^T S in one product, o = d q^T S + (q.k) delta,
+ * S' = d S + k delta^T).  The state is read once and written once.
+ *
+ *   q, k [batch][H_qk][d_k]; v, o [batch][H_v][d_v]; g, beta [batch][H_v];
+ *   state [batch][H_v][d_k][d_v] (in/out).
+ */
+gdr_status gdr_decode_step(const gdr_dims *dims, int32_t batch, const void *q, const void *k,
+                           const void *v, const float *g, const float *beta, float *state, void *o,
+                           gdr_stream_t stream);
+
+/*
+ * Speculative-verify block: n_tok <= 16 draft tokens per sequence in one pass.
+ *
+ * Copies state[s] to snapshot[s] (the state before the block), then runs the
+ * n_tok tokens of every sequence from that state as one chunk, writing all
+ * n_tok outputs and leaving the state after the whole block in state[s].
+ * After choosing how many tokens a_s to accept, the caller restores the
+ * snapshot (gdr_state_restore) and re-feeds the a_s accepted tokens with
+ * gdr_prefill_chunked (lengths a_s, zero allowed).  This is the model card's
+ * prompt-lookup decoding ("New in v2": the DeltaNet state cannot be rewound,
+ * so it is snapshotted before the 16-token check and the accepted tokens are
+ * re-fed).
+ *
+ *   q, k [n_seqs * n_tok][H_qk][d_k]; v, o [n_seqs * n_tok][H_v][d_v];
+ *   g, beta [n_seqs * n_tok][H_v]; state, snapshot [n_seqs][H_v][d_k][d_v].
+ *   snapshot must not overlap state.
+ */
+gdr_status gdr_verify_block(const gdr_dims *dims, int32_t n_seqs, int32_t n_tok, const void *q,
+                            const void *k, const void *v, const float *g, const float *beta,
+                            float *state, float *snapshot, void *o, gdr_stream_t stream);
+
+/* Copy n_seqs states (H_v * d_k * d_v floats each) from `state` to `snapshot`. */
+gdr_status gdr_state_snapshot(const gdr_dims *dims, int32_t n_seqs, const float *state,
+                              float *snapshot, gdr_stream_t stream);
+
+/* Copy n_seqs states back from `snapshot` to `state` (undo a verify block). */
+gdr_status gdr_state_restore(const gdr_dims *dims, int32_t n_seqs, const float *snapshot,
+                             float *state, gdr_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word of the
+ * current device.  *code receives GDR_OK or the first error a kernel recorded
+ * (GDR_ERR_DEVICE_TIMEOUT when a bounded wait gave up).  Returns GDR_ERR_CUDA if
+ * the synchronisation itself fails.
+ */
+gdr_status gdr_device_error(gdr_stream_t stream, int32_t *code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_H_ */

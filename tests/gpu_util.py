@@ -1,0 +1,87 @@
+"""Helpers for the GPU parity tests: move a synthetic workload to the device,
+run the library through its binding, and measure errors against the oracle.
+
+Tolerances (stated for bf16 q/k/v): the output's max-abs error relative to the
+oracle output's RMS over the whole tensor <= 2e-2, and the final state's
+relative Frobenius error <= 1e-3.  When the output is stored as bf16, its own
+rounding (up to 2^-9 of each value, and outputs reach ~20x their RMS) is added
+per element: |o - o*| <= 2e-2 RMS(o*) + 2^-8 |o*|.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+O_TOL = 2e-2
+S_TOL = 1e-3
+BF16_OUT_REL = 2.0 ** -8
+
+
+def torch_mod():
+    import torch
+    return torch
+
+
+def require_gpu():
+    torch = torch_mod()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import gated_deltanet_scan_gb300 as gdr
+    gdr.lib()  # raises if the library is missing: no fallback
+    return torch
+
+
+def dev_inputs(w, device="cuda"):
+    """q, k, v in the workload's io dtype; g, beta fp32; state fp32; cu_seqlens int32."""
+    torch = torch_mod()
+
+    def io(vals, bits):
+        if w.io == "bf16":
+            return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(device)
+        return torch.from_numpy(np.ascontiguousarray(vals, dtype=np.float32)).to(device)
+
+    return dict(
+        q=io(w.q, w.q_bits), k=io(w.k, w.k_bits), v=io(w.v, w.v_bits),
+        g=torch.from_numpy(np.ascontiguousarray(w.g)).to(device),
+        beta=torch.from_numpy(np.ascontiguousarray(w.beta)).to(device),
+        state=torch.from_numpy(np.ascontiguousarray(w.state0)).to(device),
+        cu_seqlens=torch.from_numpy(w.cu_seqlens.astype(np.int32)).to(device),
+    )
+
+
+def out_like(v, out_dtype):
+    torch = torch_mod()
+    dt = torch.float32 if out_dtype == "f32" else torch.bfloat16
+    return torch.full(v.shape, float("nan"), dtype=dt, device=v.device)
+
+
+def to_np(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def o_error(o_gpu, o_ref) -> float:
+    rms = float(np.sqrt(np.mean(o_ref * o_ref)))
+    return float(np.max(np.abs(o_gpu - o_ref))) / max(rms, 1e-30)
+
+
+def check_outputs(o_gpu, o_ref, out_dtype="f32", tol=O_TOL):
+    assert np.all(np.isfinite(o_gpu)), "non-finite outputs"
+    rms = float(np.sqrt(np.mean(o_ref * o_ref)))
+    if out_dtype == "f32":
+        err = o_error(o_gpu, o_ref)
+        assert err <= tol, f"output max-abs error {err:.3e} x RMS > {tol}"
+        return err
+    bound = tol * rms + BF16_OUT_REL * np.abs(o_ref)
+    excess = np.abs(o_gpu - o_ref) - bound
+    assert np.all(excess <= 0), f"bf16 output error beyond bound by {excess.max():.3e}"
+    return o_error(o_gpu, o_ref)
+
+
+def state_error(s_gpu, s_ref) -> float:
+    return float(np.linalg.norm(s_gpu - s_ref) / max(np.linalg.norm(s_ref), 1e-30))
+
+
+def check_state(s_gpu, s_ref, tol=S_TOL):
+    assert np.all(np.isfinite(s_gpu)), "non-finite state"
+    err = state_error(s_gpu, s_ref)
+    assert err <= tol, f"state relative Frobenius error {err:.3e} > {tol}"
+    return err

@@ -1,0 +1,129 @@
+"""The C-ABI library on the CPU: it loads, exports every entry point that
+include/gdr.h declares, and rejects bad arguments on the host before any launch.
+No call here reaches a kernel (no GPU is needed)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_deltanet_scan_gb300 as gdr
+from gated_deltanet_scan_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdr.h")
+
+A = 0x100000  # a 16-byte aligned stand-in address: validation never dereferences it
+B = 0x200000
+MISALIGNED = 0x100004
+
+
+@pytest.fixture(scope="module")
+def L():
+    gbuild.build()
+    return gdr.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdr_[a-z_]+)\s*\(", text)))
+
+
+def dims(**kw):
+    d = dict(h_qk=16, h_v=32, d_k=128, d_v=128, chunk=64, in_dtype=gdr.GDR_BF16,
+             out_dtype=gdr.GDR_F32, scale=1.0)
+    d.update(kw)
+    return gdr.gdr_dims(**d)
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert {"gdr_prefill_chunked", "gdr_decode_step", "gdr_verify_block",
+            "gdr_state_snapshot", "gdr_state_restore"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in gdr.h but not exported"
+
+
+def test_abi_version_matches_header(L):
+    m = re.search(r"#define GDR_ABI_VERSION (\d+)", open(HEADER).read())
+    assert L.gdr_abi_version() == int(m.group(1))
+
+
+def test_status_strings(L):
+    for code in range(5):
+        s = L.gdr_status_string(code).decode()
+        assert s.startswith("GDR_")
+    assert L.gdr_status_string(99).decode() == "unknown gdr_status"
+
+
+def _prefill(L, d, n=1, cu=A, t=10, q=A, k=A, v=A, g=A, beta=A, state=A, o=B):
+    return L.gdr_prefill_chunked(ctypes.byref(d) if d is not None else None, n, cu, t,
+                                 q, k, v, g, beta, state, o, None)
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(h_v=33), gdr.GDR_ERR_INVALID_ARG),
+    (dict(h_qk=0), gdr.GDR_ERR_INVALID_ARG),
+    (dict(in_dtype=7), gdr.GDR_ERR_INVALID_ARG),
+    (dict(out_dtype=-1), gdr.GDR_ERR_INVALID_ARG),
+    (dict(d_k=96, d_v=96), gdr.GDR_ERR_UNSUPPORTED),
+    (dict(d_v=64), gdr.GDR_ERR_UNSUPPORTED),
+    (dict(chunk=32), gdr.GDR_ERR_UNSUPPORTED),
+])
+def test_prefill_rejects_bad_dims(L, bad, code):
+    assert _prefill(L, dims(**bad)) == code
+
+
+def test_prefill_rejects_bad_pointers_and_counts(L):
+    d = dims()
+    assert _prefill(L, None) == gdr.GDR_ERR_INVALID_ARG
+    assert _prefill(L, d, q=None) == gdr.GDR_ERR_INVALID_ARG
+    assert _prefill(L, d, v=MISALIGNED) == gdr.GDR_ERR_INVALID_ARG
+    assert _prefill(L, d, cu=None) == gdr.GDR_ERR_INVALID_ARG
+    assert _prefill(L, d, state=None) == gdr.GDR_ERR_INVALID_ARG
+    assert _prefill(L, d, n=-1) == gdr.GDR_ERR_INVALID_ARG
+    assert _prefill(L, d, t=-5) == gdr.GDR_ERR_INVALID_ARG
+    assert _prefill(L, d, n=0, t=5) == gdr.GDR_ERR_INVALID_ARG
+    assert _prefill(L, d, n=0, t=0) == gdr.GDR_OK  # nothing to do, nothing launched
+
+
+def test_decode_and_verify_reject_bad_arguments(L):
+    d = dims()
+    dec = L.gdr_decode_step
+    assert dec(ctypes.byref(d), -1, A, A, A, A, A, A, B, None) == gdr.GDR_ERR_INVALID_ARG
+    assert dec(ctypes.byref(d), 4, A, A, None, A, A, A, B, None) == gdr.GDR_ERR_INVALID_ARG
+    assert dec(ctypes.byref(d), 4, A, A, A, A, A, A, MISALIGNED, None) == gdr.GDR_ERR_INVALID_ARG
+    assert dec(ctypes.byref(d), 0, None, None, None, None, None, None, None, None) == gdr.GDR_OK
+    ver = L.gdr_verify_block
+    assert ver(ctypes.byref(d), 2, 17, A, A, A, A, A, A, B, B, None) == gdr.GDR_ERR_INVALID_ARG
+    assert ver(ctypes.byref(d), 2, 16, A, A, A, A, A, A, A, B, None) == gdr.GDR_ERR_INVALID_ARG
+    assert ver(ctypes.byref(d), 2, 16, A, A, A, A, A, A, None, B, None) == gdr.GDR_ERR_INVALID_ARG
+    assert ver(ctypes.byref(d), -2, 16, A, A, A, A, A, A, B, B, None) == gdr.GDR_ERR_INVALID_ARG
+
+
+def test_snapshot_restore_reject_bad_arguments(L):
+    d = dims()
+    assert L.gdr_state_snapshot(ctypes.byref(d), 2, A, A, None) == gdr.GDR_ERR_INVALID_ARG
+    assert L.gdr_state_restore(ctypes.byref(d), 2, None, A, None) == gdr.GDR_ERR_INVALID_ARG
+    assert L.gdr_state_restore(ctypes.byref(d), 2, MISALIGNED, A, None) == gdr.GDR_ERR_INVALID_ARG
+    assert L.gdr_state_snapshot(ctypes.byref(d), 0, A, B, None) == gdr.GDR_OK
+    assert L.gdr_device_error(None, None) == gdr.GDR_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(gdr, "_lib", None)
+    monkeypatch.setattr(gdr, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        gdr.lib()
+
+
+def test_product_package_never_imports_the_oracle():
+    pkg = os.path.dirname(gdr.__file__)
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".c", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "gdr_oracle" not in text and "liboracle" not in text, f

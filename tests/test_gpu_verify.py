@@ -1,0 +1,108 @@
+"""Packed variable-length prefill, then a 16-token verify block per sequence from
+a state snapshot, accepting a random prefix and re-feeding it (the prompt-lookup
+decoding loop of the Qwen3.5-9B NPU model card, "New in v2"), against the
+oracle's sequential result."""
+
+import numpy as np
+import pytest
+
+import oracle
+from gated_deltanet_scan_gb300 import synth
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+def _verify_flow(w, n_verify=16):
+    import gated_deltanet_scan_gb300 as gdr
+    torch = gu.require_gpu()
+    vb = w.extra["verify"]
+    acc = np.asarray(w.extra["accepted"], dtype=np.int64)
+    n = w.n_seqs
+
+    x = gu.dev_inputs(w)
+    o = gu.out_like(x["v"], "f32")
+    gdr.gdr_prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state"], o, x["cu_seqlens"])
+    state = x["state"]
+
+    y = gu.dev_inputs(vb)
+    snap = torch.empty_like(state)
+    ov = gu.out_like(y["v"], "f32")
+    gdr.gdr_verify_block(y["q"], y["k"], y["v"], y["g"], y["beta"], state, snap, ov, n_verify)
+    state_after_block = state.clone()
+
+    # accept a_s tokens per sequence: restore the snapshot, re-feed the accepted prefix
+    gdr.gdr_state_restore(snap, state)
+    rows = np.concatenate([np.arange(s * n_verify, s * n_verify + acc[s]) for s in range(n)]).astype(np.int64)
+    cu = np.zeros(n + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(acc)
+    idx = torch.from_numpy(rows).cuda()
+    pick = {k: y[k].index_select(0, idx).contiguous() for k in ("q", "k", "v", "g", "beta")}
+    o_re = gu.out_like(pick["v"], "f32")
+    gdr.gdr_prefill_chunked(pick["q"], pick["k"], pick["v"], pick["g"], pick["beta"], state, o_re,
+                            torch.from_numpy(cu).cuda(), t_total=int(cu[-1]))
+    torch.cuda.synchronize()
+    assert gdr.gdr_device_error() == 0
+    return (gu.to_np(o), gu.to_np(ov), gu.to_np(snap), gu.to_np(state_after_block),
+            gu.to_np(o_re), gu.to_np(state), rows, acc)
+
+
+def _oracle_flow(w, n_verify=16):
+    vb = w.extra["verify"]
+    acc = np.asarray(w.extra["accepted"], dtype=np.int64)
+    o_pre, S_pre = oracle.run_workload(w)
+    # the whole 16-token block from the prefill state
+    o_blk, S_blk = oracle.gdr_sequential(vb.cu_seqlens, vb.q, vb.k, vb.v, vb.g, vb.beta, S_pre)
+    # the accepted prefix only
+    rows = np.concatenate([np.arange(s * n_verify, s * n_verify + acc[s]) for s in range(w.n_seqs)])
+    cu = np.zeros(w.n_seqs + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(acc)
+    o_acc, S_acc = oracle.gdr_sequential(cu, vb.q[rows], vb.k[rows], vb.v[rows], vb.g[rows], vb.beta[rows], S_pre)
+    return o_pre, S_pre, o_blk, S_blk, o_acc, S_acc
+
+
+def test_varlen_prefill_then_verify_and_refeed():
+    """8 sequences, lengths ~ U{512..8192}, H 16/32, d=128, bf16; verify 16 tokens
+    from the snapshot, accept a ~ U{0..16}, re-feed the accepted tokens."""
+    w = synth.varlen_verify()
+    o, ov, snap, s_blk, o_re, s_final, rows, acc = _verify_flow(w)
+    o_pre, S_pre, o_blk, S_blk, o_acc, S_acc = _oracle_flow(w)
+    gu.check_outputs(o, o_pre)
+    gu.check_state(snap, S_pre)  # snapshot holds the state before the block
+    gu.check_outputs(ov, o_blk)
+    gu.check_state(s_blk, S_blk)
+    if len(rows):
+        gu.check_outputs(o_re, o_acc)
+        # re-fed outputs equal the verify block's outputs for the accepted tokens
+        assert gu.o_error(o_re, ov[rows]) < 1e-3
+    gu.check_state(s_final, S_acc)
+
+
+@pytest.mark.parametrize("n_tok", [0, 1, 7, 16])
+def test_verify_block_lengths(n_tok):
+    import gated_deltanet_scan_gb300 as gdr
+    torch = gu.require_gpu()
+    n = 3
+    w = synth.make_workload("vb", [n_tok] * n, 16, 32, 128, 16, "bf16", seed=40 + n_tok, state_std=0.02)
+    x = gu.dev_inputs(w)
+    snap = torch.empty_like(x["state"])
+    o = gu.out_like(x["v"], "f32")
+    gdr.gdr_verify_block(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state"], snap, o, n_tok)
+    torch.cuda.synchronize()
+    o_ref, S_ref = oracle.run_workload(w)
+    np.testing.assert_array_equal(gu.to_np(snap), w.state0.astype(np.float64))
+    if n_tok:
+        gu.check_outputs(gu.to_np(o), o_ref)
+    gu.check_state(gu.to_np(x["state"]), S_ref)
+
+
+def test_snapshot_restore_roundtrip():
+    import gated_deltanet_scan_gb300 as gdr
+    torch = gu.require_gpu()
+    s = torch.randn(5, 32, 128, 128, device="cuda")
+    snap = torch.empty_like(s)
+    gdr.gdr_state_snapshot(s, snap)
+    s2 = torch.zeros_like(s)
+    gdr.gdr_state_restore(snap, s2)
+    torch.cuda.synchronize()
+    assert torch.equal(snap, s) and torch.equal(s2, s)
