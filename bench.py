@@ -1,0 +1,455 @@
+"""Benchmark of the gated delta rule hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic Qwen3.5-9B
+linear-attention inputs (16 QK heads, 32 V heads, d = 128, bf16 q/k/v, fp32
+gates and state, fp32 output):
+
+  1. gdr_prefill_chunked   B = 1, T = 16384, from a N(0, 0.02) state
+  2. gdr_verify_block      16 draft tokens on that sequence (snapshot taken)
+     gdr_state_restore     roll the state back to the snapshot
+     gdr_prefill_chunked   re-feed the accepted prefix (7 tokens)
+  3. gdr_decode_step       B = 64 independent sequences, one token each
+
+tokens/s counts the 16384 prefill, 16 verify and 64 decode tokens of a step
+(re-fed tokens are recomputation and are not counted).  Inputs are resident in
+HBM before the timed region; per step they exceed L2 (q, k, v, o and the decode
+state are > 600 MB), so no flush is needed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica of the step (the path has
+no cross-GPU exchange); rank 0 prints one JSON line.  ``--impl reference``
+times the fp64 CPU oracle (the only other implementation of this path) on a
+bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "gated-delta-rule tokens/s (prefill T=16K, decode B=64) and % of roofline, 1 GB300"
+H_QK, H_V, D = 16, 32, 128
+T_PREFILL, B_DECODE, N_VERIFY, N_ACCEPT = 16384, 64, 16, 7
+TOKENS_PER_STEP = T_PREFILL + N_VERIFY + B_DECODE
+
+# algorithmic bytes: q, k (bf16, per QK head), v (bf16), o (fp32), g, beta (fp32)
+PREFILL_BYTES_PER_TOKEN = H_QK * D * 2 * 2 + H_V * D * 2 + H_V * D * 4 + H_V * 4 * 2
+STATE_BYTES = H_V * D * D * 4
+# algorithmic FLOPs per token and V head of the chunk form at C = 64 (triangles once)
+PREFILL_FLOP_PER_TOKEN = 4.25e6
+DECODE_BYTES_PER_SEQ = 2 * STATE_BYTES + H_QK * D * 2 * 2 + H_V * D * 2 + H_V * D * 4 + H_V * 8
+
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ---------------------------------------------------------------------------------
+# inputs
+
+
+def host_inputs(seed_base=100):
+    """The step's synthetic inputs on the host (bf16 bits for q/k/v)."""
+    from gated_deltanet_scan_gb300 import synth
+
+    pre = synth.make_workload("bench_prefill", [T_PREFILL], H_QK, H_V, D, 64, "bf16",
+                              seed=seed_base, state_std=0.02)
+    ver = synth.make_workload("bench_verify", [N_VERIFY], H_QK, H_V, D, 16, "bf16", seed=seed_base + 1)
+    dec = synth.make_workload("bench_decode", [1] * B_DECODE, H_QK, H_V, D, 64, "bf16",
+                              seed=seed_base + 2, state_std=0.02)
+    return pre, ver, dec
+
+
+def _pinned(torch, w):
+    def io(bits):
+        return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+
+    return dict(q=io(w.q_bits), k=io(w.k_bits), v=io(w.v_bits),
+                g=torch.from_numpy(np.ascontiguousarray(w.g)).pin_memory(),
+                beta=torch.from_numpy(np.ascontiguousarray(w.beta)).pin_memory())
+
+
+# ---------------------------------------------------------------------------------
+# clocks
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------------
+# our arm
+
+
+def traffic_record(kernel_file: str):
+    """dram bytes per launch from the committed ncu summary, if the kernel
+    source is unchanged since it was measured (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "gated_deltanet_scan_gb300", "csrc", kernel_file)
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    except (OSError, ValueError):
+        return None
+    r = rec.get(kernel_file)
+    if not r or r.get("source_sha256_16") != digest:
+        return None
+    return r.get("dram_bytes_per_launch")
+
+
+def run_ours(args):
+    import torch
+    import gated_deltanet_scan_gb300 as gdr
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+
+    pre, ver, dec = host_inputs()
+    hp, hv, hd = _pinned(torch, pre), _pinned(torch, ver), _pinned(torch, dec)
+    dp = {k: t.to(dev) for k, t in hp.items()}
+    dv = {k: t.to(dev) for k, t in hv.items()}
+    dd = {k: t.to(dev) for k, t in hd.items()}
+    state0 = torch.from_numpy(np.ascontiguousarray(pre.state0)).to(dev)
+    state = state0.clone()
+    snap = torch.empty_like(state)
+    dstate = torch.from_numpy(np.ascontiguousarray(dec.state0)).to(dev)
+    o_pre = torch.empty((T_PREFILL, H_V, D), dtype=torch.float32, device=dev)
+    o_ver = torch.empty((N_VERIFY, H_V, D), dtype=torch.float32, device=dev)
+    o_ref = torch.empty((N_ACCEPT, H_V, D), dtype=torch.float32, device=dev)
+    o_dec = torch.empty((B_DECODE, H_V, D), dtype=torch.float32, device=dev)
+    cu_pre = torch.tensor([0, T_PREFILL], dtype=torch.int32, device=dev)
+    cu_acc = torch.tensor([0, N_ACCEPT], dtype=torch.int32, device=dev)
+    acc = {k: t[:N_ACCEPT] for k, t in dv.items()}
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    only = args.only
+
+    def step(timers=None):
+        if timers is not None:
+            timers[0].record(stream)
+        if only in ("all", "prefill"):
+            gdr.gdr_prefill_chunked(dp["q"], dp["k"], dp["v"], dp["g"], dp["beta"], state, o_pre, cu_pre,
+                                    chunk=64, stream=stream)
+        if timers is not None:
+            timers[1].record(stream)
+        if only in ("all", "verify"):
+            gdr.gdr_verify_block(dv["q"], dv["k"], dv["v"], dv["g"], dv["beta"], state, snap, o_ver,
+                                 N_VERIFY, stream=stream)
+            gdr.gdr_state_restore(snap, state, stream=stream)
+            gdr.gdr_prefill_chunked(acc["q"], acc["k"], acc["v"], acc["g"], acc["beta"], state, o_ref,
+                                    cu_acc, chunk=64, stream=stream)
+        if timers is not None:
+            timers[2].record(stream)
+        if only in ("all", "decode"):
+            gdr.gdr_decode_step(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dstate, o_dec, stream=stream)
+        if timers is not None:
+            timers[3].record(stream)
+
+    launches_per_step = {"all": 5, "prefill": 1, "verify": 3, "decode": 1}[only]
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    timers = [[ev() for _ in range(4)] for _ in range(args.steps)]
+    t_start, t_end = ev(), ev()
+    barrier()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(timers[i])
+    t_end.record(stream)
+    barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    clk = clocks.stop()
+    assert gdr.gdr_device_error(stream=stream) == 0, "a device-side wait timed out"
+
+    prefill_ms = statistics.median(t[0].elapsed_time(t[1]) for t in timers)
+    verify_ms = statistics.median(t[1].elapsed_time(t[2]) for t in timers)
+    decode_ms = statistics.median(t[2].elapsed_time(t[3]) for t in timers)
+
+    # end to end through the same public API: pinned host inputs in, outputs back out
+    outs_host = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in (o_pre, o_ver, o_dec)]
+    h2d = sum(t.numel() * t.element_size() for d in (hp, hv, hd) for t in d.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs_host)
+    e2e_steps = max(3, min(args.steps, 20)) if only == "all" else 0
+
+    def e2e_step():
+        for src, dst in ((hp, dp), (hv, dv), (hd, dd)):
+            for k in src:
+                dst[k].copy_(src[k], non_blocking=True)
+        step()
+        for o, h in zip((o_pre, o_ver, o_dec), outs_host):
+            h.copy_(o, non_blocking=True)
+
+    e2e_ms = float("nan")
+    if e2e_steps:
+        e2e_step()
+        barrier()
+        e0, e1 = ev(), ev()
+        barrier()
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    ms_step = elapsed_ms / args.steps
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms_step, e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, e2e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        return None
+
+    peaks, peak_src = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    bf16 = peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"])
+    pre_bytes = T_PREFILL * PREFILL_BYTES_PER_TOKEN + 2 * STATE_BYTES
+    pre_gbs = pre_bytes / (prefill_ms * 1e-3) / 1e9
+    pre_tflops = PREFILL_FLOP_PER_TOKEN * T_PREFILL / (prefill_ms * 1e-3) / 1e12
+    dec_bytes = B_DECODE * DECODE_BYTES_PER_SEQ
+    dec_gbs = dec_bytes / (decode_ms * 1e-3) / 1e9
+    traffic = traffic_record("gdr_prefill_tc.cu")
+    value = world * TOKENS_PER_STEP / (ms_step * 1e-3)
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64; Qwen3.5-9B linear-attention shapes)",
+        "config": {
+            "workload": "gated delta rule, Qwen3.5-9B layer: prefill B=1 T=16384 + 16-token verify "
+                        "with snapshot/restore/re-feed of 7 + decode step B=64",
+            "h_qk": H_QK, "h_v": H_V, "d_k": D, "d_v": D, "chunk": 64,
+            "io": "q/k/v bf16, g/beta fp32, state fp32, o fp32",
+            "tokens_per_step": TOKENS_PER_STEP,
+            "l2": "inputs larger than L2 (no flush)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "components": {
+            "prefill_T16384": {"ms": prefill_ms, "tokens_per_s": T_PREFILL / (prefill_ms * 1e-3),
+                               "hbm_gbs": pre_gbs, "frac_hbm": pre_gbs / hbm,
+                               "alg_tflops": pre_tflops, "frac_bf16": pre_tflops / bf16},
+            "verify16_restore_refeed7": {"ms": verify_ms},
+            "decode_B64": {"ms": decode_ms, "tokens_per_s": B_DECODE / (decode_ms * 1e-3),
+                           "hbm_gbs": dec_gbs, "frac_hbm": dec_gbs / hbm},
+        },
+        "roofline": {
+            "kernel": "prefill_tc_kernel",
+            "bound": "hbm",
+            "achieved": pre_gbs,
+            "peak": hbm,
+            "unit": "GB/s",
+            "frac": pre_gbs / hbm,
+            "peak_source": f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": pre_bytes,
+        },
+        "e2e": {"value": world * TOKENS_PER_STEP / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if only != "all":
+        line["partial_step"] = only  # a profiling run of one component, not a bench line
+        line.pop("e2e")
+    elif not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample(pre, ver, dec)
+    return line
+
+
+# ---------------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+
+
+def oracle_step_sample(pre, ver, dec, heads):
+    """The oracle over the step's tokens for `heads` of the 32 V heads (and their QK
+    heads); returns (seconds, threads)."""
+    import oracle
+
+    hv = list(range(heads))
+    hq = sorted({h // (H_V // H_QK) for h in hv})
+    threads = oracle.default_threads()
+
+    def sub(w, state0):
+        # V heads [0, heads) read QK heads [0, heads/2): keep the head map intact
+        return (w.cu_seqlens, w.q[:, hq], w.k[:, hq], w.v[:, hv], w.g[:, hv], w.beta[:, hv], state0[:, hv])
+
+    t0 = time.perf_counter()
+    _, s_pre = oracle.gdr_sequential(*sub(pre, pre.state0), threads=threads)
+    oracle.gdr_sequential(ver.cu_seqlens, ver.q[:, hq], ver.k[:, hq], ver.v[:, hv], ver.g[:, hv],
+                          ver.beta[:, hv], s_pre, threads=threads)
+    acc = slice(0, N_ACCEPT)
+    oracle.gdr_sequential([0, N_ACCEPT], ver.q[acc][:, hq], ver.k[acc][:, hq], ver.v[acc][:, hv],
+                          ver.g[acc][:, hv], ver.beta[acc][:, hv], s_pre, threads=threads)
+    oracle.gdr_sequential(*sub(dec, dec.state0), threads=threads)
+    return time.perf_counter() - t0, threads
+
+
+REF_HEADS = 4  # reference-arm step: 4 of the 32 V heads (2 of 16 QK heads), scaled to 32
+
+
+def cpu_baseline_sample(pre, ver, dec, min_seconds=10.0, max_seconds=30.0):
+    """The oracle, as it stands, over whole steps (all 32 heads) until about
+    10 s of CPU work has accumulated."""
+    secs, n = 0.0, 0
+    threads = 1
+    while secs < min_seconds and (n == 0 or secs + secs / n <= max_seconds):
+        s, threads = oracle_step_sample(pre, ver, dec, H_V)
+        secs += s
+        n += 1
+    value = n * TOKENS_PER_STEP / secs
+    return {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} full step(s) (prefill T=16384 + verify 16 + re-feed 7 + decode B=64, all 32 V "
+                      f"heads), {secs:.1f} s of fp64 CPU work on {threads} threads"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    pre, ver, dec = host_inputs()
+    times = []
+    threads = 1
+    for i in range(args.warmup + args.steps):
+        secs, threads = oracle_step_sample(pre, ver, dec, REF_HEADS)
+        if i >= args.warmup:
+            times.append(secs)
+    ms = 1e3 * statistics.mean(times) * (H_V / REF_HEADS)  # per full 32-head step
+    value = TOKENS_PER_STEP / (ms * 1e-3)
+    sample = (f"each step: the fp64 oracle over one full step's tokens on {REF_HEADS} of 32 V heads, "
+              f"scaled to 32 heads")
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (same inputs as the GPU arm)",
+        "config": {"workload": "gated delta rule, Qwen3.5-9B layer: prefill B=1 T=16384 + 16-token verify "
+                               "with snapshot/restore/re-feed of 7 + decode step B=64",
+                   "h_qk": H_QK, "h_v": H_V, "d_k": D, "d_v": D},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["all", "prefill", "verify", "decode"], default="all",
+                    help="run one component of the step (for profiling); the default runs the full step")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    line = run_ours(args) if args.impl == "ours" else run_reference(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

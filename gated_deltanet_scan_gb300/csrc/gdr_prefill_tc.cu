@@ -1,11 +1,666 @@
-// Tensor-core (tcgen05) chunked prefill -- placeholder until the kernel lands.
+// Chunked prefill on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Shapes: d_k = d_v = 128, 64-token chunks, bf16 q/k/v, fp32 state, fp32 or
+// bf16 output.  One CTA owns (sequence, V head, 64 state columns) and walks
+// that sequence's chunks in order, keeping its 128 x 64 block of the state on
+// chip for the whole sequence (fp32 in registers, bf16 hi/lo copies in shared
+// memory as MMA operands).
+//
+// Per chunk (the chunkwise-parallel form of the Qwen3.5-9B NPU model card,
+// "How it works"; forward substitution for the unit triangular factor as in
+// the Candle PR's chunked scan; log-space masking from its overflow fix):
+//   G   = inclusive running sum of g over the chunk (padding rows: g = beta = 0)
+//   G1  [K Kᵀ; Q Kᵀ] = [K; Q] Kᵀ                         (one M=128 MMA, exact bf16)
+//   N   = diag(beta) (K Kᵀ ⊙ exp(G_t - G_j))_{j<t},  P = (Q Kᵀ ⊙ exp(G_t - G_j))_{j<=t}
+//         (the exponent is only formed on the kept triangle, so it is <= 0)
+//   T   = (I + N)^-1   (16x16 forward substitution + blocked off-diagonal solves)
+//   PT  = P T
+//   MMA1 [K S; Q S] = [K; Q] S                            (S as bf16 hi + lo)
+//   R   = diag(beta) (V - diag(e^G) K S)
+//   MMA2 [D; P D] = [T; PT] R                             (hi/lo on both sides)
+//   O   = scale (diag(e^G) Q S + P D)
+//   MMA3 Y = Kᵀ D~,  D~ = diag(exp(G_C - G)) D            (D~ as hi + lo)
+//   S  <- exp(G_C) S + Y
+// which is D = (I + N)^-1 diag(beta)(V - diag(e^G) K S0), O = diag(e^G) Q S0 + P D,
+// S_C = e^{G_C} S0 + Kᵀ diag(e^{G_C - G}) D written as products on the tensor
+// cores.  The bf16 hi/lo split (x = hi + lo, both bf16) keeps every product
+// that feeds the state within ~2^-16 relative; K, Q and V are exact in bf16.
+//
+// Warp roles (384 threads).  Warps 0-3, the "chain", own TMEM lanes 0-127 and
+// run the state-dependent MMA1 -> MMA2 -> MMA3 sequence of chunk c.  Warps
+// 4-11, "stage 1", meanwhile prepare chunk c+1: gates, the Gram MMA, N and P,
+// the triangular inverse and P T, and stage [T; PT] for the chain.  They hand
+// over through mbarriers: TMA -> both roles (tiles landed), stage 1 -> chain
+// ([T; PT] and gates ready), chain -> stage 1 ([T; PT] buffer free again).
+// The chain issues the TMA for chunk c+2 into chunk c's buffers once its last
+// MMA on them has completed.
+//
+// Every mbarrier wait is bounded: on timeout a thread records
+// GDR_ERR_DEVICE_TIMEOUT in the device error word and its role stops; the
+// other role then times out on its own next wait, waits (bounded) for any
+// outstanding TMA, and the CTA frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "gdr_common.cuh"
 #include "gdr_internal.h"
+#include "tc_ptx.cuh"
 
 namespace gdr {
 
 static __device__ int32_t g_device_error;
 
-cudaError_t launch_prefill_tc(const Args &a, cudaStream_t s) { return launch_chunk_cc(a, s); }
+namespace {
+
+using namespace tc;
+
+constexpr int C = 64;
+constexpr int D = 128;
+constexpr int BV = 64;
+constexpr int NCHAIN = 128;  // warps 0-3
+constexpr int NS1 = 256;     // warps 4-11
+constexpr int NTHREADS = NCHAIN + NS1;
+constexpr int SROW = 68;  // fp32 scratch row stride in floats (bank-conflict-free float4 rows)
+constexpr uint32_t BAR_CHAIN = 1, BAR_S1 = 2;  // named barrier ids
+constexpr int ROLE_CHAIN = 0, ROLE_S1 = 1;
+
+// Shared memory map, bytes from a 1024-byte aligned base.
+constexpr uint32_t KQ_BYTES = 32768;  // [kb=0: K rows 0-63, Q rows 64-127][kb=1: same], 128-B rows
+constexpr uint32_t V_BYTES = 8192;    // V tile: 64 tokens x 64 columns
+constexpr uint32_t OFF_KQ = 0;        // two buffers
+constexpr uint32_t OFF_V = 2 * KQ_BYTES;                // two buffers
+constexpr uint32_t OFF_ATP_HI = OFF_V + 2 * V_BYTES;  // [T; PT] as K-major 128 x 64 bf16
+constexpr uint32_t OFF_ATP_LO = OFF_ATP_HI + 16384;
+constexpr uint32_t OFF_S_HI = OFF_ATP_LO + 16384;  // state block as MN-major 128 (k) x 64 (n) bf16
+constexpr uint32_t OFF_S_LO = OFF_S_HI + 16384;
+constexpr uint32_t OFF_RD_HI = OFF_S_LO + 16384;  // R, then D~: MN-major 64 (k = token) x 64 (n)
+constexpr uint32_t OFF_RD_LO = OFF_RD_HI + 8192;
+constexpr uint32_t SCR_MAT = 64 * SROW * 4;       // fp32 [64][SROW]
+constexpr uint32_t OFF_N = OFF_RD_LO + 8192;      // N, later PT
+constexpr uint32_t OFF_T = OFF_N + SCR_MAT;
+constexpr uint32_t OFF_P = OFF_T + SCR_MAT;
+constexpr uint32_t XBLK = 16 * 17;                // one 16x16 partial block, padded rows
+constexpr uint32_t OFF_X = OFF_P + SCR_MAT;       // up to 3 partial blocks
+constexpr uint32_t OFF_SMALL = OFF_X + 3 * XBLK * 4;
+constexpr uint32_t SM_GATES = OFF_SMALL;          // float [2 chunks][3][64]: G, beta, e^G
+constexpr uint32_t SM_SCAN = OFF_SMALL + 1536;    // float[4]
+constexpr uint32_t SM_BARS = OFF_SMALL + 1600;    // 8 x uint64
+constexpr uint32_t SM_TMEM = OFF_SMALL + 1664;    // uint32
+constexpr uint32_t SM_ABORT = OFF_SMALL + 1672;   // int32[2], one per role
+constexpr uint32_t SMEM_USED = OFF_SMALL + 2048;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(OFF_RD_HI % 1024 == 0 && OFF_RD_LO % 1024 == 0 && OFF_ATP_HI % 1024 == 0 && OFF_S_LO % 1024 == 0,
+              "operand tiles must be 1 KB aligned");
+
+// mbarriers
+constexpr int B_TMA0 = 0, B_MMA_CHAIN = 2, B_MMA_S1 = 3, B_ATP_FULL = 4, B_ATP_FREE = 5;
+
+// TMEM columns (fp32 accumulators, lane = row).
+constexpr uint32_t TM_G1 = 0;    // [K Kᵀ; Q Kᵀ]   (stage 1)
+constexpr uint32_t TM_KS = 64;   // [K S; Q S]     (chain)
+constexpr uint32_t TM_DP = 128;  // [D; P D]       (chain)
+constexpr uint32_t TM_Y = 192;   // Kᵀ D~          (chain)
+constexpr uint32_t TM_COLS = 256;
+
+constexpr uint32_t TMA_BYTES = 2 * 16384 + V_BYTES;  // K + Q (two 64-column halves each) + V
+constexpr long long kWaitLimit = 4000000000LL;       // SM clocks (about 2 s)
+
+constexpr uint32_t IDESC_G1 = idesc_bf16_f32(128, 64, 0, 0);  // A K-major, B K-major
+constexpr uint32_t IDESC_KS = idesc_bf16_f32(128, 64, 0, 1);  // A K-major, B MN-major
+constexpr uint32_t IDESC_DP = idesc_bf16_f32(128, 64, 0, 1);
+constexpr uint32_t IDESC_Y = idesc_bf16_f32(128, 64, 1, 1);   // A MN-major (Kᵀ), B MN-major
+
+struct TcParams {
+    int h_qk, h_v, out_bf16;
+    float scale;
+    const int32_t *cu_seqlens;
+    const float *g, *beta;
+    float *state;
+    void *o;
+};
+
+struct Ctx {
+    uint8_t *sm;
+    uint32_t sbase;
+    uint32_t tmem;
+    volatile int *abort_flag;
+    __device__ uint32_t bar(int i) const { return sbase + SM_BARS + 8 * i; }
+    __device__ float *gates(int buf) const { return reinterpret_cast<float *>(sm + SM_GATES) + buf * 192; }
+};
+
+// Bounded wait shared by all threads of one role (the chain's 128 or stage 1's
+// 256).  A thread whose wait times out records the error and raises its role's
+// abort flag; the role barrier that follows makes every thread of the role read
+// the same flag, so the role leaves its loop together and never strands a
+// sibling at a later barrier.  Each role reads only its own flag.
+__device__ __forceinline__ bool role_wait(const Ctx &x, uint32_t bar, uint32_t parity, int role) {
+    if (!mbar_wait_bounded(bar, parity, kWaitLimit)) {
+        x.abort_flag[role] = 1;
+        atomicCAS(&g_device_error, 0, (int32_t)GDR_ERR_DEVICE_TIMEOUT);
+    }
+    if (role == ROLE_CHAIN)
+        named_sync(BAR_CHAIN, NCHAIN);
+    else
+        named_sync(BAR_S1, NS1);
+    return x.abort_flag[role] == 0;
+}
+
+__device__ __forceinline__ void issue_chunk_loads(const Ctx &x, int buf, int tok, int hq, int h, int cb,
+                                                  const CUtensorMap *tmK, const CUtensorMap *tmQ,
+                                                  const CUtensorMap *tmV) {
+    const uint32_t bar = x.bar(B_TMA0 + buf);
+    mbar_arrive_expect_tx(bar, TMA_BYTES);
+    const uint32_t kq = x.sbase + OFF_KQ + buf * KQ_BYTES;
+    tma_load_3d(kq, tmK, bar, 0, hq, tok);
+    tma_load_3d(kq + 16384, tmK, bar, 64, hq, tok);
+    tma_load_3d(kq + 8192, tmQ, bar, 0, hq, tok);
+    tma_load_3d(kq + 16384 + 8192, tmQ, bar, 64, hq, tok);
+    tma_load_3d(x.sbase + OFF_V + buf * V_BYTES, tmV, bar, cb * BV, h, tok);
+}
+
+__device__ __forceinline__ void store_row_hilo(uint8_t *hi, uint8_t *lo, int row, const float *x) {
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) store_hilo_chunk(hi, lo, row, ch, x + ch * 8);
+}
+
+// ================================ stage 1 ===========================================
+// T = (I + N)^-1 for strictly lower N, then PT = P T; s = stage-1 thread index (0..255).
+__device__ void stage1_inverse_and_pt(uint8_t *sm, int s) {
+    float *N = reinterpret_cast<float *>(sm + OFF_N);
+    float *T = reinterpret_cast<float *>(sm + OFF_T);
+    const float *P = reinterpret_cast<const float *>(sm + OFF_P);
+    float *X = reinterpret_cast<float *>(sm + OFF_X);
+
+    // blocks above the block diagonal of T are zero (6 blocks x 256 entries)
+#pragma unroll
+    for (int n = 0; n < 6; ++n) {
+        const int e = s + NS1 * n, b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+        const int I = b < 3 ? 0 : (b < 5 ? 1 : 2);
+        const int J = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
+        T[(16 * I + r) * SROW + 16 * J + cc] = 0.f;
+    }
+    // 16 x 16 diagonal blocks by forward substitution, one column per thread
+    if (s < 64) {
+        const int base = (s >> 4) * 16, jj = s & 15;
+        float col[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float a0 = (r == jj) ? 1.f : 0.f, a1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                if (m < r && m >= jj) {
+                    const float nv = N[(base + r) * SROW + base + m];
+                    if (m & 1)
+                        a1 = fmaf(-nv, col[m], a1);
+                    else
+                        a0 = fmaf(-nv, col[m], a0);
+                }
+            }
+            col[r] = a0 + a1;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) T[(base + r) * SROW + base + jj] = col[r];
+    }
+    named_sync(BAR_S1, NS1);
+    // blocks below the diagonal, nearest first: T_IJ = -T_II sum_{J<=M<I} N_IM T_MJ
+#pragma unroll
+    for (int dist = 1; dist <= 3; ++dist) {
+        const int nblk = 4 - dist;
+        for (int e = s; e < nblk * 256; e += NS1) {
+            const int J = e >> 8, I = J + dist, r = (e >> 4) & 15, cc = e & 15;
+            float a0 = 0.f, a1 = 0.f;
+            for (int M = J; M < I; ++M) {
+                const float *nr = N + (16 * I + r) * SROW + 16 * M;
+                const float *tc = T + (16 * M) * SROW + 16 * J + cc;
+#pragma unroll
+                for (int m = 0; m < 16; m += 2) {
+                    a0 = fmaf(nr[m], tc[m * SROW], a0);
+                    a1 = fmaf(nr[m + 1], tc[(m + 1) * SROW], a1);
+                }
+            }
+            X[J * XBLK + r * 17 + cc] = a0 + a1;
+        }
+        named_sync(BAR_S1, NS1);
+        for (int e = s; e < nblk * 256; e += NS1) {
+            const int J = e >> 8, I = J + dist, r = (e >> 4) & 15, cc = e & 15;
+            const float *tr = T + (16 * I + r) * SROW + 16 * I;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; m += 2) {
+                a0 = fmaf(tr[m], X[J * XBLK + m * 17 + cc], a0);
+                a1 = fmaf(tr[m + 1], X[J * XBLK + (m + 1) * 17 + cc], a1);
+            }
+            T[(16 * I + r) * SROW + 16 * J + cc] = -(a0 + a1);
+        }
+        named_sync(BAR_S1, NS1);
+    }
+    // PT = P T over the 4 x 4 block grid (N is dead: PT takes its place).  Each
+    // thread owns one entry of every block, so the triangular work is balanced.
+    float *PT = N;
+#pragma unroll
+    for (int b = 0; b < 16; ++b) {
+        const int I = b >> 2, J = b & 3, r = s >> 4, cc = s & 15;
+        float a0 = 0.f, a1 = 0.f;
+        if (I >= J) {
+            for (int M = J; M <= I; ++M) {
+                const float *pr = P + (16 * I + r) * SROW + 16 * M;
+                const float *tc = T + (16 * M) * SROW + 16 * J + cc;
+#pragma unroll
+                for (int m = 0; m < 16; m += 2) {
+                    a0 = fmaf(pr[m], tc[m * SROW], a0);
+                    a1 = fmaf(pr[m + 1], tc[(m + 1) * SROW], a1);
+                }
+            }
+        }
+        PT[(16 * I + r) * SROW + 16 * J + cc] = a0 + a1;
+    }
+}
+
+__device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t t1, int nchunks, int h,
+                            const int tid) {
+    const int s = tid - NCHAIN;  // 0..255
+    const int warp = tid >> 5, lane = tid & 31;
+    const uint32_t tmem = x.tmem;
+    float *sScan = reinterpret_cast<float *>(x.sm + SM_SCAN);
+    for (int c = 0; c < nchunks; ++c) {
+        const int buf = c & 1;
+        const int64_t c0 = t0 + (int64_t)c * C;
+        const int L = (int)((t1 - c0) < C ? (t1 - c0) : C);
+        // the chunk's tiles (issued by the chain once chunk c-2 released the buffer)
+        if (!role_wait(x, x.bar(B_TMA0 + buf), (uint32_t)(c >> 1) & 1u, ROLE_S1)) break;
+
+        // gates: G = inclusive running sum of g (padding rows: g = 0, beta = 0)
+        float *gts = x.gates(buf);
+        float gt = 0.f;
+        if (s < C) {
+            float bt = 0.f;
+            if (s < L) {
+                gt = p.g[(size_t)(c0 + s) * p.h_v + h];
+                bt = p.beta[(size_t)(c0 + s) * p.h_v + h];
+            }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float u = __shfl_up_sync(0xffffffffu, gt, o);
+                if (lane >= o) gt += u;
+            }
+            if (lane == 31) sScan[s >> 5] = gt;
+            gts[64 + s] = bt;
+        }
+        // Gram products of the chunk: [K Kᵀ; Q Kᵀ] into TMEM
+        if (s == 0) {
+            tc_fence_after_sync();  // the previous chunk's reads of these TMEM columns are done
+            const uint32_t kq = x.sbase + OFF_KQ + buf * KQ_BYTES;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
+                const uint64_t a = smem_desc_sw128(kq + koff, 16, 1024);
+                mma_bf16(tmem + TM_G1, a, a, IDESC_G1, ks > 0);
+            }
+            mma_commit(x.bar(B_MMA_S1));
+        }
+        named_sync(BAR_S1, NS1);
+        if (s < C) {
+            if (s >= 32) gt += sScan[0];
+            gts[s] = gt;
+            gts[128 + s] = __expf(gt);
+        }
+        if (!role_wait(x, x.bar(B_MMA_S1), (uint32_t)c & 1u, ROLE_S1)) break;  // also publishes the gates
+        tc_fence_after_sync();
+        {
+            // row t = lane quarter of this warp; columns [32*half, 32*half + 32)
+            const int row = ((warp & 3) << 5) + lane;
+            const int half = (warp - 4) >> 2;
+            float a[32];
+            tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + TM_G1 + 32 * half, a);
+            const bool is_n = row < 64;
+            const int t = row & 63;
+            const float Gt = gts[t];
+            const float w = is_n ? gts[64 + t] : 1.f;
+            float *dst = reinterpret_cast<float *>(x.sm + (is_n ? OFF_N : OFF_P)) + t * SROW + 32 * half;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                float v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int jj = 32 * half + j + e;
+                    const bool keep = is_n ? (jj < t) : (jj <= t);
+                    v[e] = keep ? w * __expf(Gt - gts[jj]) * a[j + e] : 0.f;
+                }
+                *reinterpret_cast<float4 *>(dst + j) = make_float4(v[0], v[1], v[2], v[3]);
+            }
+        }
+        tc_fence_before_sync();
+        named_sync(BAR_S1, NS1);
+        stage1_inverse_and_pt(x.sm, s);
+        named_sync(BAR_S1, NS1);
+
+        // [T; PT] buffer: free once the chain's MMA2 of chunk c-1 has completed
+        if (c > 0 && !role_wait(x, x.bar(B_ATP_FREE), (uint32_t)(c - 1) & 1u, ROLE_S1)) break;
+        {
+            const int row = s & 127, half = s >> 7;
+            const float *src = reinterpret_cast<const float *>(x.sm + (row < 64 ? OFF_T : OFF_N)) +
+                               (row & 63) * SROW + 32 * half;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                const float4 u = *reinterpret_cast<const float4 *>(src + 8 * ch);
+                const float4 v = *reinterpret_cast<const float4 *>(src + 8 * ch + 4);
+                const float xv[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+                store_hilo_chunk(x.sm + OFF_ATP_HI, x.sm + OFF_ATP_LO, row, 4 * half + ch, xv);
+            }
+        }
+        fence_proxy_async_smem();
+        named_sync(BAR_S1, NS1);
+        if (s == 0) mbar_arrive(x.bar(B_ATP_FULL));
+    }
+}
+
+// ================================= chain ============================================
+__device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t t1, int nchunks, int h, int hq,
+                           int cb, float *Sr, const CUtensorMap *tmK, const CUtensorMap *tmQ,
+                           const CUtensorMap *tmV, const int tid, bool &ok) {
+    const int warp = tid >> 5;
+    const uint32_t tmem = x.tmem;
+    uint32_t mma_phase = 0;
+    for (int c = 0; c < nchunks; ++c) {
+        const int buf = c & 1;
+        const int64_t c0 = t0 + (int64_t)c * C;
+        const int L = (int)((t1 - c0) < C ? (t1 - c0) : C);
+        const uint32_t kq = x.sbase + OFF_KQ + buf * KQ_BYTES;
+        if (!role_wait(x, x.bar(B_TMA0 + buf), (uint32_t)(c >> 1) & 1u, ROLE_CHAIN)) break;
+
+        // ---- MMA1: [K S; Q S] = [K; Q] (S_hi + S_lo) --------------------------------
+        if (tid == 0) {
+            tc_fence_after_sync();
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
+                const uint64_t a = smem_desc_sw128(kq + koff, 16, 1024);
+                const uint64_t bh = smem_desc_sw128(x.sbase + OFF_S_HI + ks * 2048, 16, 1024);
+                const uint64_t bl = smem_desc_sw128(x.sbase + OFF_S_LO + ks * 2048, 16, 1024);
+                mma_bf16(tmem + TM_KS, a, bh, IDESC_KS, ks > 0);
+                mma_bf16(tmem + TM_KS, a, bl, IDESC_KS, 1);
+            }
+            mma_commit(x.bar(B_MMA_CHAIN));
+        }
+        // stage 1 of this chunk: gates and [T; PT]
+        if (!role_wait(x, x.bar(B_ATP_FULL), (uint32_t)c & 1u, ROLE_CHAIN)) break;
+        const float *gts = x.gates(buf);
+        const int t = tid & 63;
+        const float Gt = gts[t], bt = gts[64 + t], egt = gts[128 + t];
+        const float eGC = gts[128 + C - 1], GC = gts[C - 1];
+        if (!role_wait(x, x.bar(B_MMA_CHAIN), mma_phase, ROLE_CHAIN)) break;
+        mma_phase ^= 1;
+        tc_fence_after_sync();
+        if (tid < 64) {
+            // R = beta (V - e^G K S), staged as the hi/lo MN-major B operand of MMA2
+            const uint8_t *vt = x.sm + OFF_V + buf * V_BYTES;
+            const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + TM_KS;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float a[32];
+                tmem_ld32(taddr + 32 * half, a);
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    float v[8], r[8];
+                    load_bf16_chunk(vt, t, 4 * half + ch, v);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) r[e] = bt * (v[e] - egt * a[ch * 8 + e]);
+                    store_hilo_chunk(x.sm + OFF_RD_HI, x.sm + OFF_RD_LO, t, 4 * half + ch, r);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        named_sync(BAR_CHAIN, NCHAIN);
+
+        // ---- MMA2: [D; P D] = [T; PT] R ---------------------------------------------
+        if (tid == 0) {
+            tc_fence_after_sync();
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t ah = smem_desc_sw128(x.sbase + OFF_ATP_HI + ks * 32, 16, 1024);
+                const uint64_t al = smem_desc_sw128(x.sbase + OFF_ATP_LO + ks * 32, 16, 1024);
+                const uint64_t bh = smem_desc_sw128(x.sbase + OFF_RD_HI + ks * 2048, 16, 1024);
+                const uint64_t bl = smem_desc_sw128(x.sbase + OFF_RD_LO + ks * 2048, 16, 1024);
+                mma_bf16(tmem + TM_DP, ah, bh, IDESC_DP, ks > 0);
+                mma_bf16(tmem + TM_DP, al, bh, IDESC_DP, 1);
+                mma_bf16(tmem + TM_DP, ah, bl, IDESC_DP, 1);
+            }
+            mma_commit(x.bar(B_MMA_CHAIN));
+        }
+        if (!role_wait(x, x.bar(B_MMA_CHAIN), mma_phase, ROLE_CHAIN)) break;
+        mma_phase ^= 1;
+        tc_fence_after_sync();
+        if (tid == 0) mbar_arrive(x.bar(B_ATP_FREE));  // stage 1 may overwrite [T; PT]
+        {
+            const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+            if (tid < 64) {
+                // D~ = exp(G_C - G_t) D, staged as the hi/lo MN-major B operand of MMA3
+                const float sc = __expf(GC - Gt);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float dd[32];
+                    tmem_ld32(lane_base + TM_DP + 32 * half, dd);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) dd[j] *= sc;
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch)
+                        store_hilo_chunk(x.sm + OFF_RD_HI, x.sm + OFF_RD_LO, t, 4 * half + ch, dd + 8 * ch);
+                }
+            } else {
+                // O = scale (e^G Q S + P D) for the chunk's real rows
+                const size_t off = ((size_t)(c0 + t) * p.h_v + h) * D + cb * BV;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float pd[32], qs[32];
+                    tmem_ld32(lane_base + TM_DP + 32 * half, pd);
+                    tmem_ld32(lane_base + TM_KS + 32 * half, qs);
+                    if (t < L) {
+                        if (p.out_bf16) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + off + 32 * half);
+#pragma unroll
+                            for (int j = 0; j < 32; j += 8) {
+                                float y[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) y[e] = p.scale * fmaf(egt, qs[j + e], pd[j + e]);
+                                dst[j / 8] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                                                        pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+                            }
+                        } else {
+                            float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + off + 32 * half);
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4)
+                                dst[j / 4] = make_float4(p.scale * fmaf(egt, qs[j], pd[j]),
+                                                         p.scale * fmaf(egt, qs[j + 1], pd[j + 1]),
+                                                         p.scale * fmaf(egt, qs[j + 2], pd[j + 2]),
+                                                         p.scale * fmaf(egt, qs[j + 3], pd[j + 3]));
+                        }
+                    }
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        named_sync(BAR_CHAIN, NCHAIN);
+
+        // ---- MMA3: Y = Kᵀ (D~_hi + D~_lo) ---------------------------------------------
+        if (tid == 0) {
+            tc_fence_after_sync();
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t a = smem_desc_sw128(kq + ks * 2048, 16384, 1024);
+                const uint64_t bh = smem_desc_sw128(x.sbase + OFF_RD_HI + ks * 2048, 16, 1024);
+                const uint64_t bl = smem_desc_sw128(x.sbase + OFF_RD_LO + ks * 2048, 16, 1024);
+                mma_bf16(tmem + TM_Y, a, bh, IDESC_Y, ks > 0);
+                mma_bf16(tmem + TM_Y, a, bl, IDESC_Y, 1);
+            }
+            mma_commit(x.bar(B_MMA_CHAIN));
+        }
+        if (!role_wait(x, x.bar(B_MMA_CHAIN), mma_phase, ROLE_CHAIN)) break;
+        mma_phase ^= 1;
+        tc_fence_after_sync();
+        // chunk c's tiles are no longer read: fetch chunk c+2 into them
+        if (tid == 0 && c + 2 < nchunks) {
+            fence_proxy_async_smem();
+            issue_chunk_loads(x, buf, (int)(c0 + 2 * C), hq, h, cb, tmK, tmQ, tmV);
+        }
+        {
+            const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + TM_Y;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float y[32];
+                tmem_ld32(taddr + 32 * half, y);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) Sr[32 * half + j] = fmaf(eGC, Sr[32 * half + j], y[j]);
+            }
+            store_row_hilo(x.sm + OFF_S_HI, x.sm + OFF_S_LO, tid, Sr);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        named_sync(BAR_CHAIN, NCHAIN);
+    }
+    ok = (x.abort_flag[ROLE_CHAIN] == 0);
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmV, TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    Ctx x;
+    x.sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    x.sbase = smem_u32(x.sm);
+    x.abort_flag = reinterpret_cast<volatile int *>(x.sm + SM_ABORT);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(x.sm + SM_TMEM);
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int cb = blockIdx.x & 1;
+    const int h = (blockIdx.x >> 1) % p.h_v;
+    const int s = (blockIdx.x >> 1) / p.h_v;
+    const int hq = h / (p.h_v / p.h_qk);
+    const int64_t t0 = p.cu_seqlens[s], t1 = p.cu_seqlens[s + 1];
+    const int nchunks = (int)((t1 - t0 + C - 1) / C);
+
+    if (tid == 0) {
+        for (int i = 0; i < 6; ++i) mbar_init(x.bar(i), 1);
+        x.abort_flag[0] = 0;
+        x.abort_flag[1] = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_holder), TM_COLS);
+        tmem_relinquish();
+    }
+    // chain thread `tid` owns row `tid` (a d_k index) of the 128 x 64 state block
+    float Sr[BV];
+    float *Sg = p.state + (((size_t)s * p.h_v + h) * D + (tid & 127)) * D + cb * BV;
+    if (tid < NCHAIN) {
+#pragma unroll
+        for (int j = 0; j < BV; j += 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(Sg + j);
+            Sr[j] = v.x;
+            Sr[j + 1] = v.y;
+            Sr[j + 2] = v.z;
+            Sr[j + 3] = v.w;
+        }
+        store_row_hilo(x.sm + OFF_S_HI, x.sm + OFF_S_LO, tid, Sr);
+        fence_proxy_async_smem();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    x.tmem = *tmem_holder;
+
+    if (tid == 0) {
+        if (nchunks > 0) issue_chunk_loads(x, 0, (int)t0, hq, h, cb, &tmK, &tmQ, &tmV);
+        if (nchunks > 1) issue_chunk_loads(x, 1, (int)(t0 + C), hq, h, cb, &tmK, &tmQ, &tmV);
+    }
+
+    bool ok = true;
+    if (tid < NCHAIN)
+        chain_role(x, p, t0, t1, nchunks, h, hq, cb, Sr, &tmK, &tmQ, &tmV, tid, ok);
+    else
+        stage1_role(x, p, t0, t1, nchunks, h, tid);
+
+    if (tid < NCHAIN) {
+        if (ok) {
+#pragma unroll
+            for (int j = 0; j < BV; j += 4)
+                *reinterpret_cast<float4 *>(Sg + j) = make_float4(Sr[j], Sr[j + 1], Sr[j + 2], Sr[j + 3]);
+        } else if (tid == 0) {
+            // let any outstanding tile load land before the CTA's shared memory is released
+            for (int b = 0; b < 2; ++b) {
+                mbar_wait_bounded(x.bar(B_TMA0 + b), 0, kWaitLimit / 8);
+                mbar_wait_bounded(x.bar(B_TMA0 + b), 1, kWaitLimit / 8);
+            }
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after_sync();
+        tmem_dealloc(x.tmem, TM_COLS);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// bf16 tensor [d2][d1][d0] (d0 contiguous), box {64, 1, 64}, 128-byte swizzle.
+bool encode_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const Args &a, cudaStream_t s) {
+    if (a.n_seqs == 0 || a.t_total == 0) return cudaSuccess;  // every sequence empty: state unchanged
+    CUtensorMap tmK, tmQ, tmV;
+    if (!encode_bf16_3d(&tmK, a.k, D, (uint64_t)a.h_qk, (uint64_t)a.t_total) ||
+        !encode_bf16_3d(&tmQ, a.q, D, (uint64_t)a.h_qk, (uint64_t)a.t_total) ||
+        !encode_bf16_3d(&tmV, a.v, D, (uint64_t)a.h_v, (uint64_t)a.t_total))
+        return cudaErrorInvalidValue;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    TcParams p;
+    p.h_qk = a.h_qk;
+    p.h_v = a.h_v;
+    p.out_bf16 = a.out_bf16;
+    p.scale = a.scale;
+    p.cu_seqlens = a.cu_seqlens;
+    p.g = a.g;
+    p.beta = a.beta;
+    p.state = a.state;
+    p.o = a.o;
+    const unsigned blocks = (unsigned)a.n_seqs * (unsigned)a.h_v * (unsigned)(D / BV);
+    prefill_tc_kernel<<<blocks, NTHREADS, SMEM_BYTES, s>>>(tmK, tmQ, tmV, p);
+    return cudaGetLastError();
+}
 
 cudaError_t read_clear_device_error(cudaStream_t s, int32_t *code) {
     cudaError_t e = cudaStreamSynchronize(s);

@@ -27,7 +27,9 @@ uint16) and the exact values they encode (float32).
 
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
+import os
 import zlib
 from typing import Dict, List, Optional
 
@@ -36,7 +38,7 @@ import numpy as np
 _GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
-_BLOCK = 1 << 22
+_BLOCK = 1 << 18
 
 
 def _mix64(z: np.ndarray) -> np.ndarray:
@@ -53,6 +55,29 @@ def _scalar_mix64(x: int) -> int:
     return x ^ (x >> 31)
 
 
+def _pool():
+    global _POOL
+    if _POOL is None:
+        _POOL = concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(16, os.cpu_count() or 1)))
+    return _POOL
+
+
+_POOL = None
+
+
+def _for_blocks(n: int, fn) -> None:
+    """Run fn(lo, hi) over [0, n) in blocks; numpy releases the GIL, so blocks run
+    in parallel.  Each block depends only on its own counters, so the result does
+    not depend on the scheduling."""
+    spans = [(lo, min(n, lo + _BLOCK)) for lo in range(0, n, _BLOCK)]
+    if len(spans) <= 1:
+        for lo, hi in spans:
+            fn(lo, hi)
+        return
+    for f in [_pool().submit(fn, lo, hi) for lo, hi in spans]:
+        f.result()
+
+
 class Stream:
     """One counter-based SplitMix64 stream, keyed by (seed, name)."""
 
@@ -61,29 +86,59 @@ class Stream:
         self.base = _scalar_mix64(key + 0x632BE59BD9B4E019)
         self.pos = 0
 
+    def _raw_into(self, out: np.ndarray, first: int) -> None:
+        """out[i] = mix64(base + (first + i + 1) * gamma), in place."""
+        with np.errstate(over="ignore"):
+            np.add(np.arange(first + 1, first + 1 + out.shape[0], dtype=np.uint64), 0, out=out)
+            np.multiply(out, _GAMMA, out=out)
+            np.add(out, np.uint64(self.base), out=out)
+            t = out >> np.uint64(30)
+            np.bitwise_xor(out, t, out=out)
+            np.multiply(out, _M1, out=out)
+            np.right_shift(out, np.uint64(27), out=t)
+            np.bitwise_xor(out, t, out=out)
+            np.multiply(out, _M2, out=out)
+            np.right_shift(out, np.uint64(31), out=t)
+            np.bitwise_xor(out, t, out=out)
+
     def raw(self, n: int) -> np.ndarray:
         out = np.empty(n, dtype=np.uint64)
-        base = np.uint64(self.base)
-        with np.errstate(over="ignore"):
-            for lo in range(0, n, _BLOCK):
-                hi = min(n, lo + _BLOCK)
-                idx = np.arange(self.pos + lo + 1, self.pos + hi + 1, dtype=np.uint64)
-                out[lo:hi] = _mix64(base + idx * _GAMMA)
+        first = self.pos
+        _for_blocks(n, lambda lo, hi: self._raw_into(out[lo:hi], first + lo))
         self.pos += n
         return out
 
     def uniform(self, n: int) -> np.ndarray:
         """n doubles in [0, 1)."""
-        return (self.raw(n) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+        out = np.empty(n, dtype=np.float64)
+        first = self.pos
+
+        def blk(lo, hi):
+            r = np.empty(hi - lo, dtype=np.uint64)
+            self._raw_into(r, first + lo)
+            np.right_shift(r, np.uint64(11), out=r)
+            np.multiply(r.astype(np.float64), 2.0 ** -53, out=out[lo:hi])
+
+        _for_blocks(n, blk)
+        self.pos += n
+        return out
 
     def normal(self, n: int) -> np.ndarray:
-        """n standard normals (Box-Muller, cosine branch)."""
+        """n standard normals (Box-Muller, cosine branch; normal i uses uniforms 2i, 2i+1)."""
         out = np.empty(n, dtype=np.float64)
-        for lo in range(0, n, _BLOCK):
-            hi = min(n, lo + _BLOCK)
-            u = self.uniform(2 * (hi - lo)).reshape(-1, 2)
-            r = np.sqrt(-2.0 * np.log1p(-u[:, 0]))
-            out[lo:hi] = r * np.cos(2.0 * np.pi * u[:, 1])
+        first = self.pos
+
+        def blk(lo, hi):
+            r = np.empty(2 * (hi - lo), dtype=np.uint64)
+            self._raw_into(r, first + 2 * lo)
+            np.right_shift(r, np.uint64(11), out=r)
+            u = r.astype(np.float64).reshape(-1, 2)
+            u *= 2.0 ** -53
+            rad = np.sqrt(-2.0 * np.log1p(-u[:, 0]))
+            np.multiply(rad, np.cos(2.0 * np.pi * u[:, 1]), out=out[lo:hi])
+
+        _for_blocks(n, blk)
+        self.pos += 2 * n
         return out
 
     def integers(self, n: int, lo: int, hi: int) -> np.ndarray:
@@ -95,11 +150,19 @@ class Stream:
 def bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float values to bfloat16 (nearest, ties to even); return uint16 bits."""
     f = np.ascontiguousarray(x, dtype=np.float32)
-    b = f.view(np.uint32).astype(np.uint64)
-    rounded = (b + np.uint64(0x7FFF) + ((b >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
-    nan = np.isnan(f)
-    out = rounded.astype(np.uint16)
-    out[nan] = np.uint16(0x7FC0)
+    out = np.empty(f.shape, dtype=np.uint16)
+    fb, ob = f.reshape(-1), out.reshape(-1)
+
+    def blk(lo, hi):
+        b = fb[lo:hi].view(np.uint32)
+        r = (b >> np.uint32(16)) & np.uint32(1)
+        r += b
+        r += np.uint32(0x7FFF)
+        r >>= np.uint32(16)
+        r[np.isnan(fb[lo:hi])] = 0x7FC0
+        ob[lo:hi] = r
+
+    _for_blocks(fb.shape[0], blk)
     return out
 
 
