@@ -10,11 +10,11 @@
 // "How it works"; forward substitution for the unit triangular factor as in
 // the Candle PR's chunked scan; log-space masking from its overflow fix):
 //   G   = inclusive running sum of g over the chunk (padding rows: g = beta = 0)
-//   G1  [K Kᵀ; Q Kᵀ] = [K; Q] Kᵀ                         (one M=128 MMA, exact bf16)
+//   G1  [K Kᵀ; Q Kᵀ] = [K; Q] Kᵀ                         (M=128 MMA, exact bf16)
 //   N   = diag(beta) (K Kᵀ ⊙ exp(G_t - G_j))_{j<t},  P = (Q Kᵀ ⊙ exp(G_t - G_j))_{j<=t}
 //         (the exponent is only formed on the kept triangle, so it is <= 0)
-//   T   = (I + N)^-1   (16x16 forward substitution + blocked off-diagonal solves)
-//   PT  = P T
+//   T   = (I + N)^-1   (16x16 forward substitution, then two block-doubling levels)
+//   MPT PT = P T                                          (M=64 MMA, hi/lo)
 //   MMA1 [K S; Q S] = [K; Q] S                            (S as bf16 hi + lo)
 //   R   = diag(beta) (V - diag(e^G) K S)
 //   MMA2 [D; P D] = [T; PT] R                             (hi/lo on both sides)
@@ -26,19 +26,20 @@
 // cores.  The bf16 hi/lo split (x = hi + lo, both bf16) keeps every product
 // that feeds the state within ~2^-16 relative; K, Q and V are exact in bf16.
 //
-// Warp roles (384 threads).  Warps 0-3, the "chain", own TMEM lanes 0-127 and
-// run the state-dependent MMA1 -> MMA2 -> MMA3 sequence of chunk c.  Warps
-// 4-11, "stage 1", meanwhile prepare chunk c+1: gates, the Gram MMA, N and P,
-// the triangular inverse and P T, and stage [T; PT] for the chain.  They hand
-// over through mbarriers: TMA -> both roles (tiles landed), stage 1 -> chain
-// ([T; PT] and gates ready), chain -> stage 1 ([T; PT] buffer free again).
-// The chain issues the TMA for chunk c+2 into chunk c's buffers once its last
-// MMA on them has completed.
+// Warp roles (512 threads).  Warps 0-7, the "chain", run the state-dependent
+// MMA1 -> MMA2 -> MMA3 sequence of chunk c; warp w owns TMEM lanes
+// 32 (w % 4) .. + 31 and state columns 32 (w / 4) .. + 31 of those rows.
+// Warps 8-15, "stage 1", meanwhile prepare chunk c+1: gates, the Gram MMA,
+// N and P, the triangular inverse and the P T product, staged as [T; PT] for
+// the chain.  They hand over through mbarriers: TMA -> both roles (tiles
+// landed), stage 1 -> chain ([T; PT] and gates ready), chain -> stage 1
+// ([T; PT] buffer free again).  The chain issues the TMA for chunk c+2 into
+// chunk c's buffers once its last MMA on them has completed.
 //
 // Every mbarrier wait is bounded: on timeout a thread records
 // GDR_ERR_DEVICE_TIMEOUT in the device error word and its role stops; the
-// other role then times out on its own next wait, waits (bounded) for any
-// outstanding TMA, and the CTA frees its TMEM and returns.
+// other role then times out on its own next wait, any outstanding TMA is
+// waited for (bounded), and the CTA frees its TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -57,10 +58,11 @@ using namespace tc;
 constexpr int C = 64;
 constexpr int D = 128;
 constexpr int BV = 64;
-constexpr int NCHAIN = 128;  // warps 0-3
-constexpr int NS1 = 256;     // warps 4-11
+constexpr int NCHAIN = 256;  // warps 0-7
+constexpr int NS1 = 256;     // warps 8-15
 constexpr int NTHREADS = NCHAIN + NS1;
 constexpr int SROW = 68;  // fp32 scratch row stride in floats (bank-conflict-free float4 rows)
+constexpr int XROW = 33;  // level-2 partial product row stride
 constexpr uint32_t BAR_CHAIN = 1, BAR_S1 = 2;  // named barrier ids
 constexpr int ROLE_CHAIN = 0, ROLE_S1 = 1;
 
@@ -75,14 +77,14 @@ constexpr uint32_t OFF_S_HI = OFF_ATP_LO + 16384;  // state block as MN-major 12
 constexpr uint32_t OFF_S_LO = OFF_S_HI + 16384;
 constexpr uint32_t OFF_RD_HI = OFF_S_LO + 16384;  // R, then D~: MN-major 64 (k = token) x 64 (n)
 constexpr uint32_t OFF_RD_LO = OFF_RD_HI + 8192;
+constexpr uint32_t OFF_P_HI = OFF_RD_LO + 8192;   // P as K-major 64 x 64 bf16 (A of the PT MMA)
+constexpr uint32_t OFF_P_LO = OFF_P_HI + 8192;
 constexpr uint32_t SCR_MAT = 64 * SROW * 4;       // fp32 [64][SROW]
-constexpr uint32_t OFF_N = OFF_RD_LO + 8192;      // N, later PT
+constexpr uint32_t OFF_N = OFF_P_LO + 8192;
 constexpr uint32_t OFF_T = OFF_N + SCR_MAT;
-constexpr uint32_t OFF_P = OFF_T + SCR_MAT;
-constexpr uint32_t XBLK = 16 * 17;                // one 16x16 partial block, padded rows
-constexpr uint32_t OFF_X = OFF_P + SCR_MAT;       // up to 3 partial blocks
-constexpr uint32_t OFF_SMALL = OFF_X + 3 * XBLK * 4;
-constexpr uint32_t SM_GATES = OFF_SMALL;          // float [2 chunks][3][64]: G, beta, e^G
+constexpr uint32_t OFF_X = OFF_T + SCR_MAT;       // partial products: [32][XROW] fp32
+constexpr uint32_t OFF_SMALL = OFF_X + 32 * XROW * 4;
+constexpr uint32_t SM_GATES = OFF_SMALL;          // float [2 chunks][3][64]: G log2(e), beta, e^G
 constexpr uint32_t SM_SCAN = OFF_SMALL + 1536;    // float[4]
 constexpr uint32_t SM_BARS = OFF_SMALL + 1600;    // 8 x uint64
 constexpr uint32_t SM_TMEM = OFF_SMALL + 1664;    // uint32
@@ -90,23 +92,27 @@ constexpr uint32_t SM_ABORT = OFF_SMALL + 1672;   // int32[2], one per role
 constexpr uint32_t SMEM_USED = OFF_SMALL + 2048;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(OFF_RD_HI % 1024 == 0 && OFF_RD_LO % 1024 == 0 && OFF_ATP_HI % 1024 == 0 && OFF_S_LO % 1024 == 0,
+static_assert(OFF_RD_HI % 1024 == 0 && OFF_P_HI % 1024 == 0 && OFF_P_LO % 1024 == 0 && OFF_ATP_HI % 1024 == 0 &&
+                  OFF_S_LO % 1024 == 0,
               "operand tiles must be 1 KB aligned");
 
 // mbarriers
 constexpr int B_TMA0 = 0, B_MMA_CHAIN = 2, B_MMA_S1 = 3, B_ATP_FULL = 4, B_ATP_FREE = 5;
 
-// TMEM columns (fp32 accumulators, lane = row).
-constexpr uint32_t TM_G1 = 0;    // [K Kᵀ; Q Kᵀ]   (stage 1)
-constexpr uint32_t TM_KS = 64;   // [K S; Q S]     (chain)
-constexpr uint32_t TM_DP = 128;  // [D; P D]       (chain)
-constexpr uint32_t TM_Y = 192;   // Kᵀ D~          (chain)
-constexpr uint32_t TM_COLS = 256;
+// TMEM columns (fp32 accumulators).
+constexpr uint32_t TM_G1 = 0;    // [K Kᵀ; Q Kᵀ]   (stage 1, lane = row)
+constexpr uint32_t TM_PT = 64;   // P T            (stage 1, M=64 layout)
+constexpr uint32_t TM_KS = 128;  // [K S; Q S]     (chain)
+constexpr uint32_t TM_DP = 192;  // [D; P D]       (chain)
+constexpr uint32_t TM_Y = 256;   // Kᵀ D~          (chain)
+constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t TMA_BYTES = 2 * 16384 + V_BYTES;  // K + Q (two 64-column halves each) + V
 constexpr long long kWaitLimit = 4000000000LL;       // SM clocks (about 2 s)
+constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr uint32_t IDESC_G1 = idesc_bf16_f32(128, 64, 0, 0);  // A K-major, B K-major
+constexpr uint32_t IDESC_PT = idesc_bf16_f32(64, 64, 0, 1);   // A K-major (P), B MN-major (T)
 constexpr uint32_t IDESC_KS = idesc_bf16_f32(128, 64, 0, 1);  // A K-major, B MN-major
 constexpr uint32_t IDESC_DP = idesc_bf16_f32(128, 64, 0, 1);
 constexpr uint32_t IDESC_Y = idesc_bf16_f32(128, 64, 1, 1);   // A MN-major (Kᵀ), B MN-major
@@ -129,20 +135,24 @@ struct Ctx {
     __device__ float *gates(int buf) const { return reinterpret_cast<float *>(sm + SM_GATES) + buf * 192; }
 };
 
-// Bounded wait shared by all threads of one role (the chain's 128 or stage 1's
-// 256).  A thread whose wait times out records the error and raises its role's
-// abort flag; the role barrier that follows makes every thread of the role read
-// the same flag, so the role leaves its loop together and never strands a
-// sibling at a later barrier.  Each role reads only its own flag.
+__device__ __forceinline__ void role_sync(int role) {
+    if (role == ROLE_CHAIN)
+        named_sync(BAR_CHAIN, NCHAIN);
+    else
+        named_sync(BAR_S1, NS1);
+}
+
+// Bounded wait shared by all threads of one role.  A thread whose wait times
+// out records the error and raises its role's abort flag; the role barrier
+// that follows makes every thread of the role read the same flag, so the role
+// leaves its loop together and never strands a sibling at a later barrier.
+// Each role reads only its own flag.
 __device__ __forceinline__ bool role_wait(const Ctx &x, uint32_t bar, uint32_t parity, int role) {
     if (!mbar_wait_bounded(bar, parity, kWaitLimit)) {
         x.abort_flag[role] = 1;
         atomicCAS(&g_device_error, 0, (int32_t)GDR_ERR_DEVICE_TIMEOUT);
     }
-    if (role == ROLE_CHAIN)
-        named_sync(BAR_CHAIN, NCHAIN);
-    else
-        named_sync(BAR_S1, NS1);
+    role_sync(role);
     return x.abort_flag[role] == 0;
 }
 
@@ -159,29 +169,25 @@ __device__ __forceinline__ void issue_chunk_loads(const Ctx &x, int buf, int tok
     tma_load_3d(x.sbase + OFF_V + buf * V_BYTES, tmV, bar, cb * BV, h, tok);
 }
 
-__device__ __forceinline__ void store_row_hilo(uint8_t *hi, uint8_t *lo, int row, const float *x) {
+// 32 values as chunks [4 half, 4 half + 4) of row `row` of a hi/lo tile pair.
+__device__ __forceinline__ void store_half_hilo(uint8_t *hi, uint8_t *lo, int row, int half, const float *x) {
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) store_hilo_chunk(hi, lo, row, ch, x + ch * 8);
+    for (int ch = 0; ch < 4; ++ch) store_hilo_chunk(hi, lo, row, 4 * half + ch, x + 8 * ch);
+}
+
+__device__ __forceinline__ uint32_t lane_base(uint32_t tmem, int warp) {
+    return tmem + ((uint32_t)((warp & 3) * 32) << 16);
 }
 
 // ================================ stage 1 ===========================================
-// T = (I + N)^-1 for strictly lower N, then PT = P T; s = stage-1 thread index (0..255).
-__device__ void stage1_inverse_and_pt(uint8_t *sm, int s) {
-    float *N = reinterpret_cast<float *>(sm + OFF_N);
+// T = (I + N)^-1 for strictly lower N (fp32 scratch, row stride SROW);
+// s = stage-1 thread index (0..255).  Ends with a role barrier.
+__device__ void unit_lower_inverse(uint8_t *sm, int s) {
+    const float *N = reinterpret_cast<const float *>(sm + OFF_N);
     float *T = reinterpret_cast<float *>(sm + OFF_T);
-    const float *P = reinterpret_cast<const float *>(sm + OFF_P);
     float *X = reinterpret_cast<float *>(sm + OFF_X);
-
-    // blocks above the block diagonal of T are zero (6 blocks x 256 entries)
-#pragma unroll
-    for (int n = 0; n < 6; ++n) {
-        const int e = s + NS1 * n, b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-        const int I = b < 3 ? 0 : (b < 5 ? 1 : 2);
-        const int J = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
-        T[(16 * I + r) * SROW + 16 * J + cc] = 0.f;
-    }
-    // 16 x 16 diagonal blocks by forward substitution, one column per thread
     if (s < 64) {
+        // 16 x 16 diagonal blocks by forward substitution, one column per thread
         const int base = (s >> 4) * 16, jj = s & 15;
         float col[16];
 #pragma unroll
@@ -201,92 +207,113 @@ __device__ void stage1_inverse_and_pt(uint8_t *sm, int s) {
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) T[(base + r) * SROW + base + jj] = col[r];
+    } else {
+        // everything above the 16-block diagonal is zero
+        for (int e = s - 64; e < 6 * 256; e += NS1 - 64) {
+            const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+            const int I = b < 3 ? 0 : (b < 5 ? 1 : 2);
+            const int J = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
+            T[(16 * I + r) * SROW + 16 * J + cc] = 0.f;
+        }
     }
     named_sync(BAR_S1, NS1);
-    // blocks below the diagonal, nearest first: T_IJ = -T_II sum_{J<=M<I} N_IM T_MJ
+    // level 1: T_{I,I-1} = -T_II (N_{I,I-1} T_{I-1,I-1}) for I = 1, 3; two entries per thread
 #pragma unroll
-    for (int dist = 1; dist <= 3; ++dist) {
-        const int nblk = 4 - dist;
-        for (int e = s; e < nblk * 256; e += NS1) {
-            const int J = e >> 8, I = J + dist, r = (e >> 4) & 15, cc = e & 15;
-            float a0 = 0.f, a1 = 0.f;
-            for (int M = J; M < I; ++M) {
-                const float *nr = N + (16 * I + r) * SROW + 16 * M;
-                const float *tc = T + (16 * M) * SROW + 16 * J + cc;
-#pragma unroll
-                for (int m = 0; m < 16; m += 2) {
-                    a0 = fmaf(nr[m], tc[m * SROW], a0);
-                    a1 = fmaf(nr[m + 1], tc[(m + 1) * SROW], a1);
-                }
-            }
-            X[J * XBLK + r * 17 + cc] = a0 + a1;
-        }
-        named_sync(BAR_S1, NS1);
-        for (int e = s; e < nblk * 256; e += NS1) {
-            const int J = e >> 8, I = J + dist, r = (e >> 4) & 15, cc = e & 15;
-            const float *tr = T + (16 * I + r) * SROW + 16 * I;
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int m = 0; m < 16; m += 2) {
-                a0 = fmaf(tr[m], X[J * XBLK + m * 17 + cc], a0);
-                a1 = fmaf(tr[m + 1], X[J * XBLK + (m + 1) * 17 + cc], a1);
-            }
-            T[(16 * I + r) * SROW + 16 * J + cc] = -(a0 + a1);
-        }
-        named_sync(BAR_S1, NS1);
-    }
-    // PT = P T over the 4 x 4 block grid (N is dead: PT takes its place).  Each
-    // thread owns one entry of every block, so the triangular work is balanced.
-    float *PT = N;
-#pragma unroll
-    for (int b = 0; b < 16; ++b) {
-        const int I = b >> 2, J = b & 3, r = s >> 4, cc = s & 15;
+    for (int k = 0; k < 2; ++k) {
+        const int e = s + NS1 * k, blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+        const int I = 2 * blk + 1, J = I - 1;
+        const float *nr = N + (16 * I + r) * SROW + 16 * J;
+        const float *tc = T + (16 * J) * SROW + 16 * J + cc;
         float a0 = 0.f, a1 = 0.f;
-        if (I >= J) {
-            for (int M = J; M <= I; ++M) {
-                const float *pr = P + (16 * I + r) * SROW + 16 * M;
-                const float *tc = T + (16 * M) * SROW + 16 * J + cc;
 #pragma unroll
-                for (int m = 0; m < 16; m += 2) {
-                    a0 = fmaf(pr[m], tc[m * SROW], a0);
-                    a1 = fmaf(pr[m + 1], tc[(m + 1) * SROW], a1);
-                }
-            }
+        for (int m = 0; m < 16; m += 2) {
+            a0 = fmaf(nr[m], tc[m * SROW], a0);
+            a1 = fmaf(nr[m + 1], tc[(m + 1) * SROW], a1);
         }
-        PT[(16 * I + r) * SROW + 16 * J + cc] = a0 + a1;
+        X[(16 * blk + r) * XROW + cc] = a0 + a1;
     }
+    named_sync(BAR_S1, NS1);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int e = s + NS1 * k, blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+        const int I = 2 * blk + 1;
+        const float *tr = T + (16 * I + r) * SROW + 16 * I;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; m += 2) {
+            a0 = fmaf(tr[m], X[(16 * blk + m) * XROW + cc], a0);
+            a1 = fmaf(tr[m + 1], X[(16 * blk + m + 1) * XROW + cc], a1);
+        }
+        T[(16 * I + r) * SROW + 16 * (I - 1) + cc] = -(a0 + a1);
+    }
+    named_sync(BAR_S1, NS1);
+    // level 2: T[32:64, 0:32] = -T[32:64, 32:64] (N[32:64, 0:32] T[0:32, 0:32]);
+    // each thread a 2 x 2 tile of the 32 x 32 block
+    const int r0 = (s >> 4) * 2, c0 = (s & 15) * 2;
+    {
+        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+        const float *n0 = N + (32 + r0) * SROW, *n1 = n0 + SROW;
+#pragma unroll 8
+        for (int m = c0; m < 32; ++m) {  // T[0:32, 0:32] is lower: rows m >= c0 only
+            const float2 tv = *reinterpret_cast<const float2 *>(T + m * SROW + c0);
+            const float u0 = n0[m], u1 = n1[m];
+            a00 = fmaf(u0, tv.x, a00);
+            a01 = fmaf(u0, tv.y, a01);
+            a10 = fmaf(u1, tv.x, a10);
+            a11 = fmaf(u1, tv.y, a11);
+        }
+        X[r0 * XROW + c0] = a00;
+        X[r0 * XROW + c0 + 1] = a01;
+        X[(r0 + 1) * XROW + c0] = a10;
+        X[(r0 + 1) * XROW + c0 + 1] = a11;
+    }
+    named_sync(BAR_S1, NS1);
+    {
+        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+        const float *t0 = T + (32 + r0) * SROW + 32, *t1 = t0 + SROW;
+#pragma unroll 8
+        for (int m = 0; m <= r0 + 1; ++m) {  // T[32:64, 32:64] is lower: columns m <= row
+            const float x0 = X[m * XROW + c0], x1 = X[m * XROW + c0 + 1];
+            const float u0 = t0[m], u1 = t1[m];
+            a00 = fmaf(u0, x0, a00);
+            a01 = fmaf(u0, x1, a01);
+            a10 = fmaf(u1, x0, a10);
+            a11 = fmaf(u1, x1, a11);
+        }
+        *reinterpret_cast<float2 *>(T + (32 + r0) * SROW + c0) = make_float2(-a00, -a01);
+        *reinterpret_cast<float2 *>(T + (33 + r0) * SROW + c0) = make_float2(-a10, -a11);
+    }
+    named_sync(BAR_S1, NS1);
 }
 
 __device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t t1, int nchunks, int h,
                             const int tid) {
     const int s = tid - NCHAIN;  // 0..255
     const int warp = tid >> 5, lane = tid & 31;
+    const int half = (s >> 5) >> 2;  // column half of this warp's TMEM reads
     const uint32_t tmem = x.tmem;
     float *sScan = reinterpret_cast<float *>(x.sm + SM_SCAN);
+
+    // gates of the next chunk, loaded one chunk ahead (threads s < 64)
+    float g_next = 0.f, b_next = 0.f;
+    if (s < C && nchunks > 0 && s < t1 - t0) {
+        g_next = p.g[(size_t)(t0 + s) * p.h_v + h];
+        b_next = p.beta[(size_t)(t0 + s) * p.h_v + h];
+    }
     for (int c = 0; c < nchunks; ++c) {
         const int buf = c & 1;
         const int64_t c0 = t0 + (int64_t)c * C;
-        const int L = (int)((t1 - c0) < C ? (t1 - c0) : C);
+        float gt = g_next, bt = b_next;
+        if (s < C) {
+            g_next = b_next = 0.f;
+            if (c0 + C + s < t1) {
+                g_next = p.g[(size_t)(c0 + C + s) * p.h_v + h];
+                b_next = p.beta[(size_t)(c0 + C + s) * p.h_v + h];
+            }
+        }
         // the chunk's tiles (issued by the chain once chunk c-2 released the buffer)
         if (!role_wait(x, x.bar(B_TMA0 + buf), (uint32_t)(c >> 1) & 1u, ROLE_S1)) break;
 
-        // gates: G = inclusive running sum of g (padding rows: g = 0, beta = 0)
-        float *gts = x.gates(buf);
-        float gt = 0.f;
-        if (s < C) {
-            float bt = 0.f;
-            if (s < L) {
-                gt = p.g[(size_t)(c0 + s) * p.h_v + h];
-                bt = p.beta[(size_t)(c0 + s) * p.h_v + h];
-            }
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float u = __shfl_up_sync(0xffffffffu, gt, o);
-                if (lane >= o) gt += u;
-            }
-            if (lane == 31) sScan[s >> 5] = gt;
-            gts[64 + s] = bt;
-        }
         // Gram products of the chunk: [K Kᵀ; Q Kᵀ] into TMEM
         if (s == 0) {
             tc_fence_after_sync();  // the previous chunk's reads of these TMEM columns are done
@@ -299,57 +326,101 @@ __device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t
             }
             mma_commit(x.bar(B_MMA_S1));
         }
+        // gates: G = inclusive running sum of g, kept as G log2(e) so every decay is one
+        // ex2 (padding rows: g = 0, beta = 0)
+        float *gts = x.gates(buf);
+        gt *= kLog2e;
+        if (s < C) {
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float u = __shfl_up_sync(0xffffffffu, gt, o);
+                if (lane >= o) gt += u;
+            }
+            if (lane == 31) sScan[s >> 5] = gt;
+            gts[64 + s] = bt;
+        }
         named_sync(BAR_S1, NS1);
         if (s < C) {
             if (s >= 32) gt += sScan[0];
             gts[s] = gt;
-            gts[128 + s] = __expf(gt);
+            gts[128 + s] = fast_exp2(gt);
         }
-        if (!role_wait(x, x.bar(B_MMA_S1), (uint32_t)c & 1u, ROLE_S1)) break;  // also publishes the gates
+        if (!role_wait(x, x.bar(B_MMA_S1), 0u, ROLE_S1)) break;  // also publishes the gates
         tc_fence_after_sync();
         {
-            // row t = lane quarter of this warp; columns [32*half, 32*half + 32)
+            // row = lane quarter of this warp; columns [32 half, 32 half + 32)
             const int row = ((warp & 3) << 5) + lane;
-            const int half = (warp - 4) >> 2;
             float a[32];
-            tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + TM_G1 + 32 * half, a);
-            const bool is_n = row < 64;
+            tmem_ld32(lane_base(tmem, warp) + TM_G1 + 32 * half, a);
             const int t = row & 63;
             const float Gt = gts[t];
+            const bool is_n = row < 64;
             const float w = is_n ? gts[64 + t] : 1.f;
-            float *dst = reinterpret_cast<float *>(x.sm + (is_n ? OFF_N : OFF_P)) + t * SROW + 32 * half;
+            const int lim = is_n ? t : t + 1;  // keep j < t (N) or j <= t (P)
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
-                float v[4];
+                const float4 gj = *reinterpret_cast<const float4 *>(gts + 32 * half + j);
+                const float gv[4] = {gj.x, gj.y, gj.z, gj.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int jj = 32 * half + j + e;
-                    const bool keep = is_n ? (jj < t) : (jj <= t);
-                    v[e] = keep ? w * __expf(Gt - gts[jj]) * a[j + e] : 0.f;
+                    a[j + e] = (jj < lim) ? w * fast_exp2(Gt - gv[e]) * a[j + e] : 0.f;
                 }
-                *reinterpret_cast<float4 *>(dst + j) = make_float4(v[0], v[1], v[2], v[3]);
+            }
+            if (is_n) {
+                float *dst = reinterpret_cast<float *>(x.sm + OFF_N) + t * SROW + 32 * half;
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4 *>(dst + j) = make_float4(a[j], a[j + 1], a[j + 2], a[j + 3]);
+            } else {
+                store_half_hilo(x.sm + OFF_P_HI, x.sm + OFF_P_LO, t, half, a);
             }
         }
         tc_fence_before_sync();
         named_sync(BAR_S1, NS1);
-        stage1_inverse_and_pt(x.sm, s);
-        named_sync(BAR_S1, NS1);
+        unit_lower_inverse(x.sm, s);
 
         // [T; PT] buffer: free once the chain's MMA2 of chunk c-1 has completed
         if (c > 0 && !role_wait(x, x.bar(B_ATP_FREE), (uint32_t)(c - 1) & 1u, ROLE_S1)) break;
         {
-            const int row = s & 127, half = s >> 7;
-            const float *src = reinterpret_cast<const float *>(x.sm + (row < 64 ? OFF_T : OFF_N)) +
-                               (row & 63) * SROW + 32 * half;
+            // T rows as the top half of [T; PT] (also the B operand of the PT product)
+            const int row = s >> 2, cp = s & 3;
+            const float *src = reinterpret_cast<const float *>(x.sm + OFF_T) + row * SROW + 16 * cp;
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
+            for (int ch = 0; ch < 2; ++ch) {
                 const float4 u = *reinterpret_cast<const float4 *>(src + 8 * ch);
                 const float4 v = *reinterpret_cast<const float4 *>(src + 8 * ch + 4);
                 const float xv[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
-                store_hilo_chunk(x.sm + OFF_ATP_HI, x.sm + OFF_ATP_LO, row, 4 * half + ch, xv);
+                store_hilo_chunk(x.sm + OFF_ATP_HI, x.sm + OFF_ATP_LO, row, 2 * cp + ch, xv);
             }
         }
         fence_proxy_async_smem();
+        named_sync(BAR_S1, NS1);
+        // PT = P T  (M = 64)
+        if (s == 0) {
+            tc_fence_after_sync();
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t ah = smem_desc_sw128(x.sbase + OFF_P_HI + ks * 32, 16, 1024);
+                const uint64_t al = smem_desc_sw128(x.sbase + OFF_P_LO + ks * 32, 16, 1024);
+                const uint64_t bh = smem_desc_sw128(x.sbase + OFF_ATP_HI + ks * 2048, 16, 1024);
+                const uint64_t bl = smem_desc_sw128(x.sbase + OFF_ATP_LO + ks * 2048, 16, 1024);
+                mma_bf16(tmem + TM_PT, ah, bh, IDESC_PT, ks > 0);
+                mma_bf16(tmem + TM_PT, al, bh, IDESC_PT, 1);
+                mma_bf16(tmem + TM_PT, ah, bl, IDESC_PT, 1);
+            }
+            mma_commit(x.bar(B_MMA_S1));
+        }
+        if (!role_wait(x, x.bar(B_MMA_S1), 1u, ROLE_S1)) break;
+        tc_fence_after_sync();
+        {
+            // M = 64 accumulator: row i sits in lane 32 (i / 16) + i % 16
+            float a[32];
+            tmem_ld32(lane_base(tmem, warp) + TM_PT + 32 * half, a);
+            if (lane < 16) store_half_hilo(x.sm + OFF_ATP_HI, x.sm + OFF_ATP_LO, 64 + 16 * (warp & 3) + lane, half, a);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
         named_sync(BAR_S1, NS1);
         if (s == 0) mbar_arrive(x.bar(B_ATP_FULL));
     }
@@ -359,7 +430,11 @@ __device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t
 __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t t1, int nchunks, int h, int hq,
                            int cb, float *Sr, const CUtensorMap *tmK, const CUtensorMap *tmQ,
                            const CUtensorMap *tmV, const int tid, bool &ok) {
-    const int warp = tid >> 5;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int hc = warp >> 2;                    // column half
+    const int row = ((warp & 3) << 5) + lane;  // TMEM lane = state row (d_k index) / chunk row
+    const int t = row & 63;
+    const uint32_t lb = lane_base(x.tmem, warp);
     const uint32_t tmem = x.tmem;
     uint32_t mma_phase = 0;
     for (int c = 0; c < nchunks; ++c) {
@@ -386,28 +461,29 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
         // stage 1 of this chunk: gates and [T; PT]
         if (!role_wait(x, x.bar(B_ATP_FULL), (uint32_t)c & 1u, ROLE_CHAIN)) break;
         const float *gts = x.gates(buf);
-        const int t = tid & 63;
         const float Gt = gts[t], bt = gts[64 + t], egt = gts[128 + t];
         const float eGC = gts[128 + C - 1], GC = gts[C - 1];
         if (!role_wait(x, x.bar(B_MMA_CHAIN), mma_phase, ROLE_CHAIN)) break;
         mma_phase ^= 1;
         tc_fence_after_sync();
-        if (tid < 64) {
-            // R = beta (V - e^G K S), staged as the hi/lo MN-major B operand of MMA2
-            const uint8_t *vt = x.sm + OFF_V + buf * V_BYTES;
-            const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + TM_KS;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float a[32];
-                tmem_ld32(taddr + 32 * half, a);
+        float qse[32];  // rows 64-127: e^G Q S for this thread's columns, kept for the output
+        {
+            float a[32];
+            tmem_ld32(lb + TM_KS + 32 * hc, a);
+            if (row < 64) {
+                // R = beta (V - e^G K S), staged as the hi/lo MN-major B operand of MMA2
+                const uint8_t *vt = x.sm + OFF_V + buf * V_BYTES;
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                     float v[8], r[8];
-                    load_bf16_chunk(vt, t, 4 * half + ch, v);
+                    load_bf16_chunk(vt, t, 4 * hc + ch, v);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) r[e] = bt * (v[e] - egt * a[ch * 8 + e]);
-                    store_hilo_chunk(x.sm + OFF_RD_HI, x.sm + OFF_RD_LO, t, 4 * half + ch, r);
+                    store_hilo_chunk(x.sm + OFF_RD_HI, x.sm + OFF_RD_LO, t, 4 * hc + ch, r);
                 }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) qse[j] = egt * a[j];
             }
         }
         fence_proxy_async_smem();
@@ -434,49 +510,34 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
         tc_fence_after_sync();
         if (tid == 0) mbar_arrive(x.bar(B_ATP_FREE));  // stage 1 may overwrite [T; PT]
         {
-            const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-            if (tid < 64) {
+            float dd[32];
+            tmem_ld32(lb + TM_DP + 32 * hc, dd);
+            if (row < 64) {
                 // D~ = exp(G_C - G_t) D, staged as the hi/lo MN-major B operand of MMA3
-                const float sc = __expf(GC - Gt);
+                const float sc = fast_exp2(GC - Gt);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float dd[32];
-                    tmem_ld32(lane_base + TM_DP + 32 * half, dd);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) dd[j] *= sc;
-#pragma unroll
-                    for (int ch = 0; ch < 4; ++ch)
-                        store_hilo_chunk(x.sm + OFF_RD_HI, x.sm + OFF_RD_LO, t, 4 * half + ch, dd + 8 * ch);
-                }
-            } else {
+                for (int j = 0; j < 32; ++j) dd[j] *= sc;
+                store_half_hilo(x.sm + OFF_RD_HI, x.sm + OFF_RD_LO, t, hc, dd);
+            } else if (t < L) {
                 // O = scale (e^G Q S + P D) for the chunk's real rows
-                const size_t off = ((size_t)(c0 + t) * p.h_v + h) * D + cb * BV;
+                const size_t off = ((size_t)(c0 + t) * p.h_v + h) * D + cb * BV + 32 * hc;
+                if (p.out_bf16) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + off);
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float pd[32], qs[32];
-                    tmem_ld32(lane_base + TM_DP + 32 * half, pd);
-                    tmem_ld32(lane_base + TM_KS + 32 * half, qs);
-                    if (t < L) {
-                        if (p.out_bf16) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + off + 32 * half);
+                    for (int j = 0; j < 32; j += 8) {
+                        float y[8];
 #pragma unroll
-                            for (int j = 0; j < 32; j += 8) {
-                                float y[8];
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) y[e] = p.scale * fmaf(egt, qs[j + e], pd[j + e]);
-                                dst[j / 8] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                                                        pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
-                            }
-                        } else {
-                            float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + off + 32 * half);
-#pragma unroll
-                            for (int j = 0; j < 32; j += 4)
-                                dst[j / 4] = make_float4(p.scale * fmaf(egt, qs[j], pd[j]),
-                                                         p.scale * fmaf(egt, qs[j + 1], pd[j + 1]),
-                                                         p.scale * fmaf(egt, qs[j + 2], pd[j + 2]),
-                                                         p.scale * fmaf(egt, qs[j + 3], pd[j + 3]));
-                        }
+                        for (int e = 0; e < 8; ++e) y[e] = p.scale * (qse[j + e] + dd[j + e]);
+                        dst[j / 8] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                                                pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
                     }
+                } else {
+                    float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + off);
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        dst[j / 4] = make_float4(p.scale * (qse[j] + dd[j]), p.scale * (qse[j + 1] + dd[j + 1]),
+                                                 p.scale * (qse[j + 2] + dd[j + 2]),
+                                                 p.scale * (qse[j + 3] + dd[j + 3]));
                 }
             }
         }
@@ -506,15 +567,11 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
             issue_chunk_loads(x, buf, (int)(c0 + 2 * C), hq, h, cb, tmK, tmQ, tmV);
         }
         {
-            const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + TM_Y;
+            float y[32];
+            tmem_ld32(lb + TM_Y + 32 * hc, y);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float y[32];
-                tmem_ld32(taddr + 32 * half, y);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) Sr[32 * half + j] = fmaf(eGC, Sr[32 * half + j], y[j]);
-            }
-            store_row_hilo(x.sm + OFF_S_HI, x.sm + OFF_S_LO, tid, Sr);
+            for (int j = 0; j < 32; ++j) Sr[j] = fmaf(eGC, Sr[j], y[j]);
+            store_half_hilo(x.sm + OFF_S_HI, x.sm + OFF_S_LO, row, hc, Sr);
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
@@ -533,7 +590,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     x.abort_flag = reinterpret_cast<volatile int *>(x.sm + SM_ABORT);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(x.sm + SM_TMEM);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cb = blockIdx.x & 1;
     const int h = (blockIdx.x >> 1) % p.h_v;
     const int s = (blockIdx.x >> 1) / p.h_v;
@@ -551,19 +608,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_alloc(smem_u32(tmem_holder), TM_COLS);
         tmem_relinquish();
     }
-    // chain thread `tid` owns row `tid` (a d_k index) of the 128 x 64 state block
-    float Sr[BV];
-    float *Sg = p.state + (((size_t)s * p.h_v + h) * D + (tid & 127)) * D + cb * BV;
+    // chain thread: row `srow` (a d_k index), columns [32 hc, 32 hc + 32) of the CTA's block
+    const int srow = ((warp & 3) << 5) + lane, hc = (warp >> 2) & 1;
+    float Sr[32];
+    float *Sg = p.state + (((size_t)s * p.h_v + h) * D + srow) * D + cb * BV + 32 * hc;
     if (tid < NCHAIN) {
 #pragma unroll
-        for (int j = 0; j < BV; j += 4) {
+        for (int j = 0; j < 32; j += 4) {
             const float4 v = *reinterpret_cast<const float4 *>(Sg + j);
             Sr[j] = v.x;
             Sr[j + 1] = v.y;
             Sr[j + 2] = v.z;
             Sr[j + 3] = v.w;
         }
-        store_row_hilo(x.sm + OFF_S_HI, x.sm + OFF_S_LO, tid, Sr);
+        store_half_hilo(x.sm + OFF_S_HI, x.sm + OFF_S_LO, srow, hc, Sr);
         fence_proxy_async_smem();
     }
     tc_fence_before_sync();
@@ -585,7 +643,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (tid < NCHAIN) {
         if (ok) {
 #pragma unroll
-            for (int j = 0; j < BV; j += 4)
+            for (int j = 0; j < 32; j += 4)
                 *reinterpret_cast<float4 *>(Sg + j) = make_float4(Sr[j], Sr[j + 1], Sr[j + 2], Sr[j + 3]);
         } else if (tid == 0) {
             // let any outstanding tile load land before the CTA's shared memory is released

@@ -155,8 +155,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
 }
 
 // ---- bf16 hi/lo split into a 128-byte-swizzled row ------------------------------------
-// Writes 8 values x[0..7] as one 16-byte chunk of the high bf16 parts and one of
-// the residuals, at the swizzled position of chunk `c` of row `row`.
+// Writes 8 values x[0..7] as one 16-byte chunk of their high bf16 parts and one
+// of the residuals, at the swizzled position of chunk `chunk` of row `row`.
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -166,19 +166,27 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
 }
 __device__ __forceinline__ void store_hilo_chunk(uint8_t *hi_base, uint8_t *lo_base, int row, int chunk,
                                                  const float *x) {
-    float h[8], l[8];
+    // hi: x with its low 16 bits dropped (exactly the top half of the fp32 word);
+    // lo: the exact remainder x - hi, rounded to bf16.  |lo| < 2^-7 |x|, so
+    // hi + lo matches x to 2^-16 relative.
+    uint32_t h[4], l[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        h[i] = __bfloat162float(__float2bfloat16_rn(x[i]));
-        l[i] = x[i] - h[i];
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t a = __float_as_uint(x[2 * i]), b = __float_as_uint(x[2 * i + 1]);
+        h[i] = __byte_perm(a, b, 0x7632);
+        const float ra = x[2 * i] - __uint_as_float(a & 0xFFFF0000u);
+        const float rb = x[2 * i + 1] - __uint_as_float(b & 0xFFFF0000u);
+        l[i] = pack_bf16x2(ra, rb);
     }
-    uint4 vh = make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]),
-                          pack_bf16x2(h[6], h[7]));
-    uint4 vl = make_uint4(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]), pack_bf16x2(l[4], l[5]),
-                          pack_bf16x2(l[6], l[7]));
     const uint32_t off = sw128_offset(row, chunk);
-    *reinterpret_cast<uint4 *>(hi_base + off) = vh;
-    *reinterpret_cast<uint4 *>(lo_base + off) = vl;
+    *reinterpret_cast<uint4 *>(hi_base + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4 *>(lo_base + off) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+// 2^x on the SFU (ex2.approx, flush-to-zero); used with log2(e)-scaled gates.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 // Reads 8 bf16 values of chunk `c` of a swizzled row as floats.
 __device__ __forceinline__ void load_bf16_chunk(const uint8_t *base, int row, int chunk, float *x) {
