@@ -80,16 +80,22 @@ constexpr uint32_t OFF_RD_LO = OFF_RD_HI + 8192;
 constexpr uint32_t OFF_P_HI = OFF_RD_LO + 8192;   // P as K-major 64 x 64 bf16 (A of the PT MMA)
 constexpr uint32_t OFF_P_LO = OFF_P_HI + 8192;
 constexpr uint32_t SCR_MAT = 64 * SROW * 4;       // fp32 [64][SROW]
-constexpr uint32_t OFF_N = OFF_P_LO + 8192;
+// Stage 1's own K/Q tile for the Gram MMA (same layout as one ring buffer); once
+// that MMA has completed the region holds the fp32 scratch N, T and X.
+constexpr uint32_t OFF_S1 = OFF_P_LO + 8192;
+constexpr uint32_t OFF_N = OFF_S1;
 constexpr uint32_t OFF_T = OFF_N + SCR_MAT;
 constexpr uint32_t OFF_X = OFF_T + SCR_MAT;       // partial products: [32][XROW] fp32
-constexpr uint32_t OFF_SMALL = OFF_X + 32 * XROW * 4;
+constexpr uint32_t S1_BYTES = 40960;
+constexpr uint32_t OFF_SMALL = OFF_S1 + S1_BYTES;
+static_assert(OFF_X + 32 * XROW * 4 <= OFF_S1 + S1_BYTES && KQ_BYTES <= S1_BYTES, "stage-1 region");
 constexpr uint32_t SM_GATES = OFF_SMALL;          // float [2 chunks][3][64]: G log2(e), beta, e^G
 constexpr uint32_t SM_SCAN = OFF_SMALL + 1536;    // float[4]
+constexpr uint32_t SM_GPRIV = OFF_SMALL + 2048;   // float[3][64]: stage 1's own copy of the gates
 constexpr uint32_t SM_BARS = OFF_SMALL + 1600;    // 8 x uint64
 constexpr uint32_t SM_TMEM = OFF_SMALL + 1664;    // uint32
 constexpr uint32_t SM_ABORT = OFF_SMALL + 1672;   // int32[2], one per role
-constexpr uint32_t SMEM_USED = OFF_SMALL + 2048;
+constexpr uint32_t SMEM_USED = OFF_SMALL + 2048 + 768;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_RD_HI % 1024 == 0 && OFF_P_HI % 1024 == 0 && OFF_P_LO % 1024 == 0 && OFF_ATP_HI % 1024 == 0 &&
@@ -97,7 +103,8 @@ static_assert(OFF_RD_HI % 1024 == 0 && OFF_P_HI % 1024 == 0 && OFF_P_LO % 1024 =
               "operand tiles must be 1 KB aligned");
 
 // mbarriers
-constexpr int B_TMA0 = 0, B_MMA_CHAIN = 2, B_MMA_S1 = 3, B_ATP_FULL = 4, B_ATP_FREE = 5;
+constexpr int B_TMA0 = 0, B_MMA_CHAIN = 2, B_MMA_S1 = 3, B_ATP_FULL = 4, B_ATP_FREE = 5, B_TMA_S1 = 6;
+constexpr int NBARS = 7;
 
 // TMEM columns (fp32 accumulators).
 constexpr uint32_t TM_G1 = 0;    // [K Kᵀ; Q Kᵀ]   (stage 1, lane = row)
@@ -108,6 +115,7 @@ constexpr uint32_t TM_Y = 256;   // Kᵀ D~          (chain)
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t TMA_BYTES = 2 * 16384 + V_BYTES;  // K + Q (two 64-column halves each) + V
+constexpr uint32_t ATP_COPY_BYTES = 2 * 16384 + 192 * 4;  // [T; PT] hi + lo, and the gates
 constexpr long long kWaitLimit = 4000000000LL;       // SM clocks (about 2 s)
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -131,6 +139,8 @@ struct Ctx {
     uint32_t sbase;
     uint32_t tmem;
     volatile int *abort_flag;
+    uint32_t rank;        // this CTA's rank in its cluster of two (= its column block)
+    uint32_t peer_base;   // cluster address of the peer CTA's shared-memory base
     __device__ uint32_t bar(int i) const { return sbase + SM_BARS + 8 * i; }
     __device__ float *gates(int buf) const { return reinterpret_cast<float *>(sm + SM_GATES) + buf * 192; }
 };
@@ -167,6 +177,18 @@ __device__ __forceinline__ void issue_chunk_loads(const Ctx &x, int buf, int tok
     tma_load_3d(kq + 8192, tmQ, bar, 0, hq, tok);
     tma_load_3d(kq + 16384 + 8192, tmQ, bar, 64, hq, tok);
     tma_load_3d(x.sbase + OFF_V + buf * V_BYTES, tmV, bar, cb * BV, h, tok);
+}
+
+// Stage 1's copy of the chunk's K and Q (for the Gram MMA only).
+__device__ __forceinline__ void issue_s1_loads(const Ctx &x, int tok, int hq, const CUtensorMap *tmK,
+                                               const CUtensorMap *tmQ) {
+    const uint32_t bar = x.bar(B_TMA_S1);
+    mbar_arrive_expect_tx(bar, 2 * 16384);
+    const uint32_t kq = x.sbase + OFF_S1;
+    tma_load_3d(kq, tmK, bar, 0, hq, tok);
+    tma_load_3d(kq + 16384, tmK, bar, 64, hq, tok);
+    tma_load_3d(kq + 8192, tmQ, bar, 0, hq, tok);
+    tma_load_3d(kq + 16384 + 8192, tmQ, bar, 64, hq, tok);
 }
 
 // 32 values as chunks [4 half, 4 half + 4) of row `row` of a hi/lo tile pair.
@@ -286,38 +308,44 @@ __device__ void unit_lower_inverse(uint8_t *sm, int s) {
     named_sync(BAR_S1, NS1);
 }
 
-__device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t t1, int nchunks, int h,
-                            const int tid) {
+__device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t t1, int nchunks, int h, int hq,
+                            const CUtensorMap *tmK, const CUtensorMap *tmQ, const int tid) {
+    // The two CTAs of a cluster take turns: CTA r prepares chunks c = r, r+2, ...
+    // and writes [T; PT] and the gates into its own and its peer's shared memory.
     const int s = tid - NCHAIN;  // 0..255
     const int warp = tid >> 5, lane = tid & 31;
     const int half = (s >> 5) >> 2;  // column half of this warp's TMEM reads
     const uint32_t tmem = x.tmem;
     float *sScan = reinterpret_cast<float *>(x.sm + SM_SCAN);
+    float *gp = reinterpret_cast<float *>(x.sm + SM_GPRIV);
+    const int first = (int)x.rank;
 
-    // gates of the next chunk, loaded one chunk ahead (threads s < 64)
+    // gates of this role's next chunk, loaded one turn ahead (threads s < 64)
     float g_next = 0.f, b_next = 0.f;
-    if (s < C && nchunks > 0 && s < t1 - t0) {
-        g_next = p.g[(size_t)(t0 + s) * p.h_v + h];
-        b_next = p.beta[(size_t)(t0 + s) * p.h_v + h];
+    if (s < C && first < nchunks && t0 + (int64_t)first * C + s < t1) {
+        g_next = p.g[(size_t)(t0 + (int64_t)first * C + s) * p.h_v + h];
+        b_next = p.beta[(size_t)(t0 + (int64_t)first * C + s) * p.h_v + h];
     }
-    for (int c = 0; c < nchunks; ++c) {
+    if (s == 0 && first < nchunks) issue_s1_loads(x, (int)(t0 + (int64_t)first * C), hq, tmK, tmQ);
+    int turn = 0;
+    for (int c = first; c < nchunks; c += 2, ++turn) {
         const int buf = c & 1;
         const int64_t c0 = t0 + (int64_t)c * C;
         float gt = g_next, bt = b_next;
         if (s < C) {
             g_next = b_next = 0.f;
-            if (c0 + C + s < t1) {
-                g_next = p.g[(size_t)(c0 + C + s) * p.h_v + h];
-                b_next = p.beta[(size_t)(c0 + C + s) * p.h_v + h];
+            if (c0 + 2 * C + s < t1) {
+                g_next = p.g[(size_t)(c0 + 2 * C + s) * p.h_v + h];
+                b_next = p.beta[(size_t)(c0 + 2 * C + s) * p.h_v + h];
             }
         }
-        // the chunk's tiles (issued by the chain once chunk c-2 released the buffer)
-        if (!role_wait(x, x.bar(B_TMA0 + buf), (uint32_t)(c >> 1) & 1u, ROLE_S1)) break;
+        // this turn's K and Q tile
+        if (!role_wait(x, x.bar(B_TMA_S1), (uint32_t)turn & 1u, ROLE_S1)) break;
 
         // Gram products of the chunk: [K Kᵀ; Q Kᵀ] into TMEM
         if (s == 0) {
-            tc_fence_after_sync();  // the previous chunk's reads of these TMEM columns are done
-            const uint32_t kq = x.sbase + OFF_KQ + buf * KQ_BYTES;
+            tc_fence_after_sync();  // the previous turn's reads of these TMEM columns are done
+            const uint32_t kq = x.sbase + OFF_S1;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
@@ -328,7 +356,6 @@ __device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t
         }
         // gates: G = inclusive running sum of g, kept as G log2(e) so every decay is one
         // ex2 (padding rows: g = 0, beta = 0)
-        float *gts = x.gates(buf);
         gt *= kLog2e;
         if (s < C) {
 #pragma unroll
@@ -337,13 +364,13 @@ __device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t
                 if (lane >= o) gt += u;
             }
             if (lane == 31) sScan[s >> 5] = gt;
-            gts[64 + s] = bt;
+            gp[64 + s] = bt;
         }
         named_sync(BAR_S1, NS1);
         if (s < C) {
             if (s >= 32) gt += sScan[0];
-            gts[s] = gt;
-            gts[128 + s] = fast_exp2(gt);
+            gp[s] = gt;
+            gp[128 + s] = fast_exp2(gt);
         }
         if (!role_wait(x, x.bar(B_MMA_S1), 0u, ROLE_S1)) break;  // also publishes the gates
         tc_fence_after_sync();
@@ -353,13 +380,13 @@ __device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t
             float a[32];
             tmem_ld32(lane_base(tmem, warp) + TM_G1 + 32 * half, a);
             const int t = row & 63;
-            const float Gt = gts[t];
+            const float Gt = gp[t];
             const bool is_n = row < 64;
-            const float w = is_n ? gts[64 + t] : 1.f;
+            const float w = is_n ? gp[64 + t] : 1.f;
             const int lim = is_n ? t : t + 1;  // keep j < t (N) or j <= t (P)
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
-                const float4 gj = *reinterpret_cast<const float4 *>(gts + 32 * half + j);
+                const float4 gj = *reinterpret_cast<const float4 *>(gp + 32 * half + j);
                 const float gv[4] = {gj.x, gj.y, gj.z, gj.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -380,10 +407,10 @@ __device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t
         named_sync(BAR_S1, NS1);
         unit_lower_inverse(x.sm, s);
 
-        // [T; PT] buffer: free once the chain's MMA2 of chunk c-1 has completed
-        if (c > 0 && !role_wait(x, x.bar(B_ATP_FREE), (uint32_t)(c - 1) & 1u, ROLE_S1)) break;
+        // [T; PT] buffers of both CTAs are free once both chains finished MMA2 of chunk c-1
+        if (c > 0 && !role_wait(x, x.bar(B_ATP_FREE), (uint32_t)((c - 1) >> 1) & 1u, ROLE_S1)) break;
         {
-            // T rows as the top half of [T; PT] (also the B operand of the PT product)
+            // T rows as the top half of [T; PT] (also the B operand of the PT product), and the gates
             const int row = s >> 2, cp = s & 3;
             const float *src = reinterpret_cast<const float *>(x.sm + OFF_T) + row * SROW + 16 * cp;
 #pragma unroll
@@ -393,9 +420,12 @@ __device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t
                 const float xv[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
                 store_hilo_chunk(x.sm + OFF_ATP_HI, x.sm + OFF_ATP_LO, row, 2 * cp + ch, xv);
             }
+            if (s < 192) x.gates(buf)[s] = gp[s];
         }
         fence_proxy_async_smem();
         named_sync(BAR_S1, NS1);
+        // the scratch is spent: fetch the next turn's K and Q into it
+        if (s == 0 && c + 2 < nchunks) issue_s1_loads(x, (int)(c0 + 2 * C), hq, tmK, tmQ);
         // PT = P T  (M = 64)
         if (s == 0) {
             tc_fence_after_sync();
@@ -422,7 +452,16 @@ __device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t
         fence_proxy_async_smem();
         tc_fence_before_sync();
         named_sync(BAR_S1, NS1);
-        if (s == 0) mbar_arrive(x.bar(B_ATP_FULL));
+        if (s == 0) {
+            // local chain: [T; PT] and gates are in place; peer chain: one bulk copy of both
+            mbar_arrive(x.bar(B_ATP_FULL));
+            const uint32_t peer_full = x.peer_base + SM_BARS + 8 * B_ATP_FULL;
+            mbar_arrive_expect_tx_cluster(peer_full, ATP_COPY_BYTES);
+            bulk_copy_to_peer(x.peer_base + OFF_ATP_HI, x.sbase + OFF_ATP_HI, 16384, peer_full);
+            bulk_copy_to_peer(x.peer_base + OFF_ATP_LO, x.sbase + OFF_ATP_LO, 16384, peer_full);
+            const uint32_t goff = SM_GATES + (uint32_t)buf * 192 * 4;
+            bulk_copy_to_peer(x.peer_base + goff, x.sbase + goff, 192 * 4, peer_full);
+        }
     }
 }
 
@@ -508,7 +547,12 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
         if (!role_wait(x, x.bar(B_MMA_CHAIN), mma_phase, ROLE_CHAIN)) break;
         mma_phase ^= 1;
         tc_fence_after_sync();
-        if (tid == 0) mbar_arrive(x.bar(B_ATP_FREE));  // stage 1 may overwrite [T; PT]
+        if (tid == 0) {
+            // [T; PT] may be overwritten: tell the CTA that prepares chunk c+1
+            const uint32_t producer = (uint32_t)(c + 1) & 1u;
+            mbar_arrive_cluster(producer == x.rank ? map_to_rank(x.bar(B_ATP_FREE), x.rank)
+                                                   : x.peer_base + SM_BARS + 8 * B_ATP_FREE);
+        }
         {
             float dd[32];
             tmem_ld32(lb + TM_DP + 32 * hc, dd);
@@ -591,7 +635,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(x.sm + SM_TMEM);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int cb = blockIdx.x & 1;
+    x.rank = cluster_rank();
+    x.peer_base = map_to_rank(x.sbase, x.rank ^ 1u);
+    const int cb = (int)x.rank;
     const int h = (blockIdx.x >> 1) % p.h_v;
     const int s = (blockIdx.x >> 1) / p.h_v;
     const int hq = h / (p.h_v / p.h_qk);
@@ -599,7 +645,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int nchunks = (int)((t1 - t0 + C - 1) / C);
 
     if (tid == 0) {
-        for (int i = 0; i < 6; ++i) mbar_init(x.bar(i), 1);
+        for (int i = 0; i < NBARS; ++i) mbar_init(x.bar(i), i == B_ATP_FREE ? 2 : 1);
         x.abort_flag[0] = 0;
         x.abort_flag[1] = 0;
         fence_mbar_init();
@@ -625,7 +671,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         fence_proxy_async_smem();
     }
     tc_fence_before_sync();
-    __syncthreads();
+    cluster_sync();  // both CTAs' barriers are initialised before any remote arrive
     tc_fence_after_sync();
     x.tmem = *tmem_holder;
 
@@ -638,7 +684,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (tid < NCHAIN)
         chain_role(x, p, t0, t1, nchunks, h, hq, cb, Sr, &tmK, &tmQ, &tmV, tid, ok);
     else
-        stage1_role(x, p, t0, t1, nchunks, h, tid);
+        stage1_role(x, p, t0, t1, nchunks, h, hq, &tmK, &tmQ, tid);
 
     if (tid < NCHAIN) {
         if (ok) {
@@ -654,7 +700,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     }
     tc_fence_before_sync();
-    __syncthreads();
+    cluster_sync();  // no CTA leaves while its peer may still write into its shared memory
     if (warp == 0) {
         tc_fence_after_sync();
         tmem_dealloc(x.tmem, TM_COLS);
@@ -715,8 +761,20 @@ cudaError_t launch_prefill_tc(const Args &a, cudaStream_t s) {
     p.beta = a.beta;
     p.state = a.state;
     p.o = a.o;
-    const unsigned blocks = (unsigned)a.n_seqs * (unsigned)a.h_v * (unsigned)(D / BV);
-    prefill_tc_kernel<<<blocks, NTHREADS, SMEM_BYTES, s>>>(tmK, tmQ, tmV, p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.n_seqs * (unsigned)a.h_v * (unsigned)(D / BV));
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;  // the two column blocks of one V head
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel, tmK, tmQ, tmV, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

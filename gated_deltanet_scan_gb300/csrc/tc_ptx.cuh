@@ -26,12 +26,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
+    // acquire at cluster scope (producers may live in the peer CTA); the hint
+    // lets the hardware park the thread up to ~8 us instead of re-polling
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(8192u)
         : "memory");
     return ok != 0;
 }
@@ -49,6 +51,54 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// ---- thread-block clusters ------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Address of the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// Release-arrive on an mbarrier that may sit in another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Arrive on a (possibly remote) mbarrier and raise its expected transaction bytes.
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_addr, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr),
+                 "r"(bytes)
+                 : "memory");
+}
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a peer
+// CTA's; completes as transaction bytes on the peer's mbarrier.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                  uint32_t mbar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_cluster),
+        "r"(src_cta), "r"(bytes), "r"(mbar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Generic-proxy writes to this CTA's or a peer CTA's shared memory -> async proxy.
+__device__ __forceinline__ void fence_proxy_async_cluster() {
+    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+
 // Barrier among `count` threads (a multiple of 32) of the CTA, by id (1..15).
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -164,12 +214,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
     return (uint32_t)(row * 128 + (((chunk ^ (row & 7)) & 7) << 4));
 }
-__device__ __forceinline__ void store_hilo_chunk(uint8_t *hi_base, uint8_t *lo_base, int row, int chunk,
-                                                 const float *x) {
-    // hi: x with its low 16 bits dropped (exactly the top half of the fp32 word);
-    // lo: the exact remainder x - hi, rounded to bf16.  |lo| < 2^-7 |x|, so
-    // hi + lo matches x to 2^-16 relative.
-    uint32_t h[4], l[4];
+// hi: x with its low 16 bits dropped (exactly the top half of the fp32 word);
+// lo: the exact remainder x - hi, rounded to bf16.  |lo| < 2^-7 |x|, so
+// hi + lo matches x to 2^-16 relative.  Packs 8 values into 4 + 4 words.
+__device__ __forceinline__ void hilo_words(const float *x, uint32_t *h, uint32_t *l) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const uint32_t a = __float_as_uint(x[2 * i]), b = __float_as_uint(x[2 * i + 1]);
@@ -178,6 +226,11 @@ __device__ __forceinline__ void store_hilo_chunk(uint8_t *hi_base, uint8_t *lo_b
         const float rb = x[2 * i + 1] - __uint_as_float(b & 0xFFFF0000u);
         l[i] = pack_bf16x2(ra, rb);
     }
+}
+__device__ __forceinline__ void store_hilo_chunk(uint8_t *hi_base, uint8_t *lo_base, int row, int chunk,
+                                                 const float *x) {
+    uint32_t h[4], l[4];
+    hilo_words(x, h, l);
     const uint32_t off = sw128_offset(row, chunk);
     *reinterpret_cast<uint4 *>(hi_base + off) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint4 *>(lo_base + off) = make_uint4(l[0], l[1], l[2], l[3]);
