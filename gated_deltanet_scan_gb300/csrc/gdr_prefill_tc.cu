@@ -1,10 +1,11 @@
 // Chunked prefill on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
 // Shapes: d_k = d_v = 128, 64-token chunks, bf16 q/k/v, fp32 state, fp32 or
-// bf16 output.  One CTA owns (sequence, V head, 64 state columns) and walks
-// that sequence's chunks in order, keeping its 128 x 64 block of the state on
-// chip for the whole sequence (fp32 in registers, bf16 hi/lo copies in shared
-// memory as MMA operands).
+// bf16 output.  A cluster of four CTAs owns one (sequence, V head); CTA r of
+// the cluster owns state columns [32 r, 32 r + 32) and walks the sequence's
+// chunks in order, keeping its 128 x 32 block of the state on chip for the
+// whole sequence (fp32 in registers, bf16 hi/lo copies in shared memory as
+// MMA operands).
 //
 // Per chunk (the chunkwise-parallel form of the Qwen3.5-9B NPU model card,
 // "How it works"; forward substitution for the unit triangular factor as in
@@ -28,18 +29,16 @@
 //
 // Warp roles (512 threads).  Warps 0-7, the "chain", run the state-dependent
 // MMA1 -> MMA2 -> MMA3 sequence of chunk c; warp w owns TMEM lanes
-// 32 (w % 4) .. + 31 and state columns 32 (w / 4) .. + 31 of those rows.
-// Warps 8-15, "stage 1", meanwhile prepare chunk c+1: gates, the Gram MMA,
-// N and P, the triangular inverse and the P T product, staged as [T; PT] for
-// the chain.  They hand over through mbarriers: TMA -> both roles (tiles
-// landed), stage 1 -> chain ([T; PT] and gates ready), chain -> stage 1
-// ([T; PT] buffer free again).  The chain issues the TMA for chunk c+2 into
-// chunk c's buffers once its last MMA on them has completed.
-//
-// Every mbarrier wait is bounded: on timeout a thread records
-// GDR_ERR_DEVICE_TIMEOUT in the device error word and its role stops; the
-// other role then times out on its own next wait, any outstanding TMA is
-// waited for (bounded), and the CTA frees its TMEM and returns.
+// 32 (w % 4) .. + 31 and state columns 16 (w / 4) .. + 15 of the CTA's 32.
+// Warps 8-15, "stage 1", prepare the state-independent factors.  The four
+// CTAs of a cluster take turns: CTA r prepares chunks r, r+4, r+8, ... (gates,
+// Gram MMA, N and P, triangular inverse, P T), stages [T; PT] and the gates
+// in one of two buffers, and bulk-copies them into the three peers' shared
+// memory, completing on each peer's mbarrier.  Chains signal a buffer free
+// to the CTA that fills it next.  Every mbarrier wait is bounded: on timeout
+// a thread records GDR_ERR_DEVICE_TIMEOUT in the device error word and its
+// role stops; the peers time out on their own waits, and every CTA meets the
+// final cluster barrier, frees its TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -57,9 +56,10 @@ using namespace tc;
 
 constexpr int C = 64;
 constexpr int D = 128;
-constexpr int BV = 64;
-constexpr int NCHAIN = 256;  // warps 0-7
-constexpr int NS1 = 256;     // warps 8-15
+constexpr int NCL = 4;         // CTAs per cluster (column blocks of one V head)
+constexpr int BV = D / NCL;    // 32 state columns per CTA
+constexpr int NCHAIN = 256;    // warps 0-7
+constexpr int NS1 = 256;       // warps 8-15
 constexpr int NTHREADS = NCHAIN + NS1;
 constexpr int SROW = 68;  // fp32 scratch row stride in floats (bank-conflict-free float4 rows)
 constexpr int XROW = 33;  // level-2 partial product row stride
@@ -68,62 +68,63 @@ constexpr int ROLE_CHAIN = 0, ROLE_S1 = 1;
 
 // Shared memory map, bytes from a 1024-byte aligned base.
 constexpr uint32_t KQ_BYTES = 32768;  // [kb=0: K rows 0-63, Q rows 64-127][kb=1: same], 128-B rows
-constexpr uint32_t V_BYTES = 8192;    // V tile: 64 tokens x 64 columns
-constexpr uint32_t OFF_KQ = 0;        // two buffers
-constexpr uint32_t OFF_V = 2 * KQ_BYTES;                // two buffers
-constexpr uint32_t OFF_ATP_HI = OFF_V + 2 * V_BYTES;  // [T; PT] as K-major 128 x 64 bf16
-constexpr uint32_t OFF_ATP_LO = OFF_ATP_HI + 16384;
-constexpr uint32_t OFF_S_HI = OFF_ATP_LO + 16384;  // state block as MN-major 128 (k) x 64 (n) bf16
-constexpr uint32_t OFF_S_LO = OFF_S_HI + 16384;
-constexpr uint32_t OFF_RD_HI = OFF_S_LO + 16384;  // R, then D~: MN-major 64 (k = token) x 64 (n)
-constexpr uint32_t OFF_RD_LO = OFF_RD_HI + 8192;
-constexpr uint32_t OFF_P_HI = OFF_RD_LO + 8192;   // P as K-major 64 x 64 bf16 (A of the PT MMA)
+constexpr uint32_t V_BYTES = 4096;    // V tile: 64 tokens x 32 columns, 64-B rows
+constexpr uint32_t OFF_KQ = 0;        // two ring buffers
+constexpr uint32_t OFF_V = 2 * KQ_BYTES;  // two ring buffers
+constexpr uint32_t ATP_BYTES = 32768;     // [T; PT] hi (16 KB) + lo (16 KB), K-major 128 x 64 bf16
+constexpr uint32_t OFF_ATP = OFF_V + 2 * V_BYTES;  // two buffers (chunk parity)
+constexpr uint32_t OFF_S_HI = OFF_ATP + 2 * ATP_BYTES;  // state block, MN-major 128 (k) x 32 (n), 64-B rows
+constexpr uint32_t OFF_S_LO = OFF_S_HI + 8192;
+constexpr uint32_t OFF_RD_HI = OFF_S_LO + 8192;  // R, then D~: MN-major 64 (k = token) x 32 (n)
+constexpr uint32_t OFF_RD_LO = OFF_RD_HI + 4096;
+constexpr uint32_t OFF_P_HI = OFF_RD_LO + 4096;  // P as K-major 64 x 64 bf16 (A of the PT MMA)
 constexpr uint32_t OFF_P_LO = OFF_P_HI + 8192;
-constexpr uint32_t SCR_MAT = 64 * SROW * 4;       // fp32 [64][SROW]
-// Stage 1's own K/Q tile for the Gram MMA (same layout as one ring buffer); once
-// that MMA has completed the region holds the fp32 scratch N, T and X.
+constexpr uint32_t SCR_MAT = 64 * SROW * 4;      // fp32 [64][SROW]
+// Stage 1's own K/Q tile for the Gram MMA; once that MMA has completed the
+// region holds the fp32 scratch N, T and X.
 constexpr uint32_t OFF_S1 = OFF_P_LO + 8192;
 constexpr uint32_t OFF_N = OFF_S1;
 constexpr uint32_t OFF_T = OFF_N + SCR_MAT;
-constexpr uint32_t OFF_X = OFF_T + SCR_MAT;       // partial products: [32][XROW] fp32
+constexpr uint32_t OFF_X = OFF_T + SCR_MAT;  // partial products: [32][XROW] fp32
 constexpr uint32_t S1_BYTES = 40960;
 constexpr uint32_t OFF_SMALL = OFF_S1 + S1_BYTES;
-static_assert(OFF_X + 32 * XROW * 4 <= OFF_S1 + S1_BYTES && KQ_BYTES <= S1_BYTES, "stage-1 region");
-constexpr uint32_t SM_GATES = OFF_SMALL;          // float [2 chunks][3][64]: G log2(e), beta, e^G
-constexpr uint32_t SM_SCAN = OFF_SMALL + 1536;    // float[4]
-constexpr uint32_t SM_GPRIV = OFF_SMALL + 2048;   // float[3][64]: stage 1's own copy of the gates
-constexpr uint32_t SM_BARS = OFF_SMALL + 1600;    // 8 x uint64
-constexpr uint32_t SM_TMEM = OFF_SMALL + 1664;    // uint32
-constexpr uint32_t SM_ABORT = OFF_SMALL + 1672;   // int32[2], one per role
-constexpr uint32_t SMEM_USED = OFF_SMALL + 2048 + 768;
+constexpr uint32_t SM_GATES = OFF_SMALL;         // float [2 buffers][3][64]: G log2(e), beta, e^G
+constexpr uint32_t SM_SCAN = OFF_SMALL + 1536;   // float[4]
+constexpr uint32_t SM_BARS = OFF_SMALL + 1600;   // 8 x uint64
+constexpr uint32_t SM_TMEM = OFF_SMALL + 1664;   // uint32
+constexpr uint32_t SM_ABORT = OFF_SMALL + 1672;  // int32[2], one per role
+constexpr uint32_t SM_GPRIV = OFF_SMALL + 2048;  // float[3][64]: stage 1's own copy of the gates
+constexpr uint32_t SMEM_USED = OFF_SMALL + 3072;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(OFF_RD_HI % 1024 == 0 && OFF_P_HI % 1024 == 0 && OFF_P_LO % 1024 == 0 && OFF_ATP_HI % 1024 == 0 &&
-                  OFF_S_LO % 1024 == 0,
+static_assert(OFF_X + 32 * XROW * 4 <= OFF_S1 + S1_BYTES && KQ_BYTES <= S1_BYTES, "stage-1 region");
+static_assert(OFF_ATP % 1024 == 0 && OFF_S_HI % 1024 == 0 && OFF_RD_HI % 1024 == 0 && OFF_P_HI % 1024 == 0 &&
+                  OFF_S1 % 1024 == 0 && OFF_V % 1024 == 0,
               "operand tiles must be 1 KB aligned");
 
 // mbarriers
-constexpr int B_TMA0 = 0, B_MMA_CHAIN = 2, B_MMA_S1 = 3, B_ATP_FULL = 4, B_ATP_FREE = 5, B_TMA_S1 = 6;
-constexpr int NBARS = 7;
+constexpr int B_TMA0 = 0, B_MMA_CHAIN = 2, B_MMA_S1 = 3, B_ATP_FULL0 = 4, B_ATP_FREE = 6, B_TMA_S1 = 7;
+constexpr int NBARS = 8;
 
 // TMEM columns (fp32 accumulators).
-constexpr uint32_t TM_G1 = 0;    // [K Kᵀ; Q Kᵀ]   (stage 1, lane = row)
-constexpr uint32_t TM_PT = 64;   // P T            (stage 1, M=64 layout)
-constexpr uint32_t TM_KS = 128;  // [K S; Q S]     (chain)
-constexpr uint32_t TM_DP = 192;  // [D; P D]       (chain)
-constexpr uint32_t TM_Y = 256;   // Kᵀ D~          (chain)
-constexpr uint32_t TM_COLS = 512;
+constexpr uint32_t TM_G1 = 0;    // [K Kᵀ; Q Kᵀ]   128 x 64 (stage 1, lane = row)
+constexpr uint32_t TM_PT = 64;   // P T            64 x 64  (stage 1, M=64 layout)
+constexpr uint32_t TM_KS = 128;  // [K S; Q S]     128 x 32 (chain)
+constexpr uint32_t TM_DP = 160;  // [D; P D]       128 x 32 (chain)
+constexpr uint32_t TM_Y = 192;   // Kᵀ D~          128 x 32 (chain)
+constexpr uint32_t TM_COLS = 256;
 
-constexpr uint32_t TMA_BYTES = 2 * 16384 + V_BYTES;  // K + Q (two 64-column halves each) + V
-constexpr uint32_t ATP_COPY_BYTES = 2 * 16384 + 192 * 4;  // [T; PT] hi + lo, and the gates
-constexpr long long kWaitLimit = 4000000000LL;       // SM clocks (about 2 s)
+constexpr uint32_t TMA_BYTES = 2 * 16384 + V_BYTES;      // K + Q (two 64-column halves each) + V
+constexpr uint32_t GATE_BYTES = 192 * 4;
+constexpr uint32_t ATP_COPY_BYTES = ATP_BYTES + GATE_BYTES;
+constexpr long long kWaitLimit = 4000000000LL;  // SM clocks (about 2 s)
 constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr uint32_t IDESC_G1 = idesc_bf16_f32(128, 64, 0, 0);  // A K-major, B K-major
 constexpr uint32_t IDESC_PT = idesc_bf16_f32(64, 64, 0, 1);   // A K-major (P), B MN-major (T)
-constexpr uint32_t IDESC_KS = idesc_bf16_f32(128, 64, 0, 1);  // A K-major, B MN-major
-constexpr uint32_t IDESC_DP = idesc_bf16_f32(128, 64, 0, 1);
-constexpr uint32_t IDESC_Y = idesc_bf16_f32(128, 64, 1, 1);   // A MN-major (Kᵀ), B MN-major
+constexpr uint32_t IDESC_KS = idesc_bf16_f32(128, BV, 0, 1);  // A K-major, B MN-major
+constexpr uint32_t IDESC_DP = idesc_bf16_f32(128, BV, 0, 1);
+constexpr uint32_t IDESC_Y = idesc_bf16_f32(128, BV, 1, 1);   // A MN-major (Kᵀ), B MN-major
 
 struct TcParams {
     int h_qk, h_v, out_bf16;
@@ -139,11 +140,14 @@ struct Ctx {
     uint32_t sbase;
     uint32_t tmem;
     volatile int *abort_flag;
-    uint32_t rank;        // this CTA's rank in its cluster of two (= its column block)
-    uint32_t peer_base;   // cluster address of the peer CTA's shared-memory base
+    uint32_t rank;  // rank in the cluster = column block
     __device__ uint32_t bar(int i) const { return sbase + SM_BARS + 8 * i; }
     __device__ float *gates(int buf) const { return reinterpret_cast<float *>(sm + SM_GATES) + buf * 192; }
+    __device__ uint32_t atp_hi(int buf) const { return OFF_ATP + buf * ATP_BYTES; }
+    __device__ uint32_t atp_lo(int buf) const { return OFF_ATP + buf * ATP_BYTES + 16384; }
 };
+
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
 __device__ __forceinline__ void role_sync(int role) {
     if (role == ROLE_CHAIN)
@@ -166,7 +170,7 @@ __device__ __forceinline__ bool role_wait(const Ctx &x, uint32_t bar, uint32_t p
     return x.abort_flag[role] == 0;
 }
 
-__device__ __forceinline__ void issue_chunk_loads(const Ctx &x, int buf, int tok, int hq, int h, int cb,
+__device__ __forceinline__ void issue_chunk_loads(const Ctx &x, int buf, int tok, int hq, int h,
                                                   const CUtensorMap *tmK, const CUtensorMap *tmQ,
                                                   const CUtensorMap *tmV) {
     const uint32_t bar = x.bar(B_TMA0 + buf);
@@ -176,7 +180,7 @@ __device__ __forceinline__ void issue_chunk_loads(const Ctx &x, int buf, int tok
     tma_load_3d(kq + 16384, tmK, bar, 64, hq, tok);
     tma_load_3d(kq + 8192, tmQ, bar, 0, hq, tok);
     tma_load_3d(kq + 16384 + 8192, tmQ, bar, 64, hq, tok);
-    tma_load_3d(x.sbase + OFF_V + buf * V_BYTES, tmV, bar, cb * BV, h, tok);
+    tma_load_3d(x.sbase + OFF_V + buf * V_BYTES, tmV, bar, (int)x.rank * BV, h, tok);
 }
 
 // Stage 1's copy of the chunk's K and Q (for the Gram MMA only).
@@ -191,10 +195,15 @@ __device__ __forceinline__ void issue_s1_loads(const Ctx &x, int tok, int hq, co
     tma_load_3d(kq + 16384 + 8192, tmQ, bar, 64, hq, tok);
 }
 
-// 32 values as chunks [4 half, 4 half + 4) of row `row` of a hi/lo tile pair.
+// 32 values as chunks [4 half, 4 half + 4) of row `row` of a 128-B hi/lo tile pair.
 __device__ __forceinline__ void store_half_hilo(uint8_t *hi, uint8_t *lo, int row, int half, const float *x) {
 #pragma unroll
     for (int ch = 0; ch < 4; ++ch) store_hilo_chunk(hi, lo, row, 4 * half + ch, x + 8 * ch);
+}
+// 16 values as chunks [2 half, 2 half + 2) of row `row` of a 64-B hi/lo tile pair.
+__device__ __forceinline__ void store_quarter_hilo64(uint8_t *hi, uint8_t *lo, int row, int half, const float *x) {
+    store_hilo_chunk64(hi, lo, row, 2 * half, x);
+    store_hilo_chunk64(hi, lo, row, 2 * half + 1, x + 8);
 }
 
 __device__ __forceinline__ uint32_t lane_base(uint32_t tmem, int warp) {
@@ -310,8 +319,6 @@ __device__ void unit_lower_inverse(uint8_t *sm, int s) {
 
 __device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t t1, int nchunks, int h, int hq,
                             const CUtensorMap *tmK, const CUtensorMap *tmQ, const int tid) {
-    // The two CTAs of a cluster take turns: CTA r prepares chunks c = r, r+2, ...
-    // and writes [T; PT] and the gates into its own and its peer's shared memory.
     const int s = tid - NCHAIN;  // 0..255
     const int warp = tid >> 5, lane = tid & 31;
     const int half = (s >> 5) >> 2;  // column half of this warp's TMEM reads
@@ -328,15 +335,15 @@ __device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t
     }
     if (s == 0 && first < nchunks) issue_s1_loads(x, (int)(t0 + (int64_t)first * C), hq, tmK, tmQ);
     int turn = 0;
-    for (int c = first; c < nchunks; c += 2, ++turn) {
+    for (int c = first; c < nchunks; c += NCL, ++turn) {
         const int buf = c & 1;
         const int64_t c0 = t0 + (int64_t)c * C;
         float gt = g_next, bt = b_next;
         if (s < C) {
             g_next = b_next = 0.f;
-            if (c0 + 2 * C + s < t1) {
-                g_next = p.g[(size_t)(c0 + 2 * C + s) * p.h_v + h];
-                b_next = p.beta[(size_t)(c0 + 2 * C + s) * p.h_v + h];
+            if (c0 + NCL * C + s < t1) {
+                g_next = p.g[(size_t)(c0 + NCL * C + s) * p.h_v + h];
+                b_next = p.beta[(size_t)(c0 + NCL * C + s) * p.h_v + h];
             }
         }
         // this turn's K and Q tile
@@ -345,11 +352,10 @@ __device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t
         // Gram products of the chunk: [K Kᵀ; Q Kᵀ] into TMEM
         if (s == 0) {
             tc_fence_after_sync();  // the previous turn's reads of these TMEM columns are done
-            const uint32_t kq = x.sbase + OFF_S1;
+            const uint64_t a0 = smem_desc_sw128(x.sbase + OFF_S1, 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
-                const uint64_t a = smem_desc_sw128(kq + koff, 16, 1024);
+                const uint64_t a = desc_add(a0, (ks >> 2) * 16384 + (ks & 3) * 32);
                 mma_bf16(tmem + TM_G1, a, a, IDESC_G1, ks > 0);
             }
             mma_commit(x.bar(B_MMA_S1));
@@ -407,8 +413,8 @@ __device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t
         named_sync(BAR_S1, NS1);
         unit_lower_inverse(x.sm, s);
 
-        // [T; PT] buffers of both CTAs are free once both chains finished MMA2 of chunk c-1
-        if (c > 0 && !role_wait(x, x.bar(B_ATP_FREE), (uint32_t)((c - 1) >> 1) & 1u, ROLE_S1)) break;
+        // this parity's [T; PT] buffers are free once every chain finished MMA2 of chunk c-2
+        if (c >= 2 && !role_wait(x, x.bar(B_ATP_FREE), (uint32_t)((c - 2) >> 2) & 1u, ROLE_S1)) break;
         {
             // T rows as the top half of [T; PT] (also the B operand of the PT product), and the gates
             const int row = s >> 2, cp = s & 3;
@@ -418,23 +424,25 @@ __device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t
                 const float4 u = *reinterpret_cast<const float4 *>(src + 8 * ch);
                 const float4 v = *reinterpret_cast<const float4 *>(src + 8 * ch + 4);
                 const float xv[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
-                store_hilo_chunk(x.sm + OFF_ATP_HI, x.sm + OFF_ATP_LO, row, 2 * cp + ch, xv);
+                store_hilo_chunk(x.sm + x.atp_hi(buf), x.sm + x.atp_lo(buf), row, 2 * cp + ch, xv);
             }
             if (s < 192) x.gates(buf)[s] = gp[s];
         }
         fence_proxy_async_smem();
         named_sync(BAR_S1, NS1);
         // the scratch is spent: fetch the next turn's K and Q into it
-        if (s == 0 && c + 2 < nchunks) issue_s1_loads(x, (int)(c0 + 2 * C), hq, tmK, tmQ);
+        if (s == 0 && c + NCL < nchunks) issue_s1_loads(x, (int)(c0 + NCL * C), hq, tmK, tmQ);
         // PT = P T  (M = 64)
         if (s == 0) {
             tc_fence_after_sync();
+            const uint64_t ah0 = smem_desc_sw128(x.sbase + OFF_P_HI, 16, 1024);
+            const uint64_t al0 = smem_desc_sw128(x.sbase + OFF_P_LO, 16, 1024);
+            const uint64_t bh0 = smem_desc_sw128(x.sbase + x.atp_hi(buf), 16, 1024);
+            const uint64_t bl0 = smem_desc_sw128(x.sbase + x.atp_lo(buf), 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t ah = smem_desc_sw128(x.sbase + OFF_P_HI + ks * 32, 16, 1024);
-                const uint64_t al = smem_desc_sw128(x.sbase + OFF_P_LO + ks * 32, 16, 1024);
-                const uint64_t bh = smem_desc_sw128(x.sbase + OFF_ATP_HI + ks * 2048, 16, 1024);
-                const uint64_t bl = smem_desc_sw128(x.sbase + OFF_ATP_LO + ks * 2048, 16, 1024);
+                const uint64_t ah = desc_add(ah0, ks * 32), al = desc_add(al0, ks * 32);
+                const uint64_t bh = desc_add(bh0, ks * 2048), bl = desc_add(bl0, ks * 2048);
                 mma_bf16(tmem + TM_PT, ah, bh, IDESC_PT, ks > 0);
                 mma_bf16(tmem + TM_PT, al, bh, IDESC_PT, 1);
                 mma_bf16(tmem + TM_PT, ah, bl, IDESC_PT, 1);
@@ -447,34 +455,44 @@ __device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t
             // M = 64 accumulator: row i sits in lane 32 (i / 16) + i % 16
             float a[32];
             tmem_ld32(lane_base(tmem, warp) + TM_PT + 32 * half, a);
-            if (lane < 16) store_half_hilo(x.sm + OFF_ATP_HI, x.sm + OFF_ATP_LO, 64 + 16 * (warp & 3) + lane, half, a);
+            if (lane < 16)
+                store_half_hilo(x.sm + x.atp_hi(buf), x.sm + x.atp_lo(buf), 64 + 16 * (warp & 3) + lane, half, a);
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
         named_sync(BAR_S1, NS1);
         if (s == 0) {
-            // local chain: [T; PT] and gates are in place; peer chain: one bulk copy of both
-            mbar_arrive(x.bar(B_ATP_FULL));
-            const uint32_t peer_full = x.peer_base + SM_BARS + 8 * B_ATP_FULL;
-            mbar_arrive_expect_tx_cluster(peer_full, ATP_COPY_BYTES);
-            bulk_copy_to_peer(x.peer_base + OFF_ATP_HI, x.sbase + OFF_ATP_HI, 16384, peer_full);
-            bulk_copy_to_peer(x.peer_base + OFF_ATP_LO, x.sbase + OFF_ATP_LO, 16384, peer_full);
-            const uint32_t goff = SM_GATES + (uint32_t)buf * 192 * 4;
-            bulk_copy_to_peer(x.peer_base + goff, x.sbase + goff, 192 * 4, peer_full);
+            // local chain: [T; PT] and gates are in place; each peer: one bulk copy of both
+            mbar_arrive(x.bar(B_ATP_FULL0 + buf));
+            const uint32_t goff = SM_GATES + (uint32_t)buf * GATE_BYTES;
+#pragma unroll
+            for (uint32_t d = 1; d < NCL; ++d) {
+                const uint32_t peer = map_to_rank(x.sbase, (x.rank + d) % NCL);
+                const uint32_t full = peer + SM_BARS + 8 * (B_ATP_FULL0 + buf);
+                mbar_arrive_expect_tx_cluster(full, ATP_COPY_BYTES);
+                bulk_copy_to_peer(peer + x.atp_hi(buf), x.sbase + x.atp_hi(buf), ATP_BYTES, full);
+                bulk_copy_to_peer(peer + goff, x.sbase + goff, GATE_BYTES, full);
+            }
         }
     }
 }
 
 // ================================= chain ============================================
 __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t t1, int nchunks, int h, int hq,
-                           int cb, float *Sr, const CUtensorMap *tmK, const CUtensorMap *tmQ,
-                           const CUtensorMap *tmV, const int tid, bool &ok) {
+                           float *Sr, const CUtensorMap *tmK, const CUtensorMap *tmQ, const CUtensorMap *tmV,
+                           const int tid, bool &ok) {
     const int warp = tid >> 5, lane = tid & 31;
-    const int hc = warp >> 2;                    // column half
+    const int hc = warp >> 2;                    // column half: columns [16 hc, 16 hc + 16) of the CTA's 32
     const int row = ((warp & 3) << 5) + lane;  // TMEM lane = state row (d_k index) / chunk row
     const int t = row & 63;
     const uint32_t lb = lane_base(x.tmem, warp);
     const uint32_t tmem = x.tmem;
+    const int cb = (int)x.rank;
+    // descriptor bases (start addresses advance per MMA)
+    const uint64_t dS_hi = smem_desc(x.sbase + OFF_S_HI, 8192, 512, kSwizzle64);
+    const uint64_t dS_lo = smem_desc(x.sbase + OFF_S_LO, 8192, 512, kSwizzle64);
+    const uint64_t dRD_hi = smem_desc(x.sbase + OFF_RD_HI, 4096, 512, kSwizzle64);
+    const uint64_t dRD_lo = smem_desc(x.sbase + OFF_RD_LO, 4096, 512, kSwizzle64);
     uint32_t mma_phase = 0;
     for (int c = 0; c < nchunks; ++c) {
         const int buf = c & 1;
@@ -486,43 +504,41 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
         // ---- MMA1: [K S; Q S] = [K; Q] (S_hi + S_lo) --------------------------------
         if (tid == 0) {
             tc_fence_after_sync();
+            const uint64_t a0 = smem_desc_sw128(kq, 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
-                const uint64_t a = smem_desc_sw128(kq + koff, 16, 1024);
-                const uint64_t bh = smem_desc_sw128(x.sbase + OFF_S_HI + ks * 2048, 16, 1024);
-                const uint64_t bl = smem_desc_sw128(x.sbase + OFF_S_LO + ks * 2048, 16, 1024);
-                mma_bf16(tmem + TM_KS, a, bh, IDESC_KS, ks > 0);
-                mma_bf16(tmem + TM_KS, a, bl, IDESC_KS, 1);
+                const uint64_t a = desc_add(a0, (ks >> 2) * 16384 + (ks & 3) * 32);
+                mma_bf16(tmem + TM_KS, a, desc_add(dS_hi, ks * 1024), IDESC_KS, ks > 0);
+                mma_bf16(tmem + TM_KS, a, desc_add(dS_lo, ks * 1024), IDESC_KS, 1);
             }
             mma_commit(x.bar(B_MMA_CHAIN));
         }
         // stage 1 of this chunk: gates and [T; PT]
-        if (!role_wait(x, x.bar(B_ATP_FULL), (uint32_t)c & 1u, ROLE_CHAIN)) break;
+        if (!role_wait(x, x.bar(B_ATP_FULL0 + buf), (uint32_t)(c >> 1) & 1u, ROLE_CHAIN)) break;
         const float *gts = x.gates(buf);
         const float Gt = gts[t], bt = gts[64 + t], egt = gts[128 + t];
         const float eGC = gts[128 + C - 1], GC = gts[C - 1];
         if (!role_wait(x, x.bar(B_MMA_CHAIN), mma_phase, ROLE_CHAIN)) break;
         mma_phase ^= 1;
         tc_fence_after_sync();
-        float qse[32];  // rows 64-127: e^G Q S for this thread's columns, kept for the output
+        float qse[16];  // rows 64-127: e^G Q S for this thread's columns, kept for the output
         {
-            float a[32];
-            tmem_ld32(lb + TM_KS + 32 * hc, a);
+            float a[16];
+            tmem_ld16(lb + TM_KS + 16 * hc, a);
             if (row < 64) {
                 // R = beta (V - e^G K S), staged as the hi/lo MN-major B operand of MMA2
                 const uint8_t *vt = x.sm + OFF_V + buf * V_BYTES;
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
+                for (int ch = 0; ch < 2; ++ch) {
                     float v[8], r[8];
-                    load_bf16_chunk(vt, t, 4 * hc + ch, v);
+                    load_bf16_chunk64(vt, t, 2 * hc + ch, v);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) r[e] = bt * (v[e] - egt * a[ch * 8 + e]);
-                    store_hilo_chunk(x.sm + OFF_RD_HI, x.sm + OFF_RD_LO, t, 4 * hc + ch, r);
+                    store_hilo_chunk64(x.sm + OFF_RD_HI, x.sm + OFF_RD_LO, t, 2 * hc + ch, r);
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) qse[j] = egt * a[j];
+                for (int j = 0; j < 16; ++j) qse[j] = egt * a[j];
             }
         }
         fence_proxy_async_smem();
@@ -532,12 +548,12 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
         // ---- MMA2: [D; P D] = [T; PT] R ---------------------------------------------
         if (tid == 0) {
             tc_fence_after_sync();
+            const uint64_t ah0 = smem_desc_sw128(x.sbase + x.atp_hi(buf), 16, 1024);
+            const uint64_t al0 = smem_desc_sw128(x.sbase + x.atp_lo(buf), 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t ah = smem_desc_sw128(x.sbase + OFF_ATP_HI + ks * 32, 16, 1024);
-                const uint64_t al = smem_desc_sw128(x.sbase + OFF_ATP_LO + ks * 32, 16, 1024);
-                const uint64_t bh = smem_desc_sw128(x.sbase + OFF_RD_HI + ks * 2048, 16, 1024);
-                const uint64_t bl = smem_desc_sw128(x.sbase + OFF_RD_LO + ks * 2048, 16, 1024);
+                const uint64_t ah = desc_add(ah0, ks * 32), al = desc_add(al0, ks * 32);
+                const uint64_t bh = desc_add(dRD_hi, ks * 1024), bl = desc_add(dRD_lo, ks * 1024);
                 mma_bf16(tmem + TM_DP, ah, bh, IDESC_DP, ks > 0);
                 mma_bf16(tmem + TM_DP, al, bh, IDESC_DP, 1);
                 mma_bf16(tmem + TM_DP, ah, bl, IDESC_DP, 1);
@@ -548,27 +564,25 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
         mma_phase ^= 1;
         tc_fence_after_sync();
         if (tid == 0) {
-            // [T; PT] may be overwritten: tell the CTA that prepares chunk c+1
-            const uint32_t producer = (uint32_t)(c + 1) & 1u;
-            mbar_arrive_cluster(producer == x.rank ? map_to_rank(x.bar(B_ATP_FREE), x.rank)
-                                                   : x.peer_base + SM_BARS + 8 * B_ATP_FREE);
+            // this parity's [T; PT] may be overwritten: tell the CTA that fills it next (chunk c+2)
+            mbar_arrive_cluster(map_to_rank(x.bar(B_ATP_FREE), (uint32_t)(c + 2) % NCL));
         }
         {
-            float dd[32];
-            tmem_ld32(lb + TM_DP + 32 * hc, dd);
+            float dd[16];
+            tmem_ld16(lb + TM_DP + 16 * hc, dd);
             if (row < 64) {
                 // D~ = exp(G_C - G_t) D, staged as the hi/lo MN-major B operand of MMA3
                 const float sc = fast_exp2(GC - Gt);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) dd[j] *= sc;
-                store_half_hilo(x.sm + OFF_RD_HI, x.sm + OFF_RD_LO, t, hc, dd);
+                for (int j = 0; j < 16; ++j) dd[j] *= sc;
+                store_quarter_hilo64(x.sm + OFF_RD_HI, x.sm + OFF_RD_LO, t, hc, dd);
             } else if (t < L) {
                 // O = scale (e^G Q S + P D) for the chunk's real rows
-                const size_t off = ((size_t)(c0 + t) * p.h_v + h) * D + cb * BV + 32 * hc;
+                const size_t off = ((size_t)(c0 + t) * p.h_v + h) * D + cb * BV + 16 * hc;
                 if (p.out_bf16) {
                     uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + off);
 #pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
+                    for (int j = 0; j < 16; j += 8) {
                         float y[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e) y[e] = p.scale * (qse[j + e] + dd[j + e]);
@@ -578,7 +592,7 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
                 } else {
                     float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + off);
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
+                    for (int j = 0; j < 16; j += 4)
                         dst[j / 4] = make_float4(p.scale * (qse[j] + dd[j]), p.scale * (qse[j + 1] + dd[j + 1]),
                                                  p.scale * (qse[j + 2] + dd[j + 2]),
                                                  p.scale * (qse[j + 3] + dd[j + 3]));
@@ -592,13 +606,12 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
         // ---- MMA3: Y = Kᵀ (D~_hi + D~_lo) ---------------------------------------------
         if (tid == 0) {
             tc_fence_after_sync();
+            const uint64_t a0 = smem_desc_sw128(kq, 16384, 1024);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t a = smem_desc_sw128(kq + ks * 2048, 16384, 1024);
-                const uint64_t bh = smem_desc_sw128(x.sbase + OFF_RD_HI + ks * 2048, 16, 1024);
-                const uint64_t bl = smem_desc_sw128(x.sbase + OFF_RD_LO + ks * 2048, 16, 1024);
-                mma_bf16(tmem + TM_Y, a, bh, IDESC_Y, ks > 0);
-                mma_bf16(tmem + TM_Y, a, bl, IDESC_Y, 1);
+                const uint64_t a = desc_add(a0, ks * 2048);
+                mma_bf16(tmem + TM_Y, a, desc_add(dRD_hi, ks * 1024), IDESC_Y, ks > 0);
+                mma_bf16(tmem + TM_Y, a, desc_add(dRD_lo, ks * 1024), IDESC_Y, 1);
             }
             mma_commit(x.bar(B_MMA_CHAIN));
         }
@@ -608,14 +621,14 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
         // chunk c's tiles are no longer read: fetch chunk c+2 into them
         if (tid == 0 && c + 2 < nchunks) {
             fence_proxy_async_smem();
-            issue_chunk_loads(x, buf, (int)(c0 + 2 * C), hq, h, cb, tmK, tmQ, tmV);
+            issue_chunk_loads(x, buf, (int)(c0 + 2 * C), hq, h, tmK, tmQ, tmV);
         }
         {
-            float y[32];
-            tmem_ld32(lb + TM_Y + 32 * hc, y);
+            float y[16];
+            tmem_ld16(lb + TM_Y + 16 * hc, y);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) Sr[j] = fmaf(eGC, Sr[j], y[j]);
-            store_half_hilo(x.sm + OFF_S_HI, x.sm + OFF_S_LO, row, hc, Sr);
+            for (int j = 0; j < 16; ++j) Sr[j] = fmaf(eGC, Sr[j], y[j]);
+            store_quarter_hilo64(x.sm + OFF_S_HI, x.sm + OFF_S_LO, row, hc, Sr);
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
@@ -636,16 +649,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     x.rank = cluster_rank();
-    x.peer_base = map_to_rank(x.sbase, x.rank ^ 1u);
-    const int cb = (int)x.rank;
-    const int h = (blockIdx.x >> 1) % p.h_v;
-    const int s = (blockIdx.x >> 1) / p.h_v;
+    const int h = (blockIdx.x / NCL) % p.h_v;
+    const int s = (blockIdx.x / NCL) / p.h_v;
     const int hq = h / (p.h_v / p.h_qk);
     const int64_t t0 = p.cu_seqlens[s], t1 = p.cu_seqlens[s + 1];
     const int nchunks = (int)((t1 - t0 + C - 1) / C);
 
     if (tid == 0) {
-        for (int i = 0; i < NBARS; ++i) mbar_init(x.bar(i), i == B_ATP_FREE ? 2 : 1);
+        for (int i = 0; i < NBARS; ++i) mbar_init(x.bar(i), i == B_ATP_FREE ? NCL : 1);
         x.abort_flag[0] = 0;
         x.abort_flag[1] = 0;
         fence_mbar_init();
@@ -654,42 +665,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_alloc(smem_u32(tmem_holder), TM_COLS);
         tmem_relinquish();
     }
-    // chain thread: row `srow` (a d_k index), columns [32 hc, 32 hc + 32) of the CTA's block
+    // chain thread: row `srow` (a d_k index), columns [16 hc, 16 hc + 16) of the CTA's block
     const int srow = ((warp & 3) << 5) + lane, hc = (warp >> 2) & 1;
-    float Sr[32];
-    float *Sg = p.state + (((size_t)s * p.h_v + h) * D + srow) * D + cb * BV + 32 * hc;
+    float Sr[16];
+    float *Sg = p.state + (((size_t)s * p.h_v + h) * D + srow) * D + x.rank * BV + 16 * hc;
     if (tid < NCHAIN) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
+        for (int j = 0; j < 16; j += 4) {
             const float4 v = *reinterpret_cast<const float4 *>(Sg + j);
             Sr[j] = v.x;
             Sr[j + 1] = v.y;
             Sr[j + 2] = v.z;
             Sr[j + 3] = v.w;
         }
-        store_half_hilo(x.sm + OFF_S_HI, x.sm + OFF_S_LO, srow, hc, Sr);
+        store_quarter_hilo64(x.sm + OFF_S_HI, x.sm + OFF_S_LO, srow, hc, Sr);
         fence_proxy_async_smem();
     }
     tc_fence_before_sync();
-    cluster_sync();  // both CTAs' barriers are initialised before any remote arrive
+    cluster_sync();  // every CTA's barriers are initialised before any remote arrive
     tc_fence_after_sync();
     x.tmem = *tmem_holder;
 
     if (tid == 0) {
-        if (nchunks > 0) issue_chunk_loads(x, 0, (int)t0, hq, h, cb, &tmK, &tmQ, &tmV);
-        if (nchunks > 1) issue_chunk_loads(x, 1, (int)(t0 + C), hq, h, cb, &tmK, &tmQ, &tmV);
+        if (nchunks > 0) issue_chunk_loads(x, 0, (int)t0, hq, h, &tmK, &tmQ, &tmV);
+        if (nchunks > 1) issue_chunk_loads(x, 1, (int)(t0 + C), hq, h, &tmK, &tmQ, &tmV);
     }
 
     bool ok = true;
     if (tid < NCHAIN)
-        chain_role(x, p, t0, t1, nchunks, h, hq, cb, Sr, &tmK, &tmQ, &tmV, tid, ok);
+        chain_role(x, p, t0, t1, nchunks, h, hq, Sr, &tmK, &tmQ, &tmV, tid, ok);
     else
         stage1_role(x, p, t0, t1, nchunks, h, hq, &tmK, &tmQ, tid);
 
     if (tid < NCHAIN) {
         if (ok) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
+            for (int j = 0; j < 16; j += 4)
                 *reinterpret_cast<float4 *>(Sg + j) = make_float4(Sr[j], Sr[j + 1], Sr[j + 2], Sr[j + 3]);
         } else if (tid == 0) {
             // let any outstanding tile load land before the CTA's shared memory is released
@@ -700,7 +711,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     }
     tc_fence_before_sync();
-    cluster_sync();  // no CTA leaves while its peer may still write into its shared memory
+    cluster_sync();  // no CTA leaves while a peer may still write into its shared memory
     if (warp == 0) {
         tc_fence_after_sync();
         tmem_dealloc(x.tmem, TM_COLS);
@@ -720,16 +731,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// bf16 tensor [d2][d1][d0] (d0 contiguous), box {64, 1, 64}, 128-byte swizzle.
-bool encode_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2) {
+// bf16 tensor [d2][d1][d0] (d0 contiguous), box {box0, 1, 64}.
+bool encode_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
+                    CUtensorMapSwizzle swizzle) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[3] = {d0, d1, d2};
     cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
-    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t box[3] = {box0, 1, 64};
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -738,9 +750,9 @@ bool encode_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, 
 cudaError_t launch_prefill_tc(const Args &a, cudaStream_t s) {
     if (a.n_seqs == 0 || a.t_total == 0) return cudaSuccess;  // every sequence empty: state unchanged
     CUtensorMap tmK, tmQ, tmV;
-    if (!encode_bf16_3d(&tmK, a.k, D, (uint64_t)a.h_qk, (uint64_t)a.t_total) ||
-        !encode_bf16_3d(&tmQ, a.q, D, (uint64_t)a.h_qk, (uint64_t)a.t_total) ||
-        !encode_bf16_3d(&tmV, a.v, D, (uint64_t)a.h_v, (uint64_t)a.t_total))
+    if (!encode_bf16_3d(&tmK, a.k, D, (uint64_t)a.h_qk, (uint64_t)a.t_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_bf16_3d(&tmQ, a.q, D, (uint64_t)a.h_qk, (uint64_t)a.t_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_bf16_3d(&tmV, a.v, D, (uint64_t)a.h_v, (uint64_t)a.t_total, BV, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     static int configured_device = -1;
     int dev = 0;
@@ -762,13 +774,13 @@ cudaError_t launch_prefill_tc(const Args &a, cudaStream_t s) {
     p.state = a.state;
     p.o = a.o;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.n_seqs * (unsigned)a.h_v * (unsigned)(D / BV));
+    cfg.gridDim = dim3((unsigned)a.n_seqs * (unsigned)a.h_v * (unsigned)NCL);
     cfg.blockDim = dim3(NTHREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;  // the two column blocks of one V head
+    attr[0].val.clusterDim.x = NCL;  // the four column blocks of one V head
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;

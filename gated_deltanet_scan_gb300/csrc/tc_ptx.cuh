@@ -142,18 +142,23 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 }
 
 // ---- descriptors ----------------------------------------------------------------------
-// Shared-memory matrix descriptor, 128-byte swizzle (tiles 1024-byte aligned).
-// K-major: rows of 64 bf16 (128 B), 8-row groups SBO bytes apart, LBO unused.
-// MN-major: each 128-B row holds 64 consecutive M/N elements of one k; 8-row
-// groups along K are SBO apart, 64-element M/N blocks are LBO apart.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor for tcgen05 (tiles aligned to their swizzle atom).
+// K-major: rows of one swizzle width (128 or 64 B) along K, 8-row groups SBO
+// bytes apart, LBO unused.  MN-major: each row holds one k's consecutive M/N
+// elements; 8-row groups along K are SBO apart, M/N blocks of one row's width
+// are LBO apart.  Swizzle codes: 2 = 128-byte, 4 = 64-byte.
+constexpr uint32_t kSwizzle128 = 2, kSwizzle64 = 4;
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
     uint64_t d = 0;
     d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
     d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
     d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
-    d |= (uint64_t)2 << 61;  // SWIZZLE_128B
+    d |= (uint64_t)swizzle << 61;
     return d;
+}
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return smem_desc(addr, lbo, sbo, kSwizzle128);
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
@@ -204,6 +209,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive columns of this thread's lane (waits for completion).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+        " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // ---- bf16 hi/lo split into a 128-byte-swizzled row ------------------------------------
 // Writes 8 values x[0..7] as one 16-byte chunk of their high bf16 parts and one
 // of the residuals, at the swizzled position of chunk `chunk` of row `row`.
@@ -213,6 +233,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 }
 __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
     return (uint32_t)(row * 128 + (((chunk ^ (row & 7)) & 7) << 4));
+}
+// 64-byte rows (four 16-byte chunks), 64-byte swizzle: chunk ^= (row / 2) % 4.
+__device__ __forceinline__ uint32_t sw64_offset(int row, int chunk) {
+    return (uint32_t)(row * 64 + (((chunk ^ (row >> 1)) & 3) << 4));
 }
 // hi: x with its low 16 bits dropped (exactly the top half of the fp32 word);
 // lo: the exact remainder x - hi, rounded to bf16.  |lo| < 2^-7 |x|, so
@@ -240,6 +264,23 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+__device__ __forceinline__ void store_hilo_chunk64(uint8_t *hi_base, uint8_t *lo_base, int row, int chunk,
+                                                   const float *x) {
+    uint32_t h[4], l[4];
+    hilo_words(x, h, l);
+    const uint32_t off = sw64_offset(row, chunk);
+    *reinterpret_cast<uint4 *>(hi_base + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4 *>(lo_base + off) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+__device__ __forceinline__ void load_bf16_chunk64(const uint8_t *base, int row, int chunk, float *x) {
+    const uint4 v = *reinterpret_cast<const uint4 *>(base + sw64_offset(row, chunk));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
 }
 // Reads 8 bf16 values of chunk `c` of a swizzled row as floats.
 __device__ __forceinline__ void load_bf16_chunk(const uint8_t *base, int row, int chunk, float *x) {
