@@ -15,7 +15,7 @@ from typing import Optional
 
 __all__ = [
     "GdrError", "gdr_dims", "lib", "library_path",
-    "gdr_prefill_chunked", "gdr_decode_step", "gdr_verify_block",
+    "gdr_prefill_chunked", "gdr_prefill_workspace_bytes", "gdr_decode_step", "gdr_verify_block",
     "gdr_state_snapshot", "gdr_state_restore", "gdr_device_error", "gdr_status_string",
     "GDR_F32", "GDR_BF16",
 ]
@@ -51,8 +51,10 @@ _P = ctypes.c_void_p
 _SIGS = {
     "gdr_abi_version": ([], ctypes.c_int32),
     "gdr_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "gdr_prefill_workspace_bytes": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, ctypes.c_int64],
+                                    ctypes.c_size_t),
     "gdr_prefill_chunked": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, ctypes.c_int64,
-                             _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+                             _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "gdr_decode_step": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P],
                         ctypes.c_int),
     "gdr_verify_block": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, ctypes.c_int32,
@@ -134,19 +136,34 @@ def make_dims(q, v, o, chunk: int = 64, scale: float = 1.0) -> gdr_dims:
                     scale=float(scale))
 
 
+def gdr_prefill_workspace_bytes(q, v, o, n_seqs: int, t_total: int, *, chunk: int = 64,
+                                scale: float = 1.0) -> int:
+    """Device scratch bytes gdr_prefill_chunked needs (0 on the CUDA-core path)."""
+    dims = make_dims(q, v, o, chunk, scale)
+    return int(lib().gdr_prefill_workspace_bytes(ctypes.byref(dims), int(n_seqs), int(t_total)))
+
+
 def gdr_prefill_chunked(q, k, v, g, beta, state, o, cu_seqlens, *, chunk: int = 64,
-                        scale: float = 1.0, t_total: Optional[int] = None, stream=None) -> None:
+                        scale: float = 1.0, t_total: Optional[int] = None, workspace=None,
+                        stream=None) -> None:
     """Chunked prefill over packed sequences (see gdr_prefill_chunked in include/gdr.h).
 
     q, k [T, H_qk, d_k]; v [T, H_v, d_v]; g, beta [T, H_v] fp32;
     state [n, H_v, d_k, d_v] fp32 (in/out); o [T, H_v, d_v]; cu_seqlens int32 [n+1]
-    on the device.  ``t_total`` defaults to q.shape[0]."""
+    on the device.  ``t_total`` defaults to q.shape[0].  ``workspace`` is a
+    device tensor of at least gdr_prefill_workspace_bytes(...) bytes; when it is
+    None, one is taken from torch's caching allocator for this call."""
     dims = make_dims(q, v, o, chunk, scale)
     n = cu_seqlens.shape[0] - 1
     T = q.shape[0] if t_total is None else int(t_total)
+    need = int(lib().gdr_prefill_workspace_bytes(ctypes.byref(dims), n, T))
+    if workspace is None and need > 0:
+        workspace = _torch().empty(need, dtype=_torch().uint8, device=q.device)
+    ws_ptr = _ptr(workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = lib().gdr_prefill_chunked(
         ctypes.byref(dims), n, _ptr(cu_seqlens), T, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
-        _ptr(beta), _ptr(state), _ptr(o), _stream_handle(stream, q.device))
+        _ptr(beta), _ptr(state), _ptr(o), ws_ptr, ws_bytes, _stream_handle(stream, q.device))
     _check(st, "gdr_prefill_chunked")
 
 

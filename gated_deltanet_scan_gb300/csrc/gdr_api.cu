@@ -1,6 +1,7 @@
 // C-ABI entry points: argument checks on the host, then one launch each.
 #include <cuda_runtime.h>
 
+#include "gdr_factor_layout.h"
 #include "gdr_internal.h"
 
 namespace gdr {
@@ -71,10 +72,16 @@ const char *gdr_status_string(gdr_status st) {
     return "unknown gdr_status";
 }
 
+size_t gdr_prefill_workspace_bytes(const gdr_dims *dims, int32_t n_seqs, int64_t t_total) {
+    if (check_dims(dims) != GDR_OK || n_seqs <= 0 || t_total <= 0 || !use_tensor_core_prefill(dims)) return 0;
+    const size_t bytes = (size_t)fac::n_slots(t_total, n_seqs) * (size_t)dims->h_v * fac::SLOT_BYTES;
+    return (bytes + 255) & ~(size_t)255;
+}
+
 gdr_status gdr_prefill_chunked(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens,
                                int64_t t_total, const void *q, const void *k, const void *v,
                                const float *g, const float *beta, float *state, void *o,
-                               gdr_stream_t stream) {
+                               void *workspace, size_t workspace_bytes, gdr_stream_t stream) {
     gdr_status st = check_dims(dims);
     if (st != GDR_OK) return st;
     if (n_seqs < 0 || t_total < 0) return GDR_ERR_INVALID_ARG;
@@ -82,6 +89,8 @@ gdr_status gdr_prefill_chunked(const gdr_dims *dims, int32_t n_seqs, const int32
     if (!cu_seqlens || !aligned16(cu_seqlens) || !state || !aligned16(state)) return GDR_ERR_INVALID_ARG;
     if (t_total > 0 && !tensors_ok(q, k, v, g, beta, state, o)) return GDR_ERR_INVALID_ARG;
     if (t_total > ((int64_t)1 << 31) - 1) return GDR_ERR_UNSUPPORTED;
+    const size_t need = gdr_prefill_workspace_bytes(dims, n_seqs, t_total);
+    if (need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need)) return GDR_ERR_INVALID_ARG;
     Args a = make_args(dims);
     a.n_seqs = n_seqs;
     a.cu_seqlens = cu_seqlens;
@@ -96,7 +105,15 @@ gdr_status gdr_prefill_chunked(const gdr_dims *dims, int32_t n_seqs, const int32
     a.snapshot = nullptr;
     a.o = o;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (use_tensor_core_prefill(dims)) return from_cuda(launch_prefill_tc(a, s));
+    if (t_total == 0) return GDR_OK;  // every sequence empty: states unchanged
+    if (use_tensor_core_prefill(dims)) {
+        int32_t *err = device_error_word();
+        if (!err) return GDR_ERR_CUDA;
+        float *ws = static_cast<float *>(workspace);
+        cudaError_t e = launch_factors(a, ws, err, s);
+        if (e != cudaSuccess) return GDR_ERR_CUDA;
+        return from_cuda(launch_prefill_tc(a, ws, s));
+    }
     return from_cuda(launch_chunk_cc(a, s));
 }
 

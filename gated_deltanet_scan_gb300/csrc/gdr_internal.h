@@ -1,6 +1,7 @@
 // Internal launch interface shared by the C-ABI layer and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -26,8 +27,18 @@ struct Args {
 
 cudaError_t launch_decode(const Args &a, cudaStream_t s);
 cudaError_t launch_chunk_cc(const Args &a, cudaStream_t s);
-cudaError_t launch_prefill_tc(const Args &a, cudaStream_t s);
+// Tensor-core prefill in two launches: the per-chunk factors of every chunk
+// into `ws` (fac::n_slots(t_total, n_seqs) * h_v slots), then the chunk scan.
+cudaError_t launch_factors(const Args &a, float *ws, int32_t *err, cudaStream_t s);
+cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s);
 cudaError_t launch_copy_f32(const float *src, float *dst, size_t n, cudaStream_t s);
+
+// bf16 tensor [d2][d1][d0] (d0 contiguous) as a TMA map with box {box0, 1, 64}.
+bool encode_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
+                    CUtensorMapSwizzle swizzle);
+
+// Device address of the error word (nullptr if it cannot be resolved).
+int32_t *device_error_word();
 
 // Synchronises `s`, then reads and clears the device error word.
 cudaError_t read_clear_device_error(cudaStream_t s, int32_t *code);

@@ -1,48 +1,42 @@
-// Chunked prefill on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+// Chunk scan of the chunked prefill on the 5th-generation tensor cores
+// (tcgen05 + TMEM + TMA): carries the state from chunk to chunk, using the
+// state-independent factors (gates, T, P T) that the factor kernel stored for
+// every chunk beforehand.
 //
 // Shapes: d_k = d_v = 128, 64-token chunks, bf16 q/k/v, fp32 state, fp32 or
-// bf16 output.  A cluster of four CTAs owns one (sequence, V head); CTA r of
-// the cluster owns state columns [32 r, 32 r + 32) and walks the sequence's
-// chunks in order, keeping its 128 x 32 block of the state on chip for the
-// whole sequence (fp32 in registers, bf16 hi/lo copies in shared memory as
-// MMA operands).
+// bf16 output.  Four CTAs share one (sequence, V head); CTA `cb` owns state
+// columns [32 cb, 32 cb + 32), keeps its 128 x 32 block of the state on chip
+// for the whole sequence (fp32 in registers, bf16 hi/lo copies in shared
+// memory as MMA operands) and walks the chunks in order.  Per chunk (the
+// chunkwise-parallel form of the Qwen3.5-9B NPU model card, "How it works"):
+//   MMA1  [K S; Q S] = [K; Q] S                      A = K/Q tile, B = [S_hi | S_lo]
+//   R     = diag(beta) (V - diag(e^G) K S)
+//   MMA2  [D; P D] = [T; PT] R                       A = [T; PT]_hi and _lo, B = [R_hi | R_lo]
+//   O     = scale (diag(e^G) Q S + P D)
+//   MMA3  Y = Kᵀ D~,  D~ = diag(exp(G_C - G)) D      A = Kᵀ, B = [D~_hi | D~_lo]
+//   S    <- exp(G_C) S + Y
+// A tcgen05 MMA of N <= 64 costs the same as one of N = 32 (about 50 cycles of
+// issue each), so each B operand carries its bf16 hi and lo halves side by side
+// (N = 64) and the partial products are summed when the accumulator is read:
+// every product that feeds the state keeps ~2^-16 relative precision with
+// 8 + 8 + 4 MMAs per chunk, issued by two threads in parallel.
 //
-// Per chunk (the chunkwise-parallel form of the Qwen3.5-9B NPU model card,
-// "How it works"; forward substitution for the unit triangular factor as in
-// the Candle PR's chunked scan; log-space masking from its overflow fix):
-//   G   = inclusive running sum of g over the chunk (padding rows: g = beta = 0)
-//   G1  [K Kᵀ; Q Kᵀ] = [K; Q] Kᵀ                         (M=128 MMA, exact bf16)
-//   N   = diag(beta) (K Kᵀ ⊙ exp(G_t - G_j))_{j<t},  P = (Q Kᵀ ⊙ exp(G_t - G_j))_{j<=t}
-//         (the exponent is only formed on the kept triangle, so it is <= 0)
-//   T   = (I + N)^-1   (16x16 forward substitution, then two block-doubling levels)
-//   MPT PT = P T                                          (M=64 MMA, hi/lo)
-//   MMA1 [K S; Q S] = [K; Q] S                            (S as bf16 hi + lo)
-//   R   = diag(beta) (V - diag(e^G) K S)
-//   MMA2 [D; P D] = [T; PT] R                             (hi/lo on both sides)
-//   O   = scale (diag(e^G) Q S + P D)
-//   MMA3 Y = Kᵀ D~,  D~ = diag(exp(G_C - G)) D            (D~ as hi + lo)
-//   S  <- exp(G_C) S + Y
-// which is D = (I + N)^-1 diag(beta)(V - diag(e^G) K S0), O = diag(e^G) Q S0 + P D,
-// S_C = e^{G_C} S0 + Kᵀ diag(e^{G_C - G}) D written as products on the tensor
-// cores.  The bf16 hi/lo split (x = hi + lo, both bf16) keeps every product
-// that feeds the state within ~2^-16 relative; K, Q and V are exact in bf16.
-//
-// Warp roles (512 threads).  Warps 0-7, the "chain", run the state-dependent
-// MMA1 -> MMA2 -> MMA3 sequence of chunk c; warp w owns TMEM lanes
-// 32 (w % 4) .. + 31 and state columns 16 (w / 4) .. + 15 of the CTA's 32.
-// Warps 8-15, "stage 1", prepare the state-independent factors.  The four
-// CTAs of a cluster take turns: CTA r prepares chunks r, r+4, r+8, ... (gates,
-// Gram MMA, N and P, triangular inverse, P T), stages [T; PT] and the gates
-// in one of two buffers, and bulk-copies them into the three peers' shared
-// memory, completing on each peer's mbarrier.  Chains signal a buffer free
-// to the CTA that fills it next.  Every mbarrier wait is bounded: on timeout
-// a thread records GDR_ERR_DEVICE_TIMEOUT in the device error word and its
-// role stops; the peers time out on their own waits, and every CTA meets the
-// final cluster barrier, frees its TMEM and returns.
+// Warp roles (384 threads).  Warps 0-7, the "chain": warp w owns TMEM lanes
+// 32 (w % 4) .. + 31 (state rows, or chunk rows: K/T rows in lanes 0-63, Q/PT
+// rows in lanes 64-127) and columns 16 (w / 4) .. + 15 of the CTA's 32.  Only
+// warps of lanes 0-63 sit on the chunk-to-chunk path between MMA1 and MMA3;
+// the others form the outputs meanwhile.  Warps 8-11, the "loader": one
+// thread issues the TMA loads (K, Q and V tiles three chunks deep, factor
+// slots two deep); all four unpack a chunk's packed fp32 [T; PT] into the
+// bf16 hi/lo operand tiles while the chain runs the chunk before.  Every
+// mbarrier wait is bounded; on timeout the thread records
+// GDR_ERR_DEVICE_TIMEOUT, raises the CTA's abort flag, and both roles leave
+// their loops together at their next role barrier.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include "gdr_common.cuh"
+#include "gdr_factor_layout.h"
 #include "gdr_internal.h"
 #include "tc_ptx.cuh"
 
@@ -56,81 +50,72 @@ using namespace tc;
 
 constexpr int C = 64;
 constexpr int D = 128;
-constexpr int NCL = 4;         // CTAs per cluster (column blocks of one V head)
-constexpr int BV = D / NCL;    // 32 state columns per CTA
-constexpr int NCHAIN = 256;    // warps 0-7
-constexpr int NS1 = 256;       // warps 8-15
-constexpr int NTHREADS = NCHAIN + NS1;
-constexpr int SROW = 68;  // fp32 scratch row stride in floats (bank-conflict-free float4 rows)
-constexpr int XROW = 33;  // level-2 partial product row stride
-constexpr uint32_t BAR_CHAIN = 1, BAR_S1 = 2;  // named barrier ids
-constexpr int ROLE_CHAIN = 0, ROLE_S1 = 1;
+constexpr int BV = 32;           // state columns per CTA
+constexpr int NCOL = D / BV;     // CTAs per (sequence, V head)
+constexpr int NCHAIN = 256;      // warps 0-7
+constexpr int NLOAD = 128;       // warps 8-11
+constexpr int NTHREADS = NCHAIN + NLOAD;
+constexpr int NKQ = 3;           // K/Q/V ring depth (chunks)
+constexpr int NF = 2;            // factor ring depth (chunks)
+constexpr uint32_t BAR_CHAIN = 1, BAR_LOW = 2, BAR_LOAD = 3;  // named barriers
+constexpr int NLOW = 128;        // chain threads of TMEM lanes 0-63 (warps 0, 1, 4, 5)
 
 // Shared memory map, bytes from a 1024-byte aligned base.
-constexpr uint32_t KQ_BYTES = 32768;  // [kb=0: K rows 0-63, Q rows 64-127][kb=1: same], 128-B rows
-constexpr uint32_t V_BYTES = 4096;    // V tile: 64 tokens x 32 columns, 64-B rows
-constexpr uint32_t OFF_KQ = 0;        // two ring buffers
-constexpr uint32_t OFF_V = 2 * KQ_BYTES;  // two ring buffers
-constexpr uint32_t ATP_BYTES = 32768;     // [T; PT] hi (16 KB) + lo (16 KB), K-major 128 x 64 bf16
-constexpr uint32_t OFF_ATP = OFF_V + 2 * V_BYTES;  // two buffers (chunk parity)
-constexpr uint32_t OFF_S_HI = OFF_ATP + 2 * ATP_BYTES;  // state block, MN-major 128 (k) x 32 (n), 64-B rows
-constexpr uint32_t OFF_S_LO = OFF_S_HI + 8192;
-constexpr uint32_t OFF_RD_HI = OFF_S_LO + 8192;  // R, then D~: MN-major 64 (k = token) x 32 (n)
-constexpr uint32_t OFF_RD_LO = OFF_RD_HI + 4096;
-constexpr uint32_t OFF_P_HI = OFF_RD_LO + 4096;  // P as K-major 64 x 64 bf16 (A of the PT MMA)
-constexpr uint32_t OFF_P_LO = OFF_P_HI + 8192;
-constexpr uint32_t SCR_MAT = 64 * SROW * 4;      // fp32 [64][SROW]
-// Stage 1's own K/Q tile for the Gram MMA; once that MMA has completed the
-// region holds the fp32 scratch N, T and X.
-constexpr uint32_t OFF_S1 = OFF_P_LO + 8192;
-constexpr uint32_t OFF_N = OFF_S1;
-constexpr uint32_t OFF_T = OFF_N + SCR_MAT;
-constexpr uint32_t OFF_X = OFF_T + SCR_MAT;  // partial products: [32][XROW] fp32
-constexpr uint32_t S1_BYTES = 40960;
-constexpr uint32_t OFF_SMALL = OFF_S1 + S1_BYTES;
-constexpr uint32_t SM_GATES = OFF_SMALL;         // float [2 buffers][3][64]: G log2(e), beta, e^G
-constexpr uint32_t SM_SCAN = OFF_SMALL + 1536;   // float[4]
-constexpr uint32_t SM_BARS = OFF_SMALL + 1600;   // 8 x uint64
-constexpr uint32_t SM_TMEM = OFF_SMALL + 1664;   // uint32
-constexpr uint32_t SM_ABORT = OFF_SMALL + 1672;  // int32[2], one per role
-constexpr uint32_t SM_GPRIV = OFF_SMALL + 2048;  // float[3][64]: stage 1's own copy of the gates
-constexpr uint32_t SMEM_USED = OFF_SMALL + 3072;
+constexpr uint32_t KQ_BYTES = 32768;  // [K rows 0-63; Q rows 64-127] x 2 K-halves, 128-B swizzled rows
+constexpr uint32_t V_BYTES = 64 * BV * 2;                 // 64 tokens x 32 columns, 64-B swizzled rows
+constexpr uint32_t OFF_KQ = 0;
+constexpr uint32_t OFF_V = OFF_KQ + NKQ * KQ_BYTES;
+constexpr uint32_t OFF_F = OFF_V + NKQ * V_BYTES;         // factor slots (fac::SLOT_BYTES each)
+constexpr uint32_t OFF_ATP = ((OFF_F + NF * fac::SLOT_BYTES + 1023) / 1024) * 1024;
+constexpr uint32_t OFF_ATP_LO = OFF_ATP + 16384;          // [T; PT] hi / lo, K-major 128 x 64 bf16
+constexpr uint32_t OFF_S = OFF_ATP + 32768;               // [S_hi | S_lo]: 128 (k) rows x 64 bf16, MN-major
+constexpr uint32_t OFF_R = OFF_S + 16384;                 // [R_hi | R_lo]: 64 (token) rows x 64 bf16
+constexpr uint32_t OFF_DT = OFF_R + 8192;                 // [D~_hi | D~_lo]: 64 rows x 64 bf16
+constexpr uint32_t OFF_SMALL = OFF_DT + 8192;
+constexpr uint32_t SM_BARS = OFF_SMALL;                   // NBARS x uint64
+constexpr uint32_t SM_TMEM = OFF_SMALL + 192;
+constexpr uint32_t SM_ABORT = OFF_SMALL + 200;
+constexpr uint32_t SMEM_USED = OFF_SMALL + 256;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(OFF_X + 32 * XROW * 4 <= OFF_S1 + S1_BYTES && KQ_BYTES <= S1_BYTES, "stage-1 region");
-static_assert(OFF_ATP % 1024 == 0 && OFF_S_HI % 1024 == 0 && OFF_RD_HI % 1024 == 0 && OFF_P_HI % 1024 == 0 &&
-                  OFF_S1 % 1024 == 0 && OFF_V % 1024 == 0,
-              "operand tiles must be 1 KB aligned");
+static_assert(OFF_V % 1024 == 0 && OFF_ATP % 1024 == 0 && OFF_S % 1024 == 0 && OFF_R % 1024 == 0 &&
+                  OFF_DT % 1024 == 0 && OFF_F % 16 == 0,
+              "operand tiles must be 1 KB aligned, bulk copies 16 B aligned");
 
 // mbarriers
-constexpr int B_TMA0 = 0, B_MMA_CHAIN = 2, B_MMA_S1 = 3, B_ATP_FULL0 = 4, B_ATP_FREE = 6, B_TMA_S1 = 7;
-constexpr int NBARS = 8;
+constexpr int B_KQ_FULL = 0;                // NKQ: K, Q, V tiles landed
+constexpr int B_KQ_EMPTY = B_KQ_FULL + NKQ; // NKQ: chain done with the tiles
+constexpr int B_F_FULL = B_KQ_EMPTY + NKQ;  // NF: factor slot landed
+constexpr int B_F_EMPTY = B_F_FULL + NF;    // NF: chain done with the slot (its gates)
+constexpr int B_ATP_FULL = B_F_EMPTY + NF;  // [T; PT] operand tiles unpacked
+constexpr int B_ATP_FREE = B_ATP_FULL + 1;  // MMA2 has read them
+// MMA1, MMA2, MMA3 each complete one phase of their own barrier per chunk, so a
+// warp that reaches a wait late can never see a later group's phase instead.
+constexpr int B_MMA1 = B_ATP_FREE + 1, B_MMA2 = B_MMA1 + 1, B_MMA3 = B_MMA2 + 1;
+constexpr int NBARS = B_MMA3 + 1;
+static_assert(NBARS * 8 <= 192, "barrier space");
 
-// TMEM columns (fp32 accumulators).
-constexpr uint32_t TM_G1 = 0;    // [K Kᵀ; Q Kᵀ]   128 x 64 (stage 1, lane = row)
-constexpr uint32_t TM_PT = 64;   // P T            64 x 64  (stage 1, M=64 layout)
-constexpr uint32_t TM_KS = 128;  // [K S; Q S]     128 x 32 (chain)
-constexpr uint32_t TM_DP = 160;  // [D; P D]       128 x 32 (chain)
-constexpr uint32_t TM_Y = 192;   // Kᵀ D~          128 x 32 (chain)
-constexpr uint32_t TM_COLS = 256;
+// TMEM columns (fp32 accumulators, lane = row).  Each holds [hi-part | lo-part]
+// products in columns [0, 32) and [32, 64).  Two threads issue each MMA group
+// (MMAs from one thread issue about one per 50 cycles), each into its own
+// accumulator; readers add the two.
+constexpr uint32_t TM_KS0 = 0, TM_KS1 = 64;   // [K S; Q S], k-steps 0-3 / 4-7
+constexpr uint32_t TM_A = 128, TM_B = 192;    // [T; PT]_hi R / [T; PT]_lo R
+constexpr uint32_t TM_Y0 = 256, TM_Y1 = 320;  // Kᵀ D~, token k-steps 0-1 / 2-3
+constexpr uint32_t TM_COLS = 512;
+constexpr int NISSUE = 2;  // MMA-issuing threads: tid 0 (warp 0) and tid 32 (warp 1)
 
-constexpr uint32_t TMA_BYTES = 2 * 16384 + V_BYTES;      // K + Q (two 64-column halves each) + V
-constexpr uint32_t GATE_BYTES = 192 * 4;
-constexpr uint32_t ATP_COPY_BYTES = ATP_BYTES + GATE_BYTES;
+constexpr uint32_t KQV_TX = 2 * 16384 + V_BYTES;
 constexpr long long kWaitLimit = 4000000000LL;  // SM clocks (about 2 s)
-constexpr float kLog2e = 1.4426950408889634f;
 
-constexpr uint32_t IDESC_G1 = idesc_bf16_f32(128, 64, 0, 0);  // A K-major, B K-major
-constexpr uint32_t IDESC_PT = idesc_bf16_f32(64, 64, 0, 1);   // A K-major (P), B MN-major (T)
-constexpr uint32_t IDESC_KS = idesc_bf16_f32(128, BV, 0, 1);  // A K-major, B MN-major
-constexpr uint32_t IDESC_DP = idesc_bf16_f32(128, BV, 0, 1);
-constexpr uint32_t IDESC_Y = idesc_bf16_f32(128, BV, 1, 1);   // A MN-major (Kᵀ), B MN-major
+constexpr uint32_t IDESC_N64 = idesc_bf16_f32(128, 64, 0, 1);  // A K-major, B MN-major
+constexpr uint32_t IDESC_Y = idesc_bf16_f32(128, 64, 1, 1);    // A MN-major (Kᵀ), B MN-major
 
 struct TcParams {
     int h_qk, h_v, out_bf16;
     float scale;
     const int32_t *cu_seqlens;
-    const float *g, *beta;
+    const float *ws;  // factor slots
     float *state;
     void *o;
 };
@@ -140,501 +125,340 @@ struct Ctx {
     uint32_t sbase;
     uint32_t tmem;
     volatile int *abort_flag;
-    uint32_t rank;  // rank in the cluster = column block
     __device__ uint32_t bar(int i) const { return sbase + SM_BARS + 8 * i; }
-    __device__ float *gates(int buf) const { return reinterpret_cast<float *>(sm + SM_GATES) + buf * 192; }
-    __device__ uint32_t atp_hi(int buf) const { return OFF_ATP + buf * ATP_BYTES; }
-    __device__ uint32_t atp_lo(int buf) const { return OFF_ATP + buf * ATP_BYTES + 16384; }
+    __device__ const float *fslot(int fb) const {
+        return reinterpret_cast<const float *>(sm + OFF_F + fb * fac::SLOT_BYTES);
+    }
 };
 
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
-__device__ __forceinline__ void role_sync(int role) {
-    if (role == ROLE_CHAIN)
-        named_sync(BAR_CHAIN, NCHAIN);
-    else
-        named_sync(BAR_S1, NS1);
+// Barrier among `count` threads that also ORs a predicate across them.
+__device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
 }
 
-// Bounded wait shared by all threads of one role.  A thread whose wait times
-// out records the error and raises its role's abort flag; the role barrier
-// that follows makes every thread of the role read the same flag, so the role
-// leaves its loop together and never strands a sibling at a later barrier.
-// Each role reads only its own flag.
-__device__ __forceinline__ bool role_wait(const Ctx &x, uint32_t bar, uint32_t parity, int role) {
-    if (!mbar_wait_bounded(bar, parity, kWaitLimit)) {
-        x.abort_flag[role] = 1;
-        atomicCAS(&g_device_error, 0, (int32_t)GDR_ERR_DEVICE_TIMEOUT);
+// Bounded wait that also gives up as soon as any thread of the CTA has raised
+// the abort flag.  Returns false on either.
+__device__ bool wait_or_abort(const Ctx &x, uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*x.abort_flag) return false;
+        if (clock64() - t0 > kWaitLimit) {
+            *x.abort_flag = 1;
+            atomicCAS(&g_device_error, 0, (int32_t)GDR_ERR_DEVICE_TIMEOUT);
+            return false;
+        }
     }
-    role_sync(role);
-    return x.abort_flag[role] == 0;
 }
 
-__device__ __forceinline__ void issue_chunk_loads(const Ctx &x, int buf, int tok, int hq, int h,
-                                                  const CUtensorMap *tmK, const CUtensorMap *tmQ,
-                                                  const CUtensorMap *tmV) {
-    const uint32_t bar = x.bar(B_TMA0 + buf);
-    mbar_arrive_expect_tx(bar, TMA_BYTES);
-    const uint32_t kq = x.sbase + OFF_KQ + buf * KQ_BYTES;
-    tma_load_3d(kq, tmK, bar, 0, hq, tok);
-    tma_load_3d(kq + 16384, tmK, bar, 64, hq, tok);
-    tma_load_3d(kq + 8192, tmQ, bar, 0, hq, tok);
-    tma_load_3d(kq + 16384 + 8192, tmQ, bar, 64, hq, tok);
-    tma_load_3d(x.sbase + OFF_V + buf * V_BYTES, tmV, bar, (int)x.rank * BV, h, tok);
+// Two 32-column TMEM loads of this thread's lane, one wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t a0, uint32_t a1, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+        " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+        " {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
+          "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]),
+          "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]),
+          "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]),
+          "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(a0), "r"(a1)
+        : "memory");
 }
 
-// Stage 1's copy of the chunk's K and Q (for the Gram MMA only).
-__device__ __forceinline__ void issue_s1_loads(const Ctx &x, int tok, int hq, const CUtensorMap *tmK,
-                                               const CUtensorMap *tmQ) {
-    const uint32_t bar = x.bar(B_TMA_S1);
-    mbar_arrive_expect_tx(bar, 2 * 16384);
-    const uint32_t kq = x.sbase + OFF_S1;
-    tma_load_3d(kq, tmK, bar, 0, hq, tok);
-    tma_load_3d(kq + 16384, tmK, bar, 64, hq, tok);
-    tma_load_3d(kq + 8192, tmQ, bar, 0, hq, tok);
-    tma_load_3d(kq + 16384 + 8192, tmQ, bar, 64, hq, tok);
-}
-
-// 32 values as chunks [4 half, 4 half + 4) of row `row` of a 128-B hi/lo tile pair.
-__device__ __forceinline__ void store_half_hilo(uint8_t *hi, uint8_t *lo, int row, int half, const float *x) {
+// This thread's 16 columns (group g = j0 / 16) of two accumulators, each holding
+// [hi-part | lo-part] of those columns in TMEM columns [32 g, 32 g + 32),
+// summed: two TMEM loads, one wait.
+__device__ __forceinline__ void acc_sum2(uint32_t lanebase, uint32_t c0, uint32_t c1, int j0, float *out) {
+    uint32_t r[64];
+    tmem_ld32x2(lanebase + c0 + 2 * j0, lanebase + c1 + 2 * j0, r);
 #pragma unroll
-    for (int ch = 0; ch < 4; ++ch) store_hilo_chunk(hi, lo, row, 4 * half + ch, x + 8 * ch);
+    for (int j = 0; j < 16; ++j)
+        out[j] = (__uint_as_float(r[j]) + __uint_as_float(r[16 + j])) +
+                 (__uint_as_float(r[32 + j]) + __uint_as_float(r[48 + j]));
 }
-// 16 values as chunks [2 half, 2 half + 2) of row `row` of a 64-B hi/lo tile pair.
-__device__ __forceinline__ void store_quarter_hilo64(uint8_t *hi, uint8_t *lo, int row, int half, const float *x) {
-    store_hilo_chunk64(hi, lo, row, 2 * half, x);
-    store_hilo_chunk64(hi, lo, row, 2 * half + 1, x + 8);
+
+// Columns j0 .. j0+15 of row `row` of an N = 64 MN-major B operand with
+// 128-byte rows: group g = j0 / 16 keeps the hi parts in 16-byte chunks 4g, 4g+1
+// and the lo parts in 4g+2, 4g+3 (so each accumulator row has a thread's hi and
+// lo partial products in 32 consecutive columns).
+__device__ __forceinline__ void store_hilo_row16(uint8_t *tile, int row, int j0, const float *x) {
+    const int g4 = (j0 >> 4) * 4;
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+        uint32_t h[4], l[4];
+        hilo_words(x + 8 * ch, h, l);
+        *reinterpret_cast<uint4 *>(tile + sw128_offset(row, g4 + ch)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4 *>(tile + sw128_offset(row, g4 + 2 + ch)) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+}
+
+__device__ __forceinline__ void issue_kq_loads(const Ctx &x, int kb, int tok, int hq, int h, int cb,
+                                               const CUtensorMap *tmK, const CUtensorMap *tmQ,
+                                               const CUtensorMap *tmV) {
+    const uint32_t bar = x.bar(B_KQ_FULL + kb);
+    mbar_arrive_expect_tx(bar, KQV_TX);
+    const uint32_t kq = x.sbase + OFF_KQ + kb * KQ_BYTES;
+    tma_load_3d(kq, tmK, bar, 0, hq, tok);
+    tma_load_3d(kq + 16384, tmK, bar, 64, hq, tok);
+    tma_load_3d(kq + 8192, tmQ, bar, 0, hq, tok);
+    tma_load_3d(kq + 16384 + 8192, tmQ, bar, 64, hq, tok);
+    tma_load_3d(x.sbase + OFF_V + kb * V_BYTES, tmV, bar, cb * BV, h, tok);
+}
+
+__device__ __forceinline__ void issue_factor_load(const Ctx &x, int fb, const float *src) {
+    const uint32_t bar = x.bar(B_F_FULL + fb);
+    mbar_arrive_expect_tx(bar, fac::SLOT_BYTES);
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            x.sbase + OFF_F + fb * fac::SLOT_BYTES),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"((uint32_t)fac::SLOT_BYTES), "r"(bar)
+        : "memory");
 }
 
 __device__ __forceinline__ uint32_t lane_base(uint32_t tmem, int warp) {
     return tmem + ((uint32_t)((warp & 3) * 32) << 16);
 }
 
-// ================================ stage 1 ===========================================
-// T = (I + N)^-1 for strictly lower N (fp32 scratch, row stride SROW);
-// s = stage-1 thread index (0..255).  Ends with a role barrier.
-__device__ void unit_lower_inverse(uint8_t *sm, int s) {
-    const float *N = reinterpret_cast<const float *>(sm + OFF_N);
-    float *T = reinterpret_cast<float *>(sm + OFF_T);
-    float *X = reinterpret_cast<float *>(sm + OFF_X);
-    if (s < 64) {
-        // 16 x 16 diagonal blocks by forward substitution, one column per thread
-        const int base = (s >> 4) * 16, jj = s & 15;
-        float col[16];
+// ================================ loader ============================================
+// One thread issues every TMA; all 128 unpack [T; PT] (packed fp32 triangles)
+// into the hi/lo K-major operand tiles.  Rows t and 63 - t of T (or of PT)
+// hold 9 chunks of 8 between them; two threads share each such pair, 5 and 4
+// chunks, so every thread does the same work.  Chunks right of a row's
+// diagonal chunk stay zero from the start.
+__device__ void loader_role(const Ctx &x, const TcParams &p, int64_t t0, int nchunks, int64_t slot0, int h,
+                            int hq, int cb, const CUtensorMap *tmK, const CUtensorMap *tmQ,
+                            const CUtensorMap *tmV, int lt) {
+    const float *fsrc = p.ws + ((size_t)slot0 * p.h_v + h) * fac::SLOT_FLOATS;
+    const size_t fstride = (size_t)p.h_v * fac::SLOT_FLOATS;
+    if (lt == 0) {
+        for (int c = 0; c < nchunks && c < NKQ; ++c) issue_kq_loads(x, c, (int)(t0 + c * C), hq, h, cb, tmK, tmQ, tmV);
+        for (int c = 0; c < nchunks && c < NF; ++c) issue_factor_load(x, c, fsrc + c * fstride);
+    }
+    const int pr = lt >> 1, hf = lt & 1;
+    const int ta = pr & 31, tb = 63 - ta, nch_a = (ta >> 3) + 1;
+    const int mat = pr < 32 ? fac::OFF_T : fac::OFF_PT, rbase = pr < 32 ? 0 : 64;
+    uint8_t *hi = x.sm + OFF_ATP, *lo = x.sm + OFF_ATP_LO;
+    for (int c = 0; c < nchunks; ++c) {
+        const int fb = c % NF;
+        bool bad = !wait_or_abort(x, x.bar(B_F_FULL + fb), (uint32_t)(c / NF) & 1u);
+        if (c > 0 && !bad) bad = !wait_or_abort(x, x.bar(B_ATP_FREE), (uint32_t)(c - 1) & 1u);
+        if (!bad) {
+            const float *f = x.fslot(fb) + mat;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float a0 = (r == jj) ? 1.f : 0.f, a1 = 0.f;
-#pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                if (m < r && m >= jj) {
-                    const float nv = N[(base + r) * SROW + base + m];
-                    if (m & 1)
-                        a1 = fmaf(-nv, col[m], a1);
-                    else
-                        a0 = fmaf(-nv, col[m], a0);
+            for (int i = 0; i < 5; ++i) {
+                const int k = 5 * hf + i;
+                if (k < 9) {
+                    const bool in_a = k < nch_a;
+                    const int t = in_a ? ta : tb, j = in_a ? k : k - nch_a;
+                    const float *src = f + fac::tri8_base(t) + 8 * j;
+                    const float4 u = *reinterpret_cast<const float4 *>(src);
+                    const float4 v = *reinterpret_cast<const float4 *>(src + 4);
+                    const float xv[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
+                    uint32_t hw[4], lw[4];
+                    hilo_words(xv, hw, lw);
+                    const uint32_t off = sw128_offset(rbase + t, j);
+                    *reinterpret_cast<uint4 *>(hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4 *>(lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 }
             }
-            col[r] = a0 + a1;
+            fence_proxy_async_smem();
         }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) T[(base + r) * SROW + base + jj] = col[r];
-    } else {
-        // everything above the 16-block diagonal is zero
-        for (int e = s - 64; e < 6 * 256; e += NS1 - 64) {
-            const int b = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-            const int I = b < 3 ? 0 : (b < 5 ? 1 : 2);
-            const int J = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
-            T[(16 * I + r) * SROW + 16 * J + cc] = 0.f;
-        }
-    }
-    named_sync(BAR_S1, NS1);
-    // level 1: T_{I,I-1} = -T_II (N_{I,I-1} T_{I-1,I-1}) for I = 1, 3; two entries per thread
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int e = s + NS1 * k, blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-        const int I = 2 * blk + 1, J = I - 1;
-        const float *nr = N + (16 * I + r) * SROW + 16 * J;
-        const float *tc = T + (16 * J) * SROW + 16 * J + cc;
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; m += 2) {
-            a0 = fmaf(nr[m], tc[m * SROW], a0);
-            a1 = fmaf(nr[m + 1], tc[(m + 1) * SROW], a1);
-        }
-        X[(16 * blk + r) * XROW + cc] = a0 + a1;
-    }
-    named_sync(BAR_S1, NS1);
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int e = s + NS1 * k, blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-        const int I = 2 * blk + 1;
-        const float *tr = T + (16 * I + r) * SROW + 16 * I;
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; m += 2) {
-            a0 = fmaf(tr[m], X[(16 * blk + m) * XROW + cc], a0);
-            a1 = fmaf(tr[m + 1], X[(16 * blk + m + 1) * XROW + cc], a1);
-        }
-        T[(16 * I + r) * SROW + 16 * (I - 1) + cc] = -(a0 + a1);
-    }
-    named_sync(BAR_S1, NS1);
-    // level 2: T[32:64, 0:32] = -T[32:64, 32:64] (N[32:64, 0:32] T[0:32, 0:32]);
-    // each thread a 2 x 2 tile of the 32 x 32 block
-    const int r0 = (s >> 4) * 2, c0 = (s & 15) * 2;
-    {
-        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
-        const float *n0 = N + (32 + r0) * SROW, *n1 = n0 + SROW;
-#pragma unroll 8
-        for (int m = c0; m < 32; ++m) {  // T[0:32, 0:32] is lower: rows m >= c0 only
-            const float2 tv = *reinterpret_cast<const float2 *>(T + m * SROW + c0);
-            const float u0 = n0[m], u1 = n1[m];
-            a00 = fmaf(u0, tv.x, a00);
-            a01 = fmaf(u0, tv.y, a01);
-            a10 = fmaf(u1, tv.x, a10);
-            a11 = fmaf(u1, tv.y, a11);
-        }
-        X[r0 * XROW + c0] = a00;
-        X[r0 * XROW + c0 + 1] = a01;
-        X[(r0 + 1) * XROW + c0] = a10;
-        X[(r0 + 1) * XROW + c0 + 1] = a11;
-    }
-    named_sync(BAR_S1, NS1);
-    {
-        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
-        const float *t0 = T + (32 + r0) * SROW + 32, *t1 = t0 + SROW;
-#pragma unroll 8
-        for (int m = 0; m <= r0 + 1; ++m) {  // T[32:64, 32:64] is lower: columns m <= row
-            const float x0 = X[m * XROW + c0], x1 = X[m * XROW + c0 + 1];
-            const float u0 = t0[m], u1 = t1[m];
-            a00 = fmaf(u0, x0, a00);
-            a01 = fmaf(u0, x1, a01);
-            a10 = fmaf(u1, x0, a10);
-            a11 = fmaf(u1, x1, a11);
-        }
-        *reinterpret_cast<float2 *>(T + (32 + r0) * SROW + c0) = make_float2(-a00, -a01);
-        *reinterpret_cast<float2 *>(T + (33 + r0) * SROW + c0) = make_float2(-a10, -a11);
-    }
-    named_sync(BAR_S1, NS1);
-}
-
-__device__ void stage1_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t t1, int nchunks, int h, int hq,
-                            const CUtensorMap *tmK, const CUtensorMap *tmQ, const int tid) {
-    const int s = tid - NCHAIN;  // 0..255
-    const int warp = tid >> 5, lane = tid & 31;
-    const int half = (s >> 5) >> 2;  // column half of this warp's TMEM reads
-    const uint32_t tmem = x.tmem;
-    float *sScan = reinterpret_cast<float *>(x.sm + SM_SCAN);
-    float *gp = reinterpret_cast<float *>(x.sm + SM_GPRIV);
-    const int first = (int)x.rank;
-
-    // gates of this role's next chunk, loaded one turn ahead (threads s < 64)
-    float g_next = 0.f, b_next = 0.f;
-    if (s < C && first < nchunks && t0 + (int64_t)first * C + s < t1) {
-        g_next = p.g[(size_t)(t0 + (int64_t)first * C + s) * p.h_v + h];
-        b_next = p.beta[(size_t)(t0 + (int64_t)first * C + s) * p.h_v + h];
-    }
-    if (s == 0 && first < nchunks) issue_s1_loads(x, (int)(t0 + (int64_t)first * C), hq, tmK, tmQ);
-    int turn = 0;
-    for (int c = first; c < nchunks; c += NCL, ++turn) {
-        const int buf = c & 1;
-        const int64_t c0 = t0 + (int64_t)c * C;
-        float gt = g_next, bt = b_next;
-        if (s < C) {
-            g_next = b_next = 0.f;
-            if (c0 + NCL * C + s < t1) {
-                g_next = p.g[(size_t)(c0 + NCL * C + s) * p.h_v + h];
-                b_next = p.beta[(size_t)(c0 + NCL * C + s) * p.h_v + h];
-            }
-        }
-        // this turn's K and Q tile
-        if (!role_wait(x, x.bar(B_TMA_S1), (uint32_t)turn & 1u, ROLE_S1)) break;
-
-        // Gram products of the chunk: [K Kᵀ; Q Kᵀ] into TMEM
-        if (s == 0) {
-            tc_fence_after_sync();  // the previous turn's reads of these TMEM columns are done
-            const uint64_t a0 = smem_desc_sw128(x.sbase + OFF_S1, 16, 1024);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t a = desc_add(a0, (ks >> 2) * 16384 + (ks & 3) * 32);
-                mma_bf16(tmem + TM_G1, a, a, IDESC_G1, ks > 0);
-            }
-            mma_commit(x.bar(B_MMA_S1));
-        }
-        // gates: G = inclusive running sum of g, kept as G log2(e) so every decay is one
-        // ex2 (padding rows: g = 0, beta = 0)
-        gt *= kLog2e;
-        if (s < C) {
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float u = __shfl_up_sync(0xffffffffu, gt, o);
-                if (lane >= o) gt += u;
-            }
-            if (lane == 31) sScan[s >> 5] = gt;
-            gp[64 + s] = bt;
-        }
-        named_sync(BAR_S1, NS1);
-        if (s < C) {
-            if (s >= 32) gt += sScan[0];
-            gp[s] = gt;
-            gp[128 + s] = fast_exp2(gt);
-        }
-        if (!role_wait(x, x.bar(B_MMA_S1), 0u, ROLE_S1)) break;  // also publishes the gates
-        tc_fence_after_sync();
-        {
-            // row = lane quarter of this warp; columns [32 half, 32 half + 32)
-            const int row = ((warp & 3) << 5) + lane;
-            float a[32];
-            tmem_ld32(lane_base(tmem, warp) + TM_G1 + 32 * half, a);
-            const int t = row & 63;
-            const float Gt = gp[t];
-            const bool is_n = row < 64;
-            const float w = is_n ? gp[64 + t] : 1.f;
-            const int lim = is_n ? t : t + 1;  // keep j < t (N) or j <= t (P)
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                const float4 gj = *reinterpret_cast<const float4 *>(gp + 32 * half + j);
-                const float gv[4] = {gj.x, gj.y, gj.z, gj.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int jj = 32 * half + j + e;
-                    a[j + e] = (jj < lim) ? w * fast_exp2(Gt - gv[e]) * a[j + e] : 0.f;
+        named_sync(BAR_LOAD, NLOAD);
+        if (lt == 0 && !bad) {
+            mbar_arrive(x.bar(B_ATP_FULL));
+            // refill the ring slots the chain released with chunk c-1
+            if (c >= 1) {
+                const int kb = (c - 1) % NKQ, pf = (c - 1) % NF;
+                if (c - 1 + NKQ < nchunks) {
+                    bad = !wait_or_abort(x, x.bar(B_KQ_EMPTY + kb), (uint32_t)((c - 1) / NKQ) & 1u);
+                    if (!bad) issue_kq_loads(x, kb, (int)(t0 + (c - 1 + NKQ) * C), hq, h, cb, tmK, tmQ, tmV);
+                }
+                if (!bad && c - 1 + NF < nchunks) {
+                    bad = !wait_or_abort(x, x.bar(B_F_EMPTY + pf), (uint32_t)((c - 1) / NF) & 1u);
+                    if (!bad) issue_factor_load(x, pf, fsrc + (c - 1 + NF) * fstride);
                 }
             }
-            if (is_n) {
-                float *dst = reinterpret_cast<float *>(x.sm + OFF_N) + t * SROW + 32 * half;
-#pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4 *>(dst + j) = make_float4(a[j], a[j + 1], a[j + 2], a[j + 3]);
-            } else {
-                store_half_hilo(x.sm + OFF_P_HI, x.sm + OFF_P_LO, t, half, a);
-            }
         }
-        tc_fence_before_sync();
-        named_sync(BAR_S1, NS1);
-        unit_lower_inverse(x.sm, s);
-
-        // this parity's [T; PT] buffers are free once every chain finished MMA2 of chunk c-2
-        if (c >= 2 && !role_wait(x, x.bar(B_ATP_FREE), (uint32_t)((c - 2) >> 2) & 1u, ROLE_S1)) break;
-        {
-            // T rows as the top half of [T; PT] (also the B operand of the PT product), and the gates
-            const int row = s >> 2, cp = s & 3;
-            const float *src = reinterpret_cast<const float *>(x.sm + OFF_T) + row * SROW + 16 * cp;
-#pragma unroll
-            for (int ch = 0; ch < 2; ++ch) {
-                const float4 u = *reinterpret_cast<const float4 *>(src + 8 * ch);
-                const float4 v = *reinterpret_cast<const float4 *>(src + 8 * ch + 4);
-                const float xv[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
-                store_hilo_chunk(x.sm + x.atp_hi(buf), x.sm + x.atp_lo(buf), row, 2 * cp + ch, xv);
-            }
-            if (s < 192) x.gates(buf)[s] = gp[s];
-        }
-        fence_proxy_async_smem();
-        named_sync(BAR_S1, NS1);
-        // the scratch is spent: fetch the next turn's K and Q into it
-        if (s == 0 && c + NCL < nchunks) issue_s1_loads(x, (int)(c0 + NCL * C), hq, tmK, tmQ);
-        // PT = P T  (M = 64)
-        if (s == 0) {
-            tc_fence_after_sync();
-            const uint64_t ah0 = smem_desc_sw128(x.sbase + OFF_P_HI, 16, 1024);
-            const uint64_t al0 = smem_desc_sw128(x.sbase + OFF_P_LO, 16, 1024);
-            const uint64_t bh0 = smem_desc_sw128(x.sbase + x.atp_hi(buf), 16, 1024);
-            const uint64_t bl0 = smem_desc_sw128(x.sbase + x.atp_lo(buf), 16, 1024);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t ah = desc_add(ah0, ks * 32), al = desc_add(al0, ks * 32);
-                const uint64_t bh = desc_add(bh0, ks * 2048), bl = desc_add(bl0, ks * 2048);
-                mma_bf16(tmem + TM_PT, ah, bh, IDESC_PT, ks > 0);
-                mma_bf16(tmem + TM_PT, al, bh, IDESC_PT, 1);
-                mma_bf16(tmem + TM_PT, ah, bl, IDESC_PT, 1);
-            }
-            mma_commit(x.bar(B_MMA_S1));
-        }
-        if (!role_wait(x, x.bar(B_MMA_S1), 1u, ROLE_S1)) break;
-        tc_fence_after_sync();
-        {
-            // M = 64 accumulator: row i sits in lane 32 (i / 16) + i % 16
-            float a[32];
-            tmem_ld32(lane_base(tmem, warp) + TM_PT + 32 * half, a);
-            if (lane < 16)
-                store_half_hilo(x.sm + x.atp_hi(buf), x.sm + x.atp_lo(buf), 64 + 16 * (warp & 3) + lane, half, a);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        named_sync(BAR_S1, NS1);
-        if (s == 0) {
-            // local chain: [T; PT] and gates are in place; each peer: one bulk copy of both
-            mbar_arrive(x.bar(B_ATP_FULL0 + buf));
-            const uint32_t goff = SM_GATES + (uint32_t)buf * GATE_BYTES;
-#pragma unroll
-            for (uint32_t d = 1; d < NCL; ++d) {
-                const uint32_t peer = map_to_rank(x.sbase, (x.rank + d) % NCL);
-                const uint32_t full = peer + SM_BARS + 8 * (B_ATP_FULL0 + buf);
-                mbar_arrive_expect_tx_cluster(full, ATP_COPY_BYTES);
-                bulk_copy_to_peer(peer + x.atp_hi(buf), x.sbase + x.atp_hi(buf), ATP_BYTES, full);
-                bulk_copy_to_peer(peer + goff, x.sbase + goff, GATE_BYTES, full);
-            }
-        }
+        if (named_sync_or(BAR_LOAD, NLOAD, bad || *x.abort_flag)) break;
     }
 }
 
 // ================================= chain ============================================
-__device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t t1, int nchunks, int h, int hq,
-                           float *Sr, const CUtensorMap *tmK, const CUtensorMap *tmQ, const CUtensorMap *tmV,
-                           const int tid, bool &ok) {
+// MMAs of each group are split between two issuing threads (tid 0, tid 32),
+// each into its own accumulator and each committing to the group's barrier
+// (count 2).
+__device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t t1, int nchunks, int h,
+                           int cb, float *Sr, int tid, bool &ok) {
     const int warp = tid >> 5, lane = tid & 31;
-    const int hc = warp >> 2;                    // column half: columns [16 hc, 16 hc + 16) of the CTA's 32
-    const int row = ((warp & 3) << 5) + lane;  // TMEM lane = state row (d_k index) / chunk row
+    const int j0 = 16 * (warp >> 2);           // this thread's 16 columns of the CTA's 32
+    const int row = ((warp & 3) << 5) + lane;  // TMEM lane
+    const bool low = row < 64;                 // K / T rows (on the chunk-to-chunk path)
     const int t = row & 63;
+    const bool issuer = (tid & 31) == 0 && warp < NISSUE;
+    const int part = warp;                     // issuer 0 or 1
     const uint32_t lb = lane_base(x.tmem, warp);
     const uint32_t tmem = x.tmem;
-    const int cb = (int)x.rank;
-    // descriptor bases (start addresses advance per MMA)
-    const uint64_t dS_hi = smem_desc(x.sbase + OFF_S_HI, 8192, 512, kSwizzle64);
-    const uint64_t dS_lo = smem_desc(x.sbase + OFF_S_LO, 8192, 512, kSwizzle64);
-    const uint64_t dRD_hi = smem_desc(x.sbase + OFF_RD_HI, 4096, 512, kSwizzle64);
-    const uint64_t dRD_lo = smem_desc(x.sbase + OFF_RD_LO, 4096, 512, kSwizzle64);
-    uint32_t mma_phase = 0;
+    const uint64_t dS = smem_desc(x.sbase + OFF_S, 8192, 1024, kSwizzle128);
+    const uint64_t dR = smem_desc(x.sbase + OFF_R, 8192, 1024, kSwizzle128);
+    const uint64_t dDT = smem_desc(x.sbase + OFF_DT, 8192, 1024, kSwizzle128);
+    const uint64_t dA = smem_desc_sw128(x.sbase + (part == 0 ? OFF_ATP : OFF_ATP_LO), 16, 1024);
+    bool bad = false;
     for (int c = 0; c < nchunks; ++c) {
-        const int buf = c & 1;
+        const int kb = c % NKQ, fb = c % NF;
         const int64_t c0 = t0 + (int64_t)c * C;
         const int L = (int)((t1 - c0) < C ? (t1 - c0) : C);
-        const uint32_t kq = x.sbase + OFF_KQ + buf * KQ_BYTES;
-        if (!role_wait(x, x.bar(B_TMA0 + buf), (uint32_t)(c >> 1) & 1u, ROLE_CHAIN)) break;
-
-        // ---- MMA1: [K S; Q S] = [K; Q] (S_hi + S_lo) --------------------------------
-        if (tid == 0) {
+        const uint32_t kq = x.sbase + OFF_KQ + kb * KQ_BYTES;
+        bad = !wait_or_abort(x, x.bar(B_KQ_FULL + kb), (uint32_t)(c / NKQ) & 1u);
+        // ---- MMA1: [K S; Q S] = [K; Q] [S_hi | S_lo], k-steps 4 part .. 4 part + 3 --------
+        if (issuer && !bad) {
             tc_fence_after_sync();
             const uint64_t a0 = smem_desc_sw128(kq, 16, 1024);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t a = desc_add(a0, (ks >> 2) * 16384 + (ks & 3) * 32);
-                mma_bf16(tmem + TM_KS, a, desc_add(dS_hi, ks * 1024), IDESC_KS, ks > 0);
-                mma_bf16(tmem + TM_KS, a, desc_add(dS_lo, ks * 1024), IDESC_KS, 1);
+            for (int i = 0; i < 4; ++i) {
+                const int ks = 4 * part + i;
+                mma_bf16(tmem + (part ? TM_KS1 : TM_KS0), desc_add(a0, (ks >> 2) * 16384 + (ks & 3) * 32),
+                         desc_add(dS, ks * 2048), IDESC_N64, i > 0);
             }
-            mma_commit(x.bar(B_MMA_CHAIN));
+            mma_commit(x.bar(B_MMA1));
         }
-        // stage 1 of this chunk: gates and [T; PT]
-        if (!role_wait(x, x.bar(B_ATP_FULL0 + buf), (uint32_t)(c >> 1) & 1u, ROLE_CHAIN)) break;
-        const float *gts = x.gates(buf);
+        if (!bad) bad = !wait_or_abort(x, x.bar(B_F_FULL + fb), (uint32_t)(c / NF) & 1u);
+        const float *gts = x.fslot(fb) + fac::OFF_G;  // G log2(e), beta, exp(G)
         const float Gt = gts[t], bt = gts[64 + t], egt = gts[128 + t];
-        const float eGC = gts[128 + C - 1], GC = gts[C - 1];
-        if (!role_wait(x, x.bar(B_MMA_CHAIN), mma_phase, ROLE_CHAIN)) break;
-        mma_phase ^= 1;
+        const float GC = gts[C - 1], eGC = gts[128 + C - 1];
+        if (issuer && !bad) bad = !wait_or_abort(x, x.bar(B_ATP_FULL), (uint32_t)c & 1u);
+        const uint32_t par = (uint32_t)c & 1u;
+        if (!bad) bad = !wait_or_abort(x, x.bar(B_MMA1), par);
         tc_fence_after_sync();
-        float qse[16];  // rows 64-127: e^G Q S for this thread's columns, kept for the output
+        float qse[16];  // lanes 64-127: e^G Q S, kept for the output
         {
-            float a[16];
-            tmem_ld16(lb + TM_KS + 16 * hc, a);
-            if (row < 64) {
-                // R = beta (V - e^G K S), staged as the hi/lo MN-major B operand of MMA2
-                const uint8_t *vt = x.sm + OFF_V + buf * V_BYTES;
+            float ks[16];
+            if (!bad) acc_sum2(lb, TM_KS0, TM_KS1, j0, ks);
+            if (low) {
+                if (!bad) {
+                    // R = beta (V - e^G K S) as [R_hi | R_lo]
+                    const uint8_t *vt = x.sm + OFF_V + kb * V_BYTES;
+                    float r[16];
 #pragma unroll
-                for (int ch = 0; ch < 2; ++ch) {
-                    float v[8], r[8];
-                    load_bf16_chunk64(vt, t, 2 * hc + ch, v);
+                    for (int ch = 0; ch < 2; ++ch) {
+                        float v[8];
+                        load_bf16_chunk64(vt, t, (j0 >> 3) + ch, v);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) r[e] = bt * (v[e] - egt * a[ch * 8 + e]);
-                    store_hilo_chunk64(x.sm + OFF_RD_HI, x.sm + OFF_RD_LO, t, 2 * hc + ch, r);
+                        for (int e = 0; e < 8; ++e) r[8 * ch + e] = bt * (v[e] - egt * ks[8 * ch + e]);
+                    }
+                    store_hilo_row16(x.sm + OFF_R, t, j0, r);
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before_sync();
+                named_sync(BAR_LOW, NLOW);
+                // ---- MMA2: [D; P D] = [T; PT]_hi [R_hi | R_lo] (part 0) + [T; PT]_lo [R_hi | R_lo] (part 1)
+                if (issuer && !bad) {
+                    tc_fence_after_sync();
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        mma_bf16(tmem + (part ? TM_B : TM_A), desc_add(dA, ks * 32), desc_add(dR, ks * 2048),
+                                 IDESC_N64, ks > 0);
+                    mma_commit(x.bar(B_MMA2));
+                    mma_commit(x.bar(B_ATP_FREE));
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) qse[j] = egt * a[j];
+                for (int j = 0; j < 16; ++j) qse[j] = egt * ks[j];
             }
         }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        named_sync(BAR_CHAIN, NCHAIN);
-
-        // ---- MMA2: [D; P D] = [T; PT] R ---------------------------------------------
-        if (tid == 0) {
-            tc_fence_after_sync();
-            const uint64_t ah0 = smem_desc_sw128(x.sbase + x.atp_hi(buf), 16, 1024);
-            const uint64_t al0 = smem_desc_sw128(x.sbase + x.atp_lo(buf), 16, 1024);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t ah = desc_add(ah0, ks * 32), al = desc_add(al0, ks * 32);
-                const uint64_t bh = desc_add(dRD_hi, ks * 1024), bl = desc_add(dRD_lo, ks * 1024);
-                mma_bf16(tmem + TM_DP, ah, bh, IDESC_DP, ks > 0);
-                mma_bf16(tmem + TM_DP, al, bh, IDESC_DP, 1);
-                mma_bf16(tmem + TM_DP, ah, bl, IDESC_DP, 1);
-            }
-            mma_commit(x.bar(B_MMA_CHAIN));
-        }
-        if (!role_wait(x, x.bar(B_MMA_CHAIN), mma_phase, ROLE_CHAIN)) break;
-        mma_phase ^= 1;
+        if (!bad) bad = !wait_or_abort(x, x.bar(B_MMA2), par);
         tc_fence_after_sync();
-        if (tid == 0) {
-            // this parity's [T; PT] may be overwritten: tell the CTA that fills it next (chunk c+2)
-            mbar_arrive_cluster(map_to_rank(x.bar(B_ATP_FREE), (uint32_t)(c + 2) % NCL));
-        }
+        float ov[16];  // lanes 64-127: this chunk's outputs, stored after the chunk's last barrier
         {
-            float dd[16];
-            tmem_ld16(lb + TM_DP + 16 * hc, dd);
-            if (row < 64) {
-                // D~ = exp(G_C - G_t) D, staged as the hi/lo MN-major B operand of MMA3
-                const float sc = fast_exp2(GC - Gt);
+            float d[16];
+            if (!bad) acc_sum2(lb, TM_A, TM_B, j0, d);
+            if (low) {
+                if (!bad) {
+                    // D~ = exp(G_C - G_t) D as [D~_hi | D~_lo]
+                    const float sc = fast_exp2(GC - Gt);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) dd[j] *= sc;
-                store_quarter_hilo64(x.sm + OFF_RD_HI, x.sm + OFF_RD_LO, t, hc, dd);
-            } else if (t < L) {
-                // O = scale (e^G Q S + P D) for the chunk's real rows
-                const size_t off = ((size_t)(c0 + t) * p.h_v + h) * D + cb * BV + 16 * hc;
-                if (p.out_bf16) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + off);
-#pragma unroll
-                    for (int j = 0; j < 16; j += 8) {
-                        float y[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) y[e] = p.scale * (qse[j + e] + dd[j + e]);
-                        dst[j / 8] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                                                pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
-                    }
-                } else {
-                    float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + off);
-#pragma unroll
-                    for (int j = 0; j < 16; j += 4)
-                        dst[j / 4] = make_float4(p.scale * (qse[j] + dd[j]), p.scale * (qse[j + 1] + dd[j + 1]),
-                                                 p.scale * (qse[j + 2] + dd[j + 2]),
-                                                 p.scale * (qse[j + 3] + dd[j + 3]));
+                    for (int j = 0; j < 16; ++j) d[j] *= sc;
+                    store_hilo_row16(x.sm + OFF_DT, t, j0, d);
+                    fence_proxy_async_smem();
                 }
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        named_sync(BAR_CHAIN, NCHAIN);
-
-        // ---- MMA3: Y = Kᵀ (D~_hi + D~_lo) ---------------------------------------------
-        if (tid == 0) {
-            tc_fence_after_sync();
-            const uint64_t a0 = smem_desc_sw128(kq, 16384, 1024);
+                tc_fence_before_sync();
+                named_sync(BAR_LOW, NLOW);
+                // ---- MMA3: Y = Kᵀ [D~_hi | D~_lo], token k-steps 2 part, 2 part + 1 --------
+                if (issuer && !bad) {
+                    tc_fence_after_sync();
+                    const uint64_t a0 = smem_desc_sw128(kq, 16384, 1024);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t a = desc_add(a0, ks * 2048);
-                mma_bf16(tmem + TM_Y, a, desc_add(dRD_hi, ks * 1024), IDESC_Y, ks > 0);
-                mma_bf16(tmem + TM_Y, a, desc_add(dRD_lo, ks * 1024), IDESC_Y, 1);
+                    for (int i = 0; i < 2; ++i) {
+                        const int ks = 2 * part + i;
+                        mma_bf16(tmem + (part ? TM_Y1 : TM_Y0), desc_add(a0, ks * 2048), desc_add(dDT, ks * 2048),
+                                 IDESC_Y, i > 0);
+                    }
+                    mma_commit(x.bar(B_MMA3));
+                }
+            } else {
+                // O = scale (e^G Q S + P D)
+#pragma unroll
+                for (int j = 0; j < 16; ++j) ov[j] = p.scale * (qse[j] + d[j]);
             }
-            mma_commit(x.bar(B_MMA_CHAIN));
         }
-        if (!role_wait(x, x.bar(B_MMA_CHAIN), mma_phase, ROLE_CHAIN)) break;
-        mma_phase ^= 1;
+        if (!bad) bad = !wait_or_abort(x, x.bar(B_MMA3), par);
         tc_fence_after_sync();
-        // chunk c's tiles are no longer read: fetch chunk c+2 into them
-        if (tid == 0 && c + 2 < nchunks) {
-            fence_proxy_async_smem();
-            issue_chunk_loads(x, buf, (int)(c0 + 2 * C), hq, h, tmK, tmQ, tmV);
-        }
-        {
+        if (!bad) {
+            // S <- exp(G_C) S + Kᵀ D~, and its [S_hi | S_lo] operand copy
             float y[16];
-            tmem_ld16(lb + TM_Y + 16 * hc, y);
+            acc_sum2(lb, TM_Y0, TM_Y1, j0, y);
 #pragma unroll
             for (int j = 0; j < 16; ++j) Sr[j] = fmaf(eGC, Sr[j], y[j]);
-            store_quarter_hilo64(x.sm + OFF_S_HI, x.sm + OFF_S_LO, row, hc, Sr);
+            store_hilo_row16(x.sm + OFF_S, row, j0, Sr);
+            fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
         tc_fence_before_sync();
-        named_sync(BAR_CHAIN, NCHAIN);
+        const bool stop = named_sync_or(BAR_CHAIN, NCHAIN, bad || *x.abort_flag);
+        if (tid == 0 && !stop) {
+            mbar_arrive(x.bar(B_KQ_EMPTY + kb));
+            mbar_arrive(x.bar(B_F_EMPTY + fb));
+        }
+        if (stop) {
+            bad = true;
+            break;
+        }
+        // outputs of the chunk's real rows (after the barrier, so no proxy fence waits on them)
+        if (!low && t < L) {
+            const size_t off = ((size_t)(c0 + t) * p.h_v + h) * D + cb * BV + j0;
+            if (p.out_bf16) {
+                uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + off);
+#pragma unroll
+                for (int j = 0; j < 16; j += 8)
+                    dst[j / 8] = make_uint4(pack_bf16x2(ov[j], ov[j + 1]), pack_bf16x2(ov[j + 2], ov[j + 3]),
+                                            pack_bf16x2(ov[j + 4], ov[j + 5]), pack_bf16x2(ov[j + 6], ov[j + 7]));
+            } else {
+                float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + off);
+#pragma unroll
+                for (int j = 0; j < 16; j += 4) dst[j / 4] = make_float4(ov[j], ov[j + 1], ov[j + 2], ov[j + 3]);
+            }
+        }
     }
-    ok = (x.abort_flag[ROLE_CHAIN] == 0);
+    ok = !bad;
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -648,27 +472,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(x.sm + SM_TMEM);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    x.rank = cluster_rank();
-    const int h = (blockIdx.x / NCL) % p.h_v;
-    const int s = (blockIdx.x / NCL) / p.h_v;
+    const int cb = blockIdx.x % NCOL;
+    const int h = (blockIdx.x / NCOL) % p.h_v;
+    const int s = (blockIdx.x / NCOL) / p.h_v;
     const int hq = h / (p.h_v / p.h_qk);
     const int64_t t0 = p.cu_seqlens[s], t1 = p.cu_seqlens[s + 1];
+    if (t1 <= t0) return;  // empty sequence: the state stays as it is
     const int nchunks = (int)((t1 - t0 + C - 1) / C);
+    const int64_t slot0 = fac::slot_base(t0, s);
 
     if (tid == 0) {
-        for (int i = 0; i < NBARS; ++i) mbar_init(x.bar(i), i == B_ATP_FREE ? NCL : 1);
-        x.abort_flag[0] = 0;
-        x.abort_flag[1] = 0;
+        for (int i = 0; i < NBARS; ++i) mbar_init(x.bar(i), (i >= B_ATP_FREE) ? NISSUE : 1);
+        *x.abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_holder), TM_COLS);
         tmem_relinquish();
     }
-    // chain thread: row `srow` (a d_k index), columns [16 hc, 16 hc + 16) of the CTA's block
-    const int srow = ((warp & 3) << 5) + lane, hc = (warp >> 2) & 1;
+    // chain thread: state row `srow` (a d_k index), columns [j0, j0 + 16) of the CTA's block
+    const int srow = ((warp & 3) << 5) + lane, j0 = 16 * ((warp >> 2) & 1);
     float Sr[16];
-    float *Sg = p.state + (((size_t)s * p.h_v + h) * D + srow) * D + x.rank * BV + 16 * hc;
+    float *Sg = p.state + (((size_t)s * p.h_v + h) * D + srow) * D + cb * BV + j0;
     if (tid < NCHAIN) {
 #pragma unroll
         for (int j = 0; j < 16; j += 4) {
@@ -678,76 +503,55 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             Sr[j + 2] = v.z;
             Sr[j + 3] = v.w;
         }
-        store_quarter_hilo64(x.sm + OFF_S_HI, x.sm + OFF_S_LO, srow, hc, Sr);
+        store_hilo_row16(x.sm + OFF_S, srow, j0, Sr);
+        fence_proxy_async_smem();
+    } else {
+        // [T; PT] operand tiles: zero once (right of each row's diagonal chunk stays zero)
+        for (int i = tid - NCHAIN; i < 32768 / 16; i += NLOAD)
+            reinterpret_cast<uint4 *>(x.sm + OFF_ATP)[i] = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
     }
     tc_fence_before_sync();
-    cluster_sync();  // every CTA's barriers are initialised before any remote arrive
+    __syncthreads();
     tc_fence_after_sync();
     x.tmem = *tmem_holder;
 
-    if (tid == 0) {
-        if (nchunks > 0) issue_chunk_loads(x, 0, (int)t0, hq, h, &tmK, &tmQ, &tmV);
-        if (nchunks > 1) issue_chunk_loads(x, 1, (int)(t0 + C), hq, h, &tmK, &tmQ, &tmV);
-    }
-
     bool ok = true;
     if (tid < NCHAIN)
-        chain_role(x, p, t0, t1, nchunks, h, hq, Sr, &tmK, &tmQ, &tmV, tid, ok);
+        chain_role(x, p, t0, t1, nchunks, h, cb, Sr, tid, ok);
     else
-        stage1_role(x, p, t0, t1, nchunks, h, hq, &tmK, &tmQ, tid);
+        loader_role(x, p, t0, nchunks, slot0, h, hq, cb, &tmK, &tmQ, &tmV, tid - NCHAIN);
 
     if (tid < NCHAIN) {
-        if (ok) {
+        if (ok && *x.abort_flag == 0) {
 #pragma unroll
             for (int j = 0; j < 16; j += 4)
                 *reinterpret_cast<float4 *>(Sg + j) = make_float4(Sr[j], Sr[j + 1], Sr[j + 2], Sr[j + 3]);
-        } else if (tid == 0) {
-            // let any outstanding tile load land before the CTA's shared memory is released
-            for (int b = 0; b < 2; ++b) {
-                mbar_wait_bounded(x.bar(B_TMA0 + b), 0, kWaitLimit / 8);
-                mbar_wait_bounded(x.bar(B_TMA0 + b), 1, kWaitLimit / 8);
-            }
         }
     }
     tc_fence_before_sync();
-    cluster_sync();  // no CTA leaves while a peer may still write into its shared memory
+    __syncthreads();
+    if (*x.abort_flag && tid == NCHAIN) {
+        // let any tile or factor load still in flight land before the shared memory is released
+        for (int i = 0; i < NKQ; ++i) {
+            mbar_wait_bounded(x.bar(B_KQ_FULL + i), 0, kWaitLimit / 16);
+            mbar_wait_bounded(x.bar(B_KQ_FULL + i), 1, kWaitLimit / 16);
+        }
+        for (int i = 0; i < NF; ++i) {
+            mbar_wait_bounded(x.bar(B_F_FULL + i), 0, kWaitLimit / 16);
+            mbar_wait_bounded(x.bar(B_F_FULL + i), 1, kWaitLimit / 16);
+        }
+    }
+    __syncthreads();
     if (warp == 0) {
         tc_fence_after_sync();
         tmem_dealloc(x.tmem, TM_COLS);
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
-
-// bf16 tensor [d2][d1][d0] (d0 contiguous), box {box0, 1, 64}.
-bool encode_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
-                    CUtensorMapSwizzle swizzle) {
-    auto enc = tensor_map_encoder();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {d0, d1, d2};
-    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
-    cuuint32_t box[3] = {box0, 1, 64};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
-cudaError_t launch_prefill_tc(const Args &a, cudaStream_t s) {
+cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s) {
     if (a.n_seqs == 0 || a.t_total == 0) return cudaSuccess;  // every sequence empty: state unchanged
     CUtensorMap tmK, tmQ, tmV;
     if (!encode_bf16_3d(&tmK, a.k, D, (uint64_t)a.h_qk, (uint64_t)a.t_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -769,25 +573,18 @@ cudaError_t launch_prefill_tc(const Args &a, cudaStream_t s) {
     p.out_bf16 = a.out_bf16;
     p.scale = a.scale;
     p.cu_seqlens = a.cu_seqlens;
-    p.g = a.g;
-    p.beta = a.beta;
+    p.ws = ws;
     p.state = a.state;
     p.o = a.o;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.n_seqs * (unsigned)a.h_v * (unsigned)NCL);
-    cfg.blockDim = dim3(NTHREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = NCL;  // the four column blocks of one V head
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel, tmK, tmQ, tmV, p);
-    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)a.n_seqs * (unsigned)a.h_v * (unsigned)NCOL;
+    prefill_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, s>>>(tmK, tmQ, tmV, p);
     return cudaGetLastError();
+}
+
+int32_t *device_error_word() {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess) return nullptr;
+    return reinterpret_cast<int32_t *>(ptr);
 }
 
 cudaError_t read_clear_device_error(cudaStream_t s, int32_t *code) {

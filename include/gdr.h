@@ -16,7 +16,8 @@
  * Conventions for every entry point
  *   - Memory.  Every tensor pointer is a DEVICE pointer allocated by the caller;
  *     the library allocates nothing and keeps no pointer after the call returns.
- *     Pointers must be 16-byte aligned.
+ *     Pointers must be 16-byte aligned.  Scratch memory, where a path needs
+ *     it, is passed in by the caller (see gdr_prefill_workspace_bytes).
  *   - Layouts (row-major, token-major, sequences packed back to back):
  *         q, k   [T_total][H_qk][d_k]        in_dtype  (bf16 or fp32)
  *         v      [T_total][H_v][d_v]         in_dtype
@@ -37,8 +38,9 @@
  * Supported shapes: d_k == d_v in {32, 64, 128}; chunk in {16, 64}; any H_qk,
  * H_v with H_v % H_qk == 0.  The chunk is a tiling choice, not part of the
  * result: d_k = d_v = 128 with bf16 inputs and chunk 64 runs the tensor-core
- * (tcgen05) prefill; every other shape runs the CUDA-core chunk kernel with
- * 16-token chunks.
+ * (tcgen05) prefill, which needs a caller-provided workspace
+ * (gdr_prefill_workspace_bytes); every other shape runs the CUDA-core chunk
+ * kernel with 16-token chunks and needs none.
  */
 #ifndef GDR_H_
 #define GDR_H_
@@ -50,7 +52,7 @@
 extern "C" {
 #endif
 
-#define GDR_ABI_VERSION 1
+#define GDR_ABI_VERSION 2
 
 /* Same object as cudaStream_t; declared here so callers need no CUDA header. */
 typedef struct CUstream_st *gdr_stream_t;
@@ -83,6 +85,15 @@ int32_t gdr_abi_version(void);
 const char *gdr_status_string(gdr_status status);
 
 /*
+ * Bytes of device workspace gdr_prefill_chunked needs for this problem: 0 when
+ * the CUDA-core path runs (or for an empty problem), otherwise one
+ * 19,200-byte slot of per-chunk factors (T, P T and the gates of one chunk and
+ * V head) for each of ceil(t_total / 64) + n_seqs chunk positions and each V
+ * head, rounded up to 256 bytes.  Host-only, never fails (invalid dims: 0).
+ */
+size_t gdr_prefill_workspace_bytes(const gdr_dims *dims, int32_t n_seqs, int64_t t_total);
+
+/*
  * Chunked prefill over packed variable-length sequences.
  *
  * Computes, for every sequence s in [0, n_seqs) with tokens
@@ -99,20 +110,33 @@ const char *gdr_status_string(gdr_status status);
  * token_valid padding), which leaves the state as after the last real token;
  * padded rows are never written.
  *
+ * On the tensor-core path the call is two launches on `stream`: the
+ * state-independent factors of every chunk (gates, (I+N)^-1, P (I+N)^-1) into
+ * `workspace`, then the chunk-to-chunk scan that reads them.  The workspace
+ * holds nothing between calls.
+ *
  *   dims        shapes, dtypes, chunk, scale (host pointer, read during the call)
  *   n_seqs      number of sequences (>= 0; 0 is a no-op)
  *   cu_seqlens  DEVICE int32 [n_seqs + 1], non-decreasing, cu_seqlens[0] == 0,
  *               cu_seqlens[n_seqs] == t_total (empty sequences allowed: their
- *               state is left unchanged)
+ *               state is left unchanged).  Entries outside [0, t_total] make
+ *               the kernels skip those sequences and record
+ *               GDR_ERR_INVALID_ARG in the device error word.
  *   t_total     total tokens (host value, sizes the launch)
  *   q, k, v, g, beta   inputs (layouts above)
  *   state       in: S0 per sequence; out: state after the last token
  *   o           out: outputs of every token
+ *   workspace   DEVICE scratch of at least gdr_prefill_workspace_bytes(dims,
+ *               n_seqs, t_total) bytes, 16-byte aligned, owned by the caller,
+ *               not overlapping any other argument, not used by other work on
+ *               other streams until this call's work on `stream` is done.  May
+ *               be NULL when that size is 0.  Too small or misaligned:
+ *               GDR_ERR_INVALID_ARG before anything is launched.
  */
 gdr_status gdr_prefill_chunked(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens,
                                int64_t t_total, const void *q, const void *k, const void *v,
                                const float *g, const float *beta, float *state, void *o,
-                               gdr_stream_t stream);
+                               void *workspace, size_t workspace_bytes, gdr_stream_t stream);
 
 /*
  * One decode step for `batch` independent sequences (one token each).

@@ -58,9 +58,9 @@ def test_status_strings(L):
     assert L.gdr_status_string(99).decode() == "unknown gdr_status"
 
 
-def _prefill(L, d, n=1, cu=A, t=10, q=A, k=A, v=A, g=A, beta=A, state=A, o=B):
+def _prefill(L, d, n=1, cu=A, t=10, q=A, k=A, v=A, g=A, beta=A, state=A, o=B, ws=A, ws_bytes=1 << 40):
     return L.gdr_prefill_chunked(ctypes.byref(d) if d is not None else None, n, cu, t,
-                                 q, k, v, g, beta, state, o, None)
+                                 q, k, v, g, beta, state, o, ws, ws_bytes, None)
 
 
 @pytest.mark.parametrize("bad,code", [
@@ -87,6 +87,22 @@ def test_prefill_rejects_bad_pointers_and_counts(L):
     assert _prefill(L, d, t=-5) == gdr.GDR_ERR_INVALID_ARG
     assert _prefill(L, d, n=0, t=5) == gdr.GDR_ERR_INVALID_ARG
     assert _prefill(L, d, n=0, t=0) == gdr.GDR_OK  # nothing to do, nothing launched
+
+
+def test_prefill_workspace_size_and_checks(L):
+    d = dims()
+    # one 19,200-byte slot per (chunk position, V head); positions = ceil(T / 64) + n_seqs
+    need = L.gdr_prefill_workspace_bytes(ctypes.byref(d), 3, 1000)
+    slots = (1000 + 63) // 64 + 3
+    assert need == (slots * 32 * 19200 + 255) // 256 * 256
+    assert L.gdr_prefill_workspace_bytes(ctypes.byref(d), 0, 0) == 0
+    assert L.gdr_prefill_workspace_bytes(ctypes.byref(dims(in_dtype=gdr.GDR_F32)), 3, 1000) == 0
+    assert L.gdr_prefill_workspace_bytes(ctypes.byref(dims(chunk=16)), 3, 1000) == 0
+    assert L.gdr_prefill_workspace_bytes(None, 3, 1000) == 0
+    need10 = L.gdr_prefill_workspace_bytes(ctypes.byref(d), 1, 10)
+    assert _prefill(L, d, ws=None) == gdr.GDR_ERR_INVALID_ARG
+    assert _prefill(L, d, ws=MISALIGNED) == gdr.GDR_ERR_INVALID_ARG
+    assert _prefill(L, d, ws_bytes=need10 - 1) == gdr.GDR_ERR_INVALID_ARG
 
 
 def test_decode_and_verify_reject_bad_arguments(L):
