@@ -1,22 +1,28 @@
 // State-independent factors of the chunked prefill, computed for every chunk at
-// once (no chunk depends on another): one CTA per (chunk, QK head) writes, for
-// each V head that reads this QK head, the chunk's gates, T = (I + N)^-1 and
-// P T into the factor workspace (layout in gdr_factor_layout.h).
+// once (no chunk depends on another).  One CTA per (chunk, QK head) writes, for
+// each V head that reads the QK head, the chunk's gates, T = (I + N)^-1 and P T
+// into the factor workspace (layout in gdr_factor_layout.h).
 //
 // Per chunk (the chunkwise-parallel form of the Qwen3.5-9B NPU model card,
 // "How it works"; forward substitution for the unit triangular factor as in
 // the Candle PR's "Chunked GatedDeltaNet Scan"; log-space masking from its
 // "Float32 overflow fix"):
 //   G   = inclusive running sum of g over the chunk (padding rows: g = beta = 0)
-//   [K Kᵀ; Q Kᵀ] = [K; Q] Kᵀ                    one M=128 tcgen05 MMA group, exact
-//                                               bf16 products, fp32 accumulation
+//   [K Kᵀ; Q Kᵀ] = [K; Q] Kᵀ      one M=128 tcgen05 MMA group, exact bf16 products,
+//                                 fp32 accumulation in TMEM
 //   N   = diag(beta) (K Kᵀ ⊙ exp(G_t - G_j))_{j<t}
 //   P   =            (Q Kᵀ ⊙ exp(G_t - G_j))_{j<=t}
 //         (the exponent is formed only on the kept triangle, so it never overflows)
-//   T   = (I + N)^-1            fp32 on the CUDA cores: the four 16x16 diagonal
-//                               blocks by forward substitution, then two block-
-//                               doubling levels T21 = -T22 N21 T11 (16 -> 32 -> 64)
-//   P T                         fp32 on the CUDA cores, blockwise lower triangular
+//   T   = (I + N)^-1  blockwise forward substitution on 16 x 16 blocks:
+//         T_II = (I + N_II)^-1                    (CUDA cores, column by column)
+//         T_IJ = -T_II sum_{K=J}^{I-1} N_IK T_KJ  (I > J, by block diagonals)
+//   P T   (P T)_IJ = sum_{K=J}^{I} P_IK T_KJ
+// The block products run on warp-level bf16 tensor-core MMAs (m16n8k16) with
+// each fp32 operand split into bf16 hi + lo (x = hi + lo to ~2^-16) and three
+// products hi*hi + hi*lo + lo*hi accumulated in fp32.  Two warps share one V
+// head.  Off-diagonal blocks of T are formed transposed, T_IJᵀ = -X_IJᵀ T_IIᵀ,
+// so that X_IJᵀ comes straight out of one MMA's accumulators as the left
+// operand of the next.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -31,28 +37,41 @@ namespace {
 using namespace tc;
 
 constexpr int C = fac::C;
-constexpr int NT = 256;
-constexpr int SROW = 68;  // fp32 row stride of the 64 x 64 scratch matrices (floats)
-constexpr int XROW = 34;  // row stride of the block-doubling partial products
+constexpr int NT = 128;  // four warps: one TMEM lane quadrant each; two warps per V head
+constexpr int HP = 2;    // V heads per pass
 
-// Shared memory, bytes from a 1024-byte aligned base.  The [K; Q] tile is only
-// read by the Gram MMA; once that has completed, N and P overwrite it.
-constexpr uint32_t MAT_BYTES = 64 * SROW * 4;           // 17408
-constexpr uint32_t OFF_KQ = 0;                          // 32 KB, [K rows 0-63; Q rows 64-127] x 2 K-halves
-constexpr uint32_t OFF_N = 0;                           // N, later P T
-constexpr uint32_t OFF_P = MAT_BYTES;
-constexpr uint32_t OFF_T = 2 * MAT_BYTES;
-constexpr uint32_t OFF_X = 3 * MAT_BYTES;               // [32][XROW]
-constexpr uint32_t OFF_GATES = OFF_X + 32 * XROW * 4;   // G log2(e), beta, exp(G): 3 x 64 floats
-constexpr uint32_t OFF_SCAN = OFF_GATES + 768;
-constexpr uint32_t OFF_BARS = OFF_SCAN + 16;            // 2 mbarriers
+// A 16 x 16 block in shared memory as 16 rows of 8 pairs; pair p of row r holds
+// hi(x[r][2p]), hi(x[r][2p+1]) in one word and the matching lo parts in the
+// next.  Rows are 96 bytes apart, which keeps the 8-byte fragment loads of a
+// warp free of bank conflicts.
+constexpr int ROW_B = 96;
+constexpr int BLK_B = 16 * ROW_B;  // 1536
+__host__ __device__ constexpr int bi(int I, int J) { return I * (I + 1) / 2 + J; }  // lower block index, I >= J
+
+// Per-head scratch (bytes).  NB: the off-diagonal blocks of N (slots bi(I, J),
+// diagonal slots unused); ND: the four diagonal blocks of N in fp32; PB: the
+// ten lower blocks of P; TT: the blocks of Tᵀ on and above the diagonal, block
+// (J, K) in slot bi(K, J); TD: the four diagonal blocks of T, row-major (for
+// T_IIᵀ as a right operand).
+constexpr int OFF_NB = 0;
+constexpr int OFF_ND = OFF_NB + 10 * BLK_B;
+constexpr int OFF_PB = OFF_ND + 4 * 1024;
+constexpr int OFF_TT = OFF_PB + 10 * BLK_B;
+constexpr int OFF_TD = OFF_TT + 10 * BLK_B;
+constexpr int HEAD_B = OFF_TD + 4 * BLK_B;  // 56320
+
+// Shared memory, bytes from a 1024-byte aligned base.  The K/Q tile is only read
+// by the Gram MMA; once it has completed, the heads' scratch overwrites it.
+constexpr uint32_t OFF_KQ = 0;
+constexpr uint32_t OFF_GATES = HP * HEAD_B;               // HP x (G log2(e), beta, exp(G)) x 64 fp32
+constexpr uint32_t OFF_BARS = OFF_GATES + HP * 192 * 4;  // 2 mbarriers
 constexpr uint32_t OFF_TMEM = OFF_BARS + 16;
 constexpr uint32_t SMEM_USED = OFF_TMEM + 16;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
-static_assert(2 * MAT_BYTES >= 32768, "N and P cover the K/Q tile");
-static_assert(OFF_GATES % 16 == 0 && OFF_BARS % 8 == 0, "alignment");
+static_assert(32768 <= HP * HEAD_B, "K/Q tile fits under the scratch");
+static_assert(OFF_GATES % 16 == 0 && OFF_BARS % 8 == 0 && HEAD_B % 16 == 0, "alignment");
 
-constexpr uint32_t TM_COLS = 64;  // [K Kᵀ; Q Kᵀ], 128 lanes x 64 fp32 columns
+constexpr uint32_t TM_COLS = 64;  // the 128 x 64 fp32 Gram tile
 constexpr uint32_t IDESC_G1 = idesc_bf16_f32(128, 64, 0, 0);
 constexpr long long kWaitLimit = 4000000000LL;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -68,129 +87,210 @@ struct FacParams {
 
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
-// T = (I + N)^-1 for strictly lower N; both fp32 [64][SROW].  Entries of T above
-// the 16-block diagonal are left unwritten; everything on or below it is final.
-__device__ void unit_lower_inverse(const float *N, float *T, float *X, int tid) {
-    // diagonal 16 x 16 blocks: column jj of block I by right-looking substitution
-    if (tid < 64) {
-        const int I = tid >> 4, jj = tid & 15, base = 16 * I;
+// (hi, lo) words of the pair (x0, x1): hi = top 16 bits of each, lo = bf16(x - hi).
+__device__ __forceinline__ uint2 hl_pair(float x0, float x1) {
+    const uint32_t a = __float_as_uint(x0), b = __float_as_uint(x1);
+    const uint32_t h = __byte_perm(a, b, 0x7632);
+    const uint32_t l = pack_bf16x2(x0 - __uint_as_float(a & 0xFFFF0000u), x1 - __uint_as_float(b & 0xFFFF0000u));
+    return make_uint2(h, l);
+}
+__device__ __forceinline__ uint2 ld_pair(const uint8_t *blk, int r, int p) {
+    return *reinterpret_cast<const uint2 *>(blk + r * ROW_B + p * 8);
+}
+__device__ __forceinline__ void st_pair(uint8_t *blk, int r, int p, uint2 v) {
+    *reinterpret_cast<uint2 *>(blk + r * ROW_B + p * 8) = v;
+}
+
+// Fragments of mma.m16n8k16 (row.col, bf16): lane = 4 g + c.
+struct FragA {
+    uint32_t hi[4], lo[4];
+};
+// A = X (16 x 16) from a block of row-major X.
+__device__ __forceinline__ FragA ld_a(const uint8_t *blk, int g, int c) {
+    const uint2 v0 = ld_pair(blk, g, c), v1 = ld_pair(blk, g + 8, c), v2 = ld_pair(blk, g, c + 4),
+                v3 = ld_pair(blk, g + 8, c + 4);
+    FragA f;
+    f.hi[0] = v0.x;
+    f.hi[1] = v1.x;
+    f.hi[2] = v2.x;
+    f.hi[3] = v3.x;
+    f.lo[0] = v0.y;
+    f.lo[1] = v1.y;
+    f.lo[2] = v2.y;
+    f.lo[3] = v3.y;
+    return f;
+}
+// A from the two n8 accumulator halves of a previous product (scaled by `sign`).
+__device__ __forceinline__ FragA a_from_acc(const float *d0, const float *d1, float sign) {
+    const uint2 v0 = hl_pair(sign * d0[0], sign * d0[1]), v1 = hl_pair(sign * d0[2], sign * d0[3]);
+    const uint2 v2 = hl_pair(sign * d1[0], sign * d1[1]), v3 = hl_pair(sign * d1[2], sign * d1[3]);
+    FragA f;
+    f.hi[0] = v0.x;
+    f.hi[1] = v1.x;
+    f.hi[2] = v2.x;
+    f.hi[3] = v3.x;
+    f.lo[0] = v0.y;
+    f.lo[1] = v1.y;
+    f.lo[2] = v2.y;
+    f.lo[3] = v3.y;
+    return f;
+}
+
+__device__ __forceinline__ void mma16816(float *d, const uint32_t *a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// d[h] += A * B for both n8 halves h, where B = Yᵀ and Y is a row-major block:
+// three bf16 products per half (hi hi + hi lo + lo hi).
+__device__ __forceinline__ void mma_acc(float (*d)[4], const FragA &a, const uint8_t *yblk, int g, int c) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint2 b0 = ld_pair(yblk, 8 * h + g, c), b1 = ld_pair(yblk, 8 * h + g, c + 4);
+        mma16816(d[h], a.hi, b0.x, b1.x);
+        mma16816(d[h], a.hi, b0.y, b1.y);
+        mma16816(d[h], a.lo, b0.x, b1.x);
+    }
+}
+__device__ __forceinline__ void zero_acc(float (*d)[4]) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d[h][i] = 0.f;
+}
+
+// Gates of V head h for the chunk's 64 rows, by one warp (lane owns rows lane
+// and lane + 32): G = running sum of g in log2 units, beta, exp(G).
+__device__ __forceinline__ void chunk_gates(const FacParams &p, int64_t t0, int L, int h, float *gates, int lane) {
+    float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
+    if (lane < L) {
+        const size_t i = (size_t)(t0 + lane) * p.h_v + h;
+        g0 = p.g[i] * kLog2e;
+        b0 = p.beta[i];
+    }
+    if (lane + 32 < L) {
+        const size_t i = (size_t)(t0 + lane + 32) * p.h_v + h;
+        g1 = p.g[i] * kLog2e;
+        b1 = p.beta[i];
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float u0 = __shfl_up_sync(0xffffffffu, g0, o), u1 = __shfl_up_sync(0xffffffffu, g1, o);
+        if (lane >= o) {
+            g0 += u0;
+            g1 += u1;
+        }
+    }
+    g1 += __shfl_sync(0xffffffffu, g0, 31);
+    gates[lane] = g0;
+    gates[lane + 32] = g1;
+    gates[64 + lane] = b0;
+    gates[64 + lane + 32] = b1;
+    gates[128 + lane] = fast_exp2(g0);
+    gates[128 + lane + 32] = fast_exp2(g1);
+}
+
+// One V head's T and P T from its N and P blocks, by the two warps wi = 0, 1 of
+// named barrier `bar`; every block is stored to the slot's packed layout as
+// soon as it is formed.
+__device__ void solve_head(uint8_t *hs, float *slot_out, int wi, int lane, uint32_t bar) {
+    const int g = lane >> 2, c = lane & 3;
+    float *Tout = slot_out + fac::OFF_T, *PTout = slot_out + fac::OFF_PT;
+    // ---- diagonal blocks: each warp two, lanes 0-15 / 16-31 one block, lane = column
+    {
+        const int I = 2 * wi + (lane >> 4), jj = lane & 15;
+        const float *nd = reinterpret_cast<const float *>(hs + OFF_ND) + 256 * I;
         float col[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) col[r] = (r == jj) ? 1.f : 0.f;
 #pragma unroll
         for (int m = 0; m < 15; ++m) {
 #pragma unroll
-            for (int r = m + 1; r < 16; ++r) col[r] = fmaf(-N[(base + r) * SROW + base + m], col[m], col[r]);
+            for (int r = m + 1; r < 16; ++r) col[r] = fmaf(-nd[16 * r + m], col[m], col[r]);
         }
+        // Tᵀ_II row jj is column jj of T_II
+        uint8_t *tt = hs + OFF_TT + BLK_B * bi(I, I);
 #pragma unroll
-        for (int r = 0; r < 16; ++r) T[(base + r) * SROW + base + jj] = col[r];
-    }
-    __syncthreads();
-    // level 1: T_{I,I-1} = -T_II (N_{I,I-1} T_{I-1,I-1}) for I = 1 and 3
-    {
-        const int blk = tid >> 7, I = 2 * blk + 1, J = I - 1, r = (tid >> 3) & 15, cc = (tid & 7) * 2;
-        const float *nr = N + (16 * I + r) * SROW + 16 * J;
-        float a0 = 0.f, a1 = 0.f;
+        for (int q = 0; q < 8; ++q) st_pair(tt, jj, q, hl_pair(col[2 * q], col[2 * q + 1]));
+        // T_II row-major: lanes jj (even) and jj + 1 form the pairs of every row
+        uint8_t *td = hs + OFF_TD + BLK_B * I;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float2 tv = *reinterpret_cast<const float2 *>(T + (16 * J + m) * SROW + 16 * J + cc);
-            a0 = fmaf(nr[m], tv.x, a0);
-            a1 = fmaf(nr[m], tv.y, a1);
+        for (int r = 0; r < 16; ++r) {
+            const float nb = __shfl_down_sync(0xffffffffu, col[r], 1);
+            if ((jj & 1) == 0) st_pair(td, r, jj >> 1, hl_pair(col[r], nb));
         }
-        *reinterpret_cast<float2 *>(X + (16 * blk + r) * XROW + cc) = make_float2(a0, a1);
-    }
-    __syncthreads();
-    {
-        const int blk = tid >> 7, I = 2 * blk + 1, J = I - 1, r = (tid >> 3) & 15, cc = (tid & 7) * 2;
-        const float *tr = T + (16 * I + r) * SROW + 16 * I;
-        float a0 = 0.f, a1 = 0.f;
+        // global T: row 16 I + r, column 16 I + jj (chunks up to the diagonal)
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float2 xv = *reinterpret_cast<const float2 *>(X + (16 * blk + m) * XROW + cc);
-            a0 = fmaf(tr[m], xv.x, a0);
-            a1 = fmaf(tr[m], xv.y, a1);
+        for (int r = 0; r < 16; ++r) {
+            const int rg = 16 * I + r, cg = 16 * I + jj;
+            if ((cg >> 3) <= (rg >> 3)) Tout[fac::tri8_base(rg) + cg] = col[r];
         }
-        *reinterpret_cast<float2 *>(T + (16 * I + r) * SROW + 16 * J + cc) = make_float2(-a0, -a1);
     }
-    __syncthreads();
-    // level 2: T[32:64, 0:32] = -T[32:64, 32:64] (N[32:64, 0:32] T[0:32, 0:32]), 2 x 2 per thread
-    const int r0 = (tid >> 4) * 2, c0 = (tid & 15) * 2;
-    {
-        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
-        const float *n0 = N + (32 + r0) * SROW, *n1 = n0 + SROW;
-        for (int m = c0; m < 32; ++m) {  // T[0:32, 0:32] is lower: rows m >= c0 only
-            const float2 tv = *reinterpret_cast<const float2 *>(T + m * SROW + c0);
-            const float u0 = n0[m], u1 = n1[m];
-            a00 = fmaf(u0, tv.x, a00);
-            a01 = fmaf(u0, tv.y, a01);
-            a10 = fmaf(u1, tv.x, a10);
-            a11 = fmaf(u1, tv.y, a11);
+    named_sync(bar, 64);
+    // ---- off-diagonal blocks by diagonals d = 1 (3 blocks), 2 (2), 3 (1):
+    // X_IJᵀ = sum_K Tᵀ(J, K) N_IKᵀ, then T_IJᵀ = -X_IJᵀ T_IIᵀ
+    for (int d = 1; d <= 3; ++d) {
+        for (int J = wi; J + d <= 3; J += 2) {
+            const int I = J + d;
+            float x[2][4];
+            zero_acc(x);
+            for (int K = J; K < I; ++K)
+                mma_acc(x, ld_a(hs + OFF_TT + BLK_B * bi(K, J), g, c), hs + OFF_NB + BLK_B * bi(I, K), g, c);
+            float t[2][4];
+            zero_acc(t);
+            mma_acc(t, a_from_acc(x[0], x[1], -1.f), hs + OFF_TD + BLK_B * I, g, c);
+            // Tᵀ(J, I): rows g, g + 8; pairs 4 h + c
+            uint8_t *tt = hs + OFF_TT + BLK_B * bi(I, J);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                st_pair(tt, g, 4 * h + c, hl_pair(t[h][0], t[h][1]));
+                st_pair(tt, g + 8, 4 * h + c, hl_pair(t[h][2], t[h][3]));
+            }
+            // global T: Tᵀ(J, I)[m][n] = T[16 I + n][16 J + m]
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int n = 8 * h + 2 * c;
+                float *r0 = Tout + fac::tri8_base(16 * I + n) + 16 * J;
+                float *r1 = Tout + fac::tri8_base(16 * I + n + 1) + 16 * J;
+                r0[g] = t[h][0];
+                r1[g] = t[h][1];
+                r0[g + 8] = t[h][2];
+                r1[g + 8] = t[h][3];
+            }
         }
-        *reinterpret_cast<float2 *>(X + r0 * XROW + c0) = make_float2(a00, a01);
-        *reinterpret_cast<float2 *>(X + (r0 + 1) * XROW + c0) = make_float2(a10, a11);
+        named_sync(bar, 64);
     }
-    __syncthreads();
-    {
-        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
-        const float *t0 = T + (32 + r0) * SROW + 32, *t1 = t0 + SROW;
-        for (int m = 0; m <= r0 + 1; ++m) {  // T[32:64, 32:64] is lower: columns m <= row
-            const float2 xv = *reinterpret_cast<const float2 *>(X + m * XROW + c0);
-            const float u0 = t0[m], u1 = t1[m];
-            a00 = fmaf(u0, xv.x, a00);
-            a01 = fmaf(u0, xv.y, a01);
-            a10 = fmaf(u1, xv.x, a10);
-            a11 = fmaf(u1, xv.y, a11);
+    // ---- P T, blocks (I, J) with I >= J: warp 0 takes block column 0, warp 1 the
+    // other six; both sum ten 16 x 16 x 16 products
+    // warp 1's blocks (I, J) as nibbles: (2,1) (3,2) (3,1) (1,1) (2,2) (3,3)
+    constexpr uint32_t kIs = 0x321332u, kJs = 0x321121u;
+    const int nblk = wi == 0 ? 4 : 6;
+    for (int b = 0; b < nblk; ++b) {
+        const int I = wi == 0 ? 3 - b : (int)((kIs >> (4 * b)) & 15u);
+        const int J = wi == 0 ? 0 : (int)((kJs >> (4 * b)) & 15u);
+        float acc[2][4];
+        zero_acc(acc);
+        for (int K = J; K <= I; ++K)
+            mma_acc(acc, ld_a(hs + OFF_PB + BLK_B * bi(I, K), g, c), hs + OFF_TT + BLK_B * bi(K, J), g, c);
+        // rows 16 I + g (+ 8); columns 16 J + 8 h + 2 c, + 1 (kept chunks only)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int cg = 16 * J + 8 * h + 2 * c;
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int rg = 16 * I + g + 8 * hr;
+                if ((cg >> 3) <= (rg >> 3))
+                    *reinterpret_cast<float2 *>(PTout + fac::tri8_base(rg) + cg) =
+                        make_float2(acc[h][2 * hr], acc[h][2 * hr + 1]);
+            }
         }
-        *reinterpret_cast<float2 *>(T + (32 + r0) * SROW + c0) = make_float2(-a00, -a01);
-        *reinterpret_cast<float2 *>(T + (33 + r0) * SROW + c0) = make_float2(-a10, -a11);
-    }
-    __syncthreads();
-}
-
-// PT = P T for lower-triangular P and T (fp32 [64][SROW]); only blocks on or
-// below the 16-block diagonal are formed.  The ten blocks are split into four
-// groups of equal work (counted in 16x16x16 products: block (I, J) costs
-// I - J + 1), one group per 64 threads, 2 x 2 outputs per thread per block.
-__device__ void lower_product(const float *P, const float *T, float *PT, int tid) {
-    const int gp = tid >> 6, ti = tid & 63, rr = (ti >> 3) * 2, cc = (ti & 7) * 2;
-    // (I, J) pairs per group: {30, 00}, {20, 10}, {31, 21}, {32, 11, 22, 33}
-    const uint32_t blocks = gp == 0 ? 0x0030u : gp == 1 ? 0x1020u : gp == 2 ? 0x2131u : 0x33221132u;
-    const int nb = gp == 3 ? 4 : 2;
-    for (int b = 0; b < nb; ++b) {
-        const uint32_t code = (blocks >> (8 * b)) & 0xFFu;
-        const int I = (int)(code >> 4), J = (int)(code & 15u);
-        const int row = 16 * I + rr, col = 16 * J + cc;
-        const float *p0 = P + row * SROW, *p1 = p0 + SROW;
-        float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
-        // T rows m >= col (T lower), P columns m <= row + 1 (P lower)
-        for (int m = col; m <= row + 1; ++m) {
-            const float2 tv = *reinterpret_cast<const float2 *>(T + m * SROW + col);
-            const float u0 = p0[m], u1 = p1[m];
-            a00 = fmaf(u0, tv.x, a00);
-            a01 = fmaf(u0, tv.y, a01);
-            a10 = fmaf(u1, tv.x, a10);
-            a11 = fmaf(u1, tv.y, a11);
-        }
-        *reinterpret_cast<float2 *>(PT + row * SROW + col) = make_float2(a00, a01);
-        *reinterpret_cast<float2 *>(PT + (row + 1) * SROW + col) = make_float2(a10, a11);
     }
 }
 
-// Packs the lower triangle of a [64][SROW] matrix (rows in 8-float chunks up to
-// the diagonal chunk) into `dst`.  Four threads per row, float4 stores.
-__device__ __forceinline__ void store_packed(const float *M, float *dst, int tid) {
-    const int t = tid >> 2, nch = (t >> 3) + 1;
-    float *row = dst + fac::tri8_base(t);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int f = (tid & 3) + 4 * i;  // float4 index in the row: chunk f / 2, half f % 2
-        if ((f >> 1) < nch)
-            *reinterpret_cast<float4 *>(row + 4 * f) = *reinterpret_cast<const float4 *>(M + t * SROW + 4 * f);
-    }
-}
-
-__global__ void __launch_bounds__(NT) factor_kernel(const __grid_constant__ CUtensorMap tmK,
-                                                    const __grid_constant__ CUtensorMap tmQ, FacParams p) {
+__global__ void __launch_bounds__(NT, 2) factor_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                       const __grid_constant__ CUtensorMap tmQ, FacParams p) {
     const int64_t slot = blockIdx.x;
     const int hq = blockIdx.y;
     // the sequence whose chunk this slot holds: the last s with slot_base(s) <= slot
@@ -216,8 +316,7 @@ __global__ void __launch_bounds__(NT) factor_kernel(const __grid_constant__ CUte
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    float *sG = reinterpret_cast<float *>(sm + OFF_GATES), *sB = sG + 64, *sE = sG + 128;
-    float *sScan = reinterpret_cast<float *>(sm + OFF_SCAN);
+    float *gates = reinterpret_cast<float *>(sm + OFF_GATES);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + OFF_TMEM);
     const uint32_t bar_tma = sb + OFF_BARS, bar_mma = sb + OFF_BARS + 8;
 
@@ -225,7 +324,7 @@ __global__ void __launch_bounds__(NT) factor_kernel(const __grid_constant__ CUte
         mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(bar_tma, 32768);
+        mbar_arrive_expect_tx(bar_tma, 32768u);
         tma_load_3d(sb + OFF_KQ, &tmK, bar_tma, 0, hq, (int)t0);
         tma_load_3d(sb + OFF_KQ + 16384, &tmK, bar_tma, 64, hq, (int)t0);
         tma_load_3d(sb + OFF_KQ + 8192, &tmQ, bar_tma, 0, hq, (int)t0);
@@ -239,6 +338,10 @@ __global__ void __launch_bounds__(NT) factor_kernel(const __grid_constant__ CUte
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_holder;
+
+    const int grp = p.h_v / p.h_qk, hv0 = hq * grp;
+    // first pass's gates while the tile loads
+    if (warp < HP && warp < grp) chunk_gates(p, t0, L, hv0 + warp, gates + 192 * warp, lane);
 
     // Gram products [K Kᵀ; Q Kᵀ] into TMEM (lane = row, column = key token)
     bool ok = true;
@@ -266,69 +369,57 @@ __global__ void __launch_bounds__(NT) factor_kernel(const __grid_constant__ CUte
     }
     tc_fence_after_sync();
 
-    float *N = reinterpret_cast<float *>(sm + OFF_N), *P = reinterpret_cast<float *>(sm + OFF_P);
-    float *T = reinterpret_cast<float *>(sm + OFF_T), *X = reinterpret_cast<float *>(sm + OFF_X);
-    const int grp = p.h_v / p.h_qk;
-    for (int hh = 0; hh < grp; ++hh) {
-        const int h = hq * grp + hh;
-        // gates: G = running sum of g (kept as G log2(e) so each decay is one exp2)
-        float gl = 0.f;
-        if (tid < C) {
-            float b = 0.f;
-            if (tid < L) {
-                const size_t i = (size_t)(t0 + tid) * p.h_v + h;
-                gl = p.g[i] * kLog2e;
-                b = p.beta[i];
-            }
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float u = __shfl_up_sync(0xffffffffu, gl, o);
-                if (lane >= o) gl += u;
-            }
-            if (lane == 31) sScan[warp] = gl;
-            sB[tid] = b;
-        }
+    // this thread's Gram row: K rows (N) in lanes 0-63, Q rows (P) in lanes 64-127
+    const int row = 32 * warp + lane, t = row & 63, I = t >> 4, r16 = t & 15;
+    const bool is_n = row < 64;
+    float a[64];
+    tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16), a);
+    tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32, a + 32);
+    tc_fence_before_sync();
+    for (int pass = 0; pass < grp; pass += HP) {
+        const int np = (grp - pass) < HP ? (grp - pass) : HP;
+        if (pass > 0 && warp < np) chunk_gates(p, t0, L, hv0 + pass + warp, gates + 192 * warp, lane);
         __syncthreads();
-        if (tid < C) {
-            if (tid >= 32) gl += sScan[0];
-            sG[tid] = gl;
-            sE[tid] = fast_exp2(gl);
-        }
-        __syncthreads();
-        // N (rows 0-63 of the Gram tile) and P (rows 64-127), masked in log space
-        {
-            const int q4 = warp & 3, half = warp >> 2;
-            const int row = 32 * q4 + lane, t = row & 63;
-            float a[32];
-            tmem_ld32(tmem + ((uint32_t)(32 * q4) << 16) + 32 * half, a);
-            const float Gt = sG[t];
-            const bool is_n = row < 64;
-            const float w = is_n ? sB[t] : 1.f;
+        // N and P rows of each head of the pass, masked in log space, into blocks
+        for (int k = 0; k < np; ++k) {
+            const float *gk = gates + 192 * k;
+            uint8_t *hs = sm + HEAD_B * k;
+            const float Gt = gk[t];
+            const float w = is_n ? gk[64 + t] : 1.f;
             const int lim = is_n ? t : t + 1;  // keep j < t (N) or j <= t (P)
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int jj = 32 * half + j;
-                a[j] = (jj < lim) ? w * fast_exp2(Gt - sG[jj]) * a[j] : 0.f;
-            }
-            float *dst = (is_n ? N : P) + t * SROW + 32 * half;
+            for (int J = 0; J < 4; ++J) {
+                if (J > I) continue;
+                float v[16];
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4 *>(dst + j) = make_float4(a[j], a[j + 1], a[j + 2], a[j + 3]);
+                for (int e = 0; e < 16; ++e) {
+                    const int j = 16 * J + e;
+                    v[e] = (j < lim) ? w * fast_exp2(Gt - gk[j]) * a[j] : 0.f;
+                }
+                if (is_n && J == I) {
+                    float *nd = reinterpret_cast<float *>(hs + OFF_ND) + 256 * I + 16 * r16;
+#pragma unroll
+                    for (int e = 0; e < 16; e += 4)
+                        *reinterpret_cast<float4 *>(nd + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                } else {
+                    uint8_t *blk = hs + (is_n ? OFF_NB : OFF_PB) + BLK_B * bi(I, J);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) st_pair(blk, r16, q, hl_pair(v[2 * q], v[2 * q + 1]));
+                }
+            }
         }
-        tc_fence_before_sync();
         __syncthreads();
-        unit_lower_inverse(N, T, X, tid);  // ends with a barrier; N is free afterwards
-        lower_product(P, T, N, tid);       // P T into N's space
-        __syncthreads();
-        float *slot_out = p.ws + ((size_t)slot * p.h_v + h) * fac::SLOT_FLOATS;
-        store_packed(T, slot_out + fac::OFF_T, tid);
-        store_packed(N, slot_out + fac::OFF_PT, tid);
-        if (tid < 48) {
-            const int a = tid >> 4, e = (tid & 15) * 4;  // G, beta, exp(G): 16 float4 each
-            *reinterpret_cast<float4 *>(slot_out + fac::OFF_G + 64 * a + e) =
-                *reinterpret_cast<const float4 *>(sG + 64 * a + e);
+        if (warp < 2 * np) {
+            const int k = warp >> 1, h = hv0 + pass + k;
+            float *slot_out = p.ws + ((size_t)slot * p.h_v + h) * fac::SLOT_FLOATS;
+            solve_head(sm + HEAD_B * k, slot_out, warp & 1, lane, 1 + k);
+            if ((warp & 1) == 0) {
+                const float *gk = gates + 192 * k;
+#pragma unroll
+                for (int i = 0; i < 6; ++i) slot_out[fac::OFF_G + 32 * i + lane] = gk[32 * i + lane];
+            }
         }
-        __syncthreads();  // scratch and gates are reused by the next V head
+        __syncthreads();  // scratch and gates are reused by the next pass
     }
     if (warp == 0) {
         tc_fence_after_sync();
