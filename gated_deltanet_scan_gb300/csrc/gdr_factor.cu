@@ -1,7 +1,7 @@
 // State-independent factors of the chunked prefill, computed for every chunk at
-// once (no chunk depends on another).  One CTA per (chunk, QK head) writes, for
-// each V head that reads the QK head, the chunk's gates, T = (I + N)^-1 and P T
-// into the factor workspace (layout in gdr_factor_layout.h).
+// once (no chunk depends on another).  One CTA per (chunk, V head) writes the
+// chunk's gates, T = (I + N)^-1 and P T into the factor workspace (layout in
+// gdr_factor_layout.h).
 //
 // Per chunk (the chunkwise-parallel form of the Qwen3.5-9B NPU model card,
 // "How it works"; forward substitution for the unit triangular factor as in
@@ -19,8 +19,8 @@
 //   P T   (P T)_IJ = sum_{K=J}^{I} P_IK T_KJ
 // The block products run on warp-level bf16 tensor-core MMAs (m16n8k16) with
 // each fp32 operand split into bf16 hi + lo (x = hi + lo to ~2^-16) and three
-// products hi*hi + hi*lo + lo*hi accumulated in fp32.  Two warps share one V
-// head.  Off-diagonal blocks of T are formed transposed, T_IJᵀ = -X_IJᵀ T_IIᵀ,
+// products hi*hi + hi*lo + lo*hi accumulated in fp32.  Two warps solve for T,
+// all four form P T.  Off-diagonal blocks of T are formed transposed, T_IJᵀ = -X_IJᵀ T_IIᵀ,
 // so that X_IJᵀ comes straight out of one MMA's accumulators as the left
 // operand of the next.
 #include <cuda.h>
@@ -37,8 +37,7 @@ namespace {
 using namespace tc;
 
 constexpr int C = fac::C;
-constexpr int NT = 128;  // four warps: one TMEM lane quadrant each; two warps per V head
-constexpr int HP = 2;    // V heads per pass
+constexpr int NT = 128;  // four warps: one TMEM lane quadrant each
 
 // A 16 x 16 block in shared memory as 16 rows of 8 pairs; pair p of row r holds
 // hi(x[r][2p]), hi(x[r][2p+1]) in one word and the matching lo parts in the
@@ -48,27 +47,28 @@ constexpr int ROW_B = 96;
 constexpr int BLK_B = 16 * ROW_B;  // 1536
 __host__ __device__ constexpr int bi(int I, int J) { return I * (I + 1) / 2 + J; }  // lower block index, I >= J
 
-// Per-head scratch (bytes).  NB: the off-diagonal blocks of N (slots bi(I, J),
-// diagonal slots unused); ND: the four diagonal blocks of N in fp32; PB: the
+// Scratch (bytes).  NB: the off-diagonal blocks of N (slots bi(I, J) - I, the
+// diagonal slots left out); ND: the four diagonal blocks of N in fp32; PB: the
 // ten lower blocks of P; TT: the blocks of Tᵀ on and above the diagonal, block
 // (J, K) in slot bi(K, J); TD: the four diagonal blocks of T, row-major (for
 // T_IIᵀ as a right operand).
+__host__ __device__ constexpr int nbi(int I, int J) { return bi(I, J) - I; }  // I > J
 constexpr int OFF_NB = 0;
-constexpr int OFF_ND = OFF_NB + 10 * BLK_B;
+constexpr int OFF_ND = OFF_NB + 6 * BLK_B;
 constexpr int OFF_PB = OFF_ND + 4 * 1024;
 constexpr int OFF_TT = OFF_PB + 10 * BLK_B;
 constexpr int OFF_TD = OFF_TT + 10 * BLK_B;
-constexpr int HEAD_B = OFF_TD + 4 * BLK_B;  // 56320
+constexpr int HEAD_B = OFF_TD + 4 * BLK_B;  // 50176
 
 // Shared memory, bytes from a 1024-byte aligned base.  The K/Q tile is only read
-// by the Gram MMA; once it has completed, the heads' scratch overwrites it.
+// by the Gram MMA; once it has completed, the scratch overwrites it.
 constexpr uint32_t OFF_KQ = 0;
-constexpr uint32_t OFF_GATES = HP * HEAD_B;               // HP x (G log2(e), beta, exp(G)) x 64 fp32
-constexpr uint32_t OFF_BARS = OFF_GATES + HP * 192 * 4;  // 2 mbarriers
+constexpr uint32_t OFF_GATES = HEAD_B;           // G log2(e), beta, exp(G): 3 x 64 fp32
+constexpr uint32_t OFF_BARS = OFF_GATES + 768;  // 2 mbarriers
 constexpr uint32_t OFF_TMEM = OFF_BARS + 16;
 constexpr uint32_t SMEM_USED = OFF_TMEM + 16;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
-static_assert(32768 <= HP * HEAD_B, "K/Q tile fits under the scratch");
+static_assert(32768 <= HEAD_B, "K/Q tile fits under the scratch");
 static_assert(OFF_GATES % 16 == 0 && OFF_BARS % 8 == 0 && HEAD_B % 16 == 0, "alignment");
 
 constexpr uint32_t TM_COLS = 64;  // the 128 x 64 fp32 Gram tile
@@ -162,19 +162,9 @@ __device__ __forceinline__ void zero_acc(float (*d)[4]) {
 }
 
 // Gates of V head h for the chunk's 64 rows, by one warp (lane owns rows lane
-// and lane + 32): G = running sum of g in log2 units, beta, exp(G).
-__device__ __forceinline__ void chunk_gates(const FacParams &p, int64_t t0, int L, int h, float *gates, int lane) {
-    float g0 = 0.f, g1 = 0.f, b0 = 0.f, b1 = 0.f;
-    if (lane < L) {
-        const size_t i = (size_t)(t0 + lane) * p.h_v + h;
-        g0 = p.g[i] * kLog2e;
-        b0 = p.beta[i];
-    }
-    if (lane + 32 < L) {
-        const size_t i = (size_t)(t0 + lane + 32) * p.h_v + h;
-        g1 = p.g[i] * kLog2e;
-        b1 = p.beta[i];
-    }
+// and lane + 32): G = running sum of g in log2 units, beta, exp(G).  The raw
+// g and beta are loaded first (as early as possible), the scan done later.
+__device__ __forceinline__ void chunk_gates(float g0, float g1, float b0, float b1, float *gates, int lane) {
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const float u0 = __shfl_up_sync(0xffffffffu, g0, o), u1 = __shfl_up_sync(0xffffffffu, g1, o);
@@ -192,12 +182,11 @@ __device__ __forceinline__ void chunk_gates(const FacParams &p, int64_t t0, int 
     gates[128 + lane + 32] = fast_exp2(g1);
 }
 
-// One V head's T and P T from its N and P blocks, by the two warps wi = 0, 1 of
-// named barrier `bar`; every block is stored to the slot's packed layout as
-// soon as it is formed.
-__device__ void solve_head(uint8_t *hs, float *slot_out, int wi, int lane, uint32_t bar) {
+// The head's T from its N blocks, by warps wi = 0, 1 (named barrier `bar`);
+// every block is stored to the slot's packed layout as soon as it is formed.
+__device__ void solve_t(uint8_t *hs, float *slot_out, int wi, int lane, uint32_t bar) {
     const int g = lane >> 2, c = lane & 3;
-    float *Tout = slot_out + fac::OFF_T, *PTout = slot_out + fac::OFF_PT;
+    float *Tout = slot_out + fac::OFF_T;
     // ---- diagonal blocks: each warp two, lanes 0-15 / 16-31 one block, lane = column
     {
         const int I = 2 * wi + (lane >> 4), jj = lane & 15;
@@ -237,7 +226,7 @@ __device__ void solve_head(uint8_t *hs, float *slot_out, int wi, int lane, uint3
             float x[2][4];
             zero_acc(x);
             for (int K = J; K < I; ++K)
-                mma_acc(x, ld_a(hs + OFF_TT + BLK_B * bi(K, J), g, c), hs + OFF_NB + BLK_B * bi(I, K), g, c);
+                mma_acc(x, ld_a(hs + OFF_TT + BLK_B * bi(K, J), g, c), hs + OFF_NB + BLK_B * nbi(I, K), g, c);
             float t[2][4];
             zero_acc(t);
             mma_acc(t, a_from_acc(x[0], x[1], -1.f), hs + OFF_TD + BLK_B * I, g, c);
@@ -260,16 +249,21 @@ __device__ void solve_head(uint8_t *hs, float *slot_out, int wi, int lane, uint3
                 r1[g + 8] = t[h][3];
             }
         }
-        named_sync(bar, 64);
+        if (d < 3) named_sync(bar, 64);
     }
-    // ---- P T, blocks (I, J) with I >= J: warp 0 takes block column 0, warp 1 the
-    // other six; both sum ten 16 x 16 x 16 products
-    // warp 1's blocks (I, J) as nibbles: (2,1) (3,2) (3,1) (1,1) (2,2) (3,3)
-    constexpr uint32_t kIs = 0x321332u, kJs = 0x321121u;
-    const int nblk = wi == 0 ? 4 : 6;
+}
+
+// The head's P T from P and Tᵀ blocks, by the four warps w: block (I, J), I >= J,
+// costs I - J + 1 products; the groups {30, 00}, {20, 10}, {31, 21},
+// {32, 11, 22, 33} cost five each.
+__device__ void solve_pt(const uint8_t *hs, float *slot_out, int w, int lane) {
+    const int g = lane >> 2, c = lane & 3;
+    float *PTout = slot_out + fac::OFF_PT;
+    const uint32_t blocks = w == 0 ? 0x0030u : w == 1 ? 0x1020u : w == 2 ? 0x2131u : 0x33221132u;
+    const int nblk = w == 3 ? 4 : 2;
     for (int b = 0; b < nblk; ++b) {
-        const int I = wi == 0 ? 3 - b : (int)((kIs >> (4 * b)) & 15u);
-        const int J = wi == 0 ? 0 : (int)((kJs >> (4 * b)) & 15u);
+        const uint32_t code = (blocks >> (8 * b)) & 0xFFu;
+        const int I = (int)(code >> 4), J = (int)(code & 15u);
         float acc[2][4];
         zero_acc(acc);
         for (int K = J; K <= I; ++K)
@@ -289,10 +283,10 @@ __device__ void solve_head(uint8_t *hs, float *slot_out, int wi, int lane, uint3
     }
 }
 
-__global__ void __launch_bounds__(NT, 2) factor_kernel(const __grid_constant__ CUtensorMap tmK,
+__global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ CUtensorMap tmK,
                                                        const __grid_constant__ CUtensorMap tmQ, FacParams p) {
     const int64_t slot = blockIdx.x;
-    const int hq = blockIdx.y;
+    const int h = blockIdx.y, hq = h / (p.h_v / p.h_qk);
     // the sequence whose chunk this slot holds: the last s with slot_base(s) <= slot
     int lo = 0, hi = p.n_seqs - 1;
     while (lo < hi) {
@@ -320,6 +314,20 @@ __global__ void __launch_bounds__(NT, 2) factor_kernel(const __grid_constant__ C
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + OFF_TMEM);
     const uint32_t bar_tma = sb + OFF_BARS, bar_mma = sb + OFF_BARS + 8;
 
+    // raw gates first (warp 0): their latency overlaps the tile load
+    float rg0 = 0.f, rg1 = 0.f, rb0 = 0.f, rb1 = 0.f;
+    if (warp == 0) {
+        if (lane < L) {
+            const size_t i = (size_t)(t0 + lane) * p.h_v + h;
+            rg0 = p.g[i] * kLog2e;
+            rb0 = p.beta[i];
+        }
+        if (lane + 32 < L) {
+            const size_t i = (size_t)(t0 + lane + 32) * p.h_v + h;
+            rg1 = p.g[i] * kLog2e;
+            rb1 = p.beta[i];
+        }
+    }
     if (tid == 0) {
         mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);
@@ -338,10 +346,7 @@ __global__ void __launch_bounds__(NT, 2) factor_kernel(const __grid_constant__ C
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_holder;
-
-    const int grp = p.h_v / p.h_qk, hv0 = hq * grp;
-    // first pass's gates while the tile loads
-    if (warp < HP && warp < grp) chunk_gates(p, t0, L, hv0 + warp, gates + 192 * warp, lane);
+    if (warp == 0) chunk_gates(rg0, rg1, rb0, rb1, gates, lane);
 
     // Gram products [K Kᵀ; Q Kᵀ] into TMEM (lane = row, column = key token)
     bool ok = true;
@@ -360,7 +365,7 @@ __global__ void __launch_bounds__(NT, 2) factor_kernel(const __grid_constant__ C
     }
     ok = ok && mbar_wait_bounded(bar_mma, 0, kWaitLimit);
     if (!ok) atomicCAS(p.err, 0, (int32_t)GDR_ERR_DEVICE_TIMEOUT);
-    if (!__syncthreads_and(ok)) {
+    if (!__syncthreads_and(ok)) {  // also publishes the gates
         // let the tile load land before this CTA's shared memory is released
         if (tid == 0) mbar_wait_bounded(bar_tma, 0, kWaitLimit / 8);
         __syncthreads();
@@ -369,58 +374,48 @@ __global__ void __launch_bounds__(NT, 2) factor_kernel(const __grid_constant__ C
     }
     tc_fence_after_sync();
 
-    // this thread's Gram row: K rows (N) in lanes 0-63, Q rows (P) in lanes 64-127
-    const int row = 32 * warp + lane, t = row & 63, I = t >> 4, r16 = t & 15;
-    const bool is_n = row < 64;
-    float a[64];
-    tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16), a);
-    tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32, a + 32);
-    tc_fence_before_sync();
-    for (int pass = 0; pass < grp; pass += HP) {
-        const int np = (grp - pass) < HP ? (grp - pass) : HP;
-        if (pass > 0 && warp < np) chunk_gates(p, t0, L, hv0 + pass + warp, gates + 192 * warp, lane);
-        __syncthreads();
-        // N and P rows of each head of the pass, masked in log space, into blocks
-        for (int k = 0; k < np; ++k) {
-            const float *gk = gates + 192 * k;
-            uint8_t *hs = sm + HEAD_B * k;
-            const float Gt = gk[t];
-            const float w = is_n ? gk[64 + t] : 1.f;
-            const int lim = is_n ? t : t + 1;  // keep j < t (N) or j <= t (P)
+    // N (K rows, lanes 0-63) and P (Q rows, lanes 64-127), masked in log space,
+    // 16 Gram columns at a time into blocks
+    {
+        const int row = 32 * warp + lane, t = row & 63, I = t >> 4, r16 = t & 15;
+        const bool is_n = row < 64;
+        const float Gt = gates[t];
+        const float w = is_n ? gates[64 + t] : 1.f;
+        const int lim = is_n ? t : t + 1;  // keep j < t (N) or j <= t (P)
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
 #pragma unroll
-            for (int J = 0; J < 4; ++J) {
-                if (J > I) continue;
-                float v[16];
+        for (int J = 0; J < 4; ++J) {
+            float v[16];
+            tmem_ld16(lane_addr + 16 * J, v);
+            if (J > I) continue;
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int j = 16 * J + e;
-                    v[e] = (j < lim) ? w * fast_exp2(Gt - gk[j]) * a[j] : 0.f;
-                }
-                if (is_n && J == I) {
-                    float *nd = reinterpret_cast<float *>(hs + OFF_ND) + 256 * I + 16 * r16;
+            for (int e = 0; e < 16; ++e) {
+                const int j = 16 * J + e;
+                v[e] = (j < lim) ? w * fast_exp2(Gt - gates[j]) * v[e] : 0.f;
+            }
+            if (is_n && J == I) {
+                float *nd = reinterpret_cast<float *>(sm + OFF_ND) + 256 * I + 16 * r16;
 #pragma unroll
-                    for (int e = 0; e < 16; e += 4)
-                        *reinterpret_cast<float4 *>(nd + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-                } else {
-                    uint8_t *blk = hs + (is_n ? OFF_NB : OFF_PB) + BLK_B * bi(I, J);
+                for (int e = 0; e < 16; e += 4)
+                    *reinterpret_cast<float4 *>(nd + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+            } else {
+                uint8_t *blk = sm + (is_n ? OFF_NB + BLK_B * nbi(I, J) : OFF_PB + BLK_B * bi(I, J));
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) st_pair(blk, r16, q, hl_pair(v[2 * q], v[2 * q + 1]));
-                }
+                for (int q = 0; q < 8; ++q) st_pair(blk, r16, q, hl_pair(v[2 * q], v[2 * q + 1]));
             }
         }
-        __syncthreads();
-        if (warp < 2 * np) {
-            const int k = warp >> 1, h = hv0 + pass + k;
-            float *slot_out = p.ws + ((size_t)slot * p.h_v + h) * fac::SLOT_FLOATS;
-            solve_head(sm + HEAD_B * k, slot_out, warp & 1, lane, 1 + k);
-            if ((warp & 1) == 0) {
-                const float *gk = gates + 192 * k;
-#pragma unroll
-                for (int i = 0; i < 6; ++i) slot_out[fac::OFF_G + 32 * i + lane] = gk[32 * i + lane];
-            }
-        }
-        __syncthreads();  // scratch and gates are reused by the next pass
     }
+    tc_fence_before_sync();
+    __syncthreads();
+    float *slot_out = p.ws + ((size_t)slot * p.h_v + h) * fac::SLOT_FLOATS;
+    if (warp < 2)
+        solve_t(sm, slot_out, warp, lane, 1);
+    else if (warp == 2) {
+#pragma unroll
+        for (int i = 0; i < 6; ++i) slot_out[fac::OFF_G + 32 * i + lane] = gates[32 * i + lane];
+    }
+    __syncthreads();
+    solve_pt(sm, slot_out, warp, lane);
     if (warp == 0) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, TM_COLS);
@@ -454,7 +449,7 @@ cudaError_t launch_factors(const Args &a, float *ws, int32_t *err, cudaStream_t 
     p.ws = ws;
     p.err = err;
     const int64_t slots = fac::n_slots(a.t_total, a.n_seqs);
-    dim3 grid((unsigned)slots, (unsigned)a.h_qk);
+    dim3 grid((unsigned)slots, (unsigned)a.h_v);
     factor_kernel<<<grid, NT, SMEM_BYTES, s>>>(tmK, tmQ, p);
     return cudaGetLastError();
 }
