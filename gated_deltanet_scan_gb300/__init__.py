@@ -15,7 +15,8 @@ from typing import Optional
 
 __all__ = [
     "GdrError", "gdr_dims", "lib", "library_path",
-    "gdr_prefill_chunked", "gdr_prefill_workspace_bytes", "gdr_decode_step", "gdr_verify_block",
+    "gdr_prefill_chunked", "gdr_prefill_workspace_bytes", "gdr_prefill_chunked_static",
+    "gdr_decode_step", "gdr_verify_block",
     "gdr_state_snapshot", "gdr_state_restore", "gdr_device_error", "gdr_status_string",
     "GDR_F32", "GDR_BF16",
 ]
@@ -55,6 +56,9 @@ _SIGS = {
                                     ctypes.c_size_t),
     "gdr_prefill_chunked": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, ctypes.c_int64,
                              _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "gdr_prefill_chunked_static": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, ctypes.c_int64,
+                                    _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "gdr_prefill_static_workspace_capacity": ([], ctypes.c_size_t),
     "gdr_decode_step": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P],
                         ctypes.c_int),
     "gdr_verify_block": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, ctypes.c_int32,
@@ -165,6 +169,19 @@ def gdr_prefill_chunked(q, k, v, g, beta, state, o, cu_seqlens, *, chunk: int = 
         ctypes.byref(dims), n, _ptr(cu_seqlens), T, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
         _ptr(beta), _ptr(state), _ptr(o), ws_ptr, ws_bytes, _stream_handle(stream, q.device))
     _check(st, "gdr_prefill_chunked")
+
+
+def gdr_prefill_chunked_static(q, k, v, g, beta, state, o, cu_seqlens, *, chunk: int = 64,
+                               scale: float = 1.0, t_total: Optional[int] = None, stream=None) -> None:
+    """gdr_prefill_chunked with the library's fixed scratch array instead of a
+    workspace (nothing is allocated; see include/gdr.h for its size limit)."""
+    dims = make_dims(q, v, o, chunk, scale)
+    n = cu_seqlens.shape[0] - 1
+    T = q.shape[0] if t_total is None else int(t_total)
+    st = lib().gdr_prefill_chunked_static(
+        ctypes.byref(dims), n, _ptr(cu_seqlens), T, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+        _ptr(beta), _ptr(state), _ptr(o), _stream_handle(stream, q.device))
+    _check(st, "gdr_prefill_chunked_static")
 
 
 def gdr_decode_step(q, k, v, g, beta, state, o, *, scale: float = 1.0, stream=None) -> None:

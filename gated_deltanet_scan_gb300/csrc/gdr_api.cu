@@ -7,6 +7,23 @@
 namespace gdr {
 namespace {
 
+// Scratch of gdr_prefill_chunked_static: one fixed device array, never allocated
+// at run time.  Its device address is resolved once per device.
+constexpr size_t kStaticWorkspaceBytes = size_t(64) << 20;
+static __device__ __align__(256) uint8_t g_static_workspace[kStaticWorkspaceBytes];
+
+void *static_workspace() {
+    static void *cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!cached[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess) return nullptr;
+        cached[dev] = p;
+    }
+    return cached[dev];
+}
+
 __global__ void copy_f32_kernel(const float4 *__restrict__ src, float4 *__restrict__ dst, size_t n4) {
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride)
@@ -115,6 +132,25 @@ gdr_status gdr_prefill_chunked(const gdr_dims *dims, int32_t n_seqs, const int32
         return from_cuda(launch_prefill_tc(a, ws, s));
     }
     return from_cuda(launch_chunk_cc(a, s));
+}
+
+size_t gdr_prefill_static_workspace_capacity(void) { return kStaticWorkspaceBytes; }
+
+gdr_status gdr_prefill_chunked_static(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens,
+                                      int64_t t_total, const void *q, const void *k, const void *v,
+                                      const float *g, const float *beta, float *state, void *o,
+                                      gdr_stream_t stream) {
+    gdr_status st = check_dims(dims);
+    if (st != GDR_OK) return st;
+    if (n_seqs < 0 || t_total < 0) return GDR_ERR_INVALID_ARG;
+    const size_t need = gdr_prefill_workspace_bytes(dims, n_seqs, t_total);
+    if (need > kStaticWorkspaceBytes) return GDR_ERR_UNSUPPORTED;
+    void *ws = nullptr;
+    if (need > 0) {
+        ws = static_workspace();
+        if (!ws) return GDR_ERR_CUDA;
+    }
+    return gdr_prefill_chunked(dims, n_seqs, cu_seqlens, t_total, q, k, v, g, beta, state, o, ws, need, stream);
 }
 
 gdr_status gdr_decode_step(const gdr_dims *dims, int32_t batch, const void *q, const void *k,

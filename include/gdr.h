@@ -139,6 +139,25 @@ gdr_status gdr_prefill_chunked(const gdr_dims *dims, int32_t n_seqs, const int32
                                void *workspace, size_t workspace_bytes, gdr_stream_t stream);
 
 /*
+ * gdr_prefill_chunked without a caller workspace and without any allocation:
+ * the scratch is one fixed device array inside the library (its size is
+ * gdr_prefill_static_workspace_capacity(), 64 MiB), resolved once per device.
+ * Problems whose gdr_prefill_workspace_bytes() exceed it return
+ * GDR_ERR_UNSUPPORTED before anything is launched (about 100 chunk positions
+ * of 32 V heads: e.g. up to ~6.5K tokens of Qwen3.5-9B heads).  All calls on a
+ * device share that array, so calls on different streams must not overlap
+ * (order them on one stream, or synchronise); everything else, arguments
+ * and results, is as in gdr_prefill_chunked.
+ */
+gdr_status gdr_prefill_chunked_static(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens,
+                                      int64_t t_total, const void *q, const void *k, const void *v,
+                                      const float *g, const float *beta, float *state, void *o,
+                                      gdr_stream_t stream);
+
+/* Bytes of the fixed scratch array used by gdr_prefill_chunked_static. */
+size_t gdr_prefill_static_workspace_capacity(void);
+
+/*
  * One decode step for `batch` independent sequences (one token each).
  *
  * For each sequence b and V head h, with S = state[b][h] and d = exp(g):

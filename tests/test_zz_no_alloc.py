@@ -1,0 +1,43 @@
+"""gdr_prefill_chunked_static: the prefill with the library's fixed scratch array.
+
+Checked against gdr_prefill_chunked (caller workspace) on the same inputs, two
+calls in a row each (the second continues from the first's state), and its
+size limit checked on the host."""
+
+import ctypes
+
+import numpy as np
+import pytest
+
+import gated_deltanet_scan_gb300 as gdr
+from gated_deltanet_scan_gb300 import synth
+from tests import gpu_util as gu
+
+
+def test_static_entry_rejects_oversize_before_launch():
+    L = gdr.lib()
+    cap = L.gdr_prefill_static_workspace_capacity()
+    assert cap == 64 << 20
+    d = gdr.gdr_dims(h_qk=16, h_v=32, d_k=128, d_v=128, chunk=64, in_dtype=gdr.GDR_BF16,
+                     out_dtype=gdr.GDR_F32, scale=1.0)
+    big_t = 1 << 20
+    assert L.gdr_prefill_workspace_bytes(ctypes.byref(d), 1, big_t) > cap
+    A = 0x100000  # aligned stand-in addresses: nothing is dereferenced on this path
+    st = L.gdr_prefill_chunked_static(ctypes.byref(d), 1, A, big_t, A, A, A, A, A, A, A, None)
+    assert st == gdr.GDR_ERR_UNSUPPORTED
+
+
+@pytest.mark.gpu
+def test_static_entry_matches_workspace_entry_twice():
+    torch = gu.require_gpu()
+    w = synth.make_workload("no_alloc", [300, 77, 0, 129], 16, 32, 128, 64, "bf16", seed=71, state_std=0.02)
+    x = gu.dev_inputs(w)
+    s_ws, s_st = x["state"].clone(), x["state"].clone()
+    for _ in range(2):  # two calls in a row: the second starts from the first's state
+        o_ws, o_st = gu.out_like(x["v"], "f32"), gu.out_like(x["v"], "f32")
+        gdr.gdr_prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], s_ws, o_ws, x["cu_seqlens"])
+        gdr.gdr_prefill_chunked_static(x["q"], x["k"], x["v"], x["g"], x["beta"], s_st, o_st, x["cu_seqlens"])
+        torch.cuda.synchronize()
+        assert np.array_equal(gu.to_np(o_ws), gu.to_np(o_st))
+        assert np.array_equal(gu.to_np(s_ws), gu.to_np(s_st))
+    assert gdr.gdr_device_error(device=x["q"].device) == 0
