@@ -4,7 +4,8 @@ One step = one pass of the whole path over one batch of synthetic Qwen3.5-9B
 linear-attention inputs (16 QK heads, 32 V heads, d = 128, bf16 q/k/v, fp32
 gates and state, fp32 output):
 
-  1. gdr_prefill_chunked   B = 1, T = 16384, from a N(0, 0.02) state
+  1. gdr_prefill_chunked   B = 1, T = 16384, from a N(0, 0.02) state (two launches:
+                           the per-chunk factors of all chunks, then the chunk scan)
   2. gdr_verify_block      16 draft tokens on that sequence (snapshot taken)
      gdr_state_restore     roll the state back to the snapshot
      gdr_prefill_chunked   re-feed the accepted prefix (7 tokens)
@@ -157,19 +158,27 @@ class ClockSampler:
 # our arm
 
 
-def traffic_record(kernel_file: str):
-    """dram bytes per launch from the committed ncu summary, if the kernel
-    source is unchanged since it was measured (else None)."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "gated_deltanet_scan_gb300", "csrc", kernel_file)
+PREFILL_SOURCES = ("gdr_factor.cu", "gdr_prefill_tc.cu", "gdr_factor_layout.h", "tc_ptx.cuh")
+
+
+def prefill_source_digest():
+    h = hashlib.sha256()
+    for name in PREFILL_SOURCES:
+        with open(os.path.join(ROOT, "gated_deltanet_scan_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record():
+    """DRAM bytes of one T = 16384 prefill (both launches) from the committed ncu
+    summary, if the kernel sources are unchanged since it was measured (else None)."""
     try:
-        with open(path) as f:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)
-        with open(src, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()[:16]
+        digest = prefill_source_digest()
     except (OSError, ValueError):
         return None
-    r = rec.get(kernel_file)
+    r = rec.get("prefill_T16384")
     if not r or r.get("source_sha256_16") != digest:
         return None
     return r.get("dram_bytes_per_launch")
@@ -204,6 +213,9 @@ def run_ours(args):
     cu_pre = torch.tensor([0, T_PREFILL], dtype=torch.int32, device=dev)
     cu_acc = torch.tensor([0, N_ACCEPT], dtype=torch.int32, device=dev)
     acc = {k: t[:N_ACCEPT] for k, t in dv.items()}
+    # the prefill's factor workspace, allocated once (the re-feed needs less)
+    ws_bytes = gdr.gdr_prefill_workspace_bytes(dp["q"], dp["v"], o_pre, 1, T_PREFILL)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
     only = args.only
@@ -213,7 +225,7 @@ def run_ours(args):
             timers[0].record(stream)
         if only in ("all", "prefill"):
             gdr.gdr_prefill_chunked(dp["q"], dp["k"], dp["v"], dp["g"], dp["beta"], state, o_pre, cu_pre,
-                                    chunk=64, stream=stream)
+                                    chunk=64, workspace=ws, stream=stream)
         if timers is not None:
             timers[1].record(stream)
         if only in ("all", "verify"):
@@ -221,7 +233,7 @@ def run_ours(args):
                                  N_VERIFY, stream=stream)
             gdr.gdr_state_restore(snap, state, stream=stream)
             gdr.gdr_prefill_chunked(acc["q"], acc["k"], acc["v"], acc["g"], acc["beta"], state, o_ref,
-                                    cu_acc, chunk=64, stream=stream)
+                                    cu_acc, chunk=64, workspace=ws, stream=stream)
         if timers is not None:
             timers[2].record(stream)
         if only in ("all", "decode"):
@@ -229,7 +241,8 @@ def run_ours(args):
         if timers is not None:
             timers[3].record(stream)
 
-    launches_per_step = {"all": 5, "prefill": 1, "verify": 3, "decode": 1}[only]
+    # prefill: factor + chunk-scan launches; verify: verify, restore, re-feed (2)
+    launches_per_step = {"all": 7, "prefill": 2, "verify": 4, "decode": 1}[only]
 
     def barrier():
         if world > 1:
@@ -304,7 +317,7 @@ def run_ours(args):
     pre_tflops = PREFILL_FLOP_PER_TOKEN * T_PREFILL / (prefill_ms * 1e-3) / 1e12
     dec_bytes = B_DECODE * DECODE_BYTES_PER_SEQ
     dec_gbs = dec_bytes / (decode_ms * 1e-3) / 1e9
-    traffic = traffic_record("gdr_prefill_tc.cu")
+    traffic = traffic_record() if T_PREFILL == 16384 else None  # counters are for T = 16384
     value = world * TOKENS_PER_STEP / (ms_step * 1e-3)
     line = {
         "metric": METRIC,
@@ -337,7 +350,7 @@ def run_ours(args):
                            "hbm_gbs": dec_gbs, "frac_hbm": dec_gbs / hbm},
         },
         "roofline": {
-            "kernel": "prefill_tc_kernel",
+            "kernel": "prefill (factor_kernel + prefill_tc_kernel launches of one gdr_prefill_chunked call)",
             "bound": "hbm",
             "achieved": pre_gbs,
             "peak": hbm,
@@ -354,7 +367,12 @@ def run_ours(args):
     }
     if only != "all":
         line["partial_step"] = only  # a profiling run of one component, not a bench line
+        line["prefill_tokens"] = T_PREFILL
         line.pop("e2e")
+        keep = {"prefill": "prefill_T16384", "verify": "verify16_restore_refeed7", "decode": "decode_B64"}[only]
+        line["components"] = {keep: line["components"][keep]}
+        if only != "prefill":
+            line.pop("roofline")
     elif not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(pre, ver, dec)
     return line
@@ -443,9 +461,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["all", "prefill", "verify", "decode"], default="all",
                     help="run one component of the step (for profiling); the default runs the full step")
+    ap.add_argument("--prefill-tokens", type=int, default=T_PREFILL,
+                    help="prefill length of a profiling run (with --only prefill); not a bench line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.prefill_tokens != T_PREFILL:
+        if args.only != "prefill" or args.prefill_tokens <= 0:
+            ap.error("--prefill-tokens is for profiling runs with --only prefill")
+        globals()["T_PREFILL"] = args.prefill_tokens
     line = run_ours(args) if args.impl == "ours" else run_reference(args)
     if line is not None:
         print(json.dumps(line), flush=True)
