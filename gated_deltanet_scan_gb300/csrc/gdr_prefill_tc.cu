@@ -19,13 +19,16 @@
 // issue each), so each B operand carries its bf16 hi and lo halves side by side
 // (N = 64) and the partial products are summed when the accumulator is read:
 // every product that feeds the state keeps ~2^-16 relative precision with
-// 8 + 8 + 4 MMAs per chunk, issued by two threads in parallel.
+// 8 + 8 + 4 MMAs per chunk, all issued by one thread into one accumulator per
+// group (more issuing threads, each with its own accumulator, measured slower:
+// the readers' extra TMEM loads and sums cost more than the issue they save).
 //
 // Warp roles (384 threads).  Warps 0-7, the "chain": warp w owns TMEM lanes
 // 32 (w % 4) .. + 31 (state rows, or chunk rows: K/T rows in lanes 0-63, Q/PT
 // rows in lanes 64-127) and columns 16 (w / 4) .. + 15 of the CTA's 32.  Only
 // warps of lanes 0-63 sit on the chunk-to-chunk path between MMA1 and MMA3;
-// the others form the outputs meanwhile.  Warps 8-11, the "loader": one
+// the others form the outputs meanwhile, and lane 0 of warp 2 issues every
+// MMA (so no K/T-row warp ever waits behind an MMA issue).  Warps 8-11, the "loader": one
 // thread issues the TMA loads (K, Q and V tiles three chunks deep, factor
 // slots two deep); all four unpack a chunk's packed fp32 [T; PT] into the
 // bf16 hi/lo operand tiles while the chain runs the chunk before.  Every
@@ -96,14 +99,14 @@ constexpr int NBARS = B_MMA3 + 1;
 static_assert(NBARS * 8 <= 192, "barrier space");
 
 // TMEM columns (fp32 accumulators, lane = row).  Each holds [hi-part | lo-part]
-// products in columns [0, 32) and [32, 64).  Two threads issue each MMA group
-// (MMAs from one thread issue about one per 50 cycles), each into its own
-// accumulator; readers add the two.
-constexpr uint32_t TM_KS0 = 0, TM_KS1 = 64;   // [K S; Q S], k-steps 0-3 / 4-7
-constexpr uint32_t TM_A = 128, TM_B = 192;    // [T; PT]_hi R / [T; PT]_lo R
-constexpr uint32_t TM_Y0 = 256, TM_Y1 = 320;  // Kᵀ D~, token k-steps 0-1 / 2-3
-constexpr uint32_t TM_COLS = 512;
-constexpr int NISSUE = 2;  // MMA-issuing threads: tid 0 (warp 0) and tid 32 (warp 1)
+// products of a thread's 16 columns in 32 consecutive columns; readers add the
+// two halves.
+constexpr uint32_t TM_KS = 0;    // [K S; Q S]
+constexpr uint32_t TM_D = 64;    // [D; P D] = [T; PT]_hi R + [T; PT]_lo R
+constexpr uint32_t TM_Y = 128;   // Kᵀ D~
+constexpr uint32_t TM_COLS = 256;  // allocation (a power of two)
+constexpr int ISSUE_WARP = 2;          // lane 0 issues every MMA; a Q / PT-row warp (TMEM lanes 64-95)
+constexpr int NLOW_SYNC = NLOW + 32;  // BAR_LOW: the K / T-row threads and the issuing warp
 
 constexpr uint32_t KQV_TX = 2 * 16384 + V_BYTES;
 constexpr long long kWaitLimit = 4000000000LL;  // SM clocks (about 2 s)
@@ -163,39 +166,13 @@ __device__ bool wait_or_abort(const Ctx &x, uint32_t bar, uint32_t parity) {
     }
 }
 
-// Two 32-column TMEM loads of this thread's lane, one wait.
-__device__ __forceinline__ void tmem_ld32x2(uint32_t a0, uint32_t a1, uint32_t *r) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
-        " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
-        " {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
-          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-          "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]),
-          "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]),
-          "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]),
-          "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]),
-          "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-        : "r"(a0), "r"(a1)
-        : "memory");
-}
-
-// This thread's 16 columns (group g = j0 / 16) of two accumulators, each holding
-// [hi-part | lo-part] of those columns in TMEM columns [32 g, 32 g + 32),
-// summed: two TMEM loads, one wait.
-__device__ __forceinline__ void acc_sum2(uint32_t lanebase, uint32_t c0, uint32_t c1, int j0, float *out) {
-    uint32_t r[64];
-    tmem_ld32x2(lanebase + c0 + 2 * j0, lanebase + c1 + 2 * j0, r);
+// This thread's 16 columns of one accumulator ([hi-part | lo-part] in TMEM
+// columns [32 g, 32 g + 32)), summed: one TMEM load.
+__device__ __forceinline__ void acc_sum1(uint32_t lanebase, uint32_t c0, int j0, float *out) {
+    float r[32];
+    tmem_ld32(lanebase + c0 + 2 * j0, r);
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-        out[j] = (__uint_as_float(r[j]) + __uint_as_float(r[16 + j])) +
-                 (__uint_as_float(r[32 + j]) + __uint_as_float(r[48 + j]));
+    for (int j = 0; j < 16; ++j) out[j] = r[j] + r[16 + j];
 }
 
 // Columns j0 .. j0+15 of row `row` of an N = 64 MN-major B operand with
@@ -304,10 +281,29 @@ __device__ void loader_role(const Ctx &x, const TcParams &p, int64_t t0, int nch
     }
 }
 
+// Row t of chunk c0 of the output (16 columns at j0 of the CTA's block).
+__device__ __forceinline__ void store_out_row(const TcParams &p, int64_t c0, int t, int h, int cb, int j0,
+                                              const float *ov) {
+    const size_t off = ((size_t)(c0 + t) * p.h_v + h) * D + cb * BV + j0;
+    if (p.out_bf16) {
+        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + off);
+#pragma unroll
+        for (int j = 0; j < 16; j += 8)
+            dst[j / 8] = make_uint4(pack_bf16x2(ov[j], ov[j + 1]), pack_bf16x2(ov[j + 2], ov[j + 3]),
+                                    pack_bf16x2(ov[j + 4], ov[j + 5]), pack_bf16x2(ov[j + 6], ov[j + 7]));
+    } else {
+        float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + off);
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) dst[j / 4] = make_float4(ov[j], ov[j + 1], ov[j + 2], ov[j + 3]);
+    }
+}
+
 // ================================= chain ============================================
-// MMAs of each group are split between two issuing threads (tid 0, tid 32),
-// each into its own accumulator and each committing to the group's barrier
-// (count 2).
+// One thread, lane 0 of warp 2, issues every MMA.  That warp holds Q / PT rows,
+// which are off the chunk-to-chunk path: the K / T-row warps never wait behind
+// an MMA issue, and the issuing warp joins the K / T-row barrier (BAR_LOW) that
+// hands it R and D~.  It stores a chunk's outputs only after the next chunk's
+// MMA1 has been issued (global stores ahead of it delay the issue).
 __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t t1, int nchunks, int h,
                            int cb, float *Sr, int tid, bool &ok) {
     const int warp = tid >> 5, lane = tid & 31;
@@ -315,45 +311,50 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
     const int row = ((warp & 3) << 5) + lane;  // TMEM lane
     const bool low = row < 64;                 // K / T rows (on the chunk-to-chunk path)
     const int t = row & 63;
-    const bool issuer = (tid & 31) == 0 && warp < NISSUE;
-    const int part = warp;                     // issuer 0 or 1
+    const bool iwarp = warp == ISSUE_WARP;     // joins BAR_LOW
+    const bool issuer = iwarp && lane == 0;
     const uint32_t lb = lane_base(x.tmem, warp);
     const uint32_t tmem = x.tmem;
     const uint64_t dS = smem_desc(x.sbase + OFF_S, 8192, 1024, kSwizzle128);
     const uint64_t dR = smem_desc(x.sbase + OFF_R, 8192, 1024, kSwizzle128);
     const uint64_t dDT = smem_desc(x.sbase + OFF_DT, 8192, 1024, kSwizzle128);
-    const uint64_t dA = smem_desc_sw128(x.sbase + (part == 0 ? OFF_ATP : OFF_ATP_LO), 16, 1024);
+    const uint64_t dAh = smem_desc_sw128(x.sbase + OFF_ATP, 16, 1024);
+    const uint64_t dAl = smem_desc_sw128(x.sbase + OFF_ATP_LO, 16, 1024);
     bool bad = false;
+    float ov[16];      // lanes 64-127: a chunk's outputs, stored after its last barrier
+    int64_t ov_c0 = 0; // first token of the chunk whose outputs ov holds
+    int ov_len = 0;    // its number of real rows (0: nothing pending)
+    bool kq_ready = false;  // issuers: this chunk's K/Q/V tiles were waited for before the last barrier
     for (int c = 0; c < nchunks; ++c) {
         const int kb = c % NKQ, fb = c % NF;
         const int64_t c0 = t0 + (int64_t)c * C;
         const int L = (int)((t1 - c0) < C ? (t1 - c0) : C);
         const uint32_t kq = x.sbase + OFF_KQ + kb * KQ_BYTES;
-        bad = !wait_or_abort(x, x.bar(B_KQ_FULL + kb), (uint32_t)(c / NKQ) & 1u);
-        // ---- MMA1: [K S; Q S] = [K; Q] [S_hi | S_lo], k-steps 4 part .. 4 part + 3 --------
+        const uint32_t par = (uint32_t)c & 1u;
+        if (!kq_ready) bad = !wait_or_abort(x, x.bar(B_KQ_FULL + kb), (uint32_t)(c / NKQ) & 1u);  // K/T rows read V
+        kq_ready = false;
+        // ---- MMA1: [K S; Q S] = [K; Q] [S_hi | S_lo], 8 k-steps over d_k ----------------
         if (issuer && !bad) {
             tc_fence_after_sync();
             const uint64_t a0 = smem_desc_sw128(kq, 16, 1024);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int ks = 4 * part + i;
-                mma_bf16(tmem + (part ? TM_KS1 : TM_KS0), desc_add(a0, (ks >> 2) * 16384 + (ks & 3) * 32),
-                         desc_add(dS, ks * 2048), IDESC_N64, i > 0);
-            }
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(tmem + TM_KS, desc_add(a0, (ks >> 2) * 16384 + (ks & 3) * 32), desc_add(dS, ks * 2048),
+                         IDESC_N64, ks > 0);
             mma_commit(x.bar(B_MMA1));
         }
+        if (iwarp && t < ov_len) store_out_row(p, ov_c0, t, h, cb, j0, ov);
         if (!bad) bad = !wait_or_abort(x, x.bar(B_F_FULL + fb), (uint32_t)(c / NF) & 1u);
         const float *gts = x.fslot(fb) + fac::OFF_G;  // G log2(e), beta, exp(G)
         const float Gt = gts[t], bt = gts[64 + t], egt = gts[128 + t];
         const float GC = gts[C - 1], eGC = gts[128 + C - 1];
-        if (issuer && !bad) bad = !wait_or_abort(x, x.bar(B_ATP_FULL), (uint32_t)c & 1u);
-        const uint32_t par = (uint32_t)c & 1u;
+        if (issuer && !bad) bad = !wait_or_abort(x, x.bar(B_ATP_FULL), par);
         if (!bad) bad = !wait_or_abort(x, x.bar(B_MMA1), par);
         tc_fence_after_sync();
         float qse[16];  // lanes 64-127: e^G Q S, kept for the output
         {
             float ks[16];
-            if (!bad) acc_sum2(lb, TM_KS0, TM_KS1, j0, ks);
+            if (!bad) acc_sum1(lb, TM_KS, j0, ks);
             if (low) {
                 if (!bad) {
                     // R = beta (V - e^G K S) as [R_hi | R_lo]
@@ -369,29 +370,30 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
                     store_hilo_row16(x.sm + OFF_R, t, j0, r);
                     fence_proxy_async_smem();
                 }
-                tc_fence_before_sync();
-                named_sync(BAR_LOW, NLOW);
-                // ---- MMA2: [D; P D] = [T; PT]_hi [R_hi | R_lo] (part 0) + [T; PT]_lo [R_hi | R_lo] (part 1)
-                if (issuer && !bad) {
-                    tc_fence_after_sync();
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16(tmem + (part ? TM_B : TM_A), desc_add(dA, ks * 32), desc_add(dR, ks * 2048),
-                                 IDESC_N64, ks > 0);
-                    mma_commit(x.bar(B_MMA2));
-                    mma_commit(x.bar(B_ATP_FREE));
-                }
             } else {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) qse[j] = egt * ks[j];
             }
         }
+        if (low || iwarp) {
+            tc_fence_before_sync();
+            named_sync(BAR_LOW, NLOW_SYNC);
+        }
+        // ---- MMA2: [D; P D] = [T; PT]_hi [R_hi | R_lo] + [T; PT]_lo [R_hi | R_lo] ---------
+        if (issuer && !bad) {
+            tc_fence_after_sync();
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(tmem + TM_D, desc_add(ks < 4 ? dAh : dAl, (ks & 3) * 32), desc_add(dR, (ks & 3) * 2048),
+                         IDESC_N64, ks > 0);
+            mma_commit(x.bar(B_MMA2));
+            mma_commit(x.bar(B_ATP_FREE));
+        }
         if (!bad) bad = !wait_or_abort(x, x.bar(B_MMA2), par);
         tc_fence_after_sync();
-        float ov[16];  // lanes 64-127: this chunk's outputs, stored after the chunk's last barrier
         {
             float d[16];
-            if (!bad) acc_sum2(lb, TM_A, TM_B, j0, d);
+            if (!bad) acc_sum1(lb, TM_D, j0, d);
             if (low) {
                 if (!bad) {
                     // D~ = exp(G_C - G_t) D as [D~_hi | D~_lo]
@@ -401,32 +403,31 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
                     store_hilo_row16(x.sm + OFF_DT, t, j0, d);
                     fence_proxy_async_smem();
                 }
-                tc_fence_before_sync();
-                named_sync(BAR_LOW, NLOW);
-                // ---- MMA3: Y = Kᵀ [D~_hi | D~_lo], token k-steps 2 part, 2 part + 1 --------
-                if (issuer && !bad) {
-                    tc_fence_after_sync();
-                    const uint64_t a0 = smem_desc_sw128(kq, 16384, 1024);
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const int ks = 2 * part + i;
-                        mma_bf16(tmem + (part ? TM_Y1 : TM_Y0), desc_add(a0, ks * 2048), desc_add(dDT, ks * 2048),
-                                 IDESC_Y, i > 0);
-                    }
-                    mma_commit(x.bar(B_MMA3));
-                }
             } else {
                 // O = scale (e^G Q S + P D)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) ov[j] = p.scale * (qse[j] + d[j]);
             }
         }
+        if (low || iwarp) {
+            tc_fence_before_sync();
+            named_sync(BAR_LOW, NLOW_SYNC);
+        }
+        // ---- MMA3: Y = Kᵀ [D~_hi | D~_lo], 4 token k-steps ------------------------------
+        if (issuer && !bad) {
+            tc_fence_after_sync();
+            const uint64_t a0 = smem_desc_sw128(kq, 16384, 1024);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16(tmem + TM_Y, desc_add(a0, ks * 2048), desc_add(dDT, ks * 2048), IDESC_Y, ks > 0);
+            mma_commit(x.bar(B_MMA3));
+        }
         if (!bad) bad = !wait_or_abort(x, x.bar(B_MMA3), par);
         tc_fence_after_sync();
         if (!bad) {
             // S <- exp(G_C) S + Kᵀ D~, and its [S_hi | S_lo] operand copy
             float y[16];
-            acc_sum2(lb, TM_Y0, TM_Y1, j0, y);
+            acc_sum1(lb, TM_Y, j0, y);
 #pragma unroll
             for (int j = 0; j < 16; ++j) Sr[j] = fmaf(eGC, Sr[j], y[j]);
             store_hilo_row16(x.sm + OFF_S, row, j0, Sr);
@@ -443,21 +444,11 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
             break;
         }
         // outputs of the chunk's real rows (after the barrier, so no proxy fence waits on them)
-        if (!low && t < L) {
-            const size_t off = ((size_t)(c0 + t) * p.h_v + h) * D + cb * BV + j0;
-            if (p.out_bf16) {
-                uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + off);
-#pragma unroll
-                for (int j = 0; j < 16; j += 8)
-                    dst[j / 8] = make_uint4(pack_bf16x2(ov[j], ov[j + 1]), pack_bf16x2(ov[j + 2], ov[j + 3]),
-                                            pack_bf16x2(ov[j + 4], ov[j + 5]), pack_bf16x2(ov[j + 6], ov[j + 7]));
-            } else {
-                float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + off);
-#pragma unroll
-                for (int j = 0; j < 16; j += 4) dst[j / 4] = make_float4(ov[j], ov[j + 1], ov[j + 2], ov[j + 3]);
-            }
-        }
+        if (!low && !iwarp && t < L) store_out_row(p, c0, t, h, cb, j0, ov);
+        ov_c0 = c0;
+        ov_len = L;
     }
+    if (!bad && iwarp && t < ov_len) store_out_row(p, ov_c0, t, h, cb, j0, ov);
     ok = !bad;
 }
 
@@ -482,7 +473,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int64_t slot0 = fac::slot_base(t0, s);
 
     if (tid == 0) {
-        for (int i = 0; i < NBARS; ++i) mbar_init(x.bar(i), (i >= B_ATP_FREE) ? NISSUE : 1);
+        for (int i = 0; i < NBARS; ++i) mbar_init(x.bar(i), 1);
         *x.abort_flag = 0;
         fence_mbar_init();
     }
