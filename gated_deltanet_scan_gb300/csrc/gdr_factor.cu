@@ -3,6 +3,11 @@
 // chunk's gates, T = (I + N)^-1 and P T into the factor workspace (layout in
 // gdr_factor_layout.h).
 //
+// What is stored is ready for the chunk scan's products: Tw = diag(exp(G_C - G)) T
+// diag(beta) and PTw = P T diag(beta) (G_C = G of the chunk's last row), so
+// that Tw (V - diag(e^G) K S) is the decay-weighted correction D~ the state
+// update needs and PTw (V - diag(e^G) K S) the intra-chunk part of the output.
+//
 // Per chunk (the chunkwise-parallel form of the Qwen3.5-9B NPU model card,
 // "How it works"; forward substitution for the unit triangular factor as in
 // the Candle PR's "Chunked GatedDeltaNet Scan"; log-space masking from its
@@ -63,8 +68,8 @@ constexpr int HEAD_B = OFF_TD + 4 * BLK_B;  // 50176
 // Shared memory, bytes from a 1024-byte aligned base.  The K/Q tile is only read
 // by the Gram MMA; once it has completed, the scratch overwrites it.
 constexpr uint32_t OFF_KQ = 0;
-constexpr uint32_t OFF_GATES = HEAD_B;           // G log2(e), beta, exp(G): 3 x 64 fp32
-constexpr uint32_t OFF_BARS = OFF_GATES + 768;  // 2 mbarriers
+constexpr uint32_t OFF_GATES = HEAD_B;           // G log2(e), beta, exp(G), exp(G_C - G): 4 x 64 fp32
+constexpr uint32_t OFF_BARS = OFF_GATES + 1024;  // 2 mbarriers
 constexpr uint32_t OFF_TMEM = OFF_BARS + 16;
 constexpr uint32_t SMEM_USED = OFF_TMEM + 16;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
@@ -180,13 +185,17 @@ __device__ __forceinline__ void chunk_gates(float g0, float g1, float b0, float 
     gates[64 + lane + 32] = b1;
     gates[128 + lane] = fast_exp2(g0);
     gates[128 + lane + 32] = fast_exp2(g1);
+    const float gc = __shfl_sync(0xffffffffu, g1, 31);  // G of the chunk's last row
+    gates[192 + lane] = fast_exp2(gc - g0);
+    gates[192 + lane + 32] = fast_exp2(gc - g1);
 }
 
 // The head's T from its N blocks, by warps wi = 0, 1 (named barrier `bar`);
 // every block is stored to the slot's packed layout as soon as it is formed.
-__device__ void solve_t(uint8_t *hs, float *slot_out, int wi, int lane, uint32_t bar) {
+__device__ void solve_t(uint8_t *hs, const float *gates, float *slot_out, int wi, int lane, uint32_t bar) {
     const int g = lane >> 2, c = lane & 3;
     float *Tout = slot_out + fac::OFF_T;
+    const float *bw = gates + 64, *rw = gates + 192;  // column weights beta, row weights exp(G_C - G)
     // ---- diagonal blocks: each warp two, lanes 0-15 / 16-31 one block, lane = column
     {
         const int I = 2 * wi + (lane >> 4), jj = lane & 15;
@@ -210,11 +219,12 @@ __device__ void solve_t(uint8_t *hs, float *slot_out, int wi, int lane, uint32_t
             const float nb = __shfl_down_sync(0xffffffffu, col[r], 1);
             if ((jj & 1) == 0) st_pair(td, r, jj >> 1, hl_pair(col[r], nb));
         }
-        // global T: row 16 I + r, column 16 I + jj (chunks up to the diagonal)
+        // global Tw: row 16 I + r, column 16 I + jj (chunks up to the diagonal)
+        const float bj = bw[16 * I + jj];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
             const int rg = 16 * I + r, cg = 16 * I + jj;
-            if ((cg >> 3) <= (rg >> 3)) Tout[fac::tri8_base(rg) + cg] = col[r];
+            if ((cg >> 3) <= (rg >> 3)) Tout[fac::tri8_base(rg) + cg] = col[r] * bj * rw[rg];
         }
     }
     named_sync(bar, 64);
@@ -237,16 +247,18 @@ __device__ void solve_t(uint8_t *hs, float *slot_out, int wi, int lane, uint32_t
                 st_pair(tt, g, 4 * h + c, hl_pair(t[h][0], t[h][1]));
                 st_pair(tt, g + 8, 4 * h + c, hl_pair(t[h][2], t[h][3]));
             }
-            // global T: Tᵀ(J, I)[m][n] = T[16 I + n][16 J + m]
+            // global Tw: Tᵀ(J, I)[m][n] = T[16 I + n][16 J + m]
+            const float b0 = bw[16 * J + g], b8 = bw[16 * J + g + 8];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int n = 8 * h + 2 * c;
                 float *r0 = Tout + fac::tri8_base(16 * I + n) + 16 * J;
                 float *r1 = Tout + fac::tri8_base(16 * I + n + 1) + 16 * J;
-                r0[g] = t[h][0];
-                r1[g] = t[h][1];
-                r0[g + 8] = t[h][2];
-                r1[g + 8] = t[h][3];
+                const float w0 = rw[16 * I + n], w1 = rw[16 * I + n + 1];
+                r0[g] = t[h][0] * b0 * w0;
+                r1[g] = t[h][1] * b0 * w1;
+                r0[g + 8] = t[h][2] * b8 * w0;
+                r1[g + 8] = t[h][3] * b8 * w1;
             }
         }
         if (d < 3) named_sync(bar, 64);
@@ -256,9 +268,10 @@ __device__ void solve_t(uint8_t *hs, float *slot_out, int wi, int lane, uint32_t
 // The head's P T from P and Tᵀ blocks, by the four warps w: block (I, J), I >= J,
 // costs I - J + 1 products; the groups {30, 00}, {20, 10}, {31, 21},
 // {32, 11, 22, 33} cost five each.
-__device__ void solve_pt(const uint8_t *hs, float *slot_out, int w, int lane) {
+__device__ void solve_pt(const uint8_t *hs, const float *gates, float *slot_out, int w, int lane) {
     const int g = lane >> 2, c = lane & 3;
     float *PTout = slot_out + fac::OFF_PT;
+    const float *bw = gates + 64;  // column weights beta
     const uint32_t blocks = w == 0 ? 0x0030u : w == 1 ? 0x1020u : w == 2 ? 0x2131u : 0x33221132u;
     const int nblk = w == 3 ? 4 : 2;
     for (int b = 0; b < nblk; ++b) {
@@ -268,16 +281,17 @@ __device__ void solve_pt(const uint8_t *hs, float *slot_out, int w, int lane) {
         zero_acc(acc);
         for (int K = J; K <= I; ++K)
             mma_acc(acc, ld_a(hs + OFF_PB + BLK_B * bi(I, K), g, c), hs + OFF_TT + BLK_B * bi(K, J), g, c);
-        // rows 16 I + g (+ 8); columns 16 J + 8 h + 2 c, + 1 (kept chunks only)
+        // rows 16 I + g (+ 8); columns 16 J + 8 h + 2 c, + 1 (kept chunks only), times beta
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int cg = 16 * J + 8 * h + 2 * c;
+            const float b0 = bw[cg], b1 = bw[cg + 1];
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
                 const int rg = 16 * I + g + 8 * hr;
                 if ((cg >> 3) <= (rg >> 3))
                     *reinterpret_cast<float2 *>(PTout + fac::tri8_base(rg) + cg) =
-                        make_float2(acc[h][2 * hr], acc[h][2 * hr + 1]);
+                        make_float2(acc[h][2 * hr] * b0, acc[h][2 * hr + 1] * b1);
             }
         }
     }
@@ -409,13 +423,13 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
     __syncthreads();
     float *slot_out = p.ws + ((size_t)slot * p.h_v + h) * fac::SLOT_FLOATS;
     if (warp < 2)
-        solve_t(sm, slot_out, warp, lane, 1);
+        solve_t(sm, gates, slot_out, warp, lane, 1);
     else if (warp == 2) {
 #pragma unroll
         for (int i = 0; i < 6; ++i) slot_out[fac::OFF_G + 32 * i + lane] = gates[32 * i + lane];
     }
     __syncthreads();
-    solve_pt(sm, slot_out, warp, lane);
+    solve_pt(sm, gates, slot_out, warp, lane);
     if (warp == 0) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, TM_COLS);

@@ -1,11 +1,12 @@
 // Layout of the per-chunk factor workspace shared by the factor kernel (writer)
 // and the tensor-core chunk scan (reader).
 //
-// One slot per (chunk, V head): the unit lower-triangular T = (I + N)^-1, the
-// lower-triangular P T and the chunk's gates, fp32:
-//   [0, 2304)      T    rows packed in 8-float chunks: row t keeps chunks
+// One slot per (chunk, V head): the lower-triangular factors
+// Tw = diag(exp(G_C - G)) (I + N)^-1 diag(beta) and PTw = P (I + N)^-1 diag(beta)
+// (G_C = G of the chunk's last row) and the chunk's gates, fp32:
+//   [0, 2304)      Tw   rows packed in 8-float chunks: row t keeps chunks
 //                        0 .. t/8 (columns 0 .. 8 (t/8) + 7, zeros right of the diagonal)
-//   [2304, 4608)   P T  same packing
+//   [2304, 4608)   PTw  same packing
 //   [4608, 4672)   G log2(e)   (inclusive running sum of g; padding rows repeat the last)
 //   [4672, 4736)   beta        (0 on padding rows)
 //   [4736, 4800)   exp(G)

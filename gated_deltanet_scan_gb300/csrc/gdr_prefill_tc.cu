@@ -1,7 +1,8 @@
 // Chunk scan of the chunked prefill on the 5th-generation tensor cores
 // (tcgen05 + TMEM + TMA): carries the state from chunk to chunk, using the
-// state-independent factors (gates, T, P T) that the factor kernel stored for
-// every chunk beforehand.
+// state-independent factors that the factor kernel stored for every chunk
+// beforehand: the gates and Tw = diag(exp(G_C - G)) T diag(beta),
+// PTw = P T diag(beta), with T = (I + N)^-1.
 //
 // Shapes: d_k = d_v = 128, 64-token chunks, bf16 q/k/v, fp32 state, fp32 or
 // bf16 output.  Four CTAs share one (sequence, V head); CTA `cb` owns state
@@ -10,10 +11,11 @@
 // memory as MMA operands) and walks the chunks in order.  Per chunk (the
 // chunkwise-parallel form of the Qwen3.5-9B NPU model card, "How it works"):
 //   MMA1  [K S; Q S] = [K; Q] S                      A = K/Q tile, B = [S_hi | S_lo]
-//   R     = diag(beta) (V - diag(e^G) K S)
-//   MMA2  [D; P D] = [T; PT] R                       A = [T; PT]_hi and _lo, B = [R_hi | R_lo]
+//   R     = V - diag(e^G) K S
+//   MMA2  [D~; P D] = [Tw; PTw] R                    A = [Tw; PTw]_hi and _lo, B = [R_hi | R_lo]
+//         (D = T diag(beta) R is the chunk's delta correction, D~ = diag(exp(G_C - G)) D)
 //   O     = scale (diag(e^G) Q S + P D)
-//   MMA3  Y = Kᵀ D~,  D~ = diag(exp(G_C - G)) D      A = Kᵀ, B = [D~_hi | D~_lo]
+//   MMA3  Y = Kᵀ D~                                  A = Kᵀ, B = [D~_hi | D~_lo]
 //   S    <- exp(G_C) S + Y
 // A tcgen05 MMA of N <= 64 costs the same as one of N = 32 (about 50 cycles of
 // issue each), so each B operand carries its bf16 hi and lo halves side by side
@@ -324,15 +326,13 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
     float ov[16];      // lanes 64-127: a chunk's outputs, stored after its last barrier
     int64_t ov_c0 = 0; // first token of the chunk whose outputs ov holds
     int ov_len = 0;    // its number of real rows (0: nothing pending)
-    bool kq_ready = false;  // issuers: this chunk's K/Q/V tiles were waited for before the last barrier
     for (int c = 0; c < nchunks; ++c) {
         const int kb = c % NKQ, fb = c % NF;
         const int64_t c0 = t0 + (int64_t)c * C;
         const int L = (int)((t1 - c0) < C ? (t1 - c0) : C);
         const uint32_t kq = x.sbase + OFF_KQ + kb * KQ_BYTES;
         const uint32_t par = (uint32_t)c & 1u;
-        if (!kq_ready) bad = !wait_or_abort(x, x.bar(B_KQ_FULL + kb), (uint32_t)(c / NKQ) & 1u);  // K/T rows read V
-        kq_ready = false;
+        bad = !wait_or_abort(x, x.bar(B_KQ_FULL + kb), (uint32_t)(c / NKQ) & 1u);
         // ---- MMA1: [K S; Q S] = [K; Q] [S_hi | S_lo], 8 k-steps over d_k ----------------
         if (issuer && !bad) {
             tc_fence_after_sync();
@@ -345,9 +345,8 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
         }
         if (iwarp && t < ov_len) store_out_row(p, ov_c0, t, h, cb, j0, ov);
         if (!bad) bad = !wait_or_abort(x, x.bar(B_F_FULL + fb), (uint32_t)(c / NF) & 1u);
-        const float *gts = x.fslot(fb) + fac::OFF_G;  // G log2(e), beta, exp(G)
-        const float Gt = gts[t], bt = gts[64 + t], egt = gts[128 + t];
-        const float GC = gts[C - 1], eGC = gts[128 + C - 1];
+        const float *egs = x.fslot(fb) + fac::OFF_EG;  // exp(G)
+        const float egt = egs[t], eGC = egs[C - 1];
         if (issuer && !bad) bad = !wait_or_abort(x, x.bar(B_ATP_FULL), par);
         if (!bad) bad = !wait_or_abort(x, x.bar(B_MMA1), par);
         tc_fence_after_sync();
@@ -357,7 +356,7 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
             if (!bad) acc_sum1(lb, TM_KS, j0, ks);
             if (low) {
                 if (!bad) {
-                    // R = beta (V - e^G K S) as [R_hi | R_lo]
+                    // R = V - e^G K S as [R_hi | R_lo]
                     const uint8_t *vt = x.sm + OFF_V + kb * V_BYTES;
                     float r[16];
 #pragma unroll
@@ -365,7 +364,7 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
                         float v[8];
                         load_bf16_chunk64(vt, t, (j0 >> 3) + ch, v);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) r[8 * ch + e] = bt * (v[e] - egt * ks[8 * ch + e]);
+                        for (int e = 0; e < 8; ++e) r[8 * ch + e] = fmaf(-egt, ks[8 * ch + e], v[e]);
                     }
                     store_hilo_row16(x.sm + OFF_R, t, j0, r);
                     fence_proxy_async_smem();
@@ -379,7 +378,7 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
             tc_fence_before_sync();
             named_sync(BAR_LOW, NLOW_SYNC);
         }
-        // ---- MMA2: [D; P D] = [T; PT]_hi [R_hi | R_lo] + [T; PT]_lo [R_hi | R_lo] ---------
+        // ---- MMA2: [D~; P D] = [Tw; PTw]_hi [R_hi | R_lo] + [Tw; PTw]_lo [R_hi | R_lo] -----
         if (issuer && !bad) {
             tc_fence_after_sync();
 #pragma unroll
@@ -396,10 +395,7 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
             if (!bad) acc_sum1(lb, TM_D, j0, d);
             if (low) {
                 if (!bad) {
-                    // D~ = exp(G_C - G_t) D as [D~_hi | D~_lo]
-                    const float sc = fast_exp2(GC - Gt);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) d[j] *= sc;
+                    // D~ as [D~_hi | D~_lo]
                     store_hilo_row16(x.sm + OFF_DT, t, j0, d);
                     fence_proxy_async_smem();
                 }

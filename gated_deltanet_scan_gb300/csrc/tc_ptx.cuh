@@ -26,11 +26,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
-    // acquire at cluster scope (producers may live in the peer CTA); the hint
-    // lets the hardware park the thread up to ~8 us instead of re-polling
+    // acquire at CTA scope (every producer is in this CTA: its threads, its
+    // MMAs, or bulk copies into its own shared memory); the hint lets the
+    // hardware park the thread up to ~8 us instead of re-polling
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity), "r"(8192u)
