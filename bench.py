@@ -6,13 +6,14 @@ gates and state, fp32 output):
 
   1. gdr_prefill_chunked   B = 1, T = 16384, from a N(0, 0.02) state (two launches:
                            the per-chunk factors of all chunks, then the chunk scan)
-  2. gdr_verify_block      16 draft tokens on that sequence (snapshot taken)
-     gdr_state_restore     roll the state back to the snapshot
-     gdr_prefill_chunked   re-feed the accepted prefix (7 tokens)
+  2. gdr_verify_block      16 draft tokens on that sequence (snapshot taken, each
+                           token's correction kept)
+     gdr_verify_commit     the state after the accepted prefix (7 tokens), formed
+                           from the snapshot and the kept corrections
   3. gdr_decode_step       B = 64 independent sequences, one token each
 
 tokens/s counts the 16384 prefill, 16 verify and 64 decode tokens of a step
-(re-fed tokens are recomputation and are not counted).  Inputs are resident in
+(the committed prefix is not counted again).  Inputs are resident in
 HBM before the timed region; per step they exceed L2 (q, k, v, o and the decode
 state are > 600 MB), so no flush is needed.
 
@@ -208,12 +209,11 @@ def run_ours(args):
     dstate = torch.from_numpy(np.ascontiguousarray(dec.state0)).to(dev)
     o_pre = torch.empty((T_PREFILL, H_V, D), dtype=torch.float32, device=dev)
     o_ver = torch.empty((N_VERIFY, H_V, D), dtype=torch.float32, device=dev)
-    o_ref = torch.empty((N_ACCEPT, H_V, D), dtype=torch.float32, device=dev)
+    deltas = torch.empty((N_VERIFY, H_V, D), dtype=torch.float32, device=dev)
     o_dec = torch.empty((B_DECODE, H_V, D), dtype=torch.float32, device=dev)
     cu_pre = torch.tensor([0, T_PREFILL], dtype=torch.int32, device=dev)
-    cu_acc = torch.tensor([0, N_ACCEPT], dtype=torch.int32, device=dev)
-    acc = {k: t[:N_ACCEPT] for k, t in dv.items()}
-    # the prefill's factor workspace, allocated once (the re-feed needs less)
+    accepted = torch.tensor([N_ACCEPT], dtype=torch.int32, device=dev)
+    # the prefill's factor workspace, allocated once
     ws_bytes = gdr.gdr_prefill_workspace_bytes(dp["q"], dp["v"], o_pre, 1, T_PREFILL)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)
@@ -230,10 +230,8 @@ def run_ours(args):
             timers[1].record(stream)
         if only in ("all", "verify"):
             gdr.gdr_verify_block(dv["q"], dv["k"], dv["v"], dv["g"], dv["beta"], state, snap, o_ver,
-                                 N_VERIFY, stream=stream)
-            gdr.gdr_state_restore(snap, state, stream=stream)
-            gdr.gdr_prefill_chunked(acc["q"], acc["k"], acc["v"], acc["g"], acc["beta"], state, o_ref,
-                                    cu_acc, chunk=64, workspace=ws, stream=stream)
+                                 N_VERIFY, deltas=deltas, stream=stream)
+            gdr.gdr_verify_commit(dv["k"], dv["g"], deltas, snap, state, accepted, N_VERIFY, stream=stream)
         if timers is not None:
             timers[2].record(stream)
         if only in ("all", "decode"):
@@ -241,8 +239,8 @@ def run_ours(args):
         if timers is not None:
             timers[3].record(stream)
 
-    # prefill: factor + chunk-scan launches; verify: verify, restore, re-feed (2)
-    launches_per_step = {"all": 7, "prefill": 2, "verify": 4, "decode": 1}[only]
+    # prefill: factor + chunk-scan launches; verify: the block and the commit
+    launches_per_step = {"all": 5, "prefill": 2, "verify": 2, "decode": 1}[only]
 
     def barrier():
         if world > 1:
@@ -334,7 +332,7 @@ def run_ours(args):
         "data": "synthetic (seeded SplitMix64; Qwen3.5-9B linear-attention shapes)",
         "config": {
             "workload": "gated delta rule, Qwen3.5-9B layer: prefill B=1 T=16384 + 16-token verify "
-                        "with snapshot/restore/re-feed of 7 + decode step B=64",
+                        "with snapshot and commit of 7 accepted tokens + decode step B=64",
             "h_qk": H_QK, "h_v": H_V, "d_k": D, "d_v": D, "chunk": 64,
             "io": "q/k/v bf16, g/beta fp32, state fp32, o fp32",
             "tokens_per_step": TOKENS_PER_STEP,
@@ -345,7 +343,7 @@ def run_ours(args):
             "prefill_T16384": {"ms": prefill_ms, "tokens_per_s": T_PREFILL / (prefill_ms * 1e-3),
                                "hbm_gbs": pre_gbs, "frac_hbm": pre_gbs / hbm,
                                "alg_tflops": pre_tflops, "frac_bf16": pre_tflops / bf16},
-            "verify16_restore_refeed7": {"ms": verify_ms},
+            "verify16_commit7": {"ms": verify_ms},
             "decode_B64": {"ms": decode_ms, "tokens_per_s": B_DECODE / (decode_ms * 1e-3),
                            "hbm_gbs": dec_gbs, "frac_hbm": dec_gbs / hbm},
         },
@@ -369,7 +367,7 @@ def run_ours(args):
         line["partial_step"] = only  # a profiling run of one component, not a bench line
         line["prefill_tokens"] = T_PREFILL
         line.pop("e2e")
-        keep = {"prefill": "prefill_T16384", "verify": "verify16_restore_refeed7", "decode": "decode_B64"}[only]
+        keep = {"prefill": "prefill_T16384", "verify": "verify16_commit7", "decode": "decode_B64"}[only]
         line["components"] = {keep: line["components"][keep]}
         if only != "prefill":
             line.pop("roofline")
@@ -420,7 +418,7 @@ def cpu_baseline_sample(pre, ver, dec, min_seconds=10.0, max_seconds=30.0):
         n += 1
     value = n * TOKENS_PER_STEP / secs
     return {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"{n} full step(s) (prefill T=16384 + verify 16 + re-feed 7 + decode B=64, all 32 V "
+            "sample": f"{n} full step(s) (prefill T=16384 + verify 16 + accepted prefix 7 + decode B=64, all 32 V "
                       f"heads), {secs:.1f} s of fp64 CPU work on {threads} threads"}
 
 
@@ -445,7 +443,7 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same inputs as the GPU arm)",
         "config": {"workload": "gated delta rule, Qwen3.5-9B layer: prefill B=1 T=16384 + 16-token verify "
-                               "with snapshot/restore/re-feed of 7 + decode step B=64",
+                               "with snapshot and commit of 7 accepted tokens + decode step B=64",
                    "h_qk": H_QK, "h_v": H_V, "d_k": D, "d_v": D},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

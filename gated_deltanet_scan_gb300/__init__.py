@@ -16,7 +16,7 @@ from typing import Optional
 __all__ = [
     "GdrError", "gdr_dims", "lib", "library_path",
     "gdr_prefill_chunked", "gdr_prefill_workspace_bytes", "gdr_prefill_chunked_static",
-    "gdr_decode_step", "gdr_verify_block",
+    "gdr_decode_step", "gdr_verify_block", "gdr_verify_commit",
     "gdr_state_snapshot", "gdr_state_restore", "gdr_device_error", "gdr_status_string",
     "GDR_F32", "GDR_BF16",
 ]
@@ -62,7 +62,9 @@ _SIGS = {
     "gdr_decode_step": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P],
                         ctypes.c_int),
     "gdr_verify_block": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, ctypes.c_int32,
-                          _P, _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+                          _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "gdr_verify_commit": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, ctypes.c_int32,
+                           _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "gdr_state_snapshot": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, _P, _P], ctypes.c_int),
     "gdr_state_restore": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, _P, _P], ctypes.c_int),
     "gdr_device_error": ([_P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
@@ -194,16 +196,31 @@ def gdr_decode_step(q, k, v, g, beta, state, o, *, scale: float = 1.0, stream=No
     _check(st, "gdr_decode_step")
 
 
-def gdr_verify_block(q, k, v, g, beta, state, snapshot, o, n_tok: int, *, scale: float = 1.0,
+def gdr_verify_block(q, k, v, g, beta, state, snapshot, o, n_tok: int, *, deltas=None, scale: float = 1.0,
                      stream=None) -> None:
     """n_tok (<= 16) draft tokens per sequence from the current state; the incoming
-    state is copied to ``snapshot``.  Token rows are [n_seqs * n_tok, ...]."""
+    state is copied to ``snapshot``.  Token rows are [n_seqs * n_tok, ...].  With
+    ``deltas`` (fp32, shaped like v) each token's correction is kept for
+    gdr_verify_commit."""
     dims = make_dims(q, v, o, 16, scale)
     n = state.shape[0]
     st = lib().gdr_verify_block(
         ctypes.byref(dims), n, int(n_tok), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-        _ptr(state), _ptr(snapshot), _ptr(o), _stream_handle(stream, state.device))
+        _ptr(state), _ptr(snapshot), _ptr(o), _ptr(deltas), _stream_handle(stream, state.device))
     _check(st, "gdr_verify_block")
+
+
+def gdr_verify_commit(k, g, deltas, snapshot, state, accepted, n_tok: int, *, stream=None) -> None:
+    """State after the accepted prefix of a verify block: accepted (int32 device
+    tensor [n_seqs]) tokens per sequence, from the block's ``deltas`` and the
+    ``snapshot`` it took; writes ``state``."""
+    n, hv, dk, dv = state.shape
+    dims = gdr_dims(h_qk=k.shape[1], h_v=hv, d_k=dk, d_v=dv, chunk=16,
+                    in_dtype=_dtype_code(k), out_dtype=GDR_F32, scale=1.0)
+    st = lib().gdr_verify_commit(
+        ctypes.byref(dims), n, int(n_tok), _ptr(accepted), _ptr(k), _ptr(g), _ptr(deltas),
+        _ptr(snapshot), _ptr(state), _stream_handle(stream, state.device))
+    _check(st, "gdr_verify_commit")
 
 
 def _state_dims(state) -> gdr_dims:

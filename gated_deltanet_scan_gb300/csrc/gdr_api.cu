@@ -179,7 +179,7 @@ gdr_status gdr_decode_step(const gdr_dims *dims, int32_t batch, const void *q, c
 
 gdr_status gdr_verify_block(const gdr_dims *dims, int32_t n_seqs, int32_t n_tok, const void *q,
                             const void *k, const void *v, const float *g, const float *beta,
-                            float *state, float *snapshot, void *o, gdr_stream_t stream) {
+                            float *state, float *snapshot, void *o, float *deltas, gdr_stream_t stream) {
     gdr_status st = check_dims(dims);
     if (st != GDR_OK) return st;
     if (n_seqs < 0 || n_tok < 0 || n_tok > 16) return GDR_ERR_INVALID_ARG;
@@ -187,10 +187,12 @@ gdr_status gdr_verify_block(const gdr_dims *dims, int32_t n_seqs, int32_t n_tok,
     if (!snapshot || !aligned16(snapshot) || !state || !aligned16(state)) return GDR_ERR_INVALID_ARG;
     if (snapshot == state) return GDR_ERR_INVALID_ARG;
     if (n_tok > 0 && !tensors_ok(q, k, v, g, beta, state, o)) return GDR_ERR_INVALID_ARG;
+    if (deltas && !aligned16(deltas)) return GDR_ERR_INVALID_ARG;
     Args a = make_args(dims);
     a.n_seqs = n_seqs;
     a.cu_seqlens = nullptr;
     a.fixed_len = n_tok;
+    a.deltas = deltas;
     a.t_total = (int64_t)n_seqs * n_tok;
     a.q = q;
     a.k = k;
@@ -201,6 +203,31 @@ gdr_status gdr_verify_block(const gdr_dims *dims, int32_t n_seqs, int32_t n_tok,
     a.snapshot = snapshot;
     a.o = o;
     return from_cuda(launch_chunk_cc(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gdr_status gdr_verify_commit(const gdr_dims *dims, int32_t n_seqs, int32_t n_tok, const int32_t *accepted,
+                             const void *k, const float *g, const float *deltas, const float *snapshot,
+                             float *state, gdr_stream_t stream) {
+    gdr_status st = check_dims(dims);
+    if (st != GDR_OK) return st;
+    if (n_seqs < 0 || n_tok < 0 || n_tok > 16) return GDR_ERR_INVALID_ARG;
+    if (n_seqs == 0) return GDR_OK;
+    if (!accepted || !snapshot || !state || !aligned16(snapshot) || !aligned16(state) || snapshot == state)
+        return GDR_ERR_INVALID_ARG;
+    if (n_tok > 0 && (!k || !g || !deltas || !aligned16(k) || !aligned16(g) || !aligned16(deltas)))
+        return GDR_ERR_INVALID_ARG;
+    int32_t *err = device_error_word();
+    if (!err) return GDR_ERR_CUDA;
+    Args a = make_args(dims);
+    a.n_seqs = n_seqs;
+    a.fixed_len = n_tok;
+    a.k = k;
+    a.g = g;
+    a.deltas = const_cast<float *>(deltas);
+    a.accepted = accepted;
+    a.snapshot_in = snapshot;
+    a.state = state;
+    return from_cuda(launch_commit(a, err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 static gdr_status copy_states(const gdr_dims *dims, int32_t n_seqs, const float *src, float *dst,

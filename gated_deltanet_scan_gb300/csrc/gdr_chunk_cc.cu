@@ -195,6 +195,11 @@ __global__ void __launch_bounds__(32 * CcShape<D>::SPLIT) chunk_cc_kernel(Args a
                 dcol[t] = acc;
             }
         }
+        if (a.deltas && p == 0) {  // the corrections u_t of the chunk's real rows
+#pragma unroll
+            for (int t = 0; t < C; ++t)
+                if (t < L) a.deltas[((size_t)(c0 + t) * a.h_v + h) * D + col] = dcol[t];
+        }
         if (p == 0) {
 #pragma unroll
             for (int t = 0; t < C; ++t) {

@@ -1,0 +1,111 @@
+// Verify commit: the state after the accepted prefix of a speculative-verify
+// block, formed from the block's cached corrections in one pass over the states.
+//
+// Unrolling S_t = e^{g_t} S_{t-1} + k_t u_t^T over the a accepted tokens of the
+// block (the closed form of the state after a chunk on the Qwen3.5-9B NPU model
+// card, "How it works", taken at row a - 1):
+//     S_a = e^{G_a} S_0 + sum_{j < a} e^{G_a - G_j} k_j u_j^T,
+// G_j the running sum of g inside the block (inclusive), G_a = G_{a-1}.  The
+// corrections u_j = beta_j (v_j - e^{g_j} S_{j-1}^T k_j) of the first a tokens
+// depend on no later token, so the ones the verify block computed for all
+// n_tok tokens serve every prefix: this replaces restoring the snapshot and
+// re-feeding the accepted tokens.
+//
+// Mapping.  One block of 256 threads per (sequence, V head).  Thread t owns the
+// column quad 4 (t % (D/4)) and every (256 / (D/4))-th row, so each row of the
+// state is read and written as whole coalesced lines; its quad of the weighted
+// corrections e^{G_a - G_j} u_j stays in registers and the accepted K rows sit
+// in shared memory.
+#include "gdr_common.cuh"
+#include "gdr_internal.h"
+
+namespace gdr {
+namespace {
+
+constexpr int NT = 256;
+constexpr int MAXTOK = 16;
+
+template <int D>
+__global__ void __launch_bounds__(NT) commit_kernel(Args a, int32_t *err) {
+    constexpr int Q4 = D / 4;        // column quads per row
+    constexpr int RSTEP = NT / Q4;   // rows between a thread's rows
+    __shared__ float sK[MAXTOK][D];  // k_j of the accepted tokens, fp32
+    __shared__ float sW[MAXTOK];     // e^{G_a - G_j}
+    __shared__ float sEa;            // e^{G_a}
+
+    const int h = blockIdx.x % a.h_v, s = blockIdx.x / a.h_v;
+    const int hq = h / (a.h_v / a.h_qk);
+    const int n_tok = a.fixed_len;
+    const int acc = a.accepted[s];
+    if (acc < 0 || acc > n_tok) {  // leave the state as it is and report
+        if (threadIdx.x == 0) atomicCAS(err, 0, (int32_t)GDR_ERR_INVALID_ARG);
+        return;
+    }
+    const size_t row0 = (size_t)s * n_tok;  // the block's first token row of this sequence
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        float gj = (lane < acc) ? a.g[(row0 + lane) * a.h_v + h] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_up_sync(0xffffffffu, gj, o);
+            if (lane >= o) gj += u;
+        }
+        const float Ga = __shfl_sync(0xffffffffu, gj, acc > 0 ? acc - 1 : 0);
+        if (lane < MAXTOK) sW[lane] = (lane < acc) ? __expf(Ga - gj) : 0.f;  // exponent <= 0 for g <= 0
+        if (lane == 0) sEa = acc > 0 ? __expf(Ga) : 1.f;
+    }
+    for (int e = threadIdx.x; e < acc * D; e += NT) {
+        const int j = e / D, i = e - j * D;
+        sK[j][i] = load_in(a.k, ((row0 + j) * a.h_qk + hq) * D + i, a.in_bf16);
+    }
+    __syncthreads();
+
+    const int cq = threadIdx.x % Q4, r0 = threadIdx.x / Q4;
+    float4 u[MAXTOK];
+#pragma unroll
+    for (int j = 0; j < MAXTOK; ++j) {
+        u[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j < acc) {
+            const float4 d = *reinterpret_cast<const float4 *>(a.deltas + ((row0 + j) * a.h_v + h) * D + 4 * cq);
+            const float w = sW[j];
+            u[j] = make_float4(w * d.x, w * d.y, w * d.z, w * d.w);
+        }
+    }
+    const float ea = sEa;
+    const size_t sbase = ((size_t)s * a.h_v + h) * D * D;
+    const float4 *src = reinterpret_cast<const float4 *>(a.snapshot_in + sbase);
+    float4 *dst = reinterpret_cast<float4 *>(a.state + sbase);
+#pragma unroll 4
+    for (int r = r0; r < D; r += RSTEP) {
+        float4 x = src[r * Q4 + cq];
+        x = make_float4(ea * x.x, ea * x.y, ea * x.z, ea * x.w);
+#pragma unroll
+        for (int j = 0; j < MAXTOK; ++j) {
+            if (j < acc) {
+                const float kr = sK[j][r];
+                x.x = fmaf(kr, u[j].x, x.x);
+                x.y = fmaf(kr, u[j].y, x.y);
+                x.z = fmaf(kr, u[j].z, x.z);
+                x.w = fmaf(kr, u[j].w, x.w);
+            }
+        }
+        dst[r * Q4 + cq] = x;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_commit(const Args &a, int32_t *err, cudaStream_t s) {
+    if (a.n_seqs == 0) return cudaSuccess;
+    if (a.fixed_len < 0 || a.fixed_len > MAXTOK || !err) return cudaErrorInvalidValue;
+    const unsigned blocks = (unsigned)a.n_seqs * (unsigned)a.h_v;
+    switch (a.d) {
+        case 32: commit_kernel<32><<<blocks, NT, 0, s>>>(a, err); break;
+        case 64: commit_kernel<64><<<blocks, NT, 0, s>>>(a, err); break;
+        case 128: commit_kernel<128><<<blocks, NT, 0, s>>>(a, err); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace gdr

@@ -23,6 +23,9 @@ struct Args {
     float *state;
     float *snapshot;  // optional copy of the incoming state (verify block)
     void *o;
+    float *deltas;              // optional per-token corrections u_t (verify block), fp32 like v
+    const int32_t *accepted;    // verify commit: accepted tokens per sequence (device)
+    const float *snapshot_in;   // verify commit: the state before the block
 };
 
 cudaError_t launch_decode(const Args &a, cudaStream_t s);
@@ -32,6 +35,8 @@ cudaError_t launch_chunk_cc(const Args &a, cudaStream_t s);
 cudaError_t launch_factors(const Args &a, float *ws, int32_t *err, cudaStream_t s);
 cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s);
 cudaError_t launch_copy_f32(const float *src, float *dst, size_t n, cudaStream_t s);
+// Verify commit: state = e^{G_a} snapshot + sum_{j<a} e^{G_a - G_j} k_j u_j^T per (sequence, V head).
+cudaError_t launch_commit(const Args &a, int32_t *err, cudaStream_t s);
 
 // bf16 tensor [d2][d1][d0] (d0 contiguous) as a TMA map with box {box0, 1, 64}.
 bool encode_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,

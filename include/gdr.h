@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define GDR_ABI_VERSION 2
+#define GDR_ABI_VERSION 3
 
 /* Same object as cudaStream_t; declared here so callers need no CUDA header. */
 typedef struct CUstream_st *gdr_stream_t;
@@ -180,20 +180,49 @@ gdr_status gdr_decode_step(const gdr_dims *dims, int32_t batch, const void *q, c
  * Copies state[s] to snapshot[s] (the state before the block), then runs the
  * n_tok tokens of every sequence from that state as one chunk, writing all
  * n_tok outputs and leaving the state after the whole block in state[s].
- * After choosing how many tokens a_s to accept, the caller restores the
- * snapshot (gdr_state_restore) and re-feeds the a_s accepted tokens with
- * gdr_prefill_chunked (lengths a_s, zero allowed).  This is the model card's
- * prompt-lookup decoding ("New in v2": the DeltaNet state cannot be rewound,
- * so it is snapshotted before the 16-token check and the accepted tokens are
- * re-fed).
+ * This is the model card's prompt-lookup decoding ("New in v2": the DeltaNet
+ * state cannot be rewound, so it is snapshotted before the 16-token check and
+ * the accepted tokens are re-fed).  After choosing how many tokens a_s to
+ * accept, the caller either
+ *   - restores the snapshot (gdr_state_restore) and re-feeds the a_s accepted
+ *     tokens with gdr_prefill_chunked (lengths a_s, zero allowed), or
+ *   - passes `deltas` here and commits with gdr_verify_commit, which needs no
+ *     re-feed (one pass over the states).
  *
  *   q, k [n_seqs * n_tok][H_qk][d_k]; v, o [n_seqs * n_tok][H_v][d_v];
  *   g, beta [n_seqs * n_tok][H_v]; state, snapshot [n_seqs][H_v][d_k][d_v].
  *   snapshot must not overlap state.
+ *   deltas: NULL, or fp32 [n_seqs * n_tok][H_v][d_v] that receives each draft
+ *     token's correction u_t = beta_t (v_t - e^{g_t} S_{t-1}^T k_t), where
+ *     S_{t-1} is the state just before token t inside the block.
  */
 gdr_status gdr_verify_block(const gdr_dims *dims, int32_t n_seqs, int32_t n_tok, const void *q,
                             const void *k, const void *v, const float *g, const float *beta,
-                            float *state, float *snapshot, void *o, gdr_stream_t stream);
+                            float *state, float *snapshot, void *o, float *deltas, gdr_stream_t stream);
+
+/*
+ * Commits the accepted prefix of a verify block from its cached corrections,
+ * instead of restoring the snapshot and re-feeding the accepted tokens.
+ *
+ * For sequence s with a = accepted[s] accepted tokens (rows s * n_tok + j,
+ * j < a, of the block), writes the state after those a tokens:
+ *     state[s] = e^{G_a} snapshot[s] + sum_{j < a} e^{G_a - G_j} k_j u_j^T,
+ * with G_j = g_0 + ... + g_j (within the block), G_a = G_{a-1} (G_a = 0 and
+ * state[s] = snapshot[s] when a = 0), u_j the corrections the block wrote to
+ * `deltas`.  This unrolls the recurrence over the prefix (the model card's
+ * closed form of S_T after a chunk, "How it works", taken at row a - 1): the
+ * corrections of the first a tokens do not depend on later tokens, so they
+ * are valid for every prefix.
+ *
+ *   accepted: device int32 [n_seqs], each in [0, n_tok].  A value outside
+ *     that range leaves state[s] as it is and records GDR_ERR_INVALID_ARG in
+ *     the device error word (see gdr_device_error).
+ *   k, g, deltas: the block's tensors, as passed to gdr_verify_block.
+ *   snapshot (in), state (out): [n_seqs][H_v][d_k][d_v]; must not overlap.
+ */
+gdr_status gdr_verify_commit(const gdr_dims *dims, int32_t n_seqs, int32_t n_tok, const int32_t *accepted,
+                             const void *k, const float *g, const float *deltas, const float *snapshot,
+                             float *state, gdr_stream_t stream);
 
 /* Copy n_seqs states (H_v * d_k * d_v floats each) from `state` to `snapshot`. */
 gdr_status gdr_state_snapshot(const gdr_dims *dims, int32_t n_seqs, const float *state,

@@ -118,3 +118,25 @@ def chunk_form_factored(q, k, v, g, beta, S0, C):
         S = np.exp(G[-1]) * S + K.T @ (np.exp(G[-1] - G)[:, None] * D)
         O[c0:c0 + L] = Oc[:L]
     return O, S
+
+
+def verify_deltas(k, v, g, beta, S0):
+    """Corrections u_t of one verify block (all rows real, one chunk), the rows of
+    D = (I + N)^-1 diag(beta) (V - diag(e^G) K S0) on the model card's chunk form."""
+    K, V = np.asarray(k, np.float64), np.asarray(v, np.float64)
+    G = np.cumsum(np.asarray(g, np.float64))
+    b = np.asarray(beta, np.float64)
+    n = K.shape[0]
+    N = b[:, None] * _decay_matrix(G, strict=True) * (K @ K.T)
+    return np.linalg.solve(np.eye(n) + N, b[:, None] * (V - np.exp(G)[:, None] * (K @ S0)))
+
+
+def commit_from_deltas(k, g, D, S0, a):
+    """State after the first a tokens of a block from its corrections:
+    e^{G_a} S0 + sum_{j < a} e^{G_a - G_j} k_j u_j^T, G_a = G_{a-1} (0 for a = 0)."""
+    S0 = np.asarray(S0, np.float64)
+    if a == 0:
+        return S0.copy()
+    G = np.cumsum(np.asarray(g[:a], np.float64))
+    w = np.exp(G[-1] - G)
+    return np.exp(G[-1]) * S0 + np.asarray(k[:a], np.float64).T @ (w[:, None] * np.asarray(D[:a], np.float64))

@@ -40,7 +40,7 @@ def dims(**kw):
 
 def test_every_declared_symbol_is_exported(L):
     names = declared_functions()
-    assert {"gdr_prefill_chunked", "gdr_decode_step", "gdr_verify_block",
+    assert {"gdr_prefill_chunked", "gdr_decode_step", "gdr_verify_block", "gdr_verify_commit",
             "gdr_state_snapshot", "gdr_state_restore"} <= set(names)
     for n in names:
         assert hasattr(L, n), f"{n} declared in gdr.h but not exported"
@@ -113,10 +113,28 @@ def test_decode_and_verify_reject_bad_arguments(L):
     assert dec(ctypes.byref(d), 4, A, A, A, A, A, A, MISALIGNED, None) == gdr.GDR_ERR_INVALID_ARG
     assert dec(ctypes.byref(d), 0, None, None, None, None, None, None, None, None) == gdr.GDR_OK
     ver = L.gdr_verify_block
-    assert ver(ctypes.byref(d), 2, 17, A, A, A, A, A, A, B, B, None) == gdr.GDR_ERR_INVALID_ARG
-    assert ver(ctypes.byref(d), 2, 16, A, A, A, A, A, A, A, B, None) == gdr.GDR_ERR_INVALID_ARG
-    assert ver(ctypes.byref(d), 2, 16, A, A, A, A, A, A, None, B, None) == gdr.GDR_ERR_INVALID_ARG
-    assert ver(ctypes.byref(d), -2, 16, A, A, A, A, A, A, B, B, None) == gdr.GDR_ERR_INVALID_ARG
+    assert ver(ctypes.byref(d), 2, 17, A, A, A, A, A, A, B, B, None, None) == gdr.GDR_ERR_INVALID_ARG
+    assert ver(ctypes.byref(d), 2, 16, A, A, A, A, A, A, A, B, None, None) == gdr.GDR_ERR_INVALID_ARG
+    assert ver(ctypes.byref(d), 2, 16, A, A, A, A, A, A, None, B, None, None) == gdr.GDR_ERR_INVALID_ARG
+    assert ver(ctypes.byref(d), -2, 16, A, A, A, A, A, A, B, B, None, None) == gdr.GDR_ERR_INVALID_ARG
+    assert ver(ctypes.byref(d), 2, 16, A, A, A, A, A, A, B, B, MISALIGNED, None) == gdr.GDR_ERR_INVALID_ARG
+
+
+def test_verify_commit_rejects_bad_arguments(L):
+    d = dims(chunk=16)
+    com = L.gdr_verify_commit
+    # (dims, n_seqs, n_tok, accepted, k, g, deltas, snapshot, state, stream)
+    assert com(ctypes.byref(d), 2, 17, A, A, A, A, A, B, None) == gdr.GDR_ERR_INVALID_ARG
+    assert com(ctypes.byref(d), -1, 16, A, A, A, A, A, B, None) == gdr.GDR_ERR_INVALID_ARG
+    assert com(ctypes.byref(d), 2, 16, None, A, A, A, A, B, None) == gdr.GDR_ERR_INVALID_ARG
+    assert com(ctypes.byref(d), 2, 16, A, A, A, A, A, A, None) == gdr.GDR_ERR_INVALID_ARG  # snapshot == state
+    assert com(ctypes.byref(d), 2, 16, A, A, A, None, A, B, None) == gdr.GDR_ERR_INVALID_ARG
+    assert com(ctypes.byref(d), 2, 16, A, A, A, MISALIGNED, A, B, None) == gdr.GDR_ERR_INVALID_ARG
+    assert com(ctypes.byref(d), 2, 16, A, A, A, A, MISALIGNED, B, None) == gdr.GDR_ERR_INVALID_ARG
+    assert com(ctypes.byref(gdr.gdr_dims(h_qk=16, h_v=32, d_k=96, d_v=96, chunk=16, in_dtype=gdr.GDR_BF16,
+                                         out_dtype=gdr.GDR_F32, scale=1.0)),
+               2, 16, A, A, A, A, A, B, None) != gdr.GDR_OK
+    assert com(ctypes.byref(d), 0, 16, None, None, None, None, None, None, None) == gdr.GDR_OK
 
 
 def test_snapshot_restore_reject_bad_arguments(L):

@@ -1,7 +1,8 @@
 """Packed variable-length prefill, then a 16-token verify block per sequence from
 a state snapshot, accepting a random prefix and re-feeding it (the prompt-lookup
 decoding loop of the Qwen3.5-9B NPU model card, "New in v2"), against the
-oracle's sequential result."""
+oracle's sequential result; and the same prefix committed from the block's cached
+corrections (gdr_verify_commit) instead of re-fed."""
 
 import numpy as np
 import pytest
@@ -28,8 +29,14 @@ def _verify_flow(w, n_verify=16):
     y = gu.dev_inputs(vb)
     snap = torch.empty_like(state)
     ov = gu.out_like(y["v"], "f32")
-    gdr.gdr_verify_block(y["q"], y["k"], y["v"], y["g"], y["beta"], state, snap, ov, n_verify)
+    deltas = torch.full(y["v"].shape, float("nan"), dtype=torch.float32, device="cuda")
+    gdr.gdr_verify_block(y["q"], y["k"], y["v"], y["g"], y["beta"], state, snap, ov, n_verify, deltas=deltas)
     state_after_block = state.clone()
+
+    # commit the accepted prefix from the cached corrections (no re-feed)
+    state_commit = torch.full_like(state, float("nan"))
+    acc_dev = torch.from_numpy(acc.astype(np.int32)).cuda()
+    gdr.gdr_verify_commit(y["k"], y["g"], deltas, snap, state_commit, acc_dev, n_verify)
 
     # accept a_s tokens per sequence: restore the snapshot, re-feed the accepted prefix
     gdr.gdr_state_restore(snap, state)
@@ -44,7 +51,7 @@ def _verify_flow(w, n_verify=16):
     torch.cuda.synchronize()
     assert gdr.gdr_device_error() == 0
     return (gu.to_np(o), gu.to_np(ov), gu.to_np(snap), gu.to_np(state_after_block),
-            gu.to_np(o_re), gu.to_np(state), rows, acc)
+            gu.to_np(o_re), gu.to_np(state), rows, acc, gu.to_np(state_commit))
 
 
 def _oracle_flow(w, n_verify=16):
@@ -65,7 +72,7 @@ def test_varlen_prefill_then_verify_and_refeed():
     """8 sequences, lengths ~ U{512..8192}, H 16/32, d=128, bf16; verify 16 tokens
     from the snapshot, accept a ~ U{0..16}, re-feed the accepted tokens."""
     w = synth.varlen_verify()
-    o, ov, snap, s_blk, o_re, s_final, rows, acc = _verify_flow(w)
+    o, ov, snap, s_blk, o_re, s_final, rows, acc, s_commit = _verify_flow(w)
     o_pre, S_pre, o_blk, S_blk, o_acc, S_acc = _oracle_flow(w)
     gu.check_outputs(o, o_pre)
     gu.check_state(snap, S_pre)  # snapshot holds the state before the block
@@ -76,6 +83,9 @@ def test_varlen_prefill_then_verify_and_refeed():
         # re-fed outputs equal the verify block's outputs for the accepted tokens
         assert gu.o_error(o_re, ov[rows]) < 1e-3
     gu.check_state(s_final, S_acc)
+    # committing from the cached corrections reaches the same state as the re-feed
+    gu.check_state(s_commit, S_acc)
+    assert gu.state_error(s_commit, s_final) < 1e-4
 
 
 @pytest.mark.parametrize("n_tok", [0, 1, 7, 16])
@@ -87,13 +97,46 @@ def test_verify_block_lengths(n_tok):
     x = gu.dev_inputs(w)
     snap = torch.empty_like(x["state"])
     o = gu.out_like(x["v"], "f32")
-    gdr.gdr_verify_block(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state"], snap, o, n_tok)
+    deltas = torch.zeros(x["v"].shape, dtype=torch.float32, device="cuda")
+    gdr.gdr_verify_block(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state"], snap, o, n_tok, deltas=deltas)
+    acc = np.array([0, n_tok // 2, n_tok], dtype=np.int32)
+    committed = torch.full_like(x["state"], float("nan"))
+    gdr.gdr_verify_commit(x["k"], x["g"], deltas, snap, committed, torch.from_numpy(acc).cuda(), n_tok)
     torch.cuda.synchronize()
+    assert gdr.gdr_device_error() == 0
     o_ref, S_ref = oracle.run_workload(w)
     np.testing.assert_array_equal(gu.to_np(snap), w.state0.astype(np.float64))
     if n_tok:
         gu.check_outputs(gu.to_np(o), o_ref)
     gu.check_state(gu.to_np(x["state"]), S_ref)
+    # the accepted prefixes 0, n_tok / 2 and n_tok of the three sequences
+    rows = np.concatenate([np.arange(s * n_tok, s * n_tok + acc[s]) for s in range(n)]).astype(np.int64)
+    cu = np.zeros(n + 1, dtype=np.int64)
+    cu[1:] = np.cumsum(acc)
+    _, S_acc = oracle.gdr_sequential(cu, w.q[rows], w.k[rows], w.v[rows], w.g[rows], w.beta[rows], w.state0)
+    c = gu.to_np(committed)
+    np.testing.assert_array_equal(c[0], w.state0[0].astype(np.float64))  # a = 0: the snapshot itself
+    gu.check_state(c, S_acc)
+
+
+def test_verify_commit_rejects_out_of_range_count_on_the_device():
+    """An accepted count above n_tok is reported through the device error word and
+    leaves that sequence's state as it was; the other sequences commit normally."""
+    import gated_deltanet_scan_gb300 as gdr
+    torch = gu.require_gpu()
+    n_tok = 4
+    w = synth.make_workload("vbad", [n_tok] * 2, 16, 32, 128, 16, "bf16", seed=77, state_std=0.02)
+    x = gu.dev_inputs(w)
+    snap = torch.empty_like(x["state"])
+    o = gu.out_like(x["v"], "f32")
+    deltas = torch.zeros(x["v"].shape, dtype=torch.float32, device="cuda")
+    gdr.gdr_verify_block(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state"], snap, o, n_tok, deltas=deltas)
+    target = torch.full_like(x["state"], 7.0)
+    gdr.gdr_verify_commit(x["k"], x["g"], deltas, snap, target, torch.tensor([2, n_tok + 1], dtype=torch.int32,
+                                                                             device="cuda"), n_tok)
+    assert gdr.gdr_device_error() == gdr.GDR_ERR_INVALID_ARG
+    assert bool(torch.all(target[1] == 7.0))
+    assert gdr.gdr_device_error() == 0  # read and cleared
 
 
 def test_snapshot_restore_roundtrip():

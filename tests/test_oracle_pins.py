@@ -18,7 +18,7 @@ import numpy as np
 import pytest
 
 import oracle
-from tests.chunk_form import chunk_form_factored, chunk_form_pages
+from tests.chunk_form import chunk_form_factored, chunk_form_pages, commit_from_deltas, verify_deltas
 
 
 def _rng(seed):
@@ -354,3 +354,25 @@ def test_chunk_form_strong_decay_stays_finite():
         G = np.cumsum(g[:C]).astype(np.float32)
         inv = np.exp(-G)
     assert np.isfinite(inv[12]) and not np.isfinite(inv[13])
+
+
+# --- verify commit from cached corrections ------------------------------------------
+
+
+@pytest.mark.parametrize("n_tok", [1, 7, 16])
+def test_verify_commit_from_deltas_equals_sequential_prefix(n_tok):
+    """A verify block's corrections u_t are the recurrence's own u_t = beta_t (v_t -
+    e^{g_t} S_{t-1}^T k_t), and the state formed from them for any accepted prefix a
+    (the formula gdr_verify_commit evaluates) equals the sequential state after those
+    a tokens."""
+    q, k, v, g, beta, S0 = _rand_case(200 + n_tok, T=n_tok, dk=8, dv=6)
+    D = verify_deltas(k, v, g, beta, S0)
+    S = S0.copy()
+    for t in range(n_tok):
+        u = beta[t] * (v[t] - np.exp(g[t]) * (S.T @ k[t]))
+        assert np.allclose(D[t], u, rtol=0, atol=1e-12 * max(1.0, np.abs(u).max()))
+        _, S = _single(q[t:t + 1], k[t:t + 1], v[t:t + 1], g[t:t + 1], beta[t:t + 1], S)
+    for a in range(n_tok + 1):
+        S_ref = S0 if a == 0 else _single(q[:a], k[:a], v[:a], g[:a], beta[:a], S0)[1]
+        S_c = commit_from_deltas(k, g, D, S0, a)
+        assert np.linalg.norm(S_c - S_ref) <= 1e-12 * np.linalg.norm(S_ref)
