@@ -19,7 +19,9 @@
 // d/SPLIT state rows, lane j one column; the rows sit in registers for the
 // whole sequence.  K and Q tiles are staged in shared memory and read as
 // warp-wide broadcasts, so S^T k needs no shuffles: only the SPLIT partial sums
-// of K S and Q S go through shared memory once per chunk.
+// of K S and Q S go through shared memory once per chunk (K S, then Q S, in one
+// buffer).  Every warp holds the chunk's D column, so warp p stores the outputs
+// and corrections of the tokens t = p mod SPLIT.
 #include "gdr_common.cuh"
 #include "gdr_internal.h"
 
@@ -31,7 +33,7 @@ constexpr int BV = 32;
 
 template <int D>
 struct CcShape {
-    static constexpr int SPLIT = D / 32;  // warps per block (row groups)
+    static constexpr int SPLIT = D / 16;  // warps per block (row groups of 16 rows)
     static constexpr int RPT = D / SPLIT;  // rows per thread
 };
 
@@ -47,7 +49,7 @@ __global__ void __launch_bounds__(32 * CcShape<D>::SPLIT) chunk_cc_kernel(Args a
     __shared__ float sN[C][C + 1];  // strictly lower part of N, later T = (I+N)^-1
     __shared__ float sP[C][C + 1];
     __shared__ float sT[C][C + 1];
-    __shared__ float red[2][SPLIT][C][BV];
+    __shared__ float red[SPLIT][C][BV];
 
     const int ncb = D / BV;
     const int cb = blockIdx.x % ncb;
@@ -155,26 +157,27 @@ __global__ void __launch_bounds__(32 * CcShape<D>::SPLIT) chunk_cc_kernel(Args a
             ks[t] = x;
             qs[t] = y;
         }
-        if (SPLIT > 1) {
+        // sum the SPLIT partials: K S first, then Q S through the same buffer
 #pragma unroll
-            for (int t = 0; t < C; ++t) {
-                red[0][p][t][lane] = ks[t];
-                red[1][p][t][lane] = qs[t];
-            }
+        for (int t = 0; t < C; ++t) red[p][t][lane] = ks[t];
+        __syncthreads();
+#pragma unroll
+        for (int t = 0; t < C; ++t) {
+            float x = 0.f;
+#pragma unroll
+            for (int w = 0; w < SPLIT; ++w) x += red[w][t][lane];
+            ks[t] = x;
         }
         __syncthreads();
-        if (SPLIT > 1) {
 #pragma unroll
-            for (int t = 0; t < C; ++t) {
-                float x = 0.f, y = 0.f;
+        for (int t = 0; t < C; ++t) red[p][t][lane] = qs[t];
+        __syncthreads();
 #pragma unroll
-                for (int w = 0; w < SPLIT; ++w) {
-                    x += red[0][w][t][lane];
-                    y += red[1][w][t][lane];
-                }
-                ks[t] = x;
-                qs[t] = y;
-            }
+        for (int t = 0; t < C; ++t) {
+            float y = 0.f;
+#pragma unroll
+            for (int w = 0; w < SPLIT; ++w) y += red[w][t][lane];
+            qs[t] = y;
         }
 
         // R = diag(beta)(V - diag(e^G) K S);  D = T R;  O = scale (e^G Q S + P D).
@@ -195,15 +198,15 @@ __global__ void __launch_bounds__(32 * CcShape<D>::SPLIT) chunk_cc_kernel(Args a
                 dcol[t] = acc;
             }
         }
-        if (a.deltas && p == 0) {  // the corrections u_t of the chunk's real rows
+        if (a.deltas) {  // the corrections u_t of the chunk's real rows
 #pragma unroll
             for (int t = 0; t < C; ++t)
-                if (t < L) a.deltas[((size_t)(c0 + t) * a.h_v + h) * D + col] = dcol[t];
+                if (t < L && t % SPLIT == p) a.deltas[((size_t)(c0 + t) * a.h_v + h) * D + col] = dcol[t];
         }
-        if (p == 0) {
+        {
 #pragma unroll
             for (int t = 0; t < C; ++t) {
-                if (t < L) {
+                if (t < L && t % SPLIT == p) {
                     float acc = __expf(sG[t]) * qs[t];
 #pragma unroll
                     for (int m = 0; m <= t; ++m) acc = fmaf(sP[t][m], dcol[m], acc);

@@ -11,11 +11,12 @@
 // n_tok tokens serve every prefix: this replaces restoring the snapshot and
 // re-feeding the accepted tokens.
 //
-// Mapping.  One block of 256 threads per (sequence, V head).  Thread t owns the
-// column quad 4 (t % (D/4)) and every (256 / (D/4))-th row, so each row of the
-// state is read and written as whole coalesced lines; its quad of the weighted
-// corrections e^{G_a - G_j} u_j stays in registers and the accepted K rows sit
-// in shared memory.
+// Mapping.  One block of 256 threads per (sequence, V head, quarter of the
+// state rows), so even one sequence spreads over 4 H_v blocks.  Thread t owns
+// column quad t % (D/4) of rows t / (D/4) + k (256 / (D/4)), k < D / 4 / (256 /
+// (D/4)): every load of its rows is issued before any arithmetic, and its quad
+// of the weighted corrections e^{G_a - G_j} u_j stays in registers; the
+// accepted K rows sit in shared memory.
 #include "gdr_common.cuh"
 #include "gdr_internal.h"
 
@@ -24,72 +25,87 @@ namespace {
 
 constexpr int NT = 256;
 constexpr int MAXTOK = 16;
+constexpr int NQUART = 4;  // blocks per (sequence, V head)
 
 template <int D>
 __global__ void __launch_bounds__(NT) commit_kernel(Args a, int32_t *err) {
-    constexpr int Q4 = D / 4;        // column quads per row
-    constexpr int RSTEP = NT / Q4;   // rows between a thread's rows
-    __shared__ float sK[MAXTOK][D];  // k_j of the accepted tokens, fp32
-    __shared__ float sW[MAXTOK];     // e^{G_a - G_j}
-    __shared__ float sEa;            // e^{G_a}
+    constexpr int Q4 = D / 4;              // column quads per row
+    constexpr int RSTEP = NT / Q4;         // rows between a thread's rows
+    constexpr int ROWS = D / NQUART;       // rows per block
+    constexpr int NR = ROWS / RSTEP;       // rows per thread (D = 32: RSTEP 32 > ROWS 8, see below)
+    static_assert(D % NQUART == 0, "row quarters");
+    __shared__ float sK[MAXTOK][ROWS];     // the block's rows of k_j for the accepted tokens, fp32
+    __shared__ float sW[MAXTOK];           // e^{G_a - G_j}
+    __shared__ float sEa;                  // e^{G_a}
 
-    const int h = blockIdx.x % a.h_v, s = blockIdx.x / a.h_v;
+    const int quarter = blockIdx.x % NQUART;
+    const int h = (blockIdx.x / NQUART) % a.h_v, s = blockIdx.x / (NQUART * a.h_v);
     const int hq = h / (a.h_v / a.h_qk);
     const int n_tok = a.fixed_len;
     const int acc = a.accepted[s];
     if (acc < 0 || acc > n_tok) {  // leave the state as it is and report
-        if (threadIdx.x == 0) atomicCAS(err, 0, (int32_t)GDR_ERR_INVALID_ARG);
+        if (threadIdx.x == 0 && quarter == 0) atomicCAS(err, 0, (int32_t)GDR_ERR_INVALID_ARG);
         return;
     }
+    const int rbase = quarter * ROWS;
     const size_t row0 = (size_t)s * n_tok;  // the block's first token row of this sequence
+    const int cq = threadIdx.x % Q4, r0 = threadIdx.x / Q4;
+    const size_t sbase = ((size_t)s * a.h_v + h) * D * D;
+    const float4 *src = reinterpret_cast<const float4 *>(a.snapshot_in + sbase);
+    float4 *dst = reinterpret_cast<float4 *>(a.state + sbase);
+    // this thread's rows of the snapshot, loaded first
+    constexpr int NRT = NR > 0 ? NR : 1;
+    float4 x[NRT];
+#pragma unroll
+    for (int k = 0; k < NRT; ++k) {
+        const int r = rbase + r0 + k * RSTEP;
+        x[k] = (r0 + k * RSTEP < ROWS) ? src[r * Q4 + cq] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float4 u[MAXTOK];
+#pragma unroll
+    for (int j = 0; j < MAXTOK; ++j) {
+        u[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j < acc) u[j] = *reinterpret_cast<const float4 *>(a.deltas + ((row0 + j) * a.h_v + h) * D + 4 * cq);
+    }
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
         float gj = (lane < acc) ? a.g[(row0 + lane) * a.h_v + h] : 0.f;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const float u = __shfl_up_sync(0xffffffffu, gj, o);
-            if (lane >= o) gj += u;
+            const float t = __shfl_up_sync(0xffffffffu, gj, o);
+            if (lane >= o) gj += t;
         }
         const float Ga = __shfl_sync(0xffffffffu, gj, acc > 0 ? acc - 1 : 0);
         if (lane < MAXTOK) sW[lane] = (lane < acc) ? __expf(Ga - gj) : 0.f;  // exponent <= 0 for g <= 0
         if (lane == 0) sEa = acc > 0 ? __expf(Ga) : 1.f;
     }
-    for (int e = threadIdx.x; e < acc * D; e += NT) {
-        const int j = e / D, i = e - j * D;
-        sK[j][i] = load_in(a.k, ((row0 + j) * a.h_qk + hq) * D + i, a.in_bf16);
+    for (int e = threadIdx.x; e < acc * ROWS; e += NT) {
+        const int j = e / ROWS, i = e - j * ROWS;
+        sK[j][i] = load_in(a.k, ((row0 + j) * a.h_qk + hq) * D + rbase + i, a.in_bf16);
     }
     __syncthreads();
-
-    const int cq = threadIdx.x % Q4, r0 = threadIdx.x / Q4;
-    float4 u[MAXTOK];
 #pragma unroll
     for (int j = 0; j < MAXTOK; ++j) {
-        u[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j < acc) {
-            const float4 d = *reinterpret_cast<const float4 *>(a.deltas + ((row0 + j) * a.h_v + h) * D + 4 * cq);
-            const float w = sW[j];
-            u[j] = make_float4(w * d.x, w * d.y, w * d.z, w * d.w);
-        }
+        const float w = sW[j];
+        u[j] = make_float4(w * u[j].x, w * u[j].y, w * u[j].z, w * u[j].w);
     }
     const float ea = sEa;
-    const size_t sbase = ((size_t)s * a.h_v + h) * D * D;
-    const float4 *src = reinterpret_cast<const float4 *>(a.snapshot_in + sbase);
-    float4 *dst = reinterpret_cast<float4 *>(a.state + sbase);
-#pragma unroll 4
-    for (int r = r0; r < D; r += RSTEP) {
-        float4 x = src[r * Q4 + cq];
-        x = make_float4(ea * x.x, ea * x.y, ea * x.z, ea * x.w);
+#pragma unroll
+    for (int k = 0; k < NRT; ++k) {
+        const int rl = r0 + k * RSTEP;  // row within the block's quarter
+        if (rl >= ROWS) continue;
+        float4 y = make_float4(ea * x[k].x, ea * x[k].y, ea * x[k].z, ea * x[k].w);
 #pragma unroll
         for (int j = 0; j < MAXTOK; ++j) {
             if (j < acc) {
-                const float kr = sK[j][r];
-                x.x = fmaf(kr, u[j].x, x.x);
-                x.y = fmaf(kr, u[j].y, x.y);
-                x.z = fmaf(kr, u[j].z, x.z);
-                x.w = fmaf(kr, u[j].w, x.w);
+                const float kr = sK[j][rl];
+                y.x = fmaf(kr, u[j].x, y.x);
+                y.y = fmaf(kr, u[j].y, y.y);
+                y.z = fmaf(kr, u[j].z, y.z);
+                y.w = fmaf(kr, u[j].w, y.w);
             }
         }
-        dst[r * Q4 + cq] = x;
+        dst[(rbase + rl) * Q4 + cq] = y;
     }
 }
 
@@ -98,7 +114,7 @@ __global__ void __launch_bounds__(NT) commit_kernel(Args a, int32_t *err) {
 cudaError_t launch_commit(const Args &a, int32_t *err, cudaStream_t s) {
     if (a.n_seqs == 0) return cudaSuccess;
     if (a.fixed_len < 0 || a.fixed_len > MAXTOK || !err) return cudaErrorInvalidValue;
-    const unsigned blocks = (unsigned)a.n_seqs * (unsigned)a.h_v;
+    const unsigned blocks = (unsigned)a.n_seqs * (unsigned)a.h_v * (unsigned)NQUART;
     switch (a.d) {
         case 32: commit_kernel<32><<<blocks, NT, 0, s>>>(a, err); break;
         case 64: commit_kernel<64><<<blocks, NT, 0, s>>>(a, err); break;
