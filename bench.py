@@ -261,8 +261,14 @@ def run_ours(args):
         if timers is not None:
             timers[3].record(stream)
 
-    # prefill: factor + chunk-scan launches; verify: the block and the commit
-    launches_per_step = {"all": 5, "prefill": 2, "verify": 2, "decode": 1}[only]
+    # prefill: factor + chunk-scan launches, twice when the library splits a long
+    # prefill so that the later chunks' factors run beside the scan of the earlier
+    # ones (its rule: at least 16 chunks and at least 16 SMs left free by the
+    # scan's 4 CTAs per V head); verify: the block and the commit
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    split = (T_PREFILL + 63) // 64 >= 16 and sms - 4 * H_V >= 16
+    pre_launches = 4 if split else 2
+    launches_per_step = {"all": 3 + pre_launches, "prefill": pre_launches, "verify": 2, "decode": 1}[only]
 
     def barrier():
         if world > 1:

@@ -1,5 +1,8 @@
-// C-ABI entry points: argument checks on the host, then one launch each.
+// C-ABI entry points: argument checks on the host, then the launches.
 #include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
 
 #include "gdr_factor_layout.h"
 #include "gdr_internal.h"
@@ -52,6 +55,8 @@ Args make_args(const gdr_dims *d) {
     a.in_bf16 = d->in_dtype == GDR_BF16;
     a.out_bf16 = d->out_dtype == GDR_BF16;
     a.scale = d->scale;
+    a.c_lo = 0;
+    a.c_hi = INT_MAX;
     return a;
 }
 
@@ -67,6 +72,54 @@ gdr_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_ERR
 
 bool use_tensor_core_prefill(const gdr_dims *d) {
     return d->chunk == 64 && d->d_k == 128 && d->in_dtype == GDR_BF16;
+}
+
+// Chunk at which a prefill is split into two parts, or 0 (no split).  The
+// chunk scan runs n_seqs * h_v * 4 CTAs of one SM each; when that leaves at
+// least 16 SMs free and the prefill is long, the factors of chunks [m, n) are
+// computed on those SMs while the scan walks chunks [0, m).  Both kernels'
+// costs grow with the chunks they handle; measured at h_v = 32 with 24 free
+// SMs, the factor kernel on the free SMs keeps pace with the scan when about
+// 60% of the chunks are in the first part: the scan takes 1 / (1.125 h_v / F)
+// times as long as the factors on F free SMs.
+int split_chunk(const gdr_dims *d, int32_t n_seqs, int64_t t_total) {
+    static int sms_of[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (sms_of[dev] == 0 && cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    const int64_t nch = (t_total + 63) / 64;
+    const int64_t chain_ctas = (int64_t)n_seqs * d->h_v * 4;
+    const int64_t free_sms = sms_of[dev] - chain_ctas;
+    if (nch < 16 || free_sms < 16) return 0;
+    const double r = 1.125 * d->h_v / (double)free_sms;
+    int64_t m = (int64_t)std::ceil(r / (1.0 + r) * (double)nch);
+    if (m < 1) m = 1;
+    if (m > nch - 1) m = nch - 1;
+    return (int)m;
+}
+
+// The tensor-core prefill on `s`: factors, then the chunk scan, or, split at
+// chunk m (see split_chunk): factors [0, m), scan [0, m), factors [m, n) as a
+// programmatic dependent launch (it starts once every CTA of the scan is
+// running, on the SMs they leave free, and reads nothing the scan writes),
+// then scan [m, n) from the state the first part left.
+cudaError_t prefill_tc(const gdr_dims *dims, const Args &a, float *ws, int32_t *err, cudaStream_t s,
+                       bool allow_split) {
+    const int m = allow_split ? split_chunk(dims, a.n_seqs, a.t_total) : 0;
+    if (m == 0) {
+        cudaError_t e = launch_factors(a, ws, err, s, false);
+        if (e != cudaSuccess) return e;
+        return launch_prefill_tc(a, ws, s);
+    }
+    Args a1 = a, a2 = a;
+    a1.c_hi = m;
+    a2.c_lo = m;
+    cudaError_t e = launch_factors(a1, ws, err, s, false);
+    if (e == cudaSuccess) e = launch_prefill_tc(a1, ws, s);
+    if (e == cudaSuccess) e = launch_factors(a2, ws, err, s, true);
+    if (e == cudaSuccess) e = launch_prefill_tc(a2, ws, s);
+    return e;
 }
 
 }  // namespace
@@ -95,10 +148,15 @@ size_t gdr_prefill_workspace_bytes(const gdr_dims *dims, int32_t n_seqs, int64_t
     return (bytes + 255) & ~(size_t)255;
 }
 
-gdr_status gdr_prefill_chunked(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens,
-                               int64_t t_total, const void *q, const void *k, const void *v,
-                               const float *g, const float *beta, float *state, void *o,
-                               void *workspace, size_t workspace_bytes, gdr_stream_t stream) {
+}  // extern "C"
+
+namespace gdr {
+namespace {
+
+gdr_status prefill(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens, int64_t t_total,
+                   const void *q, const void *k, const void *v, const float *g, const float *beta,
+                   float *state, void *o, void *workspace, size_t workspace_bytes, gdr_stream_t stream,
+                   bool allow_split) {
     gdr_status st = check_dims(dims);
     if (st != GDR_OK) return st;
     if (n_seqs < 0 || t_total < 0) return GDR_ERR_INVALID_ARG;
@@ -126,12 +184,22 @@ gdr_status gdr_prefill_chunked(const gdr_dims *dims, int32_t n_seqs, const int32
     if (use_tensor_core_prefill(dims)) {
         int32_t *err = device_error_word();
         if (!err) return GDR_ERR_CUDA;
-        float *ws = static_cast<float *>(workspace);
-        cudaError_t e = launch_factors(a, ws, err, s);
-        if (e != cudaSuccess) return GDR_ERR_CUDA;
-        return from_cuda(launch_prefill_tc(a, ws, s));
+        return from_cuda(prefill_tc(dims, a, static_cast<float *>(workspace), err, s, allow_split));
     }
     return from_cuda(launch_chunk_cc(a, s));
+}
+
+}  // namespace
+}  // namespace gdr
+
+extern "C" {
+
+gdr_status gdr_prefill_chunked(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens,
+                               int64_t t_total, const void *q, const void *k, const void *v,
+                               const float *g, const float *beta, float *state, void *o,
+                               void *workspace, size_t workspace_bytes, gdr_stream_t stream) {
+    return prefill(dims, n_seqs, cu_seqlens, t_total, q, k, v, g, beta, state, o, workspace, workspace_bytes,
+                   stream, true);
 }
 
 size_t gdr_prefill_static_workspace_capacity(void) { return kStaticWorkspaceBytes; }
@@ -150,7 +218,7 @@ gdr_status gdr_prefill_chunked_static(const gdr_dims *dims, int32_t n_seqs, cons
         ws = static_workspace();
         if (!ws) return GDR_ERR_CUDA;
     }
-    return gdr_prefill_chunked(dims, n_seqs, cu_seqlens, t_total, q, k, v, g, beta, state, o, ws, need, stream);
+    return prefill(dims, n_seqs, cu_seqlens, t_total, q, k, v, g, beta, state, o, ws, need, stream, false);
 }
 
 gdr_status gdr_decode_step(const gdr_dims *dims, int32_t batch, const void *q, const void *k,

@@ -83,6 +83,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct FacParams {
     int h_qk, h_v, n_seqs;
+    int c_lo, c_hi;    // chunks of each sequence to process
+    int64_t slot_lo;   // first slot of the launch (blockIdx.x = 0)
     int64_t t_total;
     const int32_t *cu_seqlens;
     const float *g, *beta;
@@ -299,7 +301,7 @@ __device__ void solve_pt(const uint8_t *hs, const float *gates, float *slot_out,
 
 __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ CUtensorMap tmK,
                                                        const __grid_constant__ CUtensorMap tmQ, FacParams p) {
-    const int64_t slot = blockIdx.x;
+    const int64_t slot = p.slot_lo + blockIdx.x;
     const int h = blockIdx.y, hq = h / (p.h_v / p.h_qk);
     // the sequence whose chunk this slot holds: the last s with slot_base(s) <= slot
     int lo = 0, hi = p.n_seqs - 1;
@@ -317,6 +319,7 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
         return;
     }
     if (c < 0 || c * C >= ts1 - ts0) return;  // a slot between sequences: nothing to do
+    if (c < p.c_lo || c >= p.c_hi) return;     // a chunk outside this launch's range
     const int64_t t0 = ts0 + c * C;
     const int L = (int)((ts1 - t0) < C ? (ts1 - t0) : C);
 
@@ -438,7 +441,7 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
 
 }  // namespace
 
-cudaError_t launch_factors(const Args &a, float *ws, int32_t *err, cudaStream_t s) {
+cudaError_t launch_factors(const Args &a, float *ws, int32_t *err, cudaStream_t s, bool overlap) {
     CUtensorMap tmK, tmQ;
     if (!encode_bf16_3d(&tmK, a.k, 128, (uint64_t)a.h_qk, (uint64_t)a.t_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_bf16_3d(&tmQ, a.q, 128, (uint64_t)a.h_qk, (uint64_t)a.t_total, 64, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -462,10 +465,28 @@ cudaError_t launch_factors(const Args &a, float *ws, int32_t *err, cudaStream_t 
     p.beta = a.beta;
     p.ws = ws;
     p.err = err;
-    const int64_t slots = fac::n_slots(a.t_total, a.n_seqs);
-    dim3 grid((unsigned)slots, (unsigned)a.h_v);
-    factor_kernel<<<grid, NT, SMEM_BYTES, s>>>(tmK, tmQ, p);
-    return cudaGetLastError();
+    p.c_lo = a.c_lo;
+    p.c_hi = a.c_hi;
+    // one sequence: chunk c is slot c, so the launch covers exactly its range;
+    // packed sequences: every slot, each CTA checks its chunk against the range
+    int64_t slot_lo = 0, slot_hi = fac::n_slots(a.t_total, a.n_seqs);
+    if (a.n_seqs == 1) {
+        slot_lo = a.c_lo;
+        if ((int64_t)a.c_hi < slot_hi) slot_hi = a.c_hi;
+    }
+    if (slot_hi <= slot_lo) return cudaSuccess;
+    p.slot_lo = slot_lo;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(slot_hi - slot_lo), (unsigned)a.h_v);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = overlap ? &attr : nullptr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, factor_kernel, tmK, tmQ, p);
 }
 
 }  // namespace gdr

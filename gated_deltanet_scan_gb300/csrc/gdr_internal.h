@@ -26,13 +26,17 @@ struct Args {
     float *deltas;              // optional per-token corrections u_t (verify block), fp32 like v
     const int32_t *accepted;    // verify commit: accepted tokens per sequence (device)
     const float *snapshot_in;   // verify commit: the state before the block
+    // tensor-core prefill: only chunks [c_lo, c_hi) of each sequence (0, INT32_MAX: all of them)
+    int c_lo, c_hi;
 };
 
 cudaError_t launch_decode(const Args &a, cudaStream_t s);
 cudaError_t launch_chunk_cc(const Args &a, cudaStream_t s);
 // Tensor-core prefill in two launches: the per-chunk factors of every chunk
 // into `ws` (fac::n_slots(t_total, n_seqs) * h_v slots), then the chunk scan.
-cudaError_t launch_factors(const Args &a, float *ws, int32_t *err, cudaStream_t s);
+// `overlap`: launch as a programmatic dependent of the kernel before it on `s`
+// (it may start once every CTA of that kernel runs; it must not read its results).
+cudaError_t launch_factors(const Args &a, float *ws, int32_t *err, cudaStream_t s, bool overlap);
 cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s);
 cudaError_t launch_copy_f32(const float *src, float *dst, size_t n, cudaStream_t s);
 // Verify commit: state = e^{G_a} snapshot + sum_{j<a} e^{G_a - G_j} k_j u_j^T per (sequence, V head).

@@ -118,6 +118,7 @@ constexpr uint32_t IDESC_Y = idesc_bf16_f32(128, 64, 1, 1);    // A MN-major (Ká
 
 struct TcParams {
     int h_qk, h_v, out_bf16;
+    int c_lo, c_hi;  // chunks of each sequence to process; the state is read before and written after them
     float scale;
     const int32_t *cu_seqlens;
     const float *ws;  // factor slots
@@ -463,10 +464,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int h = (blockIdx.x / NCOL) % p.h_v;
     const int s = (blockIdx.x / NCOL) / p.h_v;
     const int hq = h / (p.h_v / p.h_qk);
-    const int64_t t0 = p.cu_seqlens[s], t1 = p.cu_seqlens[s + 1];
-    if (t1 <= t0) return;  // empty sequence: the state stays as it is
-    const int nchunks = (int)((t1 - t0 + C - 1) / C);
-    const int64_t slot0 = fac::slot_base(t0, s);
+    const int64_t ts0 = p.cu_seqlens[s], t1 = p.cu_seqlens[s + 1];
+    if (t1 <= ts0) return;  // empty sequence: the state stays as it is
+    const int nch_all = (int)((t1 - ts0 + C - 1) / C);
+    const int c_end = nch_all < p.c_hi ? nch_all : p.c_hi;
+    if (p.c_lo >= c_end) return;  // no chunk of this sequence in this launch: its state stays as it is
+    const int nchunks = c_end - p.c_lo;
+    const int64_t t0 = ts0 + (int64_t)p.c_lo * C;
+    const int64_t slot0 = fac::slot_base(ts0, s) + p.c_lo;
+    // a programmatic dependent launch queued behind this one (the factors of a
+    // later chunk range) may start as soon as every CTA of this grid runs
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (tid == 0) {
         for (int i = 0; i < NBARS; ++i) mbar_init(x.bar(i), 1);
@@ -558,6 +566,8 @@ cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s) {
     p.h_qk = a.h_qk;
     p.h_v = a.h_v;
     p.out_bf16 = a.out_bf16;
+    p.c_lo = a.c_lo;
+    p.c_hi = a.c_hi;
     p.scale = a.scale;
     p.cu_seqlens = a.cu_seqlens;
     p.ws = ws;
