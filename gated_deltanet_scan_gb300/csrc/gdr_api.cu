@@ -242,7 +242,9 @@ gdr_status gdr_decode_step(const gdr_dims *dims, int32_t batch, const void *q, c
     a.state = state;
     a.snapshot = nullptr;
     a.o = o;
-    return from_cuda(launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
+    int32_t *err = device_error_word();
+    if (!err) return GDR_ERR_CUDA;
+    return from_cuda(launch_decode(a, err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 gdr_status gdr_verify_block(const gdr_dims *dims, int32_t n_seqs, int32_t n_tok, const void *q,

@@ -6,159 +6,187 @@
 //
 // Design.  The op is bound by HBM: each (sequence, V head) reads and writes its
 // d x d fp32 state once (128 KiB for d = 128) and touches only ~1 KiB of
-// q/k/v/o.  One 256-thread block owns one (sequence, V head).  Lane l of every
-// warp owns the same d/32 adjacent columns; warp w owns d/8 rows, so each warp
-// load is one fully coalesced 512-byte row slab (float4 per lane at d = 128).
-// The slab stays in registers: partial S^T k and S^T q over the warp's rows go
-// through shared memory once to reduce over the 8 warps, then every thread
-// forms delta for its columns and writes d S + k delta^T straight from its
-// registers.  Loads and stores carry streaming (evict-first) hints because the
-// state is touched exactly once per step.
+// q/k/v/o.  One 256-thread block owns one (sequence, V head).  One thread
+// brings the whole state into shared memory with bulk asynchronous copies
+// completed on an mbarrier, so a block holds no state in registers (about 40
+// of them) and three blocks fit on an SM (3 x 64 KiB in flight at d = 128):
+// the SM keeps more bytes moving than with the state held in registers, which
+// matters most when the step shares the GPU with other work.  Thread t owns
+// column quad t % (d/4) of every (256 / (d/4))-th row: a warp reads whole rows
+// from shared memory, conflict free.  The partial S^T k and S^T q of its rows
+// go through shared memory once to reduce over the row groups; then every
+// thread forms delta for its columns, re-reads its rows and writes d S + k
+// delta^T straight to HBM with streaming (evict-first) stores.  The wait on
+// the copies is bounded: on timeout the block records GDR_ERR_DEVICE_TIMEOUT
+// and leaves the state as it was.
 #include "gdr_common.cuh"
 #include "gdr_internal.h"
+#include "tc_ptx.cuh"
 
 namespace gdr {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
+using namespace tc;
+
+constexpr int kThreads = 256;
+constexpr long long kWaitLimit = 4000000000LL;  // SM clocks (about 2 s)
 
 template <int D>
-struct Vec;
-template <>
-struct Vec<32> {
-    using T = float;
-    static __device__ __forceinline__ void split(const T &v, float *f) { f[0] = v; }
-    static __device__ __forceinline__ T pack(const float *f) { return f[0]; }
-};
-template <>
-struct Vec<64> {
-    using T = float2;
-    static __device__ __forceinline__ void split(const T &v, float *f) {
-        f[0] = v.x;
-        f[1] = v.y;
-    }
-    static __device__ __forceinline__ T pack(const float *f) { return make_float2(f[0], f[1]); }
-};
-template <>
-struct Vec<128> {
-    using T = float4;
-    static __device__ __forceinline__ void split(const T &v, float *f) {
-        f[0] = v.x;
-        f[1] = v.y;
-        f[2] = v.z;
-        f[3] = v.w;
-    }
-    static __device__ __forceinline__ T pack(const float *f) {
-        return make_float4(f[0], f[1], f[2], f[3]);
-    }
+struct DecShape {
+    static constexpr int Q4 = D / 4;            // column quads per row
+    static constexpr int RSTEP = kThreads / Q4;  // row groups (rows between a thread's rows)
+    static constexpr int NR = D / RSTEP;         // rows per thread
+    static constexpr uint32_t SBYTES = D * D * 4;
+    static constexpr uint32_t NCOPY = SBYTES > 16384 ? SBYTES / 16384 : 1;  // bulk copies of <= 16 KiB
+    static constexpr uint32_t CBYTES = SBYTES / NCOPY;
+    // dynamic shared memory: state, then one partial-sum table (y, then z), then the mbarrier
+    static constexpr uint32_t OFF_RED = SBYTES;
+    static constexpr uint32_t OFF_BAR = OFF_RED + RSTEP * D * 4;
+    static constexpr uint32_t SMEM = OFF_BAR + 16;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(Args a) {
-    constexpr int CPL = D / 32;     // columns per lane
-    constexpr int RPW = D / kWarps;  // rows per warp
-    using V = Vec<D>;
-    using VT = typename V::T;
-
+__global__ void __launch_bounds__(kThreads) decode_kernel(Args a, int32_t *err) {
+    using Sh = DecShape<D>;
+    extern __shared__ __align__(128) uint8_t dsm[];
+    float4 *sS = reinterpret_cast<float4 *>(dsm);
+    float *red = reinterpret_cast<float *>(dsm + Sh::OFF_RED);  // [RSTEP][D]
+    const uint32_t bar = smem_u32(dsm + Sh::OFF_BAR);
     __shared__ float sk[D], sq[D];
-    __shared__ float red[2][kWarps][D];
     __shared__ float s_qk;
 
     const int bh = blockIdx.x;
     const int b = bh / a.h_v, h = bh - b * a.h_v;
     const int hq = h / (a.h_v / a.h_qk);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int col0 = lane * CPL;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int cq = tid % Sh::Q4, rg = tid / Sh::Q4;
 
-    // Issue the state loads first: they are the only HBM-heavy traffic.
-    VT *S = reinterpret_cast<VT *>(a.state + ((size_t)b * a.h_v + h) * D * D);
-    VT sv[RPW];
+    float *S = a.state + (size_t)bh * D * D;
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(bar, Sh::SBYTES);
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) sv[r] = __ldcs(&S[(size_t)(warp * RPW + r) * (D / CPL) + lane]);
-
+        for (uint32_t i = 0; i < Sh::NCOPY; ++i)
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    smem_u32(dsm) + i * Sh::CBYTES),
+                "l"(reinterpret_cast<uint64_t>(S) + i * Sh::CBYTES), "r"(Sh::CBYTES), "r"(bar)
+                : "memory");
+    }
     const size_t qk_off = ((size_t)b * a.h_qk + hq) * D;
-    for (int i = threadIdx.x; i < D; i += kThreads) {
+    for (int i = tid; i < D; i += kThreads) {
         sk[i] = load_in(a.k, qk_off + i, a.in_bf16);
         sq[i] = load_in(a.q, qk_off + i, a.in_bf16);
     }
     const size_t vh = (size_t)b * a.h_v + h;
     const float dgate = __expf(a.g[vh]);
     const float bt = a.beta[vh];
-    float vv[CPL];
+    float vv[4];
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) vv[c] = load_in(a.v, vh * D + col0 + c, a.in_bf16);
-    __syncthreads();
-
-    float y[CPL], z[CPL];
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) y[c] = z[c] = 0.f;
-#pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-        float f[CPL];
-        V::split(sv[r], f);
-        const float kr = sk[warp * RPW + r], qr = sq[warp * RPW + r];
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-            y[c] = fmaf(f[c], kr, y[c]);
-            z[c] = fmaf(f[c], qr, z[c]);
+    for (int c = 0; c < 4; ++c) vv[c] = load_in(a.v, vh * D + 4 * cq + c, a.in_bf16);
+    __syncthreads();  // the mbarrier is initialised, sk and sq are written
+    const bool ok = mbar_wait_bounded(bar, 0, kWaitLimit);
+    if (!__syncthreads_and(ok)) {
+        // leave the state untouched; let the copies land before the block's shared memory is released
+        if (tid == 0) {
+            atomicCAS(err, 0, (int32_t)GDR_ERR_DEVICE_TIMEOUT);
+            mbar_wait_bounded(bar, 0, kWaitLimit / 8);
         }
+        __syncthreads();
+        return;
     }
+
+    // partial y = S^T k and z = S^T q over this thread's rows, for its 4 columns
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f), z = y;
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) {
-        red[0][warp][col0 + c] = y[c];
-        red[1][warp][col0 + c] = z[c];
+    for (int i = 0; i < Sh::NR; ++i) {
+        const int r = rg + i * Sh::RSTEP;
+        const float4 sv = sS[r * Sh::Q4 + cq];
+        const float kr = sk[r], qr = sq[r];
+        y.x = fmaf(sv.x, kr, y.x);
+        y.y = fmaf(sv.y, kr, y.y);
+        y.z = fmaf(sv.z, kr, y.z);
+        y.w = fmaf(sv.w, kr, y.w);
+        z.x = fmaf(sv.x, qr, z.x);
+        z.y = fmaf(sv.y, qr, z.y);
+        z.z = fmaf(sv.z, qr, z.z);
+        z.w = fmaf(sv.w, qr, z.w);
     }
+    // sum the row groups' partials: y first, then z through the same table
+    *reinterpret_cast<float4 *>(red + rg * D + 4 * cq) = y;
     if (warp == 0) {
-        float p = 0.f;
-        for (int i = lane; i < D; i += 32) p = fmaf(sk[i], sq[i], p);
-        p = warp_sum(p);
-        if (lane == 0) s_qk = p;
+        float pq = 0.f;
+        for (int i = lane; i < D; i += 32) pq = fmaf(sk[i], sq[i], pq);
+        pq = warp_sum(pq);
+        if (lane == 0) s_qk = pq;
     }
     __syncthreads();
-
-    float delta[CPL];
+    float delta[4], zt[4];
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) {
-        float yt = 0.f, zt = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            yt += red[0][w][col0 + c];
-            zt += red[1][w][col0 + c];
-        }
-        delta[c] = bt * (vv[c] - dgate * yt);
-        z[c] = zt;
+    for (int c = 0; c < 4; ++c) {
+        float ys = 0.f;
+#pragma unroll 8
+        for (int w = 0; w < Sh::RSTEP; ++w) ys += red[w * D + 4 * cq + c];
+        delta[c] = bt * (vv[c] - dgate * ys);
     }
-    if (warp == 0) {
+    __syncthreads();
+    *reinterpret_cast<float4 *>(red + rg * D + 4 * cq) = z;
+    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        float zs = 0.f;
+#pragma unroll 8
+        for (int w = 0; w < Sh::RSTEP; ++w) zs += red[w * D + 4 * cq + c];
+        zt[c] = zs;
+    }
+    if (rg == 0) {
         const float qk = s_qk;
 #pragma unroll
-        for (int c = 0; c < CPL; ++c)
-            store_out(a.o, vh * D + col0 + c, a.scale * fmaf(dgate, z[c], qk * delta[c]), a.out_bf16);
+        for (int c = 0; c < 4; ++c)
+            store_out(a.o, vh * D + 4 * cq + c, a.scale * fmaf(dgate, zt[c], qk * delta[c]), a.out_bf16);
     }
 
+    // S' = d S + k delta^T, from shared memory straight to HBM
+    float4 *Sg = reinterpret_cast<float4 *>(S);
 #pragma unroll
-    for (int r = 0; r < RPW; ++r) {
-        float f[CPL];
-        V::split(sv[r], f);
-        const float kr = sk[warp * RPW + r];
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) f[c] = fmaf(dgate, f[c], kr * delta[c]);
-        __stcs(&S[(size_t)(warp * RPW + r) * (D / CPL) + lane], V::pack(f));
+    for (int i = 0; i < Sh::NR; ++i) {
+        const int r = rg + i * Sh::RSTEP;
+        const float4 sv = sS[r * Sh::Q4 + cq];
+        const float kr = sk[r];
+        const float4 nv = make_float4(fmaf(dgate, sv.x, kr * delta[0]), fmaf(dgate, sv.y, kr * delta[1]),
+                                      fmaf(dgate, sv.z, kr * delta[2]), fmaf(dgate, sv.w, kr * delta[3]));
+        __stcs(&Sg[r * Sh::Q4 + cq], nv);
     }
+}
+
+template <int D>
+cudaError_t launch_d(const Args &a, int32_t *err, unsigned blocks, cudaStream_t s) {
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)DecShape<D>::SMEM);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    decode_kernel<D><<<blocks, kThreads, DecShape<D>::SMEM, s>>>(a, err);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const Args &a, cudaStream_t s) {
+cudaError_t launch_decode(const Args &a, int32_t *err, cudaStream_t s) {
     const unsigned blocks = (unsigned)a.n_seqs * (unsigned)a.h_v;
     if (blocks == 0) return cudaSuccess;
     switch (a.d) {
-        case 32: decode_kernel<32><<<blocks, kThreads, 0, s>>>(a); break;
-        case 64: decode_kernel<64><<<blocks, kThreads, 0, s>>>(a); break;
-        case 128: decode_kernel<128><<<blocks, kThreads, 0, s>>>(a); break;
+        case 32: return launch_d<32>(a, err, blocks, s);
+        case 64: return launch_d<64>(a, err, blocks, s);
+        case 128: return launch_d<128>(a, err, blocks, s);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace gdr
