@@ -16,7 +16,7 @@ from typing import Optional
 __all__ = [
     "GdrError", "gdr_dims", "lib", "library_path",
     "gdr_prefill_chunked", "gdr_prefill_workspace_bytes", "gdr_prefill_chunked_static",
-    "gdr_decode_step", "gdr_verify_block", "gdr_verify_commit",
+    "gdr_decode_step", "gdr_decode_step_overlapped", "gdr_verify_block", "gdr_verify_commit",
     "gdr_state_snapshot", "gdr_state_restore", "gdr_device_error", "gdr_status_string",
     "GDR_F32", "GDR_BF16",
 ]
@@ -61,6 +61,8 @@ _SIGS = {
     "gdr_prefill_static_workspace_capacity": ([], ctypes.c_size_t),
     "gdr_decode_step": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P],
                         ctypes.c_int),
+    "gdr_decode_step_overlapped": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P],
+                                   ctypes.c_int),
     "gdr_verify_block": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, ctypes.c_int32,
                           _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "gdr_verify_commit": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, ctypes.c_int32,
@@ -194,6 +196,17 @@ def gdr_decode_step(q, k, v, g, beta, state, o, *, scale: float = 1.0, stream=No
         ctypes.byref(dims), q.shape[0], _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
         _ptr(state), _ptr(o), _stream_handle(stream, q.device))
     _check(st, "gdr_decode_step")
+
+
+def gdr_decode_step_overlapped(q, k, v, g, beta, state, o, *, scale: float = 1.0, stream=None) -> None:
+    """gdr_decode_step launched as a programmatic dependent of the kernel before it
+    on the stream (see include/gdr.h): none of its inputs or states may be written
+    by that kernel."""
+    dims = make_dims(q, v, o, 64, scale)
+    st = lib().gdr_decode_step_overlapped(
+        ctypes.byref(dims), q.shape[0], _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+        _ptr(state), _ptr(o), _stream_handle(stream, q.device))
+    _check(st, "gdr_decode_step_overlapped")
 
 
 def gdr_verify_block(q, k, v, g, beta, state, snapshot, o, n_tok: int, *, deltas=None, scale: float = 1.0,

@@ -221,9 +221,13 @@ gdr_status gdr_prefill_chunked_static(const gdr_dims *dims, int32_t n_seqs, cons
     return prefill(dims, n_seqs, cu_seqlens, t_total, q, k, v, g, beta, state, o, ws, need, stream, false);
 }
 
-gdr_status gdr_decode_step(const gdr_dims *dims, int32_t batch, const void *q, const void *k,
-                           const void *v, const float *g, const float *beta, float *state, void *o,
-                           gdr_stream_t stream) {
+}  // extern "C"
+
+namespace gdr {
+namespace {
+
+gdr_status decode(const gdr_dims *dims, int32_t batch, const void *q, const void *k, const void *v,
+                  const float *g, const float *beta, float *state, void *o, gdr_stream_t stream, bool overlap) {
     gdr_status st = check_dims(dims);
     if (st != GDR_OK) return st;
     if (batch < 0) return GDR_ERR_INVALID_ARG;
@@ -244,7 +248,24 @@ gdr_status gdr_decode_step(const gdr_dims *dims, int32_t batch, const void *q, c
     a.o = o;
     int32_t *err = device_error_word();
     if (!err) return GDR_ERR_CUDA;
-    return from_cuda(launch_decode(a, err, reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_decode(a, err, reinterpret_cast<cudaStream_t>(stream), overlap));
+}
+
+}  // namespace
+}  // namespace gdr
+
+extern "C" {
+
+gdr_status gdr_decode_step(const gdr_dims *dims, int32_t batch, const void *q, const void *k,
+                           const void *v, const float *g, const float *beta, float *state, void *o,
+                           gdr_stream_t stream) {
+    return decode(dims, batch, q, k, v, g, beta, state, o, stream, false);
+}
+
+gdr_status gdr_decode_step_overlapped(const gdr_dims *dims, int32_t batch, const void *q, const void *k,
+                                      const void *v, const float *g, const float *beta, float *state,
+                                      void *o, gdr_stream_t stream) {
+    return decode(dims, batch, q, k, v, g, beta, state, o, stream, true);
 }
 
 gdr_status gdr_verify_block(const gdr_dims *dims, int32_t n_seqs, int32_t n_tok, const void *q,

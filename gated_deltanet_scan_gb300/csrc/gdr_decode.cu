@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(Args a, int32_t *err) 
 }
 
 template <int D>
-cudaError_t launch_d(const Args &a, int32_t *err, unsigned blocks, cudaStream_t s) {
+cudaError_t launch_d(const Args &a, int32_t *err, unsigned blocks, cudaStream_t s, bool overlap) {
     static int configured_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -172,19 +172,28 @@ cudaError_t launch_d(const Args &a, int32_t *err, unsigned blocks, cudaStream_t 
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    decode_kernel<D><<<blocks, kThreads, DecShape<D>::SMEM, s>>>(a, err);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = DecShape<D>::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = overlap ? &attr : nullptr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, decode_kernel<D>, a, err);
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const Args &a, int32_t *err, cudaStream_t s) {
+cudaError_t launch_decode(const Args &a, int32_t *err, cudaStream_t s, bool overlap) {
     const unsigned blocks = (unsigned)a.n_seqs * (unsigned)a.h_v;
     if (blocks == 0) return cudaSuccess;
     switch (a.d) {
-        case 32: return launch_d<32>(a, err, blocks, s);
-        case 64: return launch_d<64>(a, err, blocks, s);
-        case 128: return launch_d<128>(a, err, blocks, s);
+        case 32: return launch_d<32>(a, err, blocks, s, overlap);
+        case 64: return launch_d<64>(a, err, blocks, s, overlap);
+        case 128: return launch_d<128>(a, err, blocks, s, overlap);
         default: return cudaErrorInvalidValue;
     }
 }

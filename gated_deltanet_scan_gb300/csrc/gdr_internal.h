@@ -30,7 +30,8 @@ struct Args {
     int c_lo, c_hi;
 };
 
-cudaError_t launch_decode(const Args &a, int32_t *err, cudaStream_t s);
+// `overlap`: launch as a programmatic dependent of the kernel before it on `s`.
+cudaError_t launch_decode(const Args &a, int32_t *err, cudaStream_t s, bool overlap);
 cudaError_t launch_chunk_cc(const Args &a, cudaStream_t s);
 // Tensor-core prefill in two launches: the per-chunk factors of every chunk
 // into `ws` (fac::n_slots(t_total, n_seqs) * h_v slots), then the chunk scan.

@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define GDR_ABI_VERSION 3
+#define GDR_ABI_VERSION 4
 
 /* Same object as cudaStream_t; declared here so callers need no CUDA header. */
 typedef struct CUstream_st *gdr_stream_t;
@@ -177,6 +177,24 @@ size_t gdr_prefill_static_workspace_capacity(void);
 gdr_status gdr_decode_step(const gdr_dims *dims, int32_t batch, const void *q, const void *k,
                            const void *v, const float *g, const float *beta, float *state, void *o,
                            gdr_stream_t stream);
+
+/*
+ * gdr_decode_step launched as a programmatic dependent of the kernel before it
+ * on `stream`: it may start as soon as every CTA of that kernel is running,
+ * instead of after it completes, and use the SMs that kernel leaves free.  This
+ * is how a serving loop overlaps the decode step of some sequences with a long
+ * prefill of another: queued right after gdr_prefill_chunked, it starts beside
+ * the prefill's last chunk-scan launch (which occupies 4 SMs per V head).
+ *
+ * Contract: none of the step's inputs or states may be written by the kernel
+ * immediately before it on `stream` (work queued earlier has completed before
+ * that kernel started and is visible).  Arguments, results and errors are as in
+ * gdr_decode_step; later work on `stream` is ordered after the step as usual.
+ * Callers that cannot guarantee the contract use gdr_decode_step.
+ */
+gdr_status gdr_decode_step_overlapped(const gdr_dims *dims, int32_t batch, const void *q, const void *k,
+                                      const void *v, const float *g, const float *beta, float *state,
+                                      void *o, gdr_stream_t stream);
 
 /*
  * Speculative-verify block: n_tok <= 16 draft tokens per sequence in one pass.

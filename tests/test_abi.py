@@ -107,11 +107,11 @@ def test_prefill_workspace_size_and_checks(L):
 
 def test_decode_and_verify_reject_bad_arguments(L):
     d = dims()
-    dec = L.gdr_decode_step
-    assert dec(ctypes.byref(d), -1, A, A, A, A, A, A, B, None) == gdr.GDR_ERR_INVALID_ARG
-    assert dec(ctypes.byref(d), 4, A, A, None, A, A, A, B, None) == gdr.GDR_ERR_INVALID_ARG
-    assert dec(ctypes.byref(d), 4, A, A, A, A, A, A, MISALIGNED, None) == gdr.GDR_ERR_INVALID_ARG
-    assert dec(ctypes.byref(d), 0, None, None, None, None, None, None, None, None) == gdr.GDR_OK
+    for dec in (L.gdr_decode_step, L.gdr_decode_step_overlapped):
+        assert dec(ctypes.byref(d), -1, A, A, A, A, A, A, B, None) == gdr.GDR_ERR_INVALID_ARG
+        assert dec(ctypes.byref(d), 4, A, A, None, A, A, A, B, None) == gdr.GDR_ERR_INVALID_ARG
+        assert dec(ctypes.byref(d), 4, A, A, A, A, A, A, MISALIGNED, None) == gdr.GDR_ERR_INVALID_ARG
+        assert dec(ctypes.byref(d), 0, None, None, None, None, None, None, None, None) == gdr.GDR_OK
     ver = L.gdr_verify_block
     assert ver(ctypes.byref(d), 2, 17, A, A, A, A, A, A, B, B, None, None) == gdr.GDR_ERR_INVALID_ARG
     assert ver(ctypes.byref(d), 2, 16, A, A, A, A, A, A, A, B, None, None) == gdr.GDR_ERR_INVALID_ARG

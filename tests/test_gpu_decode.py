@@ -84,3 +84,33 @@ def test_decode_equals_one_token_prefill():
     torch.cuda.synchronize()
     assert gu.o_error(gu.to_np(o1), gu.to_np(o2)) < 1e-3
     assert gu.state_error(gu.to_np(s1), gu.to_np(s2)) < 1e-4
+
+
+def test_decode_overlapped_beside_a_prefill():
+    """A decode step queued right after a long prefill as a programmatic dependent
+    launch runs beside the prefill's last chunk-scan launch; both give the
+    oracle's results, three times in a row on one stream."""
+    import gated_deltanet_scan_gb300 as gdr
+    torch = gu.require_gpu()
+    pre = synth.make_workload("ovl_pre", [2048], 16, 32, 128, 64, "bf16", seed=41, state_std=0.02)
+    dec = synth.decode_batch(8, 3, seed=42)
+    x = gu.dev_inputs(pre)
+    o_pre = gu.out_like(x["v"], "f32")
+    dstate = torch.from_numpy(np.ascontiguousarray(dec.state0)).cuda()
+    outs = []
+    for s in range(3):
+        x["state"].copy_(torch.from_numpy(np.ascontiguousarray(pre.state0)))
+        gdr.gdr_prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state"], o_pre, x["cu_seqlens"],
+                                chunk=64)
+        q, k, v, g, beta = _step_inputs(dec, s, 8, "cuda")
+        o = gu.out_like(v, "f32")
+        gdr.gdr_decode_step_overlapped(q, k, v, g, beta, dstate, o)
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert gdr.gdr_device_error() == 0
+    o_ref, s_ref = oracle.run_workload(pre)
+    gu.check_outputs(gu.to_np(o_pre), o_ref)
+    gu.check_state(gu.to_np(x["state"]), s_ref)
+    od_ref, sd_ref = _oracle_decode(dec, 8, 3)
+    gu.check_outputs(np.concatenate([gu.to_np(o) for o in outs]), od_ref)
+    gu.check_state(gu.to_np(dstate), sd_ref)
