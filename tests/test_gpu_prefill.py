@@ -121,3 +121,13 @@ def test_packing_equals_separate_calls():
         oi, si = run_prefill(wi)
         assert gu.o_error(oi, o_all[a:b]) < 1e-5
         assert gu.state_error(si[0], s_all[i]) < 1e-6
+
+
+@pytest.mark.parametrize("lens", [[1000, 3000], [0, 2500]])
+def test_split_prefill_over_two_sequences(lens):
+    """16 V heads (8 QK heads) and two sequences: the chunk scan runs 128 CTAs, so
+    on a 152-SM GB300 the call splits at a chunk (27 of 63 for [1000, 3000], 18 of
+    40 for [0, 2500]): a sequence that ends before the split chunk, one that is cut
+    by it, and an empty one all come out as the oracle's."""
+    w = synth.make_workload("split2", lens, 8, 16, 128, 64, "bf16", seed=51 + lens[0], state_std=0.02)
+    check(w)
