@@ -43,8 +43,9 @@ __global__ void __launch_bounds__(32 * CcShape<D>::SPLIT) chunk_cc_kernel(Args a
     constexpr int RPT = CcShape<D>::RPT;
     constexpr int NT = 32 * SPLIT;
 
-    __shared__ float sK[C][D + 1];
-    __shared__ float sQ[C][D + 1];
+    constexpr int KSTR = D + 4;  // tile row stride: rows stay 16-byte aligned for float4 reads
+    __shared__ __align__(16) float sK[C][KSTR];
+    __shared__ __align__(16) float sQ[C][KSTR];
     __shared__ float sG[C], sB[C];
     __shared__ float sN[C][C + 1];  // strictly lower part of N, later T = (I+N)^-1
     __shared__ float sP[C][C + 1];
@@ -76,16 +77,49 @@ __global__ void __launch_bounds__(32 * CcShape<D>::SPLIT) chunk_cc_kernel(Args a
     for (int64_t c0 = t0; c0 < t1; c0 += C) {
         const int L = (int)((t1 - c0) < C ? (t1 - c0) : C);
         __syncthreads();  // previous chunk's readers of shared tiles are done
-        for (int e = threadIdx.x; e < C * D; e += NT) {
-            const int t = e / D, i = e - t * D;
-            float kv = 0.f, qv = 0.f;
-            if (t < L) {
-                const size_t off = ((size_t)(c0 + t) * a.h_qk + hq) * D + i;
-                kv = load_in(a.k, off, a.in_bf16);
-                qv = load_in(a.q, off, a.in_bf16);
+        // this lane's column of V for the chunk, requested before anything else
+        float vpre[C];
+#pragma unroll
+        for (int t = 0; t < C; ++t)
+            vpre[t] = (t < L) ? load_in(a.v, ((size_t)(c0 + t) * a.h_v + h) * D + col, a.in_bf16) : 0.f;
+        // K and Q tiles, 16 bytes per load (8 bf16 or 4 fp32 values)
+        if (a.in_bf16) {
+#pragma unroll
+            for (int e = threadIdx.x; e < C * D / 8; e += NT) {
+                const int t = (8 * e) / D, i = (8 * e) % D;
+                uint4 kw = make_uint4(0u, 0u, 0u, 0u), qw = kw;
+                if (t < L) {
+                    const size_t off = ((size_t)(c0 + t) * a.h_qk + hq) * D + i;
+                    kw = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(a.k) + off);
+                    qw = *reinterpret_cast<const uint4 *>(reinterpret_cast<const __nv_bfloat16 *>(a.q) + off);
+                }
+                const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w}, qq[4] = {qw.x, qw.y, qw.z, qw.w};
+                float kf[8], qf[8];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    kf[2 * u] = __uint_as_float(kk[u] << 16);
+                    kf[2 * u + 1] = __uint_as_float(kk[u] & 0xFFFF0000u);
+                    qf[2 * u] = __uint_as_float(qq[u] << 16);
+                    qf[2 * u + 1] = __uint_as_float(qq[u] & 0xFFFF0000u);
+                }
+                *reinterpret_cast<float4 *>(&sK[t][i]) = make_float4(kf[0], kf[1], kf[2], kf[3]);
+                *reinterpret_cast<float4 *>(&sK[t][i + 4]) = make_float4(kf[4], kf[5], kf[6], kf[7]);
+                *reinterpret_cast<float4 *>(&sQ[t][i]) = make_float4(qf[0], qf[1], qf[2], qf[3]);
+                *reinterpret_cast<float4 *>(&sQ[t][i + 4]) = make_float4(qf[4], qf[5], qf[6], qf[7]);
             }
-            sK[t][i] = kv;
-            sQ[t][i] = qv;
+        } else {
+#pragma unroll
+            for (int e = threadIdx.x; e < C * D / 4; e += NT) {
+                const int t = (4 * e) / D, i = (4 * e) % D;
+                float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), qv = kv;
+                if (t < L) {
+                    const size_t off = ((size_t)(c0 + t) * a.h_qk + hq) * D + i;
+                    kv = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(a.k) + off);
+                    qv = *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(a.q) + off);
+                }
+                *reinterpret_cast<float4 *>(&sK[t][i]) = kv;
+                *reinterpret_cast<float4 *>(&sQ[t][i]) = qv;
+            }
         }
         if (threadIdx.x < 32) {
             // inclusive running sum of g over the chunk (padding: g = 0, beta = 0)
@@ -113,9 +147,12 @@ __global__ void __launch_bounds__(32 * CcShape<D>::SPLIT) chunk_cc_kernel(Args a
             if (j <= t) {
                 float dk = 0.f, dq = 0.f;
 #pragma unroll 8
-                for (int i = 0; i < D; ++i) {
-                    dk = fmaf(sK[t][i], sK[j][i], dk);
-                    dq = fmaf(sQ[t][i], sK[j][i], dq);
+                for (int i = 0; i < D; i += 4) {
+                    const float4 kt = *reinterpret_cast<const float4 *>(&sK[t][i]);
+                    const float4 kj = *reinterpret_cast<const float4 *>(&sK[j][i]);
+                    const float4 qt = *reinterpret_cast<const float4 *>(&sQ[t][i]);
+                    dk = fmaf(kt.x, kj.x, fmaf(kt.y, kj.y, fmaf(kt.z, kj.z, fmaf(kt.w, kj.w, dk))));
+                    dq = fmaf(qt.x, kj.x, fmaf(qt.y, kj.y, fmaf(qt.z, kj.z, fmaf(qt.w, kj.w, dq))));
                 }
                 const float decay = __expf(sG[t] - sG[j]);  // exponent <= 0 on this triangle
                 pq = decay * dq;
@@ -150,9 +187,11 @@ __global__ void __launch_bounds__(32 * CcShape<D>::SPLIT) chunk_cc_kernel(Args a
         for (int t = 0; t < C; ++t) {
             float x = 0.f, y = 0.f;
 #pragma unroll
-            for (int r = 0; r < RPT; ++r) {
-                x = fmaf(sK[t][row0 + r], sreg[r], x);
-                y = fmaf(sQ[t][row0 + r], sreg[r], y);
+            for (int r = 0; r < RPT; r += 4) {
+                const float4 k4 = *reinterpret_cast<const float4 *>(&sK[t][row0 + r]);
+                const float4 q4 = *reinterpret_cast<const float4 *>(&sQ[t][row0 + r]);
+                x = fmaf(k4.x, sreg[r], fmaf(k4.y, sreg[r + 1], fmaf(k4.z, sreg[r + 2], fmaf(k4.w, sreg[r + 3], x))));
+                y = fmaf(q4.x, sreg[r], fmaf(q4.y, sreg[r + 1], fmaf(q4.z, sreg[r + 2], fmaf(q4.w, sreg[r + 3], y))));
             }
             ks[t] = x;
             qs[t] = y;
@@ -185,11 +224,7 @@ __global__ void __launch_bounds__(32 * CcShape<D>::SPLIT) chunk_cc_kernel(Args a
         {
             float rr[C];
 #pragma unroll
-            for (int t = 0; t < C; ++t) {
-                float vt = 0.f;
-                if (t < L) vt = load_in(a.v, ((size_t)(c0 + t) * a.h_v + h) * D + col, a.in_bf16);
-                rr[t] = sB[t] * (vt - __expf(sG[t]) * ks[t]);
-            }
+            for (int t = 0; t < C; ++t) rr[t] = sB[t] * (vpre[t] - __expf(sG[t]) * ks[t]);
 #pragma unroll
             for (int t = 0; t < C; ++t) {
                 float acc = 0.f;
@@ -221,11 +256,17 @@ __global__ void __launch_bounds__(32 * CcShape<D>::SPLIT) chunk_cc_kernel(Args a
         for (int t = 0; t < C; ++t) dcol[t] *= __expf(gl - sG[t]);
         const float eC = __expf(gl);
 #pragma unroll
-        for (int r = 0; r < RPT; ++r) {
-            float acc = eC * sreg[r];
+        for (int r = 0; r < RPT; ++r) sreg[r] *= eC;
 #pragma unroll
-            for (int t = 0; t < C; ++t) acc = fmaf(sK[t][row0 + r], dcol[t], acc);
-            sreg[r] = acc;
+        for (int t = 0; t < C; ++t) {
+#pragma unroll
+            for (int r = 0; r < RPT; r += 4) {
+                const float4 k4 = *reinterpret_cast<const float4 *>(&sK[t][row0 + r]);
+                sreg[r] = fmaf(k4.x, dcol[t], sreg[r]);
+                sreg[r + 1] = fmaf(k4.y, dcol[t], sreg[r + 1]);
+                sreg[r + 2] = fmaf(k4.z, dcol[t], sreg[r + 2]);
+                sreg[r + 3] = fmaf(k4.w, dcol[t], sreg[r + 3]);
+            }
         }
     }
 
