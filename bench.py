@@ -95,6 +95,10 @@ def host_inputs(seed_base=100):
     return pre, ver, dec
 
 
+def _bf(torch, bits):
+    return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16)
+
+
 def _pinned(torch, w):
     def io(bits):
         return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
@@ -261,10 +265,10 @@ def run_ours(args):
 
     # prefill: factor + chunk-scan launches, twice when the library splits a long
     # prefill so that the later chunks' factors run beside the scan of the earlier
-    # ones (its rule: at least 16 chunks and at least 16 SMs left free by the
-    # scan's 4 CTAs per V head); verify: the block and the commit
+    # ones (its rule: chunks x V heads >= 8 x SMs, and at least 16 SMs left free
+    # by the scan's 4 CTAs per V head); verify: the block and the commit
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    split = (T_PREFILL + 63) // 64 >= 16 and sms - 4 * H_V >= 16
+    split = (T_PREFILL + 63) // 64 * H_V >= 8 * sms and sms - 4 * H_V >= 16
     pre_launches = 4 if split else 2
     launches_per_step = {"all": 3 + pre_launches, "prefill": pre_launches, "verify": 2, "decode": 1}[only]
 
@@ -308,6 +312,41 @@ def run_ours(args):
         decode_ms = statistics.median(a.elapsed_time(b) for a, b in dts[5:])
     else:
         decode_ms = statistics.median(t[2].elapsed_time(t[3]) for t in timers)
+
+    # The other configured workloads, timed alone after the steps (informational):
+    # the Qwen3.5-9B layer prefill at T = 1024 and the packed prefill of 8
+    # sequences with lengths ~ U{512..8192}.
+    other = {}
+    if only == "all" and not args.no_other_configs:
+        from gated_deltanet_scan_gb300 import synth
+
+        def time_prefill(w, reps=10):
+            x = dict(q=_bf(torch, w.q_bits).to(dev), k=_bf(torch, w.k_bits).to(dev), v=_bf(torch, w.v_bits).to(dev),
+                     g=torch.from_numpy(np.ascontiguousarray(w.g)).to(dev),
+                     beta=torch.from_numpy(np.ascontiguousarray(w.beta)).to(dev))
+            st = torch.zeros((len(w.cu_seqlens) - 1, H_V, D, D), dtype=torch.float32, device=dev)
+            cu = torch.from_numpy(w.cu_seqlens.astype(np.int32)).to(dev)
+            o = torch.empty((int(w.cu_seqlens[-1]), H_V, D), dtype=torch.float32, device=dev)
+            n = len(w.cu_seqlens) - 1
+            wsx = torch.empty(gdr.gdr_prefill_workspace_bytes(x["q"], x["v"], o, n, o.shape[0]), dtype=torch.uint8,
+                              device=dev)
+            ts = []
+            for r in range(reps + 3):
+                a0, a1 = ev(), ev()
+                a0.record(stream)
+                gdr.gdr_prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], st, o, cu, chunk=64,
+                                        workspace=wsx, stream=stream)
+                a1.record(stream)
+                ts.append((a0, a1))
+            barrier()
+            ms = statistics.median(a.elapsed_time(b) for a, b in ts[3:])
+            tokens = int(w.cu_seqlens[-1])
+            gbs = (tokens * PREFILL_BYTES_PER_TOKEN + 2 * n * STATE_BYTES) / (ms * 1e-3) / 1e9
+            return {"ms": ms, "tokens": tokens, "tokens_per_s": tokens / (ms * 1e-3), "hbm_gbs": gbs,
+                    "frac_hbm": gbs / load_peaks()[0]["hbm_gbs"]}
+
+        other["prefill_T1024"] = time_prefill(synth.prefill_9b(1024))
+        other["packed_prefill_8_seqs"] = time_prefill(synth.varlen_verify())
 
     # End to end through the same public API: every step uploads its inputs from
     # pinned host memory and reads its outputs back.  Like a serving pipeline, the
@@ -443,6 +482,7 @@ def run_ours(args):
         },
         "e2e": {"value": world * TOKENS_PER_STEP / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "other_configs": other or None,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
@@ -450,6 +490,7 @@ def run_ours(args):
         line["partial_step"] = only  # a profiling run of one component, not a bench line
         line["prefill_tokens"] = T_PREFILL
         line.pop("e2e")
+        line.pop("other_configs")
         keep = {"prefill": "prefill_T16384", "verify": "verify16_commit7", "decode": "decode_B64"}[only]
         line["components"] = {keep: line["components"][keep]}
         if only != "prefill":
@@ -542,6 +583,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["all", "prefill", "verify", "decode"], default="all",
                     help="run one component of the step (for profiling); the default runs the full step")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the informational timing of the T=1024 and packed prefill workloads")
     ap.add_argument("--prefill-tokens", type=int, default=T_PREFILL,
                     help="prefill length of a profiling run (with --only prefill); not a bench line")
     args = ap.parse_args()

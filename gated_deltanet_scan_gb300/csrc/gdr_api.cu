@@ -76,8 +76,11 @@ bool use_tensor_core_prefill(const gdr_dims *d) {
 
 // Chunk at which a prefill is split into two parts, or 0 (no split).  The
 // chunk scan runs n_seqs * h_v * 4 CTAs of one SM each; when that leaves at
-// least 16 SMs free and the prefill is long, the factors of chunks [m, n) are
-// computed on those SMs while the scan walks chunks [0, m).  Both kernels'
+// least 16 SMs free and the factor kernel (4 CTAs per SM) needs at least two
+// waves, the factors of chunks [m, n) are computed on those SMs while the scan
+// walks chunks [0, m).  (With one wave or less the first factor launch would
+// take as long as the whole one, and the extra scan launch only costs time:
+// T = 1024 at 32 V heads measured 80 us split against 74 us whole.)  Both kernels'
 // costs grow with the chunks they handle; measured at h_v = 32 with 24 free
 // SMs, the factor kernel on the free SMs keeps pace with the scan when about
 // 60% of the chunks are in the first part: the scan takes 1 / (1.125 h_v / F)
@@ -91,7 +94,7 @@ int split_chunk(const gdr_dims *d, int32_t n_seqs, int64_t t_total) {
     const int64_t nch = (t_total + 63) / 64;
     const int64_t chain_ctas = (int64_t)n_seqs * d->h_v * 4;
     const int64_t free_sms = sms_of[dev] - chain_ctas;
-    if (nch < 16 || free_sms < 16) return 0;
+    if (nch * d->h_v < 8LL * sms_of[dev] || free_sms < 16) return 0;
     const double r = 1.125 * d->h_v / (double)free_sms;
     int64_t m = (int64_t)std::ceil(r / (1.0 + r) * (double)nch);
     if (m < 1) m = 1;

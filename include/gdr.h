@@ -113,11 +113,11 @@ size_t gdr_prefill_workspace_bytes(const gdr_dims *dims, int32_t n_seqs, int64_t
  * On the tensor-core path the call is two launches on `stream`: the
  * state-independent factors of every chunk (gates, (I+N)^-1, P (I+N)^-1) into
  * `workspace`, then the chunk-to-chunk scan that reads them.  When the scan
- * leaves at least 16 SMs free and there are at least 16 chunks (e.g. one
- * Qwen3.5-9B sequence), the call is four launches instead: factors and scan of
- * the first ~60% of the chunks, the remaining factors as a programmatic
- * dependent launch that runs on the free SMs beside that scan, then the scan
- * of the remaining chunks.  The workspace holds nothing between calls.
+ * leaves at least 16 SMs free and the factors of all chunks need at least two
+ * waves of the GPU (e.g. one Qwen3.5-9B sequence of 2.5K tokens or more), the
+ * call is four launches instead: factors and scan of the first ~60% of the
+ * chunks, the remaining factors as a programmatic dependent launch that runs
+ * on the free SMs beside that scan, then the scan of the remaining chunks.  The workspace holds nothing between calls.
  *
  *   dims        shapes, dtypes, chunk, scale (host pointer, read during the call)
  *   n_seqs      number of sequences (>= 0; 0 is a no-op)
