@@ -82,9 +82,10 @@ bool use_tensor_core_prefill(const gdr_dims *d) {
 // take as long as the whole one, and the extra scan launch only costs time:
 // T = 1024 at 32 V heads measured 80 us split against 74 us whole.)  Both kernels'
 // costs grow with the chunks they handle; measured at h_v = 32 with 24 free
-// SMs, the factor kernel on the free SMs keeps pace with the scan when about
-// 60% of the chunks are in the first part: the scan takes 1 / (1.125 h_v / F)
-// times as long as the factors on F free SMs.
+// SMs (T = 16384, a sweep of the split chunk), the prefill is fastest with
+// about 73% of the chunks in the first part (m = 175-195 of 256: 0.647 ms,
+// against 0.655 ms at 60% and 0.687 ms unsplit): m / n = r / (1 + r) with
+// r = 2.0 h_v / F for F free SMs.
 int split_chunk(const gdr_dims *d, int32_t n_seqs, int64_t t_total) {
     static int sms_of[64] = {};
     int dev = 0;
@@ -95,7 +96,7 @@ int split_chunk(const gdr_dims *d, int32_t n_seqs, int64_t t_total) {
     const int64_t chain_ctas = (int64_t)n_seqs * d->h_v * 4;
     const int64_t free_sms = sms_of[dev] - chain_ctas;
     if (nch * d->h_v < 8LL * sms_of[dev] || free_sms < 16) return 0;
-    const double r = 1.125 * d->h_v / (double)free_sms;
+    const double r = 2.0 * d->h_v / (double)free_sms;
     int64_t m = (int64_t)std::ceil(r / (1.0 + r) * (double)nch);
     if (m < 1) m = 1;
     if (m > nch - 1) m = nch - 1;
@@ -147,7 +148,7 @@ const char *gdr_status_string(gdr_status st) {
 
 size_t gdr_prefill_workspace_bytes(const gdr_dims *dims, int32_t n_seqs, int64_t t_total) {
     if (check_dims(dims) != GDR_OK || n_seqs <= 0 || t_total <= 0 || !use_tensor_core_prefill(dims)) return 0;
-    const size_t bytes = (size_t)fac::n_slots(t_total, n_seqs) * (size_t)dims->h_v * fac::SLOT_BYTES;
+    const size_t bytes = (size_t)fac::workspace_bytes(fac::n_slots(t_total, n_seqs), dims->h_v, dims->h_qk);
     return (bytes + 255) & ~(size_t)255;
 }
 

@@ -8,6 +8,12 @@
 // that Tw (V - diag(e^G) K S) is the decay-weighted correction D~ the state
 // update needs and PTw (V - diag(e^G) K S) the intra-chunk part of the output.
 //
+// For the chunk scan's lookahead it also writes, per (chunk c >= 1, QK head), the
+// state-independent product X = [K; Q]_c K_{c-1}ᵀ as bf16 hi/lo operand tiles
+// (layout in gdr_factor_layout.h): the CTA of the first V head of the QK head's
+// group computes it; warps 2-3 write its Q rows while warps 0-1 solve for T,
+// warps 0-1 its K rows at the end.
+//
 // Per chunk (the chunkwise-parallel form of the Qwen3.5-9B NPU model card,
 // "How it works"; forward substitution for the unit triangular factor as in
 // the Candle PR's "Chunked GatedDeltaNet Scan"; log-space masking from its
@@ -65,18 +71,20 @@ constexpr int OFF_TT = OFF_PB + 10 * BLK_B;
 constexpr int OFF_TD = OFF_TT + 10 * BLK_B;
 constexpr int HEAD_B = OFF_TD + 4 * BLK_B;  // 50176
 
-// Shared memory, bytes from a 1024-byte aligned base.  The K/Q tile is only read
-// by the Gram MMA; once it has completed, the scratch overwrites it.
+// Shared memory, bytes from a 1024-byte aligned base.  The K/Q tile and the
+// previous chunk's K tile are only read by the Gram and X MMAs; once those have
+// completed, the scratch overwrites them.
 constexpr uint32_t OFF_KQ = 0;
+constexpr uint32_t OFF_KP = 32768;  // K of the previous chunk: two 8 KB d_k halves
 constexpr uint32_t OFF_GATES = HEAD_B;           // G log2(e), beta, exp(G), exp(G_C - G): 4 x 64 fp32
 constexpr uint32_t OFF_BARS = OFF_GATES + 1024;  // 2 mbarriers
 constexpr uint32_t OFF_TMEM = OFF_BARS + 16;
 constexpr uint32_t SMEM_USED = OFF_TMEM + 16;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
-static_assert(32768 <= HEAD_B, "K/Q tile fits under the scratch");
+static_assert(OFF_KP + 16384 <= HEAD_B, "K/Q and previous K tiles fit under the scratch");
 static_assert(OFF_GATES % 16 == 0 && OFF_BARS % 8 == 0 && HEAD_B % 16 == 0, "alignment");
 
-constexpr uint32_t TM_COLS = 64;  // the 128 x 64 fp32 Gram tile
+constexpr uint32_t TM_COLS = 128;  // the 128 x 64 fp32 Gram tile, then X
 constexpr uint32_t IDESC_G1 = idesc_bf16_f32(128, 64, 0, 0);
 constexpr long long kWaitLimit = 4000000000LL;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -88,7 +96,8 @@ struct FacParams {
     int64_t t_total;
     const int32_t *cu_seqlens;
     const float *g, *beta;
-    float *ws;
+    uint8_t *ws;  // factor slots
+    uint8_t *xs;  // X tiles (fac::x_region_offset bytes into the workspace)
     int32_t *err;
 };
 
@@ -106,6 +115,13 @@ __device__ __forceinline__ uint2 ld_pair(const uint8_t *blk, int r, int p) {
 }
 __device__ __forceinline__ void st_pair(uint8_t *blk, int r, int p, uint2 v) {
     *reinterpret_cast<uint2 *>(blk + r * ROW_B + p * 8) = v;
+}
+// Elements (r, j), (r, j + 1) (j even) of the slot's hi and lo operand tiles.
+__device__ __forceinline__ void st_tile_pair(uint8_t *slot, int r, int j, float x0, float x1) {
+    const uint2 w = hl_pair(x0, x1);
+    const uint32_t off = fac::sw128_elem(r, j);
+    *reinterpret_cast<uint32_t *>(slot + fac::OFF_HI + off) = w.x;
+    *reinterpret_cast<uint32_t *>(slot + fac::OFF_LO + off) = w.y;
 }
 
 // Fragments of mma.m16n8k16 (row.col, bf16): lane = 4 g + c.
@@ -193,10 +209,10 @@ __device__ __forceinline__ void chunk_gates(float g0, float g1, float b0, float 
 }
 
 // The head's T from its N blocks, by warps wi = 0, 1 (named barrier `bar`);
-// every block is stored to the slot's packed layout as soon as it is formed.
-__device__ void solve_t(uint8_t *hs, const float *gates, float *slot_out, int wi, int lane, uint32_t bar) {
+// every block of Tw is stored to the slot's operand tiles (rows 0-63) as soon
+// as it is formed, adjacent columns paired across lanes.
+__device__ void solve_t(uint8_t *hs, const float *gates, uint8_t *slot, int wi, int lane, uint32_t bar) {
     const int g = lane >> 2, c = lane & 3;
-    float *Tout = slot_out + fac::OFF_T;
     const float *bw = gates + 64, *rw = gates + 192;  // column weights beta, row weights exp(G_C - G)
     // ---- diagonal blocks: each warp two, lanes 0-15 / 16-31 one block, lane = column
     {
@@ -221,12 +237,15 @@ __device__ void solve_t(uint8_t *hs, const float *gates, float *slot_out, int wi
             const float nb = __shfl_down_sync(0xffffffffu, col[r], 1);
             if ((jj & 1) == 0) st_pair(td, r, jj >> 1, hl_pair(col[r], nb));
         }
-        // global Tw: row 16 I + r, column 16 I + jj (chunks up to the diagonal)
+        // Tw: row 16 I + r, columns 16 I + jj, + 1 (jj even; 8-column chunks up to
+        // the diagonal one, the rest of the row is zero-filled separately)
         const float bj = bw[16 * I + jj];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
             const int rg = 16 * I + r, cg = 16 * I + jj;
-            if ((cg >> 3) <= (rg >> 3)) Tout[fac::tri8_base(rg) + cg] = col[r] * bj * rw[rg];
+            const float v = col[r] * bj * rw[rg];
+            const float vn = __shfl_down_sync(0xffffffffu, v, 1);
+            if ((jj & 1) == 0 && (cg >> 3) <= (rg >> 3)) st_tile_pair(slot, rg, cg, v, vn);
         }
     }
     named_sync(bar, 64);
@@ -249,18 +268,23 @@ __device__ void solve_t(uint8_t *hs, const float *gates, float *slot_out, int wi
                 st_pair(tt, g, 4 * h + c, hl_pair(t[h][0], t[h][1]));
                 st_pair(tt, g + 8, 4 * h + c, hl_pair(t[h][2], t[h][3]));
             }
-            // global Tw: Tᵀ(J, I)[m][n] = T[16 I + n][16 J + m]
+            // Tw: Tᵀ(J, I)[m][n] = T[16 I + n][16 J + m]; columns 16 J + g, + 1 paired
+            // with the lane of g + 1 (lane + 4)
             const float b0 = bw[16 * J + g], b8 = bw[16 * J + g + 8];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int n = 8 * h + 2 * c;
-                float *r0 = Tout + fac::tri8_base(16 * I + n) + 16 * J;
-                float *r1 = Tout + fac::tri8_base(16 * I + n + 1) + 16 * J;
-                const float w0 = rw[16 * I + n], w1 = rw[16 * I + n + 1];
-                r0[g] = t[h][0] * b0 * w0;
-                r1[g] = t[h][1] * b0 * w1;
-                r0[g + 8] = t[h][2] * b8 * w0;
-                r1[g + 8] = t[h][3] * b8 * w1;
+                const int n = 8 * h + 2 * c, r0 = 16 * I + n;
+                const float w0 = rw[r0], w1 = rw[r0 + 1];
+                const float v[4] = {t[h][0] * b0 * w0, t[h][1] * b0 * w1, t[h][2] * b8 * w0, t[h][3] * b8 * w1};
+                float vn[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) vn[i] = __shfl_down_sync(0xffffffffu, v[i], 4);
+                if ((g & 1) == 0) {
+                    st_tile_pair(slot, r0, 16 * J + g, v[0], vn[0]);
+                    st_tile_pair(slot, r0 + 1, 16 * J + g, v[1], vn[1]);
+                    st_tile_pair(slot, r0, 16 * J + g + 8, v[2], vn[2]);
+                    st_tile_pair(slot, r0 + 1, 16 * J + g + 8, v[3], vn[3]);
+                }
             }
         }
         if (d < 3) named_sync(bar, 64);
@@ -270,9 +294,8 @@ __device__ void solve_t(uint8_t *hs, const float *gates, float *slot_out, int wi
 // The head's P T from P and Tᵀ blocks, by the four warps w: block (I, J), I >= J,
 // costs I - J + 1 products; the groups {30, 00}, {20, 10}, {31, 21},
 // {32, 11, 22, 33} cost five each.
-__device__ void solve_pt(const uint8_t *hs, const float *gates, float *slot_out, int w, int lane) {
+__device__ void solve_pt(const uint8_t *hs, const float *gates, uint8_t *slot, int w, int lane) {
     const int g = lane >> 2, c = lane & 3;
-    float *PTout = slot_out + fac::OFF_PT;
     const float *bw = gates + 64;  // column weights beta
     const uint32_t blocks = w == 0 ? 0x0030u : w == 1 ? 0x1020u : w == 2 ? 0x2131u : 0x33221132u;
     const int nblk = w == 3 ? 4 : 2;
@@ -292,9 +315,28 @@ __device__ void solve_pt(const uint8_t *hs, const float *gates, float *slot_out,
             for (int hr = 0; hr < 2; ++hr) {
                 const int rg = 16 * I + g + 8 * hr;
                 if ((cg >> 3) <= (rg >> 3))
-                    *reinterpret_cast<float2 *>(PTout + fac::tri8_base(rg) + cg) =
-                        make_float2(acc[h][2 * hr] * b0, acc[h][2 * hr + 1] * b1);
+                    st_tile_pair(slot, 64 + rg, cg, acc[h][2 * hr] * b0, acc[h][2 * hr + 1] * b1);
             }
+        }
+    }
+}
+
+// Row `row` (a TMEM lane this warp may read) of X from TMEM columns 64-127 into
+// the X tile pair of the slot: bf16 hi and lo parts, 128-byte swizzled.
+__device__ void store_x_row(uint32_t tmem, int warp, int row, uint8_t *xpair) {
+    uint8_t *xt = xpair + (size_t)row * 128;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+#pragma unroll 1
+    for (int hf = 0; hf < 2; ++hf) {
+        float v[32];
+        tmem_ld32(lane_addr + 64 + 32 * hf, v);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t hw[4], lw[4];
+            hilo_words(v + 8 * q, hw, lw);
+            const uint32_t off = (uint32_t)((((4 * hf + q) ^ (row & 7)) & 7) << 4);
+            *reinterpret_cast<uint4 *>(xt + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4 *>(xt + fac::X_TILE_BYTES + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
     }
 }
@@ -345,15 +387,22 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
             rb1 = p.beta[i];
         }
     }
+    // X writer: the first V head of the QK head's group; the first chunk of a
+    // sequence has no X
+    const bool want_x = c >= 1 && h % (p.h_v / p.h_qk) == 0;
     if (tid == 0) {
         mbar_init(bar_tma, 1);
         mbar_init(bar_mma, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(bar_tma, 32768u);
+        mbar_arrive_expect_tx(bar_tma, want_x ? 49152u : 32768u);
         tma_load_3d(sb + OFF_KQ, &tmK, bar_tma, 0, hq, (int)t0);
         tma_load_3d(sb + OFF_KQ + 16384, &tmK, bar_tma, 64, hq, (int)t0);
         tma_load_3d(sb + OFF_KQ + 8192, &tmQ, bar_tma, 0, hq, (int)t0);
         tma_load_3d(sb + OFF_KQ + 16384 + 8192, &tmQ, bar_tma, 64, hq, (int)t0);
+        if (want_x) {
+            tma_load_3d(sb + OFF_KP, &tmK, bar_tma, 0, hq, (int)(t0 - C));
+            tma_load_3d(sb + OFF_KP + 8192, &tmK, bar_tma, 64, hq, (int)(t0 - C));
+        }
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_holder), TM_COLS);
@@ -376,6 +425,14 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
             for (int ks = 0; ks < 8; ++ks) {
                 const uint64_t a = desc_add(a0, (ks >> 2) * 16384 + (ks & 3) * 32);
                 mma_bf16(tmem, a, a, IDESC_G1, ks > 0);
+            }
+            if (want_x) {
+                // X = [K; Q] K_prevᵀ into TMEM columns 64-127
+                const uint64_t b0 = smem_desc_sw128(sb + OFF_KP, 16, 1024);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16(tmem + 64, desc_add(a0, (ks >> 2) * 16384 + (ks & 3) * 32),
+                             desc_add(b0, (ks >> 2) * 8192 + (ks & 3) * 32), IDESC_G1, ks > 0);
             }
             mma_commit(bar_mma);
         }
@@ -424,15 +481,34 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
     }
     tc_fence_before_sync();
     __syncthreads();
-    float *slot_out = p.ws + ((size_t)slot * p.h_v + h) * fac::SLOT_FLOATS;
-    if (warp < 2)
+    uint8_t *slot_out = p.ws + ((size_t)slot * p.h_v + h) * fac::SLOT_BYTES;
+    uint8_t *xpair = p.xs + ((size_t)slot * p.h_qk + hq) * fac::X_BYTES;
+    if (warp < 2) {
         solve_t(sm, gates, slot_out, warp, lane, 1);
-    else if (warp == 2) {
+    } else {
+        // exp(G); X rows 64-127 (Q rows); the zero 8-column chunks right of each
+        // row's diagonal chunk (thread i of warps 2-3: rows i of Tw and 64 + i of PTw)
+        if (warp == 2) {
+            float *eg = reinterpret_cast<float *>(slot_out + fac::OFF_EG);
+            eg[lane] = gates[128 + lane];
+            eg[lane + 32] = gates[160 + lane];
+        }
+        if (want_x) store_x_row(tmem, warp, tid, xpair);
+        const int t = tid - 64;
+        for (int k = (t >> 3) + 1; k < 8; ++k) {
 #pragma unroll
-        for (int i = 0; i < 6; ++i) slot_out[fac::OFF_G + 32 * i + lane] = gates[32 * i + lane];
+            for (int m = 0; m < 2; ++m) {
+                const uint32_t off = fac::sw128_elem(t + 64 * m, 8 * k);
+                *reinterpret_cast<uint4 *>(slot_out + fac::OFF_HI + off) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(slot_out + fac::OFF_LO + off) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
     }
     __syncthreads();
     solve_pt(sm, gates, slot_out, warp, lane);
+    if (want_x && warp < 2) store_x_row(tmem, warp, tid, xpair);  // X rows 0-63 (K rows)
+    tc_fence_before_sync();
+    __syncthreads();  // every TMEM read is done before the columns are freed
     if (warp == 0) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, TM_COLS);
@@ -463,7 +539,8 @@ cudaError_t launch_factors(const Args &a, float *ws, int32_t *err, cudaStream_t 
     p.cu_seqlens = a.cu_seqlens;
     p.g = a.g;
     p.beta = a.beta;
-    p.ws = ws;
+    p.ws = reinterpret_cast<uint8_t *>(ws);
+    p.xs = reinterpret_cast<uint8_t *>(ws) + fac::x_region_offset(fac::n_slots(a.t_total, a.n_seqs), a.h_v);
     p.err = err;
     p.c_lo = a.c_lo;
     p.c_hi = a.c_hi;

@@ -1,18 +1,32 @@
 // Layout of the per-chunk factor workspace shared by the factor kernel (writer)
 // and the tensor-core chunk scan (reader).
 //
-// One slot per (chunk, V head): the lower-triangular factors
+// One slot per (chunk, V head), 33 024 bytes, holding the chunk's
 // Tw = diag(exp(G_C - G)) (I + N)^-1 diag(beta) and PTw = P (I + N)^-1 diag(beta)
-// (G_C = G of the chunk's last row) and the chunk's gates, fp32:
-//   [0, 2304)      Tw   rows packed in 8-float chunks: row t keeps chunks
-//                        0 .. t/8 (columns 0 .. 8 (t/8) + 7, zeros right of the diagonal)
-//   [2304, 4608)   PTw  same packing
-//   [4608, 4672)   G log2(e)   (inclusive running sum of g; padding rows repeat the last)
-//   [4672, 4736)   beta        (0 on padding rows)
-//   [4736, 4800)   exp(G)
+// (G_C = G of the chunk's last row) ready to be the A operand of a tcgen05 MMA:
+//   [0, 16384)       hi tile: 128 rows (Tw rows 0-63, then PTw rows 64-127) of
+//                    64 bf16 in the 128-byte-swizzled K-major layout: 16-byte
+//                    chunk j of row r at r * 128 + 16 (j ^ (r % 8)); zeros above
+//                    the diagonal
+//   [16384, 32768)   lo tile: the same for the residuals (x = hi + lo to ~2^-16)
+//   [32768, 33024)   exp(G), 64 fp32 (G: inclusive running sum of g; padding rows
+//                    repeat the last)
+// A bulk copy of a tile to a 1024-byte aligned shared-memory address yields the
+// operand as it is.
+//
 // Chunk c of sequence s lives in slot floor(cu[s] / 64) + s + c; slots of
 // different sequences never collide and every slot index is below
 // ceil(T_total / 64) + n_seqs.
+//
+// After the slots (at x_region_offset, 1024-byte aligned) one X tile pair per
+// (slot, QK head): for the slot of chunk c >= 1 of a sequence,
+//   X = [K; Q]_c K_{c-1}ᵀ        (128 x 64: the chunk's K rows, then its Q rows,
+//                                 against the previous chunk's 64 key tokens)
+// as two bf16 tiles, hi parts then lo parts (x = hi + lo to ~2^-16), each 128
+// rows of 128 bytes in the 128-byte-swizzled K-major layout of a tcgen05 A
+// operand: 16-byte chunk j of row r at r * 128 + 16 (j ^ (r % 8)).  A bulk copy
+// to a 1024-byte aligned shared-memory address yields the operand as it is.
+// The slot of a sequence's first chunk has no X.
 #pragma once
 
 #include <stdint.h>
@@ -20,27 +34,33 @@
 namespace gdr {
 namespace fac {
 
-constexpr int C = 64;                // tokens per chunk
-constexpr int TRI_FLOATS = 2304;     // 8 * sum_t (t/8 + 1)
-constexpr int OFF_T = 0;
-constexpr int OFF_PT = TRI_FLOATS;
-constexpr int OFF_G = 2 * TRI_FLOATS;
-constexpr int OFF_BETA = OFF_G + C;
-constexpr int OFF_EG = OFF_BETA + C;
-constexpr int SLOT_FLOATS = OFF_EG + C;  // 4800
-constexpr int SLOT_BYTES = SLOT_FLOATS * 4;  // 19200, a multiple of 16
-
-// First float of row t in a packed triangle.
-__host__ __device__ constexpr int tri8_base(int t) {
-    return 8 * (4 * (t >> 3) * ((t >> 3) + 1) + (t & 7) * ((t >> 3) + 1));
-}
-static_assert(tri8_base(64) == TRI_FLOATS, "packed triangle size");
+constexpr int C = 64;                  // tokens per chunk
+constexpr int TILE_BYTES = 16384;      // 128 rows x 64 bf16
+constexpr int OFF_HI = 0;              // bytes
+constexpr int OFF_LO = TILE_BYTES;
+constexpr int OFF_EG = 2 * TILE_BYTES;
+constexpr int SLOT_BYTES = OFF_EG + C * 4;  // 33024, a multiple of 16
 static_assert(SLOT_BYTES % 16 == 0, "slots must keep 16-byte alignment");
+
+// Byte offset of the bf16 element (row r, column j) in a 128-byte-swizzled
+// K-major tile of 128-byte rows.
+__host__ __device__ constexpr uint32_t sw128_elem(int r, int j) {
+    return (uint32_t)(r * 128 + ((((j >> 3) ^ (r & 7)) & 7) << 4) + (j & 7) * 2);
+}
 
 __host__ __device__ constexpr int64_t n_slots(int64_t t_total, int64_t n_seqs) {
     return (t_total + C - 1) / C + n_seqs;
 }
 __host__ __device__ constexpr int64_t slot_base(int64_t seq_start, int64_t s) { return seq_start / C + s; }
+
+constexpr int X_TILE_BYTES = 16384;           // 128 rows x 64 bf16
+constexpr int X_BYTES = 2 * X_TILE_BYTES;     // hi tile, then lo tile
+__host__ __device__ constexpr int64_t x_region_offset(int64_t n_slots_total, int64_t h_v) {
+    return (n_slots_total * h_v * SLOT_BYTES + 1023) / 1024 * 1024;
+}
+__host__ __device__ constexpr int64_t workspace_bytes(int64_t n_slots_total, int64_t h_v, int64_t h_qk) {
+    return x_region_offset(n_slots_total, h_v) + n_slots_total * h_qk * X_BYTES;
+}
 
 }  // namespace fac
 }  // namespace gdr

@@ -1,42 +1,51 @@
 // Chunk scan of the chunked prefill on the 5th-generation tensor cores
 // (tcgen05 + TMEM + TMA): carries the state from chunk to chunk, using the
 // state-independent factors that the factor kernel stored for every chunk
-// beforehand: the gates and Tw = diag(exp(G_C - G)) T diag(beta),
-// PTw = P T diag(beta), with T = (I + N)^-1.
+// beforehand: the gates, Tw = diag(exp(G_C - G)) T diag(beta) and
+// PTw = P T diag(beta) with T = (I + N)^-1, and X_c = [K; Q]_{c+1} K_cᵀ.
 //
 // Shapes: d_k = d_v = 128, 64-token chunks, bf16 q/k/v, fp32 state, fp32 or
 // bf16 output.  Four CTAs share one (sequence, V head); CTA `cb` owns state
 // columns [32 cb, 32 cb + 32), keeps its 128 x 32 block of the state on chip
 // for the whole sequence (fp32 in registers, bf16 hi/lo copies in shared
-// memory as MMA operands) and walks the chunks in order.  Per chunk (the
-// chunkwise-parallel form of the Qwen3.5-9B NPU model card, "How it works"):
-//   MMA1  [K S; Q S] = [K; Q] S                      A = K/Q tile, B = [S_hi | S_lo]
-//   R     = V - diag(e^G) K S
-//   MMA2  [D~; P D] = [Tw; PTw] R                    A = [Tw; PTw]_hi and _lo, B = [R_hi | R_lo]
+// memory as MMA operands) and walks the chunks in order.  Per chunk c (the
+// chunkwise-parallel form of the Qwen3.5-9B NPU model card, "How it works"),
+// with S_c the state before the chunk and gamma_c = G_C its total log decay:
+//   A_c   = [K S_c; Q S_c]                          (an accumulator, see below)
+//   R     = V - diag(e^G) K S_c
+//   MMA2  [D~; P D] = [Tw; PTw] R                   A = [Tw; PTw]_hi and _lo, B = [R_hi | R_lo]
 //         (D = T diag(beta) R is the chunk's delta correction, D~ = diag(exp(G_C - G)) D)
-//   O     = scale (diag(e^G) Q S + P D)
-//   MMA3  Y = Kᵀ D~                                  A = Kᵀ, B = [D~_hi | D~_lo]
-//   S    <- exp(G_C) S + Y
-// A tcgen05 MMA of N <= 64 costs the same as one of N = 32 (about 50 cycles of
-// issue each), so each B operand carries its bf16 hi and lo halves side by side
-// (N = 64) and the partial products are summed when the accumulator is read:
-// every product that feeds the state keeps ~2^-16 relative precision with
-// 8 + 8 + 4 MMAs per chunk, all issued by one thread into one accumulator per
-// group (more issuing threads, each with its own accumulator, measured slower:
-// the readers' extra TMEM loads and sums cost more than the issue they save).
+//   O     = scale (diag(e^G) Q S_c + P D)
+//   MMA3  Y = K_cᵀ D~                                A = Kᵀ, B = [D~_hi | D~_lo]
+//   S_c+1 = e^gamma_c S_c + Y
+// The next chunk's accumulator is formed by lookahead.  Since
+// S_c+1 = e^gamma_c S_c + K_cᵀ D~_c,
+//   A_c+1 = [K; Q]_c+1 (e^gamma_c S_c) + X_c D~_c,        X_c = [K; Q]_c+1 K_cᵀ:
+// MMA1' (the first term) is issued as soon as S_c is known, in the shadow of
+// MMA2, and only MMA_X = X_c [D~_hi | D~_lo] (X_c's hi and lo tiles, four
+// token k-steps each) lies between one chunk's D~ and the next chunk's R.  The
+// chunk-to-chunk path is MMA_X, R, MMA2, D~: two dependent MMA groups per
+// chunk; MMA3 and the state update run beside it.
+// A tcgen05 MMA of N <= 64 costs about the same as one of N = 32, so each B
+// operand carries its bf16 hi and lo halves side by side (N = 64) and the
+// partial products are summed when the accumulator is read: every product that
+// feeds the state keeps ~2^-16 relative precision.
 //
-// Warp roles (384 threads).  Warps 0-7, the "chain": warp w owns TMEM lanes
-// 32 (w % 4) .. + 31 (state rows, or chunk rows: K/T rows in lanes 0-63, Q/PT
-// rows in lanes 64-127) and columns 16 (w / 4) .. + 15 of the CTA's 32.  Only
-// warps of lanes 0-63 sit on the chunk-to-chunk path between MMA1 and MMA3;
-// the others form the outputs meanwhile, and lane 0 of warp 2 issues every
-// MMA (so no K/T-row warp ever waits behind an MMA issue).  Warps 8-11, the "loader": one
-// thread issues the TMA loads (K, Q and V tiles three chunks deep, factor
-// slots two deep); all four unpack a chunk's packed fp32 [T; PT] into the
-// bf16 hi/lo operand tiles while the chain runs the chunk before.  Every
-// mbarrier wait is bounded; on timeout the thread records
-// GDR_ERR_DEVICE_TIMEOUT, raises the CTA's abort flag, and both roles leave
-// their loops together at their next role barrier.
+// Warp roles (448 threads; every role waits only on mbarriers and its own
+// named barriers, so no role can stall another's issue):
+//   warps 0-7, the "chain": warp w owns TMEM lanes 32 (w % 4) .. + 31 (chunk
+//     rows: K/T rows in lanes 0-63, Q/PT rows in lanes 64-127) and columns
+//     16 (w / 4) .. + 15 of the CTA's 32.  The warps of lanes 0-63 form R and D~
+//     (the chunk-to-chunk path); the others form and store the outputs;
+//   warps 8-11, the "loader": own the state (thread i: row i, in registers),
+//     update it from Y and write S' while MMA2 runs;
+//   warp 12 issues every MMA (converged, one elected lane);
+//   warp 13, one thread, issues every copy: K, Q and V tiles three chunks deep
+//     by TMA; the [Tw; PTw] and X operand tiles one chunk ahead and the gates two
+//     ahead by bulk copy, prefetched into L2 two chunks before.
+// Every mbarrier wait is bounded; on timeout the thread records
+// GDR_ERR_DEVICE_TIMEOUT and raises the CTA's abort flag, every role leaves its
+// loop at its next wait or role barrier, and the CTA frees its TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -59,9 +68,10 @@ constexpr int BV = 32;           // state columns per CTA
 constexpr int NCOL = D / BV;     // CTAs per (sequence, V head)
 constexpr int NCHAIN = 256;      // warps 0-7
 constexpr int NLOAD = 128;       // warps 8-11
-constexpr int NTHREADS = NCHAIN + NLOAD;
+constexpr int NISSUE = 32;       // warp 12
+constexpr int NCOPY = 32;        // warp 13
+constexpr int NTHREADS = NCHAIN + NLOAD + NISSUE + NCOPY;
 constexpr int NKQ = 3;           // K/Q/V ring depth (chunks)
-constexpr int NF = 2;            // factor ring depth (chunks)
 constexpr uint32_t BAR_CHAIN = 1, BAR_LOW = 2, BAR_LOAD = 3;  // named barriers
 constexpr int NLOW = 128;        // chain threads of TMEM lanes 0-63 (warps 0, 1, 4, 5)
 
@@ -70,45 +80,55 @@ constexpr uint32_t KQ_BYTES = 32768;  // [K rows 0-63; Q rows 64-127] x 2 K-halv
 constexpr uint32_t V_BYTES = 64 * BV * 2;                 // 64 tokens x 32 columns, 64-B swizzled rows
 constexpr uint32_t OFF_KQ = 0;
 constexpr uint32_t OFF_V = OFF_KQ + NKQ * KQ_BYTES;
-constexpr uint32_t OFF_F = OFF_V + NKQ * V_BYTES;         // factor slots (fac::SLOT_BYTES each)
-constexpr uint32_t OFF_ATP = ((OFF_F + NF * fac::SLOT_BYTES + 1023) / 1024) * 1024;
-constexpr uint32_t OFF_ATP_LO = OFF_ATP + 16384;          // [T; PT] hi / lo, K-major 128 x 64 bf16
-constexpr uint32_t OFF_S = OFF_ATP + 32768;               // [S_hi | S_lo]: 128 (k) rows x 64 bf16, MN-major
+// The operand ring: NOP slots of one 16 KB A-operand tile (K-major 128 x 64 bf16,
+// 128-byte swizzled), filled in the order the MMAs read them: per chunk c the
+// [Tw; PTw] hi and lo tiles (MMA2), then, unless c is the last chunk, X_c's hi
+// and lo tiles (MMA_X).  Item i of that sequence sits in slot i % NOP, so each
+// copy can start as soon as the item NOP places earlier has been read: at least
+// a chunk ahead of its use.
+constexpr int NOP = 5;
+constexpr uint32_t OP_BYTES = 16384;
+constexpr uint32_t OFF_OPS = OFF_V + NKQ * V_BYTES;
+constexpr uint32_t OFF_S = OFF_OPS + NOP * OP_BYTES;      // [S'_hi | S'_lo]: 128 (k) rows x 64 bf16, MN-major
 constexpr uint32_t OFF_R = OFF_S + 16384;                 // [R_hi | R_lo]: 64 (token) rows x 64 bf16
 constexpr uint32_t OFF_DT = OFF_R + 8192;                 // [D~_hi | D~_lo]: 64 rows x 64 bf16
-constexpr uint32_t OFF_SMALL = OFF_DT + 8192;
+constexpr uint32_t OFF_GATES = OFF_DT + 8192;             // exp(G) of two chunks, 64 floats each
+constexpr uint32_t OFF_SMALL = OFF_GATES + 2 * 256;
 constexpr uint32_t SM_BARS = OFF_SMALL;                   // NBARS x uint64
 constexpr uint32_t SM_TMEM = OFF_SMALL + 192;
 constexpr uint32_t SM_ABORT = OFF_SMALL + 200;
 constexpr uint32_t SMEM_USED = OFF_SMALL + 256;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(OFF_V % 1024 == 0 && OFF_ATP % 1024 == 0 && OFF_S % 1024 == 0 && OFF_R % 1024 == 0 &&
-                  OFF_DT % 1024 == 0 && OFF_F % 16 == 0,
+static_assert(OFF_V % 1024 == 0 && OFF_OPS % 1024 == 0 && OFF_S % 1024 == 0 &&
+                  OFF_R % 1024 == 0 && OFF_DT % 1024 == 0 && OFF_GATES % 16 == 0,
               "operand tiles must be 1 KB aligned, bulk copies 16 B aligned");
 
-// mbarriers
+// mbarriers.  Each completes one phase per use; no waiter can fall two phases
+// behind (the comments give what orders the next use after every wait).
 constexpr int B_KQ_FULL = 0;                // NKQ: K, Q, V tiles landed
-constexpr int B_KQ_EMPTY = B_KQ_FULL + NKQ; // NKQ: chain done with the tiles
-constexpr int B_F_FULL = B_KQ_EMPTY + NKQ;  // NF: factor slot landed
-constexpr int B_F_EMPTY = B_F_FULL + NF;    // NF: chain done with the slot (its gates)
-constexpr int B_ATP_FULL = B_F_EMPTY + NF;  // [T; PT] operand tiles unpacked
-constexpr int B_ATP_FREE = B_ATP_FULL + 1;  // MMA2 has read them
-// MMA1, MMA2, MMA3 each complete one phase of their own barrier per chunk, so a
-// warp that reaches a wait late can never see a later group's phase instead.
-constexpr int B_MMA1 = B_ATP_FREE + 1, B_MMA2 = B_MMA1 + 1, B_MMA3 = B_MMA2 + 1;
-constexpr int NBARS = B_MMA3 + 1;
+constexpr int B_KQ_EMPTY = B_KQ_FULL + NKQ; // NKQ: MMA3 of the chunk done (its tiles free)
+constexpr int B_G_FULL = B_KQ_EMPTY + NKQ; // 2: a chunk's gates landed
+constexpr int B_G_EMPTY = B_G_FULL + 2;     // 2: chain and loader done with a chunk's gates
+constexpr int B_A_FULL = B_G_EMPTY + 2;    // 2: a chunk's [Tw; PTw] hi and lo tiles landed (two arrivals)
+constexpr int B_X_FULL = B_A_FULL + 2;     // 2: a chunk's X hi and lo tiles landed (two arrivals)
+constexpr int B_OP_FREE = B_X_FULL + 2;    // NOP: an operand-ring slot's MMAs have read it
+constexpr int B_S_READY = B_OP_FREE + NOP; // S_c formed and S' = e^gamma_c S_c written (for MMA1')
+constexpr int B_ACC = B_S_READY + 1;        // a chunk's accumulator A_c complete
+constexpr int B_MMA2 = B_ACC + 1;           // [D~; P D] ready
+constexpr int B_Y = B_MMA2 + 1;             // Kᵀ D~ ready
+constexpr int NBARS = B_Y + 1;
 static_assert(NBARS * 8 <= 192, "barrier space");
 
 // TMEM columns (fp32 accumulators, lane = row).  Each holds [hi-part | lo-part]
 // products of a thread's 16 columns in 32 consecutive columns; readers add the
 // two halves.
-constexpr uint32_t TM_KS = 0;    // [K S; Q S]
-constexpr uint32_t TM_D = 64;    // [D; P D] = [T; PT]_hi R + [T; PT]_lo R
-constexpr uint32_t TM_Y = 128;   // Kᵀ D~
+constexpr uint32_t TM_ACC = 0;     // + 64 (c % 2): A_c = [K S; Q S] of chunk c
+constexpr uint32_t TM_D = 128;     // [D~; P D] = [Tw; PTw]_hi R + [Tw; PTw]_lo R
+constexpr uint32_t TM_Y = 192;     // Kᵀ D~
 constexpr uint32_t TM_COLS = 256;  // allocation (a power of two)
-constexpr int ISSUE_WARP = 2;          // lane 0 issues every MMA; a Q / PT-row warp (TMEM lanes 64-95)
-constexpr int NLOW_SYNC = NLOW + 32;  // BAR_LOW: the K / T-row threads and the issuing warp
+constexpr int NLOW_SYNC = NLOW + NISSUE;     // BAR_LOW: the K / T-row threads and the issuing warp
+constexpr int NCHAIN_SYNC = NCHAIN + NISSUE; // BAR_CHAIN: the chain and the issuing warp
 
 constexpr uint32_t KQV_TX = 2 * 16384 + V_BYTES;
 constexpr long long kWaitLimit = 4000000000LL;  // SM clocks (about 2 s)
@@ -121,7 +141,8 @@ struct TcParams {
     int c_lo, c_hi;  // chunks of each sequence to process; the state is read before and written after them
     float scale;
     const int32_t *cu_seqlens;
-    const float *ws;  // factor slots
+    const uint8_t *ws;     // factor slots
+    const uint8_t *xs;     // X tiles
     float *state;
     void *o;
 };
@@ -132,9 +153,7 @@ struct Ctx {
     uint32_t tmem;
     volatile int *abort_flag;
     __device__ uint32_t bar(int i) const { return sbase + SM_BARS + 8 * i; }
-    __device__ const float *fslot(int fb) const {
-        return reinterpret_cast<const float *>(sm + OFF_F + fb * fac::SLOT_BYTES);
-    }
+    __device__ const float *gates(int gb) const { return reinterpret_cast<const float *>(sm + OFF_GATES + 256 * gb); }
 };
 
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
@@ -193,6 +212,7 @@ __device__ __forceinline__ void store_hilo_row16(uint8_t *tile, int row, int j0,
     }
 }
 
+// One ring stage: K and Q (d_k halves, 128-byte swizzled) and this CTA's V columns.
 __device__ __forceinline__ void issue_kq_loads(const Ctx &x, int kb, int tok, int hq, int h, int cb,
                                                const CUtensorMap *tmK, const CUtensorMap *tmQ,
                                                const CUtensorMap *tmV) {
@@ -206,81 +226,161 @@ __device__ __forceinline__ void issue_kq_loads(const Ctx &x, int kb, int tok, in
     tma_load_3d(x.sbase + OFF_V + kb * V_BYTES, tmV, bar, cb * BV, h, tok);
 }
 
-__device__ __forceinline__ void issue_factor_load(const Ctx &x, int fb, const float *src) {
-    const uint32_t bar = x.bar(B_F_FULL + fb);
-    mbar_arrive_expect_tx(bar, fac::SLOT_BYTES);
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            x.sbase + OFF_F + fb * fac::SLOT_BYTES),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"((uint32_t)fac::SLOT_BYTES), "r"(bar)
-        : "memory");
+// The barrier that item i's copy completes: both tiles of a pair (hi, lo) land
+// on one barrier of two arrivals, so the issuer waits once per pair.
+__device__ __forceinline__ uint32_t op_full_bar(const Ctx &x, int i) {
+    return x.bar(((i & 2) ? B_X_FULL : B_A_FULL) + ((i >> 2) & 1));
+}
+// Item i of the operand ring: the 16 KB tile at `src` into slot i % NOP.
+__device__ __forceinline__ void issue_op_load(const Ctx &x, int i, const uint8_t *src) {
+    const uint32_t bar = op_full_bar(x, i);
+    mbar_arrive_expect_tx(bar, OP_BYTES);
+    bulk_load(x.sbase + OFF_OPS + (i % NOP) * OP_BYTES, src, OP_BYTES, bar);
+}
+// A slot's exp(G) (64 floats) into gates ring buffer gb.
+__device__ __forceinline__ void issue_gates_load(const Ctx &x, const uint8_t *slot, int gb) {
+    mbar_arrive_expect_tx(x.bar(B_G_FULL + gb), 256);
+    bulk_load(x.sbase + OFF_GATES + 256 * gb, slot + fac::OFF_EG, 256, x.bar(B_G_FULL + gb));
+}
+// Operand-ring items: 4 c + 0 / 1 are the [Tw; PTw] hi / lo tiles of chunk c,
+// 4 c + 2 / 3 X_c's hi / lo tiles (only while c + 1 < nchunks).
+__device__ __forceinline__ bool op_exists(int i, int nchunks) {
+    const int c = i >> 2;
+    return (i & 2) ? c + 1 < nchunks : c < nchunks;
 }
 
 __device__ __forceinline__ uint32_t lane_base(uint32_t tmem, int warp) {
     return tmem + ((uint32_t)((warp & 3) * 32) << 16);
 }
 
-// ================================ loader ============================================
-// One thread issues every TMA; all 128 unpack [T; PT] (packed fp32 triangles)
-// into the hi/lo K-major operand tiles.  Rows t and 63 - t of T (or of PT)
-// hold 9 chunks of 8 between them; two threads share each such pair, 5 and 4
-// chunks, so every thread does the same work.  Chunks right of a row's
-// diagonal chunk stay zero from the start.
-__device__ void loader_role(const Ctx &x, const TcParams &p, int64_t t0, int nchunks, int64_t slot0, int h,
-                            int hq, int cb, const CUtensorMap *tmK, const CUtensorMap *tmQ,
-                            const CUtensorMap *tmV, int lt) {
-    const float *fsrc = p.ws + ((size_t)slot0 * p.h_v + h) * fac::SLOT_FLOATS;
-    const size_t fstride = (size_t)p.h_v * fac::SLOT_FLOATS;
-    if (lt == 0) {
-        for (int c = 0; c < nchunks && c < NKQ; ++c) issue_kq_loads(x, c, (int)(t0 + c * C), hq, h, cb, tmK, tmQ, tmV);
-        for (int c = 0; c < nchunks && c < NF; ++c) issue_factor_load(x, c, fsrc + c * fstride);
+// ================================ copies ============================================
+// Warp 13, one thread: every copy into shared memory, in the order in which the
+// chain frees the buffers.  Before the loop: operand items 0-4, the gates of
+// chunks 0 and 1, the K/Q/V tiles of chunks 0-2, and L2 prefetches of the next
+// slots and X tiles.  Per chunk c, in the order the buffers come free: chunk
+// c+2's K/Q/V tiles (MMA3 of chunk c-1 done), operand items 4c+5 and 4c+6 (MMA2
+// of chunk c done), the gates of chunk c+2 (the chain and the loader done with
+// chunk c's), operand items 4c+7 and 4c+8 (MMA_X of chunk c done).
+__device__ void copy_role(const Ctx &x, const TcParams &p, int64_t t0, int nchunks, int64_t slot0, int h,
+                          int hq, int cb, const CUtensorMap *tmK, const CUtensorMap *tmQ, const CUtensorMap *tmV) {
+    const uint8_t *fsrc = p.ws + ((size_t)slot0 * p.h_v + h) * fac::SLOT_BYTES;
+    const size_t fstride = (size_t)p.h_v * fac::SLOT_BYTES;
+    // X tiles of chunk c (X_c = [K; Q]_c+1 K_cᵀ) sit with the slot of chunk c + 1
+    const uint8_t *xsrc = p.xs + ((size_t)(slot0 + 1) * p.h_qk + hq) * fac::X_BYTES;
+    const size_t xstride = (size_t)p.h_qk * fac::X_BYTES;
+    auto op_src = [&](int i) -> const uint8_t * {
+        const int c = i >> 2;
+        return (i & 2) ? xsrc + c * xstride + (i & 1) * fac::X_TILE_BYTES
+                       : fsrc + c * fstride + ((i & 1) ? fac::OFF_LO : fac::OFF_HI);
+    };
+    bool bad = false;
+    // item i once item i - NOP (same slot) has been read
+    auto next_op = [&](int i) {
+        if (bad || !op_exists(i, nchunks)) return;
+        if (i >= NOP) bad = !wait_or_abort(x, x.bar(B_OP_FREE + i % NOP), (uint32_t)(i / NOP - 1) & 1u);
+        if (!bad) issue_op_load(x, i, op_src(i));
+        if (!bad && op_exists(i + 8, nchunks)) prefetch_l2(op_src(i + 8), OP_BYTES);  // two chunks ahead
+    };
+    for (int i = 0; i < NOP; ++i) next_op(i);
+    for (int c = 0; c < nchunks && c < 2; ++c) issue_gates_load(x, fsrc + c * fstride, c);
+    for (int c = 0; c < nchunks && c < NKQ; ++c) issue_kq_loads(x, c, (int)(t0 + c * C), hq, h, cb, tmK, tmQ, tmV);
+    for (int i = NOP; i < NOP + 3; ++i)
+        if (op_exists(i + 3, nchunks)) prefetch_l2(op_src(i + 3), OP_BYTES);
+    for (int c = 0; c < nchunks && !bad; ++c) {
+        if (c >= 1 && c - 1 + NKQ < nchunks) {
+            const int kb = (c - 1) % NKQ;
+            bad = !wait_or_abort(x, x.bar(B_KQ_EMPTY + kb), (uint32_t)((c - 1) / NKQ) & 1u);
+            if (!bad) issue_kq_loads(x, kb, (int)(t0 + (c - 1 + NKQ) * C), hq, h, cb, tmK, tmQ, tmV);
+        }
+        next_op(4 * c + 5);
+        next_op(4 * c + 6);
+        if (!bad && c + 2 < nchunks) {
+            bad = !wait_or_abort(x, x.bar(B_G_EMPTY + (c & 1)), (uint32_t)(c >> 1) & 1u);
+            if (!bad) issue_gates_load(x, fsrc + (c + 2) * fstride, c & 1);
+        }
+        next_op(4 * c + 7);
+        next_op(4 * c + 8);
     }
-    const int pr = lt >> 1, hf = lt & 1;
-    const int ta = pr & 31, tb = 63 - ta, nch_a = (ta >> 3) + 1;
-    const int mat = pr < 32 ? fac::OFF_T : fac::OFF_PT, rbase = pr < 32 ? 0 : 64;
-    uint8_t *hi = x.sm + OFF_ATP, *lo = x.sm + OFF_ATP_LO;
-    for (int c = 0; c < nchunks; ++c) {
-        const int fb = c % NF;
-        bool bad = !wait_or_abort(x, x.bar(B_F_FULL + fb), (uint32_t)(c / NF) & 1u);
-        if (c > 0 && !bad) bad = !wait_or_abort(x, x.bar(B_ATP_FREE), (uint32_t)(c - 1) & 1u);
-        if (!bad) {
-            const float *f = x.fslot(fb) + mat;
+}
+
+// ================================ loader ============================================
+// The loader warps own the state: thread lt keeps row lt (a d_k index) of the
+// CTA's 128 x 32 block in registers, reads its row of each Y = K_cᵀ D~_c from
+// TMEM (warp 8 + i reads lanes 32 i .. 32 i + 31) and writes the bf16 hi/lo
+// operand S' = e^gamma_c S_c that MMA1' reads.  Per chunk c:
+//   S_c = e^gamma_c-1 S_c-1 + Y_c-1 (once MMA3 of chunk c-1 is done; for c = 0,
+//   once A_0 has read the S_0 tile), S' = e^gamma_c S_c.
+__device__ void loader_role(const Ctx &x, int nchunks, int lt, float *Sg, bool &ok) {
+    const uint32_t lb = lane_base(x.tmem, lt >> 5);  // warp 8 + i: lanes 32 i ..
+    float Sr[32];  // state row lt, the CTA's 32 columns (S_0 was loaded into the S tile)
 #pragma unroll
-            for (int i = 0; i < 5; ++i) {
-                const int k = 5 * hf + i;
-                if (k < 9) {
-                    const bool in_a = k < nch_a;
-                    const int t = in_a ? ta : tb, j = in_a ? k : k - nch_a;
-                    const float *src = f + fac::tri8_base(t) + 8 * j;
-                    const float4 u = *reinterpret_cast<const float4 *>(src);
-                    const float4 v = *reinterpret_cast<const float4 *>(src + 4);
-                    const float xv[8] = {u.x, u.y, u.z, u.w, v.x, v.y, v.z, v.w};
-                    uint32_t hw[4], lw[4];
-                    hilo_words(xv, hw, lw);
-                    const uint32_t off = sw128_offset(rbase + t, j);
-                    *reinterpret_cast<uint4 *>(hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4 *>(lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    for (int j = 0; j < 32; j += 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(Sg + j);
+        Sr[j] = v.x;
+        Sr[j + 1] = v.y;
+        Sr[j + 2] = v.z;
+        Sr[j + 3] = v.w;
+    }
+    bool bad = false;
+    float eGC_prev = 1.f;  // exp(gamma) of the previous chunk
+    for (int c = 0; c < nchunks; ++c) {
+        const int gb = c & 1;
+        if (!bad) bad = !wait_or_abort(x, x.bar(B_G_FULL + gb), (uint32_t)(c >> 1) & 1u);
+        const float eGC = x.gates(gb)[C - 1];
+        if (c > 0) {
+            if (!bad) bad = !wait_or_abort(x, x.bar(B_Y), (uint32_t)(c - 1) & 1u);
+            tc_fence_after_sync();
+            if (!bad) {
+#pragma unroll
+                for (int g2 = 0; g2 < 2; ++g2) {
+                    float y[16];
+                    acc_sum1(lb, TM_Y, 16 * g2, y);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) Sr[16 * g2 + j] = fmaf(eGC_prev, Sr[16 * g2 + j], y[j]);
                 }
+            }
+        } else if (!bad) {
+            bad = !wait_or_abort(x, x.bar(B_ACC), 0u);  // A_0 has read the S_0 tile
+        }
+        if (!bad && c + 1 < nchunks) {
+#pragma unroll
+            for (int g2 = 0; g2 < 2; ++g2) {
+                float sp[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) sp[j] = eGC * Sr[16 * g2 + j];
+                store_hilo_row16(x.sm + OFF_S, lt, 16 * g2, sp);
             }
             fence_proxy_async_smem();
         }
+        tc_fence_before_sync();
         named_sync(BAR_LOAD, NLOAD);
-        if (lt == 0 && !bad) {
-            mbar_arrive(x.bar(B_ATP_FULL));
-            // refill the ring slots the chain released with chunk c-1
-            if (c >= 1) {
-                const int kb = (c - 1) % NKQ, pf = (c - 1) % NF;
-                if (c - 1 + NKQ < nchunks) {
-                    bad = !wait_or_abort(x, x.bar(B_KQ_EMPTY + kb), (uint32_t)((c - 1) / NKQ) & 1u);
-                    if (!bad) issue_kq_loads(x, kb, (int)(t0 + (c - 1 + NKQ) * C), hq, h, cb, tmK, tmQ, tmV);
-                }
-                if (!bad && c - 1 + NF < nchunks) {
-                    bad = !wait_or_abort(x, x.bar(B_F_EMPTY + pf), (uint32_t)((c - 1) / NF) & 1u);
-                    if (!bad) issue_factor_load(x, pf, fsrc + (c - 1 + NF) * fstride);
-                }
-            }
+        // every chunk, also the last: the issuer waits for it before MMA3, so Y of this
+        // chunk cannot complete before this role has waited for Y of the last; and
+        // before it releases this chunk's gates
+        if (lt == 0 && !bad) mbar_arrive(x.bar(B_S_READY));
+        eGC_prev = eGC;
+        if (named_sync_or(BAR_LOAD, NLOAD, bad || *x.abort_flag)) {
+            bad = true;
+            break;
         }
-        if (named_sync_or(BAR_LOAD, NLOAD, bad || *x.abort_flag)) break;
+    }
+    // the state after the last chunk
+    if (!bad) bad = !wait_or_abort(x, x.bar(B_Y), (uint32_t)(nchunks - 1) & 1u);
+    tc_fence_after_sync();
+    if (!bad) {
+#pragma unroll
+        for (int g2 = 0; g2 < 2; ++g2) {
+            float y[16];
+            acc_sum1(lb, TM_Y, 16 * g2, y);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) Sr[16 * g2 + j] = fmaf(eGC_prev, Sr[16 * g2 + j], y[j]);
+        }
+    }
+    ok = !bad;
+    if (ok && *x.abort_flag == 0) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4 *>(Sg + j) = make_float4(Sr[j], Sr[j + 1], Sr[j + 2], Sr[j + 3]);
     }
 }
 
@@ -301,60 +401,142 @@ __device__ __forceinline__ void store_out_row(const TcParams &p, int64_t c0, int
     }
 }
 
+// ================================= issuer ===========================================
+// Warp 12 issues every MMA: the whole warp runs the issue code and its waits,
+// converged, and one elected lane issues (a lone divergent thread blocks
+// several times longer per MMA).  Per chunk c, in the tensor pipe's order:
+//   MMA2 (once the K / T-row warps hand it R at BAR_LOW),
+//   MMA1' = [K; Q]_c+1 S' into A_c+1 (once the loader has written S'),
+//   MMA_X = X_c [D~_hi | D~_lo] into A_c+1 and MMA3 = K_cᵀ [D~_hi | D~_lo]
+//   (once the chain has written D~ and read [D~; P D], at BAR_CHAIN).
+
+// [K; Q] (a ring stage) times a [hi | lo] B operand: 8 k-steps over d_k.
+__device__ __forceinline__ void issue_kq_times(uint32_t d_tmem, uint32_t kq, uint64_t dB) {
+    const uint64_t a0 = smem_desc_sw128(kq, 16, 1024);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+        mma_bf16(d_tmem, desc_add(a0, (ks >> 2) * 16384 + (ks & 3) * 32), desc_add(dB, ks * 2048), IDESC_N64,
+                 ks > 0);
+}
+
+// The EMPTY / FREE commits are made only for buffers that will be filled again.
+__device__ void issuer_role(const Ctx &x, int nchunks, int lane) {
+    const uint32_t tmem = x.tmem;
+    const uint64_t dS = smem_desc(x.sbase + OFF_S, 8192, 1024, kSwizzle128);
+    const uint64_t dR = smem_desc(x.sbase + OFF_R, 8192, 1024, kSwizzle128);
+    const uint64_t dDT = smem_desc(x.sbase + OFF_DT, 8192, 1024, kSwizzle128);
+    const uint64_t dOp0 = smem_desc_sw128(x.sbase + OFF_OPS, 16, 1024);
+    bool bad = false;  // warp-uniform
+    // the hi and lo tiles of pair i, i + 1 (i = 4 c or 4 c + 2) times [B_hi | B_lo],
+    // four k-steps each, into d_tmem: the pair is awaited once (the whole warp) and
+    // each slot released once read (if it is reused)
+    auto pair_mmas = [&](int i, uint32_t d_tmem, uint64_t dB, bool acc_first) {
+        bad = bad || __any_sync(0xffffffffu, !wait_or_abort(x, op_full_bar(x, i), (uint32_t)(i >> 3) & 1u));
+        if (bad) return;
+        tc_fence_after_sync();
+        if (elect_one()) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int slot = (i + h) % NOP;
+                const uint64_t dA = desc_add(dOp0, slot * OP_BYTES);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(d_tmem, desc_add(dA, ks * 32), desc_add(dB, ks * 2048), IDESC_N64,
+                             acc_first || h > 0 || ks > 0);
+                if (op_exists(i + h + NOP, nchunks)) mma_commit(x.bar(B_OP_FREE + slot));
+            }
+        }
+        __syncwarp();
+    };
+    // A_0 = [K; Q]_0 [S_hi | S_lo] (the S tile holds S_0)
+    bad = __any_sync(0xffffffffu, !wait_or_abort(x, x.bar(B_KQ_FULL + 0), 0u));
+    if (!bad) {
+        tc_fence_after_sync();
+        if (elect_one()) {
+            issue_kq_times(tmem + TM_ACC, x.sbase + OFF_KQ, dS);
+            mma_commit(x.bar(B_ACC));
+        }
+        __syncwarp();
+    }
+    for (int c = 0; c < nchunks; ++c) {
+        const int kb = c % NKQ, ab = c & 1;
+        const uint32_t par = (uint32_t)c & 1u;
+        const bool more = c + 1 < nchunks;
+        named_sync(BAR_LOW, NLOW_SYNC);  // R written
+        // ---- MMA2: [D~; P D] = [Tw; PTw]_hi [R_hi | R_lo] + [Tw; PTw]_lo [R_hi | R_lo] -----
+        pair_mmas(4 * c, tmem + TM_D, dR, false);
+        if (!bad) {
+            if (elect_one()) mma_commit(x.bar(B_MMA2));
+            __syncwarp();
+        }
+        // ---- MMA1': A_c+1 = [K; Q]_c+1 [S'_hi | S'_lo] -------------------------------------
+        if (!bad) bad = __any_sync(0xffffffffu, !wait_or_abort(x, x.bar(B_S_READY), par));
+        if (more && !bad) {
+            bad = __any_sync(0xffffffffu, !wait_or_abort(x, x.bar(B_KQ_FULL + (c + 1) % NKQ),
+                                                         (uint32_t)((c + 1) / NKQ) & 1u));
+            if (!bad) {
+                tc_fence_after_sync();
+                if (elect_one())
+                    issue_kq_times(tmem + TM_ACC + 64 * (ab ^ 1), x.sbase + OFF_KQ + ((c + 1) % NKQ) * KQ_BYTES, dS);
+                __syncwarp();
+            }
+        }
+        const bool stop = named_sync_or(BAR_CHAIN, NCHAIN_SYNC, bad || *x.abort_flag);  // D~ written
+        if (stop) break;
+        if (lane == 0) mbar_arrive(x.bar(B_G_EMPTY + (c & 1)));  // the chain has read the gates of chunk c
+        // ---- MMA_X: A_c+1 += X_c [D~_hi | D~_lo]; MMA3: Y = K_cᵀ [D~_hi | D~_lo] ----------
+        if (more) {
+            pair_mmas(4 * c + 2, tmem + TM_ACC + 64 * (ab ^ 1), dDT, true);
+        }
+        if (!bad) {
+            tc_fence_after_sync();
+            if (elect_one()) {
+                if (more) mma_commit(x.bar(B_ACC));
+                const uint64_t a0 = smem_desc_sw128(x.sbase + OFF_KQ + kb * KQ_BYTES, 16384, 1024);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    mma_bf16(tmem + TM_Y, desc_add(a0, ks * 2048), desc_add(dDT, ks * 2048), IDESC_Y, ks > 0);
+                mma_commit(x.bar(B_Y));
+                // every MMA reading this chunk's tiles is issued
+                if (c + NKQ < nchunks) mma_commit(x.bar(B_KQ_EMPTY + kb));
+            }
+            __syncwarp();
+        }
+    }
+}
+
 // ================================= chain ============================================
-// One thread, lane 0 of warp 2, issues every MMA.  That warp holds Q / PT rows,
-// which are off the chunk-to-chunk path: the K / T-row warps never wait behind
-// an MMA issue, and the issuing warp joins the K / T-row barrier (BAR_LOW) that
-// hands it R and D~.  It stores a chunk's outputs only after the next chunk's
-// MMA1 has been issued (global stores ahead of it delay the issue).
+// Warps 0-7.  Warp w owns TMEM lanes 32 (w % 4) .. + 31 (chunk rows: K/T rows
+// in lanes 0-63, Q/PT rows in lanes 64-127) and columns 16 (w / 4) .. + 15 of
+// the CTA's 32.  Per chunk: the K / T-row warps form R from A_c and hand it to
+// the issuer (BAR_LOW), then write D~ from MMA2's accumulator; the Q / PT-row
+// warps form the outputs and store them after the chunk's last barrier.
 __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t t1, int nchunks, int h,
-                           int cb, float *Sr, int tid, bool &ok) {
+                           int cb, int tid, bool &ok) {
     const int warp = tid >> 5, lane = tid & 31;
     const int j0 = 16 * (warp >> 2);           // this thread's 16 columns of the CTA's 32
     const int row = ((warp & 3) << 5) + lane;  // TMEM lane
     const bool low = row < 64;                 // K / T rows (on the chunk-to-chunk path)
     const int t = row & 63;
-    const bool iwarp = warp == ISSUE_WARP;     // joins BAR_LOW
-    const bool issuer = iwarp && lane == 0;
     const uint32_t lb = lane_base(x.tmem, warp);
-    const uint32_t tmem = x.tmem;
-    const uint64_t dS = smem_desc(x.sbase + OFF_S, 8192, 1024, kSwizzle128);
-    const uint64_t dR = smem_desc(x.sbase + OFF_R, 8192, 1024, kSwizzle128);
-    const uint64_t dDT = smem_desc(x.sbase + OFF_DT, 8192, 1024, kSwizzle128);
-    const uint64_t dAh = smem_desc_sw128(x.sbase + OFF_ATP, 16, 1024);
-    const uint64_t dAl = smem_desc_sw128(x.sbase + OFF_ATP_LO, 16, 1024);
     bool bad = false;
-    float ov[16];      // lanes 64-127: a chunk's outputs, stored after its last barrier
-    int64_t ov_c0 = 0; // first token of the chunk whose outputs ov holds
-    int ov_len = 0;    // its number of real rows (0: nothing pending)
+    // every thread runs every named barrier of every chunk; only the CTA-wide
+    // stop decided at BAR_CHAIN ends the loop early
     for (int c = 0; c < nchunks; ++c) {
-        const int kb = c % NKQ, fb = c % NF;
+        const int kb = c % NKQ, gb = c & 1, ab = c & 1;
         const int64_t c0 = t0 + (int64_t)c * C;
         const int L = (int)((t1 - c0) < C ? (t1 - c0) : C);
-        const uint32_t kq = x.sbase + OFF_KQ + kb * KQ_BYTES;
         const uint32_t par = (uint32_t)c & 1u;
-        bad = !wait_or_abort(x, x.bar(B_KQ_FULL + kb), (uint32_t)(c / NKQ) & 1u);
-        // ---- MMA1: [K S; Q S] = [K; Q] [S_hi | S_lo], 8 k-steps over d_k ----------------
-        if (issuer && !bad) {
-            tc_fence_after_sync();
-            const uint64_t a0 = smem_desc_sw128(kq, 16, 1024);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                mma_bf16(tmem + TM_KS, desc_add(a0, (ks >> 2) * 16384 + (ks & 3) * 32), desc_add(dS, ks * 2048),
-                         IDESC_N64, ks > 0);
-            mma_commit(x.bar(B_MMA1));
-        }
-        if (iwarp && t < ov_len) store_out_row(p, ov_c0, t, h, cb, j0, ov);
-        if (!bad) bad = !wait_or_abort(x, x.bar(B_F_FULL + fb), (uint32_t)(c / NF) & 1u);
-        const float *egs = x.fslot(fb) + fac::OFF_EG;  // exp(G)
-        const float egt = egs[t], eGC = egs[C - 1];
-        if (issuer && !bad) bad = !wait_or_abort(x, x.bar(B_ATP_FULL), par);
-        if (!bad) bad = !wait_or_abort(x, x.bar(B_MMA1), par);
+        if (!bad) bad = !wait_or_abort(x, x.bar(B_KQ_FULL + kb), (uint32_t)(c / NKQ) & 1u);  // V
+        if (!bad) bad = !wait_or_abort(x, x.bar(B_G_FULL + gb), (uint32_t)(c >> 1) & 1u);
+        const float egt = x.gates(gb)[t];
+        // ---- A_c complete: R = V - e^G K S_c ---------------------------------------------
+        if (!bad) bad = !wait_or_abort(x, x.bar(B_ACC), par);
         tc_fence_after_sync();
         float qse[16];  // lanes 64-127: e^G Q S, kept for the output
         {
             float ks[16];
-            if (!bad) acc_sum1(lb, TM_KS, j0, ks);
+            if (!bad) acc_sum1(lb, TM_ACC + 64 * ab, j0, ks);
             if (low) {
                 if (!bad) {
                     // R = V - e^G K S as [R_hi | R_lo]
@@ -370,27 +552,17 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
                     store_hilo_row16(x.sm + OFF_R, t, j0, r);
                     fence_proxy_async_smem();
                 }
+                tc_fence_before_sync();
+                named_sync(BAR_LOW, NLOW_SYNC);
             } else {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) qse[j] = egt * ks[j];
             }
         }
-        if (low || iwarp) {
-            tc_fence_before_sync();
-            named_sync(BAR_LOW, NLOW_SYNC);
-        }
-        // ---- MMA2: [D~; P D] = [Tw; PTw]_hi [R_hi | R_lo] + [Tw; PTw]_lo [R_hi | R_lo] -----
-        if (issuer && !bad) {
-            tc_fence_after_sync();
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                mma_bf16(tmem + TM_D, desc_add(ks < 4 ? dAh : dAl, (ks & 3) * 32), desc_add(dR, (ks & 3) * 2048),
-                         IDESC_N64, ks > 0);
-            mma_commit(x.bar(B_MMA2));
-            mma_commit(x.bar(B_ATP_FREE));
-        }
+        // ---- [D~; P D] from MMA2 ----------------------------------------------------------
         if (!bad) bad = !wait_or_abort(x, x.bar(B_MMA2), par);
         tc_fence_after_sync();
+        float ov[16];
         {
             float d[16];
             if (!bad) acc_sum1(lb, TM_D, j0, d);
@@ -406,46 +578,15 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
                 for (int j = 0; j < 16; ++j) ov[j] = p.scale * (qse[j] + d[j]);
             }
         }
-        if (low || iwarp) {
-            tc_fence_before_sync();
-            named_sync(BAR_LOW, NLOW_SYNC);
-        }
-        // ---- MMA3: Y = Kᵀ [D~_hi | D~_lo], 4 token k-steps ------------------------------
-        if (issuer && !bad) {
-            tc_fence_after_sync();
-            const uint64_t a0 = smem_desc_sw128(kq, 16384, 1024);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tmem + TM_Y, desc_add(a0, ks * 2048), desc_add(dDT, ks * 2048), IDESC_Y, ks > 0);
-            mma_commit(x.bar(B_MMA3));
-        }
-        if (!bad) bad = !wait_or_abort(x, x.bar(B_MMA3), par);
-        tc_fence_after_sync();
-        if (!bad) {
-            // S <- exp(G_C) S + Kᵀ D~, and its [S_hi | S_lo] operand copy
-            float y[16];
-            acc_sum1(lb, TM_Y, j0, y);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) Sr[j] = fmaf(eGC, Sr[j], y[j]);
-            store_hilo_row16(x.sm + OFF_S, row, j0, Sr);
-            fence_proxy_async_smem();
-        }
         tc_fence_before_sync();
-        const bool stop = named_sync_or(BAR_CHAIN, NCHAIN, bad || *x.abort_flag);
-        if (tid == 0 && !stop) {
-            mbar_arrive(x.bar(B_KQ_EMPTY + kb));
-            mbar_arrive(x.bar(B_F_EMPTY + fb));
-        }
+        const bool stop = named_sync_or(BAR_CHAIN, NCHAIN_SYNC, bad || *x.abort_flag);
         if (stop) {
             bad = true;
             break;
         }
         // outputs of the chunk's real rows (after the barrier, so no proxy fence waits on them)
-        if (!low && !iwarp && t < L) store_out_row(p, c0, t, h, cb, j0, ov);
-        ov_c0 = c0;
-        ov_len = L;
+        if (!low && t < L) store_out_row(p, c0, t, h, cb, j0, ov);
     }
-    if (!bad && iwarp && t < ov_len) store_out_row(p, ov_c0, t, h, cb, j0, ov);
     ok = !bad;
 }
 
@@ -477,7 +618,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (tid == 0) {
-        for (int i = 0; i < NBARS; ++i) mbar_init(x.bar(i), 1);
+        for (int i = 0; i < NBARS; ++i) mbar_init(x.bar(i), i >= B_A_FULL && i < B_A_FULL + 4 ? 2 : 1);
         *x.abort_flag = 0;
         fence_mbar_init();
     }
@@ -485,25 +626,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_alloc(smem_u32(tmem_holder), TM_COLS);
         tmem_relinquish();
     }
-    // chain thread: state row `srow` (a d_k index), columns [j0, j0 + 16) of the CTA's block
-    const int srow = ((warp & 3) << 5) + lane, j0 = 16 * ((warp >> 2) & 1);
-    float Sr[16];
-    float *Sg = p.state + (((size_t)s * p.h_v + h) * D + srow) * D + cb * BV + j0;
-    if (tid < NCHAIN) {
+    // loader thread lt: state row lt (a d_k index), the CTA's 32 columns
+    const int lt = tid - NCHAIN;
+    const bool loader = lt >= 0 && lt < NLOAD;
+    const bool issuer = warp == (NCHAIN + NLOAD) / 32;
+    float *Sg = p.state + (((size_t)s * p.h_v + h) * D + (loader ? lt : 0)) * D + cb * BV;
+    if (loader) {
+        // S_0 into the S tile (the loader role reads its row again into registers)
 #pragma unroll
-        for (int j = 0; j < 16; j += 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(Sg + j);
-            Sr[j] = v.x;
-            Sr[j + 1] = v.y;
-            Sr[j + 2] = v.z;
-            Sr[j + 3] = v.w;
+        for (int g2 = 0; g2 < 2; ++g2) {
+            float s0[16];
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(Sg + 16 * g2 + j);
+                s0[j] = v.x;
+                s0[j + 1] = v.y;
+                s0[j + 2] = v.z;
+                s0[j + 3] = v.w;
+            }
+            store_hilo_row16(x.sm + OFF_S, lt, 16 * g2, s0);
         }
-        store_hilo_row16(x.sm + OFF_S, srow, j0, Sr);
-        fence_proxy_async_smem();
-    } else {
-        // [T; PT] operand tiles: zero once (right of each row's diagonal chunk stays zero)
-        for (int i = tid - NCHAIN; i < 32768 / 16; i += NLOAD)
-            reinterpret_cast<uint4 *>(x.sm + OFF_ATP)[i] = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
     }
     tc_fence_before_sync();
@@ -513,28 +655,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     bool ok = true;
     if (tid < NCHAIN)
-        chain_role(x, p, t0, t1, nchunks, h, cb, Sr, tid, ok);
-    else
-        loader_role(x, p, t0, nchunks, slot0, h, hq, cb, &tmK, &tmQ, &tmV, tid - NCHAIN);
+        chain_role(x, p, t0, t1, nchunks, h, cb, tid, ok);
+    else if (loader)
+        loader_role(x, nchunks, lt, Sg, ok);
+    else if (issuer)
+        issuer_role(x, nchunks, lane);
+    else if (lane == 0)
+        copy_role(x, p, t0, nchunks, slot0, h, hq, cb, &tmK, &tmQ, &tmV);
 
-    if (tid < NCHAIN) {
-        if (ok && *x.abort_flag == 0) {
-#pragma unroll
-            for (int j = 0; j < 16; j += 4)
-                *reinterpret_cast<float4 *>(Sg + j) = make_float4(Sr[j], Sr[j + 1], Sr[j + 2], Sr[j + 3]);
-        }
-    }
     tc_fence_before_sync();
     __syncthreads();
     if (*x.abort_flag && tid == NCHAIN) {
-        // let any tile or factor load still in flight land before the shared memory is released
+        // let any tile, factor or X load still in flight land before the shared memory is released
         for (int i = 0; i < NKQ; ++i) {
             mbar_wait_bounded(x.bar(B_KQ_FULL + i), 0, kWaitLimit / 16);
             mbar_wait_bounded(x.bar(B_KQ_FULL + i), 1, kWaitLimit / 16);
         }
-        for (int i = 0; i < NF; ++i) {
-            mbar_wait_bounded(x.bar(B_F_FULL + i), 0, kWaitLimit / 16);
-            mbar_wait_bounded(x.bar(B_F_FULL + i), 1, kWaitLimit / 16);
+        for (int b = B_G_FULL; b < B_G_FULL + 2; ++b) {
+            mbar_wait_bounded(x.bar(b), 0, kWaitLimit / 16);
+            mbar_wait_bounded(x.bar(b), 1, kWaitLimit / 16);
+        }
+        for (int b = B_A_FULL; b < B_A_FULL + 4; ++b) {
+            mbar_wait_bounded(x.bar(b), 0, kWaitLimit / 16);
+            mbar_wait_bounded(x.bar(b), 1, kWaitLimit / 16);
         }
     }
     __syncthreads();
@@ -570,12 +713,16 @@ cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s) {
     p.c_hi = a.c_hi;
     p.scale = a.scale;
     p.cu_seqlens = a.cu_seqlens;
-    p.ws = ws;
+    p.ws = reinterpret_cast<const uint8_t *>(ws);
+    p.xs = reinterpret_cast<const uint8_t *>(ws) + fac::x_region_offset(fac::n_slots(a.t_total, a.n_seqs), a.h_v);
     p.state = a.state;
     p.o = a.o;
-    const unsigned grid = (unsigned)a.n_seqs * (unsigned)a.h_v * (unsigned)NCOL;
-    prefill_tc_kernel<<<grid, NTHREADS, SMEM_BYTES, s>>>(tmK, tmQ, tmV, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.n_seqs * (unsigned)a.h_v * (unsigned)NCOL);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = s;
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, tmK, tmQ, tmV, p);
 }
 
 int32_t *device_error_word() {

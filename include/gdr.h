@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define GDR_ABI_VERSION 4
+#define GDR_ABI_VERSION 5
 
 /* Same object as cudaStream_t; declared here so callers need no CUDA header. */
 typedef struct CUstream_st *gdr_stream_t;
@@ -86,10 +86,14 @@ const char *gdr_status_string(gdr_status status);
 
 /*
  * Bytes of device workspace gdr_prefill_chunked needs for this problem: 0 when
- * the CUDA-core path runs (or for an empty problem), otherwise one
- * 19,200-byte slot of per-chunk factors (T, P T and the gates of one chunk and
- * V head) for each of ceil(t_total / 64) + n_seqs chunk positions and each V
- * head, rounded up to 256 bytes.  Host-only, never fails (invalid dims: 0).
+ * the CUDA-core path runs (or for an empty problem), otherwise, for each of
+ * P = ceil(t_total / 64) + n_seqs chunk positions, one 33,024-byte slot of
+ * per-chunk factors per V head (T and P T as bf16 hi/lo MMA operand tiles, and
+ * the chunk's exp(G)), then, from the next 1 KiB boundary, one 32 KiB pair of
+ * bf16 hi/lo tiles per QK head of X = [K; Q]_c K_{c-1}^T (the next chunk's
+ * keys and queries against this chunk's keys), rounded up to 256 bytes:
+ * roundup(roundup(P * h_v * 33024, 1024) + P * h_qk * 32768, 256).
+ * Host-only, never fails (invalid dims: 0).
  */
 size_t gdr_prefill_workspace_bytes(const gdr_dims *dims, int32_t n_seqs, int64_t t_total);
 
@@ -111,13 +115,14 @@ size_t gdr_prefill_workspace_bytes(const gdr_dims *dims, int32_t n_seqs, int64_t
  * padded rows are never written.
  *
  * On the tensor-core path the call is two launches on `stream`: the
- * state-independent factors of every chunk (gates, (I+N)^-1, P (I+N)^-1) into
- * `workspace`, then the chunk-to-chunk scan that reads them.  When the scan
- * leaves at least 16 SMs free and the factors of all chunks need at least two
- * waves of the GPU (e.g. one Qwen3.5-9B sequence of 2.5K tokens or more), the
- * call is four launches instead: factors and scan of the first ~60% of the
- * chunks, the remaining factors as a programmatic dependent launch that runs
- * on the free SMs beside that scan, then the scan of the remaining chunks.  The workspace holds nothing between calls.
+ * state-independent factors of every chunk (gates, (I+N)^-1, P (I+N)^-1, and
+ * X = [K; Q]_c K_{c-1}^T) into `workspace`, then the chunk-to-chunk scan that
+ * reads them.  When the scan leaves at least 16 SMs free and the factors of all
+ * chunks need at least two waves of the GPU (e.g. one Qwen3.5-9B sequence of
+ * 2.5K tokens or more), the call is four launches instead: factors and scan of
+ * the first ~73% of the chunks, the remaining factors as a programmatic
+ * dependent launch that runs on the free SMs beside that scan, then the scan of
+ * the remaining chunks.  The workspace holds nothing between calls.
  *
  *   dims        shapes, dtypes, chunk, scale (host pointer, read during the call)
  *   n_seqs      number of sequences (>= 0; 0 is a no-op)

@@ -123,11 +123,19 @@ def test_packing_equals_separate_calls():
         assert gu.state_error(si[0], s_all[i]) < 1e-6
 
 
+@pytest.mark.parametrize("h_qk,h_v", [(4, 4), (2, 8)])
+def test_tensor_core_head_ratios(h_qk, h_v):
+    """One V head per QK head, and four: the factor kernel's X tiles (written by the
+    first one or two V heads of a QK head's group) reach every V head."""
+    w = synth.make_workload("ratio", [200, 64, 131], h_qk, h_v, 128, 64, "bf16", seed=60 + h_v, state_std=0.02)
+    check(w)
+
+
 @pytest.mark.parametrize("lens", [[1500, 4000], [0, 5000]])
 def test_split_prefill_over_two_sequences(lens):
     """16 V heads (8 QK heads) and two sequences: the chunk scan runs 128 CTAs and
     the factors need over two waves, so on a 152-SM GB300 the call splits at a
-    chunk (37 of 86 for [1500, 4000], 34 of 79 for [0, 5000]): a sequence that ends
+    chunk (50 of 86 for [1500, 4000], 46 of 79 for [0, 5000]): a sequence that ends
     before the split chunk, one that is cut by it, and an empty one all come out as
     the oracle's."""
     w = synth.make_workload("split2", lens, 8, 16, 128, 64, "bf16", seed=51 + lens[0], state_std=0.02)
