@@ -11,8 +11,8 @@
 // For the chunk scan's lookahead it also writes, per (chunk c >= 1, QK head), the
 // state-independent product X = [K; Q]_c K_{c-1}ᵀ as bf16 hi/lo operand tiles
 // (layout in gdr_factor_layout.h): the CTA of the first V head of the QK head's
-// group computes it; warps 2-3 write its Q rows while warps 0-1 solve for T,
-// warps 0-1 its K rows at the end.
+// group computes it with the Gram and writes it at the end, staged in the then
+// free scratch and stored by one bulk copy.
 //
 // Per chunk (the chunkwise-parallel form of the Qwen3.5-9B NPU model card,
 // "How it works"; forward substitution for the unit triangular factor as in
@@ -322,9 +322,10 @@ __device__ void solve_pt(const uint8_t *hs, const float *gates, uint8_t *slot, i
 }
 
 // Row `row` (a TMEM lane this warp may read) of X from TMEM columns 64-127 into
-// the X tile pair of the slot: bf16 hi and lo parts, 128-byte swizzled.
-__device__ void store_x_row(uint32_t tmem, int warp, int row, uint8_t *xpair) {
-    uint8_t *xt = xpair + (size_t)row * 128;
+// a shared-memory image of the X tile pair: bf16 hi and lo parts, 128-byte
+// swizzled (hi tile at `img`, lo tile 16 KB on).
+__device__ void stage_x_row(uint32_t tmem, int warp, int row, uint8_t *img) {
+    uint8_t *xt = img + (size_t)row * 128;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
 #pragma unroll 1
     for (int hf = 0; hf < 2; ++hf) {
@@ -486,14 +487,13 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
     if (warp < 2) {
         solve_t(sm, gates, slot_out, warp, lane, 1);
     } else {
-        // exp(G); X rows 64-127 (Q rows); the zero 8-column chunks right of each
+        // exp(G), and the zero 8-column chunks right of each
         // row's diagonal chunk (thread i of warps 2-3: rows i of Tw and 64 + i of PTw)
         if (warp == 2) {
             float *eg = reinterpret_cast<float *>(slot_out + fac::OFF_EG);
             eg[lane] = gates[128 + lane];
             eg[lane + 32] = gates[160 + lane];
         }
-        if (want_x) store_x_row(tmem, warp, tid, xpair);
         const int t = tid - 64;
         for (int k = (t >> 3) + 1; k < 8; ++k) {
 #pragma unroll
@@ -506,7 +506,23 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
     }
     __syncthreads();
     solve_pt(sm, gates, slot_out, warp, lane);
-    if (want_x && warp < 2) store_x_row(tmem, warp, tid, xpair);  // X rows 0-63 (K rows)
+    if (want_x) {
+        // X through the free scratch: each thread stages its row, then one bulk
+        // store writes the 32 KB tile pair (rows of 16-byte pieces at 128-byte
+        // strides, stored from registers, were the slowest part of the kernel)
+        __syncthreads();  // every warp is done with the scratch
+        stage_x_row(tmem, warp, tid, sm);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                             reinterpret_cast<uint64_t>(xpair)),
+                         "r"(sb), "r"((uint32_t)fac::X_BYTES)
+                         : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // before the CTA's memory is released
+        }
+    }
     tc_fence_before_sync();
     __syncthreads();  // every TMEM read is done before the columns are freed
     if (warp == 0) {
