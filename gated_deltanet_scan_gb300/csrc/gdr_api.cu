@@ -103,7 +103,8 @@ int split_chunk(const gdr_dims *d, int32_t n_seqs, int64_t t_total) {
     return (int)m;
 }
 
-// The tensor-core prefill on `s`: factors, then the chunk scan, or, split at
+// The tensor-core prefill on `s`: factors, then the chunk scan (a programmatic
+// dependent of the factor launch), or, split at
 // chunk m (see split_chunk): factors [0, m), scan [0, m), factors [m, n) as a
 // programmatic dependent launch (it starts once every CTA of the scan is
 // running, on the SMs they leave free, and reads nothing the scan writes),
@@ -112,17 +113,22 @@ cudaError_t prefill_tc(const gdr_dims *dims, const Args &a, float *ws, int32_t *
                        bool allow_split) {
     const int m = allow_split ? split_chunk(dims, a.n_seqs, a.t_total) : 0;
     if (m == 0) {
+        // the scan's prologue overlaps the factor grid's last wave (T = 1024: 73 -> 67 us)
         cudaError_t e = launch_factors(a, ws, err, s, false);
         if (e != cudaSuccess) return e;
-        return launch_prefill_tc(a, ws, s);
+        return launch_prefill_tc(a, ws, s, true);
     }
     Args a1 = a, a2 = a;
     a1.c_hi = m;
     a2.c_lo = m;
+    // the first scan is an ordinary launch here: as a programmatic dependent it would
+    // let the second factor launch start while the first one still runs (T = 16384
+    // measured 0.72 ms against 0.64 ms)
     cudaError_t e = launch_factors(a1, ws, err, s, false);
-    if (e == cudaSuccess) e = launch_prefill_tc(a1, ws, s);
+    if (e == cudaSuccess) e = launch_prefill_tc(a1, ws, s, false);
     if (e == cudaSuccess) e = launch_factors(a2, ws, err, s, true);
-    if (e == cudaSuccess) e = launch_prefill_tc(a2, ws, s);
+    // an ordinary launch: it reads the state the first scan writes
+    if (e == cudaSuccess) e = launch_prefill_tc(a2, ws, s, false);
     return e;
 }
 

@@ -344,6 +344,9 @@ __device__ void stage_x_row(uint32_t tmem, int warp, int row, uint8_t *img) {
 
 __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ CUtensorMap tmK,
                                                        const __grid_constant__ CUtensorMap tmQ, FacParams p) {
+    // a chunk scan queued behind this launch as a programmatic dependent may start
+    // its prologue now; it waits for this grid before it reads the workspace
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t slot = p.slot_lo + blockIdx.x;
     const int h = blockIdx.y, hq = h / (p.h_v / p.h_qk);
     // the sequence whose chunk this slot holds: the last s with slot_base(s) <= slot

@@ -38,7 +38,11 @@ cudaError_t launch_chunk_cc(const Args &a, cudaStream_t s);
 // `overlap`: launch as a programmatic dependent of the kernel before it on `s`
 // (it may start once every CTA of that kernel runs; it must not read its results).
 cudaError_t launch_factors(const Args &a, float *ws, int32_t *err, cudaStream_t s, bool overlap);
-cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s);
+// `overlap`: launch as a programmatic dependent of the factor launch just before
+// it on `s` (its prologue overlaps that grid; it reads the workspace only after
+// griddepcontrol.wait).  Only directly after the factor launch whose slots it
+// reads: the kernel waits for nothing else.
+cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s, bool overlap);
 cudaError_t launch_copy_f32(const float *src, float *dst, size_t n, cudaStream_t s);
 // Verify commit: state = e^{G_a} snapshot + sum_{j<a} e^{G_a - G_j} k_j u_j^T per (sequence, V head).
 cudaError_t launch_commit(const Args &a, int32_t *err, cudaStream_t s);

@@ -281,9 +281,12 @@ __device__ void copy_role(const Ctx &x, const TcParams &p, int64_t t0, int nchun
         if (!bad) issue_op_load(x, i, op_src(i));
         if (!bad && op_exists(i + 8, nchunks)) prefetch_l2(op_src(i + 8), OP_BYTES);  // two chunks ahead
     };
+    for (int c = 0; c < nchunks && c < NKQ; ++c) issue_kq_loads(x, c, (int)(t0 + c * C), hq, h, cb, tmK, tmQ, tmV);
+    // launched as a programmatic dependent of the factor launch: everything above
+    // reads only inputs; the workspace is read after that grid has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int i = 0; i < NOP; ++i) next_op(i);
     for (int c = 0; c < nchunks && c < 2; ++c) issue_gates_load(x, fsrc + c * fstride, c);
-    for (int c = 0; c < nchunks && c < NKQ; ++c) issue_kq_loads(x, c, (int)(t0 + c * C), hq, h, cb, tmK, tmQ, tmV);
     for (int i = NOP; i < NOP + 3; ++i)
         if (op_exists(i + 3, nchunks)) prefetch_l2(op_src(i + 3), OP_BYTES);
     for (int c = 0; c < nchunks && !bad; ++c) {
@@ -689,7 +692,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 }  // namespace
 
-cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s) {
+cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s, bool overlap) {
     if (a.n_seqs == 0 || a.t_total == 0) return cudaSuccess;  // every sequence empty: state unchanged
     CUtensorMap tmK, tmQ, tmV;
     if (!encode_bf16_3d(&tmK, a.k, D, (uint64_t)a.h_qk, (uint64_t)a.t_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -722,6 +725,11 @@ cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s) {
     cfg.blockDim = dim3(NTHREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = overlap ? &attr : nullptr;
+    cfg.numAttrs = overlap ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, tmK, tmQ, tmV, p);
 }
 
