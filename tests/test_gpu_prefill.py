@@ -49,8 +49,10 @@ def test_long_prefill_T16384(run):
 
 
 @pytest.mark.parametrize("chunk", [16, 64])
-@pytest.mark.parametrize("T", [1, 15, 16, 17, 63, 64, 65, 128, 1000])
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 63, 64, 65, 128, 192, 256, 320, 449, 1000])
 def test_lengths_around_chunk_boundaries(T, chunk):
+    """Also 3, 4, 5 and 8 chunks of 64: the tensor-core scan's five-slot operand
+    ring (four tiles per chunk, none for X after the last chunk) wraps at each."""
     w = synth.make_workload("len", [T], 16, 32, 128, chunk, "bf16", seed=T, state_std=0.02)
     check(w)
 
