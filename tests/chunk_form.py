@@ -17,6 +17,13 @@ so that one chunk of the sequential pass is
     D = U - W S,   O = Q' S + U',   S <- e^{G_C} S + K^T diag(e^{G_C - G}) D.
 T is formed by 16x16 diagonal-block forward substitution followed by blocked
 off-diagonal solves, as in the kernel.
+
+``chunk_form_lookahead`` is the grouping of the tcgen05 chunk scan: with
+Tw = diag(e^{G_C - G}) T diag(beta) and PTw = P T diag(beta), a chunk is
+    R = V - diag(e^G) K S,  D~ = Tw R,  O = diag(e^G) Q S + PTw R,
+    S <- e^{G_C} S + K^T D~,
+and the next chunk's [K S; Q S] is formed without the new S as
+    [K; Q]_{c+1} (e^{G_C} S_c) + X_c D~_c,   X_c = [K; Q]_{c+1} K_c^T.
 """
 
 from __future__ import annotations
@@ -140,3 +147,41 @@ def commit_from_deltas(k, g, D, S0, a):
     G = np.cumsum(np.asarray(g[:a], np.float64))
     w = np.exp(G[-1] - G)
     return np.exp(G[-1]) * S0 + np.asarray(k[:a], np.float64).T @ (w[:, None] * np.asarray(D[:a], np.float64))
+
+
+def chunk_form_lookahead(q, k, v, g, beta, S0, C):
+    """Same contract as ``chunk_form_pages``, in the tcgen05 chunk scan's grouping."""
+    T_len = q.shape[0]
+    n = (T_len + C - 1) // C
+    chunks = []
+    for c in range(n):
+        c0 = c * C
+        L = min(C, T_len - c0)
+        Q, K, V = (_pad(np.asarray(x[c0:c0 + L], np.float64), C) for x in (q, k, v))
+        gc = _pad(np.asarray(g[c0:c0 + L], np.float64), C)
+        bc = _pad(np.asarray(beta[c0:c0 + L], np.float64), C)
+        G = np.cumsum(gc)
+        N = bc[:, None] * _decay_matrix(G, strict=True) * (K @ K.T)
+        P = _decay_matrix(G, strict=False) * (Q @ K.T)
+        Tm = unit_lower_inverse_blocked(N, 16 if C % 16 == 0 else C)
+        Tw = np.exp(G[-1] - G)[:, None] * Tm * bc[None, :]
+        PTw = P @ Tm * bc[None, :]
+        chunks.append((c0, L, np.vstack([K, Q]), K, V, G, Tw, PTw))
+    S = np.array(S0, dtype=np.float64)
+    O = np.zeros((T_len, v.shape[1]))
+    dk = q.shape[1]
+    A = chunks[0][2] @ S  # [K S; Q S] of chunk 0
+    for c, (c0, L, KQ, K, V, G, Tw, PTw) in enumerate(chunks):
+        KS, QS = A[:C], A[C:]
+        eG = np.exp(G)[:, None]
+        R = V - eG * KS
+        Dt = Tw @ R
+        O[c0:c0 + L] = (eG * QS + PTw @ R)[:L]
+        eGC = np.exp(G[-1])
+        if c + 1 < n:
+            KQn = chunks[c + 1][2]
+            X = KQn @ K.T
+            A = KQn @ (eGC * S) + X @ Dt
+        S = eGC * S + K.T @ Dt
+    assert S.shape == (dk, v.shape[1])
+    return O, S

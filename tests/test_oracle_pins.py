@@ -18,7 +18,8 @@ import numpy as np
 import pytest
 
 import oracle
-from tests.chunk_form import chunk_form_factored, chunk_form_pages, commit_from_deltas, verify_deltas
+from tests.chunk_form import (chunk_form_factored, chunk_form_lookahead, chunk_form_pages, commit_from_deltas,
+                               verify_deltas)
 
 
 def _rng(seed):
@@ -314,8 +315,9 @@ def test_contraction_bound_per_step():
 @pytest.mark.parametrize("C", [16, 64])
 @pytest.mark.parametrize("T", [1, 15, 16, 17, 63, 64, 65, 128, 200])
 def test_chunk_forms_match_sequential(C, T):
-    """The model card's chunk form, and the kernel's regrouping of it, equal the
-    sequential recurrence for every length around the chunk boundary."""
+    """The model card's chunk form, and the kernels' regroupings of it (the factored
+    form, and the chunk scan's lookahead), equal the sequential recurrence for every
+    length around the chunk boundary."""
     r = _rng(100 + T + C)
     dk = dv = 32
     q = _unit(r.standard_normal((T, dk)))
@@ -325,7 +327,7 @@ def test_chunk_forms_match_sequential(C, T):
     beta = 1.0 / (1.0 + np.exp(-r.standard_normal(T)))
     S0 = 0.02 * r.standard_normal((dk, dv))
     o, S = _single(q, k, v, g, beta, S0)
-    for form in (chunk_form_pages, chunk_form_factored):
+    for form in (chunk_form_pages, chunk_form_factored, chunk_form_lookahead):
         oc, Sc = form(q, k, v, g, beta, S0, C)
         scale_o = np.sqrt(np.mean(o * o))
         assert np.max(np.abs(oc - o)) <= 1e-10 * max(scale_o, 1e-30), form.__name__
@@ -344,10 +346,11 @@ def test_chunk_form_strong_decay_stays_finite():
     beta = 1.0 / (1.0 + np.exp(-r.standard_normal(T)))
     S0 = 0.02 * r.standard_normal((dk, dv))
     o, S = _single(q, k, v, g, beta, S0)
-    oc, Sc = chunk_form_factored(q, k, v, g, beta, S0, C)
-    assert np.all(np.isfinite(oc)) and np.all(np.isfinite(Sc))
-    assert np.max(np.abs(oc - o)) <= 1e-10 * np.sqrt(np.mean(o * o))
-    assert np.linalg.norm(Sc - S) <= 1e-10 * np.linalg.norm(S)
+    for form in (chunk_form_factored, chunk_form_lookahead):
+        oc, Sc = form(q, k, v, g, beta, S0, C)
+        assert np.all(np.isfinite(oc)) and np.all(np.isfinite(Sc)), form.__name__
+        assert np.max(np.abs(oc - o)) <= 1e-10 * np.sqrt(np.mean(o * o)), form.__name__
+        assert np.linalg.norm(Sc - S) <= 1e-10 * np.linalg.norm(S), form.__name__
     # With the same decay, the unmasked factorisation exp(G_t) * exp(-G_j)
     # overflows fp32 within a chunk: exp(-G_j) passes FLT_MAX at j = 14.
     with np.errstate(over="ignore"):
