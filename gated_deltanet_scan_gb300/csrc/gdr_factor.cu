@@ -208,14 +208,16 @@ __device__ __forceinline__ void chunk_gates(float g0, float g1, float b0, float 
     gates[192 + lane + 32] = fast_exp2(gc - g1);
 }
 
-// The head's T from its N blocks, by warps wi = 0, 1 (named barrier `bar`);
-// every block of Tw is stored to the slot's operand tiles (rows 0-63) as soon
-// as it is formed, adjacent columns paired across lanes.
+// The head's T from its N blocks, by the CTA's four warps wi (named barrier
+// `bar`): warps 0-1 invert the diagonal blocks, then each block diagonal's
+// blocks go one per warp (3, 2, 1).  Every block of Tw is stored to the slot's
+// operand tiles (rows 0-63) as soon as it is formed, adjacent columns paired
+// across lanes.
 __device__ void solve_t(uint8_t *hs, const float *gates, uint8_t *slot, int wi, int lane, uint32_t bar) {
     const int g = lane >> 2, c = lane & 3;
     const float *bw = gates + 64, *rw = gates + 192;  // column weights beta, row weights exp(G_C - G)
-    // ---- diagonal blocks: each warp two, lanes 0-15 / 16-31 one block, lane = column
-    {
+    // ---- diagonal blocks: warps 0-1 two each, lanes 0-15 / 16-31 one block, lane = column
+    if (wi < 2) {
         const int I = 2 * wi + (lane >> 4), jj = lane & 15;
         const float *nd = reinterpret_cast<const float *>(hs + OFF_ND) + 256 * I;
         float col[16];
@@ -248,11 +250,12 @@ __device__ void solve_t(uint8_t *hs, const float *gates, uint8_t *slot, int wi, 
             if ((jj & 1) == 0 && (cg >> 3) <= (rg >> 3)) st_tile_pair(slot, rg, cg, v, vn);
         }
     }
-    named_sync(bar, 64);
-    // ---- off-diagonal blocks by diagonals d = 1 (3 blocks), 2 (2), 3 (1):
+    named_sync(bar, NT);
+    // ---- off-diagonal blocks by diagonals d = 1 (3 blocks), 2 (2), 3 (1), one per warp:
     // X_IJᵀ = sum_K Tᵀ(J, K) N_IKᵀ, then T_IJᵀ = -X_IJᵀ T_IIᵀ
     for (int d = 1; d <= 3; ++d) {
-        for (int J = wi; J + d <= 3; J += 2) {
+        if (wi + d <= 3) {
+            const int J = wi;
             const int I = J + d;
             float x[2][4];
             zero_acc(x);
@@ -287,7 +290,7 @@ __device__ void solve_t(uint8_t *hs, const float *gates, uint8_t *slot, int wi, 
                 }
             }
         }
-        if (d < 3) named_sync(bar, 64);
+        if (d < 3) named_sync(bar, NT);
     }
 }
 
@@ -487,11 +490,10 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
     __syncthreads();
     uint8_t *slot_out = p.ws + ((size_t)slot * p.h_v + h) * fac::SLOT_BYTES;
     uint8_t *xpair = p.xs + ((size_t)slot * p.h_qk + hq) * fac::X_BYTES;
-    if (warp < 2) {
-        solve_t(sm, gates, slot_out, warp, lane, 1);
-    } else {
-        // exp(G), and the zero 8-column chunks right of each
-        // row's diagonal chunk (thread i of warps 2-3: rows i of Tw and 64 + i of PTw)
+    if (warp >= 2) {
+        // while warps 0-1 invert the diagonal blocks: exp(G), and the zero 8-column
+        // chunks right of each row's diagonal chunk (thread i of warps 2-3: rows i
+        // of Tw and 64 + i of PTw)
         if (warp == 2) {
             float *eg = reinterpret_cast<float *>(slot_out + fac::OFF_EG);
             eg[lane] = gates[128 + lane];
@@ -507,6 +509,7 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
             }
         }
     }
+    solve_t(sm, gates, slot_out, warp, lane, 1);
     __syncthreads();
     solve_pt(sm, gates, slot_out, warp, lane);
     if (want_x) {
