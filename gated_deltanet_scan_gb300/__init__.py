@@ -17,7 +17,7 @@ __all__ = [
     "GdrError", "gdr_dims", "lib", "library_path",
     "gdr_prefill_chunked", "gdr_prefill_workspace_bytes", "gdr_prefill_chunked_static",
     "gdr_decode_step", "gdr_decode_step_overlapped", "gdr_verify_block", "gdr_verify_commit",
-    "gdr_state_snapshot", "gdr_state_restore", "gdr_device_error", "gdr_status_string",
+    "gdr_state_snapshot", "gdr_state_restore", "gdr_device_error", "gdr_selftest_wait_timeout", "gdr_status_string",
     "GDR_F32", "GDR_BF16",
 ]
 
@@ -70,6 +70,7 @@ _SIGS = {
     "gdr_state_snapshot": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, _P, _P], ctypes.c_int),
     "gdr_state_restore": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, _P, _P], ctypes.c_int),
     "gdr_device_error": ([_P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
+    "gdr_selftest_wait_timeout": ([ctypes.c_int64, _P], ctypes.c_int),
 }
 
 
@@ -261,3 +262,10 @@ def gdr_device_error(*, stream=None, device=None) -> int:
     code = ctypes.c_int32(0)
     _check(lib().gdr_device_error(_stream_handle(stream, device), ctypes.byref(code)), "gdr_device_error")
     return int(code.value)
+
+
+def gdr_selftest_wait_timeout(limit_cycles: int, *, stream=None, device=None) -> None:
+    """Launch the self-test block whose bounded wait on a barrier nothing arrives
+    on gives up after limit_cycles SM clocks and records GDR_ERR_DEVICE_TIMEOUT."""
+    _check(lib().gdr_selftest_wait_timeout(int(limit_cycles), _stream_handle(stream, device)),
+           "gdr_selftest_wait_timeout")

@@ -6,6 +6,7 @@
 
 #include "gdr_factor_layout.h"
 #include "gdr_internal.h"
+#include "tc_ptx.cuh"
 
 namespace gdr {
 namespace {
@@ -34,6 +35,20 @@ __global__ void copy_f32_kernel(const float4 *__restrict__ src, float4 *__restri
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// One thread waits, with the bounded wait of the kernels, on an mbarrier that
+// nothing arrives on, gives up after `limit` SM clocks and records the timeout.
+__global__ void wait_timeout_kernel(int32_t *err, long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = tc::smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        tc::mbar_init(b, 1);
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !tc::mbar_wait_bounded(b, 0u, limit))
+        atomicCAS(err, 0, (int32_t)GDR_ERR_DEVICE_TIMEOUT);
+}
 
 gdr_status check_dims(const gdr_dims *d) {
     if (!d) return GDR_ERR_INVALID_ARG;
@@ -355,6 +370,14 @@ gdr_status gdr_state_restore(const gdr_dims *dims, int32_t n_seqs, const float *
 gdr_status gdr_device_error(gdr_stream_t stream, int32_t *code) {
     if (!code) return GDR_ERR_INVALID_ARG;
     return from_cuda(read_clear_device_error(reinterpret_cast<cudaStream_t>(stream), code));
+}
+
+gdr_status gdr_selftest_wait_timeout(int64_t limit_cycles, gdr_stream_t stream) {
+    if (limit_cycles < 1 || limit_cycles > ((int64_t)1 << 31)) return GDR_ERR_INVALID_ARG;
+    int32_t *err = device_error_word();
+    if (!err) return GDR_ERR_CUDA;
+    wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err, (long long)limit_cycles);
+    return from_cuda(cudaGetLastError());
 }
 
 }  // extern "C"

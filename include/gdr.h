@@ -267,6 +267,17 @@ gdr_status gdr_state_restore(const gdr_dims *dims, int32_t n_seqs, const float *
  */
 gdr_status gdr_device_error(gdr_stream_t stream, int32_t *code);
 
+/*
+ * Self-test of the failure reporting every kernel uses: launches one block on
+ * `stream` that waits, with the kernels' bounded mbarrier wait, on a barrier
+ * nothing ever arrives on, for at most limit_cycles SM clocks (1 .. 2^31); the
+ * wait gives up and records GDR_ERR_DEVICE_TIMEOUT in the device error word
+ * (read it with gdr_device_error).  Nothing else is touched and the context
+ * stays usable.  Returns GDR_ERR_INVALID_ARG for a limit out of range,
+ * GDR_ERR_CUDA if the launch fails.
+ */
+gdr_status gdr_selftest_wait_timeout(int64_t limit_cycles, gdr_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -148,6 +148,12 @@ def test_snapshot_restore_reject_bad_arguments(L):
     assert L.gdr_device_error(None, None) == gdr.GDR_ERR_INVALID_ARG
 
 
+def test_selftest_wait_timeout_rejects_bad_limits(L):
+    # checked on the host before any launch (no GPU here)
+    for bad in (0, -5, (1 << 31) + 1):
+        assert L.gdr_selftest_wait_timeout(bad, None) == gdr.GDR_ERR_INVALID_ARG
+
+
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(gdr, "_lib", None)
     monkeypatch.setattr(gdr, "library_path", lambda: str(tmp_path / "missing.so"))
