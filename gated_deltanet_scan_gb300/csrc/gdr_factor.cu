@@ -9,7 +9,7 @@
 // update needs and PTw (V - diag(e^G) K S) the intra-chunk part of the output.
 //
 // For the chunk scan's lookahead it also writes, per (chunk c >= 1, QK head), the
-// state-independent product X = [K; Q]_c K_{c-1}ᵀ as bf16 hi/lo operand tiles
+// state-independent product X = [K; Q]_c K_{c-1}ᵀ as an fp16 operand tile
 // (layout in gdr_factor_layout.h): the CTA of the first V head of the QK head's
 // group computes it with the Gram and writes it at the end, staged in the then
 // free scratch and stored by one bulk copy.
@@ -34,6 +34,9 @@
 // all four form P T.  Off-diagonal blocks of T are formed transposed, T_IJᵀ = -X_IJᵀ T_IIᵀ,
 // so that X_IJᵀ comes straight out of one MMA's accumulators as the left
 // operand of the next.
+// Tw, PTw and X leave the kernel as fp16 MMA operand tiles (round to nearest,
+// 2^-11 relative): the chunk scan multiplies them by fp16 R and D~ in one
+// tensor-core pass each.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -116,12 +119,9 @@ __device__ __forceinline__ uint2 ld_pair(const uint8_t *blk, int r, int p) {
 __device__ __forceinline__ void st_pair(uint8_t *blk, int r, int p, uint2 v) {
     *reinterpret_cast<uint2 *>(blk + r * ROW_B + p * 8) = v;
 }
-// Elements (r, j), (r, j + 1) (j even) of the slot's hi and lo operand tiles.
+// Elements (r, j), (r, j + 1) (j even) of the slot's fp16 operand tile.
 __device__ __forceinline__ void st_tile_pair(uint8_t *slot, int r, int j, float x0, float x1) {
-    const uint2 w = hl_pair(x0, x1);
-    const uint32_t off = fac::sw128_elem(r, j);
-    *reinterpret_cast<uint32_t *>(slot + fac::OFF_HI + off) = w.x;
-    *reinterpret_cast<uint32_t *>(slot + fac::OFF_LO + off) = w.y;
+    *reinterpret_cast<uint32_t *>(slot + fac::OFF_T + fac::sw128_elem(r, j)) = pack_f16x2(x0, x1);
 }
 
 // Fragments of mma.m16n8k16 (row.col, bf16): lane = 4 g + c.
@@ -325,8 +325,7 @@ __device__ void solve_pt(const uint8_t *hs, const float *gates, uint8_t *slot, i
 }
 
 // Row `row` (a TMEM lane this warp may read) of X from TMEM columns 64-127 into
-// a shared-memory image of the X tile pair: bf16 hi and lo parts, 128-byte
-// swizzled (hi tile at `img`, lo tile 16 KB on).
+// a shared-memory image of the fp16 X tile (128-byte swizzled) at `img`.
 __device__ void stage_x_row(uint32_t tmem, int warp, int row, uint8_t *img) {
     uint8_t *xt = img + (size_t)row * 128;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
@@ -336,11 +335,10 @@ __device__ void stage_x_row(uint32_t tmem, int warp, int row, uint8_t *img) {
         tmem_ld32(lane_addr + 64 + 32 * hf, v);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            uint32_t hw[4], lw[4];
-            hilo_words(v + 8 * q, hw, lw);
+            const float *w = v + 8 * q;
             const uint32_t off = (uint32_t)((((4 * hf + q) ^ (row & 7)) & 7) << 4);
-            *reinterpret_cast<uint4 *>(xt + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4 *>(xt + fac::X_TILE_BYTES + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            *reinterpret_cast<uint4 *>(xt + off) = make_uint4(pack_f16x2(w[0], w[1]), pack_f16x2(w[2], w[3]),
+                                                              pack_f16x2(w[4], w[5]), pack_f16x2(w[6], w[7]));
         }
     }
 }
@@ -489,7 +487,7 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
     tc_fence_before_sync();
     __syncthreads();
     uint8_t *slot_out = p.ws + ((size_t)slot * p.h_v + h) * fac::SLOT_BYTES;
-    uint8_t *xpair = p.xs + ((size_t)slot * p.h_qk + hq) * fac::X_BYTES;
+    uint8_t *xtile = p.xs + ((size_t)slot * p.h_qk + hq) * fac::X_BYTES;
     if (warp >= 2) {
         // while warps 0-1 invert the diagonal blocks: exp(G), and the zero 8-column
         // chunks right of each row's diagonal chunk (thread i of warps 2-3: rows i
@@ -504,8 +502,7 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
                 const uint32_t off = fac::sw128_elem(t + 64 * m, 8 * k);
-                *reinterpret_cast<uint4 *>(slot_out + fac::OFF_HI + off) = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4 *>(slot_out + fac::OFF_LO + off) = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4 *>(slot_out + fac::OFF_T + off) = make_uint4(0u, 0u, 0u, 0u);
             }
         }
     }
@@ -514,7 +511,7 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
     solve_pt(sm, gates, slot_out, warp, lane);
     if (want_x) {
         // X through the free scratch: each thread stages its row, then one bulk
-        // store writes the 32 KB tile pair (rows of 16-byte pieces at 128-byte
+        // store writes the 16 KB tile (rows of 16-byte pieces at 128-byte
         // strides, stored from registers, were the slowest part of the kernel)
         __syncthreads();  // every warp is done with the scratch
         stage_x_row(tmem, warp, tid, sm);
@@ -522,7 +519,7 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
         __syncthreads();
         if (tid == 0) {
             asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                             reinterpret_cast<uint64_t>(xpair)),
+                             reinterpret_cast<uint64_t>(xtile)),
                          "r"(sb), "r"((uint32_t)fac::X_BYTES)
                          : "memory");
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");

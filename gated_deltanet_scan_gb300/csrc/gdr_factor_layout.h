@@ -1,32 +1,28 @@
 // Layout of the per-chunk factor workspace shared by the factor kernel (writer)
 // and the tensor-core chunk scan (reader).
 //
-// One slot per (chunk, V head), 33 024 bytes, holding the chunk's
+// One slot per (chunk, V head), 16 640 bytes, holding the chunk's
 // Tw = diag(exp(G_C - G)) (I + N)^-1 diag(beta) and PTw = P (I + N)^-1 diag(beta)
 // (G_C = G of the chunk's last row) ready to be the A operand of a tcgen05 MMA:
-//   [0, 16384)       hi tile: 128 rows (Tw rows 0-63, then PTw rows 64-127) of
-//                    64 bf16 in the 128-byte-swizzled K-major layout: 16-byte
-//                    chunk j of row r at r * 128 + 16 (j ^ (r % 8)); zeros above
-//                    the diagonal
-//   [16384, 32768)   lo tile: the same for the residuals (x = hi + lo to ~2^-16)
-//   [32768, 33024)   exp(G), 64 fp32 (G: inclusive running sum of g; padding rows
+//   [0, 16384)       the operand tile: 128 rows (Tw rows 0-63, then PTw rows
+//                    64-127) of 64 fp16 in the 128-byte-swizzled K-major layout:
+//                    16-byte chunk j of row r at r * 128 + 16 (j ^ (r % 8)); zeros
+//                    above the diagonal
+//   [16384, 16640)   exp(G), 64 fp32 (G: inclusive running sum of g; padding rows
 //                    repeat the last)
-// A bulk copy of a tile to a 1024-byte aligned shared-memory address yields the
-// operand as it is.
+// A bulk copy of the tile to a 1024-byte aligned shared-memory address yields
+// the operand as it is.
 //
 // Chunk c of sequence s lives in slot floor(cu[s] / 64) + s + c; slots of
 // different sequences never collide and every slot index is below
 // ceil(T_total / 64) + n_seqs.
 //
-// After the slots (at x_region_offset, 1024-byte aligned) one X tile pair per
+// After the slots (at x_region_offset, 1024-byte aligned) one X tile per
 // (slot, QK head): for the slot of chunk c >= 1 of a sequence,
 //   X = [K; Q]_c K_{c-1}ᵀ        (128 x 64: the chunk's K rows, then its Q rows,
 //                                 against the previous chunk's 64 key tokens)
-// as two bf16 tiles, hi parts then lo parts (x = hi + lo to ~2^-16), each 128
-// rows of 128 bytes in the 128-byte-swizzled K-major layout of a tcgen05 A
-// operand: 16-byte chunk j of row r at r * 128 + 16 (j ^ (r % 8)).  A bulk copy
-// to a 1024-byte aligned shared-memory address yields the operand as it is.
-// The slot of a sequence's first chunk has no X.
+// as one fp16 tile of 128 rows of 128 bytes in the same 128-byte-swizzled
+// K-major layout.  The slot of a sequence's first chunk has no X.
 #pragma once
 
 #include <stdint.h>
@@ -35,14 +31,13 @@ namespace gdr {
 namespace fac {
 
 constexpr int C = 64;                  // tokens per chunk
-constexpr int TILE_BYTES = 16384;      // 128 rows x 64 bf16
-constexpr int OFF_HI = 0;              // bytes
-constexpr int OFF_LO = TILE_BYTES;
-constexpr int OFF_EG = 2 * TILE_BYTES;
-constexpr int SLOT_BYTES = OFF_EG + C * 4;  // 33024, a multiple of 16
+constexpr int TILE_BYTES = 16384;      // 128 rows x 64 fp16
+constexpr int OFF_T = 0;               // bytes
+constexpr int OFF_EG = TILE_BYTES;
+constexpr int SLOT_BYTES = OFF_EG + C * 4;  // 16640, a multiple of 16
 static_assert(SLOT_BYTES % 16 == 0, "slots must keep 16-byte alignment");
 
-// Byte offset of the bf16 element (row r, column j) in a 128-byte-swizzled
+// Byte offset of the 16-bit element (row r, column j) in a 128-byte-swizzled
 // K-major tile of 128-byte rows.
 __host__ __device__ constexpr uint32_t sw128_elem(int r, int j) {
     return (uint32_t)(r * 128 + ((((j >> 3) ^ (r & 7)) & 7) << 4) + (j & 7) * 2);
@@ -53,8 +48,7 @@ __host__ __device__ constexpr int64_t n_slots(int64_t t_total, int64_t n_seqs) {
 }
 __host__ __device__ constexpr int64_t slot_base(int64_t seq_start, int64_t s) { return seq_start / C + s; }
 
-constexpr int X_TILE_BYTES = 16384;           // 128 rows x 64 bf16
-constexpr int X_BYTES = 2 * X_TILE_BYTES;     // hi tile, then lo tile
+constexpr int X_BYTES = 16384;                // 128 rows x 64 fp16
 __host__ __device__ constexpr int64_t x_region_offset(int64_t n_slots_total, int64_t h_v) {
     return (n_slots_total * h_v * SLOT_BYTES + 1023) / 1024 * 1024;
 }

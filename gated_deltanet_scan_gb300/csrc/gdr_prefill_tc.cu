@@ -13,23 +13,33 @@
 // with S_c the state before the chunk and gamma_c = G_C its total log decay:
 //   A_c   = [K S_c; Q S_c]                          (an accumulator, see below)
 //   R     = V - diag(e^G) K S_c
-//   MMA2  [D~; P D] = [Tw; PTw] R                   A = [Tw; PTw]_hi and _lo, B = [R_hi | R_lo]
+//   MMA2  [D~; P D] = [Tw; PTw] R                   A = [Tw; PTw], B = R (fp16)
 //         (D = T diag(beta) R is the chunk's delta correction, D~ = diag(exp(G_C - G)) D)
 //   O     = scale (diag(e^G) Q S_c + P D)
-//   MMA3  Y = K_cᵀ D~                                A = Kᵀ, B = [D~_hi | D~_lo]
+//   MMA3  Y = K_cᵀ D~                                A = Kᵀ, B = D~ (fp16)
 //   S_c+1 = e^gamma_c S_c + Y
 // The next chunk's accumulator is formed by lookahead.  Since
 // S_c+1 = e^gamma_c S_c + K_cᵀ D~_c,
 //   A_c+1 = [K; Q]_c+1 (e^gamma_c S_c) + X_c D~_c,        X_c = [K; Q]_c+1 K_cᵀ:
 // MMA1' (the first term) is issued as soon as S_c is known, in the shadow of
-// MMA2, and only MMA_X = X_c [D~_hi | D~_lo] (X_c's hi and lo tiles, four
-// token k-steps each) lies between one chunk's D~ and the next chunk's R.  The
-// chunk-to-chunk path is MMA_X, R, MMA2, D~: two dependent MMA groups per
-// chunk; MMA3 and the state update run beside it.
-// A tcgen05 MMA of N <= 64 costs about the same as one of N = 32, so each B
-// operand carries its bf16 hi and lo halves side by side (N = 64) and the
-// partial products are summed when the accumulator is read: every product that
-// feeds the state keeps ~2^-16 relative precision.
+// MMA2, and only MMA_X = X_c D~ (four token k-steps) lies between one chunk's
+// D~ and the next chunk's R.  The chunk-to-chunk path is MMA_X, R, MMA2, D~:
+// two dependent MMA groups per chunk; MMA3 and the state update run beside it.
+// Precision: the state-sized product MMA1' keeps ~2^-16 relative precision: its
+// B operand carries the bf16 hi and lo halves of S' side by side (N = 64; a
+// tcgen05 MMA of N <= 64 costs about the same as one of N = 32) and the reader
+// adds the two partial products; K and Q are exact in bf16.  MMA2, MMA_X and MMA3 take
+// fp16 operands (2^-11 relative rounding of Tw, PTw, X, R and D~; K converted
+// to fp16 in place, exactly, once MMA1' has read it), one pass of four k-steps
+// each: a tcgen05 MMA costs the same in fp16 as in bf16, and the hi/lo split of
+// both sides needed two.  Their fp16 B tiles keep the N = 64 layout of the
+// hi/lo tiles with the second half zero, so every accumulator has the same
+// column map.  The error this adds stays an order of magnitude below the
+// tolerances on the outputs and the state (fp16 keeps 3 more significand bits
+// than bf16) and does not grow with the number of chunks, since each chunk's
+// rounding enters the state once, scaled by the decays after it.  The fp16
+// range bounds the supported inputs: |R|, |D~| and the factors must stay below
+// 65504 (with L2-normalised q and k they are O(|v| + |S|)).
 //
 // Warp roles (448 threads; every role waits only on mbarriers and its own
 // named barriers, so no role can stall another's issue):
@@ -41,8 +51,8 @@
 //     update it from Y and write S' while MMA2 runs;
 //   warp 12 issues every MMA (converged, one elected lane);
 //   warp 13, one thread, issues every copy: K, Q and V tiles three chunks deep
-//     by TMA; the [Tw; PTw] and X operand tiles one chunk ahead and the gates two
-//     ahead by bulk copy, prefetched into L2 two chunks before.
+//     by TMA; the [Tw; PTw] and X operand tiles about two chunks ahead and the
+//     gates two ahead by bulk copy, prefetched into L2 two chunks before.
 // Every mbarrier wait is bounded; on timeout the thread records
 // GDR_ERR_DEVICE_TIMEOUT and raises the CTA's abort flag, every role leaves its
 // loop at its next wait or role barrier, and the CTA frees its TMEM.
@@ -80,18 +90,21 @@ constexpr uint32_t KQ_BYTES = 32768;  // [K rows 0-63; Q rows 64-127] x 2 K-halv
 constexpr uint32_t V_BYTES = 64 * BV * 2;                 // 64 tokens x 32 columns, 64-B swizzled rows
 constexpr uint32_t OFF_KQ = 0;
 constexpr uint32_t OFF_V = OFF_KQ + NKQ * KQ_BYTES;
-// The operand ring: NOP slots of one 16 KB A-operand tile (K-major 128 x 64 bf16,
+// The operand ring: NOP slots of one 16 KB A-operand tile (K-major 128 x 64 fp16,
 // 128-byte swizzled), filled in the order the MMAs read them: per chunk c the
-// [Tw; PTw] hi and lo tiles (MMA2), then, unless c is the last chunk, X_c's hi
-// and lo tiles (MMA_X).  Item i of that sequence sits in slot i % NOP, so each
-// copy can start as soon as the item NOP places earlier has been read: at least
-// a chunk ahead of its use.
-constexpr int NOP = 5;
+// [Tw; PTw] tile (MMA2), then, unless c is the last chunk, X_c (MMA_X).  Item i
+// of that sequence sits in slot i % NOP, so each copy can start as soon as the
+// item NOP places earlier has been read: two chunks ahead of its use.  With
+// NOP = 4 the item that frees a slot is the previous use of the same full
+// barrier (two per kind, by chunk parity), and the issuer has waited for that
+// use before issuing the MMAs that free the slot: no full barrier can complete
+// a phase its waiter has not yet seen.
+constexpr int NOP = 4;
 constexpr uint32_t OP_BYTES = 16384;
 constexpr uint32_t OFF_OPS = OFF_V + NKQ * V_BYTES;
 constexpr uint32_t OFF_S = OFF_OPS + NOP * OP_BYTES;      // [S'_hi | S'_lo]: 128 (k) rows x 64 bf16, MN-major
-constexpr uint32_t OFF_R = OFF_S + 16384;                 // [R_hi | R_lo]: 64 (token) rows x 64 bf16
-constexpr uint32_t OFF_DT = OFF_R + 8192;                 // [D~_hi | D~_lo]: 64 rows x 64 bf16
+constexpr uint32_t OFF_R = OFF_S + 16384;                 // [R | 0]: 64 (token) rows x 64 fp16, MN-major
+constexpr uint32_t OFF_DT = OFF_R + 8192;                 // [D~ | 0]: 64 rows x 64 fp16
 constexpr uint32_t OFF_GATES = OFF_DT + 8192;             // exp(G) of two chunks, 64 floats each
 constexpr uint32_t OFF_SMALL = OFF_GATES + 2 * 256;
 constexpr uint32_t SM_BARS = OFF_SMALL;                   // NBARS x uint64
@@ -110,8 +123,8 @@ constexpr int B_KQ_FULL = 0;                // NKQ: K, Q, V tiles landed
 constexpr int B_KQ_EMPTY = B_KQ_FULL + NKQ; // NKQ: MMA3 of the chunk done (its tiles free)
 constexpr int B_G_FULL = B_KQ_EMPTY + NKQ; // 2: a chunk's gates landed
 constexpr int B_G_EMPTY = B_G_FULL + 2;     // 2: chain and loader done with a chunk's gates
-constexpr int B_A_FULL = B_G_EMPTY + 2;    // 2: a chunk's [Tw; PTw] hi and lo tiles landed (two arrivals)
-constexpr int B_X_FULL = B_A_FULL + 2;     // 2: a chunk's X hi and lo tiles landed (two arrivals)
+constexpr int B_A_FULL = B_G_EMPTY + 2;    // 2: a chunk's [Tw; PTw] tile landed
+constexpr int B_X_FULL = B_A_FULL + 2;     // 2: a chunk's X tile landed
 constexpr int B_OP_FREE = B_X_FULL + 2;    // NOP: an operand-ring slot's MMAs have read it
 constexpr int B_S_READY = B_OP_FREE + NOP; // S_c formed and S' = e^gamma_c S_c written (for MMA1')
 constexpr int B_ACC = B_S_READY + 1;        // a chunk's accumulator A_c complete
@@ -120,11 +133,11 @@ constexpr int B_Y = B_MMA2 + 1;             // Kᵀ D~ ready
 constexpr int NBARS = B_Y + 1;
 static_assert(NBARS * 8 <= 192, "barrier space");
 
-// TMEM columns (fp32 accumulators, lane = row).  Each holds [hi-part | lo-part]
-// products of a thread's 16 columns in 32 consecutive columns; readers add the
-// two halves.
+// TMEM columns (fp32 accumulators, lane = row).  Each holds the products of a
+// thread's 16 columns in 32 consecutive columns: [hi-part | lo-part] of MMA1',
+// which the reader adds, or [product | 0] of an fp16 B tile.
 constexpr uint32_t TM_ACC = 0;     // + 64 (c % 2): A_c = [K S; Q S] of chunk c
-constexpr uint32_t TM_D = 128;     // [D~; P D] = [Tw; PTw]_hi R + [Tw; PTw]_lo R
+constexpr uint32_t TM_D = 128;     // [D~; P D] = [Tw; PTw] R
 constexpr uint32_t TM_Y = 192;     // Kᵀ D~
 constexpr uint32_t TM_COLS = 256;  // allocation (a power of two)
 constexpr int NLOW_SYNC = NLOW + NISSUE;     // BAR_LOW: the K / T-row threads and the issuing warp
@@ -133,8 +146,9 @@ constexpr int NCHAIN_SYNC = NCHAIN + NISSUE; // BAR_CHAIN: the chain and the iss
 constexpr uint32_t KQV_TX = 2 * 16384 + V_BYTES;
 constexpr long long kWaitLimit = 4000000000LL;  // SM clocks (about 2 s)
 
-constexpr uint32_t IDESC_N64 = idesc_bf16_f32(128, 64, 0, 1);  // A K-major, B MN-major
-constexpr uint32_t IDESC_Y = idesc_bf16_f32(128, 64, 1, 1);    // A MN-major (Kᵀ), B MN-major
+constexpr uint32_t IDESC_N64 = idesc_bf16_f32(128, 64, 0, 1);   // MMA1': A K-major, B MN-major
+constexpr uint32_t IDESC16_N64 = idesc_f16_f32(128, 64, 0, 1);  // MMA2, MMA_X
+constexpr uint32_t IDESC16_Y = idesc_f16_f32(128, 64, 1, 1);    // MMA3: A MN-major (Kᵀ), B MN-major
 
 struct TcParams {
     int h_qk, h_v, out_bf16;
@@ -196,11 +210,16 @@ __device__ __forceinline__ void acc_sum1(uint32_t lanebase, uint32_t c0, int j0,
 #pragma unroll
     for (int j = 0; j < 16; ++j) out[j] = r[j] + r[16 + j];
 }
+// The same for the product of an fp16 B tile: the second 16 columns are zero.
+__device__ __forceinline__ void acc_prod(uint32_t lanebase, uint32_t c0, int j0, float *out) {
+    tmem_ld16(lanebase + c0 + 2 * j0, out);
+}
 
 // Columns j0 .. j0+15 of row `row` of an N = 64 MN-major B operand with
 // 128-byte rows: group g = j0 / 16 keeps the hi parts in 16-byte chunks 4g, 4g+1
 // and the lo parts in 4g+2, 4g+3 (so each accumulator row has a thread's hi and
-// lo partial products in 32 consecutive columns).
+// lo partial products in 32 consecutive columns).  The fp16 tiles use chunks
+// 4g, 4g+1 alone; 4g+2, 4g+3 stay zero.
 __device__ __forceinline__ void store_hilo_row16(uint8_t *tile, int row, int j0, const float *x) {
     const int g4 = (j0 >> 4) * 4;
 #pragma unroll
@@ -209,6 +228,16 @@ __device__ __forceinline__ void store_hilo_row16(uint8_t *tile, int row, int j0,
         hilo_words(x + 8 * ch, h, l);
         *reinterpret_cast<uint4 *>(tile + sw128_offset(row, g4 + ch)) = make_uint4(h[0], h[1], h[2], h[3]);
         *reinterpret_cast<uint4 *>(tile + sw128_offset(row, g4 + 2 + ch)) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+}
+
+__device__ __forceinline__ void store_f16_row16(uint8_t *tile, int row, int j0, const float *x) {
+    const int g4 = (j0 >> 4) * 4;
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+        const float *w = x + 8 * ch;
+        *reinterpret_cast<uint4 *>(tile + sw128_offset(row, g4 + ch)) =
+            make_uint4(pack_f16x2(w[0], w[1]), pack_f16x2(w[2], w[3]), pack_f16x2(w[4], w[5]), pack_f16x2(w[6], w[7]));
     }
 }
 
@@ -226,11 +255,12 @@ __device__ __forceinline__ void issue_kq_loads(const Ctx &x, int kb, int tok, in
     tma_load_3d(x.sbase + OFF_V + kb * V_BYTES, tmV, bar, cb * BV, h, tok);
 }
 
-// The barrier that item i's copy completes: both tiles of a pair (hi, lo) land
-// on one barrier of two arrivals, so the issuer waits once per pair.
+// The barrier that item i's copy completes (item 2 c + 1 is X_c) and the parity
+// of its use by chunk c = i / 2.
 __device__ __forceinline__ uint32_t op_full_bar(const Ctx &x, int i) {
-    return x.bar(((i & 2) ? B_X_FULL : B_A_FULL) + ((i >> 2) & 1));
+    return x.bar(((i & 1) ? B_X_FULL : B_A_FULL) + ((i >> 1) & 1));
 }
+__device__ __forceinline__ uint32_t op_full_parity(int i) { return (uint32_t)(i >> 2) & 1u; }
 // Item i of the operand ring: the 16 KB tile at `src` into slot i % NOP.
 __device__ __forceinline__ void issue_op_load(const Ctx &x, int i, const uint8_t *src) {
     const uint32_t bar = op_full_bar(x, i);
@@ -242,11 +272,11 @@ __device__ __forceinline__ void issue_gates_load(const Ctx &x, const uint8_t *sl
     mbar_arrive_expect_tx(x.bar(B_G_FULL + gb), 256);
     bulk_load(x.sbase + OFF_GATES + 256 * gb, slot + fac::OFF_EG, 256, x.bar(B_G_FULL + gb));
 }
-// Operand-ring items: 4 c + 0 / 1 are the [Tw; PTw] hi / lo tiles of chunk c,
-// 4 c + 2 / 3 X_c's hi / lo tiles (only while c + 1 < nchunks).
+// Operand-ring items: 2 c is the [Tw; PTw] tile of chunk c, 2 c + 1 X_c (only
+// while c + 1 < nchunks).
 __device__ __forceinline__ bool op_exists(int i, int nchunks) {
-    const int c = i >> 2;
-    return (i & 2) ? c + 1 < nchunks : c < nchunks;
+    const int c = i >> 1;
+    return (i & 1) ? c + 1 < nchunks : c < nchunks;
 }
 
 __device__ __forceinline__ uint32_t lane_base(uint32_t tmem, int warp) {
@@ -255,12 +285,12 @@ __device__ __forceinline__ uint32_t lane_base(uint32_t tmem, int warp) {
 
 // ================================ copies ============================================
 // Warp 13, one thread: every copy into shared memory, in the order in which the
-// chain frees the buffers.  Before the loop: operand items 0-4, the gates of
-// chunks 0 and 1, the K/Q/V tiles of chunks 0-2, and L2 prefetches of the next
-// slots and X tiles.  Per chunk c, in the order the buffers come free: chunk
-// c+2's K/Q/V tiles (MMA3 of chunk c-1 done), operand items 4c+5 and 4c+6 (MMA2
-// of chunk c done), the gates of chunk c+2 (the chain and the loader done with
-// chunk c's), operand items 4c+7 and 4c+8 (MMA_X of chunk c done).
+// chain frees the buffers.  Before the loop: the K/Q/V tiles of chunks 0-2,
+// operand items 0-3 (each with an L2 prefetch of the item four places on), the
+// gates of chunks 0 and 1.  Per chunk c, in the order the buffers come free:
+// chunk c+2's K/Q/V tiles (MMA3 of chunk c-1 issued), [Tw; PTw] of chunk c+2
+// (MMA2 of chunk c done), the gates of chunk c+2 (the chain and the loader done
+// with chunk c's), X_c+2 (MMA_X of chunk c done).
 __device__ void copy_role(const Ctx &x, const TcParams &p, int64_t t0, int nchunks, int64_t slot0, int h,
                           int hq, int cb, const CUtensorMap *tmK, const CUtensorMap *tmQ, const CUtensorMap *tmV) {
     const uint8_t *fsrc = p.ws + ((size_t)slot0 * p.h_v + h) * fac::SLOT_BYTES;
@@ -269,9 +299,8 @@ __device__ void copy_role(const Ctx &x, const TcParams &p, int64_t t0, int nchun
     const uint8_t *xsrc = p.xs + ((size_t)(slot0 + 1) * p.h_qk + hq) * fac::X_BYTES;
     const size_t xstride = (size_t)p.h_qk * fac::X_BYTES;
     auto op_src = [&](int i) -> const uint8_t * {
-        const int c = i >> 2;
-        return (i & 2) ? xsrc + c * xstride + (i & 1) * fac::X_TILE_BYTES
-                       : fsrc + c * fstride + ((i & 1) ? fac::OFF_LO : fac::OFF_HI);
+        const int c = i >> 1;
+        return (i & 1) ? xsrc + c * xstride : fsrc + c * fstride + fac::OFF_T;
     };
     bool bad = false;
     // item i once item i - NOP (same slot) has been read
@@ -279,7 +308,7 @@ __device__ void copy_role(const Ctx &x, const TcParams &p, int64_t t0, int nchun
         if (bad || !op_exists(i, nchunks)) return;
         if (i >= NOP) bad = !wait_or_abort(x, x.bar(B_OP_FREE + i % NOP), (uint32_t)(i / NOP - 1) & 1u);
         if (!bad) issue_op_load(x, i, op_src(i));
-        if (!bad && op_exists(i + 8, nchunks)) prefetch_l2(op_src(i + 8), OP_BYTES);  // two chunks ahead
+        if (!bad && op_exists(i + 4, nchunks)) prefetch_l2(op_src(i + 4), OP_BYTES);  // two chunks ahead
     };
     for (int c = 0; c < nchunks && c < NKQ; ++c) issue_kq_loads(x, c, (int)(t0 + c * C), hq, h, cb, tmK, tmQ, tmV);
     // launched as a programmatic dependent of the factor launch: everything above
@@ -287,22 +316,18 @@ __device__ void copy_role(const Ctx &x, const TcParams &p, int64_t t0, int nchun
     asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int i = 0; i < NOP; ++i) next_op(i);
     for (int c = 0; c < nchunks && c < 2; ++c) issue_gates_load(x, fsrc + c * fstride, c);
-    for (int i = NOP; i < NOP + 3; ++i)
-        if (op_exists(i + 3, nchunks)) prefetch_l2(op_src(i + 3), OP_BYTES);
     for (int c = 0; c < nchunks && !bad; ++c) {
         if (c >= 1 && c - 1 + NKQ < nchunks) {
             const int kb = (c - 1) % NKQ;
             bad = !wait_or_abort(x, x.bar(B_KQ_EMPTY + kb), (uint32_t)((c - 1) / NKQ) & 1u);
             if (!bad) issue_kq_loads(x, kb, (int)(t0 + (c - 1 + NKQ) * C), hq, h, cb, tmK, tmQ, tmV);
         }
-        next_op(4 * c + 5);
-        next_op(4 * c + 6);
+        next_op(2 * c + NOP);
         if (!bad && c + 2 < nchunks) {
             bad = !wait_or_abort(x, x.bar(B_G_EMPTY + (c & 1)), (uint32_t)(c >> 1) & 1u);
             if (!bad) issue_gates_load(x, fsrc + (c + 2) * fstride, c & 1);
         }
-        next_op(4 * c + 7);
-        next_op(4 * c + 8);
+        next_op(2 * c + NOP + 1);
     }
 }
 
@@ -337,7 +362,7 @@ __device__ void loader_role(const Ctx &x, int nchunks, int lt, float *Sg, bool &
 #pragma unroll
                 for (int g2 = 0; g2 < 2; ++g2) {
                     float y[16];
-                    acc_sum1(lb, TM_Y, 16 * g2, y);
+                    acc_prod(lb, TM_Y, 16 * g2, y);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) Sr[16 * g2 + j] = fmaf(eGC_prev, Sr[16 * g2 + j], y[j]);
                 }
@@ -374,7 +399,7 @@ __device__ void loader_role(const Ctx &x, int nchunks, int lt, float *Sg, bool &
 #pragma unroll
         for (int g2 = 0; g2 < 2; ++g2) {
             float y[16];
-            acc_sum1(lb, TM_Y, 16 * g2, y);
+            acc_prod(lb, TM_Y, 16 * g2, y);
 #pragma unroll
             for (int j = 0; j < 16; ++j) Sr[16 * g2 + j] = fmaf(eGC_prev, Sr[16 * g2 + j], y[j]);
         }
@@ -410,8 +435,8 @@ __device__ __forceinline__ void store_out_row(const TcParams &p, int64_t c0, int
 // several times longer per MMA).  Per chunk c, in the tensor pipe's order:
 //   MMA2 (once the K / T-row warps hand it R at BAR_LOW),
 //   MMA1' = [K; Q]_c+1 S' into A_c+1 (once the loader has written S'),
-//   MMA_X = X_c [D~_hi | D~_lo] into A_c+1 and MMA3 = K_cᵀ [D~_hi | D~_lo]
-//   (once the chain has written D~ and read [D~; P D], at BAR_CHAIN).
+//   MMA_X = X_c D~ into A_c+1 and MMA3 = K_cᵀ D~ (once the chain has written
+//   D~, read [D~; P D] and converted K_c to fp16, at BAR_CHAIN).
 
 // [K; Q] (a ring stage) times a [hi | lo] B operand: 8 k-steps over d_k.
 __device__ __forceinline__ void issue_kq_times(uint32_t d_tmem, uint32_t kq, uint64_t dB) {
@@ -430,24 +455,19 @@ __device__ void issuer_role(const Ctx &x, int nchunks, int lane) {
     const uint64_t dDT = smem_desc(x.sbase + OFF_DT, 8192, 1024, kSwizzle128);
     const uint64_t dOp0 = smem_desc_sw128(x.sbase + OFF_OPS, 16, 1024);
     bool bad = false;  // warp-uniform
-    // the hi and lo tiles of pair i, i + 1 (i = 4 c or 4 c + 2) times [B_hi | B_lo],
-    // four k-steps each, into d_tmem: the pair is awaited once (the whole warp) and
-    // each slot released once read (if it is reused)
-    auto pair_mmas = [&](int i, uint32_t d_tmem, uint64_t dB, bool acc_first) {
-        bad = bad || __any_sync(0xffffffffu, !wait_or_abort(x, op_full_bar(x, i), (uint32_t)(i >> 3) & 1u));
+    // operand item i (fp16) times the fp16 B tile, four k-steps, into d_tmem: the
+    // item is awaited by the whole warp and its slot released once read (if reused)
+    auto op_mmas = [&](int i, uint32_t d_tmem, uint64_t dB, bool acc_first) {
+        bad = bad || __any_sync(0xffffffffu, !wait_or_abort(x, op_full_bar(x, i), op_full_parity(i)));
         if (bad) return;
         tc_fence_after_sync();
         if (elect_one()) {
+            const int slot = i % NOP;
+            const uint64_t dA = desc_add(dOp0, slot * OP_BYTES);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int slot = (i + h) % NOP;
-                const uint64_t dA = desc_add(dOp0, slot * OP_BYTES);
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(d_tmem, desc_add(dA, ks * 32), desc_add(dB, ks * 2048), IDESC_N64,
-                             acc_first || h > 0 || ks > 0);
-                if (op_exists(i + h + NOP, nchunks)) mma_commit(x.bar(B_OP_FREE + slot));
-            }
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16(d_tmem, desc_add(dA, ks * 32), desc_add(dB, ks * 2048), IDESC16_N64, acc_first || ks > 0);
+            if (op_exists(i + NOP, nchunks)) mma_commit(x.bar(B_OP_FREE + slot));
         }
         __syncwarp();
     };
@@ -466,8 +486,8 @@ __device__ void issuer_role(const Ctx &x, int nchunks, int lane) {
         const uint32_t par = (uint32_t)c & 1u;
         const bool more = c + 1 < nchunks;
         named_sync(BAR_LOW, NLOW_SYNC);  // R written
-        // ---- MMA2: [D~; P D] = [Tw; PTw]_hi [R_hi | R_lo] + [Tw; PTw]_lo [R_hi | R_lo] -----
-        pair_mmas(4 * c, tmem + TM_D, dR, false);
+        // ---- MMA2: [D~; P D] = [Tw; PTw] R ----------------------------------------------
+        op_mmas(2 * c, tmem + TM_D, dR, false);
         if (!bad) {
             if (elect_one()) mma_commit(x.bar(B_MMA2));
             __syncwarp();
@@ -484,13 +504,12 @@ __device__ void issuer_role(const Ctx &x, int nchunks, int lane) {
                 __syncwarp();
             }
         }
-        const bool stop = named_sync_or(BAR_CHAIN, NCHAIN_SYNC, bad || *x.abort_flag);  // D~ written
+        // D~ written, K_c converted
+        const bool stop = named_sync_or(BAR_CHAIN, NCHAIN_SYNC, bad || *x.abort_flag);
         if (stop) break;
         if (lane == 0) mbar_arrive(x.bar(B_G_EMPTY + (c & 1)));  // the chain has read the gates of chunk c
-        // ---- MMA_X: A_c+1 += X_c [D~_hi | D~_lo]; MMA3: Y = K_cᵀ [D~_hi | D~_lo] ----------
-        if (more) {
-            pair_mmas(4 * c + 2, tmem + TM_ACC + 64 * (ab ^ 1), dDT, true);
-        }
+        // ---- MMA_X: A_c+1 += X_c D~; MMA3: Y = K_cᵀ D~ -----------------------------------
+        if (more) op_mmas(2 * c + 1, tmem + TM_ACC + 64 * (ab ^ 1), dDT, true);
         if (!bad) {
             tc_fence_after_sync();
             if (elect_one()) {
@@ -498,7 +517,7 @@ __device__ void issuer_role(const Ctx &x, int nchunks, int lane) {
                 const uint64_t a0 = smem_desc_sw128(x.sbase + OFF_KQ + kb * KQ_BYTES, 16384, 1024);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + TM_Y, desc_add(a0, ks * 2048), desc_add(dDT, ks * 2048), IDESC_Y, ks > 0);
+                    mma_bf16(tmem + TM_Y, desc_add(a0, ks * 2048), desc_add(dDT, ks * 2048), IDESC16_Y, ks > 0);
                 mma_commit(x.bar(B_Y));
                 // every MMA reading this chunk's tiles is issued
                 if (c + NKQ < nchunks) mma_commit(x.bar(B_KQ_EMPTY + kb));
@@ -542,7 +561,7 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
             if (!bad) acc_sum1(lb, TM_ACC + 64 * ab, j0, ks);
             if (low) {
                 if (!bad) {
-                    // R = V - e^G K S as [R_hi | R_lo]
+                    // R = V - e^G K S in fp16
                     const uint8_t *vt = x.sm + OFF_V + kb * V_BYTES;
                     float r[16];
 #pragma unroll
@@ -552,7 +571,7 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
 #pragma unroll
                         for (int e = 0; e < 8; ++e) r[8 * ch + e] = fmaf(-egt, ks[8 * ch + e], v[e]);
                     }
-                    store_hilo_row16(x.sm + OFF_R, t, j0, r);
+                    store_f16_row16(x.sm + OFF_R, t, j0, r);
                     fence_proxy_async_smem();
                 }
                 tc_fence_before_sync();
@@ -560,6 +579,19 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
             } else {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) qse[j] = egt * ks[j];
+                // K_c to fp16 in place for MMA3: A_c complete means MMA1' (or, for
+                // chunk 0, the MMA forming A_0) has read it as bf16
+                if (!bad) {
+                    const int kidx = (((warp >> 2) << 1) | ((warp & 3) - 2)) * 32 + lane;  // 0-127
+                    uint8_t *kt = x.sm + OFF_KQ + kb * KQ_BYTES;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int q = kidx + 128 * i;  // 16-byte chunk of the two 8 KB K halves
+                        uint4 *pk = reinterpret_cast<uint4 *>(kt + (q >> 9) * 16384 + (q & 511) * 16);
+                        *pk = bf16x8_to_f16x8(*pk);
+                    }
+                    fence_proxy_async_smem();
+                }
             }
         }
         // ---- [D~; P D] from MMA2 ----------------------------------------------------------
@@ -568,11 +600,11 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
         float ov[16];
         {
             float d[16];
-            if (!bad) acc_sum1(lb, TM_D, j0, d);
+            if (!bad) acc_prod(lb, TM_D, j0, d);
             if (low) {
                 if (!bad) {
-                    // D~ as [D~_hi | D~_lo]
-                    store_hilo_row16(x.sm + OFF_DT, t, j0, d);
+                    // D~ in fp16
+                    store_f16_row16(x.sm + OFF_DT, t, j0, d);
                     fence_proxy_async_smem();
                 }
             } else {
@@ -621,7 +653,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (tid == 0) {
-        for (int i = 0; i < NBARS; ++i) mbar_init(x.bar(i), i >= B_A_FULL && i < B_A_FULL + 4 ? 2 : 1);
+        for (int i = 0; i < NBARS; ++i) mbar_init(x.bar(i), 1);
         *x.abort_flag = 0;
         fence_mbar_init();
     }
@@ -649,6 +681,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             store_hilo_row16(x.sm + OFF_S, lt, 16 * g2, s0);
         }
+        fence_proxy_async_smem();
+    } else if (tid < NCHAIN) {
+        // the zero second halves of the fp16 R and D~ tiles (16 KB, contiguous)
+        uint4 *z = reinterpret_cast<uint4 *>(x.sm + OFF_R) + 4 * tid;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) z[i] = make_uint4(0u, 0u, 0u, 0u);
         fence_proxy_async_smem();
     }
     tc_fence_before_sync();

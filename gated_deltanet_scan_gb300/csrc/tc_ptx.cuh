@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace gdr {
@@ -146,7 +147,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_maj
            | ((uint32_t)(M >> 4) << 24);  // M / 16
 }
 
+// The same with fp16 A/B (both operands of one kind::f16 MMA have one type).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int a_mn_major, int b_mn_major) {
+    return (1u << 4)                      // D format: f32; A and B format codes 0: f16
+           | ((uint32_t)a_mn_major << 15)
+           | ((uint32_t)b_mn_major << 16)
+           | ((uint32_t)(N >> 3) << 17)
+           | ((uint32_t)(M >> 4) << 24);
+}
+
 // ---- MMA ------------------------------------------------------------------------------
+// One kind::f16 MMA; the instruction descriptor gives the operand type (bf16 or fp16).
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -202,6 +213,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+// fp16 pair, round to nearest even: a in the low half, b in the high half.
+__device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+// Eight bf16 values (one 16-byte chunk) as eight fp16 values in place of them:
+// exact for every bf16 value inside the fp16 normal range.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = pack_f16x2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
     return (uint32_t)(row * 128 + (((chunk ^ (row & 7)) & 7) << 4));

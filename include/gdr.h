@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define GDR_ABI_VERSION 5
+#define GDR_ABI_VERSION 6
 
 /* Same object as cudaStream_t; declared here so callers need no CUDA header. */
 typedef struct CUstream_st *gdr_stream_t;
@@ -87,12 +87,12 @@ const char *gdr_status_string(gdr_status status);
 /*
  * Bytes of device workspace gdr_prefill_chunked needs for this problem: 0 when
  * the CUDA-core path runs (or for an empty problem), otherwise, for each of
- * P = ceil(t_total / 64) + n_seqs chunk positions, one 33,024-byte slot of
- * per-chunk factors per V head (T and P T as bf16 hi/lo MMA operand tiles, and
- * the chunk's exp(G)), then, from the next 1 KiB boundary, one 32 KiB pair of
- * bf16 hi/lo tiles per QK head of X = [K; Q]_c K_{c-1}^T (the next chunk's
- * keys and queries against this chunk's keys), rounded up to 256 bytes:
- * roundup(roundup(P * h_v * 33024, 1024) + P * h_qk * 32768, 256).
+ * P = ceil(t_total / 64) + n_seqs chunk positions, one 16,640-byte slot of
+ * per-chunk factors per V head (T and P T as an fp16 MMA operand tile, and the
+ * chunk's exp(G)), then, from the next 1 KiB boundary, one 16 KiB fp16 tile
+ * per QK head of X = [K; Q]_c K_{c-1}^T (the next chunk's keys and queries
+ * against this chunk's keys), rounded up to 256 bytes:
+ * roundup(roundup(P * h_v * 16640, 1024) + P * h_qk * 16384, 256).
  * Host-only, never fails (invalid dims: 0).
  */
 size_t gdr_prefill_workspace_bytes(const gdr_dims *dims, int32_t n_seqs, int64_t t_total);
@@ -141,6 +141,13 @@ size_t gdr_prefill_workspace_bytes(const gdr_dims *dims, int32_t n_seqs, int64_t
  *               other streams until this call's work on `stream` is done.  May
  *               be NULL when that size is 0.  Too small or misaligned:
  *               GDR_ERR_INVALID_ARG before anything is launched.
+ *
+ * Precision on the tensor-core path: the state is carried in fp32 and every
+ * state-sized product keeps ~2^-16 relative precision (bf16 hi/lo operand
+ * splits); the chunk-sized products with the factors (the correction D, the
+ * intra-chunk output part, X D~ and K^T D~) take fp16 operands with fp32
+ * accumulation.  Their operands must stay inside the fp16 range (|x| < 65504):
+ * with L2-normalised q and k this holds while |v| and the state entries do.
  */
 gdr_status gdr_prefill_chunked(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens,
                                int64_t t_total, const void *q, const void *k, const void *v,

@@ -91,12 +91,12 @@ def test_prefill_rejects_bad_pointers_and_counts(L):
 
 def test_prefill_workspace_size_and_checks(L):
     d = dims()
-    # one 33,024-byte slot per (chunk position, V head), positions = ceil(T / 64) + n_seqs,
-    # then from the next 1 KiB boundary one 32 KiB pair of X tiles per (position, QK head)
+    # one 16,640-byte slot per (chunk position, V head), positions = ceil(T / 64) + n_seqs,
+    # then from the next 1 KiB boundary one 16 KiB X tile per (position, QK head)
     need = L.gdr_prefill_workspace_bytes(ctypes.byref(d), 3, 1000)
     slots = (1000 + 63) // 64 + 3
-    x_off = (slots * 32 * 33024 + 1023) // 1024 * 1024
-    assert need == (x_off + slots * 16 * 32768 + 255) // 256 * 256
+    x_off = (slots * 32 * 16640 + 1023) // 1024 * 1024
+    assert need == (x_off + slots * 16 * 16384 + 255) // 256 * 256
     assert L.gdr_prefill_workspace_bytes(ctypes.byref(d), 0, 0) == 0
     assert L.gdr_prefill_workspace_bytes(ctypes.byref(dims(in_dtype=gdr.GDR_F32)), 3, 1000) == 0
     assert L.gdr_prefill_workspace_bytes(ctypes.byref(dims(chunk=16)), 3, 1000) == 0

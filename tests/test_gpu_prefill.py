@@ -51,8 +51,9 @@ def test_long_prefill_T16384(run):
 @pytest.mark.parametrize("chunk", [16, 64])
 @pytest.mark.parametrize("T", [1, 15, 16, 17, 63, 64, 65, 128, 192, 256, 320, 449, 1000])
 def test_lengths_around_chunk_boundaries(T, chunk):
-    """Also 3, 4, 5 and 8 chunks of 64: the tensor-core scan's five-slot operand
-    ring (four tiles per chunk, none for X after the last chunk) wraps at each."""
+    """Also 1 to 16 chunks of 64: the tensor-core scan's four-slot operand ring
+    (two tiles per chunk, none for X after the last chunk) wraps every two chunks,
+    and its two full barriers per tile kind alternate by chunk parity."""
     w = synth.make_workload("len", [T], 16, 32, 128, chunk, "bf16", seed=T, state_std=0.02)
     check(w)
 
@@ -84,8 +85,9 @@ def test_chunk_size_does_not_change_the_result():
     w = synth.make_workload("chunks", [333], 16, 32, 128, 64, "bf16", seed=7, state_std=0.02)
     o64, s64 = run_prefill(w, chunk=64)
     o16, s16 = run_prefill(w, chunk=16)
-    assert gu.o_error(o64, o16) < 2e-3
-    assert gu.state_error(s64, s16) < 1e-4
+    # chunk 64 runs on the tensor cores (fp16 factor operands), chunk 16 on CUDA cores in fp32
+    assert gu.o_error(o64, o16) < gu.TC_O_TOL
+    assert gu.state_error(s64, s16) < gu.TC_S_TOL
 
 
 def test_prefill_then_decode_handoff():
