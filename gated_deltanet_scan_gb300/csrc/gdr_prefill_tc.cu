@@ -13,10 +13,10 @@
 // with S_c the state before the chunk and gamma_c = G_C its total log decay:
 //   A_c   = [K S_c; Q S_c]                          (an accumulator, see below)
 //   R     = V - diag(e^G) K S_c
-//   MMA2  [D~; P D] = [Tw; PTw] R                   A = [Tw; PTw], B = R (fp16)
+//   MMA2  [D~; P D] = [Tw; PTw] R                   A = [Tw; PTw], B = R (both fp16)
 //         (D = T diag(beta) R is the chunk's delta correction, D~ = diag(exp(G_C - G)) D)
 //   O     = scale (diag(e^G) Q S_c + P D)
-//   MMA3  Y = K_cᵀ D~                                A = Kᵀ, B = D~ (fp16)
+//   MMA3  Y = K_cᵀ D~                                A = Kᵀ, B = [D~_hi | D~_lo]
 //   S_c+1 = e^gamma_c S_c + Y
 // The next chunk's accumulator is formed by lookahead.  Since
 // S_c+1 = e^gamma_c S_c + K_cᵀ D~_c,
@@ -25,21 +25,20 @@
 // MMA2, and only MMA_X = X_c D~ (four token k-steps) lies between one chunk's
 // D~ and the next chunk's R.  The chunk-to-chunk path is MMA_X, R, MMA2, D~:
 // two dependent MMA groups per chunk; MMA3 and the state update run beside it.
-// Precision: the state-sized product MMA1' keeps ~2^-16 relative precision: its
-// B operand carries the bf16 hi and lo halves of S' side by side (N = 64; a
-// tcgen05 MMA of N <= 64 costs about the same as one of N = 32) and the reader
-// adds the two partial products; K and Q are exact in bf16.  MMA2, MMA_X and MMA3 take
-// fp16 operands (2^-11 relative rounding of Tw, PTw, X, R and D~; K converted
-// to fp16 in place, exactly, once MMA1' has read it), one pass of four k-steps
-// each: a tcgen05 MMA costs the same in fp16 as in bf16, and the hi/lo split of
-// both sides needed two.  Their fp16 B tiles keep the N = 64 layout of the
-// hi/lo tiles with the second half zero, so every accumulator has the same
-// column map.  The error this adds stays an order of magnitude below the
-// tolerances on the outputs and the state (fp16 keeps 3 more significand bits
-// than bf16) and does not grow with the number of chunks, since each chunk's
-// rounding enters the state once, scaled by the decays after it.  The fp16
+// Precision: the state-sized products keep ~2^-16 relative precision: K and Q
+// are exact in bf16, and the B operands of MMA1' and MMA3 carry the bf16 hi and
+// lo halves of S' and of D~ side by side (N = 64; a tcgen05 MMA of N <= 64
+// costs about the same as one of N = 32); the reader adds the two partial
+// products.  MMA2 and MMA_X take fp16 operands instead (2^-11 relative
+// rounding of Tw, PTw, X, R and D~), one pass of four k-steps each where bf16
+// hi/lo splits of both sides needed two (a tcgen05 MMA costs the same in fp16
+// as in bf16).  Their fp16 B tiles keep the N = 64 column map with the second
+// half zero.  The rounding of Tw and PTw dominates the error this adds: on
+// Qwen3.5-9B shapes about 1e-2 of the output RMS (max-abs) and 3e-4 of the
+// state (relative Frobenius), not growing with the number of chunks, since
+// each chunk's rounding enters the state once and decays with it.  The fp16
 // range bounds the supported inputs: |R|, |D~| and the factors must stay below
-// 65504 (with L2-normalised q and k they are O(|v| + |S|)).
+// 65504 (with L2-normalised q and k they are of the order of |v| and |S|).
 //
 // Warp roles (448 threads; every role waits only on mbarriers and its own
 // named barriers, so no role can stall another's issue):
@@ -105,7 +104,8 @@ constexpr uint32_t OFF_OPS = OFF_V + NKQ * V_BYTES;
 constexpr uint32_t OFF_S = OFF_OPS + NOP * OP_BYTES;      // [S'_hi | S'_lo]: 128 (k) rows x 64 bf16, MN-major
 constexpr uint32_t OFF_R = OFF_S + 16384;                 // [R | 0]: 64 (token) rows x 64 fp16, MN-major
 constexpr uint32_t OFF_DT = OFF_R + 8192;                 // [D~ | 0]: 64 rows x 64 fp16
-constexpr uint32_t OFF_GATES = OFF_DT + 8192;             // exp(G) of two chunks, 64 floats each
+constexpr uint32_t OFF_DT2 = OFF_DT + 8192;               // [D~_hi | D~_lo]: 64 rows x 64 bf16 (MMA3)
+constexpr uint32_t OFF_GATES = OFF_DT2 + 8192;             // exp(G) of two chunks, 64 floats each
 constexpr uint32_t OFF_SMALL = OFF_GATES + 2 * 256;
 constexpr uint32_t SM_BARS = OFF_SMALL;                   // NBARS x uint64
 constexpr uint32_t SM_TMEM = OFF_SMALL + 192;
@@ -114,7 +114,7 @@ constexpr uint32_t SMEM_USED = OFF_SMALL + 256;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_V % 1024 == 0 && OFF_OPS % 1024 == 0 && OFF_S % 1024 == 0 &&
-                  OFF_R % 1024 == 0 && OFF_DT % 1024 == 0 && OFF_GATES % 16 == 0,
+                  OFF_R % 1024 == 0 && OFF_DT % 1024 == 0 && OFF_DT2 % 1024 == 0 && OFF_GATES % 16 == 0,
               "operand tiles must be 1 KB aligned, bulk copies 16 B aligned");
 
 // mbarriers.  Each completes one phase per use; no waiter can fall two phases
@@ -134,8 +134,9 @@ constexpr int NBARS = B_Y + 1;
 static_assert(NBARS * 8 <= 192, "barrier space");
 
 // TMEM columns (fp32 accumulators, lane = row).  Each holds the products of a
-// thread's 16 columns in 32 consecutive columns: [hi-part | lo-part] of MMA1',
-// which the reader adds, or [product | 0] of an fp16 B tile.
+// thread's 16 columns in 32 consecutive columns: [hi-part | lo-part] of a bf16
+// hi/lo B tile (MMA1', MMA3), which the reader adds, or [product | 0] of an fp16
+// B tile (MMA2; MMA_X adds into A's hi part).
 constexpr uint32_t TM_ACC = 0;     // + 64 (c % 2): A_c = [K S; Q S] of chunk c
 constexpr uint32_t TM_D = 128;     // [D~; P D] = [Tw; PTw] R
 constexpr uint32_t TM_Y = 192;     // Kᵀ D~
@@ -148,7 +149,7 @@ constexpr long long kWaitLimit = 4000000000LL;  // SM clocks (about 2 s)
 
 constexpr uint32_t IDESC_N64 = idesc_bf16_f32(128, 64, 0, 1);   // MMA1': A K-major, B MN-major
 constexpr uint32_t IDESC16_N64 = idesc_f16_f32(128, 64, 0, 1);  // MMA2, MMA_X
-constexpr uint32_t IDESC16_Y = idesc_f16_f32(128, 64, 1, 1);    // MMA3: A MN-major (Kᵀ), B MN-major
+constexpr uint32_t IDESC_Y = idesc_bf16_f32(128, 64, 1, 1);     // MMA3: A MN-major (Kᵀ), B MN-major
 
 struct TcParams {
     int h_qk, h_v, out_bf16;
@@ -187,9 +188,11 @@ __device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool 
 }
 
 // Bounded wait that also gives up as soon as any thread of the CTA has raised
-// the abort flag.  Returns false on either.
+// the abort flag.  Returns false on either.  Most phases have completed by the
+// time they are awaited: a non-blocking test finds those sooner than a
+// blocking try_wait does.
 __device__ bool wait_or_abort(const Ctx &x, uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -308,7 +311,8 @@ __device__ void copy_role(const Ctx &x, const TcParams &p, int64_t t0, int nchun
         if (bad || !op_exists(i, nchunks)) return;
         if (i >= NOP) bad = !wait_or_abort(x, x.bar(B_OP_FREE + i % NOP), (uint32_t)(i / NOP - 1) & 1u);
         if (!bad) issue_op_load(x, i, op_src(i));
-        if (!bad && op_exists(i + 4, nchunks)) prefetch_l2(op_src(i + 4), OP_BYTES);  // two chunks ahead
+        // two chunks ahead; a [Tw; PTw] tile with the slot's exp(G) after it
+        if (!bad && op_exists(i + 4, nchunks)) prefetch_l2(op_src(i + 4), (i & 1) ? OP_BYTES : fac::SLOT_BYTES);
     };
     for (int c = 0; c < nchunks && c < NKQ; ++c) issue_kq_loads(x, c, (int)(t0 + c * C), hq, h, cb, tmK, tmQ, tmV);
     // launched as a programmatic dependent of the factor launch: everything above
@@ -362,7 +366,7 @@ __device__ void loader_role(const Ctx &x, int nchunks, int lt, float *Sg, bool &
 #pragma unroll
                 for (int g2 = 0; g2 < 2; ++g2) {
                     float y[16];
-                    acc_prod(lb, TM_Y, 16 * g2, y);
+                    acc_sum1(lb, TM_Y, 16 * g2, y);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) Sr[16 * g2 + j] = fmaf(eGC_prev, Sr[16 * g2 + j], y[j]);
                 }
@@ -399,7 +403,7 @@ __device__ void loader_role(const Ctx &x, int nchunks, int lt, float *Sg, bool &
 #pragma unroll
         for (int g2 = 0; g2 < 2; ++g2) {
             float y[16];
-            acc_prod(lb, TM_Y, 16 * g2, y);
+            acc_sum1(lb, TM_Y, 16 * g2, y);
 #pragma unroll
             for (int j = 0; j < 16; ++j) Sr[16 * g2 + j] = fmaf(eGC_prev, Sr[16 * g2 + j], y[j]);
         }
@@ -436,7 +440,7 @@ __device__ __forceinline__ void store_out_row(const TcParams &p, int64_t c0, int
 //   MMA2 (once the K / T-row warps hand it R at BAR_LOW),
 //   MMA1' = [K; Q]_c+1 S' into A_c+1 (once the loader has written S'),
 //   MMA_X = X_c D~ into A_c+1 and MMA3 = K_cᵀ D~ (once the chain has written
-//   D~, read [D~; P D] and converted K_c to fp16, at BAR_CHAIN).
+//   D~, read [D~; P D], at BAR_CHAIN).
 
 // [K; Q] (a ring stage) times a [hi | lo] B operand: 8 k-steps over d_k.
 __device__ __forceinline__ void issue_kq_times(uint32_t d_tmem, uint32_t kq, uint64_t dB) {
@@ -453,6 +457,7 @@ __device__ void issuer_role(const Ctx &x, int nchunks, int lane) {
     const uint64_t dS = smem_desc(x.sbase + OFF_S, 8192, 1024, kSwizzle128);
     const uint64_t dR = smem_desc(x.sbase + OFF_R, 8192, 1024, kSwizzle128);
     const uint64_t dDT = smem_desc(x.sbase + OFF_DT, 8192, 1024, kSwizzle128);
+    const uint64_t dDT2 = smem_desc(x.sbase + OFF_DT2, 8192, 1024, kSwizzle128);
     const uint64_t dOp0 = smem_desc_sw128(x.sbase + OFF_OPS, 16, 1024);
     bool bad = false;  // warp-uniform
     // operand item i (fp16) times the fp16 B tile, four k-steps, into d_tmem: the
@@ -504,7 +509,7 @@ __device__ void issuer_role(const Ctx &x, int nchunks, int lane) {
                 __syncwarp();
             }
         }
-        // D~ written, K_c converted
+        // D~ written
         const bool stop = named_sync_or(BAR_CHAIN, NCHAIN_SYNC, bad || *x.abort_flag);
         if (stop) break;
         if (lane == 0) mbar_arrive(x.bar(B_G_EMPTY + (c & 1)));  // the chain has read the gates of chunk c
@@ -517,7 +522,7 @@ __device__ void issuer_role(const Ctx &x, int nchunks, int lane) {
                 const uint64_t a0 = smem_desc_sw128(x.sbase + OFF_KQ + kb * KQ_BYTES, 16384, 1024);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    mma_bf16(tmem + TM_Y, desc_add(a0, ks * 2048), desc_add(dDT, ks * 2048), IDESC16_Y, ks > 0);
+                    mma_bf16(tmem + TM_Y, desc_add(a0, ks * 2048), desc_add(dDT2, ks * 2048), IDESC_Y, ks > 0);
                 mma_commit(x.bar(B_Y));
                 // every MMA reading this chunk's tiles is issued
                 if (c + NKQ < nchunks) mma_commit(x.bar(B_KQ_EMPTY + kb));
@@ -579,19 +584,6 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
             } else {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) qse[j] = egt * ks[j];
-                // K_c to fp16 in place for MMA3: A_c complete means MMA1' (or, for
-                // chunk 0, the MMA forming A_0) has read it as bf16
-                if (!bad) {
-                    const int kidx = (((warp >> 2) << 1) | ((warp & 3) - 2)) * 32 + lane;  // 0-127
-                    uint8_t *kt = x.sm + OFF_KQ + kb * KQ_BYTES;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int q = kidx + 128 * i;  // 16-byte chunk of the two 8 KB K halves
-                        uint4 *pk = reinterpret_cast<uint4 *>(kt + (q >> 9) * 16384 + (q & 511) * 16);
-                        *pk = bf16x8_to_f16x8(*pk);
-                    }
-                    fence_proxy_async_smem();
-                }
             }
         }
         // ---- [D~; P D] from MMA2 ----------------------------------------------------------
@@ -603,8 +595,9 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
             if (!bad) acc_prod(lb, TM_D, j0, d);
             if (low) {
                 if (!bad) {
-                    // D~ in fp16
+                    // D~ in fp16 (MMA_X) and as bf16 hi/lo (MMA3)
                     store_f16_row16(x.sm + OFF_DT, t, j0, d);
+                    store_hilo_row16(x.sm + OFF_DT2, t, j0, d);
                     fence_proxy_async_smem();
                 }
             } else {

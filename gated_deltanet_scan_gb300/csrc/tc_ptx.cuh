@@ -50,6 +50,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Non-blocking test of a phase (acquire at CTA scope).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -218,15 +231,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 __device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
     __half2 v = __floats2half2_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&v);
-}
-// Eight bf16 values (one 16-byte chunk) as eight fp16 values in place of them:
-// exact for every bf16 value inside the fp16 normal range.
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) o[i] = pack_f16x2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
-    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
     return (uint32_t)(row * 128 + (((chunk ^ (row & 7)) & 7) << 4));

@@ -145,7 +145,7 @@ size_t gdr_prefill_workspace_bytes(const gdr_dims *dims, int32_t n_seqs, int64_t
  * Precision on the tensor-core path: the state is carried in fp32 and every
  * state-sized product keeps ~2^-16 relative precision (bf16 hi/lo operand
  * splits); the chunk-sized products with the factors (the correction D, the
- * intra-chunk output part, X D~ and K^T D~) take fp16 operands with fp32
+ * intra-chunk output part and X D~) take fp16 operands with fp32
  * accumulation.  Their operands must stay inside the fp16 range (|x| < 65504):
  * with L2-normalised q and k this holds while |v| and the state entries do.
  */
