@@ -144,3 +144,22 @@ def test_split_prefill_over_two_sequences(lens):
     the oracle's."""
     w = synth.make_workload("split2", lens, 8, 16, 128, 64, "bf16", seed=51 + lens[0], state_std=0.02)
     check(w)
+
+
+def test_large_values_inside_the_fp16_range():
+    """v and the initial state scaled by 2^12 (exact in bf16 and fp32): the
+    tensor-core path's fp16 operands (R, D~ up to ~2e4 here, below the fp16
+    maximum 65504) keep the same relative accuracy, and the result is 2^12 times
+    the unscaled one up to rounding."""
+    import dataclasses
+    from gated_deltanet_scan_gb300 import synth as sy
+    w = synth.make_workload("scaled", [700], 16, 32, 128, 64, "bf16", seed=11, state_std=0.02)
+    f = np.float32(4096.0)
+    v = w.v * f
+    ws = dataclasses.replace(w, name="scaled_x4096", v=v, v_bits=sy.bf16_bits(v), state0=w.state0 * f)
+    assert np.array_equal(sy.bf16_values(ws.v_bits), v)  # the scaling is exact
+    eo, es = check(ws)
+    o1, s1 = run_prefill(w)
+    o2, s2 = run_prefill(ws)
+    assert gu.o_error(o2 / 4096.0, o1) < 1e-3
+    assert gu.state_error(s2 / 4096.0, s1) < 1e-4
