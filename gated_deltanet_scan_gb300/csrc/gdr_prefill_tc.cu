@@ -37,8 +37,9 @@
 // Qwen3.5-9B shapes about 1e-2 of the output RMS (max-abs) and 3e-4 of the
 // state (relative Frobenius), not growing with the number of chunks, since
 // each chunk's rounding enters the state once and decays with it.  The fp16
-// range bounds the supported inputs: |R|, |D~| and the factors must stay below
-// 65504 (with L2-normalised q and k they are of the order of |v| and |S|).
+// range bounds the supported inputs: R and D~ scale with v and the state (the
+// factors do not); they must stay below 65504, and their RMS above ~1e-4, below
+// which the fp16 subnormals cost accuracy.
 //
 // Warp roles (448 threads; every role waits only on mbarriers and its own
 // named barriers, so no role can stall another's issue):

@@ -146,8 +146,10 @@ size_t gdr_prefill_workspace_bytes(const gdr_dims *dims, int32_t n_seqs, int64_t
  * state-sized product keeps ~2^-16 relative precision (bf16 hi/lo operand
  * splits); the chunk-sized products with the factors (the correction D, the
  * intra-chunk output part and X D~) take fp16 operands with fp32
- * accumulation.  Their operands must stay inside the fp16 range (|x| < 65504):
- * with L2-normalised q and k this holds while |v| and the state entries do.
+ * accumulation.  Their data-scaled operands (V - e^G K S and the correction D)
+ * must stay inside the fp16 range: below 65504, and with an RMS above ~1e-4, or
+ * the fp16 subnormals cost accuracy (at an RMS of 1.5e-5 the state error nears
+ * 1e-3).  With L2-normalised q and k these operands scale with v and the state.
  */
 gdr_status gdr_prefill_chunked(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens,
                                int64_t t_total, const void *q, const void *k, const void *v,

@@ -146,20 +146,25 @@ def test_split_prefill_over_two_sequences(lens):
     check(w)
 
 
-def test_large_values_inside_the_fp16_range():
-    """v and the initial state scaled by 2^12 (exact in bf16 and fp32): the
-    tensor-core path's fp16 operands (R, D~ up to ~2e4 here, below the fp16
-    maximum 65504) keep the same relative accuracy, and the result is 2^12 times
-    the unscaled one up to rounding."""
+@pytest.mark.parametrize("e", [12, -10])
+def test_scaled_values_inside_the_fp16_range(e):
+    """v and the initial state scaled by 2^e (exact in bf16 and fp32).  The
+    tensor-core path's fp16 operands R and D~ scale with them: at 2^12 they reach
+    ~2e4, below the fp16 maximum 65504; at 2^-10 the values' RMS is ~1e-3, the
+    low end of the per-head output RMS the Qwen3.5 NPU model card reports, and
+    stays in the fp16 normal range (>= 6.1e-5) but for a few small entries.
+    The result keeps its relative accuracy and is 2^e times the unscaled one up
+    to rounding.  (Far smaller values, RMS below ~1e-5, would fall into the fp16
+    subnormals and lose accuracy.)"""
     import dataclasses
     from gated_deltanet_scan_gb300 import synth as sy
     w = synth.make_workload("scaled", [700], 16, 32, 128, 64, "bf16", seed=11, state_std=0.02)
-    f = np.float32(4096.0)
+    f = np.float32(2.0 ** e)
     v = w.v * f
-    ws = dataclasses.replace(w, name="scaled_x4096", v=v, v_bits=sy.bf16_bits(v), state0=w.state0 * f)
+    ws = dataclasses.replace(w, name=f"scaled_2^{e}", v=v, v_bits=sy.bf16_bits(v), state0=w.state0 * f)
     assert np.array_equal(sy.bf16_values(ws.v_bits), v)  # the scaling is exact
-    eo, es = check(ws)
+    check(ws)
     o1, s1 = run_prefill(w)
     o2, s2 = run_prefill(ws)
-    assert gu.o_error(o2 / 4096.0, o1) < 1e-3
-    assert gu.state_error(s2 / 4096.0, s1) < 1e-4
+    assert gu.o_error(o2 / float(f), o1) < 2e-3
+    assert gu.state_error(s2 / float(f), s1) < 2e-4
