@@ -154,7 +154,7 @@ def test_scaled_values_inside_the_fp16_range(e):
     low end of the per-head output RMS the Qwen3.5 NPU model card reports, and
     stays in the fp16 normal range (>= 6.1e-5) but for a few small entries.
     The result keeps its relative accuracy and is 2^e times the unscaled one up
-    to rounding.  (Far smaller values, RMS below ~1e-5, would fall into the fp16
+    to rounding.  (Far smaller values, RMS below ~1e-5, fall into the fp16
     subnormals and lose accuracy.)"""
     import dataclasses
     from gated_deltanet_scan_gb300 import synth as sy
