@@ -462,6 +462,9 @@ def run_ours(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
+        "precision": "prefill tensor-core operands: bf16 hi/lo splits for the state products, fp16 for the "
+                     "products with the chunk factors; fp32 accumulation, state and outputs; decode and "
+                     "verify in fp32 on CUDA cores",
         "data": "synthetic (seeded SplitMix64; Qwen3.5-9B linear-attention shapes)",
         "config": {
             "workload": "gated delta rule, Qwen3.5-9B layer: prefill B=1 T=16384 + 16-token verify "
