@@ -15,16 +15,13 @@
 // log-space masking), so strong decays cannot overflow.  Tail rows past the
 // end of a sequence are padding (g = 0, beta = 0, k = q = v = 0).
 //
-// Mapping.  A block owns (sequence, V head, 32 state columns).  Warp p owns 8
-// state rows (SPLIT = d/8 warps), lane j one column; the rows sit in registers
-// for the whole sequence.  K and Q tiles are staged in shared memory and read
-// as warp-wide broadcasts, so S^T k needs no shuffles: only the SPLIT partial
-// sums of K S and Q S go through shared memory once per chunk, and each warp
-// adds up the partials of one or two of the 2C (K S or Q S, token) rows for
-// all.  Every warp holds the chunk's D column, so warp p stores the outputs and
-// corrections of the tokens t = p mod SPLIT.  The work of a 16-token chunk is
-// short and latency-bound: eight rows per warp (rather than sixteen) halves
-// each warp's dependent chains and doubles the warps that hide them.
+// Mapping.  A block owns (sequence, V head, 32 state columns).  Warp p owns
+// d/SPLIT state rows, lane j one column; the rows sit in registers for the
+// whole sequence.  K and Q tiles are staged in shared memory and read as
+// warp-wide broadcasts, so S^T k needs no shuffles: only the SPLIT partial sums
+// of K S and Q S go through shared memory once per chunk (K S, then Q S, in one
+// buffer).  Every warp holds the chunk's D column, so warp p stores the outputs
+// and corrections of the tokens t = p mod SPLIT.
 #include "gdr_common.cuh"
 #include "gdr_internal.h"
 
@@ -36,10 +33,8 @@ constexpr int BV = 32;
 
 template <int D>
 struct CcShape {
-    static constexpr int SPLIT = D / 8;    // warps per block (row groups of 8 rows)
+    static constexpr int SPLIT = D / 16;  // warps per block (row groups of 16 rows)
     static constexpr int RPT = D / SPLIT;  // rows per thread
-    // dynamic shared memory: the SPLIT partials of K S and Q S, then their sums
-    static constexpr size_t DYN_BYTES = (size_t)(2 * SPLIT + 2) * C * BV * sizeof(float);
 };
 
 template <int D>
@@ -55,9 +50,7 @@ __global__ void __launch_bounds__(32 * CcShape<D>::SPLIT) chunk_cc_kernel(Args a
     __shared__ float sN[C][C + 1];  // strictly lower part of N, later T = (I+N)^-1
     __shared__ float sP[C][C + 1];
     __shared__ float sT[C][C + 1];
-    extern __shared__ float dyn[];
-    float *red = dyn;                        // [2][SPLIT][C][BV]: partials of K S, then of Q S
-    float *sums = dyn + 2 * SPLIT * C * BV;  // [2 C][BV]: K S rows, then Q S rows
+    __shared__ float red[SPLIT][C][BV];
 
     const int ncb = D / BV;
     const int cb = blockIdx.x % ncb;
@@ -148,33 +141,25 @@ __global__ void __launch_bounds__(32 * CcShape<D>::SPLIT) chunk_cc_kernel(Args a
         __syncthreads();
 
         // Gram products for the chunk: N (strict lower, beta and decay applied), P (lower).
-        // Two adjacent lanes share one (t, j): each takes half of the d products.
-        for (int e2 = threadIdx.x; e2 < 2 * C * C; e2 += NT) {
-            const int e = e2 >> 1, half = e2 & 1;
+        for (int e = threadIdx.x; e < C * C; e += NT) {
             const int t = e / C, j = e - t * C;
-            float dk = 0.f, dq = 0.f;
+            float nk = 0.f, pq = 0.f;
             if (j <= t) {
+                float dk = 0.f, dq = 0.f;
 #pragma unroll 8
-                for (int i = half * (D / 2); i < (half + 1) * (D / 2); i += 4) {
+                for (int i = 0; i < D; i += 4) {
                     const float4 kt = *reinterpret_cast<const float4 *>(&sK[t][i]);
                     const float4 kj = *reinterpret_cast<const float4 *>(&sK[j][i]);
                     const float4 qt = *reinterpret_cast<const float4 *>(&sQ[t][i]);
                     dk = fmaf(kt.x, kj.x, fmaf(kt.y, kj.y, fmaf(kt.z, kj.z, fmaf(kt.w, kj.w, dk))));
                     dq = fmaf(qt.x, kj.x, fmaf(qt.y, kj.y, fmaf(qt.z, kj.z, fmaf(qt.w, kj.w, dq))));
                 }
+                const float decay = __expf(sG[t] - sG[j]);  // exponent <= 0 on this triangle
+                pq = decay * dq;
+                if (j < t) nk = sB[t] * decay * dk;
             }
-            dk += __shfl_xor_sync(0xffffffffu, dk, 1);
-            dq += __shfl_xor_sync(0xffffffffu, dq, 1);
-            if (half == 0) {
-                float nk = 0.f, pq = 0.f;
-                if (j <= t) {
-                    const float decay = __expf(sG[t] - sG[j]);  // exponent <= 0 on this triangle
-                    pq = decay * dq;
-                    if (j < t) nk = sB[t] * decay * dk;
-                }
-                sN[t][j] = nk;
-                sP[t][j] = pq;
-            }
+            sN[t][j] = nk;
+            sP[t][j] = pq;
         }
         __syncthreads();
 
@@ -211,26 +196,27 @@ __global__ void __launch_bounds__(32 * CcShape<D>::SPLIT) chunk_cc_kernel(Args a
             ks[t] = x;
             qs[t] = y;
         }
-        // sum the SPLIT partials: warp p adds up rows q = p, p + SPLIT, ... of the
-        // 2C rows (K S for tokens 0..C-1, then Q S) for every warp
+        // sum the SPLIT partials: K S first, then Q S through the same buffer
+#pragma unroll
+        for (int t = 0; t < C; ++t) red[p][t][lane] = ks[t];
+        __syncthreads();
 #pragma unroll
         for (int t = 0; t < C; ++t) {
-            red[(p * C + t) * BV + lane] = ks[t];
-            red[((SPLIT + p) * C + t) * BV + lane] = qs[t];
-        }
-        __syncthreads();
-        for (int q = p; q < 2 * C; q += SPLIT) {
-            const int which = q / C, t = q - which * C;
             float x = 0.f;
 #pragma unroll
-            for (int w = 0; w < SPLIT; ++w) x += red[((which * SPLIT + w) * C + t) * BV + lane];
-            sums[q * BV + lane] = x;
+            for (int w = 0; w < SPLIT; ++w) x += red[w][t][lane];
+            ks[t] = x;
         }
         __syncthreads();
 #pragma unroll
+        for (int t = 0; t < C; ++t) red[p][t][lane] = qs[t];
+        __syncthreads();
+#pragma unroll
         for (int t = 0; t < C; ++t) {
-            ks[t] = sums[t * BV + lane];
-            qs[t] = sums[(C + t) * BV + lane];
+            float y = 0.f;
+#pragma unroll
+            for (int w = 0; w < SPLIT; ++w) y += red[w][t][lane];
+            qs[t] = y;
         }
 
         // R = diag(beta)(V - diag(e^G) K S);  D = T R;  O = scale (e^G Q S + P D).
@@ -290,31 +276,16 @@ __global__ void __launch_bounds__(32 * CcShape<D>::SPLIT) chunk_cc_kernel(Args a
 
 }  // namespace
 
-template <int D>
-cudaError_t launch_cc(const Args &a, unsigned blocks, cudaStream_t s) {
-    static int configured_device = -1;  // the dynamic shared memory size is set once per device
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (configured_device != dev) {
-        e = cudaFuncSetAttribute(chunk_cc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)CcShape<D>::DYN_BYTES);
-        if (e != cudaSuccess) return e;
-        configured_device = dev;
-    }
-    chunk_cc_kernel<D><<<blocks, 32 * CcShape<D>::SPLIT, CcShape<D>::DYN_BYTES, s>>>(a);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_chunk_cc(const Args &a, cudaStream_t s) {
     if (a.n_seqs == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)a.n_seqs * (unsigned)a.h_v * (unsigned)(a.d / BV);
     switch (a.d) {
-        case 32: return launch_cc<32>(a, blocks, s);
-        case 64: return launch_cc<64>(a, blocks, s);
-        case 128: return launch_cc<128>(a, blocks, s);
+        case 32: chunk_cc_kernel<32><<<blocks, 32 * CcShape<32>::SPLIT, 0, s>>>(a); break;
+        case 64: chunk_cc_kernel<64><<<blocks, 32 * CcShape<64>::SPLIT, 0, s>>>(a); break;
+        case 128: chunk_cc_kernel<128><<<blocks, 32 * CcShape<128>::SPLIT, 0, s>>>(a); break;
         default: return cudaErrorInvalidValue;
     }
+    return cudaGetLastError();
 }
 
 }  // namespace gdr
