@@ -34,7 +34,7 @@
 // hi/lo splits of both sides needed two (a tcgen05 MMA costs the same in fp16
 // as in bf16).  Their fp16 B tiles keep the N = 64 column map with the second
 // half zero.  The rounding of Tw and PTw dominates the error this adds: on
-// Qwen3.5-9B shapes about 1e-2 of the output RMS (max-abs) and 3e-4 of the
+// Qwen3.5-9B shapes up to ~1e-2 of the output RMS (max-abs) and ~2.5e-4 of the
 // state (relative Frobenius), not growing with the number of chunks, since
 // each chunk's rounding enters the state once and decays with it.  The fp16
 // range bounds the supported inputs: R and D~ scale with v and the state (the
