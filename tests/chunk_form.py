@@ -149,8 +149,47 @@ def commit_from_deltas(k, g, D, S0, a):
     return np.exp(G[-1]) * S0 + np.asarray(k[:a], np.float64).T @ (w[:, None] * np.asarray(D[:a], np.float64))
 
 
-def chunk_form_lookahead(q, k, v, g, beta, S0, C):
-    """Same contract as ``chunk_form_pages``, in the tcgen05 chunk scan's grouping."""
+def _f32(x):
+    return np.asarray(x, np.float64).astype(np.float32)
+
+
+def round_bf16(x):
+    """fp64 -> fp32 -> bf16 (round to nearest even), back to fp64."""
+    u = _f32(x).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000).astype(np.uint32)
+    return r.view(np.float32).astype(np.float64)
+
+
+def round_f16(x):
+    """fp64 -> fp32 -> fp16 (round to nearest even, IEEE subnormals), back to fp64."""
+    with np.errstate(over="ignore", under="ignore"):
+        return _f32(x).astype(np.float16).astype(np.float64)
+
+
+def hilo_bf16(x):
+    """hi = the fp32 value with its low 16 bits dropped, lo = bf16(x - hi); returns hi + lo."""
+    f = _f32(x)
+    hi = (f.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32).astype(np.float64)
+    return hi + round_bf16(f.astype(np.float64) - hi)
+
+
+# Operand roundings of the chunk scan's products: the operands the kernel
+# rounds to fp16 (Tw, PTw, X, R and D~ for MMA_X) and the ones it splits into
+# bf16 hi/lo (S' for MMA1', D~ for MMA3).  "bf16_single" puts a single bf16
+# term where the kernel has fp16, for comparison.
+OPERANDS = {
+    "kernel": (round_f16, hilo_bf16),
+    "bf16_single": (round_bf16, hilo_bf16),
+}
+
+
+def chunk_form_lookahead(q, k, v, g, beta, S0, C, operands=None):
+    """Same contract as ``chunk_form_pages``, in the tcgen05 chunk scan's grouping.
+
+    ``operands`` names an entry of OPERANDS to round the products' operands the
+    way the kernel does (the products themselves stay in fp64); None keeps
+    every operand exact."""
+    rnd, split = OPERANDS[operands] if operands else ((lambda x: x), (lambda x: x))
     T_len = q.shape[0]
     n = (T_len + C - 1) // C
     chunks = []
@@ -170,18 +209,18 @@ def chunk_form_lookahead(q, k, v, g, beta, S0, C):
     S = np.array(S0, dtype=np.float64)
     O = np.zeros((T_len, v.shape[1]))
     dk = q.shape[1]
-    A = chunks[0][2] @ S  # [K S; Q S] of chunk 0
+    A = chunks[0][2] @ split(S)  # [K S; Q S] of chunk 0
     for c, (c0, L, KQ, K, V, G, Tw, PTw) in enumerate(chunks):
         KS, QS = A[:C], A[C:]
         eG = np.exp(G)[:, None]
-        R = V - eG * KS
-        Dt = Tw @ R
-        O[c0:c0 + L] = (eG * QS + PTw @ R)[:L]
+        R = rnd(V - eG * KS)
+        Dt = rnd(Tw) @ R
+        O[c0:c0 + L] = (eG * QS + rnd(PTw) @ R)[:L]
         eGC = np.exp(G[-1])
         if c + 1 < n:
             KQn = chunks[c + 1][2]
             X = KQn @ K.T
-            A = KQn @ (eGC * S) + X @ Dt
-        S = eGC * S + K.T @ Dt
+            A = KQn @ split(eGC * S) + rnd(X) @ rnd(Dt)
+        S = eGC * S + K.T @ split(Dt)
     assert S.shape == (dk, v.shape[1])
     return O, S

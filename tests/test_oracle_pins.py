@@ -379,3 +379,35 @@ def test_verify_commit_from_deltas_equals_sequential_prefix(n_tok):
         S_ref = S0 if a == 0 else _single(q[:a], k[:a], v[:a], g[:a], beta[:a], S0)[1]
         S_c = commit_from_deltas(k, g, D, S0, a)
         assert np.linalg.norm(S_c - S_ref) <= 1e-12 * np.linalg.norm(S_ref)
+
+
+@pytest.mark.parametrize("g_fixed", [None, -6.72])
+def test_kernel_operand_rounding_stays_inside_the_tolerances(g_fixed):
+    """The tensor-core scan's operand roundings (fp16 Tw, PTw, X, R and D~ in
+    MMA2 and MMA_X; bf16 hi/lo S' and D~ in MMA1' and MMA3), applied to the
+    lookahead grouping with exact fp64 products, against the sequential oracle on
+    one Qwen3.5-9B-sized head (d = 128, 16 chunks of 64, bf16 q/k/v values, state
+    ~ N(0, 0.02)): the error budget of that design is inside the stated
+    tolerances (2e-2 max-abs / RMS, 1e-3 relative Frobenius) with a margin of
+    two, and a single bf16 term in place of fp16 is markedly worse.  (The
+    kernel's fp32 accumulation is not modelled.)"""
+    from tests.chunk_form import round_bf16
+    r = _rng(29)
+    T, d, C = 1024, 128, 64
+    q = round_bf16(_unit(r.standard_normal((T, d))))
+    k = round_bf16(_unit(r.standard_normal((T, d))))
+    v = round_bf16(r.standard_normal((T, d)))
+    g = np.full(T, g_fixed) if g_fixed is not None else r.uniform(-8.0, -0.01, T)
+    beta = 1.0 / (1.0 + np.exp(-r.standard_normal(T)))
+    S0 = 0.02 * r.standard_normal((d, d))
+    o, S = _single(q, k, v, g, beta, S0)
+    rms = np.sqrt(np.mean(o * o))
+    err = {}
+    for name in ("kernel", "bf16_single"):
+        oc, Sc = chunk_form_lookahead(q, k, v, g, beta, S0, C, operands=name)
+        err[name] = (np.max(np.abs(oc - o)) / rms, np.linalg.norm(Sc - S) / np.linalg.norm(S))
+    eo, es = err["kernel"]
+    assert eo <= 1e-2 and es <= 5e-4, err
+    # fp16 keeps 3 more significand bits; under strong decay part of the fp16
+    # error is the underflow of the most decayed Tw rows, which bf16 keeps
+    assert err["bf16_single"][0] >= 4 * eo and err["bf16_single"][1] >= 2 * es, err
