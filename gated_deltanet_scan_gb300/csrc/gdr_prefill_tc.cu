@@ -189,14 +189,15 @@ __device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool 
 }
 
 // Bounded wait that also gives up as soon as any thread of the CTA has raised
-// the abort flag.  Returns false on either.  Most phases have completed by the
-// time they are awaited: a non-blocking test finds those sooner than a
-// blocking try_wait does.
+// the abort flag.  Returns false on either.  It spins on the non-blocking test:
+// a phase that has completed is found sooner than by a blocking try_wait, and a
+// thread parked by try_wait wakes later after the phase completes than a
+// spinning one notices it (the chain's waits are on the chunk-to-chunk path).
 __device__ bool wait_or_abort(const Ctx &x, uint32_t bar, uint32_t parity) {
     if (mbar_test_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_test_wait(bar, parity)) return true;
         if (*x.abort_flag) return false;
         if (clock64() - t0 > kWaitLimit) {
             *x.abort_flag = 1;
