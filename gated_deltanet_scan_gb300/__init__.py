@@ -161,13 +161,22 @@ def gdr_prefill_chunked(q, k, v, g, beta, state, o, cu_seqlens, *, chunk: int = 
     state [n, H_v, d_k, d_v] fp32 (in/out); o [T, H_v, d_v]; cu_seqlens int32 [n+1]
     on the device.  ``t_total`` defaults to q.shape[0].  ``workspace`` is a
     device tensor of at least gdr_prefill_workspace_bytes(...) bytes; when it is
-    None, one is taken from torch's caching allocator for this call."""
+    None, one is taken from torch's caching allocator for this call, on the
+    stream the call runs on (``stream``), so that torch hands its memory to no
+    other work before the call's kernels on that stream are done."""
+    torch = _torch()
     dims = make_dims(q, v, o, chunk, scale)
     n = cu_seqlens.shape[0] - 1
     T = q.shape[0] if t_total is None else int(t_total)
     need = int(lib().gdr_prefill_workspace_bytes(ctypes.byref(dims), n, T))
     if workspace is None and need > 0:
-        workspace = _torch().empty(need, dtype=_torch().uint8, device=q.device)
+        # allocated while the call's stream is current: the caching allocator ties
+        # the block to that stream, whatever stream is current in the caller
+        s = stream if stream is not None else torch.cuda.current_stream(q.device)
+        if isinstance(s, int):
+            s = torch.cuda.ExternalStream(s, device=q.device)
+        with torch.cuda.stream(s):
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = _ptr(workspace) if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = lib().gdr_prefill_chunked(

@@ -12,20 +12,17 @@ namespace gdr {
 namespace {
 
 // Scratch of gdr_prefill_chunked_static: one fixed device array, never allocated
-// at run time.  Its device address is resolved once per device.
+// at run time.  Its device address (a host-side name of it is not one) is
+// looked up in the current device's context on every call: nothing is cached, so
+// a reset device or a new context, or concurrent first calls from several host
+// threads, need no care; the lookup costs little next to the launches.
 constexpr size_t kStaticWorkspaceBytes = size_t(64) << 20;
 static __device__ __align__(256) uint8_t g_static_workspace[kStaticWorkspaceBytes];
 
 void *static_workspace() {
-    static void *cached[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!cached[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess) return nullptr;
-        cached[dev] = p;
-    }
-    return cached[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess) return nullptr;
+    return p;
 }
 
 __global__ void copy_f32_kernel(const float4 *__restrict__ src, float4 *__restrict__ dst, size_t n4) {

@@ -159,13 +159,16 @@ gdr_status gdr_prefill_chunked(const gdr_dims *dims, int32_t n_seqs, const int32
 /*
  * gdr_prefill_chunked without a caller workspace and without any allocation:
  * the scratch is one fixed device array inside the library (its size is
- * gdr_prefill_static_workspace_capacity(), 64 MiB), resolved once per device.
- * Problems whose gdr_prefill_workspace_bytes() exceed it return
- * GDR_ERR_UNSUPPORTED before anything is launched (about 100 chunk positions
- * of 32 V heads: e.g. up to ~6.5K tokens of Qwen3.5-9B heads).  All calls on a
- * device share that array, so calls on different streams must not overlap
- * (order them on one stream, or synchronise); everything else, arguments
- * and results, is as in gdr_prefill_chunked.
+ * gdr_prefill_static_workspace_capacity(), 64 MiB), whose device address is
+ * looked up on every call.  Problems whose gdr_prefill_workspace_bytes()
+ * exceed it return GDR_ERR_UNSUPPORTED before anything is launched.  With
+ * Qwen3.5-9B heads (16 QK, 32 V) one chunk position takes 794,624 bytes, so
+ * the array holds 84 positions: one sequence of up to 5,312 tokens, and one
+ * position less per further sequence (two sequences: 5,248 tokens in all;
+ * eight: 4,864).  All calls on a device share that array, so calls on
+ * different streams must not overlap (order them on one stream, or
+ * synchronise); everything else, arguments and results, is as in
+ * gdr_prefill_chunked.
  */
 gdr_status gdr_prefill_chunked_static(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens,
                                       int64_t t_total, const void *q, const void *k, const void *v,
@@ -200,11 +203,17 @@ gdr_status gdr_decode_step(const gdr_dims *dims, int32_t batch, const void *q, c
  * prefill of another: queued right after gdr_prefill_chunked, it starts beside
  * the prefill's last chunk-scan launch (which occupies 4 SMs per V head).
  *
- * Contract: none of the step's inputs or states may be written by the kernel
- * immediately before it on `stream` (work queued earlier has completed before
- * that kernel started and is visible).  Arguments, results and errors are as in
- * gdr_decode_step; later work on `stream` is ordered after the step as usual.
- * Callers that cannot guarantee the contract use gdr_decode_step.
+ * Contract: the step starts without waiting for the kernel immediately before
+ * it on `stream`, nor for any kernel that was still running when that kernel
+ * started (a kernel launched as a programmatic dependent starts before its own
+ * predecessor has finished: gdr_prefill_chunked's chunk scan is one, of the
+ * prefill's factor launch).  None of those kernels may write the step's q, k,
+ * v, g, beta, state or o, or read its state or o.  Work that had completed
+ * before all of them started is visible to the step.  After gdr_prefill_chunked
+ * this holds whenever the decode step's tensors do not overlap the prefill's.
+ * Arguments, results and errors are as in gdr_decode_step; later work on
+ * `stream` is ordered after the step as usual.  Callers that cannot guarantee
+ * the contract use gdr_decode_step.
  */
 gdr_status gdr_decode_step_overlapped(const gdr_dims *dims, int32_t batch, const void *q, const void *k,
                                       const void *v, const float *g, const float *beta, float *state,

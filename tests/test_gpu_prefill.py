@@ -168,3 +168,27 @@ def test_scaled_values_inside_the_fp16_range(e):
     o2, s2 = run_prefill(ws)
     assert gu.o_error(o2 / float(f), o1) < 2e-3
     assert gu.state_error(s2 / float(f), s1) < 2e-4
+
+
+def test_side_stream_without_workspace():
+    """The call runs on a side stream while another stream is current, with the
+    workspace taken from torch's allocator by the binding: the block belongs to
+    the side stream, so the current stream's allocations right after the call
+    (written at once) cannot take it while the prefill still uses it."""
+    import gated_deltanet_scan_gb300 as gdr
+    torch = gu.require_gpu()
+    w = synth.make_workload("side", [2000, 700], 16, 32, 128, 64, "bf16", seed=31, state_std=0.02)
+    x = gu.dev_inputs(w)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    o = gu.out_like(x["v"], "f32")
+    gdr.gdr_prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state"], o, x["cu_seqlens"],
+                            stream=side)
+    need = gdr.gdr_prefill_workspace_bytes(x["q"], x["v"], o, 2, o.shape[0])
+    junk = [torch.full((need // 4,), float("nan"), device="cuda") for _ in range(3)]
+    torch.cuda.synchronize()
+    del junk
+    assert gdr.gdr_device_error() == 0
+    o_ref, s_ref = oracle.run_workload(w)
+    gu.check_outputs(gu.to_np(o), o_ref)
+    gu.check_state(gu.to_np(x["state"]), s_ref)

@@ -20,11 +20,17 @@ def test_static_entry_rejects_oversize_before_launch():
     assert cap == 64 << 20
     d = gdr.gdr_dims(h_qk=16, h_v=32, d_k=128, d_v=128, chunk=64, in_dtype=gdr.GDR_BF16,
                      out_dtype=gdr.GDR_F32, scale=1.0)
-    big_t = 1 << 20
-    assert L.gdr_prefill_workspace_bytes(ctypes.byref(d), 1, big_t) > cap
     A = 0x100000  # aligned stand-in addresses: nothing is dereferenced on this path
-    st = L.gdr_prefill_chunked_static(ctypes.byref(d), 1, A, big_t, A, A, A, A, A, A, A, None)
-    assert st == gdr.GDR_ERR_UNSUPPORTED
+    # one chunk position of 32 V heads and 16 QK heads takes 32 * 16640 + 16 * 16384
+    # bytes: the 64 MiB array holds 84 positions, i.e. one sequence of up to 83
+    # chunks (5312 tokens; one position is the per-sequence spare)
+    assert L.gdr_prefill_workspace_bytes(ctypes.byref(d), 1, 5312) <= cap
+    assert L.gdr_prefill_workspace_bytes(ctypes.byref(d), 1, 5313) > cap
+    assert L.gdr_prefill_workspace_bytes(ctypes.byref(d), 2, 5248) <= cap
+    assert L.gdr_prefill_workspace_bytes(ctypes.byref(d), 2, 5249) > cap
+    for n, t in ((1, 5313), (2, 5249), (1, 1 << 20)):
+        st = L.gdr_prefill_chunked_static(ctypes.byref(d), n, A, t, A, A, A, A, A, A, A, None)
+        assert st == gdr.GDR_ERR_UNSUPPORTED, (n, t, st)
 
 
 @pytest.mark.gpu
@@ -40,4 +46,21 @@ def test_static_entry_matches_workspace_entry_twice():
         torch.cuda.synchronize()
         assert np.array_equal(gu.to_np(o_ws), gu.to_np(o_st))
         assert np.array_equal(gu.to_np(s_ws), gu.to_np(s_st))
+    assert gdr.gdr_device_error(device=x["q"].device) == 0
+
+
+@pytest.mark.gpu
+def test_static_entry_at_its_largest_single_sequence():
+    """One Qwen3.5-9B sequence of 5312 tokens fills the fixed array to its last
+    chunk position; the result equals the workspace entry's bit for bit."""
+    torch = gu.require_gpu()
+    w = synth.make_workload("no_alloc_max", [5312], 16, 32, 128, 64, "bf16", seed=72, state_std=0.02)
+    x = gu.dev_inputs(w)
+    s_ws, s_st = x["state"].clone(), x["state"].clone()
+    o_ws, o_st = gu.out_like(x["v"], "f32"), gu.out_like(x["v"], "f32")
+    gdr.gdr_prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], s_ws, o_ws, x["cu_seqlens"])
+    gdr.gdr_prefill_chunked_static(x["q"], x["k"], x["v"], x["g"], x["beta"], s_st, o_st, x["cu_seqlens"])
+    torch.cuda.synchronize()
+    assert np.array_equal(gu.to_np(o_ws), gu.to_np(o_st))
+    assert np.array_equal(gu.to_np(s_ws), gu.to_np(s_st))
     assert gdr.gdr_device_error(device=x["q"].device) == 0
