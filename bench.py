@@ -341,7 +341,7 @@ def run_ours(args):
 
         l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
 
-        def time_prefill(w, reps=10):
+        def time_prefill(w, reps=10, segments=None):
             """Median of `reps` prefills, each on the next of several copies of the
             inputs, outputs, states and workspace whose total is over twice the L2
             size (so no call finds its operands in L2 from the call before), launched
@@ -357,8 +357,9 @@ def run_ours(args):
                 x["st"] = torch.zeros((n, H_V, D, D), dtype=torch.float32, device=dev)
                 x["cu"] = torch.from_numpy(w.cu_seqlens.astype(np.int32)).to(dev)
                 x["o"] = torch.empty((tokens, H_V, D), dtype=torch.float32, device=dev)
-                x["ws"] = torch.empty(gdr.gdr_prefill_workspace_bytes(x["q"], x["v"], x["o"], n, tokens),
-                                      dtype=torch.uint8, device=dev)
+                need = (gdr.gdr_prefill_workspace_bytes(x["q"], x["v"], x["o"], n, tokens) if segments is None else
+                        gdr.gdr_prefill_segmented_workspace_bytes(x["q"], x["v"], x["o"], n, tokens, segments))
+                x["ws"] = torch.empty(need, dtype=torch.uint8, device=dev)
                 return x
 
             sets = [one_set()]
@@ -367,8 +368,12 @@ def run_ours(args):
                 sets.append(one_set())
 
             def call(x):
-                gdr.gdr_prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], x["st"], x["o"], x["cu"],
-                                        chunk=64, workspace=x["ws"], stream=stream)
+                if segments is None:
+                    gdr.gdr_prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], x["st"], x["o"], x["cu"],
+                                            chunk=64, workspace=x["ws"], stream=stream)
+                else:
+                    gdr.gdr_prefill_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"], x["st"], x["o"], x["cu"],
+                                              segments, chunk=64, workspace=x["ws"], stream=stream)
 
             def timed(launch):
                 ts = []
@@ -392,8 +397,9 @@ def run_ours(args):
                 graphs.append(gr)
             ms_graph = timed(lambda i: graphs[i].replay())
             del graphs
-            alg = tokens * PREFILL_BYTES_PER_TOKEN + 2 * n * STATE_BYTES
-            alg_survey = tokens * SURVEY_BYTES_PER_TOKEN + 2 * n * STATE_BYTES
+            hv = w.h_v / H_V  # byte counts below are for 32 V heads and 16 QK heads
+            alg = hv * (tokens * PREFILL_BYTES_PER_TOKEN + 2 * n * STATE_BYTES)
+            alg_survey = hv * (tokens * SURVEY_BYTES_PER_TOKEN + 2 * n * STATE_BYTES)
             hbm = load_peaks()[0]["hbm_gbs"]
             gbs = alg / (ms * 1e-3) / 1e9
             return {"ms": ms, "ms_graph": ms_graph, "tokens": tokens, "tokens_per_s": tokens / (ms * 1e-3),
@@ -405,6 +411,16 @@ def run_ours(args):
 
         other["prefill_T1024"] = time_prefill(synth.prefill_9b(1024))
         other["packed_prefill_8_seqs"] = time_prefill(synth.varlen_verify())
+        # few heads, one long sequence (e.g. a layer split 8 ways by heads: 2 QK, 4 V):
+        # one chain per head, against the two-level scan with the library's segment count
+        few = synth.make_workload("few_heads_T16384", [16384], 2, 4, D, 64, "bf16", seed=105, state_std=0.02)
+        q_, v_, o_ = (torch.empty((1, nh, D), dtype=dt, device=dev)
+                      for nh, dt in ((2, torch.bfloat16), (4, torch.bfloat16), (4, torch.float32)))
+        P = gdr.gdr_prefill_segments_hint(q_, v_, o_, 1, 16384)
+        plain = time_prefill(few)
+        seg = time_prefill(few, segments=P)
+        other["few_heads_T16384_hqk2_hv4"] = {"one_chain": plain, "segmented": dict(seg, segments=P),
+                                              "speedup": plain["ms"] / seg["ms"]}
 
     # End to end through the same public API: every step uploads its inputs from
     # pinned host memory and reads its outputs back.  Like a serving pipeline, the

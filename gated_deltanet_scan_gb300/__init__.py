@@ -16,6 +16,7 @@ from typing import Optional
 __all__ = [
     "GdrError", "gdr_dims", "lib", "library_path",
     "gdr_prefill_chunked", "gdr_prefill_workspace_bytes", "gdr_prefill_chunked_static",
+    "gdr_prefill_segmented", "gdr_prefill_segmented_workspace_bytes", "gdr_prefill_segments_hint",
     "gdr_decode_step", "gdr_decode_step_overlapped", "gdr_verify_block", "gdr_verify_commit",
     "gdr_state_snapshot", "gdr_state_restore", "gdr_device_error", "gdr_selftest_wait_timeout", "gdr_status_string",
     "GDR_F32", "GDR_BF16",
@@ -59,6 +60,11 @@ _SIGS = {
     "gdr_prefill_chunked_static": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, ctypes.c_int64,
                                     _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "gdr_prefill_static_workspace_capacity": ([], ctypes.c_size_t),
+    "gdr_prefill_segmented": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, ctypes.c_int64,
+                               _P, _P, _P, _P, _P, _P, _P, ctypes.c_int32, _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "gdr_prefill_segmented_workspace_bytes": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, ctypes.c_int64,
+                                               ctypes.c_int32], ctypes.c_size_t),
+    "gdr_prefill_segments_hint": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, ctypes.c_int64], ctypes.c_int32),
     "gdr_decode_step": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P],
                         ctypes.c_int),
     "gdr_decode_step_overlapped": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P],
@@ -196,6 +202,46 @@ def gdr_prefill_chunked_static(q, k, v, g, beta, state, o, cu_seqlens, *, chunk:
         ctypes.byref(dims), n, _ptr(cu_seqlens), T, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
         _ptr(beta), _ptr(state), _ptr(o), _stream_handle(stream, q.device))
     _check(st, "gdr_prefill_chunked_static")
+
+
+def gdr_prefill_segments_hint(q, v, o, n_seqs: int, t_total: int, *, chunk: int = 64, scale: float = 1.0) -> int:
+    """Segments the two-level prefill would use on the current device (1: none)."""
+    dims = make_dims(q, v, o, chunk, scale)
+    return int(lib().gdr_prefill_segments_hint(ctypes.byref(dims), int(n_seqs), int(t_total)))
+
+
+def gdr_prefill_segmented_workspace_bytes(q, v, o, n_seqs: int, t_total: int, n_segments: int, *,
+                                          chunk: int = 64, scale: float = 1.0) -> int:
+    dims = make_dims(q, v, o, chunk, scale)
+    return int(lib().gdr_prefill_segmented_workspace_bytes(ctypes.byref(dims), int(n_seqs), int(t_total),
+                                                           int(n_segments)))
+
+
+def gdr_prefill_segmented(q, k, v, g, beta, state, o, cu_seqlens, n_segments: Optional[int] = None, *,
+                          chunk: int = 64, scale: float = 1.0, t_total: Optional[int] = None, workspace=None,
+                          stream=None) -> None:
+    """Two-level (segment-parallel) prefill (see gdr_prefill_segmented in
+    include/gdr.h): arguments as gdr_prefill_chunked; ``n_segments`` defaults to
+    gdr_prefill_segments_hint.  Without ``workspace`` one is taken from torch's
+    allocator on the call's stream."""
+    torch = _torch()
+    dims = make_dims(q, v, o, chunk, scale)
+    n = cu_seqlens.shape[0] - 1
+    T = q.shape[0] if t_total is None else int(t_total)
+    P = int(lib().gdr_prefill_segments_hint(ctypes.byref(dims), n, T)) if n_segments is None else int(n_segments)
+    need = int(lib().gdr_prefill_segmented_workspace_bytes(ctypes.byref(dims), n, T, P))
+    if workspace is None and need > 0:
+        s = stream if stream is not None else torch.cuda.current_stream(q.device)
+        if isinstance(s, int):
+            s = torch.cuda.ExternalStream(s, device=q.device)
+        with torch.cuda.stream(s):
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _ptr(workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().gdr_prefill_segmented(
+        ctypes.byref(dims), n, _ptr(cu_seqlens), T, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+        _ptr(o), P, ws_ptr, ws_bytes, _stream_handle(stream, q.device))
+    _check(st, "gdr_prefill_segmented")
 
 
 def gdr_decode_step(q, k, v, g, beta, state, o, *, scale: float = 1.0, stream=None) -> None:

@@ -115,6 +115,29 @@ int split_chunk(const gdr_dims *d, int32_t n_seqs, int64_t t_total) {
     return (int)m;
 }
 
+int device_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+
+// Segments of the two-level prefill for this problem on the current device.  Its
+// scan launch runs 2P - 1 runs of n_seqs * h_v * 4 CTAs (one SM each); it pays
+// when they all fit on the GPU at once, so the segments' chains walk side by
+// side: P is the largest value up to 8 for which they do and every segment keeps
+// at least 8 chunks, else 1 (one chain per head, the ordinary prefill).
+int segments_hint(const gdr_dims *d, int32_t n_seqs, int64_t t_total) {
+    if (!use_tensor_core_prefill(d) || n_seqs <= 0 || t_total <= 0) return 1;
+    const int sms = device_sms();
+    const int64_t n_ch = (t_total + 63) / 64;
+    const int64_t per_run = (int64_t)n_seqs * d->h_v * 4;
+    int best = 1;
+    for (int P = 2; P <= 8; ++P)
+        if (per_run * (2 * P - 1) <= sms && n_ch >= 8LL * P) best = P;
+    return best;
+}
+
 // The tensor-core prefill on `s`: factors, then the chunk scan (a programmatic
 // dependent of the factor launch), or, split at
 // chunk m (see split_chunk): factors [0, m), scan [0, m), factors [m, n) as a
@@ -225,6 +248,61 @@ gdr_status gdr_prefill_chunked(const gdr_dims *dims, int32_t n_seqs, const int32
 }
 
 size_t gdr_prefill_static_workspace_capacity(void) { return kStaticWorkspaceBytes; }
+
+int32_t gdr_prefill_segments_hint(const gdr_dims *dims, int32_t n_seqs, int64_t t_total) {
+    if (check_dims(dims) != GDR_OK) return 1;
+    return segments_hint(dims, n_seqs, t_total);
+}
+
+size_t gdr_prefill_segmented_workspace_bytes(const gdr_dims *dims, int32_t n_seqs, int64_t t_total,
+                                             int32_t n_segments) {
+    const size_t factor_bytes = gdr_prefill_workspace_bytes(dims, n_seqs, t_total);
+    if (factor_bytes == 0 || n_segments < 1 || n_segments > 8) return factor_bytes;
+    const int64_t n_ch = (t_total + 63) / 64;
+    const int P = (int)(n_segments < n_ch ? n_segments : n_ch);
+    if (P <= 1) return factor_bytes;
+    return segment_layout((int64_t)factor_bytes, n_seqs, dims->h_v, t_total, P).total;
+}
+
+gdr_status gdr_prefill_segmented(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens, int64_t t_total,
+                                 const void *q, const void *k, const void *v, const float *g, const float *beta,
+                                 float *state, void *o, int32_t n_segments, void *workspace, size_t workspace_bytes,
+                                 gdr_stream_t stream) {
+    gdr_status st = check_dims(dims);
+    if (st != GDR_OK) return st;
+    if (n_segments < 1 || n_segments > 8) return GDR_ERR_INVALID_ARG;
+    if (!use_tensor_core_prefill(dims)) return GDR_ERR_UNSUPPORTED;
+    const int64_t n_ch = (t_total + 63) / 64;
+    const int P = (int)(n_segments < n_ch ? n_segments : n_ch);
+    if (P <= 1)  // one segment: the ordinary two-launch prefill
+        return prefill(dims, n_seqs, cu_seqlens, t_total, q, k, v, g, beta, state, o, workspace, workspace_bytes,
+                       stream, false);
+    if (n_seqs < 0 || t_total < 0) return GDR_ERR_INVALID_ARG;
+    if (n_seqs == 0) return t_total == 0 ? GDR_OK : GDR_ERR_INVALID_ARG;
+    if (!cu_seqlens || !aligned16(cu_seqlens) || !tensors_ok(q, k, v, g, beta, state, o)) return GDR_ERR_INVALID_ARG;
+    if (t_total > ((int64_t)1 << 31) - 1) return GDR_ERR_UNSUPPORTED;
+    const size_t need = gdr_prefill_segmented_workspace_bytes(dims, n_seqs, t_total, n_segments);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return GDR_ERR_INVALID_ARG;
+    const SegLayout L = segment_layout((int64_t)gdr_prefill_workspace_bytes(dims, n_seqs, t_total), n_seqs,
+                                       dims->h_v, t_total, P);
+    Args a = make_args(dims);
+    a.n_seqs = n_seqs;
+    a.cu_seqlens = cu_seqlens;
+    a.fixed_len = 0;
+    a.t_total = t_total;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.g = g;
+    a.beta = beta;
+    a.state = state;
+    a.snapshot = nullptr;
+    a.o = o;
+    int32_t *err = device_error_word();
+    if (!err) return GDR_ERR_CUDA;
+    return from_cuda(launch_segmented(a, P, static_cast<uint8_t *>(workspace), L, err,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
 
 gdr_status gdr_prefill_chunked_static(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens,
                                       int64_t t_total, const void *q, const void *k, const void *v,

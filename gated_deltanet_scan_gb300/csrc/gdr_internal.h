@@ -43,7 +43,33 @@ cudaError_t launch_factors(const Args &a, float *ws, int32_t *err, cudaStream_t 
 // griddepcontrol.wait).  Only directly after the factor launch whose slots it
 // reads: the kernel waits for nothing else.
 cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s, bool overlap);
+
+// One run of the chunk scan: chunks [c_lo, c_hi) of every sequence from and into
+// `state` ([n_seqs][h_v][128][128] fp32), outputs to `o` (bf16 when out_bf16),
+// values taken as zero when v_zero.  The tensor-core launch below walks up to
+// kMaxTcRuns runs side by side; every run reads the same factor workspace.
+constexpr int kMaxTcRuns = 16;
+struct TcRun {
+    int c_lo, c_hi;
+    int out_bf16, v_zero;
+    float *state;
+    void *o;
+};
+cudaError_t launch_prefill_tc_runs(const Args &a, const TcRun *runs, int n_runs, const float *ws, cudaStream_t s,
+                                   bool overlap);
 cudaError_t launch_copy_f32(const float *src, float *dst, size_t n, cudaStream_t s);
+
+// Two-level prefill (gdr_segment.cu): byte offsets of its fp32 scratch inside the
+// workspace, after the factor_bytes of the factor slots and X tiles.
+struct SegLayout {
+    size_t phi, b, x, o0, m, total;
+};
+SegLayout segment_layout(int64_t factor_bytes, int n_seqs, int h_v, int64_t t_total, int P);
+// First chunk of segment p of P over n_chunks chunks (p = P gives n_chunks).
+int segment_cut(int64_t n_chunks, int P, int p);
+// Factors, one scan launch over every segment's runs, the combine of the segment
+// starts and the later segments' outputs, all on `s`; `ws` holds L.total bytes.
+cudaError_t launch_segmented(const Args &a, int P, uint8_t *ws, const SegLayout &L, int32_t *err, cudaStream_t s);
 // Verify commit: state = e^{G_a} snapshot + sum_{j<a} e^{G_a - G_j} k_j u_j^T per (sequence, V head).
 cudaError_t launch_commit(const Args &a, int32_t *err, cudaStream_t s);
 

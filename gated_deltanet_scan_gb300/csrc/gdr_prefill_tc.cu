@@ -152,15 +152,17 @@ constexpr uint32_t IDESC_N64 = idesc_bf16_f32(128, 64, 0, 1);   // MMA1': A K-ma
 constexpr uint32_t IDESC16_N64 = idesc_f16_f32(128, 64, 0, 1);  // MMA2, MMA_X
 constexpr uint32_t IDESC_Y = idesc_bf16_f32(128, 64, 1, 1);     // MMA3: A MN-major (Kᵀ), B MN-major
 
+// One run of the scan over chunks [c_lo, c_hi) of every sequence, from and into
+// `state`, writing outputs to `o`; with v_zero the values are taken as zero (the
+// run then carries only its initial state).  A launch walks up to kMaxTcRuns
+// independent runs side by side (the segments of the two-level scan).
 struct TcParams {
-    int h_qk, h_v, out_bf16;
-    int c_lo, c_hi;  // chunks of each sequence to process; the state is read before and written after them
+    int h_qk, h_v, n_seqs, n_runs;
     float scale;
     const int32_t *cu_seqlens;
     const uint8_t *ws;     // factor slots
     const uint8_t *xs;     // X tiles
-    float *state;
-    void *o;
+    TcRun runs[kMaxTcRuns];
 };
 
 struct Ctx {
@@ -247,17 +249,18 @@ __device__ __forceinline__ void store_f16_row16(uint8_t *tile, int row, int j0, 
 }
 
 // One ring stage: K and Q (d_k halves, 128-byte swizzled) and this CTA's V columns.
+// (With zero values the V tile is not loaded: the chain does not read it.)
 __device__ __forceinline__ void issue_kq_loads(const Ctx &x, int kb, int tok, int hq, int h, int cb,
                                                const CUtensorMap *tmK, const CUtensorMap *tmQ,
-                                               const CUtensorMap *tmV) {
+                                               const CUtensorMap *tmV, bool v_zero) {
     const uint32_t bar = x.bar(B_KQ_FULL + kb);
-    mbar_arrive_expect_tx(bar, KQV_TX);
+    mbar_arrive_expect_tx(bar, v_zero ? KQV_TX - V_BYTES : KQV_TX);
     const uint32_t kq = x.sbase + OFF_KQ + kb * KQ_BYTES;
     tma_load_3d(kq, tmK, bar, 0, hq, tok);
     tma_load_3d(kq + 16384, tmK, bar, 64, hq, tok);
     tma_load_3d(kq + 8192, tmQ, bar, 0, hq, tok);
     tma_load_3d(kq + 16384 + 8192, tmQ, bar, 64, hq, tok);
-    tma_load_3d(x.sbase + OFF_V + kb * V_BYTES, tmV, bar, cb * BV, h, tok);
+    if (!v_zero) tma_load_3d(x.sbase + OFF_V + kb * V_BYTES, tmV, bar, cb * BV, h, tok);
 }
 
 // The barrier that item i's copy completes (item 2 c + 1 is X_c) and the parity
@@ -297,7 +300,8 @@ __device__ __forceinline__ uint32_t lane_base(uint32_t tmem, int warp) {
 // (MMA2 of chunk c done), the gates of chunk c+2 (the chain and the loader done
 // with chunk c's), X_c+2 (MMA_X of chunk c done).
 __device__ void copy_role(const Ctx &x, const TcParams &p, int64_t t0, int nchunks, int64_t slot0, int h,
-                          int hq, int cb, const CUtensorMap *tmK, const CUtensorMap *tmQ, const CUtensorMap *tmV) {
+                          int hq, int cb, const CUtensorMap *tmK, const CUtensorMap *tmQ, const CUtensorMap *tmV,
+                          bool v_zero) {
     const uint8_t *fsrc = p.ws + ((size_t)slot0 * p.h_v + h) * fac::SLOT_BYTES;
     const size_t fstride = (size_t)p.h_v * fac::SLOT_BYTES;
     // X tiles of chunk c (X_c = [K; Q]_c+1 K_cᵀ) sit with the slot of chunk c + 1
@@ -316,7 +320,8 @@ __device__ void copy_role(const Ctx &x, const TcParams &p, int64_t t0, int nchun
         // two chunks ahead; a [Tw; PTw] tile with the slot's exp(G) after it
         if (!bad && op_exists(i + 4, nchunks)) prefetch_l2(op_src(i + 4), (i & 1) ? OP_BYTES : fac::SLOT_BYTES);
     };
-    for (int c = 0; c < nchunks && c < NKQ; ++c) issue_kq_loads(x, c, (int)(t0 + c * C), hq, h, cb, tmK, tmQ, tmV);
+    for (int c = 0; c < nchunks && c < NKQ; ++c)
+        issue_kq_loads(x, c, (int)(t0 + c * C), hq, h, cb, tmK, tmQ, tmV, v_zero);
     // launched as a programmatic dependent of the factor launch: everything above
     // reads only inputs; the workspace is read after that grid has completed
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -326,7 +331,7 @@ __device__ void copy_role(const Ctx &x, const TcParams &p, int64_t t0, int nchun
         if (c >= 1 && c - 1 + NKQ < nchunks) {
             const int kb = (c - 1) % NKQ;
             bad = !wait_or_abort(x, x.bar(B_KQ_EMPTY + kb), (uint32_t)((c - 1) / NKQ) & 1u);
-            if (!bad) issue_kq_loads(x, kb, (int)(t0 + (c - 1 + NKQ) * C), hq, h, cb, tmK, tmQ, tmV);
+            if (!bad) issue_kq_loads(x, kb, (int)(t0 + (c - 1 + NKQ) * C), hq, h, cb, tmK, tmQ, tmV, v_zero);
         }
         next_op(2 * c + NOP);
         if (!bad && c + 2 < nchunks) {
@@ -419,17 +424,17 @@ __device__ void loader_role(const Ctx &x, int nchunks, int lt, float *Sg, bool &
 }
 
 // Row t of chunk c0 of the output (16 columns at j0 of the CTA's block).
-__device__ __forceinline__ void store_out_row(const TcParams &p, int64_t c0, int t, int h, int cb, int j0,
-                                              const float *ov) {
+__device__ __forceinline__ void store_out_row(const TcParams &p, const TcRun &run, int64_t c0, int t, int h, int cb,
+                                              int j0, const float *ov) {
     const size_t off = ((size_t)(c0 + t) * p.h_v + h) * D + cb * BV + j0;
-    if (p.out_bf16) {
-        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + off);
+    if (run.out_bf16) {
+        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(run.o) + off);
 #pragma unroll
         for (int j = 0; j < 16; j += 8)
             dst[j / 8] = make_uint4(pack_bf16x2(ov[j], ov[j + 1]), pack_bf16x2(ov[j + 2], ov[j + 3]),
                                     pack_bf16x2(ov[j + 4], ov[j + 5]), pack_bf16x2(ov[j + 6], ov[j + 7]));
     } else {
-        float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + off);
+        float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(run.o) + off);
 #pragma unroll
         for (int j = 0; j < 16; j += 4) dst[j / 4] = make_float4(ov[j], ov[j + 1], ov[j + 2], ov[j + 3]);
     }
@@ -540,8 +545,8 @@ __device__ void issuer_role(const Ctx &x, int nchunks, int lane) {
 // the CTA's 32.  Per chunk: the K / T-row warps form R from A_c and hand it to
 // the issuer (BAR_LOW), then write D~ from MMA2's accumulator; the Q / PT-row
 // warps form the outputs and store them after the chunk's last barrier.
-__device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t t1, int nchunks, int h,
-                           int cb, int tid, bool &ok) {
+__device__ void chain_role(const Ctx &x, const TcParams &p, const TcRun &run, int64_t t0, int64_t t1, int nchunks,
+                           int h, int cb, int tid, bool &ok) {
     const int warp = tid >> 5, lane = tid & 31;
     const int j0 = 16 * (warp >> 2);           // this thread's 16 columns of the CTA's 32
     const int row = ((warp & 3) << 5) + lane;  // TMEM lane
@@ -573,8 +578,8 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
                     float r[16];
 #pragma unroll
                     for (int ch = 0; ch < 2; ++ch) {
-                        float v[8];
-                        load_bf16_chunk64(vt, t, (j0 >> 3) + ch, v);
+                        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                        if (!run.v_zero) load_bf16_chunk64(vt, t, (j0 >> 3) + ch, v);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) r[8 * ch + e] = fmaf(-egt, ks[8 * ch + e], v[e]);
                     }
@@ -615,7 +620,7 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, int64_t t0, int64_t 
             break;
         }
         // outputs of the chunk's real rows (after the barrier, so no proxy fence waits on them)
-        if (!low && t < L) store_out_row(p, c0, t, h, cb, j0, ov);
+        if (!low && t < L) store_out_row(p, run, c0, t, h, cb, j0, ov);
     }
     ok = !bad;
 }
@@ -631,18 +636,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(x.sm + SM_TMEM);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int cb = blockIdx.x % NCOL;
-    const int h = (blockIdx.x / NCOL) % p.h_v;
-    const int s = (blockIdx.x / NCOL) / p.h_v;
+    const int per_run = p.n_seqs * p.h_v * NCOL;
+    const int ri = (int)blockIdx.x / per_run, bi = (int)blockIdx.x % per_run;
+    TcRun run = p.runs[0];
+#pragma unroll
+    for (int i = 1; i < kMaxTcRuns; ++i)  // static indices only: the table stays in the parameter space
+        if (i == ri) run = p.runs[i];
+    const int cb = bi % NCOL;
+    const int h = (bi / NCOL) % p.h_v;
+    const int s = (bi / NCOL) / p.h_v;
     const int hq = h / (p.h_v / p.h_qk);
     const int64_t ts0 = p.cu_seqlens[s], t1 = p.cu_seqlens[s + 1];
     if (t1 <= ts0) return;  // empty sequence: the state stays as it is
     const int nch_all = (int)((t1 - ts0 + C - 1) / C);
-    const int c_end = nch_all < p.c_hi ? nch_all : p.c_hi;
-    if (p.c_lo >= c_end) return;  // no chunk of this sequence in this launch: its state stays as it is
-    const int nchunks = c_end - p.c_lo;
-    const int64_t t0 = ts0 + (int64_t)p.c_lo * C;
-    const int64_t slot0 = fac::slot_base(ts0, s) + p.c_lo;
+    const int c_end = nch_all < run.c_hi ? nch_all : run.c_hi;
+    if (run.c_lo >= c_end) return;  // no chunk of this sequence in this run: its state stays as it is
+    const int nchunks = c_end - run.c_lo;
+    const int64_t t0 = ts0 + (int64_t)run.c_lo * C;
+    const int64_t slot0 = fac::slot_base(ts0, s) + run.c_lo;
     // a programmatic dependent launch queued behind this one (the factors of a
     // later chunk range) may start as soon as every CTA of this grid runs
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -660,7 +671,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int lt = tid - NCHAIN;
     const bool loader = lt >= 0 && lt < NLOAD;
     const bool issuer = warp == (NCHAIN + NLOAD) / 32;
-    float *Sg = p.state + (((size_t)s * p.h_v + h) * D + (loader ? lt : 0)) * D + cb * BV;
+    float *Sg = run.state + (((size_t)s * p.h_v + h) * D + (loader ? lt : 0)) * D + cb * BV;
     if (loader) {
         // S_0 into the S tile (the loader role reads its row again into registers)
 #pragma unroll
@@ -691,13 +702,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     bool ok = true;
     if (tid < NCHAIN)
-        chain_role(x, p, t0, t1, nchunks, h, cb, tid, ok);
+        chain_role(x, p, run, t0, t1, nchunks, h, cb, tid, ok);
     else if (loader)
         loader_role(x, nchunks, lt, Sg, ok);
     else if (issuer)
         issuer_role(x, nchunks, lane);
     else if (lane == 0)
-        copy_role(x, p, t0, nchunks, slot0, h, hq, cb, &tmK, &tmQ, &tmV);
+        copy_role(x, p, t0, nchunks, slot0, h, hq, cb, &tmK, &tmQ, &tmV, run.v_zero != 0);
 
     tc_fence_before_sync();
     __syncthreads();
@@ -725,8 +736,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 }  // namespace
 
-cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s, bool overlap) {
-    if (a.n_seqs == 0 || a.t_total == 0) return cudaSuccess;  // every sequence empty: state unchanged
+cudaError_t launch_prefill_tc_runs(const Args &a, const TcRun *runs, int n_runs, const float *ws, cudaStream_t s,
+                                   bool overlap) {
+    if (a.n_seqs == 0 || a.t_total == 0 || n_runs == 0) return cudaSuccess;  // nothing to walk
+    if (n_runs < 0 || n_runs > kMaxTcRuns) return cudaErrorInvalidValue;
     CUtensorMap tmK, tmQ, tmV;
     if (!encode_bf16_3d(&tmK, a.k, D, (uint64_t)a.h_qk, (uint64_t)a.t_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_bf16_3d(&tmQ, a.q, D, (uint64_t)a.h_qk, (uint64_t)a.t_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -741,20 +754,18 @@ cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s, bo
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    TcParams p;
+    TcParams p = {};
     p.h_qk = a.h_qk;
     p.h_v = a.h_v;
-    p.out_bf16 = a.out_bf16;
-    p.c_lo = a.c_lo;
-    p.c_hi = a.c_hi;
+    p.n_seqs = a.n_seqs;
+    p.n_runs = n_runs;
     p.scale = a.scale;
     p.cu_seqlens = a.cu_seqlens;
     p.ws = reinterpret_cast<const uint8_t *>(ws);
     p.xs = reinterpret_cast<const uint8_t *>(ws) + fac::x_region_offset(fac::n_slots(a.t_total, a.n_seqs), a.h_v);
-    p.state = a.state;
-    p.o = a.o;
+    for (int i = 0; i < n_runs; ++i) p.runs[i] = runs[i];
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.n_seqs * (unsigned)a.h_v * (unsigned)NCOL);
+    cfg.gridDim = dim3((unsigned)n_runs * (unsigned)a.n_seqs * (unsigned)a.h_v * (unsigned)NCOL);
     cfg.blockDim = dim3(NTHREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = s;
@@ -764,6 +775,17 @@ cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s, bo
     cfg.attrs = overlap ? &attr : nullptr;
     cfg.numAttrs = overlap ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, tmK, tmQ, tmV, p);
+}
+
+cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s, bool overlap) {
+    TcRun run = {};
+    run.c_lo = a.c_lo;
+    run.c_hi = a.c_hi;
+    run.out_bf16 = a.out_bf16;
+    run.v_zero = 0;
+    run.state = a.state;
+    run.o = a.o;
+    return launch_prefill_tc_runs(a, &run, 1, ws, s, overlap);
 }
 
 int32_t *device_error_word() {

@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define GDR_ABI_VERSION 6
+#define GDR_ABI_VERSION 7
 
 /* Same object as cudaStream_t; declared here so callers need no CUDA header. */
 typedef struct CUstream_st *gdr_stream_t;
@@ -177,6 +177,63 @@ gdr_status gdr_prefill_chunked_static(const gdr_dims *dims, int32_t n_seqs, cons
 
 /* Bytes of the fixed scratch array used by gdr_prefill_chunked_static. */
 size_t gdr_prefill_static_workspace_capacity(void);
+
+/*
+ * Two-level (segment-parallel) prefill: the same result as gdr_prefill_chunked,
+ * for problems with few (sequence, V head) pairs and long sequences, where one
+ * chain of chunks per head would leave most of the GPU idle.
+ *
+ * The chunks of every sequence are cut into n_segments consecutive segments
+ * (segment p: chunks [floor(n p / P), floor(n (p+1) / P)) of the
+ * n = ceil(t_total / 64) chunk positions; a sequence shorter than that has only
+ * its first segments).  Over a segment the recurrence is affine in the state it
+ * starts from, X: the state after it is Phi X + B and each output
+ * o_t = o0_t + X^T m_t, which follows from the closed form of the state after
+ * a chunk on the Qwen3.5-9B NPU model card ("How it works": S_T = exp(G_T) S0 +
+ * K^T diag(exp(G_T - G)) D, with D affine in S0), applied chunk after chunk.
+ * So one chunk-scan launch walks segment 0 from the real state and, beside it,
+ * every later segment twice: from X = 0 with its values (B, o0) and from X = I
+ * with zero values (Phi, and the output maps m).  A short sequential combine
+ * X_{p+1} = Phi_p X_p + B_p (fp32) then gives every segment's start state, and a
+ * last pass writes the later segments' outputs.  The chain a head walks is
+ * ~1/P of its chunks, at the cost of ~2x the chunk work for segments >= 1.
+ *
+ *   n_segments  1..8 (GDR_ERR_INVALID_ARG otherwise); more than there are chunk
+ *               positions means one per chunk; 1 runs gdr_prefill_chunked's
+ *               two-launch form.  gdr_prefill_segments_hint() gives the value
+ *               the library would pick on the current device.
+ *   workspace   DEVICE scratch of at least gdr_prefill_segmented_workspace_bytes
+ *               bytes, 16-byte aligned, as for gdr_prefill_chunked.
+ * Only the tensor-core shapes (d_k = d_v = 128, bf16 inputs, chunk 64) are
+ * supported (GDR_ERR_UNSUPPORTED otherwise).  Every other argument, the
+ * precision and the errors are as in gdr_prefill_chunked; the later segments'
+ * outputs and the final state are sums of a few more fp32 products, so they
+ * differ from gdr_prefill_chunked's by rounding only.
+ */
+gdr_status gdr_prefill_segmented(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens, int64_t t_total,
+                                 const void *q, const void *k, const void *v, const float *g, const float *beta,
+                                 float *state, void *o, int32_t n_segments, void *workspace, size_t workspace_bytes,
+                                 gdr_stream_t stream);
+
+/*
+ * Bytes of workspace gdr_prefill_segmented needs: gdr_prefill_workspace_bytes,
+ * then, 256-byte aligned, per segment after the first three fp32 states per
+ * (sequence, V head) (Phi, B and the start state, d_k * d_v floats each), and two
+ * fp32 arrays shaped like o ([t_total][H_v][d_v]) for o0 and m.  Host-only;
+ * equals gdr_prefill_workspace_bytes when n_segments is 1 (or the problem has one
+ * chunk position).
+ */
+size_t gdr_prefill_segmented_workspace_bytes(const gdr_dims *dims, int32_t n_seqs, int64_t t_total,
+                                             int32_t n_segments);
+
+/*
+ * The number of segments gdr_prefill_segmented should use on the current device
+ * (1: use gdr_prefill_chunked).  It is the largest P <= 8 for which all
+ * 2P - 1 runs of the scan launch (n_seqs * H_v * 4 CTAs of one SM each) fit on
+ * the GPU at once and every segment keeps at least 8 chunks: e.g. 5 for one
+ * 16K-token sequence of 4 V heads on a 152-SM GB300, 1 for 32 V heads.
+ */
+int32_t gdr_prefill_segments_hint(const gdr_dims *dims, int32_t n_seqs, int64_t t_total);
 
 /*
  * One decode step for `batch` independent sequences (one token each).

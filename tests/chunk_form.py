@@ -224,3 +224,45 @@ def chunk_form_lookahead(q, k, v, g, beta, S0, C, operands=None):
         S = eGC * S + K.T @ split(Dt)
     assert S.shape == (dk, v.shape[1])
     return O, S
+
+
+def segment_bounds(n_chunks: int, P: int, C: int, T: int):
+    """Token ranges of P segments over a sequence of T tokens: consecutive runs of
+    whole chunks, as even as possible (the last may end in a partial chunk)."""
+    cuts = [(n_chunks * p) // P * C for p in range(P + 1)]
+    cuts[-1] = T
+    return [(cuts[p], cuts[p + 1]) for p in range(P)]
+
+
+def segment_compose(q, k, v, g, beta, S0, C, P, run=None, mutate=None):
+    """The two-level (segment-parallel) form of one head's recurrence.
+
+    Over a segment the recurrence is affine in its start state X (the model card's
+    closed form of S_T after a chunk, "How it works", applied chunk after chunk):
+        S_t = Phi_t X + S0_t,     o_t = X^T m_t + o0_t,
+    where (S0_t, o0_t) is the run from X = 0 with the segment's values, and
+    (Phi_t, m_t) the run from X = I with all values 0 (so Phi_t = S_t and
+    m_t = Phi_t^T q_t are its state and outputs).  Segment 0 runs from the real
+    state; the others give (Phi, B = S0_end, m, o0) independently; a short
+    sequential combine X_{p+1} = Phi_p X_p + B_p yields every segment's start;
+    then each later output is o_t = o0_t + X_p^T m_t.  ``run`` computes one
+    segment from a start state (default: the model card's chunk form).
+    ``mutate`` plants a mistake for the tests that check the pins catch it:
+    "transpose" combines with Phi^T, "no_fixup" drops the X^T m_t term."""
+    run = run or (lambda q_, k_, v_, g_, b_, S_: chunk_form_pages(q_, k_, v_, g_, b_, S_, C))
+    T = q.shape[0]
+    n_chunks = (T + C - 1) // C
+    bounds = segment_bounds(n_chunks, P, C, T)
+    dk = k.shape[1]
+    O = np.zeros((T, v.shape[1]))
+    a, b = bounds[0]
+    O[a:b], X = run(q[a:b], k[a:b], v[a:b], g[a:b], beta[a:b], np.asarray(S0, np.float64))
+    trans = []
+    for a, b in bounds[1:]:
+        o0, B = run(q[a:b], k[a:b], v[a:b], g[a:b], beta[a:b], np.zeros_like(X))
+        m, Phi = run(q[a:b], k[a:b], np.zeros((b - a, dk)), g[a:b], beta[a:b], np.eye(dk))
+        trans.append((a, b, o0, B, m, Phi))
+    for a, b, o0, B, m, Phi in trans:
+        O[a:b] = o0 + (0.0 if mutate == "no_fixup" else m @ X)
+        X = (Phi.T if mutate == "transpose" else Phi) @ X + B
+    return O, X

@@ -169,3 +169,34 @@ def test_product_package_never_imports_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
                 assert "gdr_oracle" not in text and "liboracle" not in text, f
+
+
+def test_segmented_workspace_size_and_checks(L):
+    """Sizes and host-side rejections of the two-level prefill (no launch)."""
+    d = dims()
+    base = L.gdr_prefill_workspace_bytes(ctypes.byref(d), 1, 16384)
+    assert L.gdr_prefill_segmented_workspace_bytes(ctypes.byref(d), 1, 16384, 1) == base
+    # three fp32 states per (segment after the first, V head), two fp32 arrays like o
+    st, rows = 32 * 128 * 128 * 4, 16384 * 32 * 128 * 4
+    for P in (2, 4, 8):
+        got = L.gdr_prefill_segmented_workspace_bytes(ctypes.byref(d), 1, 16384, P)
+        assert got == ((base + 255) // 256 * 256) + 3 * (P - 1) * st + 2 * rows, P
+    # more segments than chunk positions: one per chunk (2 chunks here)
+    two = L.gdr_prefill_segmented_workspace_bytes(ctypes.byref(d), 1, 100, 2)
+    assert L.gdr_prefill_segmented_workspace_bytes(ctypes.byref(d), 1, 100, 8) == two
+    assert L.gdr_prefill_segmented_workspace_bytes(ctypes.byref(d), 1, 64, 8) == \
+        L.gdr_prefill_workspace_bytes(ctypes.byref(d), 1, 64)
+    ws = L.gdr_prefill_segmented_workspace_bytes(ctypes.byref(d), 1, 4096, 4)
+    args = lambda P, dd=d, w=ws, wp=A: (ctypes.byref(dd), 1, A, 4096, A, A, A, A, A, A, A, P, wp, w, None)
+    for P in (0, 9, -1):
+        assert L.gdr_prefill_segmented(*args(P)) == gdr.GDR_ERR_INVALID_ARG, P
+    assert L.gdr_prefill_segmented(*args(4, w=ws - 1)) == gdr.GDR_ERR_INVALID_ARG
+    assert L.gdr_prefill_segmented(*args(4, wp=MISALIGNED)) == gdr.GDR_ERR_INVALID_ARG
+    assert L.gdr_prefill_segmented(*args(4, dd=dims(in_dtype=gdr.GDR_F32))) == gdr.GDR_ERR_UNSUPPORTED
+    assert L.gdr_prefill_segmented(*args(4, dd=dims(chunk=16))) == gdr.GDR_ERR_UNSUPPORTED
+    assert L.gdr_prefill_segmented(*args(4, dd=dims(h_v=30))) == gdr.GDR_ERR_INVALID_ARG
+    bad_ptr = (ctypes.byref(d), 1, A, 4096, A, MISALIGNED, A, A, A, A, A, 4, A, ws, None)
+    assert L.gdr_prefill_segmented(*bad_ptr) == gdr.GDR_ERR_INVALID_ARG
+    # without a GPU the hint is 1 (no SMs to spread segments over); invalid dims: 1
+    assert L.gdr_prefill_segments_hint(None, 1, 16384) == 1
+    assert L.gdr_prefill_segments_hint(ctypes.byref(dims(chunk=16)), 1, 16384) == 1

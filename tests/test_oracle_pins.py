@@ -411,3 +411,68 @@ def test_kernel_operand_rounding_stays_inside_the_tolerances(g_fixed):
     # fp16 keeps 3 more significand bits; under strong decay part of the fp16
     # error is the underflow of the most decayed Tw rows, which bf16 keeps
     assert err["bf16_single"][0] >= 4 * eo and err["bf16_single"][1] >= 2 * es, err
+
+
+# --- two-level (segment-parallel) scan -----------------------------------------------
+
+
+def _gates(r, T, regime):
+    if regime == "slow":  # the start state's influence survives a whole segment
+        return r.uniform(-0.05, -0.001, T)
+    if regime == "fixed":
+        return np.full(T, -6.72)
+    return r.uniform(-8.0, -0.01, T)
+
+
+@pytest.mark.parametrize("T,P,regime", [(128, 2, "slow"), (1000, 3, "slow"), (1000, 4, "uniform"),
+                                        (4096, 4, "slow"), (4096, 2, "fixed"), (200, 3, "slow")])
+def test_segment_composition_equals_sequential(T, P, regime):
+    """Segments composed through their affine transitions (start state I with
+    zero values for the transition and the output maps, start state 0 for the
+    offsets, a sequential combine, then the per-token fix-up) reproduce the
+    sequential recurrence, for segment cuts at chunk boundaries with a ragged
+    last chunk.  With slow decay the transitions carry the start state across
+    whole segments (checked), so the combine and the fix-up are exercised; under
+    the strong -6.72 decay they vanish and the segments decouple."""
+    from tests.chunk_form import segment_compose
+
+    r = _rng(400 + T + P)
+    dk = dv = 32 if T > 1000 else 16
+    q = _unit(r.standard_normal((T, dk)))
+    k = _unit(r.standard_normal((T, dk)))
+    v = r.standard_normal((T, dv))
+    g = _gates(r, T, regime)
+    beta = 1.0 / (1.0 + np.exp(-r.standard_normal(T)))
+    S0 = 0.02 * r.standard_normal((dk, dv))
+    o, S = _single(q, k, v, g, beta, S0)
+    oc, Sc = segment_compose(q, k, v, g, beta, S0, 64, P)
+    assert np.max(np.abs(oc - o)) <= 1e-10 * np.sqrt(np.mean(o * o))
+    assert np.linalg.norm(Sc - S) <= 1e-10 * np.linalg.norm(S)
+    if regime == "slow":
+        bad, _ = segment_compose(q, k, v, g, beta, S0, 64, P, mutate="no_fixup")
+        assert np.max(np.abs(bad - o)) > 1e-3 * np.sqrt(np.mean(o * o))
+
+
+def test_segment_composition_is_pinned_by_the_oracle_too():
+    """The same composition with every segment run by the oracle itself (the
+    sequential recurrence from X = I with zero values gives the transition and the
+    output maps): its arithmetic alone, independent of any chunk form."""
+    from tests.chunk_form import segment_compose
+
+    r = _rng(471)
+    T, dk, dv, P = 333, 8, 8, 3
+    q = _unit(r.standard_normal((T, dk)))
+    k = _unit(r.standard_normal((T, dk)))
+    v = r.standard_normal((T, dv))
+    g = _gates(r, T, "slow")
+    beta = 1.0 / (1.0 + np.exp(-r.standard_normal(T)))
+    S0 = 0.02 * r.standard_normal((dk, dv))
+    o, S = _single(q, k, v, g, beta, S0)
+    oc, Sc = segment_compose(q, k, v, g, beta, S0, 64, P, run=lambda *a: _single(*a))
+    assert np.max(np.abs(oc - o)) <= 1e-11 * np.sqrt(np.mean(o * o))
+    assert np.linalg.norm(Sc - S) <= 1e-11 * np.linalg.norm(S)
+    # plausible mistakes: combining with the transposed transition, dropping the fix-up
+    bad_t = segment_compose(q, k, v, g, beta, S0, 64, P, run=lambda *a: _single(*a), mutate="transpose")
+    assert np.linalg.norm(bad_t[1] - S) > 1e-6 * np.linalg.norm(S)
+    bad_f = segment_compose(q, k, v, g, beta, S0, 64, P, run=lambda *a: _single(*a), mutate="no_fixup")
+    assert np.max(np.abs(bad_f[0] - o)) > 1e-6 * np.sqrt(np.mean(o * o))

@@ -52,7 +52,12 @@ def test_static_entry_matches_workspace_entry_twice():
 @pytest.mark.gpu
 def test_static_entry_at_its_largest_single_sequence():
     """One Qwen3.5-9B sequence of 5312 tokens fills the fixed array to its last
-    chunk position; the result equals the workspace entry's bit for bit."""
+    chunk position.  At this length gdr_prefill_chunked splits the prefill into
+    four launches (the static entry keeps two), which regroups a few products,
+    so the two agree to rounding: both are checked against the oracle, and
+    against each other within the tensor-core path's own spread."""
+    import oracle
+
     torch = gu.require_gpu()
     w = synth.make_workload("no_alloc_max", [5312], 16, 32, 128, 64, "bf16", seed=72, state_std=0.02)
     x = gu.dev_inputs(w)
@@ -61,6 +66,10 @@ def test_static_entry_at_its_largest_single_sequence():
     gdr.gdr_prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], s_ws, o_ws, x["cu_seqlens"])
     gdr.gdr_prefill_chunked_static(x["q"], x["k"], x["v"], x["g"], x["beta"], s_st, o_st, x["cu_seqlens"])
     torch.cuda.synchronize()
-    assert np.array_equal(gu.to_np(o_ws), gu.to_np(o_st))
-    assert np.array_equal(gu.to_np(s_ws), gu.to_np(s_st))
     assert gdr.gdr_device_error(device=x["q"].device) == 0
+    o_ref, s_ref = oracle.run_workload(w)
+    for o, s in ((o_ws, s_ws), (o_st, s_st)):
+        gu.check_outputs(gu.to_np(o), o_ref)
+        gu.check_state(gu.to_np(s), s_ref)
+    assert gu.o_error(gu.to_np(o_st), gu.to_np(o_ws)) < gu.TC_O_TOL
+    assert gu.state_error(gu.to_np(s_st), gu.to_np(s_ws)) < gu.TC_S_TOL
