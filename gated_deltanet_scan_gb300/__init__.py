@@ -17,13 +17,15 @@ __all__ = [
     "GdrError", "gdr_dims", "lib", "library_path",
     "gdr_prefill_chunked", "gdr_prefill_workspace_bytes", "gdr_prefill_chunked_static",
     "gdr_prefill_segmented", "gdr_prefill_segmented_workspace_bytes", "gdr_prefill_segments_hint",
-    "gdr_decode_step", "gdr_decode_step_overlapped", "gdr_verify_block", "gdr_verify_commit",
+    "gdr_decode_step", "gdr_decode_step_overlapped", "gdr_decode_step_gated", "gdr_gated_rmsnorm",
+    "gdr_verify_block", "gdr_verify_commit",
     "gdr_state_snapshot", "gdr_state_restore", "gdr_device_error", "gdr_selftest_wait_timeout", "gdr_status_string",
-    "GDR_F32", "GDR_BF16",
+    "GDR_F32", "GDR_BF16", "GDR_FLAG_QK_L2NORM", "GDR_FLAG_BETA_LOGITS",
 ]
 
 GDR_OK, GDR_ERR_INVALID_ARG, GDR_ERR_UNSUPPORTED, GDR_ERR_CUDA, GDR_ERR_DEVICE_TIMEOUT = range(5)
 GDR_F32, GDR_BF16 = 0, 1
+GDR_FLAG_QK_L2NORM, GDR_FLAG_BETA_LOGITS = 1, 2
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
@@ -46,6 +48,7 @@ class gdr_dims(ctypes.Structure):
         ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32),
         ("chunk", ctypes.c_int32), ("in_dtype", ctypes.c_int32),
         ("out_dtype", ctypes.c_int32), ("scale", ctypes.c_float),
+        ("flags", ctypes.c_int32),
     ]
 
 
@@ -73,6 +76,10 @@ _SIGS = {
                           _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "gdr_verify_commit": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, ctypes.c_int32,
                            _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "gdr_decode_step_gated": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P,
+                               ctypes.c_float, _P, _P], ctypes.c_int),
+    "gdr_gated_rmsnorm": ([ctypes.POINTER(gdr_dims), ctypes.c_int64, _P, _P, _P, ctypes.c_float, _P, _P],
+                          ctypes.c_int),
     "gdr_state_snapshot": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, _P, _P], ctypes.c_int),
     "gdr_state_restore": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, _P, _P], ctypes.c_int),
     "gdr_device_error": ([_P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
@@ -144,22 +151,26 @@ def _stream_handle(stream, device) -> Optional[int]:
     return stream.cuda_stream
 
 
-def make_dims(q, v, o, chunk: int = 64, scale: float = 1.0) -> gdr_dims:
+def flags_of(qk_l2norm: bool = False, beta_logits: bool = False) -> int:
+    return (GDR_FLAG_QK_L2NORM if qk_l2norm else 0) | (GDR_FLAG_BETA_LOGITS if beta_logits else 0)
+
+
+def make_dims(q, v, o, chunk: int = 64, scale: float = 1.0, flags: int = 0) -> gdr_dims:
     """dims from q [T, H_qk, d_k], v [T, H_v, d_v] and o (its dtype is the output type)."""
     return gdr_dims(h_qk=q.shape[-2], h_v=v.shape[-2], d_k=q.shape[-1], d_v=v.shape[-1],
                     chunk=chunk, in_dtype=_dtype_code(q), out_dtype=_dtype_code(o),
-                    scale=float(scale))
+                    scale=float(scale), flags=int(flags))
 
 
 def gdr_prefill_workspace_bytes(q, v, o, n_seqs: int, t_total: int, *, chunk: int = 64,
                                 scale: float = 1.0) -> int:
     """Device scratch bytes gdr_prefill_chunked needs (0 on the CUDA-core path)."""
-    dims = make_dims(q, v, o, chunk, scale)
+    dims = make_dims(q, v, o, chunk, scale, 0)
     return int(lib().gdr_prefill_workspace_bytes(ctypes.byref(dims), int(n_seqs), int(t_total)))
 
 
 def gdr_prefill_chunked(q, k, v, g, beta, state, o, cu_seqlens, *, chunk: int = 64,
-                        scale: float = 1.0, t_total: Optional[int] = None, workspace=None,
+                        scale: float = 1.0, qk_l2norm: bool = False, beta_logits: bool = False, t_total: Optional[int] = None, workspace=None,
                         stream=None) -> None:
     """Chunked prefill over packed sequences (see gdr_prefill_chunked in include/gdr.h).
 
@@ -171,7 +182,7 @@ def gdr_prefill_chunked(q, k, v, g, beta, state, o, cu_seqlens, *, chunk: int = 
     stream the call runs on (``stream``), so that torch hands its memory to no
     other work before the call's kernels on that stream are done."""
     torch = _torch()
-    dims = make_dims(q, v, o, chunk, scale)
+    dims = make_dims(q, v, o, chunk, scale, flags_of(qk_l2norm, beta_logits))
     n = cu_seqlens.shape[0] - 1
     T = q.shape[0] if t_total is None else int(t_total)
     need = int(lib().gdr_prefill_workspace_bytes(ctypes.byref(dims), n, T))
@@ -192,10 +203,11 @@ def gdr_prefill_chunked(q, k, v, g, beta, state, o, cu_seqlens, *, chunk: int = 
 
 
 def gdr_prefill_chunked_static(q, k, v, g, beta, state, o, cu_seqlens, *, chunk: int = 64,
-                               scale: float = 1.0, t_total: Optional[int] = None, stream=None) -> None:
+                               scale: float = 1.0, qk_l2norm: bool = False, beta_logits: bool = False,
+                               t_total: Optional[int] = None, stream=None) -> None:
     """gdr_prefill_chunked with the library's fixed scratch array instead of a
     workspace (nothing is allocated; see include/gdr.h for its size limit)."""
-    dims = make_dims(q, v, o, chunk, scale)
+    dims = make_dims(q, v, o, chunk, scale, flags_of(qk_l2norm, beta_logits))
     n = cu_seqlens.shape[0] - 1
     T = q.shape[0] if t_total is None else int(t_total)
     st = lib().gdr_prefill_chunked_static(
@@ -206,26 +218,26 @@ def gdr_prefill_chunked_static(q, k, v, g, beta, state, o, cu_seqlens, *, chunk:
 
 def gdr_prefill_segments_hint(q, v, o, n_seqs: int, t_total: int, *, chunk: int = 64, scale: float = 1.0) -> int:
     """Segments the two-level prefill would use on the current device (1: none)."""
-    dims = make_dims(q, v, o, chunk, scale)
+    dims = make_dims(q, v, o, chunk, scale, 0)
     return int(lib().gdr_prefill_segments_hint(ctypes.byref(dims), int(n_seqs), int(t_total)))
 
 
 def gdr_prefill_segmented_workspace_bytes(q, v, o, n_seqs: int, t_total: int, n_segments: int, *,
                                           chunk: int = 64, scale: float = 1.0) -> int:
-    dims = make_dims(q, v, o, chunk, scale)
+    dims = make_dims(q, v, o, chunk, scale, 0)
     return int(lib().gdr_prefill_segmented_workspace_bytes(ctypes.byref(dims), int(n_seqs), int(t_total),
                                                            int(n_segments)))
 
 
 def gdr_prefill_segmented(q, k, v, g, beta, state, o, cu_seqlens, n_segments: Optional[int] = None, *,
-                          chunk: int = 64, scale: float = 1.0, t_total: Optional[int] = None, workspace=None,
+                          chunk: int = 64, scale: float = 1.0, qk_l2norm: bool = False, beta_logits: bool = False, t_total: Optional[int] = None, workspace=None,
                           stream=None) -> None:
     """Two-level (segment-parallel) prefill (see gdr_prefill_segmented in
     include/gdr.h): arguments as gdr_prefill_chunked; ``n_segments`` defaults to
     gdr_prefill_segments_hint.  Without ``workspace`` one is taken from torch's
     allocator on the call's stream."""
     torch = _torch()
-    dims = make_dims(q, v, o, chunk, scale)
+    dims = make_dims(q, v, o, chunk, scale, flags_of(qk_l2norm, beta_logits))
     n = cu_seqlens.shape[0] - 1
     T = q.shape[0] if t_total is None else int(t_total)
     P = int(lib().gdr_prefill_segments_hint(ctypes.byref(dims), n, T)) if n_segments is None else int(n_segments)
@@ -244,34 +256,64 @@ def gdr_prefill_segmented(q, k, v, g, beta, state, o, cu_seqlens, n_segments: Op
     _check(st, "gdr_prefill_segmented")
 
 
-def gdr_decode_step(q, k, v, g, beta, state, o, *, scale: float = 1.0, stream=None) -> None:
+def gdr_decode_step(q, k, v, g, beta, state, o, *, scale: float = 1.0, qk_l2norm: bool = False,
+                    beta_logits: bool = False, stream=None) -> None:
     """One decode step for B sequences: q, k [B, H_qk, d]; v, o [B, H_v, d];
     g, beta [B, H_v]; state [B, H_v, d, d] updated in place."""
-    dims = make_dims(q, v, o, 64, scale)
+    dims = make_dims(q, v, o, 64, scale, flags_of(qk_l2norm, beta_logits))
     st = lib().gdr_decode_step(
         ctypes.byref(dims), q.shape[0], _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
         _ptr(state), _ptr(o), _stream_handle(stream, q.device))
     _check(st, "gdr_decode_step")
 
 
-def gdr_decode_step_overlapped(q, k, v, g, beta, state, o, *, scale: float = 1.0, stream=None) -> None:
+def gdr_decode_step_overlapped(q, k, v, g, beta, state, o, *, scale: float = 1.0, qk_l2norm: bool = False,
+                               beta_logits: bool = False, stream=None) -> None:
     """gdr_decode_step launched as a programmatic dependent of the kernel before it
     on the stream (see include/gdr.h): none of its inputs or states may be written
     by that kernel."""
-    dims = make_dims(q, v, o, 64, scale)
+    dims = make_dims(q, v, o, 64, scale, flags_of(qk_l2norm, beta_logits))
     st = lib().gdr_decode_step_overlapped(
         ctypes.byref(dims), q.shape[0], _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
         _ptr(state), _ptr(o), _stream_handle(stream, q.device))
     _check(st, "gdr_decode_step_overlapped")
 
 
+RMSNORM_EPS = 1e-6  # the epsilon of the gated RMSNorm after the rule
+
+
+def gdr_decode_step_gated(q, k, v, g, beta, state, z, weight, y, *, eps: float = RMSNORM_EPS, scale: float = 1.0,
+                          qk_l2norm: bool = False, beta_logits: bool = False, stream=None) -> None:
+    """gdr_decode_step with the gated RMSNorm fused: y = weight * o / sqrt(mean(o^2) + eps) * silu(z)
+    per (sequence, V head) row; z [B, H_v, d] like v, weight [d] fp32, y like the output."""
+    dims = make_dims(q, v, y, 64, scale, flags_of(qk_l2norm, beta_logits))
+    st = lib().gdr_decode_step_gated(
+        ctypes.byref(dims), q.shape[0], _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state), _ptr(z),
+        _ptr(weight), float(eps), _ptr(y), _stream_handle(stream, q.device))
+    _check(st, "gdr_decode_step_gated")
+
+
+def gdr_gated_rmsnorm(o, z, weight, y, *, eps: float = RMSNORM_EPS, stream=None) -> None:
+    """y = weight * o / sqrt(mean(o^2) + eps) * silu(z) over the last axis of o [..., d]
+    (o and y fp32 or bf16, z fp32 or bf16, weight [d] fp32)."""
+    d = o.shape[-1]
+    rows = o.numel() // d
+    dims = gdr_dims(h_qk=1, h_v=1, d_k=d, d_v=d, chunk=64, in_dtype=_dtype_code(z), out_dtype=_dtype_code(o),
+                    scale=1.0, flags=0)
+    if y.dtype != o.dtype:
+        raise TypeError("y must have o's dtype")
+    st = lib().gdr_gated_rmsnorm(ctypes.byref(dims), rows, _ptr(o), _ptr(z), _ptr(weight), float(eps), _ptr(y),
+                                 _stream_handle(stream, o.device))
+    _check(st, "gdr_gated_rmsnorm")
+
+
 def gdr_verify_block(q, k, v, g, beta, state, snapshot, o, n_tok: int, *, deltas=None, scale: float = 1.0,
-                     stream=None) -> None:
+                     qk_l2norm: bool = False, beta_logits: bool = False, stream=None) -> None:
     """n_tok (<= 16) draft tokens per sequence from the current state; the incoming
     state is copied to ``snapshot``.  Token rows are [n_seqs * n_tok, ...].  With
     ``deltas`` (fp32, shaped like v) each token's correction is kept for
     gdr_verify_commit."""
-    dims = make_dims(q, v, o, 16, scale)
+    dims = make_dims(q, v, o, 16, scale, flags_of(qk_l2norm, beta_logits))
     n = state.shape[0]
     st = lib().gdr_verify_block(
         ctypes.byref(dims), n, int(n_tok), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
@@ -279,13 +321,14 @@ def gdr_verify_block(q, k, v, g, beta, state, snapshot, o, n_tok: int, *, deltas
     _check(st, "gdr_verify_block")
 
 
-def gdr_verify_commit(k, g, deltas, snapshot, state, accepted, n_tok: int, *, stream=None) -> None:
+def gdr_verify_commit(k, g, deltas, snapshot, state, accepted, n_tok: int, *, qk_l2norm: bool = False,
+                      stream=None) -> None:
     """State after the accepted prefix of a verify block: accepted (int32 device
     tensor [n_seqs]) tokens per sequence, from the block's ``deltas`` and the
     ``snapshot`` it took; writes ``state``."""
     n, hv, dk, dv = state.shape
     dims = gdr_dims(h_qk=k.shape[1], h_v=hv, d_k=dk, d_v=dv, chunk=16,
-                    in_dtype=_dtype_code(k), out_dtype=GDR_F32, scale=1.0)
+                    in_dtype=_dtype_code(k), out_dtype=GDR_F32, scale=1.0, flags=flags_of(qk_l2norm))
     st = lib().gdr_verify_commit(
         ctypes.byref(dims), n, int(n_tok), _ptr(accepted), _ptr(k), _ptr(g), _ptr(deltas),
         _ptr(snapshot), _ptr(state), _stream_handle(stream, state.device))

@@ -56,6 +56,7 @@ gdr_status check_dims(const gdr_dims *d) {
     if (d->chunk != 16 && d->chunk != 64) return GDR_ERR_UNSUPPORTED;
     if (d->d_k != d->d_v) return GDR_ERR_UNSUPPORTED;
     if (d->d_k != 32 && d->d_k != 64 && d->d_k != 128) return GDR_ERR_UNSUPPORTED;
+    if (d->flags & ~(GDR_FLAG_QK_L2NORM | GDR_FLAG_BETA_LOGITS)) return GDR_ERR_INVALID_ARG;
     return GDR_OK;
 }
 
@@ -67,6 +68,8 @@ Args make_args(const gdr_dims *d) {
     a.in_bf16 = d->in_dtype == GDR_BF16;
     a.out_bf16 = d->out_dtype == GDR_BF16;
     a.scale = d->scale;
+    a.qk_norm = (d->flags & GDR_FLAG_QK_L2NORM) != 0;
+    a.beta_logits = (d->flags & GDR_FLAG_BETA_LOGITS) != 0;
     a.c_lo = 0;
     a.c_hi = INT_MAX;
     return a;
@@ -327,7 +330,8 @@ namespace gdr {
 namespace {
 
 gdr_status decode(const gdr_dims *dims, int32_t batch, const void *q, const void *k, const void *v,
-                  const float *g, const float *beta, float *state, void *o, gdr_stream_t stream, bool overlap) {
+                  const float *g, const float *beta, float *state, void *o, gdr_stream_t stream, bool overlap,
+                  const void *norm_z = nullptr, const float *norm_w = nullptr, float norm_eps = 0.f) {
     gdr_status st = check_dims(dims);
     if (st != GDR_OK) return st;
     if (batch < 0) return GDR_ERR_INVALID_ARG;
@@ -346,6 +350,9 @@ gdr_status decode(const gdr_dims *dims, int32_t batch, const void *q, const void
     a.state = state;
     a.snapshot = nullptr;
     a.o = o;
+    a.norm_z = norm_z;
+    a.norm_w = norm_w;
+    a.norm_eps = norm_eps;
     int32_t *err = device_error_word();
     if (!err) return GDR_ERR_CUDA;
     return from_cuda(launch_decode(a, err, reinterpret_cast<cudaStream_t>(stream), overlap));
@@ -366,6 +373,27 @@ gdr_status gdr_decode_step_overlapped(const gdr_dims *dims, int32_t batch, const
                                       const void *v, const float *g, const float *beta, float *state,
                                       void *o, gdr_stream_t stream) {
     return decode(dims, batch, q, k, v, g, beta, state, o, stream, true);
+}
+
+gdr_status gdr_decode_step_gated(const gdr_dims *dims, int32_t batch, const void *q, const void *k, const void *v,
+                                 const float *g, const float *beta, float *state, const void *z, const float *weight,
+                                 float eps, void *y, gdr_stream_t stream) {
+    if (!z || !weight || !aligned16(z) || !aligned16(weight) || !(eps >= 0.f)) return GDR_ERR_INVALID_ARG;
+    return decode(dims, batch, q, k, v, g, beta, state, y, stream, false, z, weight, eps);
+}
+
+gdr_status gdr_gated_rmsnorm(const gdr_dims *dims, int64_t n_rows, const void *o, const void *z, const float *weight,
+                             float eps, void *y, gdr_stream_t stream) {
+    gdr_status st = check_dims(dims);
+    if (st != GDR_OK) return st;
+    if (n_rows < 0 || !(eps >= 0.f)) return GDR_ERR_INVALID_ARG;
+    if (n_rows == 0) return GDR_OK;
+    const void *ps[] = {o, z, weight, y};
+    for (const void *p : ps)
+        if (!p || !aligned16(p)) return GDR_ERR_INVALID_ARG;
+    return from_cuda(launch_gated_rmsnorm(n_rows, dims->d_v, o, dims->out_dtype == GDR_BF16, z,
+                                          dims->in_dtype == GDR_BF16, weight, eps, y, dims->out_dtype == GDR_BF16,
+                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
 gdr_status gdr_verify_block(const gdr_dims *dims, int32_t n_seqs, int32_t n_tok, const void *q,

@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(32 * CcShape<D>::SPLIT) chunk_cc_kernel(Args a
             float gt = 0.f, bt = 0.f;
             if (lane < L) {
                 gt = a.g[(size_t)(c0 + lane) * a.h_v + h];
-                bt = a.beta[(size_t)(c0 + lane) * a.h_v + h];
+                bt = beta_of(a.beta[(size_t)(c0 + lane) * a.h_v + h], a.beta_logits);
             }
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -139,6 +139,18 @@ __global__ void __launch_bounds__(32 * CcShape<D>::SPLIT) chunk_cc_kernel(Args a
             }
         }
         __syncthreads();
+        if (a.qk_norm) {
+            // fused L2 normalisation of the chunk's k and q rows, in place (a
+            // padding row is zero and stays zero)
+            for (int rr = p; rr < 2 * C; rr += SPLIT) {
+                float *row = rr < C ? sK[rr] : sQ[rr - C];
+                float ss = 0.f;
+                for (int i = lane; i < D; i += 32) ss = fmaf(row[i], row[i], ss);
+                const float sc = l2norm_scale(warp_sum(ss));
+                for (int i = lane; i < D; i += 32) row[i] *= sc;
+            }
+            __syncthreads();
+        }
 
         // Gram products for the chunk: N (strict lower, beta and decay applied), P (lower).
         for (int e = threadIdx.x; e < C * C; e += NT) {

@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(NT) commit_kernel(Args a, int32_t *err) {
     constexpr int NR = ROWS / RSTEP;       // rows per thread (D = 32: RSTEP 32 > ROWS 8, see below)
     static_assert(D % NQUART == 0, "row quarters");
     __shared__ float sK[MAXTOK][ROWS];     // the block's rows of k_j for the accepted tokens, fp32
-    __shared__ float sW[MAXTOK];           // e^{G_a - G_j}
+    __shared__ float sW[MAXTOK];           // e^{G_a - G_j} (times 1 / |k_j| with the fused L2 norm)
     __shared__ float sEa;                  // e^{G_a}
 
     const int quarter = blockIdx.x % NQUART;
@@ -84,6 +84,21 @@ __global__ void __launch_bounds__(NT) commit_kernel(Args a, int32_t *err) {
         sK[j][i] = load_in(a.k, ((row0 + j) * a.h_qk + hq) * D + rbase + i, a.in_bf16);
     }
     __syncthreads();
+    if (a.qk_norm) {
+        // fused L2 normalisation: k_j u_j^T uses k_j / |k_j|; the whole row's norm
+        // folds into the token's weight (warp w takes tokens w, w + 8)
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        for (int j = warp; j < acc; j += NT / 32) {
+            float ss = 0.f;
+            for (int i = lane; i < D; i += 32) {
+                const float x = load_in(a.k, ((row0 + j) * a.h_qk + hq) * D + i, a.in_bf16);
+                ss = fmaf(x, x, ss);
+            }
+            ss = warp_sum(ss);
+            if (lane == 0) sW[j] *= l2norm_scale(ss);
+        }
+        __syncthreads();
+    }
 #pragma unroll
     for (int j = 0; j < MAXTOK; ++j) {
         const float w = sW[j];

@@ -31,6 +31,18 @@ __device__ __forceinline__ void seq_bounds(const int32_t *cu, int fixed_len, int
     }
 }
 
+// The epsilon of the fused q/k L2 normalisation (inside the square root).
+constexpr float kL2NormEps = 1e-6f;
+
+// 1 / sqrt(sum x^2 + eps) from a sum of squares.
+__device__ __forceinline__ float l2norm_scale(float sumsq) { return rsqrtf(sumsq + kL2NormEps); }
+
+// beta from its input: the value itself, or sigmoid of a logit.
+__device__ __forceinline__ float beta_of(float b, int logits) { return logits ? 1.f / (1.f + __expf(-b)) : b; }
+
+// silu(z) = z sigmoid(z), the gate of the output RMSNorm.
+__device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);

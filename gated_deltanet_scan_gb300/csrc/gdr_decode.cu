@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(Args a, int32_t *err) 
     float *red = reinterpret_cast<float *>(dsm + Sh::OFF_RED);  // [RSTEP][D]
     const uint32_t bar = smem_u32(dsm + Sh::OFF_BAR);
     __shared__ float sk[D], sq[D];
-    __shared__ float s_qk;
+    __shared__ float s_qk, s_rk, s_rq;
 
     const int bh = blockIdx.x;
     const int b = bh / a.h_v, h = bh - b * a.h_v;
@@ -81,11 +81,19 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(Args a, int32_t *err) 
     }
     const size_t vh = (size_t)b * a.h_v + h;
     const float dgate = __expf(a.g[vh]);
-    const float bt = a.beta[vh];
+    const float bt = beta_of(a.beta[vh], a.beta_logits);
     float vv[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) vv[c] = load_in(a.v, vh * D + 4 * cq + c, a.in_bf16);
     __syncthreads();  // the mbarrier is initialised, sk and sq are written
+    if (a.qk_norm && warp < 2) {
+        // fused L2 normalisation: per-row scales of k (warp 0) and q (warp 1)
+        const float *x = warp == 0 ? sk : sq;
+        float ss = 0.f;
+        for (int i = lane; i < D; i += 32) ss = fmaf(x[i], x[i], ss);
+        ss = warp_sum(ss);
+        if (lane == 0) (warp == 0 ? s_rk : s_rq) = l2norm_scale(ss);
+    }
     const bool ok = mbar_wait_bounded(bar, 0, kWaitLimit);
     if (!__syncthreads_and(ok)) {
         // leave the state untouched; let the copies land before the block's shared memory is released
@@ -122,13 +130,15 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(Args a, int32_t *err) 
         if (lane == 0) s_qk = pq;
     }
     __syncthreads();
+    // with the fused normalisation the sums above used the raw k and q: scale them
+    const float rk = a.qk_norm ? s_rk : 1.f, rq = a.qk_norm ? s_rq : 1.f;
     float delta[4], zt[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         float ys = 0.f;
 #pragma unroll 8
         for (int w = 0; w < Sh::RSTEP; ++w) ys += red[w * D + 4 * cq + c];
-        delta[c] = bt * (vv[c] - dgate * ys);
+        delta[c] = bt * (vv[c] - dgate * rk * ys);
     }
     __syncthreads();
     *reinterpret_cast<float4 *>(red + rg * D + 4 * cq) = z;
@@ -138,13 +148,29 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(Args a, int32_t *err) 
         float zs = 0.f;
 #pragma unroll 8
         for (int w = 0; w < Sh::RSTEP; ++w) zs += red[w * D + 4 * cq + c];
-        zt[c] = zs;
+        zt[c] = rq * zs;
     }
     if (rg == 0) {
-        const float qk = s_qk;
+        // row group 0 (lanes 0 .. D/4 - 1 of warp 0) holds the whole output row
+        const float qk = s_qk * rq * rk;
+        float ov[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            store_out(a.o, vh * D + 4 * cq + c, a.scale * fmaf(dgate, zt[c], qk * delta[c]), a.out_bf16);
+        for (int c = 0; c < 4; ++c) ov[c] = a.scale * fmaf(dgate, zt[c], qk * delta[c]);
+        if (a.norm_z) {
+            // gated RMSNorm of the row, fused: y = w o / sqrt(mean(o^2) + eps) silu(z)
+            constexpr unsigned kMask = Sh::Q4 == 32 ? 0xffffffffu : ((1u << Sh::Q4) - 1u);
+            float ss = ov[0] * ov[0] + ov[1] * ov[1] + ov[2] * ov[2] + ov[3] * ov[3];
+#pragma unroll
+            for (int off = Sh::Q4 / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(kMask, ss, off);
+            const float inv = rsqrtf(ss / D + a.norm_eps);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int col = 4 * cq + c;
+                ov[c] = a.norm_w[col] * ov[c] * inv * silu(load_in(a.norm_z, vh * D + col, a.in_bf16));
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) store_out(a.o, vh * D + 4 * cq + c, ov[c], a.out_bf16);
     }
 
     // S' = d S + k delta^T, from shared memory straight to HBM
@@ -153,7 +179,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(Args a, int32_t *err) 
     for (int i = 0; i < Sh::NR; ++i) {
         const int r = rg + i * Sh::RSTEP;
         const float4 sv = sS[r * Sh::Q4 + cq];
-        const float kr = sk[r];
+        const float kr = rk * sk[r];
         const float4 nv = make_float4(fmaf(dgate, sv.x, kr * delta[0]), fmaf(dgate, sv.y, kr * delta[1]),
                                       fmaf(dgate, sv.z, kr * delta[2]), fmaf(dgate, sv.w, kr * delta[3]));
         __stcs(&Sg[r * Sh::Q4 + cq], nv);

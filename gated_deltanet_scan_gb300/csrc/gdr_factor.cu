@@ -79,8 +79,9 @@ constexpr int HEAD_B = OFF_TD + 4 * BLK_B;  // 50176
 // completed, the scratch overwrites them.
 constexpr uint32_t OFF_KQ = 0;
 constexpr uint32_t OFF_KP = 32768;  // K of the previous chunk: two 8 KB d_k halves
-constexpr uint32_t OFF_GATES = HEAD_B;           // G log2(e), beta, exp(G), exp(G_C - G): 4 x 64 fp32
-constexpr uint32_t OFF_BARS = OFF_GATES + 1024;  // 2 mbarriers
+// G log2(e), beta, exp(G), exp(G_C - G), 1 / |k|, 1 / |q|: 6 x 64 fp32
+constexpr uint32_t OFF_GATES = HEAD_B;
+constexpr uint32_t OFF_BARS = OFF_GATES + 1536;  // 2 mbarriers
 constexpr uint32_t OFF_TMEM = OFF_BARS + 16;
 constexpr uint32_t SMEM_USED = OFF_TMEM + 16;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
@@ -94,6 +95,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct FacParams {
     int h_qk, h_v, n_seqs;
+    int qk_norm, beta_logits;  // fused q/k L2 normalisation, beta from logits
     int c_lo, c_hi;    // chunks of each sequence to process
     int64_t slot_lo;   // first slot of the launch (blockIdx.x = 0)
     int64_t t_total;
@@ -384,12 +386,12 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
         if (lane < L) {
             const size_t i = (size_t)(t0 + lane) * p.h_v + h;
             rg0 = p.g[i] * kLog2e;
-            rb0 = p.beta[i];
+            rb0 = beta_of(p.beta[i], p.beta_logits);
         }
         if (lane + 32 < L) {
             const size_t i = (size_t)(t0 + lane + 32) * p.h_v + h;
             rg1 = p.g[i] * kLog2e;
-            rb1 = p.beta[i];
+            rb1 = beta_of(p.beta[i], p.beta_logits);
         }
     }
     // X writer: the first V head of the QK head's group; the first chunk of a
@@ -443,8 +445,27 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
         }
     }
     ok = ok && mbar_wait_bounded(bar_mma, 0, kWaitLimit);
+    if (p.qk_norm && ok) {
+        // fused L2 normalisation: thread i takes row i of the [K; Q] tile (both
+        // d_k halves; the order of the sum does not matter), still intact
+        ok = mbar_wait_bounded(bar_tma, 0, kWaitLimit);  // the tile's bytes are visible to this thread
+        float ss = 0.f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                const uint4 wv = *reinterpret_cast<const uint4 *>(sm + OFF_KQ + 16384 * hf + 128 * tid + 16 * ch);
+                const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float lo = __uint_as_float(w4[u] << 16), hi = __uint_as_float(w4[u] & 0xFFFF0000u);
+                    ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+                }
+            }
+        gates[256 + tid] = l2norm_scale(ss);  // rows 0-63: 1 / |k_t|; 64-127: 1 / |q_t|
+    }
     if (!ok) atomicCAS(p.err, 0, (int32_t)GDR_ERR_DEVICE_TIMEOUT);
-    if (!__syncthreads_and(ok)) {  // also publishes the gates
+    if (!__syncthreads_and(ok)) {  // also publishes the gates and the row scales
         // let the tile load land before this CTA's shared memory is released
         if (tid == 0) mbar_wait_bounded(bar_tma, 0, kWaitLimit / 8);
         __syncthreads();
@@ -459,7 +480,8 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
         const int row = 32 * warp + lane, t = row & 63, I = t >> 4, r16 = t & 15;
         const bool is_n = row < 64;
         const float Gt = gates[t];
-        const float w = is_n ? gates[64 + t] : 1.f;
+        // row weight beta_t (N) or 1 (P), times the row's L2 scale with the fused normalisation
+        const float w = (is_n ? gates[64 + t] : 1.f) * (p.qk_norm ? gates[256 + row] : 1.f);
         const int lim = is_n ? t : t + 1;  // keep j < t (N) or j <= t (P)
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
 #pragma unroll
@@ -467,6 +489,10 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
             float v[16];
             tmem_ld16(lane_addr + 16 * J, v);
             if (J > I) continue;
+            if (p.qk_norm) {  // column scales 1 / |k_j|
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] *= gates[256 + 16 * J + e];
+            }
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const int j = 16 * J + e;
@@ -496,6 +522,11 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
             float *eg = reinterpret_cast<float *>(slot_out + fac::OFF_EG);
             eg[lane] = gates[128 + lane];
             eg[lane + 32] = gates[160 + lane];
+            if (p.qk_norm) {  // the row scales for the chunk scan: 1 / |k| (64), then 1 / |q| (64)
+                float *rs = reinterpret_cast<float *>(slot_out + fac::OFF_RK);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) rs[lane + 32 * i] = gates[256 + lane + 32 * i];
+            }
         }
         const int t = tid - 64;
         for (int k = (t >> 3) + 1; k < 8; ++k) {
@@ -554,6 +585,8 @@ cudaError_t launch_factors(const Args &a, float *ws, int32_t *err, cudaStream_t 
     p.h_qk = a.h_qk;
     p.h_v = a.h_v;
     p.n_seqs = a.n_seqs;
+    p.qk_norm = a.qk_norm;
+    p.beta_logits = a.beta_logits;
     p.t_total = a.t_total;
     p.cu_seqlens = a.cu_seqlens;
     p.g = a.g;

@@ -1,7 +1,7 @@
 // Layout of the per-chunk factor workspace shared by the factor kernel (writer)
 // and the tensor-core chunk scan (reader).
 //
-// One slot per (chunk, V head), 16 640 bytes, holding the chunk's
+// One slot per (chunk, V head), 17 152 bytes, holding the chunk's
 // Tw = diag(exp(G_C - G)) (I + N)^-1 diag(beta) and PTw = P (I + N)^-1 diag(beta)
 // (G_C = G of the chunk's last row) ready to be the A operand of a tcgen05 MMA:
 //   [0, 16384)       the operand tile: 128 rows (Tw rows 0-63, then PTw rows
@@ -10,6 +10,9 @@
 //                    above the diagonal
 //   [16384, 16640)   exp(G), 64 fp32 (G: inclusive running sum of g; padding rows
 //                    repeat the last)
+//   [16640, 17152)   with the fused q/k L2 normalisation: 1 / |k_t| then 1 / |q_t|
+//                    (64 fp32 each, |x| = sqrt(sum x^2 + 1e-6)) of the chunk's rows,
+//                    the row scales the chunk scan applies; unwritten otherwise
 // A bulk copy of the tile to a 1024-byte aligned shared-memory address yields
 // the operand as it is.
 //
@@ -34,7 +37,9 @@ constexpr int C = 64;                  // tokens per chunk
 constexpr int TILE_BYTES = 16384;      // 128 rows x 64 fp16
 constexpr int OFF_T = 0;               // bytes
 constexpr int OFF_EG = TILE_BYTES;
-constexpr int SLOT_BYTES = OFF_EG + C * 4;  // 16640, a multiple of 16
+constexpr int OFF_RK = OFF_EG + C * 4;      // row scales 1 / |k_t|, then 1 / |q_t|
+constexpr int GATE_BYTES = 3 * C * 4;       // exp(G), 1 / |k|, 1 / |q|: what the scan copies per chunk
+constexpr int SLOT_BYTES = OFF_EG + GATE_BYTES;  // 17152, a multiple of 16
 static_assert(SLOT_BYTES % 16 == 0, "slots must keep 16-byte alignment");
 
 // Byte offset of the 16-bit element (row r, column j) in a 128-byte-swizzled

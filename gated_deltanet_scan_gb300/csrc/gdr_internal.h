@@ -14,6 +14,13 @@ struct Args {
     int h_qk, h_v, d;        // d = d_k = d_v
     int in_bf16, out_bf16;   // 1 when the tensor is bf16, 0 for fp32
     float scale;
+    int qk_norm;             // GDR_FLAG_QK_L2NORM: rows of q and k scaled by 1 / sqrt(sum x^2 + 1e-6)
+    int beta_logits;         // GDR_FLAG_BETA_LOGITS: beta = sigmoid(beta input)
+    // gated RMSNorm of the outputs (decode epilogue): when norm_z is set, o receives
+    // y = w * o / sqrt(mean(o^2) + norm_eps) * silu(z) instead of o
+    const void *norm_z;      // [rows][H_v][d_v], in_dtype
+    const float *norm_w;     // [d_v]
+    float norm_eps;
     int n_seqs;
     const int32_t *cu_seqlens;  // device; nullptr => sequence s is [s*fixed_len, (s+1)*fixed_len)
     int fixed_len;
@@ -58,6 +65,9 @@ struct TcRun {
 cudaError_t launch_prefill_tc_runs(const Args &a, const TcRun *runs, int n_runs, const float *ws, cudaStream_t s,
                                    bool overlap);
 cudaError_t launch_copy_f32(const float *src, float *dst, size_t n, cudaStream_t s);
+// y = w * o / sqrt(mean(o^2) + eps) * silu(z) for `rows` rows of d values (gdr_norm.cu).
+cudaError_t launch_gated_rmsnorm(int64_t rows, int d, const void *o, int o_bf16, const void *z, int z_bf16,
+                                 const float *w, float eps, void *y, int y_bf16, cudaStream_t s);
 
 // Two-level prefill (gdr_segment.cu): byte offsets of its fp32 scratch inside the
 // workspace, after the factor_bytes of the factor slots and X tiles.

@@ -106,8 +106,10 @@ constexpr uint32_t OFF_S = OFF_OPS + NOP * OP_BYTES;      // [S'_hi | S'_lo]: 12
 constexpr uint32_t OFF_R = OFF_S + 16384;                 // [R | 0]: 64 (token) rows x 64 fp16, MN-major
 constexpr uint32_t OFF_DT = OFF_R + 8192;                 // [D~ | 0]: 64 rows x 64 fp16
 constexpr uint32_t OFF_DT2 = OFF_DT + 8192;               // [D~_hi | D~_lo]: 64 rows x 64 bf16 (MMA3)
-constexpr uint32_t OFF_GATES = OFF_DT2 + 8192;             // exp(G) of two chunks, 64 floats each
-constexpr uint32_t OFF_SMALL = OFF_GATES + 2 * 256;
+// per chunk: exp(G) (64 floats), then, with the fused q/k L2 norm, 1 / |k| and
+// 1 / |q| of its rows (64 each): two chunks' worth
+constexpr uint32_t OFF_GATES = OFF_DT2 + 8192;
+constexpr uint32_t OFF_SMALL = OFF_GATES + 2 * fac::GATE_BYTES;
 constexpr uint32_t SM_BARS = OFF_SMALL;                   // NBARS x uint64
 constexpr uint32_t SM_TMEM = OFF_SMALL + 192;
 constexpr uint32_t SM_ABORT = OFF_SMALL + 200;
@@ -158,6 +160,7 @@ constexpr uint32_t IDESC_Y = idesc_bf16_f32(128, 64, 1, 1);     // MMA3: A MN-ma
 // independent runs side by side (the segments of the two-level scan).
 struct TcParams {
     int h_qk, h_v, n_seqs, n_runs;
+    int qk_norm;  // fused q/k L2 normalisation: rows of [K S; Q S] and of D~ take the slot's row scales
     float scale;
     const int32_t *cu_seqlens;
     const uint8_t *ws;     // factor slots
@@ -171,7 +174,9 @@ struct Ctx {
     uint32_t tmem;
     volatile int *abort_flag;
     __device__ uint32_t bar(int i) const { return sbase + SM_BARS + 8 * i; }
-    __device__ const float *gates(int gb) const { return reinterpret_cast<const float *>(sm + OFF_GATES + 256 * gb); }
+    __device__ const float *gates(int gb) const {
+        return reinterpret_cast<const float *>(sm + OFF_GATES + fac::GATE_BYTES * gb);
+    }
 };
 
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
@@ -275,10 +280,12 @@ __device__ __forceinline__ void issue_op_load(const Ctx &x, int i, const uint8_t
     mbar_arrive_expect_tx(bar, OP_BYTES);
     bulk_load(x.sbase + OFF_OPS + (i % NOP) * OP_BYTES, src, OP_BYTES, bar);
 }
-// A slot's exp(G) (64 floats) into gates ring buffer gb.
-__device__ __forceinline__ void issue_gates_load(const Ctx &x, const uint8_t *slot, int gb) {
-    mbar_arrive_expect_tx(x.bar(B_G_FULL + gb), 256);
-    bulk_load(x.sbase + OFF_GATES + 256 * gb, slot + fac::OFF_EG, 256, x.bar(B_G_FULL + gb));
+// A slot's exp(G) (64 floats; with the fused L2 norm also its row scales) into
+// gates ring buffer gb.
+__device__ __forceinline__ void issue_gates_load(const Ctx &x, const uint8_t *slot, int gb, bool qk_norm) {
+    const uint32_t bytes = qk_norm ? fac::GATE_BYTES : 256u;
+    mbar_arrive_expect_tx(x.bar(B_G_FULL + gb), bytes);
+    bulk_load(x.sbase + OFF_GATES + fac::GATE_BYTES * gb, slot + fac::OFF_EG, bytes, x.bar(B_G_FULL + gb));
 }
 // Operand-ring items: 2 c is the [Tw; PTw] tile of chunk c, 2 c + 1 X_c (only
 // while c + 1 < nchunks).
@@ -326,7 +333,7 @@ __device__ void copy_role(const Ctx &x, const TcParams &p, int64_t t0, int nchun
     // reads only inputs; the workspace is read after that grid has completed
     asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int i = 0; i < NOP; ++i) next_op(i);
-    for (int c = 0; c < nchunks && c < 2; ++c) issue_gates_load(x, fsrc + c * fstride, c);
+    for (int c = 0; c < nchunks && c < 2; ++c) issue_gates_load(x, fsrc + c * fstride, c, p.qk_norm != 0);
     for (int c = 0; c < nchunks && !bad; ++c) {
         if (c >= 1 && c - 1 + NKQ < nchunks) {
             const int kb = (c - 1) % NKQ;
@@ -336,7 +343,7 @@ __device__ void copy_role(const Ctx &x, const TcParams &p, int64_t t0, int nchun
         next_op(2 * c + NOP);
         if (!bad && c + 2 < nchunks) {
             bad = !wait_or_abort(x, x.bar(B_G_EMPTY + (c & 1)), (uint32_t)(c >> 1) & 1u);
-            if (!bad) issue_gates_load(x, fsrc + (c + 2) * fstride, c & 1);
+            if (!bad) issue_gates_load(x, fsrc + (c + 2) * fstride, c & 1, p.qk_norm != 0);
         }
         next_op(2 * c + NOP + 1);
     }
@@ -564,6 +571,8 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, const TcRun &run, in
         if (!bad) bad = !wait_or_abort(x, x.bar(B_KQ_FULL + kb), (uint32_t)(c / NKQ) & 1u);  // V
         if (!bad) bad = !wait_or_abort(x, x.bar(B_G_FULL + gb), (uint32_t)(c >> 1) & 1u);
         const float egt = x.gates(gb)[t];
+        // with the fused L2 norm: this row's scale, 1 / |k_t| (K / T rows) or 1 / |q_t| (Q / PT rows)
+        const float rsc = p.qk_norm ? x.gates(gb)[(low ? 64 : 128) + t] : 1.f;
         // ---- A_c complete: R = V - e^G K S_c ---------------------------------------------
         if (!bad) bad = !wait_or_abort(x, x.bar(B_ACC), par);
         tc_fence_after_sync();
@@ -571,6 +580,10 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, const TcRun &run, in
         {
             float ks[16];
             if (!bad) acc_sum1(lb, TM_ACC + 64 * ab, j0, ks);
+            if (p.qk_norm) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) ks[j] *= rsc;
+            }
             if (low) {
                 if (!bad) {
                     // R = V - e^G K S in fp16
@@ -602,6 +615,12 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, const TcRun &run, in
             if (!bad) acc_prod(lb, TM_D, j0, d);
             if (low) {
                 if (!bad) {
+                    // with the fused L2 norm both products take diag(1 / |k|) D~ (K^T of
+                    // the normalised keys; X holds the raw keys' products)
+                    if (p.qk_norm) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) d[j] *= rsc;
+                    }
                     // D~ in fp16 (MMA_X) and as bf16 hi/lo (MMA3)
                     store_f16_row16(x.sm + OFF_DT, t, j0, d);
                     store_hilo_row16(x.sm + OFF_DT2, t, j0, d);
@@ -759,6 +778,7 @@ cudaError_t launch_prefill_tc_runs(const Args &a, const TcRun *runs, int n_runs,
     p.h_v = a.h_v;
     p.n_seqs = a.n_seqs;
     p.n_runs = n_runs;
+    p.qk_norm = a.qk_norm;
     p.scale = a.scale;
     p.cu_seqlens = a.cu_seqlens;
     p.ws = reinterpret_cast<const uint8_t *>(ws);

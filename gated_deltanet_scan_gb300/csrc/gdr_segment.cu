@@ -43,42 +43,113 @@ __global__ void segment_init_kernel(float4 *__restrict__ phi, float4 *__restrict
     }
 }
 
-// out = phi * in + b for one (sequence, V head) and 32 columns per block; with
-// `save`, `in` is also copied there.  `in` and `out` may be the same array: a
-// block reads its 32 columns of `in` completely before writing them.
-constexpr int CMB_COLS = 32;
-__global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ phi, const float *__restrict__ b,
-                                                      const float *in, float *out, float *save) {
-    __shared__ float xs[D][CMB_COLS];
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned); all of a
+// thread's copies are in flight until cp_async_wait_all.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Every segment's start, for one (sequence, V head) and 16 state columns per
+// block: X_{p+1} = Phi_p X_p + B_p for p = 1 .. P-1 in order.  The columns are
+// independent (X_{p+1}'s columns depend only on the same columns of X_p), so each
+// block walks all steps for its 16 columns with X in shared memory; Phi_{p+1}
+// is copied in (asynchronously, rows padded to 132 floats) while step p
+// computes.  X_1 is the state segment 0 left in `state`: it is saved to
+// xseg[0]; X_p goes to xseg[p-1], and the last, X_P, back to `state`.
+constexpr int CMB_COLS = 16, PHI_LD = D + 4;
+constexpr int CMB_SMEM = (2 * D * PHI_LD + 2 * D * CMB_COLS) * (int)sizeof(float);
+struct CombineParams {
+    int P;
+    size_t seg_stride;  // floats between one segment's matrices and the next's
+    const float *phi, *b;
+    float *state, *xseg;
+};
+__global__ void __launch_bounds__(256) combine_kernel(CombineParams c) {
+    extern __shared__ __align__(16) float csm[];
+    // two Phi buffers [D][PHI_LD], then two X buffers [D][CMB_COLS]
+    auto ph = [&](int i) { return csm + i * D * PHI_LD; };
+    auto xs = [&](int i) { return csm + 2 * D * PHI_LD + i * D * CMB_COLS; };
     const size_t mat = (size_t)blockIdx.x * D * D;
     const int c0 = blockIdx.y * CMB_COLS;
     const int tid = threadIdx.x;
-    for (int i = tid; i < D * CMB_COLS; i += 256) {
-        const int r = i / CMB_COLS, c = i % CMB_COLS;
-        const float x = in[mat + (size_t)r * D + c0 + c];
-        xs[r][c] = x;
-        if (save) save[mat + (size_t)r * D + c0 + c] = x;
-    }
-    __syncthreads();
-    // thread: row r, 16 of the 32 columns
-    const int r = tid >> 1, cc = (tid & 1) * 16;
-    float acc[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) acc[j] = b[mat + (size_t)r * D + c0 + cc + j];
-    const float *pr = phi + mat + (size_t)r * D;
+    auto load_phi = [&](int p, float *dst) {  // Phi_p (p >= 1) into dst
+        const float *src = c.phi + (size_t)(p - 1) * c.seg_stride + mat;
 #pragma unroll 4
-    for (int k = 0; k < D; ++k) {
-        const float a = __ldg(pr + k);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j] = fmaf(a, xs[k][cc + j], acc[j]);
+        for (int i = tid; i < D * D / 4; i += 256) {
+            const int r = i / (D / 4), q4 = i % (D / 4);
+            cp_async16(dst + r * PHI_LD + 4 * q4, src + (size_t)r * D + 4 * q4);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    // X_1 (this block's columns of the state) and Phi_1
+    for (int i = tid; i < D * CMB_COLS / 4; i += 256) {
+        const int r = i / (CMB_COLS / 4), q4 = i % (CMB_COLS / 4);
+        const float4 v = *reinterpret_cast<const float4 *>(c.state + mat + (size_t)r * D + c0 + 4 * q4);
+        reinterpret_cast<float4 *>(xs(0))[i] = v;
+        *reinterpret_cast<float4 *>(c.xseg + mat + (size_t)r * D + c0 + 4 * q4) = v;
     }
+    load_phi(1, ph(0));
+    const int r = tid >> 1, cc = (tid & 1) * 8;  // row r, 8 of the 16 columns
+    for (int p = 1; p < c.P; ++p) {
+        const int cur = (p - 1) & 1;
+        if (p + 1 < c.P) {
+            load_phi(p + 1, ph(cur ^ 1));
+            asm volatile("cp.async.wait_group 1;" ::: "memory");  // Phi_p has landed
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();  // Phi_p and X_p visible to every thread
+        const float *bb = c.b + (size_t)(p - 1) * c.seg_stride + mat + (size_t)r * D + c0 + cc;
+        float acc[8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) out[mat + (size_t)r * D + c0 + cc + j] = acc[j];
+        for (int j = 0; j < 8; j += 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(bb + j);
+            acc[j] = v.x;
+            acc[j + 1] = v.y;
+            acc[j + 2] = v.z;
+            acc[j + 3] = v.w;
+        }
+        const float *pr = ph(cur) + r * PHI_LD;
+        const float *xin = xs(cur);
+#pragma unroll 4
+        for (int k4 = 0; k4 < D / 4; ++k4) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(pr + 4 * k4);
+            const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const float4 x0 = *reinterpret_cast<const float4 *>(xin + (4 * k4 + kk) * CMB_COLS + cc);
+                const float4 x1 = *reinterpret_cast<const float4 *>(xin + (4 * k4 + kk) * CMB_COLS + cc + 4);
+                acc[0] = fmaf(av[kk], x0.x, acc[0]);
+                acc[1] = fmaf(av[kk], x0.y, acc[1]);
+                acc[2] = fmaf(av[kk], x0.z, acc[2]);
+                acc[3] = fmaf(av[kk], x0.w, acc[3]);
+                acc[4] = fmaf(av[kk], x1.x, acc[4]);
+                acc[5] = fmaf(av[kk], x1.y, acc[5]);
+                acc[6] = fmaf(av[kk], x1.z, acc[6]);
+                acc[7] = fmaf(av[kk], x1.w, acc[7]);
+            }
+        }
+        // X_{p+1}: to shared memory for the next step, and to xseg[p] (or the state)
+        float *xo = xs(cur ^ 1) + r * CMB_COLS + cc;
+        *reinterpret_cast<float4 *>(xo) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4 *>(xo + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        float *g = (p == c.P - 1 ? c.state : c.xseg + (size_t)p * c.seg_stride) + mat + (size_t)r * D + c0 + cc;
+        *reinterpret_cast<float4 *>(g) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4 *>(g + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        __syncthreads();  // every thread is done with Phi_p and X_p before they are overwritten
+    }
 }
 
-// o_t = o0_t + X_p^T m_t for the tokens of segments >= 1.  A block covers 32
-// tokens of one chunk (one segment) of one sequence, one V head and 64 of the
-// output columns; X_p's 64 columns and the 32 rows of m sit in shared memory.
+// o_t = o0_t + X_p^T m_t for the tokens of segments >= 1.  A block covers one
+// chunk (64 tokens, one segment) of one sequence and one V head: the 64 x 128
+// tile of (64 x 128) m times (128 x 128) X_p.  Both operands are staged in
+// shared memory by asynchronous copies (m's rows padded to 132 floats); each of
+// the 128 threads keeps an 8-token x 8-column tile of the result in registers
+// and walks the 128 terms four at a time.
 struct FixParams {
     int h_v, n_seqs, P, out_bf16;
     int cuts[9];  // chunk cuts: segment p is chunks [cuts[p], cuts[p+1])
@@ -88,57 +159,88 @@ struct FixParams {
     void *o;
 };
 
-constexpr int FIX_TOK = 32, FIX_COLS = 64;
-__global__ void __launch_bounds__(256) fixup_kernel(FixParams p) {
-    extern __shared__ float fsm[];
-    float *xs = fsm;                    // [D][FIX_COLS]
-    float *ms = fsm + D * FIX_COLS;     // [FIX_TOK][D]
-    const int c = p.cuts[1] + (int)blockIdx.x / 2;     // chunk index within the sequence
-    const int sub = (int)blockIdx.x % 2;               // which 32 tokens of the chunk
+constexpr int FIX_TOK = 64, M_LD = D + 4;
+constexpr int FIX_SMEM = (FIX_TOK * M_LD + D * D) * (int)sizeof(float);
+__global__ void __launch_bounds__(128, 2) fixup_kernel(FixParams p) {
+    extern __shared__ __align__(16) float fsm[];
+    float *ms = fsm;                    // [FIX_TOK][M_LD]
+    float *xs = fsm + FIX_TOK * M_LD;   // [D][D]
+    const int c = p.cuts[1] + (int)blockIdx.x;      // chunk index within the sequence
     const int s = (int)blockIdx.y / p.h_v, h = (int)blockIdx.y % p.h_v;
-    const int col0 = (int)blockIdx.z * FIX_COLS;
-    int seg = 1;
-    while (seg + 1 < p.P && c >= p.cuts[seg + 1]) ++seg;
+    int seg = 1;  // the segment of chunk c (static indices: the cuts stay in the parameter space)
+#pragma unroll
+    for (int q = 2; q < 9; ++q)
+        if (q < p.P && c >= p.cuts[q]) seg = q;
     const int64_t ts = p.cu_seqlens[s], te = p.cu_seqlens[s + 1];
-    const int64_t t0 = ts + (int64_t)c * 64 + FIX_TOK * sub;
+    const int64_t t0 = ts + (int64_t)c * 64;
     if (t0 >= te) return;  // past this sequence's end (or an empty sequence)
     const int ntok = (int)((te - t0) < FIX_TOK ? (te - t0) : FIX_TOK);
     const float *X = p.xseg + (((size_t)(seg - 1) * p.n_seqs + s) * p.h_v + h) * D * D;
     const int tid = threadIdx.x;
-    for (int i = tid; i < D * FIX_COLS / 4; i += 256) {
-        const int r = i / (FIX_COLS / 4), q4 = i % (FIX_COLS / 4);
-        reinterpret_cast<float4 *>(xs)[i] = *reinterpret_cast<const float4 *>(X + (size_t)r * D + col0 + 4 * q4);
-    }
-    for (int i = tid; i < FIX_TOK * D / 4; i += 256) {
-        const int tr = i / (D / 4), q4 = i % (D / 4);
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (tr < ntok) v = *reinterpret_cast<const float4 *>(p.m + ((size_t)(t0 + tr) * p.h_v + h) * D + 4 * q4);
-        reinterpret_cast<float4 *>(ms)[i] = v;
-    }
-    __syncthreads();
-    // thread: token row tr, 8 consecutive columns
-    const int tr = tid >> 3, cc = (tid & 7) * 8;
-    if (tr >= ntok) return;
-    const size_t orow = ((size_t)(t0 + tr) * p.h_v + h) * D + col0 + cc;
-    float acc[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = p.o0[orow + j];
-    const float *mr = ms + tr * D;
 #pragma unroll 4
-    for (int i = 0; i < D; ++i) {
-        const float mi = mr[i];
-        const float *xr = xs + i * FIX_COLS + cc;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = fmaf(mi, xr[j], acc[j]);
+    for (int i = tid; i < D * D / 4; i += 128) cp_async16(xs + 4 * i, X + 4 * (size_t)i);
+#pragma unroll 4
+    for (int i = tid; i < FIX_TOK * (D / 4); i += 128) {
+        const int t = i / (D / 4), q4 = i % (D / 4);
+        if (t < ntok) cp_async16(ms + t * M_LD + 4 * q4, p.m + ((size_t)(t0 + t) * p.h_v + h) * D + 4 * q4);
     }
-    if (p.out_bf16) {
-        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.o) + orow;
+    cp_async_wait_all();
+    __syncthreads();
+    const int tg = tid >> 4, cg = tid & 15;  // tokens 8 tg .. + 7, columns 8 cg .. + 7
+    float acc[8][8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) dst[j] = __float2bfloat16_rn(acc[j]);
-    } else {
-        float *dst = reinterpret_cast<float *>(p.o) + orow;
+    for (int a = 0; a < 8; ++a)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) dst[j] = acc[j];
+        for (int j = 0; j < 8; ++j) acc[a][j] = 0.f;
+#pragma unroll 1
+    for (int i4 = 0; i4 < D / 4; ++i4) {
+        float xv[4][8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 x0 = *reinterpret_cast<const float4 *>(xs + (4 * i4 + q) * D + 8 * cg);
+            const float4 x1 = *reinterpret_cast<const float4 *>(xs + (4 * i4 + q) * D + 8 * cg + 4);
+            xv[q][0] = x0.x;
+            xv[q][1] = x0.y;
+            xv[q][2] = x0.z;
+            xv[q][3] = x0.w;
+            xv[q][4] = x1.x;
+            xv[q][5] = x1.y;
+            xv[q][6] = x1.z;
+            xv[q][7] = x1.w;
+        }
+#pragma unroll
+        for (int a = 0; a < 8; ++a) {
+            const float4 m4 = *reinterpret_cast<const float4 *>(ms + (8 * tg + a) * M_LD + 4 * i4);
+            const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[a][j] = fmaf(mv[q], xv[q][j], acc[a][j]);
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+        const int t = 8 * tg + a;
+        if (t >= ntok) break;
+        const size_t orow = ((size_t)(t0 + t) * p.h_v + h) * D + 8 * cg;
+        const float4 b0 = *reinterpret_cast<const float4 *>(p.o0 + orow);
+        const float4 b1 = *reinterpret_cast<const float4 *>(p.o0 + orow + 4);
+        const float y[8] = {b0.x + acc[a][0], b0.y + acc[a][1], b0.z + acc[a][2], b0.w + acc[a][3],
+                            b1.x + acc[a][4], b1.y + acc[a][5], b1.z + acc[a][6], b1.w + acc[a][7]};
+        if (p.out_bf16) {
+            uint4 pk;
+            __nv_bfloat162 v0 = __floats2bfloat162_rn(y[0], y[1]), v1 = __floats2bfloat162_rn(y[2], y[3]),
+                            v2 = __floats2bfloat162_rn(y[4], y[5]), v3 = __floats2bfloat162_rn(y[6], y[7]);
+            pk.x = *reinterpret_cast<uint32_t *>(&v0);
+            pk.y = *reinterpret_cast<uint32_t *>(&v1);
+            pk.z = *reinterpret_cast<uint32_t *>(&v2);
+            pk.w = *reinterpret_cast<uint32_t *>(&v3);
+            *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + orow) = pk;
+        } else {
+            float *dst = reinterpret_cast<float *>(p.o) + orow;
+            *reinterpret_cast<float4 *>(dst) = make_float4(y[0], y[1], y[2], y[3]);
+            *reinterpret_cast<float4 *>(dst + 4) = make_float4(y[4], y[5], y[6], y[7]);
+        }
     }
 }
 
@@ -170,6 +272,17 @@ cudaError_t launch_segmented(const Args &a, int P, uint8_t *ws, const SegLayout 
     float *m = reinterpret_cast<float *>(ws + L.m);
     const size_t per_seg = (size_t)a.n_seqs * a.h_v;  // matrices per segment
     const size_t mat_floats = (size_t)D * D;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return e0;
+    if (configured_device != dev) {
+        e0 = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CMB_SMEM);
+        if (e0 == cudaSuccess)
+            e0 = cudaFuncSetAttribute(fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FIX_SMEM);
+        if (e0 != cudaSuccess) return e0;
+        configured_device = dev;
+    }
     // 1. start states of the transition (I) and offset (0) runs
     {
         const size_t n4 = (size_t)(P - 1) * per_seg * (mat_floats / 4);
@@ -193,14 +306,16 @@ cudaError_t launch_segmented(const Args &a, int P, uint8_t *ws, const SegLayout 
     }
     e = launch_prefill_tc_runs(a, runs, n_runs, reinterpret_cast<float *>(ws), s, true);
     if (e != cudaSuccess) return e;
-    // 4. segment starts, in order: X_1 is the state segment 0 left in `state`
-    for (int p = 1; p < P; ++p) {
-        const float *in = p == 1 ? a.state : xseg + (size_t)(p - 1) * per_seg * mat_floats;
-        float *out = p == P - 1 ? a.state : xseg + (size_t)p * per_seg * mat_floats;
-        float *save = p == 1 ? xseg : nullptr;
-        combine_kernel<<<dim3((unsigned)per_seg, D / CMB_COLS), 256, 0, s>>>(
-            phi + (size_t)(p - 1) * per_seg * mat_floats, bb + (size_t)(p - 1) * per_seg * mat_floats, in, out,
-            save);
+    // 4. every segment's start (X_1 is the state segment 0 left in `state`)
+    {
+        CombineParams cp;
+        cp.P = P;
+        cp.seg_stride = per_seg * mat_floats;
+        cp.phi = phi;
+        cp.b = bb;
+        cp.state = a.state;
+        cp.xseg = xseg;
+        combine_kernel<<<dim3((unsigned)per_seg, D / CMB_COLS), 256, CMB_SMEM, s>>>(cp);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -218,17 +333,7 @@ cudaError_t launch_segmented(const Args &a, int P, uint8_t *ws, const SegLayout 
     fp.o = a.o;
     const int fix_chunks = (int)(n_ch - fp.cuts[1]);
     if (fix_chunks <= 0) return cudaSuccess;
-    const int smem = (D * FIX_COLS + FIX_TOK * D) * (int)sizeof(float);
-    static int configured_device = -1;
-    int dev = 0;
-    e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (configured_device != dev) {
-        e = cudaFuncSetAttribute(fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        configured_device = dev;
-    }
-    fixup_kernel<<<dim3((unsigned)fix_chunks * 2, (unsigned)per_seg, D / FIX_COLS), 256, smem, s>>>(fp);
+    fixup_kernel<<<dim3((unsigned)fix_chunks, (unsigned)per_seg), 128, FIX_SMEM, s>>>(fp);
     return cudaGetLastError();
 }
 

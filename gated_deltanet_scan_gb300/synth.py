@@ -208,9 +208,19 @@ def _unit_rows(x: np.ndarray) -> np.ndarray:
     return x / np.maximum(n, 1e-300)
 
 
-def _draw_qkv(st: Dict[str, Stream], t: int, h_qk: int, h_v: int, d_k: int, d_v: int, io: str):
-    q = _unit_rows(st["q"].normal(t * h_qk * d_k).reshape(t, h_qk, d_k))
-    k = _unit_rows(st["k"].normal(t * h_qk * d_k).reshape(t, h_qk, d_k))
+def _draw_qkv(st: Dict[str, Stream], t: int, h_qk: int, h_v: int, d_k: int, d_v: int, io: str,
+              qk_raw_scale=None):
+    if qk_raw_scale is None:
+        q = _unit_rows(st["q"].normal(t * h_qk * d_k).reshape(t, h_qk, d_k))
+        k = _unit_rows(st["k"].normal(t * h_qk * d_k).reshape(t, h_qk, d_k))
+    else:
+        # raw rows for the fused normalisation: N(0, 1) times a per-row factor drawn
+        # log-uniformly in [lo, hi]
+        lo, hi = np.log(qk_raw_scale[0]), np.log(qk_raw_scale[1])
+        fq = np.exp(lo + (hi - lo) * st["qscale"].uniform(t * h_qk)).reshape(t, h_qk, 1)
+        fk = np.exp(lo + (hi - lo) * st["kscale"].uniform(t * h_qk)).reshape(t, h_qk, 1)
+        q = st["q"].normal(t * h_qk * d_k).reshape(t, h_qk, d_k) * fq
+        k = st["k"].normal(t * h_qk * d_k).reshape(t, h_qk, d_k) * fk
     v = st["v"].normal(t * h_v * d_v).reshape(t, h_v, d_v)
     out = {}
     for name, x in (("q", q), ("k", k), ("v", v)):
@@ -241,24 +251,31 @@ def make_workload(
     state_std: float = 0.0,
     tag: str = "",
     n_states: Optional[int] = None,
+    qk_raw_scale=None,
+    beta_logits: bool = False,
 ) -> Workload:
     """Draw one packed batch.
 
     q, k ~ N(0, 1) then L2-normalised per (token, head) in fp64 before rounding
     to the io type; v ~ N(0, 1); log alpha ~ U[g_range] (or fixed);
     beta = sigmoid(N(0, 1)); initial state ~ N(0, state_std) (std, not variance).
+    With ``qk_raw_scale = (lo, hi)`` q and k are left unnormalised, each row
+    scaled by a factor log-uniform in [lo, hi] (inputs for the fused
+    normalisation); with ``beta_logits`` the beta array holds the N(0, 1) logits
+    themselves.
     """
     cu = np.zeros(len(seqlens) + 1, dtype=np.int32)
     cu[1:] = np.cumsum(np.asarray(seqlens, dtype=np.int64))
     t = int(cu[-1])
-    st = {n: Stream(seed, tag + n) for n in ("q", "k", "v", "g", "beta", "state")}
-    qkv = _draw_qkv(st, t, h_qk, h_v, d, d, io)
+    st = {n: Stream(seed, tag + n) for n in ("q", "k", "v", "g", "beta", "state", "qscale", "kscale")}
+    qkv = _draw_qkv(st, t, h_qk, h_v, d, d, io, qk_raw_scale)
     if g_fixed is not None:
         g = np.full((t, h_v), g_fixed, dtype=np.float32)
     else:
         lo, hi = g_range
         g = (lo + (hi - lo) * st["g"].uniform(t * h_v)).astype(np.float32).reshape(t, h_v)
-    beta = _sigmoid(st["beta"].normal(t * h_v)).astype(np.float32).reshape(t, h_v)
+    logits = st["beta"].normal(t * h_v)
+    beta = (logits if beta_logits else _sigmoid(logits)).astype(np.float32).reshape(t, h_v)
     n = len(seqlens) if n_states is None else n_states
     if state_std > 0.0:
         s0 = (state_std * st["state"].normal(n * h_v * d * d)).astype(np.float32)

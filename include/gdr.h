@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define GDR_ABI_VERSION 7
+#define GDR_ABI_VERSION 8
 
 /* Same object as cudaStream_t; declared here so callers need no CUDA header. */
 typedef struct CUstream_st *gdr_stream_t;
@@ -76,7 +76,26 @@ typedef struct gdr_dims {
     int32_t in_dtype;  /* gdr_dtype of q, k, v */
     int32_t out_dtype; /* gdr_dtype of o */
     float scale;       /* multiplies every output; 1.0 reproduces o_t = S_t^T q_t */
+    int32_t flags;     /* GDR_FLAG_* below, or 0 */
 } gdr_dims;
+
+/*
+ * Steps on either side of the rule, fused into every kernel (gdr_dims.flags):
+ *   GDR_FLAG_QK_L2NORM    q and k are passed raw; every (token, QK head) row x is
+ *                         used as x / sqrt(sum_i x_i^2 + 1e-6).  The workloads of
+ *                         the pages feed L2-normalised q and k to the rule; the
+ *                         pages give no epsilon for it (1e-6 inside the square
+ *                         root is this library's reading).  The kernels apply it
+ *                         as per-row scales of the exact bf16/fp32 products, in
+ *                         fp32, so the normalised values are never rounded to the
+ *                         input type.
+ *   GDR_FLAG_BETA_LOGITS  beta holds logits b; the rule uses beta = 1 / (1 + exp(-b))
+ *                         (the workloads draw beta = sigmoid(N(0, 1))).
+ * The gated RMSNorm after the rule is gdr_gated_rmsnorm (and is fused into
+ * gdr_decode_step_gated).  No flag changes a layout or a size.
+ */
+#define GDR_FLAG_QK_L2NORM 1
+#define GDR_FLAG_BETA_LOGITS 2
 
 /* GDR_ABI_VERSION of the loaded library. */
 int32_t gdr_abi_version(void);
@@ -87,12 +106,12 @@ const char *gdr_status_string(gdr_status status);
 /*
  * Bytes of device workspace gdr_prefill_chunked needs for this problem: 0 when
  * the CUDA-core path runs (or for an empty problem), otherwise, for each of
- * P = ceil(t_total / 64) + n_seqs chunk positions, one 16,640-byte slot of
- * per-chunk factors per V head (T and P T as an fp16 MMA operand tile, and the
- * chunk's exp(G)), then, from the next 1 KiB boundary, one 16 KiB fp16 tile
+ * P = ceil(t_total / 64) + n_seqs chunk positions, one 17,152-byte slot of
+ * per-chunk factors per V head (T and P T as an fp16 MMA operand tile, the
+ * chunk's exp(G), and room for the row scales of the fused q/k L2 norm), then, from the next 1 KiB boundary, one 16 KiB fp16 tile
  * per QK head of X = [K; Q]_c K_{c-1}^T (the next chunk's keys and queries
  * against this chunk's keys), rounded up to 256 bytes:
- * roundup(roundup(P * h_v * 16640, 1024) + P * h_qk * 16384, 256).
+ * roundup(roundup(P * h_v * 17152, 1024) + P * h_qk * 16384, 256).
  * Host-only, never fails (invalid dims: 0).
  */
 size_t gdr_prefill_workspace_bytes(const gdr_dims *dims, int32_t n_seqs, int64_t t_total);
@@ -162,10 +181,10 @@ gdr_status gdr_prefill_chunked(const gdr_dims *dims, int32_t n_seqs, const int32
  * gdr_prefill_static_workspace_capacity(), 64 MiB), whose device address is
  * looked up on every call.  Problems whose gdr_prefill_workspace_bytes()
  * exceed it return GDR_ERR_UNSUPPORTED before anything is launched.  With
- * Qwen3.5-9B heads (16 QK, 32 V) one chunk position takes 794,624 bytes, so
- * the array holds 84 positions: one sequence of up to 5,312 tokens, and one
- * position less per further sequence (two sequences: 5,248 tokens in all;
- * eight: 4,864).  All calls on a device share that array, so calls on
+ * Qwen3.5-9B heads (16 QK, 32 V) one chunk position takes 811,008 bytes, so
+ * the array holds 82 positions: one sequence of up to 5,184 tokens, and one
+ * position less per further sequence (two sequences: 5,120 tokens in all;
+ * eight: 4,736).  All calls on a device share that array, so calls on
  * different streams must not overlap (order them on one stream, or
  * synchronise); everything else, arguments and results, is as in
  * gdr_prefill_chunked.
@@ -275,6 +294,36 @@ gdr_status gdr_decode_step(const gdr_dims *dims, int32_t batch, const void *q, c
 gdr_status gdr_decode_step_overlapped(const gdr_dims *dims, int32_t batch, const void *q, const void *k,
                                       const void *v, const float *g, const float *beta, float *state,
                                       void *o, gdr_stream_t stream);
+
+/*
+ * gdr_decode_step with the gated RMSNorm after the rule fused into it: instead of
+ * o, y = weight * o / sqrt(mean(o^2) + eps) * silu(z) is written for every
+ * (sequence, V head) row of d_v outputs (the norm described at
+ * gdr_gated_rmsnorm).  z [batch][H_v][d_v] in in_dtype, weight [d_v] fp32, y
+ * [batch][H_v][d_v] in out_dtype; o itself is not stored.  Arguments and errors
+ * otherwise as gdr_decode_step (GDR_ERR_INVALID_ARG also for a null or
+ * misaligned z or weight, or a negative eps).
+ */
+gdr_status gdr_decode_step_gated(const gdr_dims *dims, int32_t batch, const void *q, const void *k, const void *v,
+                                 const float *g, const float *beta, float *state, const void *z, const float *weight,
+                                 float eps, void *y, gdr_stream_t stream);
+
+/*
+ * Gated RMSNorm of the rule's outputs, the step right after the rule: for each
+ * of n_rows rows of d_v values (a (token, V head) row of o),
+ *     y = weight * o / sqrt(mean(o^2) + eps) * silu(z),   silu(z) = z / (1 + exp(-z)),
+ * one weight per channel.  The Qwen3.5-9B NPU model card ("fp16 precision of the
+ * DeltaNet output") has a gated RMSNorm right after the rule; the Candle PR's
+ * bug log ("Bug 7") gives its epsilon, 1e-6.  The form of the gate, silu(z), is
+ * not on the pages: it is this library's reading.
+ *   o      [n_rows][d_v] in dims->out_dtype (as gdr_prefill_chunked / gdr_verify_block wrote it)
+ *   z      [n_rows][d_v] in dims->in_dtype
+ *   weight [d_v] fp32;  y [n_rows][d_v] in dims->out_dtype (may be o)
+ * One read of o and z and one write of y (HBM-bound).  GDR_ERR_INVALID_ARG for a
+ * null or misaligned pointer, a negative n_rows or eps.
+ */
+gdr_status gdr_gated_rmsnorm(const gdr_dims *dims, int64_t n_rows, const void *o, const void *z, const float *weight,
+                             float eps, void *y, gdr_stream_t stream);
 
 /*
  * Speculative-verify block: n_tok <= 16 draft tokens per sequence in one pass.

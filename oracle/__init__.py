@@ -6,8 +6,10 @@ no CPU fallback.
 
 The arithmetic lives in ``gdr_oracle.c`` (plain C, fp64, one token at a time,
 in the order of the per-token Loop on the Qwen3.5-9B NPU model card, section
-"How it works").  This module compiles it with gcc on first use and marshals
-numpy arrays to it; it adds no arithmetic of its own.
+"How it works"; and the plain row-wise steps on either side of the rule: q/k
+L2 normalisation, beta from its logit, the gated RMSNorm of the outputs).
+This module compiles it with gcc on first use and marshals numpy arrays to it;
+it adds no arithmetic of its own.
 """
 
 from __future__ import annotations
@@ -49,6 +51,12 @@ def _bind(path: str):
         dp, dp, dp, dp, dp, ctypes.c_double, dp, dp, ctypes.c_int,
     ]
     f.restype = ctypes.c_int
+    lib.oracle_l2norm_rows.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_double, dp, dp]
+    lib.oracle_l2norm_rows.restype = ctypes.c_int
+    lib.oracle_sigmoid.argtypes = [ctypes.c_int64, dp, dp]
+    lib.oracle_sigmoid.restype = ctypes.c_int
+    lib.oracle_gated_rmsnorm.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_double, dp, dp, dp, dp]
+    lib.oracle_gated_rmsnorm.restype = ctypes.c_int
     return lib
 
 
@@ -132,3 +140,53 @@ def gdr_sequential(
 def run_workload(w, threads: Optional[int] = None, scale: float = 1.0):
     """The oracle on a ``synth.Workload`` (its exact input values widened to fp64)."""
     return gdr_sequential(w.cu_seqlens, w.q, w.k, w.v, w.g, w.beta, w.state0, scale, threads)
+
+
+# --- steps on either side of the rule (row-wise, fp64) ------------------------------
+
+L2NORM_EPS = 1e-6   # reading: inside the square root (the pages give no eps for it)
+RMSNORM_EPS = 1e-6  # the norm epsilon named in the Candle PR's bug log ("Bug 7")
+
+
+def l2norm_rows(x, eps: float = L2NORM_EPS) -> np.ndarray:
+    """x / sqrt(sum x^2 + eps) over the last axis."""
+    a = _f64(x)
+    d = a.shape[-1]
+    y = np.empty_like(a)
+    if _load().oracle_l2norm_rows(a.size // d, d, float(eps), _ptr(a), _ptr(y)) != 0:
+        raise ValueError("oracle_l2norm_rows rejected its arguments")
+    return y
+
+
+def sigmoid(b) -> np.ndarray:
+    a = _f64(b)
+    y = np.empty_like(a)
+    if _load().oracle_sigmoid(a.size, _ptr(a), _ptr(y)) != 0:
+        raise ValueError("oracle_sigmoid rejected its arguments")
+    return y
+
+
+def gated_rmsnorm(o, z, w, eps: float = RMSNORM_EPS) -> np.ndarray:
+    """w * o / sqrt(mean(o^2) + eps) * silu(z) over the last axis (w: one weight per channel)."""
+    a, zz, ww = _f64(o), _f64(z), _f64(w)
+    d = a.shape[-1]
+    assert zz.shape == a.shape and ww.shape == (d,)
+    y = np.empty_like(a)
+    if _load().oracle_gated_rmsnorm(a.size // d, d, float(eps), _ptr(a), _ptr(zz), _ptr(ww), _ptr(y)) != 0:
+        raise ValueError("oracle_gated_rmsnorm rejected its arguments")
+    return y
+
+
+def gdr_fused(cu_seqlens, q_raw, k_raw, v, g, beta_or_logits, state0, *, qk_l2norm: bool, beta_logits: bool,
+              z=None, norm_weight=None, scale: float = 1.0, threads: Optional[int] = None):
+    """The rule with its steps on either side, in order: q and k L2-normalised
+    (when qk_l2norm), beta = sigmoid(logit) (when beta_logits), the recurrence,
+    then (when z is given) the gated RMSNorm of every output row.  Returns
+    (o or y, final state)."""
+    q = l2norm_rows(q_raw) if qk_l2norm else _f64(q_raw)
+    k = l2norm_rows(k_raw) if qk_l2norm else _f64(k_raw)
+    beta = sigmoid(beta_or_logits) if beta_logits else _f64(beta_or_logits)
+    o, s = gdr_sequential(cu_seqlens, q, k, v, g, beta, state0, scale, threads)
+    if z is not None:
+        o = gated_rmsnorm(o, z, norm_weight)
+    return o, s

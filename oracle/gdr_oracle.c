@@ -31,8 +31,24 @@
  *     g, beta [T_total][H_v]          state [n_seqs][H_v][d_k][d_v]  (in: S0, out: S_T)
  * Every array is double; callers widen the exact fp32/bf16 values.
  *
+ * The steps on either side of the rule (the fused pre- and post-processing
+ * of the library's GDR_FLAG_* options) are here too, each a plain loop:
+ *   oracle_l2norm_rows      x / sqrt(sum x^2 + eps) per row (q and k before the
+ *                           rule; the pages name the normalisation, not its eps:
+ *                           eps = 1e-6 inside the square root is the reading taken)
+ *   oracle_sigmoid          beta = 1 / (1 + exp(-b)) (beta from its logit, as the
+ *                           workloads draw it: beta = sigmoid(N(0, 1)))
+ *   oracle_gated_rmsnorm    y = w * o / sqrt(mean(o^2) + eps) * silu(z) per row of
+ *                           d_v, eps = 1e-6 (the RMSNorm right after the rule on
+ *                           the NPU model card, "fp16 precision of the DeltaNet
+ *                           output", with the 1e-6 epsilon of the Candle PR's bug
+ *                           log, "Bug 7"); the gate's form silu(z) = z sigmoid(z)
+ *                           is a reading: the pages do not give it.
+ *
  * Parity pins: see tests/test_oracle_pins.py (closed forms, exact rational
- * brute force, invariants).  Nothing in this file is "parity unpinned".
+ * brute force, invariants).  The recurrence and both norms are pinned; the
+ * output gate's form (silu) is "parity unpinned" against the pages, which do
+ * not state it: only its arithmetic is pinned (closed forms of silu).
  */
 #include <math.h>
 #include <pthread.h>
@@ -160,5 +176,52 @@ int oracle_gdr_sequential(int n_seqs, const int64_t *cu_seqlens, int h_qk, int h
         free(th);
     }
     pthread_mutex_destroy(&J.lock);
+    return 0;
+}
+
+/* ---- steps on either side of the rule ------------------------------------------- */
+
+/* y[r] = x[r] / sqrt(sum_i x[r][i]^2 + eps) for n rows of d values (y may be x). */
+int oracle_l2norm_rows(int64_t n, int d, double eps, const double *x, double *y) {
+    if (n < 0 || d <= 0 || !(eps >= 0.0)) return -1;
+    for (int64_t r = 0; r < n; ++r) {
+        const double *xr = x + (size_t)r * d;
+        double ss = 0.0;
+        for (int i = 0; i < d; ++i) ss += xr[i] * xr[i];
+        const double inv = 1.0 / sqrt(ss + eps);
+        double *yr = y + (size_t)r * d;
+        for (int i = 0; i < d; ++i) yr[i] = xr[i] * inv;
+    }
+    return 0;
+}
+
+/* beta[i] = 1 / (1 + exp(-b[i])) for n values. */
+int oracle_sigmoid(int64_t n, const double *b, double *beta) {
+    if (n < 0) return -1;
+    for (int64_t i = 0; i < n; ++i) beta[i] = 1.0 / (1.0 + exp(-b[i]));
+    return 0;
+}
+
+/*
+ * y[r][j] = w[j] * o[r][j] / sqrt(mean_i o[r][i]^2 + eps) * silu(z[r][j]) for n rows
+ * of d values, silu(z) = z / (1 + exp(-z)).  w has d entries (one weight per
+ * channel, shared by every row).
+ */
+int oracle_gated_rmsnorm(int64_t n, int d, double eps, const double *o, const double *z, const double *w,
+                         double *y) {
+    if (n < 0 || d <= 0 || !(eps >= 0.0)) return -1;
+    for (int64_t r = 0; r < n; ++r) {
+        const double *orow = o + (size_t)r * d;
+        const double *zrow = z + (size_t)r * d;
+        double ss = 0.0;
+        for (int i = 0; i < d; ++i) ss += orow[i] * orow[i];
+        const double inv = 1.0 / sqrt(ss / d + eps);
+        double *yr = y + (size_t)r * d;
+        for (int j = 0; j < d; ++j) {
+            const double zz = zrow[j];
+            const double silu = zz / (1.0 + exp(-zz));
+            yr[j] = w[j] * orow[j] * inv * silu;
+        }
+    }
     return 0;
 }

@@ -91,11 +91,11 @@ def test_prefill_rejects_bad_pointers_and_counts(L):
 
 def test_prefill_workspace_size_and_checks(L):
     d = dims()
-    # one 16,640-byte slot per (chunk position, V head), positions = ceil(T / 64) + n_seqs,
+    # one 17,152-byte slot per (chunk position, V head), positions = ceil(T / 64) + n_seqs,
     # then from the next 1 KiB boundary one 16 KiB X tile per (position, QK head)
     need = L.gdr_prefill_workspace_bytes(ctypes.byref(d), 3, 1000)
     slots = (1000 + 63) // 64 + 3
-    x_off = (slots * 32 * 16640 + 1023) // 1024 * 1024
+    x_off = (slots * 32 * 17152 + 1023) // 1024 * 1024
     assert need == (x_off + slots * 16 * 16384 + 255) // 256 * 256
     assert L.gdr_prefill_workspace_bytes(ctypes.byref(d), 0, 0) == 0
     assert L.gdr_prefill_workspace_bytes(ctypes.byref(dims(in_dtype=gdr.GDR_F32)), 3, 1000) == 0
@@ -200,3 +200,20 @@ def test_segmented_workspace_size_and_checks(L):
     # without a GPU the hint is 1 (no SMs to spread segments over); invalid dims: 1
     assert L.gdr_prefill_segments_hint(None, 1, 16384) == 1
     assert L.gdr_prefill_segments_hint(ctypes.byref(dims(chunk=16)), 1, 16384) == 1
+
+
+def test_flags_and_gated_rmsnorm_checks(L):
+    """Unknown flag bits and bad norm arguments are rejected on the host."""
+    assert L.gdr_decode_step(ctypes.byref(dims(flags=4)), 1, A, A, A, A, A, A, A, None) == gdr.GDR_ERR_INVALID_ARG
+    ok = dims(flags=gdr.GDR_FLAG_QK_L2NORM | gdr.GDR_FLAG_BETA_LOGITS)
+    assert L.gdr_prefill_workspace_bytes(ctypes.byref(ok), 1, 1000) == L.gdr_prefill_workspace_bytes(
+        ctypes.byref(dims()), 1, 1000)  # flags change no size
+    nrm = L.gdr_gated_rmsnorm
+    assert nrm(ctypes.byref(dims()), 0, A, A, A, 1e-6, A, None) == gdr.GDR_OK
+    assert nrm(ctypes.byref(dims()), -1, A, A, A, 1e-6, A, None) == gdr.GDR_ERR_INVALID_ARG
+    assert nrm(ctypes.byref(dims()), 5, A, A, A, -1.0, A, None) == gdr.GDR_ERR_INVALID_ARG
+    assert nrm(ctypes.byref(dims()), 5, MISALIGNED, A, A, 1e-6, A, None) == gdr.GDR_ERR_INVALID_ARG
+    assert nrm(ctypes.byref(dims()), 5, A, None, A, 1e-6, A, None) == gdr.GDR_ERR_INVALID_ARG
+    gated = L.gdr_decode_step_gated
+    assert gated(ctypes.byref(dims()), 1, A, A, A, A, A, A, None, A, 1e-6, A, None) == gdr.GDR_ERR_INVALID_ARG
+    assert gated(ctypes.byref(dims()), 1, A, A, A, A, A, A, A, MISALIGNED, 1e-6, A, None) == gdr.GDR_ERR_INVALID_ARG

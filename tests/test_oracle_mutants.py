@@ -45,6 +45,16 @@ MUTANTS = {
         ("        /* o_t <- scale S^T q_t */\n", "        continue;\n        readout: ;\n"),
         ("        for (int j = 0; j < dv; ++j) ot[j] *= J->scale;\n", "        for (int j = 0; j < dv; ++j) ot[j] *= J->scale;\n        goto back;\n"),
     ],
+    # L2 norm: epsilon outside the square root
+    "l2norm_eps_outside": [("const double inv = 1.0 / sqrt(ss + eps);", "const double inv = 1.0 / (sqrt(ss) + eps);")],
+    # RMSNorm: sum of squares instead of their mean
+    "rmsnorm_sum_not_mean": [("const double inv = 1.0 / sqrt(ss / d + eps);", "const double inv = 1.0 / sqrt(ss + eps);")],
+    # gate: sigmoid(z) instead of silu(z)
+    "gate_sigmoid_not_silu": [("const double silu = zz / (1.0 + exp(-zz));", "const double silu = 1.0 / (1.0 + exp(-zz));")],
+    # norm weight dropped
+    "rmsnorm_no_weight": [("yr[j] = w[j] * orow[j] * inv * silu;", "yr[j] = orow[j] * inv * silu;")],
+    # beta logit with the wrong sign
+    "sigmoid_sign": [("beta[i] = 1.0 / (1.0 + exp(-b[i]));", "beta[i] = 1.0 / (1.0 + exp(b[i]));")],
 }
 
 PIN_CASES = [
@@ -60,6 +70,9 @@ PIN_CASES = [
     pins.test_qk_head_shared_by_contiguous_pair_of_v_heads,
     pins.test_contraction_bound_per_step,
     lambda: pins.test_chunk_forms_match_sequential(16, 40),
+    pins.test_l2norm_rows_closed_forms,
+    pins.test_sigmoid_closed_forms,
+    pins.test_gated_rmsnorm_by_hand_and_invariants,
 ]
 
 

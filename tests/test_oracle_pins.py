@@ -476,3 +476,85 @@ def test_segment_composition_is_pinned_by_the_oracle_too():
     assert np.linalg.norm(bad_t[1] - S) > 1e-6 * np.linalg.norm(S)
     bad_f = segment_compose(q, k, v, g, beta, S0, 64, P, run=lambda *a: _single(*a), mutate="no_fixup")
     assert np.max(np.abs(bad_f[0] - o)) > 1e-6 * np.sqrt(np.mean(o * o))
+
+
+# --- steps on either side of the rule (q/k L2 norm, beta from logits, gated RMSNorm) ---
+
+
+def test_l2norm_rows_closed_forms():
+    """(3, 4) -> (3, 4) / sqrt(25 + 1e-6); a zero row stays zero; every row of
+    random input comes out with unit norm up to the epsilon; positive scaling of a
+    row does not change it (up to the epsilon)."""
+    y = oracle.l2norm_rows(np.array([[3.0, 4.0], [0.0, 0.0]]))
+    assert np.allclose(y[0], np.array([3.0, 4.0]) / np.sqrt(25.0 + 1e-6), rtol=0, atol=1e-15)
+    assert np.all(y[1] == 0.0)
+    r = _rng(501)
+    x = r.standard_normal((40, 128)) * r.uniform(0.1, 10.0, (40, 1))
+    y = oracle.l2norm_rows(x)
+    n2 = np.sum(x * x, axis=1)
+    assert np.allclose(np.linalg.norm(y, axis=1), np.sqrt(n2 / (n2 + 1e-6)), rtol=1e-14)
+    assert np.allclose(oracle.l2norm_rows(7.5 * x), y, rtol=1e-7, atol=0)
+    assert np.allclose(oracle.l2norm_rows(x, eps=0.0), x / np.sqrt(n2)[:, None], rtol=1e-14)
+
+
+def test_sigmoid_closed_forms():
+    b = np.array([0.0, np.log(3.0), -np.log(3.0), 30.0, -30.0])
+    s = oracle.sigmoid(b)
+    assert s[0] == 0.5 and abs(s[1] - 0.75) < 1e-15 and abs(s[2] - 0.25) < 1e-15
+    r = _rng(502).standard_normal(100)
+    assert np.allclose(oracle.sigmoid(r) + oracle.sigmoid(-r), 1.0, rtol=0, atol=1e-15)
+
+
+def test_gated_rmsnorm_by_hand_and_invariants():
+    """Row (1, -1, 1, -1) has mean square 1: y_j = w_j o_j silu(z_j) / sqrt(1 + eps),
+    with silu(z) = z / (1 + e^-z) written out here for z = 0, 1, 2, -3.  The norm is
+    invariant to scaling o (up to the epsilon), linear in the weights, zero where
+    z = 0, and silu(z) - silu(-z) = z."""
+    o = np.array([[1.0, -1.0, 1.0, -1.0]])
+    z = np.array([[0.0, 1.0, 2.0, -3.0]])
+    w = np.array([1.0, 2.0, 3.0, 4.0])
+    silu = np.array([0.0, 1.0 / (1.0 + np.exp(-1.0)), 2.0 / (1.0 + np.exp(-2.0)), -3.0 / (1.0 + np.exp(3.0))])
+    want = w * o[0] * silu / np.sqrt(1.0 + 1e-6)
+    assert np.allclose(oracle.gated_rmsnorm(o, z, w)[0], want, rtol=1e-15, atol=0)
+    r = _rng(503)
+    o = r.standard_normal((20, 128))
+    z = r.standard_normal((20, 128))
+    w = r.uniform(0.5, 1.5, 128)
+    y = oracle.gated_rmsnorm(o, z, w)
+    assert np.allclose(oracle.gated_rmsnorm(4.0 * o, z, w), y, rtol=1e-6)
+    assert np.allclose(oracle.gated_rmsnorm(o, z, 2.0 * w), 2.0 * y, rtol=1e-15)
+    assert np.all(oracle.gated_rmsnorm(o, np.zeros_like(z), w) == 0.0)
+    ones = np.ones(128)
+    unit = o / np.sqrt(np.mean(o * o, axis=1, keepdims=True) + 1e-6)
+    assert np.allclose(oracle.gated_rmsnorm(o, z, ones) - oracle.gated_rmsnorm(o, -z, ones), unit * z, rtol=1e-12)
+    # the epsilon sits inside the square root: a row of tiny values is scaled by ~1/sqrt(eps)
+    tiny = np.full((1, 128), 1e-5)
+    assert np.allclose(oracle.gated_rmsnorm(tiny, np.full((1, 128), 50.0), ones),
+                       1e-5 * 50.0 / np.sqrt(1e-10 + 1e-6), rtol=1e-12)
+
+
+def test_fused_steps_compose_around_the_rule():
+    """Normalising raw q and k and forming beta from logits before the rule, then
+    the gated norm after it, equals doing those steps by hand around the plain
+    oracle; the normalisation makes the rule invariant to q and k scaling."""
+    r = _rng(504)
+    T, dk, dv = 30, 16, 16
+    q = r.standard_normal((T, 1, dk)) * 3.0
+    k = r.standard_normal((T, 1, dk)) * 0.2
+    v = r.standard_normal((T, 1, dv))
+    g = r.uniform(-2.0, -0.01, (T, 1))
+    b = r.standard_normal((T, 1))
+    S0 = 0.02 * r.standard_normal((1, 1, dk, dv))
+    z = r.standard_normal((T, 1, dv))
+    w = r.uniform(0.5, 1.5, dv)
+    y, S = oracle.gdr_fused([0, T], q, k, v, g, b, S0, qk_l2norm=True, beta_logits=True, z=z, norm_weight=w)
+    qn = q / np.sqrt(np.sum(q * q, -1, keepdims=True) + 1e-6)
+    kn = k / np.sqrt(np.sum(k * k, -1, keepdims=True) + 1e-6)
+    o2, S2 = oracle.gdr_sequential([0, T], qn, kn, v, g, 1 / (1 + np.exp(-b)), S0)
+    y2 = w * o2 / np.sqrt(np.mean(o2 * o2, -1, keepdims=True) + 1e-6) * (z / (1 + np.exp(-z)))
+    assert np.allclose(y, y2, rtol=1e-12, atol=1e-15) and np.allclose(S, S2, rtol=1e-12, atol=1e-15)
+    y3, S3 = oracle.gdr_fused([0, T], 5.0 * q, 0.5 * k, v, g, b, S0, qk_l2norm=True, beta_logits=True, z=z,
+                              norm_weight=w)
+    # up to the epsilon's share of |k|^2 (~1e-5 here)
+    assert np.linalg.norm(S3 - S) <= 1e-4 * np.linalg.norm(S)
+    assert np.max(np.abs(y3 - y)) <= 1e-4 * np.sqrt(np.mean(y * y))

@@ -21,14 +21,14 @@ def test_static_entry_rejects_oversize_before_launch():
     d = gdr.gdr_dims(h_qk=16, h_v=32, d_k=128, d_v=128, chunk=64, in_dtype=gdr.GDR_BF16,
                      out_dtype=gdr.GDR_F32, scale=1.0)
     A = 0x100000  # aligned stand-in addresses: nothing is dereferenced on this path
-    # one chunk position of 32 V heads and 16 QK heads takes 32 * 16640 + 16 * 16384
-    # bytes: the 64 MiB array holds 84 positions, i.e. one sequence of up to 83
-    # chunks (5312 tokens; one position is the per-sequence spare)
-    assert L.gdr_prefill_workspace_bytes(ctypes.byref(d), 1, 5312) <= cap
-    assert L.gdr_prefill_workspace_bytes(ctypes.byref(d), 1, 5313) > cap
-    assert L.gdr_prefill_workspace_bytes(ctypes.byref(d), 2, 5248) <= cap
-    assert L.gdr_prefill_workspace_bytes(ctypes.byref(d), 2, 5249) > cap
-    for n, t in ((1, 5313), (2, 5249), (1, 1 << 20)):
+    # one chunk position of 32 V heads and 16 QK heads takes 32 * 17152 + 16 * 16384
+    # bytes: the 64 MiB array holds 82 positions, i.e. one sequence of up to 81
+    # chunks (5184 tokens; one position is the per-sequence spare)
+    assert L.gdr_prefill_workspace_bytes(ctypes.byref(d), 1, 5184) <= cap
+    assert L.gdr_prefill_workspace_bytes(ctypes.byref(d), 1, 5185) > cap
+    assert L.gdr_prefill_workspace_bytes(ctypes.byref(d), 2, 5120) <= cap
+    assert L.gdr_prefill_workspace_bytes(ctypes.byref(d), 2, 5121) > cap
+    for n, t in ((1, 5185), (2, 5121), (1, 1 << 20)):
         st = L.gdr_prefill_chunked_static(ctypes.byref(d), n, A, t, A, A, A, A, A, A, A, None)
         assert st == gdr.GDR_ERR_UNSUPPORTED, (n, t, st)
 
@@ -51,7 +51,7 @@ def test_static_entry_matches_workspace_entry_twice():
 
 @pytest.mark.gpu
 def test_static_entry_at_its_largest_single_sequence():
-    """One Qwen3.5-9B sequence of 5312 tokens fills the fixed array to its last
+    """One Qwen3.5-9B sequence of 5184 tokens fills the fixed array to its last
     chunk position.  At this length gdr_prefill_chunked splits the prefill into
     four launches (the static entry keeps two), which regroups a few products,
     so the two agree to rounding: both are checked against the oracle, and
@@ -59,7 +59,7 @@ def test_static_entry_at_its_largest_single_sequence():
     import oracle
 
     torch = gu.require_gpu()
-    w = synth.make_workload("no_alloc_max", [5312], 16, 32, 128, 64, "bf16", seed=72, state_std=0.02)
+    w = synth.make_workload("no_alloc_max", [5184], 16, 32, 128, 64, "bf16", seed=72, state_std=0.02)
     x = gu.dev_inputs(w)
     s_ws, s_st = x["state"].clone(), x["state"].clone()
     o_ws, o_st = gu.out_like(x["v"], "f32"), gu.out_like(x["v"], "f32")
