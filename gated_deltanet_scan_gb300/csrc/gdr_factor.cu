@@ -79,14 +79,16 @@ constexpr int HEAD_B = OFF_TD + 4 * BLK_B;  // 50176
 // completed, the scratch overwrites them.
 constexpr uint32_t OFF_KQ = 0;
 constexpr uint32_t OFF_KP = 32768;  // K of the previous chunk: two 8 KB d_k halves
-// G log2(e), beta, exp(G), exp(G_C - G), 1 / |k|, 1 / |q|: 6 x 64 fp32
+// G log2(e), beta, exp(G), exp(G_C - G): 4 x 64 fp32; with the fused L2 norm also
+// 1 / |k| and 1 / |q| (2 x 64 more)
 constexpr uint32_t OFF_GATES = HEAD_B;
-constexpr uint32_t OFF_BARS = OFF_GATES + 1536;  // 2 mbarriers
-constexpr uint32_t OFF_TMEM = OFF_BARS + 16;
-constexpr uint32_t SMEM_USED = OFF_TMEM + 16;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
+__host__ __device__ constexpr uint32_t gates_bytes(bool qkn) { return qkn ? 1536u : 1024u; }
+__host__ __device__ constexpr uint32_t off_bars(bool qkn) { return OFF_GATES + gates_bytes(qkn); }  // 2 mbarriers
+__host__ __device__ constexpr uint32_t off_tmem(bool qkn) { return off_bars(qkn) + 16; }
+__host__ __device__ constexpr uint32_t smem_bytes(bool qkn) { return off_tmem(qkn) + 16 + 1024; }
 static_assert(OFF_KP + 16384 <= HEAD_B, "K/Q and previous K tiles fit under the scratch");
-static_assert(OFF_GATES % 16 == 0 && OFF_BARS % 8 == 0 && HEAD_B % 16 == 0, "alignment");
+static_assert(OFF_GATES % 16 == 0 && off_bars(false) % 8 == 0 && off_bars(true) % 8 == 0 && HEAD_B % 16 == 0,
+              "alignment");
 
 constexpr uint32_t TM_COLS = 128;  // the 128 x 64 fp32 Gram tile, then X
 constexpr uint32_t IDESC_G1 = idesc_bf16_f32(128, 64, 0, 0);
@@ -95,7 +97,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct FacParams {
     int h_qk, h_v, n_seqs;
-    int qk_norm, beta_logits;  // fused q/k L2 normalisation, beta from logits
     int c_lo, c_hi;    // chunks of each sequence to process
     int64_t slot_lo;   // first slot of the launch (blockIdx.x = 0)
     int64_t t_total;
@@ -215,7 +216,7 @@ __device__ __forceinline__ void chunk_gates(float g0, float g1, float b0, float 
 // blocks go one per warp (3, 2, 1).  Every block of Tw is stored to the slot's
 // operand tiles (rows 0-63) as soon as it is formed, adjacent columns paired
 // across lanes.
-__device__ void solve_t(uint8_t *hs, const float *gates, uint8_t *slot, int wi, int lane, uint32_t bar) {
+__device__ __forceinline__ void solve_t(uint8_t *hs, const float *gates, uint8_t *slot, int wi, int lane, uint32_t bar) {
     const int g = lane >> 2, c = lane & 3;
     const float *bw = gates + 64, *rw = gates + 192;  // column weights beta, row weights exp(G_C - G)
     // ---- diagonal blocks: warps 0-1 two each, lanes 0-15 / 16-31 one block, lane = column
@@ -299,7 +300,7 @@ __device__ void solve_t(uint8_t *hs, const float *gates, uint8_t *slot, int wi, 
 // The head's P T from P and Tᵀ blocks, by the four warps w: block (I, J), I >= J,
 // costs I - J + 1 products; the groups {30, 00}, {20, 10}, {31, 21},
 // {32, 11, 22, 33} cost five each.
-__device__ void solve_pt(const uint8_t *hs, const float *gates, uint8_t *slot, int w, int lane) {
+__device__ __forceinline__ void solve_pt(const uint8_t *hs, const float *gates, uint8_t *slot, int w, int lane) {
     const int g = lane >> 2, c = lane & 3;
     const float *bw = gates + 64;  // column weights beta
     const uint32_t blocks = w == 0 ? 0x0030u : w == 1 ? 0x1020u : w == 2 ? 0x2131u : 0x33221132u;
@@ -328,7 +329,7 @@ __device__ void solve_pt(const uint8_t *hs, const float *gates, uint8_t *slot, i
 
 // Row `row` (a TMEM lane this warp may read) of X from TMEM columns 64-127 into
 // a shared-memory image of the fp16 X tile (128-byte swizzled) at `img`.
-__device__ void stage_x_row(uint32_t tmem, int warp, int row, uint8_t *img) {
+__device__ __forceinline__ void stage_x_row(uint32_t tmem, int warp, int row, uint8_t *img) {
     uint8_t *xt = img + (size_t)row * 128;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
 #pragma unroll 1
@@ -345,8 +346,10 @@ __device__ void stage_x_row(uint32_t tmem, int warp, int row, uint8_t *img) {
     }
 }
 
-__global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ CUtensorMap tmK,
-                                                       const __grid_constant__ CUtensorMap tmQ, FacParams p) {
+// QKN: the fused q/k L2 normalisation; BL: beta from logits (compile-time, so the
+// default kernel carries no code for either).
+template <bool QKN, bool BL>
+__device__ __forceinline__ void factor_body(const CUtensorMap &tmK, const CUtensorMap &tmQ, const FacParams &p) {
     // a chunk scan queued behind this launch as a programmatic dependent may start
     // its prologue now; it waits for this grid before it reads the workspace
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -377,8 +380,8 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     float *gates = reinterpret_cast<float *>(sm + OFF_GATES);
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + OFF_TMEM);
-    const uint32_t bar_tma = sb + OFF_BARS, bar_mma = sb + OFF_BARS + 8;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + off_tmem(QKN));
+    const uint32_t bar_tma = sb + off_bars(QKN), bar_mma = sb + off_bars(QKN) + 8;
 
     // raw gates first (warp 0): their latency overlaps the tile load
     float rg0 = 0.f, rg1 = 0.f, rb0 = 0.f, rb1 = 0.f;
@@ -386,12 +389,12 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
         if (lane < L) {
             const size_t i = (size_t)(t0 + lane) * p.h_v + h;
             rg0 = p.g[i] * kLog2e;
-            rb0 = beta_of(p.beta[i], p.beta_logits);
+            rb0 = beta_of(p.beta[i], BL);
         }
         if (lane + 32 < L) {
             const size_t i = (size_t)(t0 + lane + 32) * p.h_v + h;
             rg1 = p.g[i] * kLog2e;
-            rb1 = beta_of(p.beta[i], p.beta_logits);
+            rb1 = beta_of(p.beta[i], BL);
         }
     }
     // X writer: the first V head of the QK head's group; the first chunk of a
@@ -445,7 +448,7 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
         }
     }
     ok = ok && mbar_wait_bounded(bar_mma, 0, kWaitLimit);
-    if (p.qk_norm && ok) {
+    if (QKN && ok) {
         // fused L2 normalisation: thread i takes row i of the [K; Q] tile (both
         // d_k halves; the order of the sum does not matter), still intact
         ok = mbar_wait_bounded(bar_tma, 0, kWaitLimit);  // the tile's bytes are visible to this thread
@@ -481,7 +484,7 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
         const bool is_n = row < 64;
         const float Gt = gates[t];
         // row weight beta_t (N) or 1 (P), times the row's L2 scale with the fused normalisation
-        const float w = (is_n ? gates[64 + t] : 1.f) * (p.qk_norm ? gates[256 + row] : 1.f);
+        const float w = QKN ? (is_n ? gates[64 + t] : 1.f) * gates[256 + row] : (is_n ? gates[64 + t] : 1.f);
         const int lim = is_n ? t : t + 1;  // keep j < t (N) or j <= t (P)
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
 #pragma unroll
@@ -489,7 +492,7 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
             float v[16];
             tmem_ld16(lane_addr + 16 * J, v);
             if (J > I) continue;
-            if (p.qk_norm) {  // column scales 1 / |k_j|
+            if constexpr (QKN) {  // column scales 1 / |k_j|
 #pragma unroll
                 for (int e = 0; e < 16; ++e) v[e] *= gates[256 + 16 * J + e];
             }
@@ -522,7 +525,7 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
             float *eg = reinterpret_cast<float *>(slot_out + fac::OFF_EG);
             eg[lane] = gates[128 + lane];
             eg[lane + 32] = gates[160 + lane];
-            if (p.qk_norm) {  // the row scales for the chunk scan: 1 / |k| (64), then 1 / |q| (64)
+            if constexpr (QKN) {  // the row scales for the chunk scan: 1 / |k| (64), then 1 / |q| (64)
                 float *rs = reinterpret_cast<float *>(slot_out + fac::OFF_RK);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) rs[lane + 32 * i] = gates[256 + lane + 32 * i];
@@ -565,6 +568,27 @@ __global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ C
     }
 }
 
+// One kernel per option set (the default one first).
+__global__ void __launch_bounds__(NT, 4) factor_kernel(const __grid_constant__ CUtensorMap tmK,
+                                                       const __grid_constant__ CUtensorMap tmQ, FacParams p) {
+    factor_body<false, false>(tmK, tmQ, p);
+}
+__global__ void __launch_bounds__(NT, 4) factor_kernel_beta_logits(const __grid_constant__ CUtensorMap tmK,
+                                                                   const __grid_constant__ CUtensorMap tmQ,
+                                                                   FacParams p) {
+    factor_body<false, true>(tmK, tmQ, p);
+}
+__global__ void __launch_bounds__(NT, 4) factor_kernel_qk_l2norm(const __grid_constant__ CUtensorMap tmK,
+                                                                 const __grid_constant__ CUtensorMap tmQ,
+                                                                 FacParams p) {
+    factor_body<true, false>(tmK, tmQ, p);
+}
+__global__ void __launch_bounds__(NT, 4) factor_kernel_qk_l2norm_beta_logits(const __grid_constant__ CUtensorMap tmK,
+                                                                             const __grid_constant__ CUtensorMap tmQ,
+                                                                             FacParams p) {
+    factor_body<true, true>(tmK, tmQ, p);
+}
+
 }  // namespace
 
 cudaError_t launch_factors(const Args &a, float *ws, int32_t *err, cudaStream_t s, bool overlap) {
@@ -577,7 +601,17 @@ cudaError_t launch_factors(const Args &a, float *ws, int32_t *err, cudaStream_t 
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(factor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        e = cudaFuncSetAttribute(factor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem_bytes(false));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(factor_kernel_beta_logits, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem_bytes(false));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(factor_kernel_qk_l2norm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem_bytes(true));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(factor_kernel_qk_l2norm_beta_logits, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem_bytes(true));
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
@@ -585,8 +619,6 @@ cudaError_t launch_factors(const Args &a, float *ws, int32_t *err, cudaStream_t 
     p.h_qk = a.h_qk;
     p.h_v = a.h_v;
     p.n_seqs = a.n_seqs;
-    p.qk_norm = a.qk_norm;
-    p.beta_logits = a.beta_logits;
     p.t_total = a.t_total;
     p.cu_seqlens = a.cu_seqlens;
     p.g = a.g;
@@ -608,14 +640,16 @@ cudaError_t launch_factors(const Args &a, float *ws, int32_t *err, cudaStream_t 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(slot_hi - slot_lo), (unsigned)a.h_v);
     cfg.blockDim = dim3(NT);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.dynamicSmemBytes = smem_bytes(a.qk_norm != 0);
     cfg.stream = s;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = overlap ? &attr : nullptr;
     cfg.numAttrs = overlap ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, factor_kernel, tmK, tmQ, p);
+    auto kern = a.qk_norm ? (a.beta_logits ? factor_kernel_qk_l2norm_beta_logits : factor_kernel_qk_l2norm)
+                          : (a.beta_logits ? factor_kernel_beta_logits : factor_kernel);
+    return cudaLaunchKernelEx(&cfg, kern, tmK, tmQ, p);
 }
 
 }  // namespace gdr

@@ -37,9 +37,11 @@
 // Qwen3.5-9B shapes up to ~1e-2 of the output RMS (max-abs) and ~2.5e-4 of the
 // state (relative Frobenius), not growing with the number of chunks, since
 // each chunk's rounding enters the state once and decays with it.  The fp16
-// range bounds the supported inputs: R and D~ scale with v and the state (the
-// factors do not); they must stay below 65504, and their RMS above ~1e-4, below
-// which the fp16 subnormals cost accuracy.
+// range: R and D~ scale with v and the state (the factors do not), so each CTA
+// multiplies them by a power of two sigma, chosen once from its first V tile and
+// initial state (sigma_exponent), and takes it out where they leave the fp16
+// domain (the state update, the outputs): exact, and the relative accuracy no
+// longer depends on the data's scale.
 //
 // Warp roles (448 threads; every role waits only on mbarriers and its own
 // named barriers, so no role can stall another's issue):
@@ -82,7 +84,7 @@ constexpr int NISSUE = 32;       // warp 12
 constexpr int NCOPY = 32;        // warp 13
 constexpr int NTHREADS = NCHAIN + NLOAD + NISSUE + NCOPY;
 constexpr int NKQ = 3;           // K/Q/V ring depth (chunks)
-constexpr uint32_t BAR_CHAIN = 1, BAR_LOW = 2, BAR_LOAD = 3;  // named barriers
+constexpr uint32_t BAR_CHAIN = 1, BAR_LOW = 2, BAR_LOAD = 3, BAR_SIG = 4;  // named barriers
 constexpr int NLOW = 128;        // chain threads of TMEM lanes 0-63 (warps 0, 1, 4, 5)
 
 // Shared memory map, bytes from a 1024-byte aligned base.
@@ -113,7 +115,10 @@ constexpr uint32_t OFF_SMALL = OFF_GATES + 2 * fac::GATE_BYTES;
 constexpr uint32_t SM_BARS = OFF_SMALL;                   // NBARS x uint64
 constexpr uint32_t SM_TMEM = OFF_SMALL + 192;
 constexpr uint32_t SM_ABORT = OFF_SMALL + 200;
-constexpr uint32_t SMEM_USED = OFF_SMALL + 256;
+constexpr uint32_t SM_SIGMA = OFF_SMALL + 208;   // the operand scale sigma (fp32)
+constexpr uint32_t SM_WMAX = OFF_SMALL + 224;    // 4 floats: per K-row warp, max |V_0| and |S_0|
+constexpr uint32_t SM_ROWMAX = OFF_SMALL + 256;  // 128 floats: per state row, max |S_0| over the CTA's columns
+constexpr uint32_t SMEM_USED = OFF_SMALL + 256 + 512;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_V % 1024 == 0 && OFF_OPS % 1024 == 0 && OFF_S % 1024 == 0 &&
@@ -133,7 +138,8 @@ constexpr int B_S_READY = B_OP_FREE + NOP; // S_c formed and S' = e^gamma_c S_c 
 constexpr int B_ACC = B_S_READY + 1;        // a chunk's accumulator A_c complete
 constexpr int B_MMA2 = B_ACC + 1;           // [D~; P D] ready
 constexpr int B_Y = B_MMA2 + 1;             // Kᵀ D~ ready
-constexpr int NBARS = B_Y + 1;
+constexpr int B_SIG = B_Y + 1;              // the operand scale sigma is set (once, chunk 0)
+constexpr int NBARS = B_SIG + 1;
 static_assert(NBARS * 8 <= 192, "barrier space");
 
 // TMEM columns (fp32 accumulators, lane = row).  Each holds the products of a
@@ -174,6 +180,7 @@ struct Ctx {
     uint32_t tmem;
     volatile int *abort_flag;
     __device__ uint32_t bar(int i) const { return sbase + SM_BARS + 8 * i; }
+    __device__ float *fsmall(uint32_t off) const { return reinterpret_cast<float *>(sm + off); }
     __device__ const float *gates(int gb) const {
         return reinterpret_cast<const float *>(sm + OFF_GATES + fac::GATE_BYTES * gb);
     }
@@ -212,6 +219,21 @@ __device__ bool wait_or_abort(const Ctx &x, uint32_t bar, uint32_t parity) {
             return false;
         }
     }
+}
+
+// The operand scale of a CTA, from the largest magnitude M of its first V tile
+// and initial state: 1 while M is in [2^-4, 2^13), where the fp16 tiles R and D~
+// (which scale with v and the state; the factors do not) keep away from fp16's
+// subnormals and its maximum; otherwise the power of two sigma with sigma M in
+// [8, 16), so that they sit in the middle of fp16's range whatever the data's
+// scale.  Exact: multiplying by a power of two changes no mantissa.  (1 also
+// when M is zero, NaN or inf.)
+__device__ __forceinline__ int sigma_exponent(float M) {
+    if (!(M > 0.f) || !(M <= 3.0e38f)) return 0;
+    int e = ((__float_as_int(M) >> 23) & 0xff) - 127;  // floor(log2 M) (M normal)
+    if (e >= -4 && e < 13) return 0;
+    e = e < -120 ? -120 : (e > 120 ? 120 : e);
+    return 3 - e;
 }
 
 // This thread's 16 columns of one accumulator ([hi-part | lo-part] in TMEM
@@ -356,18 +378,12 @@ __device__ void copy_role(const Ctx &x, const TcParams &p, int64_t t0, int nchun
 // operand S' = e^gamma_c S_c that MMA1' reads.  Per chunk c:
 //   S_c = e^gamma_c-1 S_c-1 + Y_c-1 (once MMA3 of chunk c-1 is done; for c = 0,
 //   once A_0 has read the S_0 tile), S' = e^gamma_c S_c.
-__device__ void loader_role(const Ctx &x, int nchunks, int lt, float *Sg, bool &ok) {
+// SC: the CTA's operand scale sigma is not 1 (compile-time, see chain_loop): Y
+// comes in units of sigma (D~ does) and S' goes out in them.
+template <bool SC>
+__device__ __forceinline__ void loader_loop(const Ctx &x, int nchunks, int lt, float *Sg, float (&Sr)[32], float sig,
+                                            float isig, bool bad, bool &ok) {
     const uint32_t lb = lane_base(x.tmem, lt >> 5);  // warp 8 + i: lanes 32 i ..
-    float Sr[32];  // state row lt, the CTA's 32 columns (S_0 was loaded into the S tile)
-#pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(Sg + j);
-        Sr[j] = v.x;
-        Sr[j + 1] = v.y;
-        Sr[j + 2] = v.z;
-        Sr[j + 3] = v.w;
-    }
-    bool bad = false;
     float eGC_prev = 1.f;  // exp(gamma) of the previous chunk
     for (int c = 0; c < nchunks; ++c) {
         const int gb = c & 1;
@@ -382,18 +398,20 @@ __device__ void loader_role(const Ctx &x, int nchunks, int lt, float *Sg, bool &
                     float y[16];
                     acc_sum1(lb, TM_Y, 16 * g2, y);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) Sr[16 * g2 + j] = fmaf(eGC_prev, Sr[16 * g2 + j], y[j]);
+                    for (int j = 0; j < 16; ++j)
+                        Sr[16 * g2 + j] = fmaf(eGC_prev, Sr[16 * g2 + j], SC ? y[j] * isig : y[j]);
                 }
             }
         } else if (!bad) {
             bad = !wait_or_abort(x, x.bar(B_ACC), 0u);  // A_0 has read the S_0 tile
         }
         if (!bad && c + 1 < nchunks) {
+            const float f = SC ? sig * eGC : eGC;
 #pragma unroll
             for (int g2 = 0; g2 < 2; ++g2) {
                 float sp[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) sp[j] = eGC * Sr[16 * g2 + j];
+                for (int j = 0; j < 16; ++j) sp[j] = f * Sr[16 * g2 + j];
                 store_hilo_row16(x.sm + OFF_S, lt, 16 * g2, sp);
             }
             fence_proxy_async_smem();
@@ -419,7 +437,7 @@ __device__ void loader_role(const Ctx &x, int nchunks, int lt, float *Sg, bool &
             float y[16];
             acc_sum1(lb, TM_Y, 16 * g2, y);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) Sr[16 * g2 + j] = fmaf(eGC_prev, Sr[16 * g2 + j], y[j]);
+            for (int j = 0; j < 16; ++j) Sr[16 * g2 + j] = fmaf(eGC_prev, Sr[16 * g2 + j], SC ? y[j] * isig : y[j]);
         }
     }
     ok = !bad;
@@ -428,6 +446,26 @@ __device__ void loader_role(const Ctx &x, int nchunks, int lt, float *Sg, bool &
         for (int j = 0; j < 32; j += 4)
             *reinterpret_cast<float4 *>(Sg + j) = make_float4(Sr[j], Sr[j + 1], Sr[j + 2], Sr[j + 3]);
     }
+}
+
+// The loader warps own the state (see loader_loop); they first wait for the
+// operand scale the chain sets before its loop.
+__device__ void loader_role(const Ctx &x, int nchunks, int lt, float *Sg, bool &ok) {
+    float Sr[32];  // state row lt, the CTA's 32 columns (S_0 was loaded into the S tile)
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(Sg + j);
+        Sr[j] = v.x;
+        Sr[j + 1] = v.y;
+        Sr[j + 2] = v.z;
+        Sr[j + 3] = v.w;
+    }
+    bool bad = !wait_or_abort(x, x.bar(B_SIG), 0u);
+    const float sig = bad ? 1.f : *x.fsmall(SM_SIGMA);
+    if (sig == 1.f)
+        loader_loop<false>(x, nchunks, lt, Sg, Sr, 1.f, 1.f, bad, ok);
+    else
+        loader_loop<true>(x, nchunks, lt, Sg, Sr, sig, 1.f / sig, bad, ok);
 }
 
 // Row t of chunk c0 of the output (16 columns at j0 of the CTA's block).
@@ -547,20 +585,19 @@ __device__ void issuer_role(const Ctx &x, int nchunks, int lane) {
 }
 
 // ================================= chain ============================================
-// Warps 0-7.  Warp w owns TMEM lanes 32 (w % 4) .. + 31 (chunk rows: K/T rows
-// in lanes 0-63, Q/PT rows in lanes 64-127) and columns 16 (w / 4) .. + 15 of
-// the CTA's 32.  Per chunk: the K / T-row warps form R from A_c and hand it to
-// the issuer (BAR_LOW), then write D~ from MMA2's accumulator; the Q / PT-row
-// warps form the outputs and store them after the chunk's last barrier.
-__device__ void chain_role(const Ctx &x, const TcParams &p, const TcRun &run, int64_t t0, int64_t t1, int nchunks,
-                           int h, int cb, int tid, bool &ok) {
+// The chunk loop of the chain.  QKN: the fused q/k L2 normalisation (row scales
+// from the slots); SC: the CTA's operand scale sigma is not 1 (data outside
+// fp16's comfortable range).  Both are compile-time, so the default loop carries
+// no code for either.
+template <bool QKN, bool SC>
+__device__ void chain_loop(const Ctx &x, const TcParams &p, const TcRun &run, int64_t t0, int64_t t1, int nchunks,
+                           int h, int cb, int tid, float sig, float isig, bool bad, bool &ok) {
     const int warp = tid >> 5, lane = tid & 31;
     const int j0 = 16 * (warp >> 2);           // this thread's 16 columns of the CTA's 32
     const int row = ((warp & 3) << 5) + lane;  // TMEM lane
     const bool low = row < 64;                 // K / T rows (on the chunk-to-chunk path)
     const int t = row & 63;
     const uint32_t lb = lane_base(x.tmem, warp);
-    bool bad = false;
     // every thread runs every named barrier of every chunk; only the CTA-wide
     // stop decided at BAR_CHAIN ends the loop early
     for (int c = 0; c < nchunks; ++c) {
@@ -572,7 +609,8 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, const TcRun &run, in
         if (!bad) bad = !wait_or_abort(x, x.bar(B_G_FULL + gb), (uint32_t)(c >> 1) & 1u);
         const float egt = x.gates(gb)[t];
         // with the fused L2 norm: this row's scale, 1 / |k_t| (K / T rows) or 1 / |q_t| (Q / PT rows)
-        const float rsc = p.qk_norm ? x.gates(gb)[(low ? 64 : 128) + t] : 1.f;
+        float rsc = 1.f;
+        if constexpr (QKN) rsc = x.gates(gb)[(low ? 64 : 128) + t];
         // ---- A_c complete: R = V - e^G K S_c ---------------------------------------------
         if (!bad) bad = !wait_or_abort(x, x.bar(B_ACC), par);
         tc_fence_after_sync();
@@ -580,21 +618,23 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, const TcRun &run, in
         {
             float ks[16];
             if (!bad) acc_sum1(lb, TM_ACC + 64 * ab, j0, ks);
-            if (p.qk_norm) {
+            if constexpr (QKN) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) ks[j] *= rsc;
             }
             if (low) {
                 if (!bad) {
-                    // R = V - e^G K S in fp16
+                    // R = V - e^G K S in fp16; with the operand scale, sigma (V - e^G K S)
+                    // (A_0 came from the unscaled S_0 tile, every later A is in units of sigma)
                     const uint8_t *vt = x.sm + OFF_V + kb * V_BYTES;
+                    const float ea = SC ? -egt * (c == 0 ? sig : 1.f) : -egt;
                     float r[16];
 #pragma unroll
                     for (int ch = 0; ch < 2; ++ch) {
                         float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                         if (!run.v_zero) load_bf16_chunk64(vt, t, (j0 >> 3) + ch, v);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) r[8 * ch + e] = fmaf(-egt, ks[8 * ch + e], v[e]);
+                        for (int e = 0; e < 8; ++e) r[8 * ch + e] = fmaf(ea, ks[8 * ch + e], SC ? sig * v[e] : v[e]);
                     }
                     store_f16_row16(x.sm + OFF_R, t, j0, r);
                     fence_proxy_async_smem();
@@ -617,7 +657,7 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, const TcRun &run, in
                 if (!bad) {
                     // with the fused L2 norm both products take diag(1 / |k|) D~ (K^T of
                     // the normalised keys; X holds the raw keys' products)
-                    if (p.qk_norm) {
+                    if constexpr (QKN) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j) d[j] *= rsc;
                     }
@@ -626,6 +666,11 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, const TcRun &run, in
                     store_hilo_row16(x.sm + OFF_DT2, t, j0, d);
                     fence_proxy_async_smem();
                 }
+            } else if constexpr (SC) {
+                // O = scale (e^G Q S + P D); P D is in units of sigma, so is e^G Q S after chunk 0
+                const float fq = p.scale * (c == 0 ? 1.f : isig), fd = p.scale * isig;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) ov[j] = fmaf(fq, qse[j], fd * d[j]);
             } else {
                 // O = scale (e^G Q S + P D)
 #pragma unroll
@@ -644,6 +689,57 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, const TcRun &run, in
     ok = !bad;
 }
 
+// Warps 0-7.  Warp w owns TMEM lanes 32 (w % 4) .. + 31 (chunk rows: K/T rows
+// in lanes 0-63, Q/PT rows in lanes 64-127) and columns 16 (w / 4) .. + 15 of
+// the CTA's 32.  Per chunk: the K / T-row warps form R from A_c and hand it to
+// the issuer (BAR_LOW), then write D~ from MMA2's accumulator; the Q / PT-row
+// warps form the outputs and store them after the chunk's last barrier.
+// Before the loop the K / T-row threads set the CTA's operand scale from the
+// first V tile and the initial state's row maxima (every one of them takes part,
+// also after an abort, and one publishes it on B_SIG); the Q / PT-row threads
+// wait for it.  Then every chain thread runs the loop for that scale.
+template <bool QKN>
+__device__ void chain_role(const Ctx &x, const TcParams &p, const TcRun &run, int64_t t0, int64_t t1, int nchunks,
+                           int h, int cb, int tid, bool &ok) {
+    const int warp = tid >> 5, lane = tid & 31;
+    const bool low = (warp & 3) < 2;
+    const int t = (((warp & 3) << 5) + lane) & 63;
+    const int j0 = 16 * (warp >> 2);
+    bool bad = false;
+    float sig = 1.f;
+    if (low) {
+        const int kidx = ((warp >> 2) << 6) + ((warp & 3) << 5) + lane;  // 0 .. 127
+        float mx = x.fsmall(SM_ROWMAX)[kidx];
+        if (!bad) bad = !wait_or_abort(x, x.bar(B_KQ_FULL + 0), 0u);  // the first V tile
+        if (!bad && !run.v_zero) {
+            float v[16];
+            const uint8_t *vt = x.sm + OFF_V;
+#pragma unroll
+            for (int ch = 0; ch < 2; ++ch) load_bf16_chunk64(vt, t, (j0 >> 3) + ch, v + 8 * ch);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) mx = fmaxf(mx, fabsf(v[j]));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        if (lane == 0) x.fsmall(SM_WMAX)[kidx >> 5] = mx;
+        named_sync(BAR_SIG, NLOW);
+        const float *wm = x.fsmall(SM_WMAX);
+        sig = ldexpf(1.f, sigma_exponent(fmaxf(fmaxf(wm[0], wm[1]), fmaxf(wm[2], wm[3]))));
+        if (kidx == 0) {
+            *x.fsmall(SM_SIGMA) = sig;
+            mbar_arrive(x.bar(B_SIG));  // release: the Q / PT-row threads and the state warps read it
+        }
+    } else {
+        if (!bad) bad = !wait_or_abort(x, x.bar(B_SIG), 0u);
+        if (!bad) sig = *x.fsmall(SM_SIGMA);
+    }
+    if (sig == 1.f)
+        chain_loop<QKN, false>(x, p, run, t0, t1, nchunks, h, cb, tid, 1.f, 1.f, bad, ok);
+    else
+        chain_loop<QKN, true>(x, p, run, t0, t1, nchunks, h, cb, tid, sig, 1.f / sig, bad, ok);
+}
+
+template <bool QKN>
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmV, TcParams p) {
@@ -693,6 +789,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float *Sg = run.state + (((size_t)s * p.h_v + h) * D + (loader ? lt : 0)) * D + cb * BV;
     if (loader) {
         // S_0 into the S tile (the loader role reads its row again into registers)
+        float rmax = 0.f;
 #pragma unroll
         for (int g2 = 0; g2 < 2; ++g2) {
             float s0[16];
@@ -705,7 +802,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 s0[j + 3] = v.w;
             }
             store_hilo_row16(x.sm + OFF_S, lt, 16 * g2, s0);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) rmax = fmaxf(rmax, fabsf(s0[j]));
         }
+        x.fsmall(SM_ROWMAX)[lt] = rmax;  // read by the chain when it sets the operand scale
         fence_proxy_async_smem();
     } else if (tid < NCHAIN) {
         // the zero second halves of the fp16 R and D~ tiles (16 KB, contiguous)
@@ -721,7 +821,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     bool ok = true;
     if (tid < NCHAIN)
-        chain_role(x, p, run, t0, t1, nchunks, h, cb, tid, ok);
+        chain_role<QKN>(x, p, run, t0, t1, nchunks, h, cb, tid, ok);
     else if (loader)
         loader_role(x, nchunks, lt, Sg, ok);
     else if (issuer)
@@ -769,7 +869,11 @@ cudaError_t launch_prefill_tc_runs(const Args &a, const TcRun *runs, int n_runs,
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        e = cudaFuncSetAttribute(prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
@@ -794,7 +898,8 @@ cudaError_t launch_prefill_tc_runs(const Args &a, const TcRun *runs, int n_runs,
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = overlap ? &attr : nullptr;
     cfg.numAttrs = overlap ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, tmK, tmQ, tmV, p);
+    return a.qk_norm ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true>, tmK, tmQ, tmV, p)
+                     : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false>, tmK, tmQ, tmV, p);
 }
 
 cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s, bool overlap) {

@@ -166,9 +166,12 @@ size_t gdr_prefill_workspace_bytes(const gdr_dims *dims, int32_t n_seqs, int64_t
  * splits); the chunk-sized products with the factors (the correction D, the
  * intra-chunk output part and X D~) take fp16 operands with fp32
  * accumulation.  Their data-scaled operands (V - e^G K S and the correction D)
- * must stay inside the fp16 range: below 65504, and with an RMS above ~1e-4, or
- * the fp16 subnormals cost accuracy (at an RMS of 1.5e-5 the state error nears
- * 1e-3).  With L2-normalised q and k these operands scale with v and the state.
+ * are multiplied by a power of two chosen per scan CTA from its first chunk's
+ * values and its initial state (largest magnitude brought to [8, 16)), so the
+ * result's relative accuracy does not depend on the data's scale (tested from
+ * 2^-20 to 2^16 times unit-RMS values).  Data that grows by more than ~4000x
+ * over a sequence beyond its first chunk and initial state would approach the
+ * fp16 maximum.
  */
 gdr_status gdr_prefill_chunked(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens,
                                int64_t t_total, const void *q, const void *k, const void *v,
