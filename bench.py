@@ -187,7 +187,8 @@ class ClockSampler:
 # our arm
 
 
-PREFILL_SOURCES = ("gdr_factor.cu", "gdr_prefill_tc.cu", "gdr_factor_layout.h", "tc_ptx.cuh")
+PREFILL_SOURCES = ("gdr_factor.cu", "gdr_prefill_tc.cu", "gdr_factor_layout.h", "tc_ptx.cuh", "gdr_common.cuh",
+                   "gdr_internal.h")
 
 
 def prefill_source_digest():
@@ -331,6 +332,33 @@ def run_ours(args):
         decode_ms = statistics.median(a.elapsed_time(b) for a, b in dts[5:])
     else:
         decode_ms = statistics.median(t[2].elapsed_time(t[3]) for t in timers)
+    verify_alone_ms = None
+    if only in ("all", "verify"):
+        # verify block + commit alone, replayed from a CUDA graph of 20 pairs: the
+        # pair's own time with graph launch gaps and its inputs in L2 (inside the
+        # step they follow the prefill, cold, after eager launches)
+        def pair():
+            gdr.gdr_verify_block(dv["q"], dv["k"], dv["v"], dv["g"], dv["beta"], state, snap, o_ver,
+                                 N_VERIFY, deltas=deltas, stream=stream)
+            gdr.gdr_verify_commit(dv["k"], dv["g"], deltas, snap, state, accepted, N_VERIFY, stream=stream)
+        for _ in range(3):
+            pair()
+        barrier()
+        vg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(vg, stream=stream):
+            for _ in range(20):
+                pair()
+        barrier()
+        vts = []
+        for _ in range(5):
+            v0, v1 = ev(), ev()
+            v0.record(stream)
+            vg.replay()
+            v1.record(stream)
+            vts.append((v0, v1))
+        barrier()
+        verify_alone_ms = statistics.median(a.elapsed_time(b) for a, b in vts) / 20
+        del vg
 
     # The other configured workloads, timed alone after the steps (informational):
     # the Qwen3.5-9B layer prefill at T = 1024 and the packed prefill of 8
@@ -541,7 +569,7 @@ def run_ours(args):
                                "hbm_gbs": pre_gbs, "frac_hbm": pre_gbs / hbm,
                                "frac_hbm_survey_bytes": pre_gbs_survey / hbm,
                                "alg_tflops": pre_tflops, "frac_bf16": pre_tflops / bf16},
-            "verify16_commit7": {"ms": verify_ms},
+            "verify16_commit7": {"ms": verify_ms, "ms_alone_graph": verify_alone_ms},
             "decode_B64": {"ms": decode_ms, "tokens_per_s": B_DECODE / (decode_ms * 1e-3),
                            "hbm_gbs": dec_gbs, "frac_hbm": dec_gbs / hbm},
         },

@@ -421,7 +421,13 @@ gdr_status gdr_verify_block(const gdr_dims *dims, int32_t n_seqs, int32_t n_tok,
     a.state = state;
     a.snapshot = snapshot;
     a.o = o;
-    return from_cuda(launch_chunk_cc(a, reinterpret_cast<cudaStream_t>(stream)));
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (n_tok == 0) {  // no tokens: the snapshot only, the state stays as it is
+        const size_t n = (size_t)n_seqs * dims->h_v * dims->d_k * dims->d_v;
+        return from_cuda(launch_copy_f32(state, snapshot, n, cs));
+    }
+    if (a.in_bf16) return from_cuda(launch_verify(a, cs));
+    return from_cuda(launch_chunk_cc(a, cs));
 }
 
 gdr_status gdr_verify_commit(const gdr_dims *dims, int32_t n_seqs, int32_t n_tok, const int32_t *accepted,

@@ -42,18 +42,15 @@ __global__ void __launch_bounds__(NT) commit_kernel(Args a, int32_t *err) {
     const int h = (blockIdx.x / NQUART) % a.h_v, s = blockIdx.x / (NQUART * a.h_v);
     const int hq = h / (a.h_v / a.h_qk);
     const int n_tok = a.fixed_len;
-    const int acc = a.accepted[s];
-    if (acc < 0 || acc > n_tok) {  // leave the state as it is and report
-        if (threadIdx.x == 0 && quarter == 0) atomicCAS(err, 0, (int32_t)GDR_ERR_INVALID_ARG);
-        return;
-    }
+    // every load is issued before the accepted count is known: the block's rows of
+    // the snapshot, all n_tok corrections, k rows and gates (the count only masks them)
+    const int acc_in = a.accepted[s];
     const int rbase = quarter * ROWS;
     const size_t row0 = (size_t)s * n_tok;  // the block's first token row of this sequence
     const int cq = threadIdx.x % Q4, r0 = threadIdx.x / Q4;
     const size_t sbase = ((size_t)s * a.h_v + h) * D * D;
     const float4 *src = reinterpret_cast<const float4 *>(a.snapshot_in + sbase);
     float4 *dst = reinterpret_cast<float4 *>(a.state + sbase);
-    // this thread's rows of the snapshot, loaded first
     constexpr int NRT = NR > 0 ? NR : 1;
     float4 x[NRT];
 #pragma unroll
@@ -65,11 +62,22 @@ __global__ void __launch_bounds__(NT) commit_kernel(Args a, int32_t *err) {
 #pragma unroll
     for (int j = 0; j < MAXTOK; ++j) {
         u[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j < acc) u[j] = *reinterpret_cast<const float4 *>(a.deltas + ((row0 + j) * a.h_v + h) * D + 4 * cq);
+        if (j < n_tok) u[j] = *reinterpret_cast<const float4 *>(a.deltas + ((row0 + j) * a.h_v + h) * D + 4 * cq);
     }
+    float graw = 0.f;
+    if (threadIdx.x < 32 && threadIdx.x < n_tok) graw = a.g[(row0 + threadIdx.x) * a.h_v + h];
+    for (int e = threadIdx.x; e < n_tok * ROWS; e += NT) {
+        const int j = e / ROWS, i = e - j * ROWS;
+        sK[j][i] = load_in(a.k, ((row0 + j) * a.h_qk + hq) * D + rbase + i, a.in_bf16);
+    }
+    if (acc_in < 0 || acc_in > n_tok) {  // leave the state as it is and report
+        if (threadIdx.x == 0 && quarter == 0) atomicCAS(err, 0, (int32_t)GDR_ERR_INVALID_ARG);
+        return;
+    }
+    const int acc = acc_in;
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
-        float gj = (lane < acc) ? a.g[(row0 + lane) * a.h_v + h] : 0.f;
+        float gj = lane < acc ? graw : 0.f;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const float t = __shfl_up_sync(0xffffffffu, gj, o);
@@ -78,10 +86,6 @@ __global__ void __launch_bounds__(NT) commit_kernel(Args a, int32_t *err) {
         const float Ga = __shfl_sync(0xffffffffu, gj, acc > 0 ? acc - 1 : 0);
         if (lane < MAXTOK) sW[lane] = (lane < acc) ? __expf(Ga - gj) : 0.f;  // exponent <= 0 for g <= 0
         if (lane == 0) sEa = acc > 0 ? __expf(Ga) : 1.f;
-    }
-    for (int e = threadIdx.x; e < acc * ROWS; e += NT) {
-        const int j = e / ROWS, i = e - j * ROWS;
-        sK[j][i] = load_in(a.k, ((row0 + j) * a.h_qk + hq) * D + rbase + i, a.in_bf16);
     }
     __syncthreads();
     if (a.qk_norm) {

@@ -40,6 +40,8 @@ struct Args {
 // `overlap`: launch as a programmatic dependent of the kernel before it on `s`.
 cudaError_t launch_decode(const Args &a, int32_t *err, cudaStream_t s, bool overlap);
 cudaError_t launch_chunk_cc(const Args &a, cudaStream_t s);
+// The verify block on tensor cores (gdr_verify.cu): bf16 inputs, 1 <= fixed_len <= 16 tokens.
+cudaError_t launch_verify(const Args &a, cudaStream_t s);
 // Tensor-core prefill in two launches: the per-chunk factors of every chunk
 // into `ws` (fac::n_slots(t_total, n_seqs) * h_v slots), then the chunk scan.
 // `overlap`: launch as a programmatic dependent of the kernel before it on `s`

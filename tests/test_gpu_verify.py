@@ -149,3 +149,39 @@ def test_snapshot_restore_roundtrip():
     gdr.gdr_state_restore(snap, s2)
     torch.cuda.synchronize()
     assert torch.equal(snap, s) and torch.equal(s2, s)
+
+
+@pytest.mark.parametrize("d,io,out,n_tok,heads", [
+    (128, "bf16", "f32", 16, (16, 32)),
+    (128, "bf16", "bf16", 11, (16, 32)),
+    (64, "bf16", "f32", 16, (2, 4)),
+    (32, "bf16", "f32", 9, (4, 4)),
+    (32, "f32", "f32", 16, (2, 4)),
+    (128, "f32", "f32", 3, (1, 4)),
+])
+def test_verify_block_shapes(d, io, out, n_tok, heads):
+    """Every head size and input type of the verify block (bf16 inputs on the
+    tensor-core verify kernel, fp32 inputs on the CUDA-core chunk kernel) from a
+    random state, against the oracle: outputs, the state after the block, the
+    snapshot (bit-exact) and the corrections (through a full commit)."""
+    import gated_deltanet_scan_gb300 as gdr
+    torch = gu.require_gpu()
+    n = 2
+    w = synth.make_workload("vs", [n_tok] * n, heads[0], heads[1], d, 16, io, seed=90 + d + n_tok, state_std=0.05)
+    x = gu.dev_inputs(w)
+    snap = torch.empty_like(x["state"])
+    o = gu.out_like(x["v"], out)
+    deltas = torch.full(x["v"].shape, float("nan"), dtype=torch.float32, device="cuda")
+    gdr.gdr_verify_block(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state"], snap, o, n_tok, deltas=deltas)
+    committed = torch.full_like(x["state"], float("nan"))
+    gdr.gdr_verify_commit(x["k"], x["g"], deltas, snap, committed,
+                          torch.full((n,), n_tok, dtype=torch.int32, device="cuda"), n_tok)
+    torch.cuda.synchronize()
+    assert gdr.gdr_device_error() == 0
+    o_ref, S_ref = oracle.run_workload(w)
+    np.testing.assert_array_equal(gu.to_np(snap), w.state0.astype(np.float64))
+    # both kernels keep fp32-level precision (the tensor-core one splits the state
+    # into bf16 hi and lo halves): far inside the tolerances of the tensor-core prefill
+    gu.check_outputs(gu.to_np(o), o_ref, out, tol=1e-3 if out == "f32" else gu.O_TOL)
+    gu.check_state(gu.to_np(x["state"]), S_ref, tol=1e-4)
+    gu.check_state(gu.to_np(committed), S_ref, tol=1e-4)
