@@ -262,14 +262,20 @@ def run_ours(args):
         o_pre, o_ver, o_dec = [(main_set if bufs is None else bufs)[n] for n in ("o_pre", "o_ver", "o_dec")]
         if timers is not None:
             timers[0].record(stream)
-        if only in ("all", "prefill"):
-            gdr.gdr_prefill_chunked(dp["q"], dp["k"], dp["v"], dp["g"], dp["beta"], state, o_pre, cu_pre,
-                                    chunk=64, workspace=ws, stream=stream)
-        if only == "all":
-            # beside the prefill's last chunk-scan launch (no event between them:
-            # a stream operation there would end the overlap)
-            gdr.gdr_decode_step_overlapped(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dstate, o_dec,
-                                           stream=stream)
+        if only == "all" and args.decode_in_scan:
+            # one launch carries the prefill's last chunk scan and the decode step
+            gdr.gdr_prefill_with_decode(dp["q"], dp["k"], dp["v"], dp["g"], dp["beta"], state, o_pre, cu_pre,
+                                        dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dstate, o_dec,
+                                        workspace=ws, stream=stream)
+        else:
+            if only in ("all", "prefill"):
+                gdr.gdr_prefill_chunked(dp["q"], dp["k"], dp["v"], dp["g"], dp["beta"], state, o_pre, cu_pre,
+                                        chunk=64, workspace=ws, stream=stream)
+            if only == "all":
+                # beside the prefill's last chunk-scan launch (no event between them:
+                # a stream operation there would end the overlap)
+                gdr.gdr_decode_step_overlapped(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dstate, o_dec,
+                                               stream=stream)
         if timers is not None:
             timers[1].record(stream)
         if only in ("all", "verify"):
@@ -291,6 +297,8 @@ def run_ours(args):
     split = (T_PREFILL + 63) // 64 * H_V >= 8 * sms and sms - 4 * H_V >= 16
     pre_launches = 4 if split else 2
     launches_per_step = {"all": 3 + pre_launches, "prefill": pre_launches, "verify": 2, "decode": 1}[only]
+    if only == "all" and args.decode_in_scan:
+        launches_per_step -= 1  # the decode step rides the last chunk-scan launch
 
     def barrier():
         if world > 1:
@@ -721,6 +729,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-in-scan", action="store_true",
+                    help="run the decode step inside the prefill's last chunk-scan launch (gdr_prefill_with_decode) "
+                         "instead of as a programmatic dependent launch beside it")
     ap.add_argument("--only", choices=["all", "prefill", "verify", "decode"], default="all",
                     help="run one component of the step (for profiling); the default runs the full step")
     ap.add_argument("--no-other-configs", action="store_true",

@@ -18,6 +18,7 @@ __all__ = [
     "gdr_prefill_chunked", "gdr_prefill_workspace_bytes", "gdr_prefill_chunked_static",
     "gdr_prefill_segmented", "gdr_prefill_segmented_workspace_bytes", "gdr_prefill_segments_hint",
     "gdr_decode_step", "gdr_decode_step_overlapped", "gdr_decode_step_gated", "gdr_gated_rmsnorm",
+    "gdr_prefill_with_decode",
     "gdr_verify_block", "gdr_verify_commit",
     "gdr_state_snapshot", "gdr_state_restore", "gdr_device_error", "gdr_selftest_wait_timeout", "gdr_status_string",
     "GDR_F32", "GDR_BF16", "GDR_FLAG_QK_L2NORM", "GDR_FLAG_BETA_LOGITS",
@@ -72,6 +73,9 @@ _SIGS = {
                         ctypes.c_int),
     "gdr_decode_step_overlapped": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P],
                                    ctypes.c_int),
+    "gdr_prefill_with_decode": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, _P, ctypes.c_int64,
+                                 _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, ctypes.c_int32,
+                                 _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "gdr_verify_block": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, ctypes.c_int32,
                           _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "gdr_verify_commit": ([ctypes.POINTER(gdr_dims), ctypes.c_int32, ctypes.c_int32,
@@ -265,6 +269,31 @@ def gdr_decode_step(q, k, v, g, beta, state, o, *, scale: float = 1.0, qk_l2norm
         ctypes.byref(dims), q.shape[0], _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
         _ptr(state), _ptr(o), _stream_handle(stream, q.device))
     _check(st, "gdr_decode_step")
+
+
+def gdr_prefill_with_decode(q, k, v, g, beta, state, o, cu_seqlens, dq, dk, dv, dg, dbeta, dstate, d_o, *,
+                            scale: float = 1.0, qk_l2norm: bool = False, beta_logits: bool = False,
+                            t_total: Optional[int] = None, workspace=None, stream=None) -> None:
+    """A prefill (as gdr_prefill_chunked) and one decode step of another batch (as
+    gdr_decode_step) in the same chunk-scan launch (see include/gdr.h)."""
+    torch = _torch()
+    dims = make_dims(q, v, o, 64, scale, flags_of(qk_l2norm, beta_logits))
+    n = cu_seqlens.shape[0] - 1
+    T = q.shape[0] if t_total is None else int(t_total)
+    need = int(lib().gdr_prefill_workspace_bytes(ctypes.byref(dims), n, T))
+    if workspace is None and need > 0:
+        s = stream if stream is not None else torch.cuda.current_stream(q.device)
+        if isinstance(s, int):
+            s = torch.cuda.ExternalStream(s, device=q.device)
+        with torch.cuda.stream(s):
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = _ptr(workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().gdr_prefill_with_decode(
+        ctypes.byref(dims), n, _ptr(cu_seqlens), T, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+        _ptr(o), ws_ptr, ws_bytes, dq.shape[0], _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dstate),
+        _ptr(d_o), _stream_handle(stream, q.device))
+    _check(st, "gdr_prefill_with_decode")
 
 
 def gdr_decode_step_overlapped(q, k, v, g, beta, state, o, *, scale: float = 1.0, qk_l2norm: bool = False,

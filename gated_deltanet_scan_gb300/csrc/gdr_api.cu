@@ -1,6 +1,7 @@
 // C-ABI entry points: argument checks on the host, then the launches.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 
@@ -148,13 +149,18 @@ int segments_hint(const gdr_dims *d, int32_t n_seqs, int64_t t_total) {
 // running, on the SMs they leave free, and reads nothing the scan writes),
 // then scan [m, n) from the state the first part left.
 cudaError_t prefill_tc(const gdr_dims *dims, const Args &a, float *ws, int32_t *err, cudaStream_t s,
-                       bool allow_split) {
+                       bool allow_split, const Args *dec = nullptr) {
     const int m = allow_split ? split_chunk(dims, a.n_seqs, a.t_total) : 0;
+    // decode blocks of a mixed launch: eight (sequence, V head) pairs each, so that
+    // the hardware places them on the SMs the scan leaves free and, once its CTAs
+    // finish, on every SM
+    int dec_blocks = 0;
+    if (dec) dec_blocks = (int)std::max<int64_t>(1, ((int64_t)dec->n_seqs * dec->h_v + 7) / 8);
     if (m == 0) {
         // the scan's prologue overlaps the factor grid's last wave (T = 1024: 73 -> 67 us)
         cudaError_t e = launch_factors(a, ws, err, s, false);
         if (e != cudaSuccess) return e;
-        return launch_prefill_tc(a, ws, s, true);
+        return launch_prefill_tc(a, ws, s, true, dec, dec_blocks);
     }
     Args a1 = a, a2 = a;
     a1.c_hi = m;
@@ -166,7 +172,7 @@ cudaError_t prefill_tc(const gdr_dims *dims, const Args &a, float *ws, int32_t *
     if (e == cudaSuccess) e = launch_prefill_tc(a1, ws, s, false);
     if (e == cudaSuccess) e = launch_factors(a2, ws, err, s, true);
     // an ordinary launch: it reads the state the first scan writes
-    if (e == cudaSuccess) e = launch_prefill_tc(a2, ws, s, false);
+    if (e == cudaSuccess) e = launch_prefill_tc(a2, ws, s, false, dec, dec_blocks);
     return e;
 }
 
@@ -204,7 +210,7 @@ namespace {
 gdr_status prefill(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens, int64_t t_total,
                    const void *q, const void *k, const void *v, const float *g, const float *beta,
                    float *state, void *o, void *workspace, size_t workspace_bytes, gdr_stream_t stream,
-                   bool allow_split) {
+                   bool allow_split, const Args *dec = nullptr) {
     gdr_status st = check_dims(dims);
     if (st != GDR_OK) return st;
     if (n_seqs < 0 || t_total < 0) return GDR_ERR_INVALID_ARG;
@@ -228,12 +234,18 @@ gdr_status prefill(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqle
     a.snapshot = nullptr;
     a.o = o;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (t_total == 0) return GDR_OK;  // every sequence empty: states unchanged
+    if (t_total == 0) {  // every sequence empty: states unchanged
+        if (!dec) return GDR_OK;
+        int32_t *err = device_error_word();
+        if (!err) return GDR_ERR_CUDA;
+        return from_cuda(launch_decode(*dec, err, s, false));
+    }
     if (use_tensor_core_prefill(dims)) {
         int32_t *err = device_error_word();
         if (!err) return GDR_ERR_CUDA;
-        return from_cuda(prefill_tc(dims, a, static_cast<float *>(workspace), err, s, allow_split));
+        return from_cuda(prefill_tc(dims, a, static_cast<float *>(workspace), err, s, allow_split, dec));
     }
+    if (dec) return GDR_ERR_UNSUPPORTED;
     return from_cuda(launch_chunk_cc(a, s));
 }
 
@@ -322,6 +334,36 @@ gdr_status gdr_prefill_chunked_static(const gdr_dims *dims, int32_t n_seqs, cons
         if (!ws) return GDR_ERR_CUDA;
     }
     return prefill(dims, n_seqs, cu_seqlens, t_total, q, k, v, g, beta, state, o, ws, need, stream, false);
+}
+
+gdr_status gdr_prefill_with_decode(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens, int64_t t_total,
+                                   const void *q, const void *k, const void *v, const float *g, const float *beta,
+                                   float *state, void *o, void *workspace, size_t workspace_bytes, int32_t dec_batch,
+                                   const void *dq, const void *dk, const void *dv, const float *dg, const float *dbeta,
+                                   float *dstate, void *d_o, gdr_stream_t stream) {
+    gdr_status st = check_dims(dims);
+    if (st != GDR_OK) return st;
+    if (!use_tensor_core_prefill(dims)) return GDR_ERR_UNSUPPORTED;
+    if (dec_batch < 0) return GDR_ERR_INVALID_ARG;
+    if (dec_batch == 0)
+        return prefill(dims, n_seqs, cu_seqlens, t_total, q, k, v, g, beta, state, o, workspace, workspace_bytes,
+                       stream, true);
+    if (!tensors_ok(dq, dk, dv, dg, dbeta, dstate, d_o) || dstate == state) return GDR_ERR_INVALID_ARG;
+    Args d = make_args(dims);
+    d.n_seqs = dec_batch;
+    d.cu_seqlens = nullptr;
+    d.fixed_len = 1;
+    d.t_total = dec_batch;
+    d.q = dq;
+    d.k = dk;
+    d.v = dv;
+    d.g = dg;
+    d.beta = dbeta;
+    d.state = dstate;
+    d.snapshot = nullptr;
+    d.o = d_o;
+    return prefill(dims, n_seqs, cu_seqlens, t_total, q, k, v, g, beta, state, o, workspace, workspace_bytes, stream,
+                   true, &d);
 }
 
 }  // extern "C"

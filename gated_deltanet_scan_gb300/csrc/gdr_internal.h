@@ -51,7 +51,11 @@ cudaError_t launch_factors(const Args &a, float *ws, int32_t *err, cudaStream_t 
 // it on `s` (its prologue overlaps that grid; it reads the workspace only after
 // griddepcontrol.wait).  Only directly after the factor launch whose slots it
 // reads: the kernel waits for nothing else.
-cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s, bool overlap);
+// `dec` (optional): one decode step of another batch (dec->n_seqs sequences, one
+// token each, dims as `a`) carried by `dec_blocks` extra blocks of the same
+// launch, on the SMs the scan leaves free.
+cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s, bool overlap, const Args *dec = nullptr,
+                              int dec_blocks = 0);
 
 // One run of the chunk scan: chunks [c_lo, c_hi) of every sequence from and into
 // `state` ([n_seqs][h_v][128][128] fp32), outputs to `o` (bf16 when out_bf16),
@@ -65,7 +69,8 @@ struct TcRun {
     void *o;
 };
 cudaError_t launch_prefill_tc_runs(const Args &a, const TcRun *runs, int n_runs, const float *ws, cudaStream_t s,
-                                   bool overlap);
+                                   bool overlap,
+                                   const Args *dec = nullptr, int dec_blocks = 0);
 cudaError_t launch_copy_f32(const float *src, float *dst, size_t n, cudaStream_t s);
 // y = w * o / sqrt(mean(o^2) + eps) * silu(z) for `rows` rows of d values (gdr_norm.cu).
 cudaError_t launch_gated_rmsnorm(int64_t rows, int d, const void *o, int o_bf16, const void *z, int z_bf16,

@@ -740,9 +740,8 @@ __device__ void chain_role(const Ctx &x, const TcParams &p, const TcRun &run, in
 }
 
 template <bool QKN>
-__global__ void __launch_bounds__(NTHREADS, 1)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
-                      const __grid_constant__ CUtensorMap tmV, TcParams p) {
+__device__ __forceinline__ void prefill_tc_body(const CUtensorMap &tmK, const CUtensorMap &tmQ,
+                                                const CUtensorMap &tmV, const TcParams &p) {
     extern __shared__ uint8_t smem_raw[];
     Ctx x;
     x.sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -853,11 +852,214 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
+template <bool QKN>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmV, TcParams p) {
+    prefill_tc_body<QKN>(tmK, tmQ, tmV, p);
+}
+
+// ============================ decode blocks (mixed launch) ===========================
+// A chunk-scan launch can carry one decode step of another batch (continuous
+// batching: prefill chunks and decode steps in one launch).  The blocks after
+// the scan's CTAs take the SMs the scan leaves free and walk the batch's
+// (sequence, V head) pairs, block j taking pairs j, j + n_blocks, ...  Each
+// step is the one-token rule of gdr_decode.cu with the same arithmetic, in the
+// same order (so the results are bit-identical to gdr_decode_step's): with
+// d = exp(g), y = S^T k, z = S^T q, delta = beta (v - d y),
+//     o = scale (d z + (q.k) delta),      S' = d S + k delta^T.
+// A block uses the CTA's large shared memory as a ring of three state buffers:
+// one thread bulk-copies the state and the q, k, v rows of a pair three pairs
+// ahead of the 256 threads that compute (thread t: column quad t % 32 of every
+// 8th row; the row groups' partial S^T k and S^T q are summed through a table).
+struct DecBatch {
+    int n_pairs;   // batch * h_v (0: no decode blocks)
+    int n_blocks;  // decode blocks after the scan's CTAs
+    int h_qk, h_v;
+    int in_bf16, out_bf16, qk_norm, beta_logits;
+    float scale;
+    const void *q, *k, *v;
+    const float *g, *beta;
+    float *state;
+    void *o;
+};
+
+constexpr int DEC_NBUF = 3;
+constexpr int DEC_NT = 256;                          // compute threads (warps 0-7)
+constexpr uint32_t DEC_SBYTES = D * D * 4;           // one state
+constexpr uint32_t DEC_VEC = 512;                    // room for one q, k or v row (fp32 at most)
+constexpr uint32_t DEC_BUF = DEC_SBYTES + 3 * DEC_VEC;
+constexpr uint32_t DEC_OFF_RED = DEC_NBUF * DEC_BUF;           // [8][D] partial sums
+constexpr uint32_t DEC_OFF_SMALL = DEC_OFF_RED + 8 * D * 4;    // s_qk, s_rk, s_rq
+constexpr uint32_t DEC_OFF_BARS = DEC_OFF_SMALL + 16;          // DEC_NBUF mbarriers
+constexpr uint32_t DEC_OFF_FLAG = DEC_OFF_BARS + 8 * DEC_NBUF;
+static_assert(DEC_OFF_FLAG + 16 <= SMEM_USED, "the decode ring fits in the scan's shared memory");
+
+__device__ __forceinline__ float dec_in(const uint8_t *row, int i, int is_bf16) {
+    return is_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(row)[i])
+                   : reinterpret_cast<const float *>(row)[i];
+}
+
+__device__ __forceinline__ void dec_issue(const DecBatch &d, uint8_t *sm, int buf, int pr) {
+    const uint32_t bar = smem_u32(sm + DEC_OFF_BARS + 8 * buf);
+    const uint32_t dst = smem_u32(sm + (size_t)buf * DEC_BUF);
+    const int b = pr / d.h_v, h = pr - b * d.h_v, hq = h / (d.h_v / d.h_qk);
+    const uint32_t rowb = (uint32_t)D * (d.in_bf16 ? 2u : 4u);
+    mbar_arrive_expect_tx(bar, DEC_SBYTES + 3 * rowb);
+    const uint8_t *S = reinterpret_cast<const uint8_t *>(d.state + (size_t)pr * D * D);
+#pragma unroll
+    for (uint32_t i = 0; i < 4; ++i) bulk_load(dst + i * 16384u, S + i * 16384u, 16384u, bar);
+    const size_t qk_off = ((size_t)b * d.h_qk + hq) * rowb;
+    bulk_load(dst + DEC_SBYTES, reinterpret_cast<const uint8_t *>(d.q) + qk_off, rowb, bar);
+    bulk_load(dst + DEC_SBYTES + DEC_VEC, reinterpret_cast<const uint8_t *>(d.k) + qk_off, rowb, bar);
+    bulk_load(dst + DEC_SBYTES + 2 * DEC_VEC, reinterpret_cast<const uint8_t *>(d.v) + (size_t)pr * rowb, rowb,
+              bar);
+}
+
+__device__ void decode_blocks(const DecBatch &d, int dblk) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int npairs = dblk < d.n_pairs ? (d.n_pairs - dblk + d.n_blocks - 1) / d.n_blocks : 0;
+    float *red = reinterpret_cast<float *>(sm + DEC_OFF_RED);
+    float *small = reinterpret_cast<float *>(sm + DEC_OFF_SMALL);
+    volatile int *stop = reinterpret_cast<volatile int *>(sm + DEC_OFF_FLAG);
+    const bool producer = tid == DEC_NT;
+    if (producer) {
+        for (int i = 0; i < DEC_NBUF; ++i) mbar_init(smem_u32(sm + DEC_OFF_BARS + 8 * i), 1);
+        fence_mbar_init();
+        *stop = 0;
+        for (int i = 0; i < DEC_NBUF && i < npairs; ++i) dec_issue(d, sm, i, dblk + i * d.n_blocks);
+    }
+    __syncthreads();
+    constexpr int Q4 = D / 4, RSTEP = DEC_NT / Q4, NR = D / RSTEP;
+    const int cq = tid % Q4, rg = tid / Q4;
+    const uint32_t rowb = (uint32_t)D * (d.in_bf16 ? 2u : 4u);
+    for (int i = 0; i < npairs; ++i) {
+        const int buf = i % DEC_NBUF, pr = dblk + i * d.n_blocks;
+        const uint8_t *base = sm + (size_t)buf * DEC_BUF;
+        const float4 *sS = reinterpret_cast<const float4 *>(base);
+        const uint8_t *qrow = base + DEC_SBYTES, *krow = qrow + DEC_VEC, *vrow = krow + DEC_VEC;
+        if (tid < DEC_NT) {
+            const float dgate = __expf(d.g[pr]);
+            const float bt = beta_of(d.beta[pr], d.beta_logits);
+            const bool ok = mbar_wait_bounded(smem_u32(sm + DEC_OFF_BARS + 8 * buf), (uint32_t)(i / DEC_NBUF) & 1u,
+                                              kWaitLimit);
+            if (!ok) {
+                *stop = 1;
+                atomicCAS(&g_device_error, 0, (int32_t)GDR_ERR_DEVICE_TIMEOUT);
+            }
+            named_sync(BAR_CHAIN, DEC_NT);
+            if (*stop) goto release;
+            {
+                float vv[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) vv[c] = dec_in(vrow, 4 * cq + c, d.in_bf16);
+                if (d.qk_norm && warp < 2) {
+                    const uint8_t *xr = warp == 0 ? krow : qrow;
+                    float ss = 0.f;
+                    for (int j = lane; j < D; j += 32) {
+                        const float xv = dec_in(xr, j, d.in_bf16);
+                        ss = fmaf(xv, xv, ss);
+                    }
+                    ss = warp_sum(ss);
+                    if (lane == 0) small[warp == 0 ? 1 : 2] = l2norm_scale(ss);
+                }
+                float4 y = make_float4(0.f, 0.f, 0.f, 0.f), z = y;
+#pragma unroll
+                for (int k = 0; k < NR; ++k) {
+                    const int r = rg + k * RSTEP;
+                    const float4 sv = sS[r * Q4 + cq];
+                    const float kr = dec_in(krow, r, d.in_bf16), qr = dec_in(qrow, r, d.in_bf16);
+                    y.x = fmaf(sv.x, kr, y.x);
+                    y.y = fmaf(sv.y, kr, y.y);
+                    y.z = fmaf(sv.z, kr, y.z);
+                    y.w = fmaf(sv.w, kr, y.w);
+                    z.x = fmaf(sv.x, qr, z.x);
+                    z.y = fmaf(sv.y, qr, z.y);
+                    z.z = fmaf(sv.z, qr, z.z);
+                    z.w = fmaf(sv.w, qr, z.w);
+                }
+                *reinterpret_cast<float4 *>(red + rg * D + 4 * cq) = y;
+                if (warp == 0) {
+                    float pq = 0.f;
+                    for (int j = lane; j < D; j += 32) pq = fmaf(dec_in(krow, j, d.in_bf16), dec_in(qrow, j, d.in_bf16), pq);
+                    pq = warp_sum(pq);
+                    if (lane == 0) small[0] = pq;
+                }
+                named_sync(BAR_CHAIN, DEC_NT);
+                const float rk = d.qk_norm ? small[1] : 1.f, rq = d.qk_norm ? small[2] : 1.f;
+                float delta[4], zt[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float ys = 0.f;
+#pragma unroll 8
+                    for (int w = 0; w < RSTEP; ++w) ys += red[w * D + 4 * cq + c];
+                    delta[c] = bt * (vv[c] - dgate * rk * ys);
+                }
+                named_sync(BAR_CHAIN, DEC_NT);
+                *reinterpret_cast<float4 *>(red + rg * D + 4 * cq) = z;
+                named_sync(BAR_CHAIN, DEC_NT);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float zs = 0.f;
+#pragma unroll 8
+                    for (int w = 0; w < RSTEP; ++w) zs += red[w * D + 4 * cq + c];
+                    zt[c] = rq * zs;
+                }
+                if (rg == 0) {
+                    const float qk = small[0] * rq * rk;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        store_out(d.o, (size_t)pr * D + 4 * cq + c, d.scale * fmaf(dgate, zt[c], qk * delta[c]),
+                                  d.out_bf16);
+                }
+                float4 *Sg = reinterpret_cast<float4 *>(d.state + (size_t)pr * D * D);
+#pragma unroll
+                for (int k = 0; k < NR; ++k) {
+                    const int r = rg + k * RSTEP;
+                    const float4 sv = sS[r * Q4 + cq];
+                    const float kr = rk * dec_in(krow, r, d.in_bf16);
+                    const float4 nv = make_float4(fmaf(dgate, sv.x, kr * delta[0]), fmaf(dgate, sv.y, kr * delta[1]),
+                                                  fmaf(dgate, sv.z, kr * delta[2]), fmaf(dgate, sv.w, kr * delta[3]));
+                    __stcs(&Sg[r * Q4 + cq], nv);
+                }
+            }
+        }
+    release:
+        __syncthreads();  // every read of this buffer (and of the table) is done
+        if (*stop) break;
+        if (producer && i + DEC_NBUF < npairs) dec_issue(d, sm, buf, dblk + (i + DEC_NBUF) * d.n_blocks);
+    }
+    (void)rowb;
+    if (producer && *stop) {
+        // let the copies in flight land before the shared memory is released
+        for (int b = 0; b < DEC_NBUF; ++b) {
+            mbar_wait_bounded(smem_u32(sm + DEC_OFF_BARS + 8 * b), 0, kWaitLimit / 16);
+            mbar_wait_bounded(smem_u32(sm + DEC_OFF_BARS + 8 * b), 1, kWaitLimit / 16);
+        }
+    }
+}
+
+template <bool QKN>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    prefill_tc_mixed_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ,
+                            const __grid_constant__ CUtensorMap tmV, TcParams p, DecBatch d) {
+    const int n_scan = p.n_runs * p.n_seqs * p.h_v * NCOL;
+    if ((int)blockIdx.x >= n_scan) {
+        decode_blocks(d, (int)blockIdx.x - n_scan);
+        return;
+    }
+    prefill_tc_body<QKN>(tmK, tmQ, tmV, p);
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_tc_runs(const Args &a, const TcRun *runs, int n_runs, const float *ws, cudaStream_t s,
-                                   bool overlap) {
+                                   bool overlap, const Args *dec, int dec_blocks) {
     if (a.n_seqs == 0 || a.t_total == 0 || n_runs == 0) return cudaSuccess;  // nothing to walk
+    if (dec && (dec->n_seqs <= 0 || dec_blocks <= 0 || dec->d != D)) return cudaErrorInvalidValue;
     if (n_runs < 0 || n_runs > kMaxTcRuns) return cudaErrorInvalidValue;
     CUtensorMap tmK, tmQ, tmV;
     if (!encode_bf16_3d(&tmK, a.k, D, (uint64_t)a.h_qk, (uint64_t)a.t_total, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -874,6 +1076,12 @@ cudaError_t launch_prefill_tc_runs(const Args &a, const TcRun *runs, int n_runs,
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefill_tc_mixed_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(prefill_tc_mixed_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
@@ -889,7 +1097,8 @@ cudaError_t launch_prefill_tc_runs(const Args &a, const TcRun *runs, int n_runs,
     p.xs = reinterpret_cast<const uint8_t *>(ws) + fac::x_region_offset(fac::n_slots(a.t_total, a.n_seqs), a.h_v);
     for (int i = 0; i < n_runs; ++i) p.runs[i] = runs[i];
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)n_runs * (unsigned)a.n_seqs * (unsigned)a.h_v * (unsigned)NCOL);
+    const unsigned n_scan = (unsigned)n_runs * (unsigned)a.n_seqs * (unsigned)a.h_v * (unsigned)NCOL;
+    cfg.gridDim = dim3(n_scan + (dec ? (unsigned)dec_blocks : 0u));
     cfg.blockDim = dim3(NTHREADS);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = s;
@@ -898,11 +1107,33 @@ cudaError_t launch_prefill_tc_runs(const Args &a, const TcRun *runs, int n_runs,
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = overlap ? &attr : nullptr;
     cfg.numAttrs = overlap ? 1 : 0;
+    if (dec) {
+        DecBatch d = {};
+        d.n_pairs = dec->n_seqs * dec->h_v;
+        d.n_blocks = dec_blocks;
+        d.h_qk = dec->h_qk;
+        d.h_v = dec->h_v;
+        d.in_bf16 = dec->in_bf16;
+        d.out_bf16 = dec->out_bf16;
+        d.qk_norm = dec->qk_norm;
+        d.beta_logits = dec->beta_logits;
+        d.scale = dec->scale;
+        d.q = dec->q;
+        d.k = dec->k;
+        d.v = dec->v;
+        d.g = dec->g;
+        d.beta = dec->beta;
+        d.state = dec->state;
+        d.o = dec->o;
+        return a.qk_norm ? cudaLaunchKernelEx(&cfg, prefill_tc_mixed_kernel<true>, tmK, tmQ, tmV, p, d)
+                         : cudaLaunchKernelEx(&cfg, prefill_tc_mixed_kernel<false>, tmK, tmQ, tmV, p, d);
+    }
     return a.qk_norm ? cudaLaunchKernelEx(&cfg, prefill_tc_kernel<true>, tmK, tmQ, tmV, p)
                      : cudaLaunchKernelEx(&cfg, prefill_tc_kernel<false>, tmK, tmQ, tmV, p);
 }
 
-cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s, bool overlap) {
+cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s, bool overlap, const Args *dec,
+                              int dec_blocks) {
     TcRun run = {};
     run.c_lo = a.c_lo;
     run.c_hi = a.c_hi;
@@ -910,7 +1141,7 @@ cudaError_t launch_prefill_tc(const Args &a, const float *ws, cudaStream_t s, bo
     run.v_zero = 0;
     run.state = a.state;
     run.o = a.o;
-    return launch_prefill_tc_runs(a, &run, 1, ws, s, overlap);
+    return launch_prefill_tc_runs(a, &run, 1, ws, s, overlap, dec, dec_blocks);
 }
 
 int32_t *device_error_word() {

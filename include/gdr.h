@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define GDR_ABI_VERSION 8
+#define GDR_ABI_VERSION 9
 
 /* Same object as cudaStream_t; declared here so callers need no CUDA header. */
 typedef struct CUstream_st *gdr_stream_t;
@@ -297,6 +297,34 @@ gdr_status gdr_decode_step(const gdr_dims *dims, int32_t batch, const void *q, c
 gdr_status gdr_decode_step_overlapped(const gdr_dims *dims, int32_t batch, const void *q, const void *k,
                                       const void *v, const float *g, const float *beta, float *state,
                                       void *o, gdr_stream_t stream);
+
+/*
+ * A prefill and one decode step of another batch in the same chunk-scan launch:
+ * the continuous batching of prefill chunks and decode steps (the mixed batch of
+ * serving; the prefill-to-decode handoff of a sequence is two calls, since a
+ * decode step reads the state its prefill leaves).  The prefill is exactly
+ * gdr_prefill_chunked(dims, n_seqs, cu_seqlens, t_total, q, k, v, g, beta,
+ * state, o, workspace, workspace_bytes, stream), launches and results alike,
+ * except that its last chunk-scan launch carries extra blocks on the SMs the
+ * scan leaves free (one per free SM, at least one), which walk the decode
+ * batch's (sequence, V head) pairs with the arithmetic of gdr_decode_step:
+ * do_ and dstate come out bit-identical to gdr_decode_step(dims, dec_batch, dq,
+ * dk, dv, dg, dbeta, dstate, d_o, stream).  The decode tensors have the
+ * decode layouts (dq, dk [dec_batch][H_qk][d_k]; dv, d_o [dec_batch][H_v][d_v];
+ * dg, dbeta [dec_batch][H_v]; dstate [dec_batch][H_v][d_k][d_v]) and must not
+ * overlap the prefill's.  Only the tensor-core prefill shapes (bf16 inputs,
+ * d_k = 128, chunk 64) have this launch (else GDR_ERR_UNSUPPORTED, nothing
+ * launched); the gated output norm is not offered here.  dec_batch = 0 is
+ * gdr_prefill_chunked; t_total = 0 is gdr_decode_step.  Errors: as
+ * gdr_prefill_chunked, plus GDR_ERR_INVALID_ARG for a null or unaligned
+ * decode tensor or dstate == state; device-side wait timeouts of the decode
+ * blocks are reported as GDR_ERR_DEVICE_TIMEOUT through gdr_device_error.
+ */
+gdr_status gdr_prefill_with_decode(const gdr_dims *dims, int32_t n_seqs, const int32_t *cu_seqlens, int64_t t_total,
+                                   const void *q, const void *k, const void *v, const float *g, const float *beta,
+                                   float *state, void *o, void *workspace, size_t workspace_bytes, int32_t dec_batch,
+                                   const void *dq, const void *dk, const void *dv, const float *dg, const float *dbeta,
+                                   float *dstate, void *d_o, gdr_stream_t stream);
 
 /*
  * gdr_decode_step with the gated RMSNorm after the rule fused into it: instead of

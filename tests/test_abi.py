@@ -217,3 +217,19 @@ def test_flags_and_gated_rmsnorm_checks(L):
     gated = L.gdr_decode_step_gated
     assert gated(ctypes.byref(dims()), 1, A, A, A, A, A, A, None, A, 1e-6, A, None) == gdr.GDR_ERR_INVALID_ARG
     assert gated(ctypes.byref(dims()), 1, A, A, A, A, A, A, A, MISALIGNED, 1e-6, A, None) == gdr.GDR_ERR_INVALID_ARG
+
+
+def test_prefill_with_decode_checks(L):
+    """Host-side rejections of the mixed prefill + decode launch (nothing launched)."""
+    d = dims()
+
+    def args(dd=d, nd=4, dq=A, dstate=B):
+        # dims, n_seqs, cu, T, q, k, v, g, beta, state, o, ws, ws_bytes, dec_batch, dq, dk, dv, dg, dbeta, dstate, do
+        return (ctypes.byref(dd), 1, A, 4096, A, A, A, A, A, A, A, A, 1 << 30, nd, dq, A, A, A, A, dstate, A, None)
+    assert L.gdr_prefill_with_decode(*args(dd=dims(in_dtype=gdr.GDR_F32))) == gdr.GDR_ERR_UNSUPPORTED
+    assert L.gdr_prefill_with_decode(*args(dd=dims(chunk=16))) == gdr.GDR_ERR_UNSUPPORTED
+    assert L.gdr_prefill_with_decode(*args(dd=dims(h_v=30))) == gdr.GDR_ERR_INVALID_ARG
+    assert L.gdr_prefill_with_decode(*args(nd=-1)) == gdr.GDR_ERR_INVALID_ARG
+    assert L.gdr_prefill_with_decode(*args(dq=None)) == gdr.GDR_ERR_INVALID_ARG
+    assert L.gdr_prefill_with_decode(*args(dq=MISALIGNED)) == gdr.GDR_ERR_INVALID_ARG
+    assert L.gdr_prefill_with_decode(*args(dstate=A)) == gdr.GDR_ERR_INVALID_ARG  # the prefill's own state
