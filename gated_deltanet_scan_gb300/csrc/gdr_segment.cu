@@ -159,12 +159,38 @@ struct FixParams {
     void *o;
 };
 
-constexpr int FIX_TOK = 64, M_LD = D + 4;
-constexpr int FIX_SMEM = (FIX_TOK * M_LD + D * D) * (int)sizeof(float);
+constexpr int FIX_TOK = 64, M_LD = D + 4, X_LD = D + 4;
+constexpr int FIX_SMEM = (FIX_TOK * M_LD + D * X_LD) * (int)sizeof(float);
+
+// bf16 hi and lo words of the pair (x0, x1): hi = the top 16 bits of each, lo =
+// bf16(x - hi); x0 in the low half.
+__device__ __forceinline__ void hilo2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const uint32_t a = __float_as_uint(x0), b = __float_as_uint(x1);
+    hi = __byte_perm(a, b, 0x7632);
+    __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __uint_as_float(a & 0xFFFF0000u), x1 - __uint_as_float(b & 0xFFFF0000u));
+    lo = *reinterpret_cast<uint32_t *>(&l);
+}
+// d += A B for one 16 x 8 tile (m16n8k16, bf16 operands, fp32 accumulation;
+// lane = 4 g + c holds rows g, g + 8 and columns 2c, 2c + 1 of d).
+__device__ __forceinline__ void mma_bf16x(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// One block per (64-token chunk of a later segment, sequence x V head): the
+// chunk's maps m (64 x d_k) and its segment's start state X (d_k x d_v) staged in
+// shared memory by cp.async, then O = o0 + M X on warp-level bf16 tensor-core
+// MMAs, each fp32 operand split into bf16 hi + lo parts and three products
+// (hi hi + hi lo + lo hi) accumulated in fp32: 2^-16 relative precision, as the
+// chunk scan's state products.  Warp w takes tokens 32 (w & 1) .. + 31 and
+// columns 64 (w >> 1) .. + 63.
 __global__ void __launch_bounds__(128, 2) fixup_kernel(FixParams p) {
     extern __shared__ __align__(16) float fsm[];
     float *ms = fsm;                    // [FIX_TOK][M_LD]
-    float *xs = fsm + FIX_TOK * M_LD;   // [D][D]
+    float *xs = fsm + FIX_TOK * M_LD;   // [D][X_LD]
     const int c = p.cuts[1] + (int)blockIdx.x;      // chunk index within the sequence
     const int s = (int)blockIdx.y / p.h_v, h = (int)blockIdx.y % p.h_v;
     int seg = 1;  // the segment of chunk c (static indices: the cuts stay in the parameter space)
@@ -178,70 +204,79 @@ __global__ void __launch_bounds__(128, 2) fixup_kernel(FixParams p) {
     const float *X = p.xseg + (((size_t)(seg - 1) * p.n_seqs + s) * p.h_v + h) * D * D;
     const int tid = threadIdx.x;
 #pragma unroll 4
-    for (int i = tid; i < D * D / 4; i += 128) cp_async16(xs + 4 * i, X + 4 * (size_t)i);
+    for (int i = tid; i < D * D / 4; i += 128) {
+        const int r = i / (D / 4), q4 = i % (D / 4);
+        cp_async16(xs + r * X_LD + 4 * q4, X + (size_t)r * D + 4 * q4);
+    }
 #pragma unroll 4
     for (int i = tid; i < FIX_TOK * (D / 4); i += 128) {
         const int t = i / (D / 4), q4 = i % (D / 4);
-        if (t < ntok) cp_async16(ms + t * M_LD + 4 * q4, p.m + ((size_t)(t0 + t) * p.h_v + h) * D + 4 * q4);
+        if (t < ntok)
+            cp_async16(ms + t * M_LD + 4 * q4, p.m + ((size_t)(t0 + t) * p.h_v + h) * D + 4 * q4);
+        else
+            *reinterpret_cast<float4 *>(ms + t * M_LD + 4 * q4) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     cp_async_wait_all();
     __syncthreads();
-    const int tg = tid >> 4, cg = tid & 15;  // tokens 8 tg .. + 7, columns 8 cg .. + 7
-    float acc[8][8];
+    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, cc = lane & 3;
+    const int tb = 32 * (warp & 1), nb = 64 * (warp >> 1);
+    float acc[2][8][4];
 #pragma unroll
-    for (int a = 0; a < 8; ++a)
+    for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[a][j] = 0.f;
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
 #pragma unroll 1
-    for (int i4 = 0; i4 < D / 4; ++i4) {
-        float xv[4][8];
+    for (int k0 = 0; k0 < D; k0 += 16) {
+        uint32_t ah[2][4], al[2][4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 x0 = *reinterpret_cast<const float4 *>(xs + (4 * i4 + q) * D + 8 * cg);
-            const float4 x1 = *reinterpret_cast<const float4 *>(xs + (4 * i4 + q) * D + 8 * cg + 4);
-            xv[q][0] = x0.x;
-            xv[q][1] = x0.y;
-            xv[q][2] = x0.z;
-            xv[q][3] = x0.w;
-            xv[q][4] = x1.x;
-            xv[q][5] = x1.y;
-            xv[q][6] = x1.z;
-            xv[q][7] = x1.w;
+        for (int mt = 0; mt < 2; ++mt) {
+            const float *mr = ms + (tb + 16 * mt + g) * M_LD + k0 + 2 * cc;
+            const float2 v0 = *reinterpret_cast<const float2 *>(mr);
+            const float2 v1 = *reinterpret_cast<const float2 *>(mr + 8 * M_LD);
+            const float2 v2 = *reinterpret_cast<const float2 *>(mr + 8);
+            const float2 v3 = *reinterpret_cast<const float2 *>(mr + 8 * M_LD + 8);
+            hilo2(v0.x, v0.y, ah[mt][0], al[mt][0]);
+            hilo2(v1.x, v1.y, ah[mt][1], al[mt][1]);
+            hilo2(v2.x, v2.y, ah[mt][2], al[mt][2]);
+            hilo2(v3.x, v3.y, ah[mt][3], al[mt][3]);
         }
 #pragma unroll
-        for (int a = 0; a < 8; ++a) {
-            const float4 m4 = *reinterpret_cast<const float4 *>(ms + (8 * tg + a) * M_LD + 4 * i4);
-            const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+        for (int nt = 0; nt < 8; ++nt) {
+            const float *xr = xs + (k0 + 2 * cc) * X_LD + nb + 8 * nt + g;
+            uint32_t b0h, b0l, b1h, b1l;
+            hilo2(xr[0], xr[X_LD], b0h, b0l);
+            hilo2(xr[8 * X_LD], xr[9 * X_LD], b1h, b1l);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[a][j] = fmaf(mv[q], xv[q][j], acc[a][j]);
-        }
-    }
-#pragma unroll
-    for (int a = 0; a < 8; ++a) {
-        const int t = 8 * tg + a;
-        if (t >= ntok) break;
-        const size_t orow = ((size_t)(t0 + t) * p.h_v + h) * D + 8 * cg;
-        const float4 b0 = *reinterpret_cast<const float4 *>(p.o0 + orow);
-        const float4 b1 = *reinterpret_cast<const float4 *>(p.o0 + orow + 4);
-        const float y[8] = {b0.x + acc[a][0], b0.y + acc[a][1], b0.z + acc[a][2], b0.w + acc[a][3],
-                            b1.x + acc[a][4], b1.y + acc[a][5], b1.z + acc[a][6], b1.w + acc[a][7]};
-        if (p.out_bf16) {
-            uint4 pk;
-            __nv_bfloat162 v0 = __floats2bfloat162_rn(y[0], y[1]), v1 = __floats2bfloat162_rn(y[2], y[3]),
-                            v2 = __floats2bfloat162_rn(y[4], y[5]), v3 = __floats2bfloat162_rn(y[6], y[7]);
-            pk.x = *reinterpret_cast<uint32_t *>(&v0);
-            pk.y = *reinterpret_cast<uint32_t *>(&v1);
-            pk.z = *reinterpret_cast<uint32_t *>(&v2);
-            pk.w = *reinterpret_cast<uint32_t *>(&v3);
-            *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + orow) = pk;
-        } else {
-            float *dst = reinterpret_cast<float *>(p.o) + orow;
-            *reinterpret_cast<float4 *>(dst) = make_float4(y[0], y[1], y[2], y[3]);
-            *reinterpret_cast<float4 *>(dst + 4) = make_float4(y[4], y[5], y[6], y[7]);
+            for (int mt = 0; mt < 2; ++mt) {
+                mma_bf16x(acc[mt][nt], ah[mt], b0h, b1h);
+                mma_bf16x(acc[mt][nt], ah[mt], b0l, b1l);
+                mma_bf16x(acc[mt][nt], al[mt], b0h, b1h);
+            }
         }
     }
+    // o = o0 + acc: rows tb + 16 mt + g (+ 8), columns nb + 8 nt + 2 cc (+ 1)
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int t = tb + 16 * mt + g + 8 * hh;
+            if (t >= ntok) continue;
+            const size_t orow = ((size_t)(t0 + t) * p.h_v + h) * D;
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                const int col = nb + 8 * nt + 2 * cc;
+                const float2 b = *reinterpret_cast<const float2 *>(p.o0 + orow + col);
+                const float y0 = b.x + acc[mt][nt][2 * hh], y1 = b.y + acc[mt][nt][2 * hh + 1];
+                if (p.out_bf16) {
+                    __nv_bfloat162 v = __floats2bfloat162_rn(y0, y1);
+                    *reinterpret_cast<__nv_bfloat162 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + orow + col) = v;
+                } else {
+                    *reinterpret_cast<float2 *>(reinterpret_cast<float *>(p.o) + orow + col) = make_float2(y0, y1);
+                }
+            }
+        }
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
