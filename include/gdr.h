@@ -377,6 +377,10 @@ gdr_status gdr_gated_rmsnorm(const gdr_dims *dims, int64_t n_rows, const void *o
  *   deltas: NULL, or fp32 [n_seqs * n_tok][H_v][d_v] that receives each draft
  *     token's correction u_t = beta_t (v_t - e^{g_t} S_{t-1}^T k_t), where
  *     S_{t-1} is the state just before token t inside the block.
+ * With bf16 inputs the products with d-long inner dimensions run on warp-level
+ * tensor-core MMAs, the state split into bf16 hi and lo halves (2^-16
+ * relative, fp32 accumulation); fp32 inputs run on CUDA cores in fp32.
+ * n_tok = 0 writes the snapshot and leaves the state as it is.
  */
 gdr_status gdr_verify_block(const gdr_dims *dims, int32_t n_seqs, int32_t n_tok, const void *q,
                             const void *k, const void *v, const float *g, const float *beta,
