@@ -868,10 +868,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // same order (so the results are bit-identical to gdr_decode_step's): with
 // d = exp(g), y = S^T k, z = S^T q, delta = beta (v - d y),
 //     o = scale (d z + (q.k) delta),      S' = d S + k delta^T.
-// A block uses the CTA's large shared memory as a ring of three state buffers:
-// one thread bulk-copies the state and the q, k, v rows of a pair three pairs
-// ahead of the 256 threads that compute (thread t: column quad t % 32 of every
-// 8th row; the row groups' partial S^T k and S^T q are summed through a table).
+// A block uses the CTA's large shared memory as a ring of three state buffers,
+// filled three pairs ahead by bulk copies (the state and the q, k, v rows), and
+// splits each pair's work between two warp groups so that consecutive pairs
+// overlap: warps 0-7 (thread t: column quad t % 32 of every 8th row) form the
+// row groups' partial S^T k and S^T q, sum them through a table, and write
+// delta and o; warps 8-13 then write S' = d S + k delta^T of that pair from the
+// buffer while warps 0-7 go on to the next pair, and one of them refills the
+// buffer once every element has been read.
 struct DecBatch {
     int n_pairs;   // batch * h_v (0: no decode blocks)
     int n_blocks;  // decode blocks after the scan's CTAs
@@ -885,15 +889,19 @@ struct DecBatch {
 };
 
 constexpr int DEC_NBUF = 3;
-constexpr int DEC_NT = 256;                          // compute threads (warps 0-7)
+constexpr int DEC_NT = 256;                          // the reducing group (warps 0-7)
+constexpr int DEC_NW = NTHREADS - DEC_NT;            // the writing group (warps 8-13)
 constexpr uint32_t DEC_SBYTES = D * D * 4;           // one state
 constexpr uint32_t DEC_VEC = 512;                    // room for one q, k or v row (fp32 at most)
-constexpr uint32_t DEC_BUF = DEC_SBYTES + 3 * DEC_VEC;
+constexpr uint32_t DEC_PAR = (D + 4) * 4;            // delta (D floats), then d and 1 / |k|
+constexpr uint32_t DEC_BUF = DEC_SBYTES + 3 * DEC_VEC + DEC_PAR;
 constexpr uint32_t DEC_OFF_RED = DEC_NBUF * DEC_BUF;           // [8][D] partial sums
 constexpr uint32_t DEC_OFF_SMALL = DEC_OFF_RED + 8 * D * 4;    // s_qk, s_rk, s_rq
-constexpr uint32_t DEC_OFF_BARS = DEC_OFF_SMALL + 16;          // DEC_NBUF mbarriers
-constexpr uint32_t DEC_OFF_FLAG = DEC_OFF_BARS + 8 * DEC_NBUF;
+constexpr uint32_t DEC_OFF_BARS = DEC_OFF_SMALL + 16;          // full[DEC_NBUF], reduced[DEC_NBUF]
+constexpr uint32_t DEC_OFF_FLAG = DEC_OFF_BARS + 16 * DEC_NBUF;
+constexpr uint32_t DEC_BAR_R = 1, DEC_BAR_W = 2;               // named barriers of the two groups
 static_assert(DEC_OFF_FLAG + 16 <= SMEM_USED, "the decode ring fits in the scan's shared memory");
+static_assert(DEC_BUF % 16 == 0 && DEC_NW % 32 == 0, "alignment and whole warps");
 
 __device__ __forceinline__ float dec_in(const uint8_t *row, int i, int is_bf16) {
     return is_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(row)[i])
@@ -925,119 +933,140 @@ __device__ void decode_blocks(const DecBatch &d, int dblk) {
     float *red = reinterpret_cast<float *>(sm + DEC_OFF_RED);
     float *small = reinterpret_cast<float *>(sm + DEC_OFF_SMALL);
     volatile int *stop = reinterpret_cast<volatile int *>(sm + DEC_OFF_FLAG);
-    const bool producer = tid == DEC_NT;
+    auto full_bar = [&](int b) { return smem_u32(sm + DEC_OFF_BARS + 8 * b); };
+    auto reduced_bar = [&](int b) { return smem_u32(sm + DEC_OFF_BARS + 8 * (DEC_NBUF + b)); };
+    const bool producer = tid == DEC_NT;  // the writing group's first thread
     if (producer) {
-        for (int i = 0; i < DEC_NBUF; ++i) mbar_init(smem_u32(sm + DEC_OFF_BARS + 8 * i), 1);
+        for (int i = 0; i < 2 * DEC_NBUF; ++i) mbar_init(smem_u32(sm + DEC_OFF_BARS + 8 * i), 1);
         fence_mbar_init();
         *stop = 0;
         for (int i = 0; i < DEC_NBUF && i < npairs; ++i) dec_issue(d, sm, i, dblk + i * d.n_blocks);
     }
     __syncthreads();
     constexpr int Q4 = D / 4, RSTEP = DEC_NT / Q4, NR = D / RSTEP;
-    const int cq = tid % Q4, rg = tid / Q4;
-    const uint32_t rowb = (uint32_t)D * (d.in_bf16 ? 2u : 4u);
-    for (int i = 0; i < npairs; ++i) {
-        const int buf = i % DEC_NBUF, pr = dblk + i * d.n_blocks;
-        const uint8_t *base = sm + (size_t)buf * DEC_BUF;
-        const float4 *sS = reinterpret_cast<const float4 *>(base);
-        const uint8_t *qrow = base + DEC_SBYTES, *krow = qrow + DEC_VEC, *vrow = krow + DEC_VEC;
-        if (tid < DEC_NT) {
+    if (tid < DEC_NT) {
+        // ---- the reducing group: partial sums, delta and o of every pair, in order
+        const int cq = tid % Q4, rg = tid / Q4;
+        for (int i = 0; i < npairs; ++i) {
+            const int buf = i % DEC_NBUF, pr = dblk + i * d.n_blocks;
+            uint8_t *base = sm + (size_t)buf * DEC_BUF;
+            const float4 *sS = reinterpret_cast<const float4 *>(base);
+            const uint8_t *qrow = base + DEC_SBYTES, *krow = qrow + DEC_VEC, *vrow = krow + DEC_VEC;
+            float *par = reinterpret_cast<float *>(base + DEC_SBYTES + 3 * DEC_VEC);
             const float dgate = __expf(d.g[pr]);
             const float bt = beta_of(d.beta[pr], d.beta_logits);
-            const bool ok = mbar_wait_bounded(smem_u32(sm + DEC_OFF_BARS + 8 * buf), (uint32_t)(i / DEC_NBUF) & 1u,
-                                              kWaitLimit);
-            if (!ok) {
+            if (!mbar_wait_bounded(full_bar(buf), (uint32_t)(i / DEC_NBUF) & 1u, kWaitLimit)) {
                 *stop = 1;
                 atomicCAS(&g_device_error, 0, (int32_t)GDR_ERR_DEVICE_TIMEOUT);
             }
-            named_sync(BAR_CHAIN, DEC_NT);
-            if (*stop) goto release;
-            {
-                float vv[4];
+            named_sync(DEC_BAR_R, DEC_NT);
+            if (*stop) break;
+            float vv[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) vv[c] = dec_in(vrow, 4 * cq + c, d.in_bf16);
-                if (d.qk_norm && warp < 2) {
-                    const uint8_t *xr = warp == 0 ? krow : qrow;
-                    float ss = 0.f;
-                    for (int j = lane; j < D; j += 32) {
-                        const float xv = dec_in(xr, j, d.in_bf16);
-                        ss = fmaf(xv, xv, ss);
-                    }
-                    ss = warp_sum(ss);
-                    if (lane == 0) small[warp == 0 ? 1 : 2] = l2norm_scale(ss);
+            for (int c = 0; c < 4; ++c) vv[c] = dec_in(vrow, 4 * cq + c, d.in_bf16);
+            if (d.qk_norm && warp < 2) {
+                const uint8_t *xr = warp == 0 ? krow : qrow;
+                float ss = 0.f;
+                for (int j = lane; j < D; j += 32) {
+                    const float xv = dec_in(xr, j, d.in_bf16);
+                    ss = fmaf(xv, xv, ss);
                 }
-                float4 y = make_float4(0.f, 0.f, 0.f, 0.f), z = y;
+                ss = warp_sum(ss);
+                if (lane == 0) small[warp == 0 ? 1 : 2] = l2norm_scale(ss);
+            }
+            float4 y = make_float4(0.f, 0.f, 0.f, 0.f), z = y;
 #pragma unroll
-                for (int k = 0; k < NR; ++k) {
-                    const int r = rg + k * RSTEP;
-                    const float4 sv = sS[r * Q4 + cq];
-                    const float kr = dec_in(krow, r, d.in_bf16), qr = dec_in(qrow, r, d.in_bf16);
-                    y.x = fmaf(sv.x, kr, y.x);
-                    y.y = fmaf(sv.y, kr, y.y);
-                    y.z = fmaf(sv.z, kr, y.z);
-                    y.w = fmaf(sv.w, kr, y.w);
-                    z.x = fmaf(sv.x, qr, z.x);
-                    z.y = fmaf(sv.y, qr, z.y);
-                    z.z = fmaf(sv.z, qr, z.z);
-                    z.w = fmaf(sv.w, qr, z.w);
-                }
-                *reinterpret_cast<float4 *>(red + rg * D + 4 * cq) = y;
-                if (warp == 0) {
-                    float pq = 0.f;
-                    for (int j = lane; j < D; j += 32) pq = fmaf(dec_in(krow, j, d.in_bf16), dec_in(qrow, j, d.in_bf16), pq);
-                    pq = warp_sum(pq);
-                    if (lane == 0) small[0] = pq;
-                }
-                named_sync(BAR_CHAIN, DEC_NT);
-                const float rk = d.qk_norm ? small[1] : 1.f, rq = d.qk_norm ? small[2] : 1.f;
-                float delta[4], zt[4];
+            for (int k = 0; k < NR; ++k) {
+                const int r = rg + k * RSTEP;
+                const float4 sv = sS[r * Q4 + cq];
+                const float kr = dec_in(krow, r, d.in_bf16), qr = dec_in(qrow, r, d.in_bf16);
+                y.x = fmaf(sv.x, kr, y.x);
+                y.y = fmaf(sv.y, kr, y.y);
+                y.z = fmaf(sv.z, kr, y.z);
+                y.w = fmaf(sv.w, kr, y.w);
+                z.x = fmaf(sv.x, qr, z.x);
+                z.y = fmaf(sv.y, qr, z.y);
+                z.z = fmaf(sv.z, qr, z.z);
+                z.w = fmaf(sv.w, qr, z.w);
+            }
+            *reinterpret_cast<float4 *>(red + rg * D + 4 * cq) = y;
+            if (warp == 0) {
+                float pq = 0.f;
+                for (int j = lane; j < D; j += 32) pq = fmaf(dec_in(krow, j, d.in_bf16), dec_in(qrow, j, d.in_bf16), pq);
+                pq = warp_sum(pq);
+                if (lane == 0) small[0] = pq;
+            }
+            named_sync(DEC_BAR_R, DEC_NT);
+            const float rk = d.qk_norm ? small[1] : 1.f, rq = d.qk_norm ? small[2] : 1.f;
+            float delta[4], zt[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float ys = 0.f;
+#pragma unroll 8
+                for (int w = 0; w < RSTEP; ++w) ys += red[w * D + 4 * cq + c];
+                delta[c] = bt * (vv[c] - dgate * rk * ys);
+            }
+            named_sync(DEC_BAR_R, DEC_NT);
+            *reinterpret_cast<float4 *>(red + rg * D + 4 * cq) = z;
+            named_sync(DEC_BAR_R, DEC_NT);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float zs = 0.f;
+#pragma unroll 8
+                for (int w = 0; w < RSTEP; ++w) zs += red[w * D + 4 * cq + c];
+                zt[c] = rq * zs;
+            }
+            if (rg == 0) {
+                const float qk = small[0] * rq * rk;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    float ys = 0.f;
-#pragma unroll 8
-                    for (int w = 0; w < RSTEP; ++w) ys += red[w * D + 4 * cq + c];
-                    delta[c] = bt * (vv[c] - dgate * rk * ys);
+                    store_out(d.o, (size_t)pr * D + 4 * cq + c, d.scale * fmaf(dgate, zt[c], qk * delta[c]),
+                              d.out_bf16);
+                    par[4 * cq + c] = delta[c];
                 }
-                named_sync(BAR_CHAIN, DEC_NT);
-                *reinterpret_cast<float4 *>(red + rg * D + 4 * cq) = z;
-                named_sync(BAR_CHAIN, DEC_NT);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float zs = 0.f;
-#pragma unroll 8
-                    for (int w = 0; w < RSTEP; ++w) zs += red[w * D + 4 * cq + c];
-                    zt[c] = rq * zs;
-                }
-                if (rg == 0) {
-                    const float qk = small[0] * rq * rk;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        store_out(d.o, (size_t)pr * D + 4 * cq + c, d.scale * fmaf(dgate, zt[c], qk * delta[c]),
-                                  d.out_bf16);
-                }
-                float4 *Sg = reinterpret_cast<float4 *>(d.state + (size_t)pr * D * D);
-#pragma unroll
-                for (int k = 0; k < NR; ++k) {
-                    const int r = rg + k * RSTEP;
-                    const float4 sv = sS[r * Q4 + cq];
-                    const float kr = rk * dec_in(krow, r, d.in_bf16);
-                    const float4 nv = make_float4(fmaf(dgate, sv.x, kr * delta[0]), fmaf(dgate, sv.y, kr * delta[1]),
-                                                  fmaf(dgate, sv.z, kr * delta[2]), fmaf(dgate, sv.w, kr * delta[3]));
-                    __stcs(&Sg[r * Q4 + cq], nv);
+                if (cq == 0) {
+                    par[D] = dgate;
+                    par[D + 1] = rk;
                 }
             }
+            named_sync(DEC_BAR_R, DEC_NT);  // every read of the table and of `small` is done; delta is written
+            if (tid == 0) mbar_arrive(reduced_bar(buf));  // release: delta, d, 1 / |k| for the writing group
         }
-    release:
-        __syncthreads();  // every read of this buffer (and of the table) is done
-        if (*stop) break;
-        if (producer && i + DEC_NBUF < npairs) dec_issue(d, sm, buf, dblk + (i + DEC_NBUF) * d.n_blocks);
+    } else {
+        // ---- the writing group: S' = d S + k delta^T of every pair, then the refill
+        const int wt = tid - DEC_NT;
+        for (int i = 0; i < npairs; ++i) {
+            const int buf = i % DEC_NBUF, pr = dblk + i * d.n_blocks;
+            const uint8_t *base = sm + (size_t)buf * DEC_BUF;
+            const float4 *sS = reinterpret_cast<const float4 *>(base);
+            const uint8_t *krow = base + DEC_SBYTES + DEC_VEC;
+            const float *par = reinterpret_cast<const float *>(base + DEC_SBYTES + 3 * DEC_VEC);
+            bool ok = mbar_wait_bounded(reduced_bar(buf), (uint32_t)(i / DEC_NBUF) & 1u, kWaitLimit);
+            if (!ok || *stop) {
+                if (!ok) atomicCAS(&g_device_error, 0, (int32_t)GDR_ERR_DEVICE_TIMEOUT);
+                *stop = 1;
+                break;
+            }
+            const float dgate = par[D], rk = par[D + 1];
+            float4 *Sg = reinterpret_cast<float4 *>(d.state + (size_t)pr * D * D);
+            for (int e = wt; e < D * Q4; e += DEC_NW) {
+                const int r = e / Q4, cq = e - r * Q4;
+                const float4 sv = sS[e];
+                const float4 dl = *reinterpret_cast<const float4 *>(par + 4 * cq);
+                const float kr = rk * dec_in(krow, r, d.in_bf16);
+                __stcs(&Sg[e], make_float4(fmaf(dgate, sv.x, kr * dl.x), fmaf(dgate, sv.y, kr * dl.y),
+                                           fmaf(dgate, sv.z, kr * dl.z), fmaf(dgate, sv.w, kr * dl.w)));
+            }
+            named_sync(DEC_BAR_W, DEC_NW);  // every read of this buffer is done
+            if (producer && i + DEC_NBUF < npairs) dec_issue(d, sm, buf, dblk + (i + DEC_NBUF) * d.n_blocks);
+        }
     }
-    (void)rowb;
+    __syncthreads();
     if (producer && *stop) {
         // let the copies in flight land before the shared memory is released
         for (int b = 0; b < DEC_NBUF; ++b) {
-            mbar_wait_bounded(smem_u32(sm + DEC_OFF_BARS + 8 * b), 0, kWaitLimit / 16);
-            mbar_wait_bounded(smem_u32(sm + DEC_OFF_BARS + 8 * b), 1, kWaitLimit / 16);
+            mbar_wait_bounded(full_bar(b), 0, kWaitLimit / 16);
+            mbar_wait_bounded(full_bar(b), 1, kWaitLimit / 16);
         }
     }
 }
