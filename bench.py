@@ -617,6 +617,48 @@ def run_ours(args):
     return line
 
 
+def run_segmented_profile(args):
+    """A profiling run (no bench line): the two-level prefill of one sequence of
+    T = 16384 with 2 QK / 4 V heads (the `other_configs` few-head case), W
+    warm-up and K timed calls on one buffer set, CUDA events around each."""
+    import torch
+    import gated_deltanet_scan_gb300 as gdr
+    from gated_deltanet_scan_gb300 import synth
+
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
+    w = synth.make_workload("few_heads_T16384", [16384], 2, 4, D, 64, "bf16", seed=105, state_std=0.02)
+    x = dict(q=_bf(torch, w.q_bits).to(dev), k=_bf(torch, w.k_bits).to(dev), v=_bf(torch, w.v_bits).to(dev),
+             g=torch.from_numpy(np.ascontiguousarray(w.g)).to(dev),
+             beta=torch.from_numpy(np.ascontiguousarray(w.beta)).to(dev),
+             cu=torch.from_numpy(w.cu_seqlens.astype(np.int32)).to(dev))
+    st = torch.zeros((1, 4, D, D), dtype=torch.float32, device=dev)
+    o = torch.empty((16384, 4, D), dtype=torch.float32, device=dev)
+    P = gdr.gdr_prefill_segments_hint(x["q"], x["v"], o, 1, 16384)
+    ws = torch.empty(gdr.gdr_prefill_segmented_workspace_bytes(x["q"], x["v"], o, 1, 16384, P), dtype=torch.uint8,
+                     device=dev)
+
+    def call():
+        gdr.gdr_prefill_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"], st, o, x["cu"], P, chunk=64,
+                                  workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        call()
+    ts = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize(dev)
+    assert gdr.gdr_device_error(stream=stream) == 0, "a device-side wait timed out"
+    ms = statistics.median(a.elapsed_time(b) for a, b in ts) if ts else float("nan")
+    return {"partial_step": "segmented", "workload": "one sequence T=16384, 2 QK / 4 V heads, two-level prefill",
+            "segments": P, "steps": args.steps, "warmup": args.warmup, "ms": ms}
+
+
 # ---------------------------------------------------------------------------------
 # CPU oracle (baseline and reference arm)
 
@@ -732,8 +774,9 @@ def main():
     ap.add_argument("--decode-in-scan", action="store_true",
                     help="run the decode step inside the prefill's last chunk-scan launch (gdr_prefill_with_decode) "
                          "instead of as a programmatic dependent launch beside it")
-    ap.add_argument("--only", choices=["all", "prefill", "verify", "decode"], default="all",
-                    help="run one component of the step (for profiling); the default runs the full step")
+    ap.add_argument("--only", choices=["all", "prefill", "verify", "decode", "segmented"], default="all",
+                    help="run one component of the step (for profiling; 'segmented': the two-level prefill of "
+                         "one 16K-token sequence of 2 QK / 4 V heads); the default runs the full step")
     ap.add_argument("--no-other-configs", action="store_true",
                     help="skip the informational timing of the T=1024 and packed prefill workloads")
     ap.add_argument("--prefill-tokens", type=int, default=T_PREFILL,
@@ -745,7 +788,10 @@ def main():
         if args.only != "prefill" or args.prefill_tokens <= 0:
             ap.error("--prefill-tokens is for profiling runs with --only prefill")
         globals()["T_PREFILL"] = args.prefill_tokens
-    line = run_ours(args) if args.impl == "ours" else run_reference(args)
+    if args.impl == "ours" and args.only == "segmented":
+        line = run_segmented_profile(args)
+    else:
+        line = run_ours(args) if args.impl == "ours" else run_reference(args)
     if line is not None:
         print(json.dumps(line), flush=True)
 
