@@ -79,7 +79,7 @@ cudaError_t launch_gated_rmsnorm(int64_t rows, int d, const void *o, int o_bf16,
 // Two-level prefill (gdr_segment.cu): byte offsets of its fp32 scratch inside the
 // workspace, after the factor_bytes of the factor slots and X tiles.
 struct SegLayout {
-    size_t phi, b, x, o0, m, total;
+    size_t phi, b, x, xt, o0, m, total;
 };
 SegLayout segment_layout(int64_t factor_bytes, int n_seqs, int h_v, int64_t t_total, int P);
 // First chunk of segment p of P over n_chunks chunks (p = P gives n_chunks).

@@ -15,18 +15,49 @@
 // outputs o_t = o0_t + X_p^T m_t (fixup_kernel).  The final X is the state after
 // the sequence.
 //
-// Scratch (fp32, inside the caller's workspace, after the factor slots):
-//   Phi[P-1], B[P-1], X[P-1]  [n_seqs][h_v][d][d]   (X[j] = start of segment j+1)
-//   O0, M                     [t_total][h_v][d]     (rows of segments >= 1 only)
+// Scratch (inside the caller's workspace, after the factor slots):
+//   Phi[P-1], B[P-1], X[P-1]  fp32 [n_seqs][h_v][d][d]   (X[j] = start of segment j+1)
+//   XT[P-1]   per (sequence, V head) X[j]^T as bf16 hi and lo tensor-core operand
+//             tiles (64 KB; see xt_offset)
+//   O0, M     fp32 [t_total][h_v][d]     (rows of segments >= 1 only)
 #include <cuda_bf16.h>
 
 #include "gdr_factor_layout.h"
 #include "gdr_internal.h"
+#include "tc_ptx.cuh"
 
 namespace gdr {
 namespace {
 
 constexpr int D = 128;
+using namespace tc;
+
+__device__ __forceinline__ uint64_t desc_add_bytes(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
+// A 128 x 128 bf16 tensor-core operand, K-major with 128-byte swizzled rows: two
+// 16 KB halves (columns 0-63, 64-127), 16-byte chunk j of row r of a half at
+// r * 128 + 16 (j ^ (r % 8)).  The fix-up's operands are pairs of such tiles
+// (the bf16 hi and lo parts of an fp32 matrix): hi at 0, lo at 32 KB.
+__host__ __device__ constexpr uint32_t kt_chunk_offset(int r, int j) {  // j: 16-byte chunk 0..15 of row r
+    return (uint32_t)((j >> 3) * 16384 + r * 128 + (((j & 7) ^ (r & 7)) << 4));
+}
+constexpr uint32_t KT_BYTES = 32768, KT_PAIR = 2 * KT_BYTES;
+
+// bf16 hi and lo words of (x0, x1): hi = the top 16 bits of each, lo = bf16(x - hi); x0 low.
+__device__ __forceinline__ void hilo_word(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const uint32_t a = __float_as_uint(x0), b = __float_as_uint(x1);
+    hi = __byte_perm(a, b, 0x7632);
+    __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __uint_as_float(a & 0xFFFF0000u), x1 - __uint_as_float(b & 0xFFFF0000u));
+    lo = *reinterpret_cast<uint32_t *>(&l);
+}
+// Eight consecutive fp32 values as one 16-byte chunk of the hi tile and one of the lo tile.
+__device__ __forceinline__ void store_hilo_chunk(uint8_t *pair, uint32_t off, const float *x) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) hilo_word(x[2 * i], x[2 * i + 1], h[i], l[i]);
+    *reinterpret_cast<uint4 *>(pair + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4 *>(pair + KT_BYTES + off) = make_uint4(l[0], l[1], l[2], l[3]);
+}
 
 // Phi = I and B = 0 for every (segment >= 1, sequence, V head): the start states
 // of the transition and offset runs.
@@ -67,6 +98,7 @@ struct CombineParams {
     size_t seg_stride;  // floats between one segment's matrices and the next's
     const float *phi, *b;
     float *state, *xseg;
+    uint8_t *xt;        // XT[p-1]: X_p^T operand tiles for the fix-up, KT_PAIR bytes per matrix
 };
 __global__ void __launch_bounds__(256) combine_kernel(CombineParams c) {
     extern __shared__ __align__(16) float csm[];
@@ -93,6 +125,16 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams c) {
         *reinterpret_cast<float4 *>(c.xseg + mat + (size_t)r * D + c0 + 4 * q4) = v;
     }
     load_phi(1, ph(0));
+    // X_p^T as the fix-up's B operand: rows = this block's 16 columns of X_p, 128 k
+    // each, hi and lo (thread: column c0 + tid / 16, k = 8 (tid % 16) .. + 7)
+    auto write_tiles = [&](const float *xsm, int p) {
+        const int nl = tid >> 4, j = tid & 15;
+        float x8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x8[i] = xsm[(8 * j + i) * CMB_COLS + nl];
+        store_hilo_chunk(c.xt + ((size_t)(p - 1) * (c.seg_stride / (D * D)) + blockIdx.x) * KT_PAIR,
+                         kt_chunk_offset(c0 + nl, j), x8);
+    };
     const int r = tid >> 1, cc = (tid & 1) * 8;  // row r, 8 of the 16 columns
     for (int p = 1; p < c.P; ++p) {
         const int cur = (p - 1) & 1;
@@ -103,6 +145,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams c) {
             asm volatile("cp.async.wait_group 0;" ::: "memory");
         }
         __syncthreads();  // Phi_p and X_p visible to every thread
+        if (p == 1) write_tiles(xs(0), 1);
         const float *bb = c.b + (size_t)(p - 1) * c.seg_stride + mat + (size_t)r * D + c0 + cc;
         float acc[8];
 #pragma unroll
@@ -141,142 +184,174 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams c) {
         *reinterpret_cast<float4 *>(g) = make_float4(acc[0], acc[1], acc[2], acc[3]);
         *reinterpret_cast<float4 *>(g + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
         __syncthreads();  // every thread is done with Phi_p and X_p before they are overwritten
+        if (p + 1 < c.P) write_tiles(xs(cur ^ 1), p + 1);
     }
 }
 
-// o_t = o0_t + X_p^T m_t for the tokens of segments >= 1.  A block covers one
-// chunk (64 tokens, one segment) of one sequence and one V head: the 64 x 128
-// tile of (64 x 128) m times (128 x 128) X_p.  Both operands are staged in
-// shared memory by asynchronous copies (m's rows padded to 132 floats); each of
-// the 128 threads keeps an 8-token x 8-column tile of the result in registers
-// and walks the 128 terms four at a time.
+// o_t = o0_t + X_p^T m_t for the tokens of segments >= 1, on tcgen05: a CTA
+// covers up to 128 tokens (two chunks) of one segment of one sequence and one V
+// head, the 128 x 128 product of those tokens' maps M (rows) and X_p.  The
+// combine kernel left X_p^T as bf16 hi and lo K-major tiles (bulk-copied in);
+// the CTA splits its rows of M into hi and lo tiles itself; three products
+// (hi hi + hi lo + lo hi, fp32 accumulation in TMEM: 2^-16 relative, as the
+// chunk scan's state products), 8 k-steps of M = 128, N = 128 MMAs each; thread
+// t then adds its TMEM row to o0 and stores o.
 struct FixParams {
     int h_v, n_seqs, P, out_bf16;
-    int cuts[9];  // chunk cuts: segment p is chunks [cuts[p], cuts[p+1])
+    int cuts[9];    // chunk cuts: segment p is chunks [cuts[p], cuts[p+1])
+    int tiles[9];   // first CTA (blockIdx.x) of segment p's 128-token tiles, p >= 1; tiles[P] = total
     const int32_t *cu_seqlens;
-    const float *xseg;  // X[p-1] = start of segment p, [n_seqs][h_v][d][d]
+    const uint8_t *xt;  // XT[p-1], KT_PAIR bytes per (sequence, V head)
     const float *o0, *m;
     void *o;
+    int32_t *err;
 };
 
-constexpr int FIX_TOK = 64, M_LD = D + 4, X_LD = D + 4;
-constexpr int FIX_SMEM = (FIX_TOK * M_LD + D * X_LD) * (int)sizeof(float);
+// Shared memory: the A and B tile pairs, an fp32 staging row per thread (its row
+// of M, later of o0, brought in by cp.async with every copy in flight at once),
+// then 2 mbarriers and the TMEM address.
+constexpr int STAGE_LD = D + 4;  // staging row stride (floats): conflict-free 16-byte reads of a row per thread
+constexpr uint32_t FIX_A = 0, FIX_B = KT_PAIR, FIX_STAGE = 2 * KT_PAIR, FIX_BARS = FIX_STAGE + 128 * STAGE_LD * 4;
+constexpr int FIX_SMEM = (int)(FIX_BARS + 32 + 1024);
+constexpr uint32_t IDESC_FIX = idesc_bf16_f32(128, 128, 0, 0);
+constexpr long long kFixWait = 4000000000LL;  // SM clocks (about 2 s)
 
-// bf16 hi and lo words of the pair (x0, x1): hi = the top 16 bits of each, lo =
-// bf16(x - hi); x0 in the low half.
-__device__ __forceinline__ void hilo2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
-    const uint32_t a = __float_as_uint(x0), b = __float_as_uint(x1);
-    hi = __byte_perm(a, b, 0x7632);
-    __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __uint_as_float(a & 0xFFFF0000u), x1 - __uint_as_float(b & 0xFFFF0000u));
-    lo = *reinterpret_cast<uint32_t *>(&l);
-}
-// d += A B for one 16 x 8 tile (m16n8k16, bf16 operands, fp32 accumulation;
-// lane = 4 g + c holds rows g, g + 8 and columns 2c, 2c + 1 of d).
-__device__ __forceinline__ void mma_bf16x(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// One block per (64-token chunk of a later segment, sequence x V head): the
-// chunk's maps m (64 x d_k) and its segment's start state X (d_k x d_v) staged in
-// shared memory by cp.async, then O = o0 + M X on warp-level bf16 tensor-core
-// MMAs, each fp32 operand split into bf16 hi + lo parts and three products
-// (hi hi + hi lo + lo hi) accumulated in fp32: 2^-16 relative precision, as the
-// chunk scan's state products.  Warp w takes tokens 32 (w & 1) .. + 31 and
-// columns 64 (w >> 1) .. + 63.
-__global__ void __launch_bounds__(128, 2) fixup_kernel(FixParams p) {
-    extern __shared__ __align__(16) float fsm[];
-    float *ms = fsm;                    // [FIX_TOK][M_LD]
-    float *xs = fsm + FIX_TOK * M_LD;   // [D][X_LD]
-    const int c = p.cuts[1] + (int)blockIdx.x;      // chunk index within the sequence
-    const int s = (int)blockIdx.y / p.h_v, h = (int)blockIdx.y % p.h_v;
-    int seg = 1;  // the segment of chunk c (static indices: the cuts stay in the parameter space)
+__global__ void __launch_bounds__(128, 1) fixup_kernel(FixParams p) {
+    extern __shared__ uint8_t fsm_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(fsm_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    const uint32_t bar_x = sb + FIX_BARS, bar_mma = sb + FIX_BARS + 8;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(sm + FIX_BARS + 16);
+    const int bx = (int)blockIdx.x;
+    int seg = 1;  // the segment of this CTA's tile (static indices: the tables stay in the parameter space)
 #pragma unroll
     for (int q = 2; q < 9; ++q)
-        if (q < p.P && c >= p.cuts[q]) seg = q;
+        if (q < p.P && bx >= p.tiles[q]) seg = q;
+    int cseg_lo = 0, cseg_hi = 0, tile0 = 0;  // the segment's chunks [cseg_lo, cseg_hi), its first tile
+#pragma unroll
+    for (int q = 1; q < 9; ++q)
+        if (q == seg) {
+            cseg_lo = p.cuts[q];
+            tile0 = p.tiles[q];
+        }
+#pragma unroll
+    for (int q = 2; q < 9; ++q)
+        if (q == seg + 1) cseg_hi = p.cuts[q];
+    const int c0 = cseg_lo + 2 * (bx - tile0);  // first chunk of the tile
+    const int s = (int)blockIdx.y / p.h_v, h = (int)blockIdx.y % p.h_v;
     const int64_t ts = p.cu_seqlens[s], te = p.cu_seqlens[s + 1];
-    const int64_t t0 = ts + (int64_t)c * 64;
-    if (t0 >= te) return;  // past this sequence's end (or an empty sequence)
-    const int ntok = (int)((te - t0) < FIX_TOK ? (te - t0) : FIX_TOK);
-    const float *X = p.xseg + (((size_t)(seg - 1) * p.n_seqs + s) * p.h_v + h) * D * D;
-    const int tid = threadIdx.x;
-#pragma unroll 4
-    for (int i = tid; i < D * D / 4; i += 128) {
-        const int r = i / (D / 4), q4 = i % (D / 4);
-        cp_async16(xs + r * X_LD + 4 * q4, X + (size_t)r * D + 4 * q4);
+    const int64_t t0 = ts + (int64_t)c0 * 64;
+    int64_t tend = ts + (int64_t)cseg_hi * 64;
+    if (tend > te) tend = te;
+    if (t0 >= tend) return;  // past this sequence's end in this segment (or an empty sequence)
+    const int ntok = (int)((tend - t0) < 128 ? (tend - t0) : 128);
+    const int tid = threadIdx.x, warp = tid >> 5;
+
+    if (tid == 0) {
+        mbar_init(bar_x, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+        const uint8_t *src = p.xt + ((size_t)(seg - 1) * p.n_seqs * p.h_v + blockIdx.y) * KT_PAIR;
+        mbar_arrive_expect_tx(bar_x, KT_PAIR);
+#pragma unroll
+        for (uint32_t i = 0; i < 4; ++i) bulk_load(sb + FIX_B + i * 16384u, src + i * 16384u, 16384u, bar_x);
     }
-#pragma unroll 4
-    for (int i = tid; i < FIX_TOK * (D / 4); i += 128) {
-        const int t = i / (D / 4), q4 = i % (D / 4);
-        if (t < ntok)
-            cp_async16(ms + t * M_LD + 4 * q4, p.m + ((size_t)(t0 + t) * p.h_v + h) * D + 4 * q4);
-        else
-            *reinterpret_cast<float4 *>(ms + t * M_LD + 4 * q4) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_holder), 128);
+        tmem_relinquish();
+    }
+    // this thread's row of M, staged by cp.async, as hi and lo A tiles (rows past the
+    // tile's tokens: zero); then its row of o0 into the same staging row
+    float *stage = reinterpret_cast<float *>(sm + FIX_STAGE) + tid * STAGE_LD;
+    const size_t grow = ((size_t)(t0 + tid) * p.h_v + h) * D;
+    if (tid < ntok) {
+#pragma unroll
+        for (int j = 0; j < D / 4; ++j) cp_async16(stage + 4 * j, p.m + grow + 4 * j);
     }
     cp_async_wait_all();
-    __syncthreads();
-    const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, cc = lane & 3;
-    const int tb = 32 * (warp & 1), nb = 64 * (warp >> 1);
-    float acc[2][8][4];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
-#pragma unroll 1
-    for (int k0 = 0; k0 < D; k0 += 16) {
-        uint32_t ah[2][4], al[2][4];
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-            const float *mr = ms + (tb + 16 * mt + g) * M_LD + k0 + 2 * cc;
-            const float2 v0 = *reinterpret_cast<const float2 *>(mr);
-            const float2 v1 = *reinterpret_cast<const float2 *>(mr + 8 * M_LD);
-            const float2 v2 = *reinterpret_cast<const float2 *>(mr + 8);
-            const float2 v3 = *reinterpret_cast<const float2 *>(mr + 8 * M_LD + 8);
-            hilo2(v0.x, v0.y, ah[mt][0], al[mt][0]);
-            hilo2(v1.x, v1.y, ah[mt][1], al[mt][1]);
-            hilo2(v2.x, v2.y, ah[mt][2], al[mt][2]);
-            hilo2(v3.x, v3.y, ah[mt][3], al[mt][3]);
+#pragma unroll 4
+    for (int j = 0; j < 16; ++j) {
+        float x8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (tid < ntok) {
+            const float4 a = *reinterpret_cast<const float4 *>(stage + 8 * j);
+            const float4 b = *reinterpret_cast<const float4 *>(stage + 8 * j + 4);
+            x8[0] = a.x; x8[1] = a.y; x8[2] = a.z; x8[3] = a.w;
+            x8[4] = b.x; x8[5] = b.y; x8[6] = b.z; x8[7] = b.w;
         }
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-            const float *xr = xs + (k0 + 2 * cc) * X_LD + nb + 8 * nt + g;
-            uint32_t b0h, b0l, b1h, b1l;
-            hilo2(xr[0], xr[X_LD], b0h, b0l);
-            hilo2(xr[8 * X_LD], xr[9 * X_LD], b1h, b1l);
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                mma_bf16x(acc[mt][nt], ah[mt], b0h, b1h);
-                mma_bf16x(acc[mt][nt], ah[mt], b0l, b1l);
-                mma_bf16x(acc[mt][nt], al[mt], b0h, b1h);
-            }
-        }
+        store_hilo_chunk(sm + FIX_A, kt_chunk_offset(tid, j), x8);
     }
-    // o = o0 + acc: rows tb + 16 mt + g (+ 8), columns nb + 8 nt + 2 cc (+ 1)
+    if (tid < ntok) {  // o0, read in the epilogue; lands while the MMAs run
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+        for (int j = 0; j < D / 4; ++j) cp_async16(stage + 4 * j, p.o0 + grow + 4 * j);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_holder;
+    bool ok = true;
+    if (tid == 0) {
+        ok = mbar_wait_bounded(bar_x, 0, kFixWait);
+        if (ok) {
+            tc_fence_after_sync();
+            const uint64_t ah = smem_desc_sw128(sb + FIX_A, 16, 1024), al = desc_add_bytes(ah, KT_BYTES);
+            const uint64_t bh = smem_desc_sw128(sb + FIX_B, 16, 1024), bl = desc_add_bytes(bh, KT_BYTES);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int t = tb + 16 * mt + g + 8 * hh;
-            if (t >= ntok) continue;
-            const size_t orow = ((size_t)(t0 + t) * p.h_v + h) * D;
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t off = (uint32_t)((ks >> 2) * 16384 + (ks & 3) * 32);
+                mma_bf16(tmem, desc_add_bytes(ah, off), desc_add_bytes(bh, off), IDESC_FIX, ks > 0);
+                mma_bf16(tmem, desc_add_bytes(ah, off), desc_add_bytes(bl, off), IDESC_FIX, 1);
+                mma_bf16(tmem, desc_add_bytes(al, off), desc_add_bytes(bh, off), IDESC_FIX, 1);
+            }
+            mma_commit(bar_mma);
+        } else {
+            atomicCAS(p.err, 0, (int32_t)GDR_ERR_DEVICE_TIMEOUT);
+        }
+        *reinterpret_cast<volatile int *>(tmem_holder + 1) = ok ? 1 : 0;
+    }
+    __syncthreads();
+    const bool issued = *reinterpret_cast<volatile int *>(tmem_holder + 1) != 0;
+    bool done = issued && mbar_wait_bounded(bar_mma, 0, kFixWait);
+    if (issued && !done) atomicCAS(p.err, 0, (int32_t)GDR_ERR_DEVICE_TIMEOUT);
+    if (done) {
+        tc_fence_after_sync();
+        // thread t: TMEM lane t, the tile's token row t
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+        const size_t orow = grow;
+        asm volatile("cp.async.wait_group 0;" ::: "memory");  // this thread's row of o0
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+            float acc[32];
+            tmem_ld32(lane_addr + 32 * q, acc);
+            if (tid < ntok) {
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-                const int col = nb + 8 * nt + 2 * cc;
-                const float2 b = *reinterpret_cast<const float2 *>(p.o0 + orow + col);
-                const float y0 = b.x + acc[mt][nt][2 * hh], y1 = b.y + acc[mt][nt][2 * hh + 1];
-                if (p.out_bf16) {
-                    __nv_bfloat162 v = __floats2bfloat162_rn(y0, y1);
-                    *reinterpret_cast<__nv_bfloat162 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + orow + col) = v;
-                } else {
-                    *reinterpret_cast<float2 *>(reinterpret_cast<float *>(p.o) + orow + col) = make_float2(y0, y1);
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 b = *reinterpret_cast<const float4 *>(stage + 32 * q + e);
+                    const float y0 = b.x + acc[e], y1 = b.y + acc[e + 1], y2 = b.z + acc[e + 2], y3 = b.w + acc[e + 3];
+                    if (p.out_bf16) {
+                        __nv_bfloat162 v0 = __floats2bfloat162_rn(y0, y1), v1 = __floats2bfloat162_rn(y2, y3);
+                        uint2 pk;
+                        pk.x = *reinterpret_cast<uint32_t *>(&v0);
+                        pk.y = *reinterpret_cast<uint32_t *>(&v1);
+                        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + orow + 32 * q + e) = pk;
+                    } else {
+                        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + orow + 32 * q + e) =
+                            make_float4(y0, y1, y2, y3);
+                    }
                 }
             }
         }
+    } else if (tid == 0 && !issued) {
+        mbar_wait_bounded(bar_x, 0, kFixWait / 8);  // let the tile copy land before the memory is released
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");  // no copy of this thread still in flight
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 128);
+    }
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -290,7 +365,8 @@ SegLayout segment_layout(int64_t factor_bytes, int n_seqs, int h_v, int64_t t_to
     L.phi = align256((size_t)factor_bytes);
     L.b = L.phi + align256(mats);
     L.x = L.b + align256(mats);
-    L.o0 = L.x + align256(mats);
+    L.xt = L.x + align256(mats);  // one KT_PAIR (64 KB, the size of an fp32 state) per matrix
+    L.o0 = L.xt + align256(mats);
     L.m = L.o0 + align256(rows);
     L.total = L.m + align256(rows);
     return L;
@@ -305,6 +381,7 @@ cudaError_t launch_segmented(const Args &a, int P, uint8_t *ws, const SegLayout 
     float *xseg = reinterpret_cast<float *>(ws + L.x);
     float *o0 = reinterpret_cast<float *>(ws + L.o0);
     float *m = reinterpret_cast<float *>(ws + L.m);
+    uint8_t *xt = ws + L.xt;
     const size_t per_seg = (size_t)a.n_seqs * a.h_v;  // matrices per segment
     const size_t mat_floats = (size_t)D * D;
     static int configured_device = -1;
@@ -350,6 +427,7 @@ cudaError_t launch_segmented(const Args &a, int P, uint8_t *ws, const SegLayout 
         cp.b = bb;
         cp.state = a.state;
         cp.xseg = xseg;
+        cp.xt = xt;
         combine_kernel<<<dim3((unsigned)per_seg, D / CMB_COLS), 256, CMB_SMEM, s>>>(cp);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -362,13 +440,19 @@ cudaError_t launch_segmented(const Args &a, int P, uint8_t *ws, const SegLayout 
     fp.out_bf16 = a.out_bf16;
     for (int p = 0; p <= P; ++p) fp.cuts[p] = segment_cut(n_ch, P, p);
     fp.cu_seqlens = a.cu_seqlens;
-    fp.xseg = xseg;
+    fp.xt = xt;
     fp.o0 = o0;
     fp.m = m;
     fp.o = a.o;
-    const int fix_chunks = (int)(n_ch - fp.cuts[1]);
-    if (fix_chunks <= 0) return cudaSuccess;
-    fixup_kernel<<<dim3((unsigned)fix_chunks, (unsigned)per_seg), 128, FIX_SMEM, s>>>(fp);
+    fp.err = err;
+    int n_tiles = 0;  // 128-token tiles of segments >= 1, segment by segment
+    for (int p = 1; p < P; ++p) {
+        fp.tiles[p] = n_tiles;
+        n_tiles += (fp.cuts[p + 1] - fp.cuts[p] + 1) / 2;
+    }
+    fp.tiles[P] = n_tiles;
+    if (n_tiles <= 0) return cudaSuccess;
+    fixup_kernel<<<dim3((unsigned)n_tiles, (unsigned)per_seg), 128, FIX_SMEM, s>>>(fp);
     return cudaGetLastError();
 }
 

@@ -239,9 +239,11 @@ gdr_status gdr_prefill_segmented(const gdr_dims *dims, int32_t n_seqs, const int
 
 /*
  * Bytes of workspace gdr_prefill_segmented needs: gdr_prefill_workspace_bytes,
- * then, 256-byte aligned, per segment after the first three fp32 states per
- * (sequence, V head) (Phi, B and the start state, d_k * d_v floats each), and two
- * fp32 arrays shaped like o ([t_total][H_v][d_v]) for o0 and m.  Host-only;
+ * then, 256-byte aligned, per segment after the first four state-sized blocks
+ * per (sequence, V head) (Phi, B and the start state in fp32, d_k * d_v floats
+ * each, and the start state's transpose as bf16 hi and lo tensor-core operand
+ * tiles, the same size), and two fp32 arrays shaped like o ([t_total][H_v][d_v])
+ * for o0 and m.  Host-only;
  * equals gdr_prefill_workspace_bytes when n_segments is 1 (or the problem has one
  * chunk position).
  */

@@ -176,11 +176,12 @@ def test_segmented_workspace_size_and_checks(L):
     d = dims()
     base = L.gdr_prefill_workspace_bytes(ctypes.byref(d), 1, 16384)
     assert L.gdr_prefill_segmented_workspace_bytes(ctypes.byref(d), 1, 16384, 1) == base
-    # three fp32 states per (segment after the first, V head), two fp32 arrays like o
+    # four state-sized blocks per (segment after the first, V head): Phi, B and the
+    # start state in fp32, the start state's bf16 hi/lo operand tiles; two fp32 arrays like o
     st, rows = 32 * 128 * 128 * 4, 16384 * 32 * 128 * 4
     for P in (2, 4, 8):
         got = L.gdr_prefill_segmented_workspace_bytes(ctypes.byref(d), 1, 16384, P)
-        assert got == ((base + 255) // 256 * 256) + 3 * (P - 1) * st + 2 * rows, P
+        assert got == ((base + 255) // 256 * 256) + 4 * (P - 1) * st + 2 * rows, P
     # more segments than chunk positions: one per chunk (2 chunks here)
     two = L.gdr_prefill_segmented_workspace_bytes(ctypes.byref(d), 1, 100, 2)
     assert L.gdr_prefill_segmented_workspace_bytes(ctypes.byref(d), 1, 100, 8) == two
