@@ -84,14 +84,14 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-// Every segment's start, for one (sequence, V head) and 16 state columns per
+// Every segment's start, for one (sequence, V head) and 4 state columns per
 // block: X_{p+1} = Phi_p X_p + B_p for p = 1 .. P-1 in order.  The columns are
 // independent (X_{p+1}'s columns depend only on the same columns of X_p), so each
 // block walks all steps for its 16 columns with X in shared memory; Phi_{p+1}
 // is copied in (asynchronously, rows padded to 132 floats) while step p
 // computes.  X_1 is the state segment 0 left in `state`: it is saved to
 // xseg[0]; X_p goes to xseg[p-1], and the last, X_P, back to `state`.
-constexpr int CMB_COLS = 16, PHI_LD = D + 4;
+constexpr int CMB_COLS = 4, PHI_LD = D + 4;
 constexpr int CMB_SMEM = (2 * D * PHI_LD + 2 * D * CMB_COLS) * (int)sizeof(float);
 struct CombineParams {
     int P;
@@ -125,9 +125,10 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams c) {
         *reinterpret_cast<float4 *>(c.xseg + mat + (size_t)r * D + c0 + 4 * q4) = v;
     }
     load_phi(1, ph(0));
-    // X_p^T as the fix-up's B operand: rows = this block's 16 columns of X_p, 128 k
-    // each, hi and lo (thread: column c0 + tid / 16, k = 8 (tid % 16) .. + 7)
+    // X_p^T as the fix-up's B operand: rows = this block's 4 columns of X_p, 128 k
+    // each, hi and lo (thread t < 128: column c0 + t / 16, k = 8 (t % 16) .. + 7)
     auto write_tiles = [&](const float *xsm, int p) {
+        if (tid >= CMB_COLS * 16) return;
         const int nl = tid >> 4, j = tid & 15;
         float x8[8];
 #pragma unroll
@@ -135,7 +136,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams c) {
         store_hilo_chunk(c.xt + ((size_t)(p - 1) * (c.seg_stride / (D * D)) + blockIdx.x) * KT_PAIR,
                          kt_chunk_offset(c0 + nl, j), x8);
     };
-    const int r = tid >> 1, cc = (tid & 1) * 8;  // row r, 8 of the 16 columns
+    const int r = tid >> 1, cc = (tid & 1) * 2;  // row r, 2 of the 4 columns
     for (int p = 1; p < c.P; ++p) {
         const int cur = (p - 1) & 1;
         if (p + 1 < c.P) {
@@ -147,14 +148,11 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams c) {
         __syncthreads();  // Phi_p and X_p visible to every thread
         if (p == 1) write_tiles(xs(0), 1);
         const float *bb = c.b + (size_t)(p - 1) * c.seg_stride + mat + (size_t)r * D + c0 + cc;
-        float acc[8];
-#pragma unroll
-        for (int j = 0; j < 8; j += 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(bb + j);
-            acc[j] = v.x;
-            acc[j + 1] = v.y;
-            acc[j + 2] = v.z;
-            acc[j + 3] = v.w;
+        float acc[2];
+        {
+            const float2 v = *reinterpret_cast<const float2 *>(bb);
+            acc[0] = v.x;
+            acc[1] = v.y;
         }
         const float *pr = ph(cur) + r * PHI_LD;
         const float *xin = xs(cur);
@@ -164,25 +162,16 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams c) {
             const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                const float4 x0 = *reinterpret_cast<const float4 *>(xin + (4 * k4 + kk) * CMB_COLS + cc);
-                const float4 x1 = *reinterpret_cast<const float4 *>(xin + (4 * k4 + kk) * CMB_COLS + cc + 4);
+                const float2 x0 = *reinterpret_cast<const float2 *>(xin + (4 * k4 + kk) * CMB_COLS + cc);
                 acc[0] = fmaf(av[kk], x0.x, acc[0]);
                 acc[1] = fmaf(av[kk], x0.y, acc[1]);
-                acc[2] = fmaf(av[kk], x0.z, acc[2]);
-                acc[3] = fmaf(av[kk], x0.w, acc[3]);
-                acc[4] = fmaf(av[kk], x1.x, acc[4]);
-                acc[5] = fmaf(av[kk], x1.y, acc[5]);
-                acc[6] = fmaf(av[kk], x1.z, acc[6]);
-                acc[7] = fmaf(av[kk], x1.w, acc[7]);
             }
         }
         // X_{p+1}: to shared memory for the next step, and to xseg[p] (or the state)
         float *xo = xs(cur ^ 1) + r * CMB_COLS + cc;
-        *reinterpret_cast<float4 *>(xo) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        *reinterpret_cast<float4 *>(xo + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        *reinterpret_cast<float2 *>(xo) = make_float2(acc[0], acc[1]);
         float *g = (p == c.P - 1 ? c.state : c.xseg + (size_t)p * c.seg_stride) + mat + (size_t)r * D + c0 + cc;
-        *reinterpret_cast<float4 *>(g) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        *reinterpret_cast<float4 *>(g + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        *reinterpret_cast<float2 *>(g) = make_float2(acc[0], acc[1]);
         __syncthreads();  // every thread is done with Phi_p and X_p before they are overwritten
         if (p + 1 < c.P) write_tiles(xs(cur ^ 1), p + 1);
     }
