@@ -296,6 +296,8 @@ gdr_status gdr_prefill_segmented(const gdr_dims *dims, int32_t n_seqs, const int
     if (n_seqs == 0) return t_total == 0 ? GDR_OK : GDR_ERR_INVALID_ARG;
     if (!cu_seqlens || !aligned16(cu_seqlens) || !tensors_ok(q, k, v, g, beta, state, o)) return GDR_ERR_INVALID_ARG;
     if (t_total > ((int64_t)1 << 31) - 1) return GDR_ERR_UNSUPPORTED;
+    // the combine and fix-up grids index (sequence, V head) pairs in one grid dimension
+    if ((int64_t)n_seqs * dims->h_v > 65535) return GDR_ERR_UNSUPPORTED;
     const size_t need = gdr_prefill_segmented_workspace_bytes(dims, n_seqs, t_total, n_segments);
     if (!workspace || !aligned16(workspace) || workspace_bytes < need) return GDR_ERR_INVALID_ARG;
     const SegLayout L = segment_layout((int64_t)gdr_prefill_workspace_bytes(dims, n_seqs, t_total), n_seqs,

@@ -222,7 +222,8 @@ size_t gdr_prefill_static_workspace_capacity(void);
  *
  *   n_segments  1..8 (GDR_ERR_INVALID_ARG otherwise); more than there are chunk
  *               positions means one per chunk; 1 runs gdr_prefill_chunked's
- *               two-launch form.  gdr_prefill_segments_hint() gives the value
+ *               two-launch form.  With 2 or more segments n_seqs * H_v must not
+ *               exceed 65535 (GDR_ERR_UNSUPPORTED, nothing launched).  gdr_prefill_segments_hint() gives the value
  *               the library would pick on the current device.
  *   workspace   DEVICE scratch of at least gdr_prefill_segmented_workspace_bytes
  *               bytes, 16-byte aligned, as for gdr_prefill_chunked.

@@ -196,6 +196,9 @@ def test_segmented_workspace_size_and_checks(L):
     assert L.gdr_prefill_segmented(*args(4, dd=dims(in_dtype=gdr.GDR_F32))) == gdr.GDR_ERR_UNSUPPORTED
     assert L.gdr_prefill_segmented(*args(4, dd=dims(chunk=16))) == gdr.GDR_ERR_UNSUPPORTED
     assert L.gdr_prefill_segmented(*args(4, dd=dims(h_v=30))) == gdr.GDR_ERR_INVALID_ARG
+    # more (sequence, V head) pairs than one grid dimension indexes
+    many = (ctypes.byref(d), 2048, A, 4096, A, A, A, A, A, A, A, 4, A, 1 << 40, None)
+    assert L.gdr_prefill_segmented(*many) == gdr.GDR_ERR_UNSUPPORTED
     bad_ptr = (ctypes.byref(d), 1, A, 4096, A, MISALIGNED, A, A, A, A, A, 4, A, ws, None)
     assert L.gdr_prefill_segmented(*bad_ptr) == gdr.GDR_ERR_INVALID_ARG
     # without a GPU the hint is 1 (no SMs to spread segments over); invalid dims: 1
