@@ -168,3 +168,26 @@ def test_prefill_with_decode_sweep(c):
     od_ref, ds_ref = _oracle(dw, c["fused"])
     gu.check_outputs(gu.to_np(od), od_ref, c["out"])
     gu.check_state(gu.to_np(dx["state"]), ds_ref)
+
+
+@pytest.mark.parametrize("entry", ["chunked", "segmented"])
+def test_many_short_sequences(entry):
+    """64 packed sequences of 0..200 tokens (Qwen3.5-9B heads): the factor kernel's
+    search over cu_seqlens, one spare chunk position per sequence, and the
+    two-level prefill's segments over packed sequences."""
+    import gated_deltanet_scan_gb300 as gdr
+    torch = gu.require_gpu()
+    rng = np.random.default_rng(4242)
+    lens = [int(x) for x in rng.integers(0, 201, 64)]
+    w = synth.make_workload("many_short", lens, 16, 32, 128, 64, "bf16", seed=4243, state_std=0.02)
+    x = gu.dev_inputs(w)
+    o = gu.out_like(x["v"], "f32")
+    if entry == "chunked":
+        gdr.gdr_prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state"], o, x["cu_seqlens"])
+    else:
+        gdr.gdr_prefill_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state"], o, x["cu_seqlens"], 2)
+    torch.cuda.synchronize()
+    assert gdr.gdr_device_error() == 0
+    o_ref, s_ref = oracle.run_workload(w)
+    gu.check_outputs(gu.to_np(o), o_ref)
+    gu.check_state(gu.to_np(x["state"]), s_ref)
