@@ -249,15 +249,21 @@ __global__ void __launch_bounds__(128, 1) fixup_kernel(FixParams p) {
         tmem_alloc(smem_u32(tmem_holder), 128);
         tmem_relinquish();
     }
-    // this thread's row of M, staged by cp.async, as hi and lo A tiles (rows past the
-    // tile's tokens: zero); then its row of o0 into the same staging row
-    float *stage = reinterpret_cast<float *>(sm + FIX_STAGE) + tid * STAGE_LD;
-    const size_t grow = ((size_t)(t0 + tid) * p.h_v + h) * D;
-    if (tid < ntok) {
-#pragma unroll
-        for (int j = 0; j < D / 4; ++j) cp_async16(stage + 4 * j, p.m + grow + 4 * j);
+    // The tile's rows of M, staged by cp.async (warp w: rows 32 w .. + 31, one whole
+    // 512-byte row per instruction), as hi and lo A tiles (rows past the tile's tokens:
+    // zero); then its rows of o0 into the same staging rows.  Thread tid reads and
+    // writes staging row tid only, which its own warp brought in.
+    const int lane = tid & 31;
+    float *stage_all = reinterpret_cast<float *>(sm + FIX_STAGE);
+    float *stage = stage_all + tid * STAGE_LD;
+    auto grow = [&](int r) { return ((size_t)(t0 + r) * p.h_v + h) * D; };
+#pragma unroll 4
+    for (int i = 0; i < 32; ++i) {
+        const int r = 32 * warp + i;
+        if (r < ntok) cp_async16(stage_all + r * STAGE_LD + 4 * lane, p.m + grow(r) + 4 * lane);
     }
     cp_async_wait_all();
+    __syncwarp();
 #pragma unroll 4
     for (int j = 0; j < 16; ++j) {
         float x8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -269,9 +275,11 @@ __global__ void __launch_bounds__(128, 1) fixup_kernel(FixParams p) {
         }
         store_hilo_chunk(sm + FIX_A, kt_chunk_offset(tid, j), x8);
     }
-    if (tid < ntok) {  // o0, read in the epilogue; lands while the MMAs run
-#pragma unroll
-        for (int j = 0; j < D / 4; ++j) cp_async16(stage + 4 * j, p.o0 + grow + 4 * j);
+    __syncwarp();  // every lane is done with the rows of M before o0 replaces them
+#pragma unroll 4
+    for (int i = 0; i < 32; ++i) {  // o0, read in the epilogue; lands while the MMAs run
+        const int r = 32 * warp + i;
+        if (r < ntok) cp_async16(stage_all + r * STAGE_LD + 4 * lane, p.o0 + grow(r) + 4 * lane);
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
     fence_proxy_async_smem();
@@ -305,29 +313,36 @@ __global__ void __launch_bounds__(128, 1) fixup_kernel(FixParams p) {
     if (issued && !done) atomicCAS(p.err, 0, (int32_t)GDR_ERR_DEVICE_TIMEOUT);
     if (done) {
         tc_fence_after_sync();
-        // thread t: TMEM lane t, the tile's token row t
+        // thread t: TMEM lane t, the tile's token row t; o = o0 + M X written back into
+        // the staging row, then the warp stores its rows whole (one row per instruction)
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
-        const size_t orow = grow;
-        asm volatile("cp.async.wait_group 0;" ::: "memory");  // this thread's row of o0
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncwarp();  // the warp's rows of o0 have landed
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {
             float acc[32];
             tmem_ld32(lane_addr + 32 * q, acc);
-            if (tid < ntok) {
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const float4 b = *reinterpret_cast<const float4 *>(stage + 32 * q + e);
-                    const float y0 = b.x + acc[e], y1 = b.y + acc[e + 1], y2 = b.z + acc[e + 2], y3 = b.w + acc[e + 3];
-                    if (p.out_bf16) {
-                        __nv_bfloat162 v0 = __floats2bfloat162_rn(y0, y1), v1 = __floats2bfloat162_rn(y2, y3);
-                        uint2 pk;
-                        pk.x = *reinterpret_cast<uint32_t *>(&v0);
-                        pk.y = *reinterpret_cast<uint32_t *>(&v1);
-                        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + orow + 32 * q + e) = pk;
-                    } else {
-                        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + orow + 32 * q + e) =
-                            make_float4(y0, y1, y2, y3);
-                    }
+            for (int e = 0; e < 32; e += 4) {
+                float4 *b = reinterpret_cast<float4 *>(stage + 32 * q + e);
+                const float4 v = *b;
+                *b = make_float4(v.x + acc[e], v.y + acc[e + 1], v.z + acc[e + 2], v.w + acc[e + 3]);
+            }
+        }
+        __syncwarp();
+#pragma unroll 4
+        for (int i = 0; i < 32; ++i) {
+            const int r = 32 * warp + i;
+            if (r < ntok) {
+                const float4 y = *reinterpret_cast<const float4 *>(stage_all + r * STAGE_LD + 4 * lane);
+                if (p.out_bf16) {
+                    __nv_bfloat162 v0 = __floats2bfloat162_rn(y.x, y.y), v1 = __floats2bfloat162_rn(y.z, y.w);
+                    uint2 pk;
+                    pk.x = *reinterpret_cast<uint32_t *>(&v0);
+                    pk.y = *reinterpret_cast<uint32_t *>(&v1);
+                    *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.o) + grow(r) + 4 * lane) = pk;
+                } else {
+                    *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.o) + grow(r) + 4 * lane) = y;
                 }
             }
         }
