@@ -609,7 +609,10 @@ def run_ours(args):
         line.pop("e2e")
         line.pop("other_configs")
         keep = {"prefill": "prefill_T16384", "verify": "verify16_commit7", "decode": "decode_B64"}[only]
-        line["components"] = {keep: line["components"][keep]}
+        comp = line["components"][keep]
+        if only == "prefill":  # named for the prefill length actually timed (--prefill-tokens)
+            keep = f"prefill_T{T_PREFILL}"
+        line["components"] = {keep: comp}
         if only != "prefill":
             line.pop("roofline")
     elif not args.no_cpu_baseline:
