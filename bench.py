@@ -377,7 +377,7 @@ def run_ours(args):
 
         l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
 
-        def time_prefill(w, reps=10, segments=None):
+        def time_prefill(w, reps=10, segments=None, flags=None):
             """Median of `reps` prefills, each on the next of several copies of the
             inputs, outputs, states and workspace whose total is over twice the L2
             size (so no call finds its operands in L2 from the call before), launched
@@ -406,7 +406,7 @@ def run_ours(args):
             def call(x):
                 if segments is None:
                     gdr.gdr_prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], x["st"], x["o"], x["cu"],
-                                            chunk=64, workspace=x["ws"], stream=stream)
+                                            chunk=64, workspace=x["ws"], stream=stream, **(flags or {}))
                 else:
                     gdr.gdr_prefill_segmented(x["q"], x["k"], x["v"], x["g"], x["beta"], x["st"], x["o"], x["cu"],
                                               segments, chunk=64, workspace=x["ws"], stream=stream)
@@ -457,6 +457,53 @@ def run_ours(args):
         seg = time_prefill(few, segments=P)
         other["few_heads_T16384_hqk2_hv4"] = {"one_chain": plain, "segmented": dict(seg, segments=P),
                                               "speedup": plain["ms"] / seg["ms"]}
+        del few, plain, seg
+
+        # The steps on either side of the rule, on the same shapes with the options on:
+        # raw q/k normalised inside the kernels and beta from logits (the T = 16384
+        # prefill; the B = 64 decode step, also with the gated RMSNorm fused in), and
+        # the one-pass gated RMSNorm over the prefill's output.
+        fw = synth.make_workload("fused_T16384", [T_PREFILL], H_QK, H_V, D, 64, "bf16", seed=106, state_std=0.02,
+                                 qk_raw_scale=(0.3, 3.0), beta_logits=True)
+        fused = {"prefill_T16384_plain_alone": time_prefill(pre),
+                 "prefill_T16384_qk_l2norm_beta_logits": time_prefill(fw, flags=dict(qk_l2norm=True, beta_logits=True))}
+        del fw
+        hbm_peak = load_peaks()[0]["hbm_gbs"]
+
+        def time_calls(fn, reps=20):
+            ts = []
+            for _ in range(reps + 5):
+                a0, a1 = ev(), ev()
+                a0.record(stream)
+                fn()
+                a1.record(stream)
+                ts.append((a0, a1))
+            barrier()
+            return statistics.median(a.elapsed_time(b) for a, b in ts[5:])
+
+        def bw(nbytes, ms):
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            return {"ms": ms, "bytes": nbytes, "hbm_gbs": gbs, "frac_hbm": gbs / hbm_peak}
+
+        st2 = dstate.clone()
+        w_norm = torch.ones(D, dtype=torch.float32, device=dev)
+        ms = time_calls(lambda: gdr.gdr_decode_step(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], st2, o_dec,
+                                                    qk_l2norm=True, beta_logits=True, stream=stream))
+        fused["decode_B64_qk_l2norm_beta_logits"] = dict(bw(B_DECODE * DECODE_BYTES_PER_SEQ, ms),
+                                                         plain_decode_ms=decode_ms)
+        # z is the v rows (any bf16 values serve for the timing); y replaces o
+        ms = time_calls(lambda: gdr.gdr_decode_step_gated(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], st2,
+                                                          dd["v"], w_norm, o_dec, stream=stream))
+        fused["decode_B64_gated_rmsnorm"] = dict(bw(B_DECODE * (DECODE_BYTES_PER_SEQ + H_V * D * 2), ms),
+                                                 plain_decode_ms=decode_ms)
+        del st2
+        # over the prefill's fp32 output rows, z = the prefill's bf16 v rows, y fp32
+        y_norm = torch.empty_like(o_pre)
+        ms = time_calls(lambda: gdr.gdr_gated_rmsnorm(o_pre, dp["v"], w_norm, y_norm, stream=stream), reps=10)
+        fused["gated_rmsnorm_T16384"] = dict(bw(T_PREFILL * H_V * D * (4 + 2 + 4), ms),
+                                             rows=T_PREFILL * H_V, io="o fp32, z bf16, y fp32")
+        del y_norm
+        other["fused_steps"] = fused
 
     # End to end through the same public API: every step uploads its inputs from
     # pinned host memory and reads its outputs back.  Like a serving pipeline, the
