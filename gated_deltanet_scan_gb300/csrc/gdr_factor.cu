@@ -447,16 +447,20 @@ __device__ __forceinline__ void factor_body(const CUtensorMap &tmK, const CUtens
             mma_commit(bar_mma);
         }
     }
-    ok = ok && mbar_wait_bounded(bar_mma, 0, kWaitLimit);
     if (QKN && ok) {
-        // fused L2 normalisation: thread i takes row i of the [K; Q] tile (both
-        // d_k halves; the order of the sum does not matter), still intact
+        // fused L2 normalisation, while the Gram MMAs run (they only read the tile
+        // too): thread i takes row i of the [K; Q] tile (both d_k halves; the order
+        // of the sum does not matter).  Thread i starts at 16-byte piece i % 8 of the
+        // row, so that a warp's loads spread over the banks (the same piece of 32
+        // rows would hit one bank group).  Summed after the Gram had completed and
+        // with that bank pattern, the option made the factor kernel 1.4x slower.
         ok = mbar_wait_bounded(bar_tma, 0, kWaitLimit);  // the tile's bytes are visible to this thread
         float ss = 0.f;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
+            for (int c8 = 0; c8 < 8; ++c8) {
+                const int ch = (c8 + tid) & 7;
                 const uint4 wv = *reinterpret_cast<const uint4 *>(sm + OFF_KQ + 16384 * hf + 128 * tid + 16 * ch);
                 const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
@@ -467,6 +471,7 @@ __device__ __forceinline__ void factor_body(const CUtensorMap &tmK, const CUtens
             }
         gates[256 + tid] = l2norm_scale(ss);  // rows 0-63: 1 / |k_t|; 64-127: 1 / |q_t|
     }
+    ok = ok && mbar_wait_bounded(bar_mma, 0, kWaitLimit);
     if (!ok) atomicCAS(p.err, 0, (int32_t)GDR_ERR_DEVICE_TIMEOUT);
     if (!__syncthreads_and(ok)) {  // also publishes the gates and the row scales
         // let the tile load land before this CTA's shared memory is released
