@@ -447,13 +447,12 @@ __device__ __forceinline__ void factor_body(const CUtensorMap &tmK, const CUtens
             mma_commit(bar_mma);
         }
     }
-    if (QKN && ok) {
-        // fused L2 normalisation, while the Gram MMAs run (they only read the tile
-        // too): thread i takes row i of the [K; Q] tile (both d_k halves; the order
-        // of the sum does not matter).  Thread i starts at 16-byte piece i % 8 of the
-        // row, so that a warp's loads spread over the banks (the same piece of 32
-        // rows would hit one bank group).  Summed after the Gram had completed and
-        // with that bank pattern, the option made the factor kernel 1.4x slower.
+    if (QKN && ok && tid >= 64) {
+        // fused L2 normalisation of the Q rows, while the Gram MMAs run (they only read
+        // the tile too): thread i takes row i of the [K; Q] tile (both d_k halves; the
+        // order of the sum does not matter).  Thread i starts at 16-byte piece i % 8 of
+        // the row, so that a warp's loads spread over the banks (the same piece of 32
+        // rows would hit one bank group).  (The K rows' norms are the Gram's diagonal.)
         ok = mbar_wait_bounded(bar_tma, 0, kWaitLimit);  // the tile's bytes are visible to this thread
         float ss = 0.f;
 #pragma unroll
@@ -469,9 +468,20 @@ __device__ __forceinline__ void factor_body(const CUtensorMap &tmK, const CUtens
                     ss = fmaf(lo, lo, fmaf(hi, hi, ss));
                 }
             }
-        gates[256 + tid] = l2norm_scale(ss);  // rows 0-63: 1 / |k_t|; 64-127: 1 / |q_t|
+        gates[256 + tid] = l2norm_scale(ss);  // rows 64-127: 1 / |q_t|
     }
     ok = ok && mbar_wait_bounded(bar_mma, 0, kWaitLimit);
+    if (QKN && warp < 2) {
+        // the K rows' norms: |k_t|^2 = (K Kᵀ)[t][t], the Gram's diagonal in TMEM (lane t,
+        // column t: warp w reads columns 32 w .. + 31 of its lanes)
+        tc_fence_after_sync();
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32 * warp, v);
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) ss = (e == lane) ? v[e] : ss;
+        if (ok) gates[256 + tid] = l2norm_scale(ss);  // rows 0-63: 1 / |k_t|
+    }
     if (!ok) atomicCAS(p.err, 0, (int32_t)GDR_ERR_DEVICE_TIMEOUT);
     if (!__syncthreads_and(ok)) {  // also publishes the gates and the row scales
         // let the tile load land before this CTA's shared memory is released
