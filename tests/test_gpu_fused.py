@@ -166,3 +166,37 @@ def test_gated_rmsnorm_standalone_and_fused_in_decode(out_dtype):
     check_gated(gu.to_np(yd), yd_ref, zd, wt, out_dtype)
     gu.check_state(gu.to_np(d["state"]), Sd_ref)
     assert gdr.gdr_device_error() == 0
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("o_dtype,z_dtype", [("f32", "bf16"), ("bf16", "bf16"), ("f32", "f32"), ("bf16", "f32")])
+def test_gated_rmsnorm_shapes_and_dtypes(d, o_dtype, z_dtype):
+    """The one-pass norm for every head size (a lane holds d / 32 values: vector and
+    scalar accesses) and every dtype pairing, over row counts that leave the last
+    step of the two-rows-per-warp loop with one row or none (1, 7, 1001, and more
+    rows than the grid has warps), against the oracle's norm of the same values."""
+    import gated_deltanet_scan_gb300 as gdr
+    torch = gu.require_gpu()
+    st = synth.Stream(4242 + d, f"norm_{o_dtype}_{z_dtype}")
+    wt = (0.5 + st.uniform(d)).astype(np.float32)
+    wdev = torch.from_numpy(wt).cuda()
+    for rows in (1, 7, 1001, 50001):
+        o = st.normal(rows * d).reshape(rows, d).astype(np.float32) * np.float32(0.3)
+        z = st.normal(rows * d).reshape(rows, d).astype(np.float32) * np.float32(2.0)
+
+        def dev(a, dt):
+            if dt == "bf16":
+                return torch.from_numpy(synth.bf16_bits(a).view(np.int16).copy()).view(torch.bfloat16).cuda()
+            return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+        odev, zdev = dev(o, o_dtype), dev(z, z_dtype)
+        y = torch.empty_like(odev)
+        gdr.gdr_gated_rmsnorm(odev, zdev, wdev, y)
+        torch.cuda.synchronize()
+        ref = oracle.gated_rmsnorm(gu.to_np(odev), gu.to_np(zdev), wt)  # the values the kernel read
+        got = gu.to_np(y)
+        bound = 1e-5 * np.abs(ref) + 1e-6 * np.sqrt(np.mean(ref ** 2))
+        if o_dtype == "bf16":
+            bound = bound + 2.0 ** -8 * np.abs(ref)
+        assert np.all(np.abs(got - ref) <= bound), (d, o_dtype, z_dtype, rows)
+    assert gdr.gdr_device_error() == 0
