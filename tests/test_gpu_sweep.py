@@ -191,3 +191,26 @@ def test_many_short_sequences(entry):
     o_ref, s_ref = oracle.run_workload(w)
     gu.check_outputs(gu.to_np(o), o_ref)
     gu.check_state(gu.to_np(x["state"]), s_ref)
+
+
+@pytest.mark.parametrize("n,ties", [(2, True), (32, False), (32, True), (33, False)])
+def test_packed_sequence_order(n, ties):
+    """The chunk scan takes 2..32 packed sequences longest first (ranked by every warp
+    with shuffles; equal lengths by index) and more in order: 2 and 32 sequences with
+    and without equal lengths, 33 sequences (natural order), against the oracle."""
+    import gated_deltanet_scan_gb300 as gdr
+    torch = gu.require_gpu()
+    rng = np.random.default_rng(900 + n + (1000 if ties else 0))
+    lens = [int(x) for x in rng.integers(0, 160, n)]
+    if ties:
+        lens = [lens[0]] * n if n == 2 else [int(x) for x in rng.choice([0, 64, 65, 130], n)]
+    lens[-1] = max(lens[-1], 1)
+    w = synth.make_workload(f"order{n}", lens, 4, 8, 128, 64, "bf16", seed=901 + n, state_std=0.02)
+    x = gu.dev_inputs(w)
+    o = gu.out_like(x["v"], "f32")
+    gdr.gdr_prefill_chunked(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state"], o, x["cu_seqlens"])
+    torch.cuda.synchronize()
+    assert gdr.gdr_device_error() == 0
+    o_ref, s_ref = oracle.run_workload(w)
+    gu.check_outputs(gu.to_np(o), o_ref)
+    gu.check_state(gu.to_np(x["state"]), s_ref)
