@@ -85,6 +85,16 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(Args a, int32_t *err) 
     float vv[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) vv[c] = load_in(a.v, vh * D + 4 * cq + c, a.in_bf16);
+    // the gated RMSNorm's gate and weights for the output row (row group 0), loaded
+    // with the other vectors, off the path after the reductions
+    float gz[4] = {0.f, 0.f, 0.f, 0.f}, gw[4] = {0.f, 0.f, 0.f, 0.f};
+    if (a.norm_z && rg == 0) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            gz[c] = silu(load_in(a.norm_z, vh * D + 4 * cq + c, a.in_bf16));
+            gw[c] = a.norm_w[4 * cq + c];
+        }
+    }
     __syncthreads();  // the mbarrier is initialised, sk and sq are written
     if (a.qk_norm && warp < 2) {
         // fused L2 normalisation: per-row scales of k (warp 0) and q (warp 1)
@@ -164,10 +174,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(Args a, int32_t *err) 
             for (int off = Sh::Q4 / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(kMask, ss, off);
             const float inv = rsqrtf(ss / D + a.norm_eps);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int col = 4 * cq + c;
-                ov[c] = a.norm_w[col] * ov[c] * inv * silu(load_in(a.norm_z, vh * D + col, a.in_bf16));
-            }
+            for (int c = 0; c < 4; ++c) ov[c] = gw[c] * ov[c] * inv * gz[c];
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) store_out(a.o, vh * D + 4 * cq + c, ov[c], a.out_bf16);
