@@ -12,8 +12,9 @@
 // re-feeding the accepted tokens.
 //
 // Mapping.  One block of 256 threads per (sequence, V head, eighth of the state
-// rows), so even one sequence spreads over 8 H_v blocks (with 4, the commit took
-// 6% longer: fewer loads in flight).  Thread t owns
+// rows), so even one sequence spreads over 8 H_v blocks (verify block + commit:
+// 9.3 us with 4, 8.8 us with 8, 10.3 us with 16, where every block reloads all
+// n_tok corrections of its columns for fewer rows).  Thread t owns
 // column quad t % (D/4) of rows t / (D/4) + k (256 / (D/4)), k < D / 4 / (256 /
 // (D/4)): every load of its rows is issued before any arithmetic, and its quad
 // of the weighted corrections e^{G_a - G_j} u_j stays in registers; the
